@@ -1,0 +1,345 @@
+"""Oracle for the Clebsch-Gordan tensor product -- TEST INFRASTRUCTURE ONLY.
+
+A plain, slow fp64 CPU restatement of what the GPU library computes, used to
+check it.  Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg
+of ``bench.py`` may import this package; the product path
+(``clebsch_gordan_tensor_gb300``) never does and shares no code with it.
+
+The arithmetic lives in ``cgtp_oracle.c`` (compiled with gcc on first use).
+This module adds what is plain bookkeeping: parsing irreps strings, listing the
+'uvu' paths, and the double-backward identity written as sums of the
+first-order pieces.
+
+Sources: "An Efficient Sparse Kernel Generator for O(3)-Equivariant Deep
+Networks" (arXiv 2501.13986), abstract -- the CG tensor product of two dense
+irrep vectors with a structured sparse tensor, fused with a graph convolution,
+with its gradient and the higher partial derivatives used for forces; NVIDIA's
+SE(3)-Transformer blog, section "TFN fusion" -- degree-d features have
+dimension 2d+1 and pairwise degree convolutions are summed per output degree.
+
+Parity pins: every function here is pinned in ``tests/test_oracle_*.py`` against
+textbook closed forms, library routines (sympy CG, scipy spherical harmonics),
+invariants (orthogonality, equivariance under rotations and inversion, adjoint
+identities) or finite differences.  The pages print no worked numbers, so the
+absolute values are "parity unpinned" against the pages themselves.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import subprocess
+import threading
+from dataclasses import dataclass
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_BUILD = os.path.join(_HERE, "_build")
+_SO = os.path.join(_BUILD, "libcgtp_oracle.so")
+_SRC = os.path.join(_HERE, "cgtp_oracle.c")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the C oracle with gcc (plain -O2, no FMA contraction)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if force or not os.path.exists(_SO) or os.path.getmtime(_SO) < os.path.getmtime(_SRC):
+        tmp = _SO + f".{os.getpid()}.tmp"
+        subprocess.check_call(["gcc", "-O2", "-std=gnu11", "-fPIC", "-shared",
+                               "-ffp-contract=off", _SRC, "-lm", "-o", tmp])
+        os.replace(tmp, _SO)
+    return _SO
+
+
+class _Path(ctypes.Structure):
+    _fields_ = [("l1", ctypes.c_int), ("l2", ctypes.c_int), ("l3", ctypes.c_int),
+                ("mul", ctypes.c_int), ("off1", ctypes.c_int64), ("off2", ctypes.c_int64),
+                ("off3", ctypes.c_int64), ("offw", ctypes.c_int64)]
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            P = ctypes.POINTER
+            d, i64, i32 = ctypes.c_double, ctypes.c_int64, ctypes.c_int
+            pd = P(d)
+            pi32 = P(ctypes.c_int32)
+            lib.oracle_cg_real.argtypes = [i32, i32, i32, pd]
+            lib.oracle_sh.argtypes = [i32, i64, pd, pd]
+            lib.oracle_sh_vjp.argtypes = [i32, i64, pd, pd, pd]
+            lib.oracle_sh_jvp.argtypes = [i32, i64, pd, pd, pd]
+            lib.oracle_tp_forward.argtypes = [i32, P(_Path), i64, i64, i64, i64, i64, i64,
+                                              pd, pd, pd, pd]
+            lib.oracle_tp_backward.argtypes = [i32, P(_Path), i64, i64, i64, i64, i64, i64,
+                                               pd, pd, pd, pd, pd, pd, pd]
+            lib.oracle_conv_forward.argtypes = [i32, P(_Path), i64, i64, pi32, pi32, i64, i64,
+                                                i64, i64, i64, pd, pd, pd, d, pd, i64,
+                                                P(ctypes.c_int64)]
+            lib.oracle_conv_backward.argtypes = [i32, P(_Path), i64, i64, pi32, pi32, i64, i64,
+                                                 i64, i64, i64, pd, pd, pd, d, pd, pd, pd, pd,
+                                                 P(ctypes.c_uint8), P(ctypes.c_uint8)]
+            lib.oracle_edge_forces.argtypes = [i64, i64, pi32, pi32, pd, pd]
+            for f in ("oracle_cg_real", "oracle_sh", "oracle_sh_vjp", "oracle_sh_jvp",
+                      "oracle_tp_forward", "oracle_tp_backward", "oracle_conv_forward",
+                      "oracle_conv_backward", "oracle_edge_forces"):
+                getattr(lib, f).restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _f64(a):
+    return np.ascontiguousarray(a, dtype=np.float64)
+
+
+def _i32(a):
+    return np.ascontiguousarray(a, dtype=np.int32)
+
+
+def _p(a, t=ctypes.c_double):
+    if a is None:
+        return None
+    return a.ctypes.data_as(ctypes.POINTER(t))
+
+
+# --------------------------------------------------------------- irreps ---
+
+_IRREP = re.compile(r"^\s*(?:(\d+)\s*x\s*)?(\d+)\s*([eo])\s*$")
+
+
+def parse_irreps(s: str):
+    """'16x0e+16x1o' -> [(mul, l, parity)] with parity +1 (e) / -1 (o)."""
+    out = []
+    for tok in s.split("+"):
+        m = _IRREP.match(tok)
+        if not m:
+            raise ValueError(f"bad irrep {tok!r} in {s!r}")
+        mul = int(m.group(1)) if m.group(1) else 1
+        out.append((mul, int(m.group(2)), 1 if m.group(3) == "e" else -1))
+    return out
+
+
+def irreps_dim(irreps) -> int:
+    return sum(mul * (2 * l + 1) for mul, l, _ in irreps)
+
+
+@dataclass
+class Problem:
+    """Irreps of the two inputs and the output plus the 'uvu' path list."""
+    in1: list
+    in2: list
+    out: list
+    paths: list  # (i1, i2, i3, l1, l2, l3, mul, off1, off2, off3, offw)
+    dim1: int
+    dim2: int
+    dimo: int
+    wdim: int
+
+    def ctypes_paths(self):
+        arr = (_Path * max(1, len(self.paths)))()
+        for k, (_, _, _, l1, l2, l3, mul, o1, o2, o3, ow) in enumerate(self.paths):
+            arr[k] = _Path(l1, l2, l3, mul, o1, o2, o3, ow)
+        return arr
+
+
+def make_problem(irreps_in1: str, irreps_in2: str, irreps_out: str) -> Problem:
+    """All parity-allowed 'uvu' paths: for every (in1, in2, out) irrep triple with
+    |l1-l2| <= l3 <= l1+l2, p3 = p1 p2, mul(out) = mul(in1), mul(in2) = 1.
+    Paths are listed with in1 outermost, then in2, then out; weights of one
+    path form one block of mul in that order."""
+    a, b, c = parse_irreps(irreps_in1), parse_irreps(irreps_in2), parse_irreps(irreps_out)
+
+    def offsets(ir):
+        off, res = 0, []
+        for mul, l, _ in ir:
+            res.append(off)
+            off += mul * (2 * l + 1)
+        return res
+
+    oa, ob, oc = offsets(a), offsets(b), offsets(c)
+    paths, offw = [], 0
+    for i1, (m1, l1, p1) in enumerate(a):
+        for i2, (m2, l2, p2) in enumerate(b):
+            for i3, (m3, l3, p3) in enumerate(c):
+                if abs(l1 - l2) <= l3 <= l1 + l2 and p3 == p1 * p2 and m3 == m1 and m2 == 1:
+                    paths.append((i1, i2, i3, l1, l2, l3, m1, oa[i1], ob[i2], oc[i3], offw))
+                    offw += m1
+    return Problem(a, b, c, paths, irreps_dim(a), irreps_dim(b), irreps_dim(c), offw)
+
+
+# ------------------------------------------------------------------- CG ---
+
+def cg_real(l1: int, l2: int, l3: int) -> np.ndarray:
+    """Real-basis CG tensor [2l1+1, 2l2+1, 2l3+1] (zero if the triangle rule fails)."""
+    out = np.zeros((2 * l1 + 1) * (2 * l2 + 1) * (2 * l3 + 1))
+    r = _load().oracle_cg_real(l1, l2, l3, _p(out))
+    if r < 0:
+        raise ValueError("l out of range")
+    return out.reshape(2 * l1 + 1, 2 * l2 + 1, 2 * l3 + 1)
+
+
+# ------------------------------------------------- spherical harmonics ---
+
+def sh(lmax: int, vec) -> np.ndarray:
+    v = _f64(vec).reshape(-1, 3)
+    y = np.empty((v.shape[0], (lmax + 1) ** 2))
+    if _load().oracle_sh(lmax, v.shape[0], _p(v), _p(y)):
+        raise ValueError("lmax out of range")
+    return y
+
+
+def sh_vjp(lmax: int, vec, grad_y) -> np.ndarray:
+    v, g = _f64(vec).reshape(-1, 3), _f64(grad_y)
+    out = np.empty_like(v)
+    _load().oracle_sh_vjp(lmax, v.shape[0], _p(v), _p(g), _p(out))
+    return out
+
+
+def sh_jvp(lmax: int, vec, tangent_vec) -> np.ndarray:
+    v, t = _f64(vec).reshape(-1, 3), _f64(tangent_vec).reshape(-1, 3)
+    out = np.empty((v.shape[0], (lmax + 1) ** 2))
+    _load().oracle_sh_jvp(lmax, v.shape[0], _p(v), _p(t), _p(out))
+    return out
+
+
+# --------------------------------------------------------- tensor product --
+
+def _wstride(prob, w, rows):
+    w = _f64(w)
+    if w.ndim == 1:
+        return w, 0
+    return w, prob.wdim
+
+
+def tp_forward(prob: Problem, x, y, w) -> np.ndarray:
+    """out[b] = sum over paths of the 'uvu' CG product of x[b], y[b], w[b]
+    (a 1-D ``w`` is one weight row shared by every sample)."""
+    x, y = _f64(x), _f64(y)
+    B = x.shape[0]
+    w, ws = _wstride(prob, w, B)
+    out = np.zeros((B, prob.dimo))
+    r = _load().oracle_tp_forward(len(prob.paths), prob.ctypes_paths(), B, prob.dim1,
+                                  prob.dim2, prob.wdim, prob.dimo, ws, _p(x), _p(y), _p(w),
+                                  _p(out))
+    assert r == 0
+    return out
+
+
+def tp_backward(prob: Problem, x, y, w, g):
+    """(dL/dx, dL/dy, dL/dw) for dL/dout = g."""
+    x, y, g = _f64(x), _f64(y), _f64(g)
+    B = x.shape[0]
+    w, ws = _wstride(prob, w, B)
+    gx, gy = np.zeros_like(x), np.zeros_like(y)
+    gw = np.zeros((B, prob.wdim)) if ws else np.zeros(prob.wdim)
+    r = _load().oracle_tp_backward(len(prob.paths), prob.ctypes_paths(), B, prob.dim1,
+                                   prob.dim2, prob.wdim, prob.dimo, ws, _p(x), _p(y), _p(w),
+                                   _p(g), _p(gx), _p(gy), _p(gw))
+    assert r == 0
+    return gx, gy, gw
+
+
+def tp_double_backward(prob: Problem, x, y, w, g, ggx=None, ggy=None, ggw=None):
+    """Gradients of S = <ggx, dL/dx> + <ggy, dL/dy> + <ggw, dL/dw> with respect
+    to x, y, w and g, where (dL/dx, dL/dy, dL/dw) = tp_backward(x, y, w, g).
+
+    The pages name "a novel identity for the higher partial derivatives" but do
+    not state it.  Reading: f(x, y, w) is linear in each argument, so with the
+    first-order partials f_x, f_y, f_w,
+      d_g = f(ggx, y, w) + f(x, ggy, w) + f(x, y, ggw)
+      d_x = f_x(g; ggy, w) + f_x(g; y, ggw)
+      d_y = f_y(g; ggx, w) + f_y(g; x, ggw)
+      d_w = f_w(g; ggx, y) + f_w(g; x, ggy)
+    Absent cotangents are zero.  Returns (d_x, d_y, d_w, d_g)."""
+    x, y, w, g = _f64(x), _f64(y), _f64(w), _f64(g)
+    z = lambda a: np.zeros_like(a)
+    ggx = z(x) if ggx is None else _f64(ggx)
+    ggy = z(y) if ggy is None else _f64(ggy)
+    ggw = z(w) if ggw is None else _f64(ggw)
+    d_g = tp_forward(prob, ggx, y, w) + tp_forward(prob, x, ggy, w) + tp_forward(prob, x, y, ggw)
+    a = tp_backward(prob, x, ggy, w, g)   # f_x(g; ggy, w), f_w(g; x, ggy)
+    b = tp_backward(prob, x, y, ggw, g)   # f_x(g; y, ggw), f_y(g; x, ggw)
+    c = tp_backward(prob, ggx, y, w, g)   # f_y(g; ggx, w), f_w(g; ggx, y)
+    return a[0] + b[0], c[1] + b[1], c[2] + a[2], d_g
+
+
+# ------------------------------------------------------ graph convolution --
+
+def conv_forward(prob: Problem, rowptr, sender, x, y, w, scale: float, receivers=None):
+    """out[n] = scale * sum over the receiver's edges, in edge order, of
+    TP(x[sender[e]], y[e], w[e]).  With ``receivers`` only those rows are
+    computed (the others stay zero)."""
+    rowptr, sender = _i32(rowptr), _i32(sender)
+    x, y = _f64(x), _f64(y)
+    N, E = rowptr.shape[0] - 1, sender.shape[0]
+    w, ws = _wstride(prob, w, E)
+    out = np.zeros((N, prob.dimo))
+    sel = None if receivers is None else np.ascontiguousarray(receivers, dtype=np.int64)
+    r = _load().oracle_conv_forward(
+        len(prob.paths), prob.ctypes_paths(), N, E, _p(rowptr, ctypes.c_int32),
+        _p(sender, ctypes.c_int32), prob.dim1, prob.dim2, prob.wdim, prob.dimo, ws, _p(x),
+        _p(y), _p(w), float(scale), _p(out), 0 if sel is None else sel.shape[0],
+        _p(sel, ctypes.c_int64))
+    assert r == 0
+    return out
+
+
+def conv_backward(prob: Problem, rowptr, sender, x, y, w, scale: float, g, nodes=None,
+                  edges=None):
+    """(dL/dx [N, dim1], dL/dy [E, dim2], dL/dw [E, wdim]) for dL/dout = g.
+    dL/dx[s] sums over the edges whose sender is s, in edge order.  ``nodes`` /
+    ``edges`` restrict which rows are computed (others stay zero)."""
+    rowptr, sender = _i32(rowptr), _i32(sender)
+    x, y, g = _f64(x), _f64(y), _f64(g)
+    N, E = rowptr.shape[0] - 1, sender.shape[0]
+    w, ws = _wstride(prob, w, E)
+    gx, gy = np.zeros((N, prob.dim1)), np.zeros((E, prob.dim2))
+    gw = np.zeros((E, prob.wdim)) if ws else np.zeros(prob.wdim)
+    nm = em = None
+    if nodes is not None:
+        nm = np.zeros(N, dtype=np.uint8)
+        nm[np.asarray(nodes)] = 1
+    if edges is not None:
+        em = np.zeros(E, dtype=np.uint8)
+        em[np.asarray(edges)] = 1
+    r = _load().oracle_conv_backward(
+        len(prob.paths), prob.ctypes_paths(), N, E, _p(rowptr, ctypes.c_int32),
+        _p(sender, ctypes.c_int32), prob.dim1, prob.dim2, prob.wdim, prob.dimo, ws, _p(x),
+        _p(y), _p(w), float(scale), _p(g), _p(gx), _p(gy), _p(gw), _p(nm, ctypes.c_uint8),
+        _p(em, ctypes.c_uint8))
+    assert r == 0
+    return gx, gy, gw
+
+
+def conv_double_backward(prob: Problem, rowptr, sender, x, y, w, scale, g, ggx=None, ggy=None,
+                         ggw=None):
+    """The trilinear identity of ``tp_double_backward`` applied to the fused
+    convolution (gather by sender, TP per edge, receiver sum, scale).
+    Returns (d_x, d_y, d_w, d_g)."""
+    x, y, w, g = _f64(x), _f64(y), _f64(w), _f64(g)
+    z = lambda a: np.zeros_like(a)
+    ggx = z(x) if ggx is None else _f64(ggx)
+    ggy = z(y) if ggy is None else _f64(ggy)
+    ggw = z(w) if ggw is None else _f64(ggw)
+    f = lambda a, b, c: conv_forward(prob, rowptr, sender, a, b, c, scale)
+    bwd = lambda a, b, c: conv_backward(prob, rowptr, sender, a, b, c, scale, g)
+    d_g = f(ggx, y, w) + f(x, ggy, w) + f(x, y, ggw)
+    a = bwd(x, ggy, w)
+    b = bwd(x, y, ggw)
+    c = bwd(ggx, y, w)
+    return a[0] + b[0], c[1] + b[1], c[2] + a[2], d_g
+
+
+def edge_forces(rowptr, sender, dEdr) -> np.ndarray:
+    """F_i = -sum_e dE/dr_e (delta(i, recv e) - delta(i, send e)),
+    r_e = pos[recv] - pos[send]."""
+    rowptr, sender = _i32(rowptr), _i32(sender)
+    d = _f64(dEdr).reshape(-1, 3)
+    N = rowptr.shape[0] - 1
+    F = np.zeros((N, 3))
+    _load().oracle_edge_forces(N, sender.shape[0], _p(rowptr, ctypes.c_int32),
+                               _p(sender, ctypes.c_int32), _p(d), _p(F))
+    return F
