@@ -69,6 +69,8 @@ def _load():
             pd = P(d)
             pi32 = P(ctypes.c_int32)
             lib.oracle_cg_real.argtypes = [i32, i32, i32, pd]
+            lib.oracle_cg_complex.argtypes = [i32] * 6
+            lib.oracle_cg_complex.restype = d
             lib.oracle_sh.argtypes = [i32, i64, pd, pd]
             lib.oracle_sh_vjp.argtypes = [i32, i64, pd, pd, pd]
             lib.oracle_sh_jvp.argtypes = [i32, i64, pd, pd, pd]
@@ -171,6 +173,11 @@ def make_problem(irreps_in1: str, irreps_in2: str, irreps_out: str) -> Problem:
 
 
 # ------------------------------------------------------------------- CG ---
+
+def cg_complex(l1: int, m1: int, l2: int, m2: int, l3: int, m3: int) -> float:
+    """<l1 m1 l2 m2 | l3 m3> (Condon-Shortley phase), Racah's closed form."""
+    return float(_load().oracle_cg_complex(l1, m1, l2, m2, l3, m3))
+
 
 def cg_real(l1: int, l2: int, l3: int) -> np.ndarray:
     """Real-basis CG tensor [2l1+1, 2l2+1, 2l3+1] (zero if the triangle rule fails)."""

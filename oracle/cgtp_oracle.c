@@ -77,6 +77,11 @@ static long double cg_complex(int l1, int m1, int l2, int m2, int l3, int m3) {
     return sqrtl(pre) * sqrtl(mterm) * s;
 }
 
+/* Exported for the pin against a library CG table. */
+double oracle_cg_complex(int l1, int m1, int l2, int m2, int l3, int m3) {
+    return (double)cg_complex(l1, m1, l2, m2, l3, m3);
+}
+
 /* Row r (real m = r - l) of the map from complex to real spherical harmonics:
  *   real m<0 : (i/sqrt2) (Y^m - (-1)^m Y^-m)
  *   real m=0 : Y^0
