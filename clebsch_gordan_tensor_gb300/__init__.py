@@ -1,0 +1,361 @@
+"""Clebsch-Gordan tensor products on GB300 (sm_103a): Python binding.
+
+A thin ctypes layer over the C ABI of ``libcgtp.so`` (declared in
+``include/cgtp.h``).  It marshals torch CUDA tensors into pointers and the
+current torch stream; every step of the computation runs in the library's own
+kernels.  If the library has not been built, every entry point raises -- there
+is no CPU fallback.
+
+Operations (see "An Efficient Sparse Kernel Generator for O(3)-Equivariant
+Deep Networks", abstract): the CG tensor product of irrep features x and
+spherical harmonics y under per-edge 'uvu' weights, standalone and fused with
+the graph convolution, with gradients and higher derivatives; spherical
+harmonics of edge vectors (NVIDIA SE(3)-Transformer blog, "Basis
+precomputation") and interatomic forces from edge gradients.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libcgtp.so")
+
+_lock = threading.Lock()
+_lib = None
+
+F32, F64 = 0, 1
+W_PER_EDGE, W_SHARED = 0, 1
+
+
+class CgtpError(RuntimeError):
+    pass
+
+
+class _Instr(ctypes.Structure):
+    _fields_ = [("i_in1", ctypes.c_int), ("i_in2", ctypes.c_int), ("i_out", ctypes.c_int),
+                ("mode", ctypes.c_char * 4)]
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded C library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise CgtpError(f"{LIB_PATH} is missing: build it with "
+                                "`python -m clebsch_gordan_tensor_gb300.build`")
+            L = ctypes.CDLL(LIB_PATH)
+            vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+            P = ctypes.POINTER
+            sig = {
+                "cgtp_plan_create": [P(vp), ctypes.c_char_p, ctypes.c_char_p, ctypes.c_char_p,
+                                     P(_Instr), i32, i32, i32, ctypes.c_uint],
+                "cgtp_plan_destroy": [vp],
+                "cgtp_plan_info": [vp, P(i64), P(i64), P(i64), P(i64), P(i32)],
+                "cgtp_plan_path": [vp, i32, P(i32), P(i32), P(i32), P(i32), P(i32), P(i32)],
+                "cgtp_plan_coefficients": [vp, i32, P(ctypes.c_double)],
+                "cgtp_plan_compile": [vp, ctypes.c_char_p, ctypes.c_size_t],
+                "cgtp_plan_source": [vp, ctypes.c_char_p, ctypes.c_size_t, P(ctypes.c_size_t)],
+                "cgtp_forward": [vp, i64, vp, vp, vp, vp, vp],
+                "cgtp_backward": [vp, i64, vp, vp, vp, vp, vp, vp, vp, vp],
+                "cgtp_double_backward": [vp, i64, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp],
+                "cgtp_conv_forward": [vp, i64, i64, vp, vp, vp, vp, vp, ctypes.c_double, vp, vp],
+                "cgtp_conv_backward": [vp, i64, i64, vp, vp, vp, vp, vp, vp, vp, vp,
+                                       ctypes.c_double, vp, vp, vp, vp, vp],
+                "cgtp_conv_double_backward": [vp, i64, i64, vp, vp, vp, vp, vp, vp, vp, vp,
+                                              ctypes.c_double, vp, vp, vp, vp, vp, vp, vp, vp,
+                                              vp],
+                "cgtp_sh_forward": [i32, i32, i64, vp, vp, vp],
+                "cgtp_sh_backward": [i32, i32, i64, vp, vp, vp, vp],
+                "cgtp_sh_jvp": [i32, i32, i64, vp, vp, vp, vp],
+                "cgtp_edge_forces": [i32, i64, i64, vp, vp, vp, vp, vp, vp],
+                "cgtp_edge_forces_adjoint": [i32, i64, i64, vp, vp, vp, vp, vp],
+                "cgtp_last_cuda_error": [P(i32)],
+            }
+            for name, args in sig.items():
+                f = getattr(L, name)
+                f.argtypes = args
+                f.restype = ctypes.c_int
+            L.cgtp_status_str.argtypes = [ctypes.c_int]
+            L.cgtp_status_str.restype = ctypes.c_char_p
+            L.cgtp_last_error_message.argtypes = []
+            L.cgtp_last_error_message.restype = ctypes.c_char_p
+            L.cgtp_launch_count.argtypes = []
+            L.cgtp_launch_count.restype = ctypes.c_int64
+            _lib = L
+    return _lib
+
+
+def _check(st: int) -> None:
+    if st != 0:
+        L = lib()
+        msg = L.cgtp_last_error_message().decode(errors="replace")
+        raise CgtpError(f"{L.cgtp_status_str(st).decode()} (status {st}): {msg}")
+
+
+def launch_count() -> int:
+    """Kernel launches issued through the library by this process."""
+    return int(lib().cgtp_launch_count())
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _dt(dtype) -> int:
+    if dtype == torch.float32:
+        return F32
+    if dtype == torch.float64:
+        return F64
+    raise CgtpError(f"unsupported dtype {dtype}")
+
+
+def _need(t, name, dtype, shape=None):
+    if t is None:
+        return
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise CgtpError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise CgtpError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if not t.is_contiguous():
+        raise CgtpError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise CgtpError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+class Graph:
+    """Receiver-sorted CSR (rowptr, sender) plus the sender-grouped view
+    (s_rowptr, s_perm, s_recv), as int32 CUDA tensors."""
+
+    def __init__(self, N, rowptr, sender, s_rowptr=None, s_perm=None, s_recv=None):
+        self.N = int(N)
+        self.rowptr, self.sender = rowptr, sender
+        self.s_rowptr, self.s_perm, self.s_recv = s_rowptr, s_perm, s_recv
+        self.E = int(sender.shape[0])
+        for n, t in (("rowptr", rowptr), ("sender", sender), ("s_rowptr", s_rowptr),
+                     ("s_perm", s_perm), ("s_recv", s_recv)):
+            _need(t, n, torch.int32)
+        if rowptr.shape[0] != self.N + 1:
+            raise CgtpError("rowptr must have N+1 entries")
+
+    @classmethod
+    def from_numpy(cls, g, device="cuda"):
+        """From a workloads.Graph-like object with numpy int32 arrays."""
+        t = lambda a: torch.from_numpy(a).to(device=device, dtype=torch.int32).contiguous()
+        return cls(g.N, t(g.rowptr), t(g.sender), t(g.s_rowptr), t(g.s_perm), t(g.s_recv))
+
+
+class Plan:
+    """A tensor-product plan: irreps, 'uvu' paths and the real CG tables, with
+    its kernels compiled for sm_103a on first use."""
+
+    def __init__(self, irreps_in1: str, irreps_in2: str, irreps_out: str,
+                 dtype=torch.float32, shared_weights: bool = False, instructions=None):
+        L = lib()
+        self.dtype = dtype
+        self.irreps = (irreps_in1, irreps_in2, irreps_out)
+        h = ctypes.c_void_p()
+        arr, n = None, 0
+        if instructions is not None:
+            n = len(instructions)
+            arr = (_Instr * max(1, n))()
+            for k, (a, b, c) in enumerate(instructions):
+                arr[k] = _Instr(a, b, c, b"uvu")
+        _check(L.cgtp_plan_create(ctypes.byref(h), irreps_in1.encode(), irreps_in2.encode(),
+                                  irreps_out.encode(), arr, n, _dt(dtype),
+                                  W_SHARED if shared_weights else W_PER_EDGE, 0))
+        self._h = h
+        d1, d2, do, wn = (ctypes.c_int64() for _ in range(4))
+        npth = ctypes.c_int()
+        _check(L.cgtp_plan_info(h, ctypes.byref(d1), ctypes.byref(d2), ctypes.byref(do),
+                                ctypes.byref(wn), ctypes.byref(npth)))
+        self.dim_in1, self.dim_in2, self.dim_out = d1.value, d2.value, do.value
+        self.weight_numel, self.n_paths = wn.value, npth.value
+        self.shared_weights = shared_weights
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h is not None and _lib is not None:
+            _lib.cgtp_plan_destroy(h)
+            self._h = None
+
+    # ---- host queries
+    def path(self, p: int):
+        vals = [ctypes.c_int() for _ in range(6)]
+        _check(lib().cgtp_plan_path(self._h, p, *[ctypes.byref(v) for v in vals]))
+        return tuple(v.value for v in vals)
+
+    def coefficients(self, p: int):
+        import numpy as np
+        l1, l2, l3 = self.path(p)[:3]
+        out = np.zeros((2 * l1 + 1) * (2 * l2 + 1) * (2 * l3 + 1))
+        _check(lib().cgtp_plan_coefficients(self._h, p, out.ctypes.data_as(
+            ctypes.POINTER(ctypes.c_double))))
+        return out.reshape(2 * l1 + 1, 2 * l2 + 1, 2 * l3 + 1)
+
+    def compile(self) -> str:
+        buf = ctypes.create_string_buffer(1 << 16)
+        _check(lib().cgtp_plan_compile(self._h, buf, len(buf)))
+        return buf.value.decode(errors="replace")
+
+    def source(self) -> str:
+        need = ctypes.c_size_t()
+        _check(lib().cgtp_plan_source(self._h, None, 0, ctypes.byref(need)))
+        buf = ctypes.create_string_buffer(need.value)
+        _check(lib().cgtp_plan_source(self._h, buf, need.value, None))
+        return buf.value.decode()
+
+    def _wshape(self, rows):
+        return (self.weight_numel,) if self.shared_weights else (rows, self.weight_numel)
+
+    # ---- standalone
+    def forward(self, x, y, w, out=None):
+        B = x.shape[0]
+        _need(x, "x", self.dtype, (B, self.dim_in1))
+        _need(y, "y", self.dtype, (B, self.dim_in2))
+        _need(w, "w", self.dtype, self._wshape(B))
+        if out is None:
+            out = torch.empty(B, self.dim_out, dtype=self.dtype, device=x.device)
+        _need(out, "out", self.dtype, (B, self.dim_out))
+        _check(lib().cgtp_forward(self._h, B, _ptr(x), _ptr(y), _ptr(w), _ptr(out), _stream()))
+        return out
+
+    def backward(self, x, y, w, grad_out, need=(True, True, True)):
+        B = x.shape[0]
+        _need(x, "x", self.dtype, (B, self.dim_in1))
+        _need(y, "y", self.dtype, (B, self.dim_in2))
+        _need(w, "w", self.dtype, self._wshape(B))
+        _need(grad_out, "grad_out", self.dtype, (B, self.dim_out))
+        gx = torch.empty_like(x) if need[0] else None
+        gy = torch.empty_like(y) if need[1] else None
+        gw = torch.empty_like(w) if need[2] else None
+        _check(lib().cgtp_backward(self._h, B, _ptr(x), _ptr(y), _ptr(w), _ptr(grad_out),
+                                   _ptr(gx), _ptr(gy), _ptr(gw), _stream()))
+        return gx, gy, gw
+
+    def double_backward(self, x, y, w, grad_out, gg_x=None, gg_y=None, gg_w=None,
+                        need=(True, True, True, True)):
+        B = x.shape[0]
+        for n, t, s in (("x", x, (B, self.dim_in1)), ("y", y, (B, self.dim_in2)),
+                        ("w", w, self._wshape(B)), ("grad_out", grad_out, (B, self.dim_out)),
+                        ("gg_x", gg_x, (B, self.dim_in1)), ("gg_y", gg_y, (B, self.dim_in2)),
+                        ("gg_w", gg_w, self._wshape(B))):
+            _need(t, n, self.dtype, s)
+        dx = torch.empty_like(x) if need[0] else None
+        dy = torch.empty_like(y) if need[1] else None
+        dw = torch.empty_like(w) if need[2] else None
+        dg = torch.empty_like(grad_out) if need[3] else None
+        _check(lib().cgtp_double_backward(self._h, B, _ptr(x), _ptr(y), _ptr(w), _ptr(grad_out),
+                                          _ptr(gg_x), _ptr(gg_y), _ptr(gg_w), _ptr(dx), _ptr(dy),
+                                          _ptr(dw), _ptr(dg), _stream()))
+        return dx, dy, dw, dg
+
+    # ---- fused convolution
+    def _conv_check(self, g: Graph, x, y, w):
+        _need(x, "x", self.dtype, (g.N, self.dim_in1))
+        _need(y, "y", self.dtype, (g.E, self.dim_in2))
+        _need(w, "w", self.dtype, self._wshape(g.E))
+
+    def conv_forward(self, g: Graph, x, y, w, scale: float = 1.0, out=None):
+        self._conv_check(g, x, y, w)
+        if out is None:
+            out = torch.empty(g.N, self.dim_out, dtype=self.dtype, device=x.device)
+        _need(out, "out", self.dtype, (g.N, self.dim_out))
+        _check(lib().cgtp_conv_forward(self._h, g.N, g.E, _ptr(g.rowptr), _ptr(g.sender),
+                                       _ptr(x), _ptr(y), _ptr(w), float(scale), _ptr(out),
+                                       _stream()))
+        return out
+
+    def conv_backward(self, g: Graph, x, y, w, scale, grad_out, need=(True, True, True),
+                      out=None):
+        self._conv_check(g, x, y, w)
+        _need(grad_out, "grad_out", self.dtype, (g.N, self.dim_out))
+        if out is not None:
+            gx, gy, gw = out
+        else:
+            gx = torch.empty_like(x) if need[0] else None
+            gy = torch.empty_like(y) if need[1] else None
+            gw = torch.empty_like(w) if need[2] else None
+        _check(lib().cgtp_conv_backward(self._h, g.N, g.E, _ptr(g.rowptr), _ptr(g.sender),
+                                        _ptr(g.s_rowptr), _ptr(g.s_perm), _ptr(g.s_recv),
+                                        _ptr(x), _ptr(y), _ptr(w), float(scale), _ptr(grad_out),
+                                        _ptr(gx), _ptr(gy), _ptr(gw), _stream()))
+        return gx, gy, gw
+
+    def conv_double_backward(self, g: Graph, x, y, w, scale, grad_out, gg_x=None, gg_y=None,
+                             gg_w=None, need=(True, True, True, True)):
+        self._conv_check(g, x, y, w)
+        _need(grad_out, "grad_out", self.dtype, (g.N, self.dim_out))
+        _need(gg_x, "gg_x", self.dtype, (g.N, self.dim_in1))
+        _need(gg_y, "gg_y", self.dtype, (g.E, self.dim_in2))
+        _need(gg_w, "gg_w", self.dtype, self._wshape(g.E))
+        dx = torch.empty_like(x) if need[0] else None
+        dy = torch.empty_like(y) if need[1] else None
+        dw = torch.empty_like(w) if need[2] else None
+        dg = torch.empty_like(grad_out) if need[3] else None
+        _check(lib().cgtp_conv_double_backward(
+            self._h, g.N, g.E, _ptr(g.rowptr), _ptr(g.sender), _ptr(g.s_rowptr), _ptr(g.s_perm),
+            _ptr(g.s_recv), _ptr(x), _ptr(y), _ptr(w), float(scale), _ptr(grad_out), _ptr(gg_x),
+            _ptr(gg_y), _ptr(gg_w), _ptr(dx), _ptr(dy), _ptr(dw), _ptr(dg), _stream()))
+        return dx, dy, dw, dg
+
+
+# ------------------------------------------------------ spherical harmonics
+
+def sh_forward(vec, lmax: int, out=None):
+    E = vec.shape[0]
+    _need(vec, "vec", vec.dtype, (E, 3))
+    if out is None:
+        out = torch.empty(E, (lmax + 1) ** 2, dtype=vec.dtype, device=vec.device)
+    _need(out, "out", vec.dtype, (E, (lmax + 1) ** 2))
+    _check(lib().cgtp_sh_forward(lmax, _dt(vec.dtype), E, _ptr(vec), _ptr(out), _stream()))
+    return out
+
+
+def sh_backward(vec, grad_y, lmax: int, out=None):
+    E = vec.shape[0]
+    _need(vec, "vec", vec.dtype, (E, 3))
+    _need(grad_y, "grad_y", vec.dtype, (E, (lmax + 1) ** 2))
+    if out is None:
+        out = torch.empty_like(vec)
+    _check(lib().cgtp_sh_backward(lmax, _dt(vec.dtype), E, _ptr(vec), _ptr(grad_y), _ptr(out),
+                                  _stream()))
+    return out
+
+
+def sh_jvp(vec, tangent_vec, lmax: int, out=None):
+    E = vec.shape[0]
+    _need(vec, "vec", vec.dtype, (E, 3))
+    _need(tangent_vec, "tangent_vec", vec.dtype, (E, 3))
+    if out is None:
+        out = torch.empty(E, (lmax + 1) ** 2, dtype=vec.dtype, device=vec.device)
+    _check(lib().cgtp_sh_jvp(lmax, _dt(vec.dtype), E, _ptr(vec), _ptr(tangent_vec), _ptr(out),
+                             _stream()))
+    return out
+
+
+def edge_forces(g: Graph, dEdr, out=None):
+    _need(dEdr, "dEdr", dEdr.dtype, (g.E, 3))
+    if out is None:
+        out = torch.empty(g.N, 3, dtype=dEdr.dtype, device=dEdr.device)
+    _check(lib().cgtp_edge_forces(_dt(dEdr.dtype), g.N, g.E, _ptr(g.rowptr), _ptr(g.s_rowptr),
+                                  _ptr(g.s_perm), _ptr(dEdr), _ptr(out), _stream()))
+    return out
+
+
+def edge_forces_adjoint(g: Graph, grad_forces, out=None):
+    _need(grad_forces, "grad_forces", grad_forces.dtype, (g.N, 3))
+    if out is None:
+        out = torch.empty(g.E, 3, dtype=grad_forces.dtype, device=grad_forces.device)
+    _check(lib().cgtp_edge_forces_adjoint(_dt(grad_forces.dtype), g.N, g.E, _ptr(g.rowptr),
+                                          _ptr(g.sender), _ptr(grad_forces), _ptr(out),
+                                          _stream()))
+    return out

@@ -1,0 +1,510 @@
+// extern "C" entry points of the CG tensor-product library (declared in cgtp.h).
+//
+// Every call validates its arguments on the host, then launches kernels on the
+// caller's stream.  Nothing here allocates device memory.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <climits>
+#include <cstring>
+#include <new>
+#include <string>
+
+#include "cgtp.h"
+#include "internal.hpp"
+
+struct cgtp_plan_s {
+    cgtp::Plan p;
+};
+
+namespace cgtp {
+
+static thread_local int t_cuda_err = 0;
+static thread_local std::string t_msg;
+static std::atomic<int64_t> g_launches{0};
+
+void set_cuda_error(cudaError_t e) { t_cuda_err = (int)e; }
+void set_error_message(const std::string& m) { t_msg = m; }
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+static cgtp_status fail(cgtp_status s, const std::string& m) {
+    t_msg = m;
+    return s;
+}
+
+static cgtp_status cuda_fail(cudaError_t e, const char* what) {
+    t_cuda_err = (int)e;
+    t_msg = std::string(what) + ": " + cudaGetErrorString(e);
+    return CGTP_E_CUDA;
+}
+
+static bool aligned(const void* p, size_t a) { return p == nullptr || ((uintptr_t)p % a) == 0; }
+
+// Alignment the plan's kernels need for feature, weight and gradient rows.
+static size_t row_align(const Plan& p) {
+    return p.dtype == CGTP_F64 ? 8 : (p.cpt == 2 ? 8 : 4);
+}
+
+static cgtp_status check_rows(const Plan& p, std::initializer_list<const void*> ptrs) {
+    const size_t a = row_align(p);
+    for (const void* q : ptrs)
+        if (!aligned(q, a))
+            return fail(CGTP_E_ARG, "tensor pointer not aligned to " + std::to_string(a) + " bytes");
+    return CGTP_OK;
+}
+
+static cgtp_status launch_tp(Plan& p, const char* name, int64_t n_items, void** args,
+                             cudaStream_t s) {
+    if (n_items <= 0) return CGTP_OK;
+    std::shared_ptr<Module> m;
+    std::string err;
+    cgtp_status st = get_module(p, true, m, err);
+    if (st != CGTP_OK) return fail(st, err);
+    int64_t blocks = (n_items + p.slots - 1) / p.slots;
+    if (blocks > INT_MAX) blocks = INT_MAX;
+    cudaError_t e = cudaLaunchKernel((const void*)m->kernels[name], dim3((unsigned)blocks),
+                                     dim3(p.block), args, 0, s);
+    if (e != cudaSuccess) return cuda_fail(e, name);
+    count_launch();
+    return CGTP_OK;
+}
+
+// One forward-shaped launch: out (=|+=) scale * sum TP(a, b, c).
+static cgtp_status fwd_launch(Plan& p, bool conv, int64_t n_items, const int32_t* rowptr,
+                              const int32_t* sender, const void* a, const void* b, const void* c,
+                              double scale, void* out, int accumulate, cudaStream_t s) {
+    long long n = n_items;
+    long long ws = p.wmode == CGTP_W_SHARED ? 0 : p.wdim;
+    float sf = (float)scale;
+    double sd = scale;
+    void* sp = p.dtype == CGTP_F64 ? (void*)&sd : (void*)&sf;
+    if (conv) {
+        void* args[] = {&n, &rowptr, &sender, &a, &b, &c, &ws, &out, sp, &accumulate};
+        return launch_tp(p, "cgtp_fwd_conv", n_items, args, s);
+    }
+    void* args[] = {&n, &a, &b, &c, &ws, &out, sp, &accumulate};
+    return launch_tp(p, "cgtp_fwd_single", n_items, args, s);
+}
+
+// One backward-shaped launch over items (senders or samples).
+static cgtp_status bwd_launch(Plan& p, bool conv, int64_t n_items, const int32_t* s_rowptr,
+                              const int32_t* s_perm, const int32_t* s_recv, const void* x,
+                              const void* y, const void* w, const void* g, double scale, void* gx,
+                              void* gy, void* gw, int mgx, int mgy, int mgw, cudaStream_t s) {
+    if (!mgx && !mgy && !mgw) return CGTP_OK;
+    long long n = n_items;
+    long long ws = p.wmode == CGTP_W_SHARED ? 0 : p.wdim;
+    float sf = (float)scale;
+    double sd = scale;
+    void* sp = p.dtype == CGTP_F64 ? (void*)&sd : (void*)&sf;
+    void* args[] = {&n, &s_rowptr, &s_perm, &s_recv, &x, &y, &w, &ws, &g, sp,
+                    &gx, &gy, &gw, &mgx, &mgy, &mgw};
+    const char* name = conv ? (mgy ? "cgtp_bwd_conv" : "cgtp_bwd_conv_nogy")
+                            : (mgy ? "cgtp_bwd_single" : "cgtp_bwd_single_nogy");
+    return launch_tp(p, name, n_items, args, s);
+}
+
+static size_t esize(const Plan& p) { return p.dtype == CGTP_F64 ? 8 : 4; }
+
+static cgtp_status zero(void* ptr, int64_t bytes, cudaStream_t s) {
+    if (!ptr || bytes <= 0) return CGTP_OK;
+    cudaError_t e = launch_fill_zero(ptr, bytes, s);
+    if (e != cudaSuccess) return cuda_fail(e, "fill_zero");
+    count_launch();
+    return CGTP_OK;
+}
+
+// Shared body of the standalone and convolution double backward.
+static cgtp_status double_backward(Plan& p, bool conv, int64_t n_x, int64_t n_e,
+                                   int64_t n_out, const int32_t* rowptr, const int32_t* sender,
+                                   const int32_t* s_rowptr, const int32_t* s_perm,
+                                   const int32_t* s_recv, const void* x, const void* y,
+                                   const void* w, double scale, const void* g, const void* ggx,
+                                   const void* ggy, const void* ggw, void* dx, void* dy, void* dw,
+                                   void* dg, cudaStream_t s) {
+    cgtp_status st;
+    if (p.wmode == CGTP_W_SHARED && dw)
+        return fail(CGTP_E_UNSUPPORTED, "weight gradient of shared weights is not implemented");
+    if (dg) {
+        int acc = 0;
+        const void* terms[3][3] = {{ggx, y, w}, {x, ggy, w}, {x, y, ggw}};
+        const bool live[3] = {ggx != nullptr, ggy != nullptr, ggw != nullptr};
+        for (int t = 0; t < 3; ++t) {
+            if (!live[t]) continue;
+            st = fwd_launch(p, conv, n_out, rowptr, sender, terms[t][0], terms[t][1], terms[t][2],
+                            scale, dg, acc, s);
+            if (st != CGTP_OK) return st;
+            acc = 1;
+        }
+        if (!acc && (st = zero(dg, n_out * p.dimo * (int64_t)esize(p), s)) != CGTP_OK) return st;
+    }
+    int wx = 0, wy = 0, ww = 0;  // already written?
+    auto mode = [](void* out, int& written) {
+        if (!out) return 0;
+        const int m = written ? 2 : 1;
+        written = 1;
+        return m;
+    };
+    if (ggy) {  // f_x(g; ggy, w) -> dx, f_w(g; x, ggy) -> dw
+        const int mx = mode(dx, wx), mw = mode(dw, ww);
+        st = bwd_launch(p, conv, n_x, s_rowptr, s_perm, s_recv, x, ggy, w, g, scale, dx, nullptr,
+                        dw, mx, 0, mw, s);
+        if (st != CGTP_OK) return st;
+    }
+    if (ggw) {  // f_x(g; y, ggw) -> dx, f_y(g; x, ggw) -> dy
+        const int mx = mode(dx, wx), my = mode(dy, wy);
+        st = bwd_launch(p, conv, n_x, s_rowptr, s_perm, s_recv, x, y, ggw, g, scale, dx, dy,
+                        nullptr, mx, my, 0, s);
+        if (st != CGTP_OK) return st;
+    }
+    if (ggx) {  // f_y(g; ggx, w) -> dy, f_w(g; ggx, y) -> dw
+        const int my = mode(dy, wy), mw = mode(dw, ww);
+        st = bwd_launch(p, conv, n_x, s_rowptr, s_perm, s_recv, ggx, y, w, g, scale, nullptr, dy,
+                        dw, 0, my, mw, s);
+        if (st != CGTP_OK) return st;
+    }
+    const int64_t es = esize(p);
+    if (dx && !wx && (st = zero(dx, n_x * p.dimx * es, s)) != CGTP_OK) return st;
+    if (dy && !wy && (st = zero(dy, n_e * p.dimy * es, s)) != CGTP_OK) return st;
+    if (dw && !ww && (st = zero(dw, n_e * p.wdim * es, s)) != CGTP_OK) return st;
+    return CGTP_OK;
+}
+
+}  // namespace cgtp
+
+using namespace cgtp;
+
+#define GUARD_BEGIN try {
+#define GUARD_END                                                  \
+    }                                                              \
+    catch (const std::bad_alloc&) {                                \
+        return fail(CGTP_E_NOMEM, "host allocation failed");       \
+    }                                                              \
+    catch (...) {                                                  \
+        return fail(CGTP_E_ARG, "unexpected internal exception");  \
+    }
+
+static inline cudaStream_t S(cgtp_stream s) { return reinterpret_cast<cudaStream_t>(s); }
+
+extern "C" {
+
+cgtp_status cgtp_plan_create(cgtp_plan* out, const char* irreps_in1, const char* irreps_in2,
+                             const char* irreps_out, const cgtp_instr* instr, int n_instr,
+                             cgtp_dtype dtype, cgtp_wmode wmode, unsigned flags) {
+    GUARD_BEGIN
+    if (!out) return fail(CGTP_E_ARG, "out is NULL");
+    *out = nullptr;
+    if (dtype != CGTP_F32 && dtype != CGTP_F64) return fail(CGTP_E_ARG, "bad dtype");
+    if (wmode != CGTP_W_PER_EDGE && wmode != CGTP_W_SHARED) return fail(CGTP_E_ARG, "bad wmode");
+    auto* h = new cgtp_plan_s();
+    h->p.dtype = dtype;
+    h->p.wmode = wmode;
+    h->p.flags = flags;
+    std::string err;
+    cgtp_status st = build_plan(h->p, irreps_in1, irreps_in2, irreps_out, instr, n_instr, err);
+    if (st != CGTP_OK) {
+        delete h;
+        return fail(st, err);
+    }
+    *out = h;
+    return CGTP_OK;
+    GUARD_END
+}
+
+cgtp_status cgtp_plan_destroy(cgtp_plan plan) {
+    GUARD_BEGIN
+    delete plan;
+    return CGTP_OK;
+    GUARD_END
+}
+
+cgtp_status cgtp_plan_info(cgtp_plan plan, int64_t* dim_in1, int64_t* dim_in2, int64_t* dim_out,
+                           int64_t* weight_numel, int* n_paths) {
+    if (!plan) return fail(CGTP_E_ARG, "plan is NULL");
+    const Plan& p = plan->p;
+    if (dim_in1) *dim_in1 = p.dimx;
+    if (dim_in2) *dim_in2 = p.dimy;
+    if (dim_out) *dim_out = p.dimo;
+    if (weight_numel) *weight_numel = p.wdim;
+    if (n_paths) *n_paths = (int)p.paths.size();
+    return CGTP_OK;
+}
+
+cgtp_status cgtp_plan_path(cgtp_plan plan, int q, int* l1, int* l2, int* l3, int* i1, int* i2,
+                           int* i3) {
+    if (!plan || q < 0 || q >= (int)plan->p.paths.size()) return fail(CGTP_E_ARG, "bad path");
+    const Path& P = plan->p.paths[q];
+    if (l1) *l1 = P.l1;
+    if (l2) *l2 = P.l2;
+    if (l3) *l3 = P.l3;
+    if (i1) *i1 = P.i1;
+    if (i2) *i2 = P.i2;
+    if (i3) *i3 = P.i3;
+    return CGTP_OK;
+}
+
+cgtp_status cgtp_plan_coefficients(cgtp_plan plan, int q, double* out) {
+    if (!plan || !out || q < 0 || q >= (int)plan->p.paths.size())
+        return fail(CGTP_E_ARG, "bad path or NULL out");
+    const auto& c = plan->p.paths[q].cg;
+    memcpy(out, c.data(), c.size() * sizeof(double));
+    return CGTP_OK;
+}
+
+cgtp_status cgtp_plan_compile(cgtp_plan plan, char* log, size_t cap) {
+    GUARD_BEGIN
+    if (!plan) return fail(CGTP_E_ARG, "plan is NULL");
+    std::shared_ptr<Module> m;
+    std::string err;
+    cgtp_status st = get_module(plan->p, false, m, err);
+    if (st != CGTP_OK) return fail(st, err);
+    if (log && cap) {
+        strncpy(log, m->log.c_str(), cap - 1);
+        log[cap - 1] = 0;
+    }
+    return CGTP_OK;
+    GUARD_END
+}
+
+cgtp_status cgtp_plan_source(cgtp_plan plan, char* buf, size_t cap, size_t* needed) {
+    GUARD_BEGIN
+    if (!plan) return fail(CGTP_E_ARG, "plan is NULL");
+    const std::string src = plan->p.kernel_source();
+    if (needed) *needed = src.size() + 1;
+    if (buf && cap) {
+        strncpy(buf, src.c_str(), cap - 1);
+        buf[cap - 1] = 0;
+    }
+    return CGTP_OK;
+    GUARD_END
+}
+
+cgtp_status cgtp_forward(cgtp_plan plan, int64_t B, const void* x, const void* y, const void* w,
+                         void* out, cgtp_stream stream) {
+    GUARD_BEGIN
+    if (!plan) return fail(CGTP_E_ARG, "plan is NULL");
+    if (B < 0) return fail(CGTP_E_ARG, "B < 0");
+    if (B == 0) return CGTP_OK;
+    if (!x || !y || !w || !out) return fail(CGTP_E_ARG, "NULL tensor");
+    Plan& p = plan->p;
+    cgtp_status st = check_rows(p, {x, w, out});
+    if (st != CGTP_OK) return st;
+    return fwd_launch(p, false, B, nullptr, nullptr, x, y, w, 1.0, out, 0, S(stream));
+    GUARD_END
+}
+
+cgtp_status cgtp_backward(cgtp_plan plan, int64_t B, const void* x, const void* y, const void* w,
+                          const void* grad_out, void* grad_x, void* grad_y, void* grad_w,
+                          cgtp_stream stream) {
+    GUARD_BEGIN
+    if (!plan) return fail(CGTP_E_ARG, "plan is NULL");
+    if (B < 0) return fail(CGTP_E_ARG, "B < 0");
+    if (B == 0) return CGTP_OK;
+    if (!x || !y || !w || !grad_out) return fail(CGTP_E_ARG, "NULL input tensor");
+    Plan& p = plan->p;
+    if (p.wmode == CGTP_W_SHARED && grad_w)
+        return fail(CGTP_E_UNSUPPORTED, "weight gradient of shared weights is not implemented");
+    cgtp_status st = check_rows(p, {x, w, grad_out, grad_x, grad_w});
+    if (st != CGTP_OK) return st;
+    return bwd_launch(p, false, B, nullptr, nullptr, nullptr, x, y, w, grad_out, 1.0, grad_x,
+                      grad_y, grad_w, grad_x ? 1 : 0, grad_y ? 1 : 0, grad_w ? 1 : 0, S(stream));
+    GUARD_END
+}
+
+cgtp_status cgtp_double_backward(cgtp_plan plan, int64_t B, const void* x, const void* y,
+                                 const void* w, const void* grad_out, const void* gg_x,
+                                 const void* gg_y, const void* gg_w, void* d_x, void* d_y,
+                                 void* d_w, void* d_grad_out, cgtp_stream stream) {
+    GUARD_BEGIN
+    if (!plan) return fail(CGTP_E_ARG, "plan is NULL");
+    if (B < 0) return fail(CGTP_E_ARG, "B < 0");
+    if (B == 0) return CGTP_OK;
+    if (!x || !y || !w || !grad_out) return fail(CGTP_E_ARG, "NULL input tensor");
+    Plan& p = plan->p;
+    cgtp_status st = check_rows(p, {x, w, grad_out, gg_x, gg_w, d_x, d_w, d_grad_out});
+    if (st != CGTP_OK) return st;
+    return double_backward(p, false, B, B, B, nullptr, nullptr, nullptr, nullptr, nullptr, x, y,
+                           w, 1.0, grad_out, gg_x, gg_y, gg_w, d_x, d_y, d_w, d_grad_out,
+                           S(stream));
+    GUARD_END
+}
+
+static cgtp_status check_graph(int64_t N, int64_t E, const void* a, const void* b) {
+    if (N < 0 || E < 0) return fail(CGTP_E_GRAPH, "negative graph size");
+    if (N >= INT_MAX || E >= INT_MAX) return fail(CGTP_E_GRAPH, "graph too large for int32 CSR");
+    if (N > 0 && !a) return fail(CGTP_E_GRAPH, "NULL CSR row pointer");
+    if (E > 0 && !b) return fail(CGTP_E_GRAPH, "NULL CSR index array");
+    return CGTP_OK;
+}
+
+cgtp_status cgtp_conv_forward(cgtp_plan plan, int64_t N, int64_t E, const int32_t* rowptr,
+                              const int32_t* sender, const void* x, const void* y, const void* w,
+                              double scale, void* out, cgtp_stream stream) {
+    GUARD_BEGIN
+    if (!plan) return fail(CGTP_E_ARG, "plan is NULL");
+    cgtp_status st = check_graph(N, E, rowptr, sender);
+    if (st != CGTP_OK) return st;
+    if (N == 0) return CGTP_OK;
+    if (!out || (E > 0 && (!x || !y || !w))) return fail(CGTP_E_ARG, "NULL tensor");
+    Plan& p = plan->p;
+    if ((st = check_rows(p, {x, w, out})) != CGTP_OK) return st;
+    return fwd_launch(p, true, N, rowptr, sender, x, y, w, scale, out, 0, S(stream));
+    GUARD_END
+}
+
+cgtp_status cgtp_conv_backward(cgtp_plan plan, int64_t N, int64_t E, const int32_t* rowptr,
+                               const int32_t* sender, const int32_t* s_rowptr,
+                               const int32_t* s_perm, const int32_t* s_recv, const void* x,
+                               const void* y, const void* w, double scale, const void* grad_out,
+                               void* grad_x, void* grad_y, void* grad_w, cgtp_stream stream) {
+    GUARD_BEGIN
+    if (!plan) return fail(CGTP_E_ARG, "plan is NULL");
+    cgtp_status st = check_graph(N, E, s_rowptr, s_perm);
+    if (st != CGTP_OK) return st;
+    if (E > 0 && !s_recv) return fail(CGTP_E_GRAPH, "NULL s_recv");
+    (void)rowptr;
+    (void)sender;
+    if (N == 0) return CGTP_OK;
+    Plan& p = plan->p;
+    if (p.wmode == CGTP_W_SHARED && grad_w)
+        return fail(CGTP_E_UNSUPPORTED, "weight gradient of shared weights is not implemented");
+    if (!x || !grad_out || (E > 0 && (!y || !w))) return fail(CGTP_E_ARG, "NULL input tensor");
+    if ((st = check_rows(p, {x, w, grad_out, grad_x, grad_w})) != CGTP_OK) return st;
+    return bwd_launch(p, true, N, s_rowptr, s_perm, s_recv, x, y, w, grad_out, scale, grad_x,
+                      grad_y, grad_w, grad_x ? 1 : 0, grad_y ? 1 : 0, grad_w ? 1 : 0, S(stream));
+    GUARD_END
+}
+
+cgtp_status cgtp_conv_double_backward(cgtp_plan plan, int64_t N, int64_t E, const int32_t* rowptr,
+                                      const int32_t* sender, const int32_t* s_rowptr,
+                                      const int32_t* s_perm, const int32_t* s_recv, const void* x,
+                                      const void* y, const void* w, double scale,
+                                      const void* grad_out, const void* gg_x, const void* gg_y,
+                                      const void* gg_w, void* d_x, void* d_y, void* d_w,
+                                      void* d_grad_out, cgtp_stream stream) {
+    GUARD_BEGIN
+    if (!plan) return fail(CGTP_E_ARG, "plan is NULL");
+    cgtp_status st = check_graph(N, E, rowptr, sender);
+    if (st != CGTP_OK) return st;
+    if ((st = check_graph(N, E, s_rowptr, s_perm)) != CGTP_OK) return st;
+    if (E > 0 && !s_recv) return fail(CGTP_E_GRAPH, "NULL s_recv");
+    if (N == 0) return CGTP_OK;
+    if (!x || !grad_out || (E > 0 && (!y || !w))) return fail(CGTP_E_ARG, "NULL input tensor");
+    Plan& p = plan->p;
+    if ((st = check_rows(p, {x, w, grad_out, gg_x, gg_w, d_x, d_w, d_grad_out})) != CGTP_OK)
+        return st;
+    return double_backward(p, true, N, E, N, rowptr, sender, s_rowptr, s_perm, s_recv, x, y, w,
+                           scale, grad_out, gg_x, gg_y, gg_w, d_x, d_y, d_w, d_grad_out,
+                           S(stream));
+    GUARD_END
+}
+
+static cgtp_status sh_check(int lmax, cgtp_dtype dt, int64_t E) {
+    if (lmax < 0 || lmax > 6) return fail(CGTP_E_UNSUPPORTED, "lmax must be 0..6");
+    if (dt != CGTP_F32 && dt != CGTP_F64) return fail(CGTP_E_ARG, "bad dtype");
+    if (E < 0) return fail(CGTP_E_ARG, "E < 0");
+    return CGTP_OK;
+}
+
+cgtp_status cgtp_sh_forward(int lmax, cgtp_dtype dtype, int64_t E, const void* vec, void* y,
+                            cgtp_stream stream) {
+    GUARD_BEGIN
+    cgtp_status st = sh_check(lmax, dtype, E);
+    if (st != CGTP_OK || E == 0) return st;
+    if (!vec || !y) return fail(CGTP_E_ARG, "NULL tensor");
+    cudaError_t e = launch_sh_forward(lmax, dtype == CGTP_F64, E, vec, y, S(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "sh_forward");
+    count_launch();
+    return CGTP_OK;
+    GUARD_END
+}
+
+cgtp_status cgtp_sh_backward(int lmax, cgtp_dtype dtype, int64_t E, const void* vec,
+                             const void* grad_y, void* grad_vec, cgtp_stream stream) {
+    GUARD_BEGIN
+    cgtp_status st = sh_check(lmax, dtype, E);
+    if (st != CGTP_OK || E == 0) return st;
+    if (!vec || !grad_y || !grad_vec) return fail(CGTP_E_ARG, "NULL tensor");
+    cudaError_t e = launch_sh_backward(lmax, dtype == CGTP_F64, E, vec, grad_y, grad_vec, S(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "sh_backward");
+    count_launch();
+    return CGTP_OK;
+    GUARD_END
+}
+
+cgtp_status cgtp_sh_jvp(int lmax, cgtp_dtype dtype, int64_t E, const void* vec,
+                        const void* tangent_vec, void* tangent_y, cgtp_stream stream) {
+    GUARD_BEGIN
+    cgtp_status st = sh_check(lmax, dtype, E);
+    if (st != CGTP_OK || E == 0) return st;
+    if (!vec || !tangent_vec || !tangent_y) return fail(CGTP_E_ARG, "NULL tensor");
+    cudaError_t e = launch_sh_jvp(lmax, dtype == CGTP_F64, E, vec, tangent_vec, tangent_y, S(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "sh_jvp");
+    count_launch();
+    return CGTP_OK;
+    GUARD_END
+}
+
+cgtp_status cgtp_edge_forces(cgtp_dtype dtype, int64_t N, int64_t E, const int32_t* rowptr,
+                             const int32_t* s_rowptr, const int32_t* s_perm, const void* dEdr,
+                             void* forces, cgtp_stream stream) {
+    GUARD_BEGIN
+    if (dtype != CGTP_F32 && dtype != CGTP_F64) return fail(CGTP_E_ARG, "bad dtype");
+    cgtp_status st = check_graph(N, E, rowptr, s_perm);
+    if (st != CGTP_OK) return st;
+    if (N > 0 && !s_rowptr) return fail(CGTP_E_GRAPH, "NULL s_rowptr");
+    if (N == 0) return CGTP_OK;
+    if (!forces || (E > 0 && !dEdr)) return fail(CGTP_E_ARG, "NULL tensor");
+    cudaError_t e = launch_edge_forces(dtype == CGTP_F64, N, rowptr, s_rowptr, s_perm, dEdr,
+                                       forces, S(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "edge_forces");
+    count_launch();
+    return CGTP_OK;
+    GUARD_END
+}
+
+cgtp_status cgtp_edge_forces_adjoint(cgtp_dtype dtype, int64_t N, int64_t E,
+                                     const int32_t* rowptr, const int32_t* sender,
+                                     const void* grad_forces, void* grad_dEdr,
+                                     cgtp_stream stream) {
+    GUARD_BEGIN
+    if (dtype != CGTP_F32 && dtype != CGTP_F64) return fail(CGTP_E_ARG, "bad dtype");
+    cgtp_status st = check_graph(N, E, rowptr, sender);
+    if (st != CGTP_OK) return st;
+    if (N == 0 || E == 0) return CGTP_OK;
+    if (!grad_forces || !grad_dEdr) return fail(CGTP_E_ARG, "NULL tensor");
+    cudaError_t e = launch_edge_forces_adjoint(dtype == CGTP_F64, N, rowptr, sender, grad_forces,
+                                               grad_dEdr, S(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "edge_forces_adjoint");
+    count_launch();
+    return CGTP_OK;
+    GUARD_END
+}
+
+const char* cgtp_status_str(cgtp_status s) {
+    switch (s) {
+        case CGTP_OK: return "ok";
+        case CGTP_E_ARG: return "invalid argument";
+        case CGTP_E_IRREPS: return "irreps string does not parse";
+        case CGTP_E_PATH: return "instruction is not an allowed path";
+        case CGTP_E_UNSUPPORTED: return "unsupported";
+        case CGTP_E_GRAPH: return "inconsistent graph";
+        case CGTP_E_NOMEM: return "out of host memory";
+        case CGTP_E_CUDA: return "CUDA error";
+        case CGTP_E_COMPILE: return "kernel compilation failed";
+        case CGTP_E_DEVICE: return "device-side error flag";
+    }
+    return "unknown status";
+}
+
+cgtp_status cgtp_last_cuda_error(int* cuda_err) {
+    if (!cuda_err) return CGTP_E_ARG;
+    *cuda_err = t_cuda_err;
+    return CGTP_OK;
+}
+
+const char* cgtp_last_error_message(void) { return t_msg.c_str(); }
+
+int64_t cgtp_launch_count(void) { return g_launches.load(); }
+
+}  // extern "C"

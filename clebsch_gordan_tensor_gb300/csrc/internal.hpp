@@ -1,0 +1,45 @@
+// Internal declarations shared by the C-ABI, the JIT and the fixed kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <map>
+#include <memory>
+#include <string>
+#include <vector>
+
+#include "plan.hpp"
+
+namespace cgtp {
+
+struct Module {
+    std::vector<char> cubin;
+    std::string log;  // NVRTC / ptxas log (register and spill report)
+    cudaLibrary_t lib = nullptr;
+    std::map<std::string, cudaKernel_t> kernels;
+    ~Module();
+};
+
+cgtp_status get_module(Plan& p, bool load, std::shared_ptr<Module>& out, std::string& err);
+
+// Thread-local error state of the C ABI.
+void set_cuda_error(cudaError_t e);
+void set_error_message(const std::string& m);
+void count_launch();
+
+// Fixed kernels (sh.cu, graph.cu).  They return a cudaError_t of the launch.
+cudaError_t launch_sh_forward(int lmax, bool f64, int64_t E, const void* vec, void* y,
+                              cudaStream_t s);
+cudaError_t launch_sh_backward(int lmax, bool f64, int64_t E, const void* vec, const void* gy,
+                               void* gvec, cudaStream_t s);
+cudaError_t launch_sh_jvp(int lmax, bool f64, int64_t E, const void* vec, const void* tvec,
+                          void* ty, cudaStream_t s);
+cudaError_t launch_edge_forces(bool f64, int64_t N, const int32_t* rowptr,
+                               const int32_t* s_rowptr, const int32_t* s_perm, const void* dEdr,
+                               void* F, cudaStream_t s);
+cudaError_t launch_edge_forces_adjoint(bool f64, int64_t N, const int32_t* rowptr,
+                                       const int32_t* sender, const void* gF, void* q,
+                                       cudaStream_t s);
+cudaError_t launch_fill_zero(void* p, int64_t bytes, cudaStream_t s);
+
+}  // namespace cgtp

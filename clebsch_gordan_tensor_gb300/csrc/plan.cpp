@@ -1,0 +1,516 @@
+// Host planner of the CG tensor-product library: irreps, paths, real CG
+// coefficients, and the per-plan CUDA source handed to NVRTC.
+//
+// "static analysis at model compile-time ... break the tensor product into a
+// series of smaller kernels with operands that fit entirely into registers ...
+// emit long arithmetic instruction streams" ("An Efficient Sparse Kernel
+// Generator for O(3)-Equivariant Deep Networks", abstract).  Here the analysis
+// produces, per plan, one fully unrolled stream per direction in which every
+// CG coefficient is an immediate and every operand index is a constant.
+#include <algorithm>
+#include <cmath>
+#include <complex>
+#include <cstdio>
+#include <cstring>
+#include <sstream>
+
+#include "plan.hpp"
+
+namespace cgtp {
+
+extern const char* kTpKernelsSource;  // tp_kernels.cuh, embedded at build time
+
+static constexpr int kMaxL = 6;
+
+// ------------------------------------------------------------------ irreps
+
+static bool parse_irreps(const char* s, std::vector<Irrep>& out, std::string& err) {
+    out.clear();
+    if (!s) {
+        err = "irreps string is NULL";
+        return false;
+    }
+    std::string str(s);
+    size_t pos = 0;
+    while (pos <= str.size()) {
+        size_t plus = str.find('+', pos);
+        std::string tok = str.substr(pos, plus == std::string::npos ? std::string::npos : plus - pos);
+        tok.erase(std::remove_if(tok.begin(), tok.end(), [](char c) { return c == ' '; }), tok.end());
+        int mul = 1, l = -1;
+        char par = 0;
+        size_t xp = tok.find('x');
+        std::string body = tok;
+        if (xp != std::string::npos) {
+            if (xp == 0 || sscanf(tok.substr(0, xp).c_str(), "%d", &mul) != 1 || mul <= 0) {
+                err = "bad multiplicity in irrep '" + tok + "'";
+                return false;
+            }
+            for (size_t i = 0; i < xp; ++i)
+                if (tok[i] < '0' || tok[i] > '9') {
+                    err = "bad multiplicity in irrep '" + tok + "'";
+                    return false;
+                }
+            body = tok.substr(xp + 1);
+        }
+        if (body.size() < 2) {
+            err = "bad irrep '" + tok + "'";
+            return false;
+        }
+        par = body.back();
+        std::string ls = body.substr(0, body.size() - 1);
+        for (char c : ls)
+            if (c < '0' || c > '9') {
+                err = "bad degree in irrep '" + tok + "'";
+                return false;
+            }
+        l = atoi(ls.c_str());
+        if ((par != 'e' && par != 'o') || l < 0) {
+            err = "bad irrep '" + tok + "'";
+            return false;
+        }
+        if (l > kMaxL) {
+            err = "degree above 6 in '" + tok + "'";
+            return false;
+        }
+        out.push_back({mul, l, par == 'e' ? 1 : -1});
+        if (plus == std::string::npos) break;
+        pos = plus + 1;
+    }
+    return !out.empty();
+}
+
+// ------------------------------------------------- Clebsch-Gordan (planner)
+//
+// Complex CG by the angular-momentum ladder: the top state |J, J> of the
+// coupled pair is the unit vector annihilated by J+ = J1+ + J2+ with positive
+// <j1 j1; j2 J-j1 | J J> (Condon-Shortley), and each lower |J, M-1> is
+// J- |J, M> / sqrt(J(J+1) - M(M-1)).
+
+static double ladder(int j, int m, int dm) {  // <j m+dm | J(dm) | j m>
+    return std::sqrt(double(j * (j + 1) - m * (m + dm)));
+}
+
+// tab[(m1 + j1) * (2J+1) + (M + J)] = <j1 m1 j2 M-m1 | J M>
+static void complex_cg_ladder(int j1, int j2, int J, std::vector<double>& tab) {
+    const int d1 = 2 * j1 + 1, dJ = 2 * J + 1;
+    tab.assign((size_t)d1 * dJ, 0.0);
+    auto at = [&](int m1, int M) -> double& { return tab[(size_t)(m1 + j1) * dJ + (M + J)]; };
+    // top state
+    const int lo = std::max(-j1, J - j2);
+    std::vector<double> a(d1, 0.0);
+    a[lo + j1] = 1.0;
+    for (int k = lo + 1; k <= j1; ++k)  // coefficient of |k, J+1-k> in J+|J J> vanishes
+        a[k + j1] = -a[k - 1 + j1] * ladder(j1, k - 1, +1) / ladder(j2, J - k, +1);
+    double nrm = 0;
+    for (double v : a) nrm += v * v;
+    nrm = std::sqrt(nrm);
+    const double sgn = a[2 * j1] >= 0 ? 1.0 : -1.0;
+    for (int m1 = -j1; m1 <= j1; ++m1) at(m1, J) = sgn * a[m1 + j1] / nrm;
+    // lower
+    for (int M = J; M > -J; --M) {
+        const double cJ = ladder(J, M, -1);
+        for (int m1 = -j1; m1 <= j1; ++m1) {
+            const int m2 = M - 1 - m1;
+            if (m2 < -j2 || m2 > j2) continue;
+            double v = 0;
+            if (m1 + 1 <= j1 && std::abs(M - m1 - 1) <= j2) v += at(m1 + 1, M) * ladder(j1, m1 + 1, -1);
+            if (std::abs(M - m1) <= j2) v += at(m1, M) * ladder(j2, M - m1, -1);
+            at(m1, M - 1) = v / cJ;
+        }
+    }
+}
+
+// The real spherical-harmonic basis vector of real index m as a combination of
+// complex ones: up to two (complex m, weight) terms.
+//   m > 0: (|-m> + (-1)^m |m>) / sqrt2,  m = 0: |0>,  m < 0: i (|m> - (-1)^m |-m>) / sqrt2
+struct CTerm {
+    int mc;
+    std::complex<double> c;
+};
+static int real_basis(int m, CTerm out[2]) {
+    const double r = 1.0 / std::sqrt(2.0);
+    const double s = (std::abs(m) % 2) ? -1.0 : 1.0;
+    if (m == 0) {
+        out[0] = {0, 1.0};
+        return 1;
+    }
+    if (m > 0) {
+        out[0] = {-m, r};
+        out[1] = {m, s * r};
+        return 2;
+    }
+    out[0] = {m, std::complex<double>(0, r)};
+    out[1] = {-m, std::complex<double>(0, -s * r)};
+    return 2;
+}
+
+bool real_cg(int l1, int l2, int l3, std::vector<double>& out) {
+    const int d1 = 2 * l1 + 1, d2 = 2 * l2 + 1, d3 = 2 * l3 + 1;
+    out.assign((size_t)d1 * d2 * d3, 0.0);
+    if (l3 < std::abs(l1 - l2) || l3 > l1 + l2) return false;
+    std::vector<double> tab;
+    complex_cg_ladder(l1, l2, l3, tab);
+    const int dJ = 2 * l3 + 1;
+    std::vector<std::complex<double>> z((size_t)d1 * d2 * d3);
+    double mre = 0, mim = 0;
+    for (int a = -l1; a <= l1; ++a) {
+        CTerm A[2];
+        const int na = real_basis(a, A);
+        for (int b = -l2; b <= l2; ++b) {
+            CTerm B[2];
+            const int nb = real_basis(b, B);
+            for (int c = -l3; c <= l3; ++c) {
+                CTerm Cc[2];
+                const int nc = real_basis(c, Cc);
+                std::complex<double> acc = 0;
+                for (int i = 0; i < na; ++i)
+                    for (int j = 0; j < nb; ++j)
+                        for (int k = 0; k < nc; ++k) {
+                            if (A[i].mc + B[j].mc != Cc[k].mc) continue;
+                            const double cg = tab[(size_t)(A[i].mc + l1) * dJ + (Cc[k].mc + l3)];
+                            acc += Cc[k].c * cg * std::conj(A[i].c) * std::conj(B[j].c);
+                        }
+                const size_t idx = ((size_t)(a + l1) * d2 + (b + l2)) * d3 + (c + l3);
+                z[idx] = acc;
+                mre = std::max(mre, std::abs(acc.real()));
+                mim = std::max(mim, std::abs(acc.imag()));
+            }
+        }
+    }
+    const bool im = mim > mre;
+    double sign = 0;
+    for (size_t i = 0; i < z.size(); ++i) {
+        double v = im ? z[i].imag() : z[i].real();
+        if (std::abs(v) < 1e-14) v = 0;
+        if (sign == 0 && v != 0) sign = v > 0 ? 1 : -1;
+        out[i] = v;
+    }
+    for (double& v : out) v *= sign;
+    return true;
+}
+
+// ---------------------------------------------------------------- planning
+
+static int next_pow2(int v) {
+    int p = 1;
+    while (p < v) p <<= 1;
+    return p;
+}
+
+cgtp_status build_plan(Plan& p, const char* s1, const char* s2, const char* so,
+                       const cgtp_instr* instr, int n_instr, std::string& err) {
+    if (!parse_irreps(s1, p.in1, err) || !parse_irreps(s2, p.in2, err) ||
+        !parse_irreps(so, p.out, err))
+        return CGTP_E_IRREPS;
+    p.s1 = s1;
+    p.s2 = s2;
+    p.so = so;
+    for (auto& ir : p.in2)
+        if (ir.mul != 1) {
+            err = "irreps_in2 must have multiplicity 1 per irrep";
+            return CGTP_E_UNSUPPORTED;
+        }
+    p.mul = p.in1[0].mul;
+    for (auto& ir : p.in1)
+        if (ir.mul != p.mul) {
+            err = "all irreps_in1 entries must share one multiplicity";
+            return CGTP_E_UNSUPPORTED;
+        }
+    for (auto& ir : p.out)
+        if (ir.mul != p.mul) {
+            err = "irreps_out must share the multiplicity of irreps_in1";
+            return CGTP_E_UNSUPPORTED;
+        }
+    std::vector<int> r1(p.in1.size()), o2(p.in2.size()), r3(p.out.size());
+    int acc = 0;
+    for (size_t i = 0; i < p.in1.size(); ++i) r1[i] = acc, acc += 2 * p.in1[i].l + 1;
+    p.nx = acc;
+    acc = 0;
+    for (size_t i = 0; i < p.in2.size(); ++i) o2[i] = acc, acc += 2 * p.in2[i].l + 1;
+    p.ny = acc;
+    acc = 0;
+    for (size_t i = 0; i < p.out.size(); ++i) r3[i] = acc, acc += 2 * p.out[i].l + 1;
+    p.no = acc;
+
+    auto allowed = [&](int a, int b, int c) {
+        const Irrep &A = p.in1[a], &B = p.in2[b], &C = p.out[c];
+        return C.l >= std::abs(A.l - B.l) && C.l <= A.l + B.l && C.parity == A.parity * B.parity;
+    };
+    auto add = [&](int a, int b, int c) {
+        Path q{a, b, c, p.in1[a].l, p.in2[b].l, p.out[c].l, r1[a], o2[b], r3[c], {}};
+        real_cg(q.l1, q.l2, q.l3, q.cg);
+        p.paths.push_back(std::move(q));
+    };
+    if (instr == nullptr) {
+        for (int a = 0; a < (int)p.in1.size(); ++a)
+            for (int b = 0; b < (int)p.in2.size(); ++b)
+                for (int c = 0; c < (int)p.out.size(); ++c)
+                    if (allowed(a, b, c)) add(a, b, c);
+    } else {
+        if (n_instr < 0) {
+            err = "negative instruction count";
+            return CGTP_E_ARG;
+        }
+        for (int k = 0; k < n_instr; ++k) {
+            const cgtp_instr& I = instr[k];
+            if (I.i_in1 < 0 || I.i_in1 >= (int)p.in1.size() || I.i_in2 < 0 ||
+                I.i_in2 >= (int)p.in2.size() || I.i_out < 0 || I.i_out >= (int)p.out.size()) {
+                err = "instruction " + std::to_string(k) + " indexes outside the irreps";
+                return CGTP_E_PATH;
+            }
+            if (strncmp(I.mode, "uvu", 3) != 0) {
+                err = "instruction " + std::to_string(k) + ": only mode 'uvu' is supported";
+                return CGTP_E_UNSUPPORTED;
+            }
+            if (!allowed(I.i_in1, I.i_in2, I.i_out)) {
+                err = "instruction " + std::to_string(k) + " violates the triangle or parity rule";
+                return CGTP_E_PATH;
+            }
+            add(I.i_in1, I.i_in2, I.i_out);
+        }
+    }
+    p.dimx = (int64_t)p.nx * p.mul;
+    p.dimy = p.ny;
+    p.dimo = (int64_t)p.no * p.mul;
+    p.wdim = (int64_t)p.paths.size() * p.mul;
+
+    // T entries
+    p.maxterms = 1;
+    for (int q = 0; q < (int)p.paths.size(); ++q) {
+        const Path& P = p.paths[q];
+        const int d1 = 2 * P.l1 + 1, d2 = 2 * P.l2 + 1, d3 = 2 * P.l3 + 1;
+        for (int a = 0; a < d1; ++a)
+            for (int c = 0; c < d3; ++c) {
+                TEntry t{q, a, c, {}};
+                for (int b = 0; b < d2; ++b) {
+                    const double v = P.cg[((size_t)a * d2 + b) * d3 + c];
+                    if (v != 0.0) t.terms.push_back({P.o2 + b, v});
+                }
+                if (!t.terms.empty()) {
+                    p.maxterms = std::max(p.maxterms, (int)t.terms.size());
+                    p.T.push_back(std::move(t));
+                }
+            }
+    }
+
+    // launch geometry
+    p.cpt = (p.dtype == CGTP_F32 && p.mul % 2 == 0) ? 2 : 1;
+    p.nch = p.mul / p.cpt;
+    p.lanes = p.nch <= 32 ? next_pow2(p.nch) : ((p.nch + 31) / 32) * 32;
+    if (p.lanes > 1024) {
+        err = "multiplicity too large (more than 1024 channel groups)";
+        return CGTP_E_UNSUPPORTED;
+    }
+    p.slots = std::max(1, 128 / p.lanes);
+    if (p.lanes > 32) p.slots = std::min(p.slots, 15);
+    const int nt = (int)p.T.size();
+    const size_t vr = p.cpt == 2 ? 8 : (p.dtype == CGTP_F64 ? 8 : 4);
+    auto smem = [&](int slots) {
+        const size_t ntp = std::max(2, nt + (nt & 1));
+        const size_t nyp = next_pow2(std::max(1, p.ny));
+        const size_t real = p.dtype == CGTP_F64 ? 8 : 4;
+        return slots * (ntp * vr + nyp * real + (p.lanes > 32 ? (p.lanes / 32) * nyp * real : 0));
+    };
+    while (p.slots > 1 && smem(p.slots) > 40 * 1024) --p.slots;
+    if (smem(p.slots) > 40 * 1024) {
+        err = "too many CG entries for the shared-memory staging of one work slot";
+        return CGTP_E_UNSUPPORTED;
+    }
+    p.block = p.slots * p.lanes;
+    return CGTP_OK;
+}
+
+// -------------------------------------------------------------- code gen
+
+static std::string lit(double v, bool f64) {
+    char buf[64];
+    if (f64)
+        snprintf(buf, sizeof buf, "%.17g", v);
+    else
+        snprintf(buf, sizeof buf, "%.9gf", (double)(float)v);
+    std::string s(buf);
+    if (s.find_first_of(".eEn") == std::string::npos) {  // integral: make it a float literal
+        if (f64)
+            s += ".0";
+        else
+            s.insert(s.size() - 1, ".0");
+    }
+    return s;
+}
+
+// Emits T(k) loads: with two fp32 channels per lane, T entries are stored as
+// duplicated pairs and fetched two at a time with one 128-bit shared load.
+struct TLoader {
+    int cpt;
+    std::vector<bool> loaded;
+    std::ostringstream* os;
+    std::string get(int k) {
+        if (cpt != 2) return "Ts[" + std::to_string(k) + "]";
+        const int q = k / 2;
+        if (!loaded[q]) {
+            *os << "    const ulonglong2 tq" << q << " = Tq[" << q << "];\n";
+            loaded[q] = true;
+        }
+        return "tq" + std::to_string(q) + (k % 2 ? ".y" : ".x");
+    }
+};
+
+std::string Plan::kernel_source() const {
+    const bool f64 = dtype == CGTP_F64;
+    const int nt = (int)T.size();
+    const int ntp = std::max(2, nt + (nt & 1));
+    const int nyp = next_pow2(std::max(1, ny));
+    std::ostringstream os;
+    os << "// generated for " << s1 << " (x) " << s2 << " -> " << so << ", " << paths.size()
+       << " uvu paths, " << (f64 ? "fp64" : "fp32") << "\n";
+    os << "#define REAL " << (f64 ? "double" : "float") << "\n";
+    os << "#define IS_F64 " << (f64 ? 1 : 0) << "\n";
+    os << "#define CPT " << cpt << "\n#define MUL " << mul << "\n#define NCH " << nch
+       << "\n#define LANES " << lanes << "\n#define SLOTS " << slots << "\n#define BLOCK " << block
+       << "\n#define NX " << nx << "\n#define NY " << ny << "\n#define NYP " << nyp
+       << "\n#define NO " << no << "\n#define NP " << paths.size() << "\n#define NT " << nt
+       << "\n#define NTP " << ntp << "\n#define MAXTERMS " << maxterms << "\n#define YPF "
+       << (ny + lanes - 1) / lanes << "\n";
+    // T tables
+    os << "__device__ const short T_IDX[" << std::max(1, nt * maxterms) << "] = {";
+    for (int k = 0; k < nt; ++k)
+        for (int q = 0; q < maxterms; ++q)
+            os << (q < (int)T[k].terms.size() ? T[k].terms[q].first : 0) << ",";
+    if (nt == 0) os << "0";
+    os << "};\n";
+    os << "__device__ const REAL T_CO[" << std::max(1, nt * maxterms) << "] = {";
+    for (int k = 0; k < nt; ++k)
+        for (int q = 0; q < maxterms; ++q)
+            os << (q < (int)T[k].terms.size() ? lit(T[k].terms[q].second, f64) : (f64 ? "0.0" : "0.0f"))
+               << ",";
+    if (nt == 0) os << "0";
+    os << "};\n";
+
+    std::string tmpl(kTpKernelsSource);
+    const std::string marker = "// @@GENERATED@@";
+    const size_t cut = tmpl.find(marker);
+    std::string head = tmpl.substr(0, cut), tail = tmpl.substr(cut);
+
+    // T entries are grouped by path: k0[q] .. k0[q+1]-1 belong to path q
+    std::vector<int> k0(paths.size() + 1, nt);
+    {
+        int k = 0;
+        for (int q = 0; q < (int)paths.size(); ++q) {
+            while (k < nt && T[k].path < q) ++k;
+            k0[q] = k;
+        }
+    }
+
+    std::ostringstream g;
+    // ---- forward stream
+    g << "__device__ __forceinline__ void gen_fwd(VR (&acc)[NO], const VR* __restrict__ Ts,\n"
+         "    const VR (&xr)[NX], const REAL* __restrict__ wrow, int ch) {\n";
+    if (cpt == 2) g << "    const ulonglong2* __restrict__ Tq = reinterpret_cast<const ulonglong2*>(Ts);\n";
+    {
+        TLoader L{cpt, std::vector<bool>(ntp / 2 + 1, false), &g};
+        for (int q = 0; q < (int)paths.size(); ++q) {
+            const Path& P = paths[q];
+            const int d1 = 2 * P.l1 + 1, d3 = 2 * P.l3 + 1;
+            g << "  { // path " << q << ": " << P.l1 << " x " << P.l2 << " -> " << P.l3 << "\n";
+            g << "    const VR w = LDW(" << q << ");\n";
+            std::fill(L.loaded.begin(), L.loaded.end(), false);  // loads are block-scoped
+            if (d1 <= d3) {
+                for (int a = 0; a < d1; ++a)
+                    g << "    const VR z" << a << " = vmul(w, xr[" << P.r1 + a << "]);\n";
+                for (int k = k0[q]; k < k0[q + 1]; ++k) {
+                    const std::string t = L.get(k);
+                    const int o = P.r3 + T[k].m3;
+                    g << "    acc[" << o << "] = vfma(" << t << ", z" << T[k].m1 << ", acc[" << o << "]);\n";
+                }
+            } else {
+                std::vector<bool> started(d3, false);
+                for (int k = k0[q]; k < k0[q + 1]; ++k) {
+                    const std::string t = L.get(k);
+                    const int c = T[k].m3;
+                    const std::string xv = "xr[" + std::to_string(P.r1 + T[k].m1) + "]";
+                    if (!started[c]) {
+                        g << "    VR t" << c << " = vmul(" << t << ", " << xv << ");\n";
+                        started[c] = true;
+                    } else {
+                        g << "    t" << c << " = vfma(" << t << ", " << xv << ", t" << c << ");\n";
+                    }
+                }
+                for (int c = 0; c < d3; ++c)
+                    if (started[c])
+                        g << "    acc[" << P.r3 + c << "] = vfma(w, t" << c << ", acc[" << P.r3 + c
+                          << "]);\n";
+            }
+            g << "  }\n";
+        }
+    }
+    g << "}\n\n";
+
+    // ---- backward stream
+    g << "template <bool GY>\n__device__ __forceinline__ void gen_bwd(VR (&gxa)[NX], REAL (&gyl)[NYP],\n"
+         "    const VR* __restrict__ Ts, const VR (&xr)[NX], const VR (&gr)[NO],\n"
+         "    const REAL* __restrict__ wrow, REAL* __restrict__ gwrow, int ch, VR sc, bool dogx,\n"
+         "    int mgw) {\n";
+    if (cpt == 2) g << "    const ulonglong2* __restrict__ Tq = reinterpret_cast<const ulonglong2*>(Ts);\n";
+    {
+        TLoader L{cpt, std::vector<bool>(ntp / 2 + 1, false), &g};
+        for (int q = 0; q < (int)paths.size(); ++q) {
+            const Path& P = paths[q];
+            const int d1 = 2 * P.l1 + 1, d3 = 2 * P.l3 + 1;
+            g << "  { // path " << q << ": " << P.l1 << " x " << P.l2 << " -> " << P.l3 << "\n";
+            g << "    const VR w = LDW(" << q << ");\n";
+            std::fill(L.loaded.begin(), L.loaded.end(), false);  // loads are block-scoped
+            // h[m1] = sum_m3 T[m1,m3] g[m3]
+            std::vector<bool> hs(d1, false);
+            for (int k = k0[q]; k < k0[q + 1]; ++k) {
+                const std::string t = L.get(k);
+                const int a = T[k].m1;
+                const std::string gv = "gr[" + std::to_string(P.r3 + T[k].m3) + "]";
+                if (!hs[a]) {
+                    g << "    VR h" << a << " = vmul(" << t << ", " << gv << ");\n";
+                    hs[a] = true;
+                } else {
+                    g << "    h" << a << " = vfma(" << t << ", " << gv << ", h" << a << ");\n";
+                }
+            }
+            g << "    if (dogx) {\n";
+            for (int a = 0; a < d1; ++a)
+                if (hs[a])
+                    g << "      gxa[" << P.r1 + a << "] = vfma(w, h" << a << ", gxa[" << P.r1 + a
+                      << "]);\n";
+            g << "    }\n    if (mgw) {\n      VR s = vzero();\n";
+            for (int a = 0; a < d1; ++a)
+                if (hs[a]) g << "      s = vfma(xr[" << P.r1 + a << "], h" << a << ", s);\n";
+            g << "      s = vmul(s, sc);\n      REAL* gp = gwrow + " << (long long)q * mul << ";\n"
+              << "      if (mgw == 2) s = vadd(s, ldv_plain(gp, ch));\n"
+              << "      if (CH_ACTIVE(ch)) stv(gp, ch, s);\n    }\n";
+            // gy partials
+            g << "    if (GY) {\n";
+            const bool zx = d1 <= d3;
+            if (zx) {
+                for (int a = 0; a < d1; ++a)
+                    g << "      const VR z" << a << " = vmul(w, xr[" << P.r1 + a << "]);\n";
+            } else {
+                for (int c = 0; c < d3; ++c)
+                    g << "      const VR z" << c << " = vmul(w, gr[" << P.r3 + c << "]);\n";
+            }
+            for (int k = k0[q]; k < k0[q + 1]; ++k) {
+                const TEntry& t = T[k];
+                const std::string lhs =
+                    zx ? "z" + std::to_string(t.m1) : "xr[" + std::to_string(P.r1 + t.m1) + "]";
+                const std::string rhs =
+                    zx ? "gr[" + std::to_string(P.r3 + t.m3) + "]" : "z" + std::to_string(t.m3);
+                g << "      { const REAL d = vdot(" << lhs << ", " << rhs << ");\n";
+                for (auto& term : t.terms)
+                    g << "        gyl[" << term.first << "] = fma(" << lit(term.second, f64)
+                      << ", d, gyl[" << term.first << "]);\n";
+                g << "      }\n";
+            }
+            g << "    }\n  }\n";
+        }
+    }
+    g << "}\n\n";
+
+    return os.str() + head + g.str() + tail;
+}
+
+}  // namespace cgtp

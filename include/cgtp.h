@@ -1,0 +1,217 @@
+/*
+ * cgtp.h -- C ABI of the GB300 (sm_103a) Clebsch-Gordan tensor-product library.
+ *
+ * The operation (from "An Efficient Sparse Kernel Generator for O(3)-Equivariant
+ * Deep Networks", arXiv 2501.13986, abstract): the CG tensor product contracts
+ * two dense irrep feature vectors x (irreps_in1) and y (irreps_in2) with the
+ * fixed, highly structured sparse Clebsch-Gordan tensor into a dense output
+ * (irreps_out); it is fused with the graph convolution around it; the library
+ * also provides its gradient and the higher partial derivatives used for
+ * interatomic forces.  The per-edge weights are the "radial profile" of the
+ * TFN layer (NVIDIA SE(3)-Transformer blog, "Fused key and value computation");
+ * a layer is the sum over degree pairs of the pairwise convolutions (same blog,
+ * "TFN fusion", Fig. 5); a degree-l block has 2l+1 components.
+ *
+ * Conventions (the pages are silent; these are the library's):
+ *  - Irreps strings: "16x0e+16x1o" (mul x l parity, parity e/o).
+ *  - Paths are 'uvu': out[u] += w[path][u] * sum C[m1,m2,m3] x[u,m1] y[m2]; in2
+ *    irreps have mul 1 and every in1 / out irrep has the same mul.  With
+ *    instr == NULL every parity-allowed (|l1-l2| <= l3 <= l1+l2, p3 = p1 p2)
+ *    triple is a path, listed with in1 outermost, then in2, then out.
+ *  - CG coefficients are real-basis, unitary (sum_{m1,m2} C C' = delta), with
+ *    the first nonzero entry of each path positive.  Real spherical harmonics
+ *    are component-normalised (sum_m Y_lm^2 = 2l+1), m = -l..l, so that
+ *    Y_1 = sqrt(3) (y, z, x).
+ *  - Feature rows hold irrep blocks in irreps order; inside a block the element
+ *    (m, u) sits at (m + l) * mul + u (channel fastest).  Weight rows hold one
+ *    block of mul per path, in path order (weight_numel = n_paths * mul).
+ *  - Graphs: rowptr[N+1] / sender[E] is a CSR over receivers (edges sorted by
+ *    receiver).  The sender-grouped view (for gradients) is s_rowptr[N+1],
+ *    s_perm[E] (edge ids grouped by sender, ascending within a sender) and
+ *    s_recv[E] (receiver of edge s_perm[j]).  Edge vectors are
+ *    pos[receiver] - pos[sender].
+ *
+ * Memory and errors:
+ *  - Every tensor pointer is caller-owned DEVICE memory, contiguous, row-major,
+ *    of the plan's dtype (int32 for graph arrays), 8-byte aligned at least.
+ *    The library never allocates device memory in these calls.
+ *  - Outputs are overwritten, never accumulated.  NULL outputs are skipped.
+ *  - Calls are asynchronous on `stream` (NULL = legacy default stream).
+ *    Argument errors return synchronously without launching.  A CUDA launch
+ *    error returns CGTP_E_CUDA (cgtp_last_cuda_error gives the code).
+ *  - No C++ exception crosses this interface.  Plans are immutable after
+ *    creation and may be shared between threads.
+ *  - The first GPU call of a plan compiles its kernels with NVRTC for sm_103a
+ *    (tens of milliseconds to seconds); later calls reuse them.
+ */
+#ifndef CGTP_H
+#define CGTP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* cgtp_stream; /* == cudaStream_t */
+typedef struct cgtp_plan_s* cgtp_plan;
+
+typedef enum {
+    CGTP_OK = 0,
+    CGTP_E_ARG = 1,         /* bad pointer, size, or NULL where required */
+    CGTP_E_IRREPS = 2,      /* irreps string does not parse */
+    CGTP_E_PATH = 3,        /* an instruction is not an allowed path */
+    CGTP_E_UNSUPPORTED = 4, /* valid request the library does not implement */
+    CGTP_E_GRAPH = 5,       /* inconsistent graph sizes */
+    CGTP_E_NOMEM = 6,       /* host allocation failed */
+    CGTP_E_CUDA = 7,        /* CUDA runtime error */
+    CGTP_E_COMPILE = 8,     /* NVRTC compilation or module load failed */
+    CGTP_E_DEVICE = 9       /* a kernel reported an error flag */
+} cgtp_status;
+
+typedef enum { CGTP_F32 = 0, CGTP_F64 = 1 } cgtp_dtype;
+typedef enum { CGTP_W_PER_EDGE = 0, CGTP_W_SHARED = 1 } cgtp_wmode;
+
+/* One tensor-product path: irrep indices into in1, in2, out; mode "uvu". */
+typedef struct {
+    int i_in1, i_in2, i_out;
+    char mode[4];
+} cgtp_instr;
+
+/* ------------------------------------------------------------- planning -- */
+
+/* Parse the irreps, list or check the paths, compute the real-basis CG
+ * coefficients (complex CG by the angular-momentum lowering recursion, taken to
+ * the real basis) and lay out the per-path work.  Host only; no GPU needed.
+ * irreps_in2 must have mul 1 per irrep (spherical harmonics); in1 and out must
+ * share one mul.  l <= 6.  flags: reserved, pass 0. */
+cgtp_status cgtp_plan_create(cgtp_plan* out, const char* irreps_in1, const char* irreps_in2,
+                             const char* irreps_out, const cgtp_instr* instr, int n_instr,
+                             cgtp_dtype dtype, cgtp_wmode wmode, unsigned flags);
+cgtp_status cgtp_plan_destroy(cgtp_plan plan);
+
+/* Row widths (elements) of x, y, out; weight elements per row; path count. */
+cgtp_status cgtp_plan_info(cgtp_plan plan, int64_t* dim_in1, int64_t* dim_in2, int64_t* dim_out,
+                           int64_t* weight_numel, int* n_paths);
+
+/* Path p: l1, l2, l3 and the irrep indices it couples. */
+cgtp_status cgtp_plan_path(cgtp_plan plan, int p, int* l1, int* l2, int* l3, int* i_in1,
+                           int* i_in2, int* i_out);
+
+/* Dense real CG tensor of path p, out[((m1+l1)*(2l2+1) + m2+l2)*(2l3+1) + m3+l3]
+ * (host memory, caller-owned, (2l1+1)(2l2+1)(2l3+1) doubles). */
+cgtp_status cgtp_plan_coefficients(cgtp_plan plan, int p, double* out);
+
+/* Compile the plan's kernels for sm_103a with NVRTC now (host only, no GPU
+ * needed) instead of at the first GPU call.  If log != NULL, copies up to cap-1
+ * bytes of the compiler log (ptxas register / spill report) into it. */
+cgtp_status cgtp_plan_compile(cgtp_plan plan, char* log, size_t cap);
+
+/* The CUDA source generated for the plan (constants, CG tables and unrolled
+ * contraction streams).  *needed = bytes including the terminator. */
+cgtp_status cgtp_plan_source(cgtp_plan plan, char* buf, size_t cap, size_t* needed);
+
+/* ------------------------------------------- standalone tensor product -- */
+
+/* out[b] = sum_paths w[b,p,u] sum C x[b,l1,m1,u] y[b,l2,m2]   (b < B)
+ * x [B, dim_in1], y [B, dim_in2], w [B, weight_numel] (or [weight_numel] for a
+ * CGTP_W_SHARED plan), out [B, dim_out]. */
+cgtp_status cgtp_forward(cgtp_plan plan, int64_t B, const void* x, const void* y, const void* w,
+                         void* out, cgtp_stream stream);
+
+/* Gradient for grad_out = dL/dout [B, dim_out]:
+ *   grad_x[b,l1,m1,u] = sum C y[m2] w[p,u] g[l3,m3,u]
+ *   grad_y[b,l2,m2]   = sum C x[m1,u] w[p,u] g[m3,u]   (summed over channels)
+ *   grad_w[b,p,u]     = sum C x[m1,u] y[m2] g[m3,u]
+ * Any output may be NULL.  CGTP_W_SHARED plans: grad_w is not supported here
+ * (CGTP_E_UNSUPPORTED if non-NULL). */
+cgtp_status cgtp_backward(cgtp_plan plan, int64_t B, const void* x, const void* y, const void* w,
+                          const void* grad_out, void* grad_x, void* grad_y, void* grad_w,
+                          cgtp_stream stream);
+
+/* Higher partial derivatives ("a novel identity for the higher partial
+ * derivatives", abstract of arXiv 2501.13986; the identity is not printed).
+ * The library uses the trilinearity of f(x, y, w): with cotangents gg_x, gg_y,
+ * gg_w (NULL = zero) of grad_x, grad_y, grad_w,
+ *   d_grad_out = f(gg_x, y, w) + f(x, gg_y, w) + f(x, y, gg_w)
+ *   d_x = f_x(g; gg_y, w) + f_x(g; y, gg_w)
+ *   d_y = f_y(g; gg_x, w) + f_y(g; x, gg_w)
+ *   d_w = f_w(g; gg_x, y) + f_w(g; x, gg_y)
+ * Outputs may be NULL (skipped). */
+cgtp_status cgtp_double_backward(cgtp_plan plan, int64_t B, const void* x, const void* y,
+                                 const void* w, const void* grad_out, const void* gg_x,
+                                 const void* gg_y, const void* gg_w, void* d_x, void* d_y,
+                                 void* d_w, void* d_grad_out, cgtp_stream stream);
+
+/* -------------------------------------------- fused graph convolution -- */
+
+/* out[n] = scale * sum_{e=rowptr[n]}^{rowptr[n+1]-1} TP(x[sender[e]], y[e], w[e])
+ * ("fusing the CG tensor product with a subsequent graph convolution", abstract
+ * of arXiv 2501.13986).  Every receiver row is written (zero if no edges).
+ * x [N, dim_in1], y [E, dim_in2], w [E, weight_numel], out [N, dim_out]. */
+cgtp_status cgtp_conv_forward(cgtp_plan plan, int64_t N, int64_t E, const int32_t* rowptr,
+                              const int32_t* sender, const void* x, const void* y, const void* w,
+                              double scale, void* out, cgtp_stream stream);
+
+/* Gradient of cgtp_conv_forward for grad_out [N, dim_out]:
+ *   grad_x[s] = scale * sum_{edges e with sender s} f_x(g[recv e]; y[e], w[e])
+ *   grad_y[e] = scale * f_y(g[recv e]; x[sender e], w[e])
+ *   grad_w[e] = scale * f_w(g[recv e]; x[sender e], y[e])
+ * Uses the sender-grouped view (s_rowptr, s_perm, s_recv); no atomics. */
+cgtp_status cgtp_conv_backward(cgtp_plan plan, int64_t N, int64_t E, const int32_t* rowptr,
+                               const int32_t* sender, const int32_t* s_rowptr,
+                               const int32_t* s_perm, const int32_t* s_recv, const void* x,
+                               const void* y, const void* w, double scale, const void* grad_out,
+                               void* grad_x, void* grad_y, void* grad_w, cgtp_stream stream);
+
+/* The identity of cgtp_double_backward applied to the fused convolution. */
+cgtp_status cgtp_conv_double_backward(cgtp_plan plan, int64_t N, int64_t E, const int32_t* rowptr,
+                                      const int32_t* sender, const int32_t* s_rowptr,
+                                      const int32_t* s_perm, const int32_t* s_recv, const void* x,
+                                      const void* y, const void* w, double scale,
+                                      const void* grad_out, const void* gg_x, const void* gg_y,
+                                      const void* gg_w, void* d_x, void* d_y, void* d_w,
+                                      void* d_grad_out, cgtp_stream stream);
+
+/* --------------------------------------------- spherical harmonics ------ */
+/* The per-edge basis "depends on spherical harmonics" of the relative position
+ * (NVIDIA SE(3)-Transformer blog, "Basis precomputation").  Component
+ * normalisation, vectors normalised first, 0 <= lmax <= 6; y [E, (lmax+1)^2]. */
+cgtp_status cgtp_sh_forward(int lmax, cgtp_dtype dtype, int64_t E, const void* vec, void* y,
+                            cgtp_stream stream);
+/* grad_vec[e] = J(vec[e])^T grad_y[e], J = dY/dvec. */
+cgtp_status cgtp_sh_backward(int lmax, cgtp_dtype dtype, int64_t E, const void* vec,
+                             const void* grad_y, void* grad_vec, cgtp_stream stream);
+/* tangent_y[e] = J(vec[e]) tangent_vec[e] (the derivative of cgtp_sh_backward with
+ * respect to grad_y, used by the force-loss chain). */
+cgtp_status cgtp_sh_jvp(int lmax, cgtp_dtype dtype, int64_t E, const void* vec,
+                        const void* tangent_vec, void* tangent_y, cgtp_stream stream);
+
+/* ---------------------------------------------------------- forces ------ */
+/* Interatomic forces from per-edge energy gradients ("higher partial
+ * derivatives required to predict interatomic forces", abstract of arXiv
+ * 2501.13986), edge vector r_e = pos[recv] - pos[send]:
+ *   forces[i] = -sum_{e: recv e = i} dEdr[e] + sum_{e: send e = i} dEdr[e]
+ * dEdr [E, 3], forces [N, 3]; receiver CSR and sender-grouped view. */
+cgtp_status cgtp_edge_forces(cgtp_dtype dtype, int64_t N, int64_t E, const int32_t* rowptr,
+                             const int32_t* s_rowptr, const int32_t* s_perm, const void* dEdr,
+                             void* forces, cgtp_stream stream);
+/* Adjoint of cgtp_edge_forces: grad_dEdr[e] = grad_forces[sender e] - grad_forces[recv e]. */
+cgtp_status cgtp_edge_forces_adjoint(cgtp_dtype dtype, int64_t N, int64_t E,
+                                     const int32_t* rowptr, const int32_t* sender,
+                                     const void* grad_forces, void* grad_dEdr, cgtp_stream stream);
+
+/* ------------------------------------------------------------ misc ------ */
+const char* cgtp_status_str(cgtp_status s);
+/* CUDA error code behind the calling thread's last CGTP_E_CUDA / CGTP_E_COMPILE. */
+cgtp_status cgtp_last_cuda_error(int* cuda_err);
+/* Text of the calling thread's last error (NVRTC log, argument detail). */
+const char* cgtp_last_error_message(void);
+/* Number of kernel launches this process has issued through the library. */
+int64_t cgtp_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CGTP_H */

@@ -1,0 +1,130 @@
+"""Host-side checks of the C-ABI library (no GPU needed).
+
+The library loads, exports every symbol declared in include/cgtp.h, plans the
+five workloads, computes CG coefficients that agree with the oracle's (an
+independent route: ladder recursion vs Racah's sum), reports bad arguments with
+status codes, and its generated kernels compile for sm_103a with NVRTC.
+"""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle as O
+import workloads as W
+import clebsch_gordan_tensor_gb300 as cg
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+ALL_CFGS = [W.CFG0, W.CFG1, W.CFG2, W.CFG3, W.CFG4]
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "cgtp.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(cgtp_\w+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol():
+    L = cg.lib()
+    names = _declared()
+    assert len(names) >= 20
+    for n in names:
+        assert hasattr(L, n), n
+
+
+@pytest.mark.parametrize("irreps", ALL_CFGS)
+def test_plan_matches_oracle_problem(irreps):
+    plan = cg.Plan(*irreps)
+    prob = O.make_problem(*irreps)
+    assert (plan.dim_in1, plan.dim_in2, plan.dim_out, plan.weight_numel, plan.n_paths) == (
+        prob.dim1, prob.dim2, prob.dimo, prob.wdim, len(prob.paths))
+    for p, path in enumerate(prob.paths):
+        i1, i2, i3, l1, l2, l3 = path[:6]
+        assert plan.path(p) == (l1, l2, l3, i1, i2, i3)
+        assert np.abs(plan.coefficients(p) - O.cg_real(l1, l2, l3)).max() < 1e-14
+
+
+def test_planner_cg_agrees_with_racah_up_to_l6():
+    """Ladder recursion (library) vs Racah's closed form (oracle) for every
+    triple with l <= 6; the error grows with l (1e-14 at l <= 3)."""
+    worst = {}
+    for l1 in range(7):
+        for l2 in range(7):
+            outs = list(range(abs(l1 - l2), min(6, l1 + l2) + 1))
+            par = "e" if l2 % 2 == 0 else "o"  # in1 is even: p3 = p2
+            out = "+".join(f"1x{l3}{par}" for l3 in outs)
+            plan = cg.Plan(f"1x{l1}e", f"{l2}{'e' if l2 % 2 == 0 else 'o'}", out)
+            assert plan.n_paths == len(outs)
+            for p in range(plan.n_paths):
+                a, b, c = plan.path(p)[:3]
+                err = np.abs(plan.coefficients(p) - O.cg_real(a, b, c)).max()
+                key = max(a, b, c)
+                worst[key] = max(worst.get(key, 0.0), err)
+    assert max(v for k, v in worst.items() if k <= 3) < 1e-14
+    assert max(worst.values()) < 1e-12
+
+
+def test_explicit_instructions_and_errors():
+    plan = cg.Plan("4x0e+4x1o", "0e+1o", "4x1o", instructions=[(0, 1, 0), (1, 0, 0)])
+    assert plan.n_paths == 2 and plan.weight_numel == 8
+    with pytest.raises(cg.CgtpError, match="allowed path"):
+        cg.Plan("4x0e", "0e", "4x1o", instructions=[(0, 0, 0)])
+    with pytest.raises(cg.CgtpError, match="allowed path"):
+        cg.Plan("4x0e", "0e", "4x0e", instructions=[(0, 3, 0)])
+    with pytest.raises(cg.CgtpError, match="irreps"):
+        cg.Plan("4x1q", "0e", "4x1o")
+    with pytest.raises(cg.CgtpError, match="irreps"):
+        cg.Plan("", "0e", "4x1o")
+    with pytest.raises(cg.CgtpError, match="irreps"):
+        cg.Plan("4x7e", "0e", "4x7e")
+    with pytest.raises(cg.CgtpError, match="unsupported"):
+        cg.Plan("4x0e+8x1o", "0e", "4x0e")
+    with pytest.raises(cg.CgtpError, match="unsupported"):
+        cg.Plan("4x0e", "2x0e", "4x0e")
+
+
+def test_c_abi_argument_errors():
+    L = cg.lib()
+    h = ctypes.c_void_p()
+    assert L.cgtp_plan_create(None, b"1x0e", b"0e", b"1x0e", None, 0, 0, 0, 0) == 1
+    assert L.cgtp_plan_create(ctypes.byref(h), b"1x0e", b"0e", b"1x0e", None, 0, 7, 0, 0) == 1
+    assert L.cgtp_plan_create(ctypes.byref(h), b"4x0e", b"0e", b"4x0e", None, 0, 0, 0, 0) == 0
+    null = ctypes.c_void_p()
+    # size and pointer checks return before any CUDA call
+    assert L.cgtp_forward(h, -1, null, null, null, null, null) == 1
+    assert L.cgtp_forward(h, 0, null, null, null, null, null) == 0
+    assert L.cgtp_forward(h, 5, null, null, null, null, null) == 1
+    misaligned = ctypes.c_void_p(0x1004)
+    assert L.cgtp_forward(h, 5, misaligned, misaligned, misaligned, misaligned, null) == 1
+    assert L.cgtp_conv_forward(h, -1, 0, null, null, null, null, null, 1.0, null, null) == 5
+    assert L.cgtp_conv_forward(h, 3, 4, null, null, null, null, null, 1.0, null, null) == 5
+    assert L.cgtp_conv_forward(h, 0, 0, null, null, null, null, null, 1.0, null, null) == 0
+    assert L.cgtp_sh_forward(9, 0, 4, null, null, null) == 4
+    assert L.cgtp_sh_forward(3, 0, 0, null, null, null) == 0
+    assert L.cgtp_sh_forward(3, 0, 4, null, null, null) == 1
+    assert L.cgtp_forward(None, 1, null, null, null, null, null) == 1
+    assert L.cgtp_status_str(7) == b"CUDA error"
+    err = ctypes.c_int(-1)
+    assert L.cgtp_last_cuda_error(ctypes.byref(err)) == 0
+    assert L.cgtp_plan_destroy(h) == 0
+    s = cg.Plan("2x0e", "0e", "2x0e", shared_weights=True)
+    gx = ctypes.c_void_p(0x1000)
+    assert L.cgtp_backward(s._h, 1, gx, gx, gx, gx, null, null, gx, null) == 4
+
+
+@pytest.mark.parametrize("irreps,dtype", [(W.CFG0, "f32"), (W.CFG2, "f32"), (W.CFG4, "f32"),
+                                          (W.CFG1, "f32"), (W.CFG3, "f64")])
+def test_generated_kernels_compile_for_sm103a(irreps, dtype):
+    import torch
+    plan = cg.Plan(*irreps, dtype=torch.float64 if dtype == "f64" else torch.float32)
+    log = plan.compile()
+    assert "sm_103a" in log
+    spills = dict(re.findall(r"Function properties for (\w+)\n.*?(\d+) bytes spill stores", log))
+    assert set(spills) == {"cgtp_fwd_conv", "cgtp_fwd_single", "cgtp_bwd_conv",
+                           "cgtp_bwd_conv_nogy", "cgtp_bwd_single", "cgtp_bwd_single_nogy"}
+    assert int(spills["cgtp_fwd_conv"]) == 0 and int(spills["cgtp_fwd_single"]) == 0, log
+    assert max(int(v) for v in spills.values()) <= 128, log
+    src = plan.source()
+    assert "fma.rn.f32x2" in src or dtype == "f64"
