@@ -1,0 +1,154 @@
+"""GPU parity at the workloads' full sizes, in the launch configuration the
+benchmark times.  The GPU computes every output; the oracle computes sampled
+rows (receivers, senders, edges or samples) one by one.
+
+Workloads (seeded recipes in ``workloads``):
+  0  standalone TP, B = 1000, fp32                       (compared in full)
+  1  standalone TP, B = 200,000, 128 channels, fp32      (sampled rows)
+  2  fused conv, N = 10,000 atoms, ~525k edges, fp32     (sampled rows)
+  3  fused conv, N = 5,000 atoms, 128 channels, fp64     (forward, sampled)
+  4  TFN layer on 1000 molecules, fwd + bwd + double backward and forces, fp32
+"""
+import numpy as np
+import pytest
+
+import oracle as O
+import workloads as W
+from tests.gpu_util import assert_close, dev, host, need_gpu, torch
+
+pytestmark = pytest.mark.gpu
+
+
+def _cg():
+    import clebsch_gordan_tensor_gb300 as cg
+    return cg
+
+
+def _sample(rng, n, k):
+    idx = rng.choice(n, size=min(k, n), replace=False)
+    return np.unique(np.concatenate([idx, [0, n - 1]]))
+
+
+def test_config0_full():
+    need_gpu()
+    cg = _cg()
+    cfg = W.config0()
+    prob = O.make_problem(*cfg["irreps"])
+    plan = cg.Plan(*cfg["irreps"])
+    x, v, w = cfg["x"], cfg["vec"], cfg["w"]
+    y = cg.sh_forward(dev(v), 2)
+    out = plan.forward(dev(x), y, dev(w))
+    yr = O.sh(2, v)
+    assert_close(host(y), yr, np.float32, "Y")
+    assert_close(host(out), O.tp_forward(prob, x, yr, w), np.float32, "out")
+    g = np.random.default_rng(0).standard_normal(out.shape).astype(np.float32)
+    gx, gy, gw = plan.backward(dev(x), y, dev(w), dev(g))
+    rx, ry, rw = O.tp_backward(prob, x, yr, w, g)
+    for a, b, n in ((gx, rx, "gx"), (gy, ry, "gy"), (gw, rw, "gw")):
+        assert_close(host(a), b, np.float32, n)
+
+
+def test_config1_sampled():
+    need_gpu()
+    cg = _cg()
+    cfg = W.config1()
+    prob = O.make_problem(*cfg["irreps"])
+    plan = cg.Plan(*cfg["irreps"])
+    B = cfg["B"]
+    x, v, w = dev(cfg["x"]), dev(cfg["vec"]), dev(cfg["w"])
+    y = cg.sh_forward(v, 3)
+    out = plan.forward(x, y, w)
+    rng = np.random.default_rng(1)
+    idx = _sample(rng, B, 256)
+    yr = O.sh(3, cfg["vec"][idx])
+    ref = O.tp_forward(prob, cfg["x"][idx], yr, cfg["w"][idx])
+    assert_close(host(out[torch.from_numpy(idx).cuda()]), ref, np.float32, "out rows")
+    g = torch.randn(B, plan.dim_out, device="cuda", generator=torch.Generator("cuda").manual_seed(1))
+    gx, gy, gw = plan.backward(x, y, w, g)
+    ti = torch.from_numpy(idx).cuda()
+    rx, ry, rw = O.tp_backward(prob, cfg["x"][idx], yr, cfg["w"][idx], host(g[ti]))
+    assert_close(host(gx[ti]), rx, np.float32, "gx rows")
+    assert_close(host(gy[ti]), ry, np.float32, "gy rows")
+    assert_close(host(gw[ti]), rw, np.float32, "gw rows")
+
+
+def _conv_sampled(cfg, dt, do_bwd: bool):
+    cg = _cg()
+    gr = cfg["graph"]
+    prob = O.make_problem(*cfg["irreps"])
+    plan = cg.Plan(*cfg["irreps"], dtype=torch.float64 if dt == np.float64 else torch.float32)
+    G = cg.Graph.from_numpy(gr)
+    x, v, w = dev(cfg["x"]), dev(cfg["vec"]), dev(cfg["w"])
+    y = cg.sh_forward(v, 3)
+    out = plan.conv_forward(G, x, y, w, cfg["scale"])
+    yr = O.sh(3, cfg["vec"])
+    assert_close(host(y), yr, dt, "Y")
+    rng = np.random.default_rng(2)
+    nodes = _sample(rng, gr.N, 120)
+    ref = O.conv_forward(prob, gr.rowptr, gr.sender, cfg["x"], yr, cfg["w"], cfg["scale"],
+                         receivers=nodes)
+    assert_close(host(out)[nodes], ref[nodes], dt, "conv out rows")
+    if not do_bwd:
+        return
+    g = np.random.default_rng(3).standard_normal((gr.N, prob.dimo)).astype(dt)
+    gx, gy, gw = plan.conv_backward(G, x, y, w, cfg["scale"], dev(g))
+    edges = _sample(rng, gr.E, 400)
+    rx, ry, rw = O.conv_backward(prob, gr.rowptr, gr.sender, cfg["x"], yr, cfg["w"],
+                                 cfg["scale"], g, nodes=nodes, edges=edges)
+    assert_close(host(gx)[nodes], rx[nodes], dt, "gx rows")
+    assert_close(host(gy)[edges], ry[edges], dt, "gy rows")
+    assert_close(host(gw)[edges], rw[edges], dt, "gw rows")
+
+
+def test_config2_sampled():
+    need_gpu()
+    _conv_sampled(W.config2(), np.float32, True)
+
+
+def test_config3_sampled_fp64():
+    need_gpu()
+    _conv_sampled(W.config3(), np.float64, False)
+
+
+def test_config4_chain_sampled():
+    need_gpu()
+    cg = _cg()
+    from tests.test_gpu_conv import tfn_chain_gpu
+
+    cfg = W.config4()
+    gr = cfg["graph"]
+    prob = O.make_problem(*W.CFG4)
+    plan = cg.Plan(*W.CFG4)
+    G = cg.Graph.from_numpy(gr)
+    res = tfn_chain_gpu(cg, plan, G, dev(cfg["x"]), dev(cfg["vec"]), dev(cfg["w"]),
+                        dev(cfg["c"]), dev(cfg["gF"]))
+    res = {k: host(t) for k, t in res.items()}
+    rng = np.random.default_rng(4)
+    x, w, c, gF, vec = cfg["x"], cfg["w"], cfg["c"], cfg["gF"], cfg["vec"]
+    yr = O.sh(3, vec)
+    assert_close(res["y"], yr, np.float32, "Y")
+    nodes = _sample(rng, gr.N, 100)
+    assert_close(res["out"][nodes],
+                 O.conv_forward(prob, gr.rowptr, gr.sender, x, yr, w, 1.0, receivers=nodes)[nodes],
+                 np.float32, "out rows")
+    # edges incident to the sampled nodes (for the forces there)
+    inc = np.zeros(gr.E, dtype=bool)
+    inc[np.isin(gr.receiver, nodes) | np.isin(gr.sender, nodes)] = True
+    edges = np.nonzero(inc)[0]
+    rx, ry, rw = O.conv_backward(prob, gr.rowptr, gr.sender, x, yr, w, 1.0, c, nodes=nodes,
+                                 edges=edges)
+    assert_close(res["gx"][nodes], rx[nodes], np.float32, "gx rows")
+    assert_close(res["gy"][edges], ry[edges], np.float32, "gy rows")
+    assert_close(res["gw"][edges], rw[edges], np.float32, "gw rows")
+    dEdr = np.zeros((gr.E, 3))
+    dEdr[edges] = O.sh_vjp(3, vec[edges], ry[edges])
+    assert_close(res["dEdr"][edges], dEdr[edges], np.float32, "dE/dr rows")
+    F = O.edge_forces(gr.rowptr, gr.sender, dEdr)
+    assert_close(res["F"][nodes], F[nodes], np.float32, "forces rows")
+    q = gF[gr.sender].astype(np.float64) - gF[gr.receiver]
+    ggy = O.sh_jvp(3, vec, q)
+    assert_close(res["ggy"], ggy, np.float32, "ggY")
+    dx, _, dw = O.conv_backward(prob, gr.rowptr, gr.sender, x, ggy, w, 1.0, c, nodes=nodes,
+                                edges=edges)
+    assert_close(res["d_x"][nodes], dx[nodes], np.float32, "dL/dx rows")
+    assert_close(res["d_w"][edges], dw[edges], np.float32, "dL/dw rows")
