@@ -154,7 +154,7 @@ def run_gpu(args):
     dist, rank, world = _dist()
     local = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(local)
-    cfg = W.config2()
+    cfg = W.config2(N=args.atoms)
     gr = cfg["graph"]
     N, E = gr.N, gr.E
     plan = cg.Plan(*cfg["irreps"])
@@ -217,7 +217,7 @@ def run_gpu(args):
     ms_step = ms_total / args.steps
 
     # ---- e2e: host buffers, copies inside the timed region
-    e2e = run_e2e(args, plan, G, cfg, g, scale, N, E)
+    e2e = None if args.no_e2e else run_e2e(args, plan, G, cfg, g, scale, N, E)
 
     if rank != 0:
         return None
@@ -259,7 +259,8 @@ def run_gpu(args):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded periodic atom cloud, random radial-MLP weights)",
-        "config": {"workload": WORKLOAD, "N": N, "E": E, "mul": 64, "paths": plan.n_paths,
+        "config": {"workload": WORKLOAD if N == 10_000 else WORKLOAD.replace("N=10000", f"N={N}"),
+                   "N": N, "E": E, "mul": 64, "paths": plan.n_paths,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "inputs larger than L2 (3.2 GB weight stream per step)"},
         "fwd": {"value": E * world / (per["conv_fwd"] * 1e-3 + per["sh_fwd"] * 1e-3),
@@ -342,7 +343,9 @@ def _oracle_subgraph_step(prob, cfg, R):
     import oracle as O
     gr = cfg["graph"]
     e1 = int(gr.rowptr[R])
-    rowptr, sender = gr.rowptr[:R + 1], gr.sender[:e1]
+    # receivers R.. keep no edges; senders still index all N nodes
+    rowptr = np.concatenate([gr.rowptr[:R + 1], np.full(gr.N - R, e1, dtype=gr.rowptr.dtype)])
+    sender = gr.sender[:e1]
     vec, w = cfg["vec"][:e1], cfg["w"][:e1]
     y = O.sh(3, vec)
     out = O.conv_forward(prob, rowptr, sender, cfg["x"], y, w, cfg["scale"])
@@ -405,6 +408,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--atoms", type=int, default=10_000,
+                    help="atom count (10000 is the benchmark workload; smaller for profiling)")
+    ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args()
     line = run_reference(args) if args.impl == "reference" else run_gpu(args)
     if line is not None:

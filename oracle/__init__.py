@@ -275,6 +275,20 @@ def tp_double_backward(prob: Problem, x, y, w, g, ggx=None, ggy=None, ggw=None):
 
 # ------------------------------------------------------ graph convolution --
 
+def _check_graph(prob, rowptr, sender, x, y, w, ws):
+    N, E = rowptr.shape[0] - 1, sender.shape[0]
+    if x.shape != (N, prob.dim1):
+        raise ValueError(f"x has shape {x.shape}, expected {(N, prob.dim1)}")
+    if y.shape != (E, prob.dim2):
+        raise ValueError(f"y has shape {y.shape}, expected {(E, prob.dim2)}")
+    if ws and w.shape != (E, prob.wdim):
+        raise ValueError(f"w has shape {w.shape}, expected {(E, prob.wdim)}")
+    if rowptr[0] != 0 or rowptr[-1] != E or np.any(np.diff(rowptr) < 0):
+        raise ValueError("rowptr is not a CSR row pointer over the edges")
+    if E and (sender.min() < 0 or sender.max() >= N):
+        raise ValueError("sender index out of range")
+
+
 def conv_forward(prob: Problem, rowptr, sender, x, y, w, scale: float, receivers=None):
     """out[n] = scale * sum over the receiver's edges, in edge order, of
     TP(x[sender[e]], y[e], w[e]).  With ``receivers`` only those rows are
@@ -283,6 +297,7 @@ def conv_forward(prob: Problem, rowptr, sender, x, y, w, scale: float, receivers
     x, y = _f64(x), _f64(y)
     N, E = rowptr.shape[0] - 1, sender.shape[0]
     w, ws = _wstride(prob, w, E)
+    _check_graph(prob, rowptr, sender, x, y, w, ws)
     out = np.zeros((N, prob.dimo))
     sel = None if receivers is None else np.ascontiguousarray(receivers, dtype=np.int64)
     r = _load().oracle_conv_forward(
@@ -303,6 +318,8 @@ def conv_backward(prob: Problem, rowptr, sender, x, y, w, scale: float, g, nodes
     x, y, g = _f64(x), _f64(y), _f64(g)
     N, E = rowptr.shape[0] - 1, sender.shape[0]
     w, ws = _wstride(prob, w, E)
+    _check_graph(prob, rowptr, sender, x, y, w, ws)
+    g = g.reshape(N, prob.dimo)
     gx, gy = np.zeros((N, prob.dim1)), np.zeros((E, prob.dim2))
     gw = np.zeros((E, prob.wdim)) if ws else np.zeros(prob.wdim)
     nm = em = None
@@ -346,6 +363,8 @@ def edge_forces(rowptr, sender, dEdr) -> np.ndarray:
     rowptr, sender = _i32(rowptr), _i32(sender)
     d = _f64(dEdr).reshape(-1, 3)
     N = rowptr.shape[0] - 1
+    if d.shape[0] != sender.shape[0] or (sender.size and (sender.min() < 0 or sender.max() >= N)):
+        raise ValueError("dEdr / sender do not match the graph")
     F = np.zeros((N, 3))
     _load().oracle_edge_forces(N, sender.shape[0], _p(rowptr, ctypes.c_int32),
                                _p(sender, ctypes.c_int32), _p(d), _p(F))
