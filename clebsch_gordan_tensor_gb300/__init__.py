@@ -75,6 +75,7 @@ def lib() -> ctypes.CDLL:
                 "cgtp_edge_forces": [i32, i64, i64, vp, vp, vp, vp, vp, vp],
                 "cgtp_edge_forces_adjoint": [i32, i64, i64, vp, vp, vp, vp, vp],
                 "cgtp_last_cuda_error": [P(i32)],
+                "cgtp_plan_device_status": [vp, P(i32)],
             }
             for name, args in sig.items():
                 f = getattr(L, name)
@@ -200,6 +201,13 @@ class Plan:
         _check(lib().cgtp_plan_coefficients(self._h, p, out.ctypes.data_as(
             ctypes.POINTER(ctypes.c_double))))
         return out.reshape(2 * l1 + 1, 2 * l2 + 1, 2 * l3 + 1)
+
+    def device_status(self) -> int:
+        """Raise if a staged kernel of this plan reported a device-side error
+        (bounded wait timed out); synchronises with the device."""
+        code = ctypes.c_int(0)
+        _check(lib().cgtp_plan_device_status(self._h, ctypes.byref(code)))
+        return code.value
 
     def compile(self) -> str:
         buf = ctypes.create_string_buffer(1 << 16)

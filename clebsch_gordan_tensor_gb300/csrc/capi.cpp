@@ -4,7 +4,9 @@
 // caller's stream.  Nothing here allocates device memory.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
+#include <mutex>
 #include <climits>
 #include <cstring>
 #include <new>
@@ -54,19 +56,69 @@ static cgtp_status check_rows(const Plan& p, std::initializer_list<const void*> 
 }
 
 static cgtp_status launch_tp(Plan& p, const char* name, int64_t n_items, void** args,
-                             cudaStream_t s) {
+                             cudaStream_t s, bool staged = false, size_t smem = 0) {
     if (n_items <= 0) return CGTP_OK;
     std::shared_ptr<Module> m;
     std::string err;
     cgtp_status st = get_module(p, true, m, err);
     if (st != CGTP_OK) return fail(st, err);
-    int64_t blocks = (n_items + p.slots - 1) / p.slots;
-    if (blocks > INT_MAX) blocks = INT_MAX;
-    cudaError_t e = cudaLaunchKernel((const void*)m->kernels[name], dim3((unsigned)blocks),
-                                     dim3(p.block), args, 0, s);
+    cudaKernel_t k = m->kernels[name];
+    if (!k) return fail(CGTP_E_ARG, std::string("kernel not in module: ") + name);
+    cudaError_t e;
+    if (!staged) {
+        int64_t blocks = (n_items + p.slots - 1) / p.slots;
+        if (blocks > INT_MAX) blocks = INT_MAX;
+        e = cudaLaunchKernel((const void*)k, dim3((unsigned)blocks), dim3(p.block), args, 0, s);
+    } else {
+        int dev = 0;
+        if ((e = cudaGetDevice(&dev)) != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+        int per_sm = 0, sms = 0;
+        {
+            std::lock_guard<std::mutex> g(p.mu);
+            if (!m->smem_set.count(dev)) {
+                const size_t need = std::max(p.fwd_smem, p.bwd_smem);
+                e = cudaKernelSetAttributeForDevice(m->kernels["cgtp_fwd_conv_tma"],
+                                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                    (int)need, dev);
+                for (const char* kn : {"cgtp_fwd_single_tma", "cgtp_bwd_conv_tma",
+                                       "cgtp_bwd_conv_nogy_tma", "cgtp_bwd_single_tma",
+                                       "cgtp_bwd_single_nogy_tma"})
+                    if (e == cudaSuccess)
+                        e = cudaKernelSetAttributeForDevice(
+                            m->kernels[kn], cudaFuncAttributeMaxDynamicSharedMemorySize, (int)need,
+                            dev);
+                if (e != cudaSuccess) return cuda_fail(e, "set max dynamic shared memory");
+                m->smem_set[dev] = 1;
+            }
+            auto key = std::make_pair(dev, std::string(name));
+            auto it = m->ctas_per_sm.find(key);
+            if (it == m->ctas_per_sm.end()) {
+                int n = 0;
+                if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, (const void*)k, p.lanes,
+                                                                  smem) != cudaSuccess || n < 1) {
+                    cudaGetLastError();
+                    n = std::max(1, (int)((220 * 1024) / (smem + 4096)));
+                }
+                m->ctas_per_sm[key] = n;
+                per_sm = n;
+            } else {
+                per_sm = it->second;
+            }
+        }
+        if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+            return cuda_fail(e, "cudaDeviceGetAttribute");
+        const int64_t grid = std::min<int64_t>(n_items, (int64_t)sms * per_sm);
+        e = cudaLaunchKernel((const void*)k, dim3((unsigned)grid), dim3(p.lanes), args, smem, s);
+    }
     if (e != cudaSuccess) return cuda_fail(e, name);
     count_launch();
     return CGTP_OK;
+}
+
+static bool a16(std::initializer_list<const void*> ptrs) {
+    for (const void* q : ptrs)
+        if (q && ((uintptr_t)q % 16) != 0) return false;
+    return true;
 }
 
 // One forward-shaped launch: out (=|+=) scale * sum TP(a, b, c).
@@ -78,12 +130,15 @@ static cgtp_status fwd_launch(Plan& p, bool conv, int64_t n_items, const int32_t
     float sf = (float)scale;
     double sd = scale;
     void* sp = p.dtype == CGTP_F64 ? (void*)&sd : (void*)&sf;
+    const bool staged = p.staged && a16({a, b, c, out});
     if (conv) {
         void* args[] = {&n, &rowptr, &sender, &a, &b, &c, &ws, &out, sp, &accumulate};
-        return launch_tp(p, "cgtp_fwd_conv", n_items, args, s);
+        return launch_tp(p, staged ? "cgtp_fwd_conv_tma" : "cgtp_fwd_conv", n_items, args, s,
+                         staged, p.fwd_smem);
     }
     void* args[] = {&n, &a, &b, &c, &ws, &out, sp, &accumulate};
-    return launch_tp(p, "cgtp_fwd_single", n_items, args, s);
+    return launch_tp(p, staged ? "cgtp_fwd_single_tma" : "cgtp_fwd_single", n_items, args, s,
+                     staged, p.fwd_smem);
 }
 
 // One backward-shaped launch over items (senders or samples).
@@ -99,9 +154,11 @@ static cgtp_status bwd_launch(Plan& p, bool conv, int64_t n_items, const int32_t
     void* sp = p.dtype == CGTP_F64 ? (void*)&sd : (void*)&sf;
     void* args[] = {&n, &s_rowptr, &s_perm, &s_recv, &x, &y, &w, &ws, &g, sp,
                     &gx, &gy, &gw, &mgx, &mgy, &mgw};
-    const char* name = conv ? (mgy ? "cgtp_bwd_conv" : "cgtp_bwd_conv_nogy")
+    const bool staged = p.staged && a16({x, y, w, g});
+    std::string name = conv ? (mgy ? "cgtp_bwd_conv" : "cgtp_bwd_conv_nogy")
                             : (mgy ? "cgtp_bwd_single" : "cgtp_bwd_single_nogy");
-    return launch_tp(p, name, n_items, args, s);
+    if (staged) name += "_tma";
+    return launch_tp(p, name.c_str(), n_items, args, s, staged, p.bwd_smem);
 }
 
 static size_t esize(const Plan& p) { return p.dtype == CGTP_F64 ? 8 : 4; }
@@ -274,6 +331,31 @@ cgtp_status cgtp_plan_source(cgtp_plan plan, char* buf, size_t cap, size_t* need
     if (buf && cap) {
         strncpy(buf, src.c_str(), cap - 1);
         buf[cap - 1] = 0;
+    }
+    return CGTP_OK;
+    GUARD_END
+}
+
+cgtp_status cgtp_plan_device_status(cgtp_plan plan, int* code) {
+    GUARD_BEGIN
+    if (!plan) return fail(CGTP_E_ARG, "plan is NULL");
+    if (code) *code = 0;
+    std::shared_ptr<Module> m;
+    {
+        std::lock_guard<std::mutex> g(plan->p.mu);
+        auto it = plan->p.modules.find("tp");
+        if (it == plan->p.modules.end() || !it->second->lib || !it->second->err_flag) return CGTP_OK;
+        m = it->second;
+    }
+    int v = 0;
+    cudaError_t e = cudaMemcpy(&v, m->err_flag, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "read device error flag");
+    if (code) *code = v;
+    if (v) {
+        const int zero = 0;
+        cudaMemcpy(m->err_flag, &zero, sizeof(int), cudaMemcpyHostToDevice);
+        return fail(CGTP_E_DEVICE, "a kernel timed out waiting for a bulk copy (code " +
+                                       std::to_string(v) + ")");
     }
     return CGTP_OK;
     GUARD_END

@@ -17,6 +17,9 @@ struct Module {
     std::string log;  // NVRTC / ptxas log (register and spill report)
     cudaLibrary_t lib = nullptr;
     std::map<std::string, cudaKernel_t> kernels;
+    void* err_flag = nullptr;           // device address of cgtp_device_error (staged)
+    std::map<int, int> smem_set;        // device -> dynamic smem attribute already set
+    std::map<std::pair<int, std::string>, int> ctas_per_sm;
     ~Module();
 };
 

@@ -4,15 +4,20 @@
 #include <nvrtc.h>
 
 #include <cstring>
+#include <iterator>
+#include <vector>
 #include <string>
 
 #include "internal.hpp"
 
 namespace cgtp {
 
-static const char* kKernelNames[] = {"cgtp_fwd_conv",     "cgtp_fwd_single",
-                                     "cgtp_bwd_conv",     "cgtp_bwd_conv_nogy",
-                                     "cgtp_bwd_single",   "cgtp_bwd_single_nogy"};
+static const char* kKernelNames[] = {"cgtp_fwd_conv",   "cgtp_fwd_single",
+                                     "cgtp_bwd_conv",   "cgtp_bwd_conv_nogy",
+                                     "cgtp_bwd_single", "cgtp_bwd_single_nogy"};
+static const char* kStagedNames[] = {"cgtp_fwd_conv_tma",   "cgtp_fwd_single_tma",
+                                     "cgtp_bwd_conv_tma",   "cgtp_bwd_conv_nogy_tma",
+                                     "cgtp_bwd_single_tma", "cgtp_bwd_single_nogy_tma"};
 
 cgtp_status compile_module(const std::string& src, const std::string& name, Module& m,
                            std::string& err) {
@@ -42,7 +47,7 @@ cgtp_status compile_module(const std::string& src, const std::string& name, Modu
     return CGTP_OK;
 }
 
-cgtp_status load_module(Module& m, std::string& err) {
+cgtp_status load_module(Module& m, bool staged, std::string& err) {
     if (m.lib) return CGTP_OK;
     cudaLibrary_t lib = nullptr;
     cudaError_t ce = cudaLibraryLoadData(&lib, m.cubin.data(), nullptr, nullptr, 0, nullptr,
@@ -52,7 +57,9 @@ cgtp_status load_module(Module& m, std::string& err) {
         err = std::string("cudaLibraryLoadData: ") + cudaGetErrorString(ce);
         return CGTP_E_CUDA;
     }
-    for (const char* k : kKernelNames) {
+    std::vector<const char*> names(std::begin(kKernelNames), std::end(kKernelNames));
+    if (staged) names.insert(names.end(), std::begin(kStagedNames), std::end(kStagedNames));
+    for (const char* k : names) {
         cudaKernel_t kern = nullptr;
         ce = cudaLibraryGetKernel(&kern, lib, k);
         if (ce != cudaSuccess) {
@@ -64,6 +71,10 @@ cgtp_status load_module(Module& m, std::string& err) {
         m.kernels[k] = kern;
     }
     m.lib = lib;
+    if (cudaLibraryGetGlobal(&m.err_flag, nullptr, lib, "cgtp_device_error") != cudaSuccess) {
+        m.err_flag = nullptr;
+        cudaGetLastError();
+    }
     return CGTP_OK;
 }
 
@@ -85,7 +96,7 @@ cgtp_status get_module(Plan& p, bool load, std::shared_ptr<Module>& out, std::st
         m = it->second;
     }
     if (load) {
-        cgtp_status st = load_module(*m, err);
+        cgtp_status st = load_module(*m, p.staged, err);
         if (st != CGTP_OK) return st;
     }
     out = m;

@@ -294,7 +294,14 @@ cgtp_status build_plan(Plan& p, const char* s1, const char* s2, const char* so,
     }
 
     // launch geometry
-    p.cpt = (p.dtype == CGTP_F32 && p.mul % 2 == 0) ? 2 : 1;
+    // fp32: two channels per lane (packed f32x2) when that still fills whole
+    // warps; otherwise one.  fp64: one channel per lane.
+    if (p.dtype == CGTP_F32 && p.mul % 64 == 0)
+        p.cpt = 2;
+    else if (p.dtype == CGTP_F32 && p.mul % 32 != 0 && p.mul % 2 == 0)
+        p.cpt = 2;
+    else
+        p.cpt = 1;
     p.nch = p.mul / p.cpt;
     p.lanes = p.nch <= 32 ? next_pow2(p.nch) : ((p.nch + 31) / 32) * 32;
     if (p.lanes > 1024) {
@@ -317,6 +324,26 @@ cgtp_status build_plan(Plan& p, const char* s1, const char* s2, const char* so,
         return CGTP_E_UNSUPPORTED;
     }
     p.block = p.slots * p.lanes;
+
+    // staged kernels: whole warps of full channel groups, 16-byte rows
+    const size_t es = p.dtype == CGTP_F64 ? 8 : 4;
+    const size_t WB = (size_t)p.wdim * es, XB = (size_t)p.dimx * es, GB = (size_t)p.dimo * es,
+                 YB = (size_t)p.ny * es;
+    const bool rows16 = WB % 16 == 0 && XB % 16 == 0 && GB % 16 == 0 && YB % 16 == 0;
+    if (p.nch == p.lanes && p.lanes % 32 == 0 && rows16 && !p.paths.empty()) {
+        const size_t fst = WB + XB + YB, bst = WB + GB + YB + 16;
+        const size_t stat = (size_t)std::max(2, nt + (nt & 1)) * vr + 1024;
+        for (int st = 3; st >= 2; --st) {
+            const size_t f = st * fst, b = st * bst + 2 * XB;
+            if (f + stat <= 200 * 1024 && b + stat <= 200 * 1024) {
+                p.staged = true;
+                p.stages = st;
+                p.fwd_smem = f;
+                p.bwd_smem = b;
+                break;
+            }
+        }
+    }
     return CGTP_OK;
 }
 
@@ -371,6 +398,8 @@ std::string Plan::kernel_source() const {
        << "\n#define NO " << no << "\n#define NP " << paths.size() << "\n#define NT " << nt
        << "\n#define NTP " << ntp << "\n#define MAXTERMS " << maxterms << "\n#define YPF "
        << (ny + lanes - 1) / lanes << "\n";
+    os << "#define STAGED " << (staged ? 1 : 0) << "\n#define STAGES " << stages
+       << "\n#define MINB_FWD 1\n#define MINB_BWD 1\n";
     // T tables
     os << "__device__ const short T_IDX[" << std::max(1, nt * maxterms) << "] = {";
     for (int k = 0; k < nt; ++k)
@@ -403,8 +432,8 @@ std::string Plan::kernel_source() const {
 
     std::ostringstream g;
     // ---- forward stream
-    g << "__device__ __forceinline__ void gen_fwd(VR (&acc)[NO], const VR* __restrict__ Ts,\n"
-         "    const VR (&xr)[NX], const REAL* __restrict__ wrow, int ch) {\n";
+    g << "template <class FX, class FW>\n__device__ __forceinline__ void gen_fwd(VR (&acc)[NO],\n"
+         "    const VR* __restrict__ Ts, FX&& X, FW&& W) {\n";
     if (cpt == 2) g << "    const ulonglong2* __restrict__ Tq = reinterpret_cast<const ulonglong2*>(Ts);\n";
     {
         TLoader L{cpt, std::vector<bool>(ntp / 2 + 1, false), &g};
@@ -412,11 +441,11 @@ std::string Plan::kernel_source() const {
             const Path& P = paths[q];
             const int d1 = 2 * P.l1 + 1, d3 = 2 * P.l3 + 1;
             g << "  { // path " << q << ": " << P.l1 << " x " << P.l2 << " -> " << P.l3 << "\n";
-            g << "    const VR w = LDW(" << q << ");\n";
+            g << "    const VR w = W(" << q << ");\n";
             std::fill(L.loaded.begin(), L.loaded.end(), false);  // loads are block-scoped
             if (d1 <= d3) {
                 for (int a = 0; a < d1; ++a)
-                    g << "    const VR z" << a << " = vmul(w, xr[" << P.r1 + a << "]);\n";
+                    g << "    const VR z" << a << " = vmul(w, X(" << P.r1 + a << "));\n";
                 for (int k = k0[q]; k < k0[q + 1]; ++k) {
                     const std::string t = L.get(k);
                     const int o = P.r3 + T[k].m3;
@@ -427,7 +456,7 @@ std::string Plan::kernel_source() const {
                 for (int k = k0[q]; k < k0[q + 1]; ++k) {
                     const std::string t = L.get(k);
                     const int c = T[k].m3;
-                    const std::string xv = "xr[" + std::to_string(P.r1 + T[k].m1) + "]";
+                    const std::string xv = "X(" + std::to_string(P.r1 + T[k].m1) + ")";
                     if (!started[c]) {
                         g << "    VR t" << c << " = vmul(" << t << ", " << xv << ");\n";
                         started[c] = true;
@@ -446,10 +475,9 @@ std::string Plan::kernel_source() const {
     g << "}\n\n";
 
     // ---- backward stream
-    g << "template <bool GY>\n__device__ __forceinline__ void gen_bwd(VR (&gxa)[NX], REAL (&gyl)[NYP],\n"
-         "    const VR* __restrict__ Ts, const VR (&xr)[NX], const VR (&gr)[NO],\n"
-         "    const REAL* __restrict__ wrow, REAL* __restrict__ gwrow, int ch, VR sc, bool dogx,\n"
-         "    int mgw) {\n";
+    g << "template <bool GY, class FX, class FG, class FW>\n__device__ __forceinline__ void gen_bwd(\n"
+         "    VR (&gxa)[NX], REAL (&gyl)[NYP], const VR* __restrict__ Ts, FX&& X, FG&& G, FW&& W,\n"
+         "    REAL* __restrict__ gwrow, int ch, VR sc, bool dogx, int mgw) {\n";
     if (cpt == 2) g << "    const ulonglong2* __restrict__ Tq = reinterpret_cast<const ulonglong2*>(Ts);\n";
     {
         TLoader L{cpt, std::vector<bool>(ntp / 2 + 1, false), &g};
@@ -457,14 +485,14 @@ std::string Plan::kernel_source() const {
             const Path& P = paths[q];
             const int d1 = 2 * P.l1 + 1, d3 = 2 * P.l3 + 1;
             g << "  { // path " << q << ": " << P.l1 << " x " << P.l2 << " -> " << P.l3 << "\n";
-            g << "    const VR w = LDW(" << q << ");\n";
+            g << "    const VR w = W(" << q << ");\n";
             std::fill(L.loaded.begin(), L.loaded.end(), false);  // loads are block-scoped
             // h[m1] = sum_m3 T[m1,m3] g[m3]
             std::vector<bool> hs(d1, false);
             for (int k = k0[q]; k < k0[q + 1]; ++k) {
                 const std::string t = L.get(k);
                 const int a = T[k].m1;
-                const std::string gv = "gr[" + std::to_string(P.r3 + T[k].m3) + "]";
+                const std::string gv = "G(" + std::to_string(P.r3 + T[k].m3) + ")";
                 if (!hs[a]) {
                     g << "    VR h" << a << " = vmul(" << t << ", " << gv << ");\n";
                     hs[a] = true;
@@ -479,7 +507,7 @@ std::string Plan::kernel_source() const {
                       << "]);\n";
             g << "    }\n    if (mgw) {\n      VR s = vzero();\n";
             for (int a = 0; a < d1; ++a)
-                if (hs[a]) g << "      s = vfma(xr[" << P.r1 + a << "], h" << a << ", s);\n";
+                if (hs[a]) g << "      s = vfma(X(" << P.r1 + a << "), h" << a << ", s);\n";
             g << "      s = vmul(s, sc);\n      REAL* gp = gwrow + " << (long long)q * mul << ";\n"
               << "      if (mgw == 2) s = vadd(s, ldv_plain(gp, ch));\n"
               << "      if (CH_ACTIVE(ch)) stv(gp, ch, s);\n    }\n";
@@ -488,17 +516,17 @@ std::string Plan::kernel_source() const {
             const bool zx = d1 <= d3;
             if (zx) {
                 for (int a = 0; a < d1; ++a)
-                    g << "      const VR z" << a << " = vmul(w, xr[" << P.r1 + a << "]);\n";
+                    g << "      const VR z" << a << " = vmul(w, X(" << P.r1 + a << "));\n";
             } else {
                 for (int c = 0; c < d3; ++c)
-                    g << "      const VR z" << c << " = vmul(w, gr[" << P.r3 + c << "]);\n";
+                    g << "      const VR z" << c << " = vmul(w, G(" << P.r3 + c << "));\n";
             }
             for (int k = k0[q]; k < k0[q + 1]; ++k) {
                 const TEntry& t = T[k];
                 const std::string lhs =
-                    zx ? "z" + std::to_string(t.m1) : "xr[" + std::to_string(P.r1 + t.m1) + "]";
+                    zx ? "z" + std::to_string(t.m1) : "X(" + std::to_string(P.r1 + t.m1) + ")";
                 const std::string rhs =
-                    zx ? "gr[" + std::to_string(P.r3 + t.m3) + "]" : "z" + std::to_string(t.m3);
+                    zx ? "G(" + std::to_string(P.r3 + t.m3) + ")" : "z" + std::to_string(t.m3);
                 g << "      { const REAL d = vdot(" << lhs << ", " << rhs << ");\n";
                 for (auto& term : t.terms)
                     g << "        gyl[" << term.first << "] = fma(" << lit(term.second, f64)

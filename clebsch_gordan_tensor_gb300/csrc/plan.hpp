@@ -60,6 +60,10 @@ struct Plan {
     int lanes = 0;  // threads per work slot (power of two <= 32, or multiple of 32)
     int slots = 0;  // slots per CTA
     int block = 0;  // threads per CTA
+    // staged (TMA) kernels: one slot of `lanes` threads per CTA
+    bool staged = false;
+    int stages = 3;
+    size_t fwd_smem = 0, bwd_smem = 0;  // dynamic shared memory per CTA
 
     std::mutex mu;
     std::map<std::string, std::shared_ptr<Module>> modules;

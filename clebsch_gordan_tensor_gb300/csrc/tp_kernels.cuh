@@ -87,8 +87,11 @@ __device__ __forceinline__ VR ldv_m(const REAL* p, int ch) {
     return CH_ACTIVE(ch) ? ldv(p, ch) : vzero();
 }
 
-// Weight of path p for this lane's channels.
-#define LDW(p) ldv_m(wrow + (long long)(p) * MUL, ch)
+// Weight of path p for this lane's channels, from global memory (direct
+// kernels) or from the shared-memory stage (staged kernels).
+__device__ __forceinline__ VR lds_v(const REAL* p, int ch) {
+    return reinterpret_cast<const VR*>(p)[ch];
+}
 
 #if LANES <= 32
 __device__ __forceinline__ unsigned slot_mask() {
@@ -211,7 +214,8 @@ __device__ __forceinline__ void fwd_body(long long n_items, const int* __restric
 #pragma unroll
             for (int r = 0; r < NX; ++r) xr[r] = ldv_m(xrow + r * MUL, ch);
             const REAL* wrow = w + e * w_stride;
-            gen_fwd(acc, Ts, xr, wrow, ch);
+            gen_fwd(acc, Ts, [&](int r) { return xr[r]; },
+                    [&](int p) { return ldv_m(wrow + (long long)p * MUL, ch); });
             slot_sync(slot);
         }
         if (CH_ACTIVE(ch)) {
@@ -333,7 +337,9 @@ __device__ __forceinline__ void bwd_body(long long n_items, const int* __restric
             REAL gyl[NYP];
 #pragma unroll
             for (int i = 0; i < NYP; ++i) gyl[i] = (REAL)0;
-            gen_bwd<GY>(gxa, gyl, Ts, xr, gr, wrow, gwrow, ch, sc, mgx != 0, mgw);
+            gen_bwd<GY>(gxa, gyl, Ts, [&](int r) { return xr[r]; }, [&](int r) { return gr[r]; },
+                        [&](int p) { return ldv_m(wrow + (long long)p * MUL, ch); }, gwrow, ch,
+                        sc, mgx != 0, mgw);
             if (GY && mgy) {
                 int base = 0;
                 bool owner = true;
@@ -392,3 +398,421 @@ CGTP_BWD_ENTRY(cgtp_bwd_conv, true, true)
 CGTP_BWD_ENTRY(cgtp_bwd_conv_nogy, true, false)
 CGTP_BWD_ENTRY(cgtp_bwd_single, false, true)
 CGTP_BWD_ENTRY(cgtp_bwd_single_nogy, false, false)
+
+// ===================================================================== staged
+//
+// Staged kernels (generated when every lane has a full channel group, rows are
+// 16-byte multiples and the plan fits): one slot per CTA, persistent grid, each
+// CTA owns a contiguous item range balanced by edge count.  Thread 0 streams the
+// per-edge rows (weights, the gathered x or g row, y) into an S-deep ring of
+// shared-memory stages with cp.async.bulk (TMA, completion on an mbarrier),
+// STAGES-1 edges ahead of the edge being computed, so HBM latency overlaps the
+// FMA stream.  Every wait is bounded: on timeout the kernel records an error
+// code in cgtp_device_error and stops.
+
+#if STAGED
+
+__device__ int cgtp_device_error;
+
+__device__ __forceinline__ unsigned smem_u32(const void* p) {
+    return (unsigned)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(unsigned long long* b, unsigned count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(b)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(unsigned long long* b, unsigned bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(b)),
+                 "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned bytes,
+                                         unsigned long long* b) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(b)) : "memory");
+}
+// Bounded wait for phase `parity` of barrier b.  Returns false on timeout.
+__device__ __forceinline__ bool mbar_wait(unsigned long long* b, unsigned parity) {
+    const unsigned a = smem_u32(b);
+    for (unsigned it = 0; it < (1u << 22); ++it) {
+        unsigned ok;
+        asm volatile(
+            "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+            : "=r"(ok) : "r"(a), "r"(parity) : "memory");
+        if (ok) return true;
+        if (it > 64) __nanosleep(256);
+    }
+    return false;
+}
+
+// First index n in [0, N] with ptr[n] >= target (ptr non-decreasing), computed
+// by one warp with 32-way probes.
+__device__ __forceinline__ long long warp_lower_bound(const int* __restrict__ ptr, long long N,
+                                                      long long target) {
+    const int lane = threadIdx.x & 31;
+    long long lo = 0, hi = N;  // answer in [lo, hi]
+    while (hi - lo > 32) {
+        const long long step = (hi - lo + 31) / 32;
+        long long probe = lo + (long long)lane * step;
+        if (probe > hi) probe = hi;
+        const bool ge = __ldg(ptr + probe) >= target;
+        const unsigned m = __ballot_sync(0xffffffffu, ge);
+        const int f = m ? __ffs(m) - 1 : 32;  // first probe with ptr >= target
+        const long long nhi = f < 32 ? lo + (long long)f * step : hi;
+        const long long nlo = f > 0 ? lo + (long long)(f - 1) * step : lo;
+        lo = nlo;
+        hi = nhi < hi ? nhi : hi;
+    }
+    const long long probe = lo + lane;
+    const bool ge = probe <= hi && __ldg(ptr + probe) >= target;
+    const unsigned m = __ballot_sync(0xffffffffu, ge);
+    return m ? lo + (__ffs(m) - 1) : hi;
+}
+
+// Item range of this CTA: items whose first edge lies in its share of edges.
+__device__ __forceinline__ void cta_items(const int* __restrict__ ptr, long long n_items,
+                                          long long& i0, long long& i1) {
+    __shared__ long long sh_range[2];
+    if (threadIdx.x < 32) {
+        const long long total = ptr ? (long long)__ldg(ptr + n_items) : n_items;
+        const long long c = blockIdx.x, nc = gridDim.x;
+        const long long t0 = total * c / nc, t1 = total * (c + 1) / nc;
+        long long a, b;
+        if (ptr) {
+            a = c == 0 ? 0 : warp_lower_bound(ptr, n_items, t0);
+            b = c == nc - 1 ? n_items : warp_lower_bound(ptr, n_items, t1);
+        } else {
+            a = t0;
+            b = t1;
+        }
+        if (threadIdx.x == 0) {
+            sh_range[0] = a;
+            sh_range[1] = b;
+        }
+    }
+    __syncthreads();
+    i0 = sh_range[0];
+    i1 = sh_range[1];
+}
+
+__device__ __forceinline__ void cta_sync() {
+#if LANES == 32
+    __syncwarp();
+#else
+    __syncthreads();
+#endif
+}
+// Barrier that also agrees on a flag: true only if every thread's ok is true.
+__device__ __forceinline__ bool cta_all(bool ok) {
+#if LANES == 32
+    return __all_sync(0xffffffffu, ok);
+#else
+    return __syncthreads_and(ok) != 0;
+#endif
+}
+// After a timed-out wait: record the error, give every stage a short bounded
+// wait so no copy is left writing into this CTA's shared memory, then return.
+__device__ __noinline__ void fail_and_drain(int code, unsigned long long* bars, int n) {
+    if (threadIdx.x == 0) atomicExch(&cgtp_device_error, code);
+    for (int s = 0; s < n; ++s)
+        for (unsigned ph = 0; ph < 2; ++ph) {
+            const unsigned a = smem_u32(&bars[s]);
+            for (int it = 0; it < 4096; ++it) {
+                unsigned ok;
+                asm volatile(
+                    "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+                    : "=r"(ok) : "r"(a), "r"(ph) : "memory");
+                if (ok) break;
+                __nanosleep(1000);
+            }
+        }
+}
+
+// Stage layout: [W row][x or g row][y row][int header]; all offsets 16-aligned.
+constexpr unsigned SZ = sizeof(REAL);
+constexpr unsigned WB = (unsigned)(NP * MUL) * SZ;
+constexpr unsigned XB = (unsigned)(NX * MUL) * SZ;
+constexpr unsigned GB = (unsigned)(NO * MUL) * SZ;
+constexpr unsigned YB = (unsigned)NY * SZ;
+constexpr unsigned FWD_STAGE = WB + XB + YB;
+constexpr unsigned BWD_STAGE = WB + GB + YB + 16;
+
+// A 32-entry window of an int array, held one entry per lane of warp 0, with
+// the next window prefetched.  get(j) must be called by all lanes of warp 0
+// with non-decreasing j.
+struct IdxWindow {
+    const int* __restrict__ a;
+    long long end, base;
+    int cur, nxt;
+    __device__ __forceinline__ void init(const int* __restrict__ arr, long long b, long long e) {
+        a = arr;
+        end = e;
+        base = b;
+        const int lane = threadIdx.x & 31;
+        cur = base + lane < end ? __ldg(a + base + lane) : 0;
+        nxt = base + 32 + lane < end ? __ldg(a + base + 32 + lane) : 0;
+    }
+    __device__ __forceinline__ int get(long long j) {
+        while (j >= base + 32) {
+            base += 32;
+            cur = nxt;
+            const int lane = threadIdx.x & 31;
+            nxt = base + 32 + lane < end ? __ldg(a + base + 32 + lane) : 0;
+        }
+        return __shfl_sync(0xffffffffu, cur, (int)(j - base));
+    }
+};
+
+// ----------------------------------------------------------- staged forward
+
+template <bool CONV>
+__device__ __forceinline__ void fwd_staged(long long n_items, const int* __restrict__ rowptr,
+                                           const int* __restrict__ sender,
+                                           const REAL* __restrict__ x, const REAL* __restrict__ y,
+                                           const REAL* __restrict__ w, long long w_stride,
+                                           REAL* __restrict__ out, REAL scale, int accumulate) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ __align__(8) unsigned long long full[STAGES];
+    __shared__ __align__(16) VR Ts[NTP];
+    const int tid = threadIdx.x, ch = tid;
+    long long i0, i1;
+    cta_items(CONV ? rowptr : nullptr, n_items, i0, i1);
+    if (i0 >= i1) return;
+    const long long e_begin = CONV ? (long long)__ldg(rowptr + i0) : i0;
+    const long long e_end = CONV ? (long long)__ldg(rowptr + i1) : i1;
+    if (tid == 0) {
+        for (int s = 0; s < STAGES; ++s) mbar_init(&full[s], 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    IdxWindow win;
+    if (CONV && tid < 32) win.init(sender, e_begin, e_end);
+    auto issue = [&](long long j) {  // all of warp 0 calls; thread 0 issues
+        const long long src = CONV ? (long long)win.get(j) : j;
+        if (tid == 0) {
+            unsigned char* st = smem + (size_t)((j - e_begin) % STAGES) * FWD_STAGE;
+            unsigned long long* b = &full[(j - e_begin) % STAGES];
+            mbar_expect_tx(b, FWD_STAGE);
+            bulk_g2s(st, w + j * w_stride, WB, b);
+            bulk_g2s(st + WB, x + src * DIMX, XB, b);
+            bulk_g2s(st + WB + XB, y + j * NY, YB, b);
+        }
+    };
+    if (tid < 32)
+        for (long long j = e_begin; j < e_begin + STAGES && j < e_end; ++j) issue(j);
+    long long j = e_begin;
+    long long nend = CONV ? (long long)__ldg(rowptr + i0 + 1) : i0 + 1;
+    const VR sc = vsplat(scale);
+    for (long long item = i0; item < i1; ++item) {
+        const long long e1 = nend;
+        if (item + 1 < i1) nend = CONV ? (long long)__ldg(rowptr + item + 2) : item + 2;
+        VR acc[NO];
+#pragma unroll
+        for (int r = 0; r < NO; ++r) acc[r] = vzero();
+        for (; j < e1; ++j) {
+            const long long k = j - e_begin;
+            const unsigned char* st = smem + (size_t)(k % STAGES) * FWD_STAGE;
+            const bool ok = mbar_wait(&full[k % STAGES], (unsigned)((k / STAGES) & 1));
+            build_T(Ts, reinterpret_cast<const REAL*>(st + WB + XB), tid);
+            if (!cta_all(ok)) {
+                fail_and_drain(1, full, STAGES);
+                return;
+            }
+            const REAL* xs = reinterpret_cast<const REAL*>(st + WB);
+            const REAL* ws = reinterpret_cast<const REAL*>(st);
+            gen_fwd(acc, Ts, [&](int r) { return lds_v(xs + r * MUL, ch); },
+                    [&](int p) { return lds_v(ws + p * MUL, ch); });
+            cta_sync();
+            if (tid < 32 && j + STAGES < e_end) issue(j + STAGES);
+        }
+        REAL* orow = out + item * DIMO;
+#pragma unroll
+        for (int r = 0; r < NO; ++r) {
+            VR v = vmul(acc[r], sc);
+            if (accumulate) v = vadd(v, ldv_plain(orow + r * MUL, ch));
+            stv(orow + r * MUL, ch, v);
+        }
+    }
+}
+
+extern "C" __global__ void __launch_bounds__(LANES, MINB_FWD)
+cgtp_fwd_conv_tma(long long n_items, const int* __restrict__ rowptr,
+                  const int* __restrict__ sender, const REAL* __restrict__ x,
+                  const REAL* __restrict__ y, const REAL* __restrict__ w, long long w_stride,
+                  REAL* __restrict__ out, REAL scale, int accumulate) {
+    fwd_staged<true>(n_items, rowptr, sender, x, y, w, w_stride, out, scale, accumulate);
+}
+
+extern "C" __global__ void __launch_bounds__(LANES, MINB_FWD)
+cgtp_fwd_single_tma(long long n_items, const REAL* __restrict__ x, const REAL* __restrict__ y,
+                    const REAL* __restrict__ w, long long w_stride, REAL* __restrict__ out,
+                    REAL scale, int accumulate) {
+    fwd_staged<false>(n_items, nullptr, nullptr, x, y, w, w_stride, out, scale, accumulate);
+}
+
+// ---------------------------------------------------------- staged backward
+//
+// Items are senders (or samples).  Stages carry w[e], g[n] and y[e] of the
+// item's edges (e = s_perm[j], n = s_recv[j]); the item's own x row comes
+// through a second, double-buffered TMA slot.
+
+template <bool CONV, bool GY>
+__device__ __forceinline__ void bwd_staged(long long n_items, const int* __restrict__ s_rowptr,
+                                           const int* __restrict__ s_perm,
+                                           const int* __restrict__ s_recv,
+                                           const REAL* __restrict__ x, const REAL* __restrict__ y,
+                                           const REAL* __restrict__ w, long long w_stride,
+                                           const REAL* __restrict__ g, REAL scale,
+                                           REAL* __restrict__ gx, REAL* __restrict__ gy,
+                                           REAL* __restrict__ gw, int mgx, int mgy, int mgw) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ __align__(8) unsigned long long full[STAGES];
+    __shared__ __align__(8) unsigned long long xfull[2];
+    __shared__ __align__(16) VR Ts[NTP];
+#if LANES > 32
+    __shared__ REAL Gy[LANES / 32][NYP];
+#endif
+    const int tid = threadIdx.x, ch = tid, lane = tid & 31;
+    unsigned char* xbuf = smem + (size_t)STAGES * BWD_STAGE;  // 2 x XB
+    long long i0, i1;
+    cta_items(CONV ? s_rowptr : nullptr, n_items, i0, i1);
+    if (i0 >= i1) return;
+    const long long j_begin = CONV ? (long long)__ldg(s_rowptr + i0) : i0;
+    const long long j_end = CONV ? (long long)__ldg(s_rowptr + i1) : i1;
+    if (tid == 0) {
+        for (int s = 0; s < STAGES; ++s) mbar_init(&full[s], 1);
+        mbar_init(&xfull[0], 1);
+        mbar_init(&xfull[1], 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    IdxWindow we, wn;
+    if (CONV && tid < 32) {
+        we.init(s_perm, j_begin, j_end);
+        wn.init(s_recv, j_begin, j_end);
+    }
+    auto issue = [&](long long j) {  // all of warp 0 calls; thread 0 issues
+        const long long e = CONV ? (long long)we.get(j) : j;
+        const long long n = CONV ? (long long)wn.get(j) : j;
+        if (tid == 0) {
+            unsigned char* st = smem + (size_t)((j - j_begin) % STAGES) * BWD_STAGE;
+            unsigned long long* b = &full[(j - j_begin) % STAGES];
+            int* hdr = reinterpret_cast<int*>(st + WB + GB + YB);
+            hdr[0] = (int)e;
+            mbar_expect_tx(b, WB + GB + YB);
+            bulk_g2s(st, w + e * w_stride, WB, b);
+            bulk_g2s(st + WB, g + n * DIMO, GB, b);
+            bulk_g2s(st + WB + GB, y + e * NY, YB, b);
+        }
+    };
+    auto issue_x = [&](long long item, int slot) {
+        if (tid == 0) {
+            mbar_expect_tx(&xfull[slot], XB);
+            bulk_g2s(xbuf + (size_t)slot * XB, x + item * DIMX, XB, &xfull[slot]);
+        }
+    };
+    if (tid < 32)
+        for (long long j = j_begin; j < j_begin + STAGES && j < j_end; ++j) issue(j);
+    issue_x(i0, 0);
+    long long j = j_begin;
+    long long nend = CONV ? (long long)__ldg(s_rowptr + i0 + 1) : i0 + 1;
+    const VR sc = vsplat(scale);
+    for (long long item = i0; item < i1; ++item) {
+        const long long kk = item - i0;
+        const long long e1 = nend;
+        if (item + 1 < i1) nend = CONV ? (long long)__ldg(s_rowptr + item + 2) : item + 2;
+        if (!cta_all(mbar_wait(&xfull[kk & 1], (unsigned)((kk >> 1) & 1)))) {
+            fail_and_drain(2, full, STAGES);
+            fail_and_drain(2, xfull, 2);
+            return;
+        }
+        VR xr[NX], gxa[NX];
+        const REAL* xs = reinterpret_cast<const REAL*>(xbuf + (size_t)(kk & 1) * XB);
+#pragma unroll
+        for (int r = 0; r < NX; ++r) {
+            xr[r] = lds_v(xs + r * MUL, ch);
+            gxa[r] = vzero();
+        }
+        cta_sync();  // every thread holds its x before the slot is refilled
+        if (item + 1 < i1) issue_x(item + 1, (int)((kk + 1) & 1));
+        for (; j < e1; ++j) {
+            const long long k = j - j_begin;
+            const unsigned char* st = smem + (size_t)(k % STAGES) * BWD_STAGE;
+            const bool ok = mbar_wait(&full[k % STAGES], (unsigned)((k / STAGES) & 1));
+            const long long e = *reinterpret_cast<const int*>(st + WB + GB + YB);
+            build_T(Ts, reinterpret_cast<const REAL*>(st + WB + GB), tid);
+            if (!cta_all(ok)) {
+                fail_and_drain(3, full, STAGES);
+                fail_and_drain(3, xfull, 2);
+                return;
+            }
+            const REAL* gs = reinterpret_cast<const REAL*>(st + WB);
+            const REAL* ws = reinterpret_cast<const REAL*>(st);
+            REAL gyl[NYP];
+#pragma unroll
+            for (int i = 0; i < NYP; ++i) gyl[i] = (REAL)0;
+            REAL* gwrow = gw ? gw + e * WDIM : nullptr;
+            gen_bwd<GY>(gxa, gyl, Ts, [&](int r) { return xr[r]; },
+                        [&](int r) { return lds_v(gs + r * MUL, ch); },
+                        [&](int p) { return lds_v(ws + p * MUL, ch); }, gwrow, ch, sc, mgx != 0,
+                        mgw);
+            if (GY && mgy) {
+                int base = 0;
+                bool owner = true;
+                seg_reduce<16, NYP>(gyl, lane, 0xffffffffu, base, owner);
+#if LANES > 32
+                if (owner)
+                    for (int i = 0; i < NRED; ++i) Gy[tid / 32][base + i] = gyl[i];
+                __syncthreads();
+                for (int q = tid; q < NY; q += LANES) {
+                    REAL t = (REAL)0;
+                    for (int wq = 0; wq < LANES / 32; ++wq) t += Gy[wq][q];
+                    t *= scale;
+                    if (mgy == 2) t += gy[e * NY + q];
+                    gy[e * NY + q] = t;
+                }
+#else
+                if (owner) {
+#pragma unroll
+                    for (int i = 0; i < NRED; ++i) {
+                        const int q = base + i;
+                        if (q < NY) {
+                            REAL t = gyl[i] * scale;
+                            if (mgy == 2) t += gy[e * NY + q];
+                            gy[e * NY + q] = t;
+                        }
+                    }
+                }
+#endif
+            }
+            cta_sync();
+            if (tid < 32 && j + STAGES < j_end) issue(j + STAGES);
+        }
+        if (mgx) {
+            REAL* orow = gx + item * DIMX;
+#pragma unroll
+            for (int r = 0; r < NX; ++r) {
+                VR v = vmul(gxa[r], sc);
+                if (mgx == 2) v = vadd(v, ldv_plain(orow + r * MUL, ch));
+                stv(orow + r * MUL, ch, v);
+            }
+        }
+    }
+}
+
+#define CGTP_BWD_TMA_ENTRY(NAME, CONV, GY)                                                      \
+    extern "C" __global__ void __launch_bounds__(LANES, MINB_BWD) NAME(                       \
+        long long n_items, const int* __restrict__ s_rowptr, const int* __restrict__ s_perm,  \
+        const int* __restrict__ s_recv, const REAL* __restrict__ x,                           \
+        const REAL* __restrict__ y, const REAL* __restrict__ w, long long w_stride,           \
+        const REAL* __restrict__ g, REAL scale, REAL* __restrict__ gx, REAL* __restrict__ gy, \
+        REAL* __restrict__ gw, int mgx, int mgy, int mgw) {                                   \
+        bwd_staged<CONV, GY>(n_items, s_rowptr, s_perm, s_recv, x, y, w, w_stride, g, scale,  \
+                             gx, gy, gw, mgx, mgy, mgw);                                      \
+    }
+
+CGTP_BWD_TMA_ENTRY(cgtp_bwd_conv_tma, true, true)
+CGTP_BWD_TMA_ENTRY(cgtp_bwd_conv_nogy_tma, true, false)
+CGTP_BWD_TMA_ENTRY(cgtp_bwd_single_tma, false, true)
+CGTP_BWD_TMA_ENTRY(cgtp_bwd_single_nogy_tma, false, false)
+
+#endif  // STAGED

@@ -112,6 +112,11 @@ cgtp_status cgtp_plan_compile(cgtp_plan plan, char* log, size_t cap);
  * contraction streams).  *needed = bytes including the terminator. */
 cgtp_status cgtp_plan_source(cgtp_plan plan, char* buf, size_t cap, size_t* needed);
 
+/* Device-side error flag of the plan's kernels: CGTP_E_DEVICE (and *code != 0)
+ * if a staged kernel gave up on a bounded wait for one of its bulk copies since
+ * the last call; the flag is then cleared.  Synchronises with the device. */
+cgtp_status cgtp_plan_device_status(cgtp_plan plan, int* code);
+
 /* ------------------------------------------- standalone tensor product -- */
 
 /* out[b] = sum_paths w[b,p,u] sum C x[b,l1,m1,u] y[b,l2,m2]   (b < B)

@@ -191,3 +191,48 @@ def test_tfn_force_chain_small():
     ref = tfn_chain_oracle(prob, gr, cfg["x"], cfg["vec"], cfg["w"], cfg["c"], cfg["gF"])
     for k in ("y", "out", "gx", "gy", "gw", "dEdr", "F", "ggy", "d_x", "d_w"):
         assert_close(host(gpu[k]), ref[k], np.float32, k)
+
+
+def _offset_view(a, dtype):
+    """Device copy of a whose data pointer is 8 but not 16 bytes aligned, so
+    the library takes its direct-load kernels instead of the staged ones."""
+    t = torch.from_numpy(np.ascontiguousarray(a)).to(dtype)
+    k = 8 // t.element_size()
+    buf = torch.zeros(t.numel() + k, dtype=dtype, device="cuda")
+    v = buf[k:].view(t.shape)
+    v.copy_(t.cuda())
+    assert v.data_ptr() % 16 == 8
+    return v
+
+
+@pytest.mark.parametrize("case", [CASES[1], CASES[3], CASES[6]],
+                         ids=lambda c: f"{c[0][:12]}-{np.dtype(c[3]).name}")
+def test_staged_and_direct_paths_agree(case):
+    """The staged (TMA) and direct kernels give the oracle's result; the
+    direct ones are selected by 16-byte-misaligned inputs."""
+    need_gpu()
+    cg = _cg()
+    a, b, c, dt = case
+    tdt = torch.float64 if dt == np.float64 else torch.float32
+    prob = O.make_problem(a, b, c)
+    plan = cg.Plan(a, b, c, dtype=tdt)
+    rng = np.random.default_rng(11)
+    gr = _graph(rng, 70, max_deg=12)
+    G = cg.Graph.from_numpy(gr)
+    x = rng.standard_normal((gr.N, prob.dim1)).astype(dt)
+    y = rng.standard_normal((gr.E, prob.dim2)).astype(dt)
+    w = rng.standard_normal((gr.E, prob.wdim)).astype(dt)
+    g = rng.standard_normal((gr.N, prob.dimo)).astype(dt)
+    ref = O.conv_forward(prob, gr.rowptr, gr.sender, x, y, w, 0.5)
+    rx, ry, rw = O.conv_backward(prob, gr.rowptr, gr.sender, x, y, w, 0.5, g)
+    for mk in (dev, lambda arr: _offset_view(arr, tdt)):
+        xs, ys, ws, gs = mk(x), mk(y), mk(w), mk(g)
+        out = plan.conv_forward(G, xs, ys, ws, 0.5)
+        assert_close(host(out), ref, dt, "forward")
+        gx, gy, gw = plan.conv_backward(G, xs, ys, ws, 0.5, gs)
+        assert_close(host(gx), rx, dt, "grad_x")
+        assert_close(host(gy), ry, dt, "grad_y")
+        assert_close(host(gw), rw, dt, "grad_w")
+    code = __import__("ctypes").c_int(-1)
+    assert cg.lib().cgtp_plan_device_status(plan._h, __import__("ctypes").byref(code)) == 0
+    assert code.value == 0
