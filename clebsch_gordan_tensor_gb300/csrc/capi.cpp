@@ -56,7 +56,8 @@ static cgtp_status check_rows(const Plan& p, std::initializer_list<const void*> 
 }
 
 static cgtp_status launch_tp(Plan& p, const char* name, int64_t n_items, void** args,
-                             cudaStream_t s, bool staged = false, size_t smem = 0) {
+                             cudaStream_t s, bool staged = false, size_t smem = 0,
+                             int threads = 0) {
     if (n_items <= 0) return CGTP_OK;
     std::shared_ptr<Module> m;
     std::string err;
@@ -94,7 +95,7 @@ static cgtp_status launch_tp(Plan& p, const char* name, int64_t n_items, void** 
             auto it = m->ctas_per_sm.find(key);
             if (it == m->ctas_per_sm.end()) {
                 int n = 0;
-                if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, (const void*)k, p.lanes,
+                if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, (const void*)k, threads,
                                                                   smem) != cudaSuccess || n < 1) {
                     cudaGetLastError();
                     n = std::max(1, (int)((220 * 1024) / (smem + 4096)));
@@ -108,7 +109,7 @@ static cgtp_status launch_tp(Plan& p, const char* name, int64_t n_items, void** 
         if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
             return cuda_fail(e, "cudaDeviceGetAttribute");
         const int64_t grid = std::min<int64_t>(n_items, (int64_t)sms * per_sm);
-        e = cudaLaunchKernel((const void*)k, dim3((unsigned)grid), dim3(p.lanes), args, smem, s);
+        e = cudaLaunchKernel((const void*)k, dim3((unsigned)grid), dim3(threads), args, smem, s);
     }
     if (e != cudaSuccess) return cuda_fail(e, name);
     count_launch();
@@ -134,11 +135,11 @@ static cgtp_status fwd_launch(Plan& p, bool conv, int64_t n_items, const int32_t
     if (conv) {
         void* args[] = {&n, &rowptr, &sender, &a, &b, &c, &ws, &out, sp, &accumulate};
         return launch_tp(p, staged ? "cgtp_fwd_conv_tma" : "cgtp_fwd_conv", n_items, args, s,
-                         staged, p.fwd_smem);
+                         staged, p.fwd_smem, (int)p.fwd_groups.size() * p.lanes);
     }
     void* args[] = {&n, &a, &b, &c, &ws, &out, sp, &accumulate};
     return launch_tp(p, staged ? "cgtp_fwd_single_tma" : "cgtp_fwd_single", n_items, args, s,
-                     staged, p.fwd_smem);
+                     staged, p.fwd_smem, (int)p.fwd_groups.size() * p.lanes);
 }
 
 // One backward-shaped launch over items (senders or samples).
@@ -158,7 +159,8 @@ static cgtp_status bwd_launch(Plan& p, bool conv, int64_t n_items, const int32_t
     std::string name = conv ? (mgy ? "cgtp_bwd_conv" : "cgtp_bwd_conv_nogy")
                             : (mgy ? "cgtp_bwd_single" : "cgtp_bwd_single_nogy");
     if (staged) name += "_tma";
-    return launch_tp(p, name.c_str(), n_items, args, s, staged, p.bwd_smem);
+    return launch_tp(p, name.c_str(), n_items, args, s, staged, p.bwd_smem,
+                     (int)p.bwd_groups.size() * p.lanes);
 }
 
 static size_t esize(const Plan& p) { return p.dtype == CGTP_F64 ? 8 : 4; }

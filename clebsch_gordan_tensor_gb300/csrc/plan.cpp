@@ -331,10 +331,39 @@ cgtp_status build_plan(Plan& p, const char* s1, const char* s2, const char* so,
                  YB = (size_t)p.ny * es;
     const bool rows16 = WB % 16 == 0 && XB % 16 == 0 && GB % 16 == 0 && YB % 16 == 0;
     if (p.nch == p.lanes && p.lanes % 32 == 0 && rows16 && !p.paths.empty()) {
-        const size_t fst = WB + XB + YB, bst = WB + GB + YB + 16;
-        const size_t stat = (size_t)std::max(2, nt + (nt & 1)) * vr + 1024;
+        // per-path costs in FMA-pipe cycles per channel group
+        std::vector<double> cf(p.paths.size(), 0.0), cb(p.paths.size(), 0.0);
+        std::vector<int> nTp(p.paths.size(), 0), nnzp(p.paths.size(), 0);
+        for (auto& t : p.T) {
+            nTp[t.path] += 1;
+            nnzp[t.path] += (int)t.terms.size();
+        }
+        for (size_t q = 0; q < p.paths.size(); ++q) {
+            const int d1 = 2 * p.paths[q].l1 + 1, d3 = 2 * p.paths[q].l3 + 1;
+            cf[q] = nTp[q] + std::min(d1, d3);
+            cb[q] = 2.0 * (nTp[q] + 3 * d1) + 2.0 * nTp[q] + nnzp[q];
+        }
+        const int G = std::max(1, std::min(4, 128 / p.lanes));
+        auto lpt = [&](const std::vector<double>& c) {
+            std::vector<int> order(c.size());
+            for (size_t i = 0; i < order.size(); ++i) order[i] = (int)i;
+            std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return c[a] > c[b]; });
+            std::vector<std::vector<int>> grp(G);
+            std::vector<double> load(G, 0.0);
+            for (int q : order) {
+                int j = (int)(std::min_element(load.begin(), load.end()) - load.begin());
+                grp[j].push_back(q);
+                load[j] += c[q];
+            }
+            for (auto& v : grp) std::sort(v.begin(), v.end());
+            return grp;
+        };
+        p.fwd_groups = lpt(cf);
+        p.bwd_groups = lpt(cb);
+        const size_t stat = (size_t)std::max(2, nt + (nt & 1)) * vr + 2048;
         for (int st = 3; st >= 2; --st) {
-            const size_t f = st * fst, b = st * bst + 2 * XB;
+            const size_t f = st * (WB + XB + YB) + GB;           // + output combine buffer
+            const size_t b = st * (WB + GB + YB + 16) + 2 * XB + XB;  // + x ring + gx buffer
             if (f + stat <= 200 * 1024 && b + stat <= 200 * 1024) {
                 p.staged = true;
                 p.stages = st;
@@ -382,6 +411,186 @@ struct TLoader {
     }
 };
 
+
+// Per-group streams of the staged kernels.  Group g of the forward owns the
+// paths fwd_groups[g]; its accumulators cover only the output rows those paths
+// touch and its x registers only the rows they read.  The backward groups keep
+// x rows and partial grad_x for their paths' input rows.
+void Plan::gen_groups(std::ostringstream& g, const std::vector<int>& k0, bool f64) const {
+    const int ntp = std::max(2, (int)T.size() + ((int)T.size() & 1));
+    auto emit_tloader = [&](TLoader& L) { std::fill(L.loaded.begin(), L.loaded.end(), false); };
+    // ---------------------------------------------------------------- forward
+    g << "template <int GRP> struct FwdG;\n";
+    for (size_t gi = 0; gi < fwd_groups.size(); ++gi) {
+        const auto& P_ = fwd_groups[gi];
+        std::vector<int> rows, xrows;
+        for (int q : P_) {
+            const Path& P = paths[q];
+            for (int c = 0; c < 2 * P.l3 + 1; ++c) rows.push_back(P.r3 + c);
+            for (int a = 0; a < 2 * P.l1 + 1; ++a) xrows.push_back(P.r1 + a);
+        }
+        std::sort(rows.begin(), rows.end());
+        rows.erase(std::unique(rows.begin(), rows.end()), rows.end());
+        std::sort(xrows.begin(), xrows.end());
+        xrows.erase(std::unique(xrows.begin(), xrows.end()), xrows.end());
+        std::map<int, int> ri, xi;
+        for (size_t i = 0; i < rows.size(); ++i) ri[rows[i]] = (int)i;
+        for (size_t i = 0; i < xrows.size(); ++i) xi[xrows[i]] = (int)i;
+        g << "template <> struct FwdG<" << gi << "> {\n  static constexpr int NR = "
+          << std::max<size_t>(1, rows.size()) << ", NXR = " << std::max<size_t>(1, xrows.size())
+          << ";\n";
+        g << "  __device__ static __forceinline__ void loadx(VR (&xr)[NXR], const REAL* xs, int ch) {\n";
+        for (size_t i = 0; i < xrows.size(); ++i)
+            g << "    xr[" << i << "] = lds_v(xs + " << xrows[i] << " * MUL, ch);\n";
+        g << "  }\n";
+        g << "  template <class FW>\n  __device__ static __forceinline__ void edge(VR (&acc)[NR], "
+             "const VR* __restrict__ Ts, const VR (&xr)[NXR], FW&& W) {\n";
+        if (cpt == 2) g << "    const ulonglong2* __restrict__ Tq = reinterpret_cast<const ulonglong2*>(Ts);\n";
+        TLoader L{cpt, std::vector<bool>(ntp / 2 + 1, false), &g};
+        for (int q : P_) {
+            const Path& P = paths[q];
+            const int d1 = 2 * P.l1 + 1, d3 = 2 * P.l3 + 1;
+            g << "    { // path " << q << ": " << P.l1 << " x " << P.l2 << " -> " << P.l3 << "\n";
+            g << "    const VR w = W(" << q << ");\n";
+            emit_tloader(L);
+            if (d1 <= d3) {
+                for (int a = 0; a < d1; ++a)
+                    g << "    const VR z" << a << " = vmul(w, xr[" << xi[P.r1 + a] << "]);\n";
+                for (int k = k0[q]; k < k0[q + 1]; ++k) {
+                    const std::string t = L.get(k);
+                    const int o = ri[P.r3 + T[k].m3];
+                    g << "    acc[" << o << "] = vfma(" << t << ", z" << T[k].m1 << ", acc[" << o << "]);\n";
+                }
+            } else {
+                std::vector<bool> started(d3, false);
+                for (int k = k0[q]; k < k0[q + 1]; ++k) {
+                    const std::string t = L.get(k);
+                    const int c = T[k].m3;
+                    const std::string xv = "xr[" + std::to_string(xi[P.r1 + T[k].m1]) + "]";
+                    if (!started[c]) {
+                        g << "    VR t" << c << " = vmul(" << t << ", " << xv << ");\n";
+                        started[c] = true;
+                    } else {
+                        g << "    t" << c << " = vfma(" << t << ", " << xv << ", t" << c << ");\n";
+                    }
+                }
+                for (int c = 0; c < d3; ++c)
+                    if (started[c])
+                        g << "    acc[" << ri[P.r3 + c] << "] = vfma(w, t" << c << ", acc["
+                          << ri[P.r3 + c] << "]);\n";
+            }
+            g << "    }\n";
+        }
+        g << "  }\n";
+        // combine: group 0 writes every row (zeros where it has none), others add
+        g << "  __device__ static __forceinline__ void first(REAL* buf, const VR (&acc)[NR], int ch) {\n";
+        for (int r = 0; r < no; ++r) {
+            if (ri.count(r))
+                g << "    stv(buf + " << r << " * MUL, ch, acc[" << ri[r] << "]);\n";
+            else
+                g << "    stv(buf + " << r << " * MUL, ch, vzero());\n";
+        }
+        g << "  }\n  __device__ static __forceinline__ void add(REAL* buf, const VR (&acc)[NR], int ch) {\n";
+        for (size_t i = 0; i < rows.size(); ++i)
+            g << "    stv(buf + " << rows[i] << " * MUL, ch, vadd(lds_v(buf + " << rows[i]
+              << " * MUL, ch), acc[" << i << "]));\n";
+        g << "  }\n};\n\n";
+    }
+    // --------------------------------------------------------------- backward
+    g << "template <int GRP> struct BwdG;\n";
+    for (size_t gi = 0; gi < bwd_groups.size(); ++gi) {
+        const auto& P_ = bwd_groups[gi];
+        std::vector<int> xrows;
+        for (int q : P_)
+            for (int a = 0; a < 2 * paths[q].l1 + 1; ++a) xrows.push_back(paths[q].r1 + a);
+        std::sort(xrows.begin(), xrows.end());
+        xrows.erase(std::unique(xrows.begin(), xrows.end()), xrows.end());
+        std::map<int, int> xi;
+        for (size_t i = 0; i < xrows.size(); ++i) xi[xrows[i]] = (int)i;
+        g << "template <> struct BwdG<" << gi << "> {\n  static constexpr int NXR = "
+          << std::max<size_t>(1, xrows.size()) << ";\n";
+        g << "  __device__ static __forceinline__ void loadx(VR (&xr)[NXR], const REAL* xs, int ch) {\n";
+        for (size_t i = 0; i < xrows.size(); ++i)
+            g << "    xr[" << i << "] = lds_v(xs + " << xrows[i] << " * MUL, ch);\n";
+        g << "  }\n";
+        g << "  template <bool GY, class FG, class FW>\n  __device__ static __forceinline__ void edge("
+             "VR (&gxa)[NXR], REAL (&gyl)[NYP], const VR* __restrict__ Ts, const VR (&xr)[NXR],\n"
+             "      FG&& G, FW&& W, REAL* __restrict__ gwrow, int ch, VR sc, bool dogx, int mgw) {\n";
+        if (cpt == 2) g << "    const ulonglong2* __restrict__ Tq = reinterpret_cast<const ulonglong2*>(Ts);\n";
+        TLoader L{cpt, std::vector<bool>(ntp / 2 + 1, false), &g};
+        for (int q : P_) {
+            const Path& P = paths[q];
+            const int d1 = 2 * P.l1 + 1, d3 = 2 * P.l3 + 1;
+            g << "    { // path " << q << ": " << P.l1 << " x " << P.l2 << " -> " << P.l3 << "\n";
+            g << "    const VR w = W(" << q << ");\n";
+            emit_tloader(L);
+            // h[m1] = sum_m3 T[m1,m3] g[m3]; entries ordered m3-major to interleave chains
+            std::vector<int> ks;
+            for (int k = k0[q]; k < k0[q + 1]; ++k) ks.push_back(k);
+            std::stable_sort(ks.begin(), ks.end(), [&](int a, int b) { return T[a].m3 < T[b].m3; });
+            for (int k = k0[q]; k < k0[q + 1]; ++k) L.get(k);  // load all T of the path first
+            std::vector<bool> hs(d1, false);
+            for (int k : ks) {
+                const std::string t = L.get(k);
+                const int a = T[k].m1;
+                const std::string gv = "G(" + std::to_string(P.r3 + T[k].m3) + ")";
+                if (!hs[a]) {
+                    g << "    VR h" << a << " = vmul(" << t << ", " << gv << ");\n";
+                    hs[a] = true;
+                } else {
+                    g << "    h" << a << " = vfma(" << t << ", " << gv << ", h" << a << ");\n";
+                }
+            }
+            g << "    if (dogx) {\n";
+            for (int a = 0; a < d1; ++a)
+                if (hs[a])
+                    g << "      gxa[" << xi[P.r1 + a] << "] = vfma(w, h" << a << ", gxa["
+                      << xi[P.r1 + a] << "]);\n";
+            g << "    }\n    if (mgw) {\n      VR s = vzero();\n";
+            for (int a = 0; a < d1; ++a)
+                if (hs[a]) g << "      s = vfma(xr[" << xi[P.r1 + a] << "], h" << a << ", s);\n";
+            g << "      s = vmul(s, sc);\n      REAL* gp = gwrow + " << (long long)q * mul << ";\n"
+              << "      if (mgw == 2) s = vadd(s, ldv_plain(gp, ch));\n"
+              << "      stv(gp, ch, s);\n    }\n";
+            g << "    if (GY) {\n";
+            const bool zx = d1 <= d3;
+            if (zx) {
+                for (int a = 0; a < d1; ++a)
+                    g << "      const VR z" << a << " = vmul(w, xr[" << xi[P.r1 + a] << "]);\n";
+            } else {
+                for (int c = 0; c < d3; ++c)
+                    g << "      const VR z" << c << " = vmul(w, G(" << P.r3 + c << "));\n";
+            }
+            for (int k = k0[q]; k < k0[q + 1]; ++k) {
+                const TEntry& t = T[k];
+                const std::string lhs =
+                    zx ? "z" + std::to_string(t.m1) : "xr[" + std::to_string(xi[P.r1 + t.m1]) + "]";
+                const std::string rhs =
+                    zx ? "G(" + std::to_string(P.r3 + t.m3) + ")" : "z" + std::to_string(t.m3);
+                g << "      { const REAL d = vdot(" << lhs << ", " << rhs << ");\n";
+                for (auto& term : t.terms)
+                    g << "        gyl[" << term.first << "] = fma(" << lit(term.second, f64)
+                      << ", d, gyl[" << term.first << "]);\n";
+                g << "      }\n";
+            }
+            g << "    }\n    }\n";
+        }
+        g << "  }\n";
+        g << "  __device__ static __forceinline__ void first(REAL* buf, const VR (&gxa)[NXR], int ch) {\n";
+        for (int r = 0; r < nx; ++r) {
+            if (xi.count(r))
+                g << "    stv(buf + " << r << " * MUL, ch, gxa[" << xi[r] << "]);\n";
+            else
+                g << "    stv(buf + " << r << " * MUL, ch, vzero());\n";
+        }
+        g << "  }\n  __device__ static __forceinline__ void add(REAL* buf, const VR (&gxa)[NXR], int ch) {\n";
+        for (size_t i = 0; i < xrows.size(); ++i)
+            g << "    stv(buf + " << xrows[i] << " * MUL, ch, vadd(lds_v(buf + " << xrows[i]
+              << " * MUL, ch), gxa[" << i << "]));\n";
+        g << "  }\n};\n\n";
+    }
+}
+
 std::string Plan::kernel_source() const {
     const bool f64 = dtype == CGTP_F64;
     const int nt = (int)T.size();
@@ -399,7 +608,8 @@ std::string Plan::kernel_source() const {
        << "\n#define NTP " << ntp << "\n#define MAXTERMS " << maxterms << "\n#define YPF "
        << (ny + lanes - 1) / lanes << "\n";
     os << "#define STAGED " << (staged ? 1 : 0) << "\n#define STAGES " << stages
-       << "\n#define MINB_FWD 1\n#define MINB_BWD 1\n";
+       << "\n#define GF " << std::max<size_t>(1, fwd_groups.size()) << "\n#define GB "
+       << std::max<size_t>(1, bwd_groups.size()) << "\n";
     // T tables
     os << "__device__ const short T_IDX[" << std::max(1, nt * maxterms) << "] = {";
     for (int k = 0; k < nt; ++k)
@@ -538,6 +748,7 @@ std::string Plan::kernel_source() const {
     }
     g << "}\n\n";
 
+    if (staged) gen_groups(g, k0, f64);
     return os.str() + head + g.str() + tail;
 }
 

@@ -11,6 +11,7 @@
 #include <map>
 #include <memory>
 #include <mutex>
+#include <sstream>
 #include <string>
 #include <vector>
 
@@ -64,11 +65,15 @@ struct Plan {
     bool staged = false;
     int stages = 3;
     size_t fwd_smem = 0, bwd_smem = 0;  // dynamic shared memory per CTA
+    // warp groups of the staged kernels: each group of `lanes` threads runs the
+    // generated stream of a subset of paths (longest-processing-time split)
+    std::vector<std::vector<int>> fwd_groups, bwd_groups;
 
     std::mutex mu;
     std::map<std::string, std::shared_ptr<Module>> modules;
 
     std::string kernel_source() const;  // full NVRTC source of the TP module
+    void gen_groups(std::ostringstream& g, const std::vector<int>& k0, bool f64) const;
 };
 
 // plan.cpp

@@ -494,22 +494,10 @@ __device__ __forceinline__ void cta_items(const int* __restrict__ ptr, long long
     i1 = sh_range[1];
 }
 
-__device__ __forceinline__ void cta_sync() {
-#if LANES == 32
-    __syncwarp();
-#else
-    __syncthreads();
-#endif
-}
+__device__ __forceinline__ void cta_sync() { __syncthreads(); }
 // Barrier that also agrees on a flag: true only if every thread's ok is true.
-__device__ __forceinline__ bool cta_all(bool ok) {
-#if LANES == 32
-    return __all_sync(0xffffffffu, ok);
-#else
-    return __syncthreads_and(ok) != 0;
-#endif
-}
-// After a timed-out wait: record the error, give every stage a short bounded
+__device__ __forceinline__ bool cta_all(bool ok) { return __syncthreads_and(ok) != 0; }
+// After a timed-out wait: record the error, give every barrier a short bounded
 // wait so no copy is left writing into this CTA's shared memory, then return.
 __device__ __noinline__ void fail_and_drain(int code, unsigned long long* bars, int n) {
     if (threadIdx.x == 0) atomicExch(&cgtp_device_error, code);
@@ -527,14 +515,38 @@ __device__ __noinline__ void fail_and_drain(int code, unsigned long long* bars, 
         }
 }
 
+// T entries of one edge, computed by all NTHR threads of the CTA.
+template <int NTHR>
+__device__ __forceinline__ void build_T_cta(VR* __restrict__ Ts, const REAL* __restrict__ Ys) {
+    constexpr int ROUNDS = (NT + NTHR - 1) / NTHR;
+    REAL t[ROUNDS];
+#pragma unroll
+    for (int r = 0; r < ROUNDS; ++r) {
+        const int k = threadIdx.x + r * NTHR;
+        t[r] = (REAL)0;
+        if (k < NT) {
+#pragma unroll
+            for (int q = 0; q < MAXTERMS; ++q)
+                t[r] = fma(__ldg(&T_CO[k * MAXTERMS + q]), Ys[__ldg(&T_IDX[k * MAXTERMS + q])], t[r]);
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < ROUNDS; ++r) {
+        const int k = threadIdx.x + r * NTHR;
+        if (k < NT) Ts[k] = vsplat(t[r]);
+    }
+}
+
 // Stage layout: [W row][x or g row][y row][int header]; all offsets 16-aligned.
 constexpr unsigned SZ = sizeof(REAL);
 constexpr unsigned WB = (unsigned)(NP * MUL) * SZ;
 constexpr unsigned XB = (unsigned)(NX * MUL) * SZ;
-constexpr unsigned GB = (unsigned)(NO * MUL) * SZ;
+constexpr unsigned GB_ = (unsigned)(NO * MUL) * SZ;
 constexpr unsigned YB = (unsigned)NY * SZ;
 constexpr unsigned FWD_STAGE = WB + XB + YB;
-constexpr unsigned BWD_STAGE = WB + GB + YB + 16;
+constexpr unsigned BWD_STAGE = WB + GB_ + YB + 16;
+constexpr int NTF = GF * LANES;  // threads of a forward CTA
+constexpr int NTB = GB * LANES;  // threads of a backward CTA
 
 // A 32-entry window of an int array, held one entry per lane of warp 0, with
 // the next window prefetched.  get(j) must be called by all lanes of warp 0
@@ -564,185 +576,238 @@ struct IdxWindow {
 
 // ----------------------------------------------------------- staged forward
 
+struct FwdArgs {
+    long long n_items;
+    const int* __restrict__ rowptr;
+    const int* __restrict__ sender;
+    const REAL* __restrict__ x;
+    const REAL* __restrict__ y;
+    const REAL* __restrict__ w;
+    long long w_stride;
+    REAL* __restrict__ out;
+    REAL scale;
+    int accumulate;
+};
+
+struct FwdShared {
+    unsigned char* stages;
+    REAL* buf;
+    unsigned long long* full;
+    VR* Ts;
+    long long i0, i1, e_begin, e_end;
+};
+
+// Called by all of warp 0: stream edge j's rows into its stage.
 template <bool CONV>
-__device__ __forceinline__ void fwd_staged(long long n_items, const int* __restrict__ rowptr,
-                                           const int* __restrict__ sender,
-                                           const REAL* __restrict__ x, const REAL* __restrict__ y,
-                                           const REAL* __restrict__ w, long long w_stride,
-                                           REAL* __restrict__ out, REAL scale, int accumulate) {
+__device__ __forceinline__ void fwd_issue(const FwdArgs& A, const FwdShared& S, IdxWindow& win,
+                                          long long j) {
+    const long long src = CONV ? (long long)win.get(j) : j;
+    if (threadIdx.x == 0) {
+        unsigned char* st = S.stages + (size_t)((j - S.e_begin) % STAGES) * FWD_STAGE;
+        unsigned long long* b = &S.full[(j - S.e_begin) % STAGES];
+        mbar_expect_tx(b, FWD_STAGE);
+        bulk_g2s(st, A.w + j * A.w_stride, WB, b);
+        bulk_g2s(st + WB, A.x + src * DIMX, XB, b);
+        bulk_g2s(st + WB + XB, A.y + j * NY, YB, b);
+    }
+}
+
+template <int GRP, bool CONV>
+__device__ __forceinline__ void fwd_group(const FwdArgs& A, const FwdShared& S, IdxWindow& win) {
+    using FG = FwdG<GRP>;
+    const int tid = threadIdx.x, ch = tid % LANES;
+    const VR sc = vsplat(A.scale);
+    VR acc[FG::NR];
+    long long j = S.e_begin;
+    long long nend = CONV ? (long long)__ldg(A.rowptr + S.i0 + 1) : S.i0 + 1;
+    for (long long item = S.i0; item < S.i1; ++item) {
+        const long long e1 = nend;
+        if (item + 1 < S.i1) nend = CONV ? (long long)__ldg(A.rowptr + item + 2) : item + 2;
+#pragma unroll
+        for (int r = 0; r < FG::NR; ++r) acc[r] = vzero();
+        for (; j < e1; ++j) {
+            const long long k = j - S.e_begin;
+            const unsigned char* st = S.stages + (size_t)(k % STAGES) * FWD_STAGE;
+            const bool ok = mbar_wait(&S.full[k % STAGES], (unsigned)((k / STAGES) & 1));
+            build_T_cta<NTF>(S.Ts, reinterpret_cast<const REAL*>(st + WB + XB));
+            if (!cta_all(ok)) {
+                fail_and_drain(1, S.full, STAGES);
+                return;
+            }
+            VR xr[FG::NXR];
+            FG::loadx(xr, reinterpret_cast<const REAL*>(st + WB), ch);
+            const REAL* ws = reinterpret_cast<const REAL*>(st);
+            FG::edge(acc, S.Ts, xr, [&](int p) { return lds_v(ws + p * MUL, ch); });
+            cta_sync();
+            if constexpr (GRP == 0)
+                if (tid < 32 && j + STAGES < S.e_end) fwd_issue<CONV>(A, S, win, j + STAGES);
+        }
+        // partial sums of the groups, added in group order
+        if constexpr (GRP == 0) FG::first(S.buf, acc, ch);
+        cta_sync();
+#pragma unroll
+        for (int g = 1; g < GF; ++g) {
+            if (g == GRP) FG::add(S.buf, acc, ch);
+            cta_sync();
+        }
+        REAL* orow = A.out + item * DIMO;
+        for (int i = tid; i < NO * NCH; i += NTF) {
+            const int r = i / NCH, c = i % NCH;
+            VR v = vmul(lds_v(S.buf + r * MUL, c), sc);
+            if (A.accumulate) v = vadd(v, ldv_plain(orow + r * MUL, c));
+            stv(orow + r * MUL, c, v);
+        }
+        cta_sync();
+    }
+}
+
+template <bool CONV>
+__device__ __forceinline__ void fwd_staged(const FwdArgs& A) {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ __align__(8) unsigned long long full[STAGES];
     __shared__ __align__(16) VR Ts[NTP];
-    const int tid = threadIdx.x, ch = tid;
-    long long i0, i1;
-    cta_items(CONV ? rowptr : nullptr, n_items, i0, i1);
-    if (i0 >= i1) return;
-    const long long e_begin = CONV ? (long long)__ldg(rowptr + i0) : i0;
-    const long long e_end = CONV ? (long long)__ldg(rowptr + i1) : i1;
-    if (tid == 0) {
+    FwdShared S;
+    cta_items(CONV ? A.rowptr : nullptr, A.n_items, S.i0, S.i1);
+    if (S.i0 >= S.i1) return;
+    S.stages = smem;
+    S.buf = reinterpret_cast<REAL*>(smem + (size_t)STAGES * FWD_STAGE);
+    S.full = full;
+    S.Ts = Ts;
+    S.e_begin = CONV ? (long long)__ldg(A.rowptr + S.i0) : S.i0;
+    S.e_end = CONV ? (long long)__ldg(A.rowptr + S.i1) : S.i1;
+    if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) mbar_init(&full[s], 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
     IdxWindow win;
-    if (CONV && tid < 32) win.init(sender, e_begin, e_end);
-    auto issue = [&](long long j) {  // all of warp 0 calls; thread 0 issues
-        const long long src = CONV ? (long long)win.get(j) : j;
-        if (tid == 0) {
-            unsigned char* st = smem + (size_t)((j - e_begin) % STAGES) * FWD_STAGE;
-            unsigned long long* b = &full[(j - e_begin) % STAGES];
-            mbar_expect_tx(b, FWD_STAGE);
-            bulk_g2s(st, w + j * w_stride, WB, b);
-            bulk_g2s(st + WB, x + src * DIMX, XB, b);
-            bulk_g2s(st + WB + XB, y + j * NY, YB, b);
-        }
-    };
-    if (tid < 32)
-        for (long long j = e_begin; j < e_begin + STAGES && j < e_end; ++j) issue(j);
-    long long j = e_begin;
-    long long nend = CONV ? (long long)__ldg(rowptr + i0 + 1) : i0 + 1;
-    const VR sc = vsplat(scale);
-    for (long long item = i0; item < i1; ++item) {
-        const long long e1 = nend;
-        if (item + 1 < i1) nend = CONV ? (long long)__ldg(rowptr + item + 2) : item + 2;
-        VR acc[NO];
-#pragma unroll
-        for (int r = 0; r < NO; ++r) acc[r] = vzero();
-        for (; j < e1; ++j) {
-            const long long k = j - e_begin;
-            const unsigned char* st = smem + (size_t)(k % STAGES) * FWD_STAGE;
-            const bool ok = mbar_wait(&full[k % STAGES], (unsigned)((k / STAGES) & 1));
-            build_T(Ts, reinterpret_cast<const REAL*>(st + WB + XB), tid);
-            if (!cta_all(ok)) {
-                fail_and_drain(1, full, STAGES);
-                return;
-            }
-            const REAL* xs = reinterpret_cast<const REAL*>(st + WB);
-            const REAL* ws = reinterpret_cast<const REAL*>(st);
-            gen_fwd(acc, Ts, [&](int r) { return lds_v(xs + r * MUL, ch); },
-                    [&](int p) { return lds_v(ws + p * MUL, ch); });
-            cta_sync();
-            if (tid < 32 && j + STAGES < e_end) issue(j + STAGES);
-        }
-        REAL* orow = out + item * DIMO;
-#pragma unroll
-        for (int r = 0; r < NO; ++r) {
-            VR v = vmul(acc[r], sc);
-            if (accumulate) v = vadd(v, ldv_plain(orow + r * MUL, ch));
-            stv(orow + r * MUL, ch, v);
-        }
+    if (threadIdx.x < 32) {
+        if (CONV) win.init(A.sender, S.e_begin, S.e_end);
+        for (long long j = S.e_begin; j < S.e_begin + STAGES && j < S.e_end; ++j)
+            fwd_issue<CONV>(A, S, win, j);
     }
+    const int grp = threadIdx.x / LANES;
+    if (grp == 0) fwd_group<0, CONV>(A, S, win);
+#if GF > 1
+    else if (grp == 1) fwd_group<1, CONV>(A, S, win);
+#endif
+#if GF > 2
+    else if (grp == 2) fwd_group<2, CONV>(A, S, win);
+#endif
+#if GF > 3
+    else if (grp == 3) fwd_group<3, CONV>(A, S, win);
+#endif
 }
 
-extern "C" __global__ void __launch_bounds__(LANES, MINB_FWD)
+extern "C" __global__ void __launch_bounds__(NTF)
 cgtp_fwd_conv_tma(long long n_items, const int* __restrict__ rowptr,
                   const int* __restrict__ sender, const REAL* __restrict__ x,
                   const REAL* __restrict__ y, const REAL* __restrict__ w, long long w_stride,
                   REAL* __restrict__ out, REAL scale, int accumulate) {
-    fwd_staged<true>(n_items, rowptr, sender, x, y, w, w_stride, out, scale, accumulate);
+    fwd_staged<true>(FwdArgs{n_items, rowptr, sender, x, y, w, w_stride, out, scale, accumulate});
 }
 
-extern "C" __global__ void __launch_bounds__(LANES, MINB_FWD)
+extern "C" __global__ void __launch_bounds__(NTF)
 cgtp_fwd_single_tma(long long n_items, const REAL* __restrict__ x, const REAL* __restrict__ y,
                     const REAL* __restrict__ w, long long w_stride, REAL* __restrict__ out,
                     REAL scale, int accumulate) {
-    fwd_staged<false>(n_items, nullptr, nullptr, x, y, w, w_stride, out, scale, accumulate);
+    fwd_staged<false>(FwdArgs{n_items, nullptr, nullptr, x, y, w, w_stride, out, scale, accumulate});
 }
 
 // ---------------------------------------------------------- staged backward
 //
 // Items are senders (or samples).  Stages carry w[e], g[n] and y[e] of the
 // item's edges (e = s_perm[j], n = s_recv[j]); the item's own x row comes
-// through a second, double-buffered TMA slot.
+// through a second, double-buffered TMA slot.  grad_w is stored by the group
+// owning the path; grad_y is reduced per warp, then across warps in warp order;
+// grad_x partials are added in group order at the end of the item.
 
-template <bool CONV, bool GY>
-__device__ __forceinline__ void bwd_staged(long long n_items, const int* __restrict__ s_rowptr,
-                                           const int* __restrict__ s_perm,
-                                           const int* __restrict__ s_recv,
-                                           const REAL* __restrict__ x, const REAL* __restrict__ y,
-                                           const REAL* __restrict__ w, long long w_stride,
-                                           const REAL* __restrict__ g, REAL scale,
-                                           REAL* __restrict__ gx, REAL* __restrict__ gy,
-                                           REAL* __restrict__ gw, int mgx, int mgy, int mgw) {
-    extern __shared__ __align__(128) unsigned char smem[];
-    __shared__ __align__(8) unsigned long long full[STAGES];
-    __shared__ __align__(8) unsigned long long xfull[2];
-    __shared__ __align__(16) VR Ts[NTP];
-#if LANES > 32
-    __shared__ REAL Gy[LANES / 32][NYP];
-#endif
-    const int tid = threadIdx.x, ch = tid, lane = tid & 31;
-    unsigned char* xbuf = smem + (size_t)STAGES * BWD_STAGE;  // 2 x XB
-    long long i0, i1;
-    cta_items(CONV ? s_rowptr : nullptr, n_items, i0, i1);
-    if (i0 >= i1) return;
-    const long long j_begin = CONV ? (long long)__ldg(s_rowptr + i0) : i0;
-    const long long j_end = CONV ? (long long)__ldg(s_rowptr + i1) : i1;
-    if (tid == 0) {
-        for (int s = 0; s < STAGES; ++s) mbar_init(&full[s], 1);
-        mbar_init(&xfull[0], 1);
-        mbar_init(&xfull[1], 1);
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+struct BwdArgs {
+    long long n_items;
+    const int* __restrict__ s_rowptr;
+    const int* __restrict__ s_perm;
+    const int* __restrict__ s_recv;
+    const REAL* __restrict__ x;
+    const REAL* __restrict__ y;
+    const REAL* __restrict__ w;
+    long long w_stride;
+    const REAL* __restrict__ g;
+    REAL scale;
+    REAL* __restrict__ gx;
+    REAL* __restrict__ gy;
+    REAL* __restrict__ gw;
+    int mgx, mgy, mgw;
+};
+
+constexpr int NWB = NTB / 32;  // warps of a backward CTA
+
+struct BwdShared {
+    unsigned char* stages;
+    unsigned char* xring;
+    REAL* buf;
+    unsigned long long* full;
+    unsigned long long* xfull;
+    VR* Ts;
+    REAL (*gyS)[NYP];
+    long long i0, i1, j_begin, j_end;
+};
+
+template <bool CONV>
+__device__ __forceinline__ void bwd_issue(const BwdArgs& A, const BwdShared& S, IdxWindow& we,
+                                          IdxWindow& wn, long long j) {
+    const long long e = CONV ? (long long)we.get(j) : j;
+    const long long n = CONV ? (long long)wn.get(j) : j;
+    if (threadIdx.x == 0) {
+        unsigned char* st = S.stages + (size_t)((j - S.j_begin) % STAGES) * BWD_STAGE;
+        unsigned long long* b = &S.full[(j - S.j_begin) % STAGES];
+        *reinterpret_cast<int*>(st + WB + GB_ + YB) = (int)e;
+        mbar_expect_tx(b, WB + GB_ + YB);
+        bulk_g2s(st, A.w + e * A.w_stride, WB, b);
+        bulk_g2s(st + WB, A.g + n * DIMO, GB_, b);
+        bulk_g2s(st + WB + GB_, A.y + e * NY, YB, b);
     }
-    __syncthreads();
-    IdxWindow we, wn;
-    if (CONV && tid < 32) {
-        we.init(s_perm, j_begin, j_end);
-        wn.init(s_recv, j_begin, j_end);
+}
+
+__device__ __forceinline__ void bwd_issue_x(const BwdArgs& A, const BwdShared& S, long long item,
+                                            int slot) {
+    if (threadIdx.x == 0) {
+        mbar_expect_tx(&S.xfull[slot], XB);
+        bulk_g2s(S.xring + (size_t)slot * XB, A.x + item * DIMX, XB, &S.xfull[slot]);
     }
-    auto issue = [&](long long j) {  // all of warp 0 calls; thread 0 issues
-        const long long e = CONV ? (long long)we.get(j) : j;
-        const long long n = CONV ? (long long)wn.get(j) : j;
-        if (tid == 0) {
-            unsigned char* st = smem + (size_t)((j - j_begin) % STAGES) * BWD_STAGE;
-            unsigned long long* b = &full[(j - j_begin) % STAGES];
-            int* hdr = reinterpret_cast<int*>(st + WB + GB + YB);
-            hdr[0] = (int)e;
-            mbar_expect_tx(b, WB + GB + YB);
-            bulk_g2s(st, w + e * w_stride, WB, b);
-            bulk_g2s(st + WB, g + n * DIMO, GB, b);
-            bulk_g2s(st + WB + GB, y + e * NY, YB, b);
-        }
-    };
-    auto issue_x = [&](long long item, int slot) {
-        if (tid == 0) {
-            mbar_expect_tx(&xfull[slot], XB);
-            bulk_g2s(xbuf + (size_t)slot * XB, x + item * DIMX, XB, &xfull[slot]);
-        }
-    };
-    if (tid < 32)
-        for (long long j = j_begin; j < j_begin + STAGES && j < j_end; ++j) issue(j);
-    issue_x(i0, 0);
-    long long j = j_begin;
-    long long nend = CONV ? (long long)__ldg(s_rowptr + i0 + 1) : i0 + 1;
-    const VR sc = vsplat(scale);
-    for (long long item = i0; item < i1; ++item) {
-        const long long kk = item - i0;
+}
+
+template <int GRP, bool CONV, bool GY>
+__device__ __forceinline__ void bwd_group(const BwdArgs& A, const BwdShared& S, IdxWindow& we,
+                                          IdxWindow& wn) {
+    using BG = BwdG<GRP>;
+    const int tid = threadIdx.x, ch = tid % LANES, lane = tid & 31;
+    const VR sc = vsplat(A.scale);
+    long long j = S.j_begin;
+    long long nend = CONV ? (long long)__ldg(A.s_rowptr + S.i0 + 1) : S.i0 + 1;
+    for (long long item = S.i0; item < S.i1; ++item) {
+        const long long kk = item - S.i0;
         const long long e1 = nend;
-        if (item + 1 < i1) nend = CONV ? (long long)__ldg(s_rowptr + item + 2) : item + 2;
-        if (!cta_all(mbar_wait(&xfull[kk & 1], (unsigned)((kk >> 1) & 1)))) {
-            fail_and_drain(2, full, STAGES);
-            fail_and_drain(2, xfull, 2);
+        if (item + 1 < S.i1) nend = CONV ? (long long)__ldg(A.s_rowptr + item + 2) : item + 2;
+        if (!cta_all(mbar_wait(&S.xfull[kk & 1], (unsigned)((kk >> 1) & 1)))) {
+            fail_and_drain(2, S.full, STAGES);
+            fail_and_drain(2, S.xfull, 2);
             return;
         }
-        VR xr[NX], gxa[NX];
-        const REAL* xs = reinterpret_cast<const REAL*>(xbuf + (size_t)(kk & 1) * XB);
+        VR xr[BG::NXR], gxa[BG::NXR];
+        BG::loadx(xr, reinterpret_cast<const REAL*>(S.xring + (size_t)(kk & 1) * XB), ch);
 #pragma unroll
-        for (int r = 0; r < NX; ++r) {
-            xr[r] = lds_v(xs + r * MUL, ch);
-            gxa[r] = vzero();
-        }
+        for (int r = 0; r < BG::NXR; ++r) gxa[r] = vzero();
         cta_sync();  // every thread holds its x before the slot is refilled
-        if (item + 1 < i1) issue_x(item + 1, (int)((kk + 1) & 1));
+        if (item + 1 < S.i1) bwd_issue_x(A, S, item + 1, (int)((kk + 1) & 1));
         for (; j < e1; ++j) {
-            const long long k = j - j_begin;
-            const unsigned char* st = smem + (size_t)(k % STAGES) * BWD_STAGE;
-            const bool ok = mbar_wait(&full[k % STAGES], (unsigned)((k / STAGES) & 1));
-            const long long e = *reinterpret_cast<const int*>(st + WB + GB + YB);
-            build_T(Ts, reinterpret_cast<const REAL*>(st + WB + GB), tid);
+            const long long k = j - S.j_begin;
+            const unsigned char* st = S.stages + (size_t)(k % STAGES) * BWD_STAGE;
+            const bool ok = mbar_wait(&S.full[k % STAGES], (unsigned)((k / STAGES) & 1));
+            const long long e = *reinterpret_cast<const int*>(st + WB + GB_ + YB);
+            build_T_cta<NTB>(S.Ts, reinterpret_cast<const REAL*>(st + WB + GB_));
             if (!cta_all(ok)) {
-                fail_and_drain(3, full, STAGES);
-                fail_and_drain(3, xfull, 2);
+                fail_and_drain(3, S.full, STAGES);
+                fail_and_drain(3, S.xfull, 2);
                 return;
             }
             const REAL* gs = reinterpret_cast<const REAL*>(st + WB);
@@ -750,64 +815,109 @@ __device__ __forceinline__ void bwd_staged(long long n_items, const int* __restr
             REAL gyl[NYP];
 #pragma unroll
             for (int i = 0; i < NYP; ++i) gyl[i] = (REAL)0;
-            REAL* gwrow = gw ? gw + e * WDIM : nullptr;
-            gen_bwd<GY>(gxa, gyl, Ts, [&](int r) { return xr[r]; },
-                        [&](int r) { return lds_v(gs + r * MUL, ch); },
-                        [&](int p) { return lds_v(ws + p * MUL, ch); }, gwrow, ch, sc, mgx != 0,
-                        mgw);
-            if (GY && mgy) {
+            REAL* gwrow = A.gw ? A.gw + e * WDIM : nullptr;
+            BG::template edge<GY>(gxa, gyl, S.Ts, xr,
+                                  [&](int r) { return lds_v(gs + r * MUL, ch); },
+                                  [&](int p) { return lds_v(ws + p * MUL, ch); }, gwrow, ch, sc,
+                                  A.mgx != 0, A.mgw);
+            if (GY && A.mgy) {
                 int base = 0;
                 bool owner = true;
                 seg_reduce<16, NYP>(gyl, lane, 0xffffffffu, base, owner);
-#if LANES > 32
                 if (owner)
-                    for (int i = 0; i < NRED; ++i) Gy[tid / 32][base + i] = gyl[i];
-                __syncthreads();
-                for (int q = tid; q < NY; q += LANES) {
-                    REAL t = (REAL)0;
-                    for (int wq = 0; wq < LANES / 32; ++wq) t += Gy[wq][q];
-                    t *= scale;
-                    if (mgy == 2) t += gy[e * NY + q];
-                    gy[e * NY + q] = t;
-                }
-#else
-                if (owner) {
 #pragma unroll
-                    for (int i = 0; i < NRED; ++i) {
-                        const int q = base + i;
-                        if (q < NY) {
-                            REAL t = gyl[i] * scale;
-                            if (mgy == 2) t += gy[e * NY + q];
-                            gy[e * NY + q] = t;
-                        }
-                    }
-                }
-#endif
+                    for (int i = 0; i < NRED; ++i) S.gyS[tid / 32][base + i] = gyl[i];
             }
             cta_sync();
-            if (tid < 32 && j + STAGES < j_end) issue(j + STAGES);
-        }
-        if (mgx) {
-            REAL* orow = gx + item * DIMX;
+            if (GY && A.mgy && tid < NY) {
+                REAL t = (REAL)0;
 #pragma unroll
-            for (int r = 0; r < NX; ++r) {
-                VR v = vmul(gxa[r], sc);
-                if (mgx == 2) v = vadd(v, ldv_plain(orow + r * MUL, ch));
-                stv(orow + r * MUL, ch, v);
+                for (int q = 0; q < NWB; ++q) t += S.gyS[q][tid];
+                t *= A.scale;
+                if (A.mgy == 2) t += A.gy[e * NY + tid];
+                A.gy[e * NY + tid] = t;
             }
+            if constexpr (GRP == 0)
+                if (tid < 32 && j + STAGES < S.j_end) bwd_issue<CONV>(A, S, we, wn, j + STAGES);
+        }
+        if (A.mgx) {
+            if constexpr (GRP == 0) BG::first(S.buf, gxa, ch);
+            cta_sync();
+#pragma unroll
+            for (int g = 1; g < GB; ++g) {
+                if (g == GRP) BG::add(S.buf, gxa, ch);
+                cta_sync();
+            }
+            REAL* orow = A.gx + item * DIMX;
+            for (int i = tid; i < NX * NCH; i += NTB) {
+                const int r = i / NCH, c = i % NCH;
+                VR v = vmul(lds_v(S.buf + r * MUL, c), sc);
+                if (A.mgx == 2) v = vadd(v, ldv_plain(orow + r * MUL, c));
+                stv(orow + r * MUL, c, v);
+            }
+            cta_sync();
         }
     }
 }
 
+template <bool CONV, bool GY>
+__device__ __forceinline__ void bwd_staged(const BwdArgs& A) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ __align__(8) unsigned long long full[STAGES];
+    __shared__ __align__(8) unsigned long long xfull[2];
+    __shared__ __align__(16) VR Ts[NTP];
+    __shared__ REAL gyS[NWB][NYP];
+    BwdShared S;
+    cta_items(CONV ? A.s_rowptr : nullptr, A.n_items, S.i0, S.i1);
+    if (S.i0 >= S.i1) return;
+    S.stages = smem;
+    S.xring = smem + (size_t)STAGES * BWD_STAGE;
+    S.buf = reinterpret_cast<REAL*>(S.xring + 2 * (size_t)XB);
+    S.full = full;
+    S.xfull = xfull;
+    S.Ts = Ts;
+    S.gyS = gyS;
+    S.j_begin = CONV ? (long long)__ldg(A.s_rowptr + S.i0) : S.i0;
+    S.j_end = CONV ? (long long)__ldg(A.s_rowptr + S.i1) : S.i1;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) mbar_init(&full[s], 1);
+        mbar_init(&xfull[0], 1);
+        mbar_init(&xfull[1], 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    IdxWindow we, wn;
+    if (threadIdx.x < 32) {
+        if (CONV) {
+            we.init(A.s_perm, S.j_begin, S.j_end);
+            wn.init(A.s_recv, S.j_begin, S.j_end);
+        }
+        for (long long j = S.j_begin; j < S.j_begin + STAGES && j < S.j_end; ++j)
+            bwd_issue<CONV>(A, S, we, wn, j);
+    }
+    bwd_issue_x(A, S, S.i0, 0);
+    const int grp = threadIdx.x / LANES;
+    if (grp == 0) bwd_group<0, CONV, GY>(A, S, we, wn);
+#if GB > 1
+    else if (grp == 1) bwd_group<1, CONV, GY>(A, S, we, wn);
+#endif
+#if GB > 2
+    else if (grp == 2) bwd_group<2, CONV, GY>(A, S, we, wn);
+#endif
+#if GB > 3
+    else if (grp == 3) bwd_group<3, CONV, GY>(A, S, we, wn);
+#endif
+}
+
 #define CGTP_BWD_TMA_ENTRY(NAME, CONV, GY)                                                      \
-    extern "C" __global__ void __launch_bounds__(LANES, MINB_BWD) NAME(                       \
+    extern "C" __global__ void __launch_bounds__(NTB) NAME(                                   \
         long long n_items, const int* __restrict__ s_rowptr, const int* __restrict__ s_perm,  \
         const int* __restrict__ s_recv, const REAL* __restrict__ x,                           \
         const REAL* __restrict__ y, const REAL* __restrict__ w, long long w_stride,           \
         const REAL* __restrict__ g, REAL scale, REAL* __restrict__ gx, REAL* __restrict__ gy, \
         REAL* __restrict__ gw, int mgx, int mgy, int mgw) {                                   \
-        bwd_staged<CONV, GY>(n_items, s_rowptr, s_perm, s_recv, x, y, w, w_stride, g, scale,  \
-                             gx, gy, gw, mgx, mgy, mgw);                                      \
+        bwd_staged<CONV, GY>(BwdArgs{n_items, s_rowptr, s_perm, s_recv, x, y, w, w_stride, g, \
+                                     scale, gx, gy, gw, mgx, mgy, mgw});                      \
     }
 
 CGTP_BWD_TMA_ENTRY(cgtp_bwd_conv_tma, true, true)
