@@ -360,17 +360,31 @@ cgtp_status build_plan(Plan& p, const char* s1, const char* s2, const char* so,
         };
         p.fwd_groups = lpt(cf);
         p.bwd_groups = lpt(cb);
+        // Ring depth: keep the CTAs that fit one SM (4 forward, 2 backward CTAs
+        // of 128 threads, the register-limited counts) streaming ~130-170 KB,
+        // i.e. several microseconds of HBM latency ahead of the FMA stream.
         const size_t stat = (size_t)std::max(2, nt + (nt & 1)) * vr + 2048;
-        for (int st = 3; st >= 2; --st) {
-            const size_t f = st * (WB + XB + YB) + GB;           // + output combine buffer
-            const size_t b = st * (WB + GB + YB + 16) + 2 * XB + XB;  // + x ring + gx buffer
-            if (f + stat <= 200 * 1024 && b + stat <= 200 * 1024) {
-                p.staged = true;
-                p.stages = st;
-                p.fwd_smem = f;
-                p.bwd_smem = b;
-                break;
+        const size_t fst = WB + XB + YB, bst = WB + GB + YB + 16;
+        const size_t budget = 216 * 1024;
+        auto depth = [&](size_t stage, size_t extra, int ctas) {
+            const long long room = (long long)(budget / ctas) - (long long)(extra + stat);
+            return (int)std::max<long long>(0, std::min<long long>(12, room / (long long)stage));
+        };
+        auto pick = [&](size_t stage, size_t extra, std::initializer_list<int> ks) {
+            int best = 0;
+            for (int k : ks) {  // most CTAs per SM that still keep a ring of >= 4 edges
+                best = depth(stage, extra, k);
+                if (best >= 4) break;
             }
+            return best;
+        };
+        const int sf = pick(fst, GB, {4, 3, 2, 1}), sb = pick(bst, 3 * XB, {2, 1});
+        if (sf >= 2 && sb >= 2) {
+            p.staged = true;
+            p.stages_f = sf;
+            p.stages_b = sb;
+            p.fwd_smem = sf * fst + GB;
+            p.bwd_smem = sb * bst + 3 * XB;
         }
     }
     return CGTP_OK;
@@ -607,7 +621,8 @@ std::string Plan::kernel_source() const {
        << "\n#define NO " << no << "\n#define NP " << paths.size() << "\n#define NT " << nt
        << "\n#define NTP " << ntp << "\n#define MAXTERMS " << maxterms << "\n#define YPF "
        << (ny + lanes - 1) / lanes << "\n";
-    os << "#define STAGED " << (staged ? 1 : 0) << "\n#define STAGES " << stages
+    os << "#define STAGED " << (staged ? 1 : 0) << "\n#define STAGES_F " << stages_f
+       << "\n#define STAGES_B " << stages_b
        << "\n#define GF " << std::max<size_t>(1, fwd_groups.size()) << "\n#define GB "
        << std::max<size_t>(1, bwd_groups.size()) << "\n";
     // T tables

@@ -63,7 +63,7 @@ struct Plan {
     int block = 0;  // threads per CTA
     // staged (TMA) kernels: one slot of `lanes` threads per CTA
     bool staged = false;
-    int stages = 3;
+    int stages_f = 3, stages_b = 3;  // TMA ring depths (forward, backward)
     size_t fwd_smem = 0, bwd_smem = 0;  // dynamic shared memory per CTA
     // warp groups of the staged kernels: each group of `lanes` threads runs the
     // generated stream of a subset of paths (longest-processing-time split)

@@ -433,13 +433,14 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned by
 // Bounded wait for phase `parity` of barrier b.  Returns false on timeout.
 __device__ __forceinline__ bool mbar_wait(unsigned long long* b, unsigned parity) {
     const unsigned a = smem_u32(b);
-    for (unsigned it = 0; it < (1u << 22); ++it) {
+    // about a second at most: 2^24 polls, sleeping 64 ns between late polls
+    for (unsigned it = 0; it < (1u << 24); ++it) {
         unsigned ok;
         asm volatile(
             "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
             : "=r"(ok) : "r"(a), "r"(parity) : "memory");
         if (ok) return true;
-        if (it > 64) __nanosleep(256);
+        if (it > 1024) __nanosleep(64);
     }
     return false;
 }
@@ -603,8 +604,8 @@ __device__ __forceinline__ void fwd_issue(const FwdArgs& A, const FwdShared& S, 
                                           long long j) {
     const long long src = CONV ? (long long)win.get(j) : j;
     if (threadIdx.x == 0) {
-        unsigned char* st = S.stages + (size_t)((j - S.e_begin) % STAGES) * FWD_STAGE;
-        unsigned long long* b = &S.full[(j - S.e_begin) % STAGES];
+        unsigned char* st = S.stages + (size_t)((j - S.e_begin) % STAGES_F) * FWD_STAGE;
+        unsigned long long* b = &S.full[(j - S.e_begin) % STAGES_F];
         mbar_expect_tx(b, FWD_STAGE);
         bulk_g2s(st, A.w + j * A.w_stride, WB, b);
         bulk_g2s(st + WB, A.x + src * DIMX, XB, b);
@@ -627,11 +628,11 @@ __device__ __forceinline__ void fwd_group(const FwdArgs& A, const FwdShared& S, 
         for (int r = 0; r < FG::NR; ++r) acc[r] = vzero();
         for (; j < e1; ++j) {
             const long long k = j - S.e_begin;
-            const unsigned char* st = S.stages + (size_t)(k % STAGES) * FWD_STAGE;
-            const bool ok = mbar_wait(&S.full[k % STAGES], (unsigned)((k / STAGES) & 1));
+            const unsigned char* st = S.stages + (size_t)(k % STAGES_F) * FWD_STAGE;
+            const bool ok = mbar_wait(&S.full[k % STAGES_F], (unsigned)((k / STAGES_F) & 1));
             build_T_cta<NTF>(S.Ts, reinterpret_cast<const REAL*>(st + WB + XB));
             if (!cta_all(ok)) {
-                fail_and_drain(1, S.full, STAGES);
+                fail_and_drain(1, S.full, STAGES_F);
                 return;
             }
             VR xr[FG::NXR];
@@ -640,7 +641,7 @@ __device__ __forceinline__ void fwd_group(const FwdArgs& A, const FwdShared& S, 
             FG::edge(acc, S.Ts, xr, [&](int p) { return lds_v(ws + p * MUL, ch); });
             cta_sync();
             if constexpr (GRP == 0)
-                if (tid < 32 && j + STAGES < S.e_end) fwd_issue<CONV>(A, S, win, j + STAGES);
+                if (tid < 32 && j + STAGES_F < S.e_end) fwd_issue<CONV>(A, S, win, j + STAGES_F);
         }
         // partial sums of the groups, added in group order
         if constexpr (GRP == 0) FG::first(S.buf, acc, ch);
@@ -664,26 +665,26 @@ __device__ __forceinline__ void fwd_group(const FwdArgs& A, const FwdShared& S, 
 template <bool CONV>
 __device__ __forceinline__ void fwd_staged(const FwdArgs& A) {
     extern __shared__ __align__(128) unsigned char smem[];
-    __shared__ __align__(8) unsigned long long full[STAGES];
+    __shared__ __align__(8) unsigned long long full[STAGES_F];
     __shared__ __align__(16) VR Ts[NTP];
     FwdShared S;
     cta_items(CONV ? A.rowptr : nullptr, A.n_items, S.i0, S.i1);
     if (S.i0 >= S.i1) return;
     S.stages = smem;
-    S.buf = reinterpret_cast<REAL*>(smem + (size_t)STAGES * FWD_STAGE);
+    S.buf = reinterpret_cast<REAL*>(smem + (size_t)STAGES_F * FWD_STAGE);
     S.full = full;
     S.Ts = Ts;
     S.e_begin = CONV ? (long long)__ldg(A.rowptr + S.i0) : S.i0;
     S.e_end = CONV ? (long long)__ldg(A.rowptr + S.i1) : S.i1;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) mbar_init(&full[s], 1);
+        for (int s = 0; s < STAGES_F; ++s) mbar_init(&full[s], 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
     IdxWindow win;
     if (threadIdx.x < 32) {
         if (CONV) win.init(A.sender, S.e_begin, S.e_end);
-        for (long long j = S.e_begin; j < S.e_begin + STAGES && j < S.e_end; ++j)
+        for (long long j = S.e_begin; j < S.e_begin + STAGES_F && j < S.e_end; ++j)
             fwd_issue<CONV>(A, S, win, j);
     }
     const int grp = threadIdx.x / LANES;
@@ -758,8 +759,8 @@ __device__ __forceinline__ void bwd_issue(const BwdArgs& A, const BwdShared& S, 
     const long long e = CONV ? (long long)we.get(j) : j;
     const long long n = CONV ? (long long)wn.get(j) : j;
     if (threadIdx.x == 0) {
-        unsigned char* st = S.stages + (size_t)((j - S.j_begin) % STAGES) * BWD_STAGE;
-        unsigned long long* b = &S.full[(j - S.j_begin) % STAGES];
+        unsigned char* st = S.stages + (size_t)((j - S.j_begin) % STAGES_B) * BWD_STAGE;
+        unsigned long long* b = &S.full[(j - S.j_begin) % STAGES_B];
         *reinterpret_cast<int*>(st + WB + GB_ + YB) = (int)e;
         mbar_expect_tx(b, WB + GB_ + YB);
         bulk_g2s(st, A.w + e * A.w_stride, WB, b);
@@ -789,7 +790,7 @@ __device__ __forceinline__ void bwd_group(const BwdArgs& A, const BwdShared& S, 
         const long long e1 = nend;
         if (item + 1 < S.i1) nend = CONV ? (long long)__ldg(A.s_rowptr + item + 2) : item + 2;
         if (!cta_all(mbar_wait(&S.xfull[kk & 1], (unsigned)((kk >> 1) & 1)))) {
-            fail_and_drain(2, S.full, STAGES);
+            fail_and_drain(2, S.full, STAGES_B);
             fail_and_drain(2, S.xfull, 2);
             return;
         }
@@ -801,12 +802,12 @@ __device__ __forceinline__ void bwd_group(const BwdArgs& A, const BwdShared& S, 
         if (item + 1 < S.i1) bwd_issue_x(A, S, item + 1, (int)((kk + 1) & 1));
         for (; j < e1; ++j) {
             const long long k = j - S.j_begin;
-            const unsigned char* st = S.stages + (size_t)(k % STAGES) * BWD_STAGE;
-            const bool ok = mbar_wait(&S.full[k % STAGES], (unsigned)((k / STAGES) & 1));
+            const unsigned char* st = S.stages + (size_t)(k % STAGES_B) * BWD_STAGE;
+            const bool ok = mbar_wait(&S.full[k % STAGES_B], (unsigned)((k / STAGES_B) & 1));
             const long long e = *reinterpret_cast<const int*>(st + WB + GB_ + YB);
             build_T_cta<NTB>(S.Ts, reinterpret_cast<const REAL*>(st + WB + GB_));
             if (!cta_all(ok)) {
-                fail_and_drain(3, S.full, STAGES);
+                fail_and_drain(3, S.full, STAGES_B);
                 fail_and_drain(3, S.xfull, 2);
                 return;
             }
@@ -838,7 +839,7 @@ __device__ __forceinline__ void bwd_group(const BwdArgs& A, const BwdShared& S, 
                 A.gy[e * NY + tid] = t;
             }
             if constexpr (GRP == 0)
-                if (tid < 32 && j + STAGES < S.j_end) bwd_issue<CONV>(A, S, we, wn, j + STAGES);
+                if (tid < 32 && j + STAGES_B < S.j_end) bwd_issue<CONV>(A, S, we, wn, j + STAGES_B);
         }
         if (A.mgx) {
             if constexpr (GRP == 0) BG::first(S.buf, gxa, ch);
@@ -863,7 +864,7 @@ __device__ __forceinline__ void bwd_group(const BwdArgs& A, const BwdShared& S, 
 template <bool CONV, bool GY>
 __device__ __forceinline__ void bwd_staged(const BwdArgs& A) {
     extern __shared__ __align__(128) unsigned char smem[];
-    __shared__ __align__(8) unsigned long long full[STAGES];
+    __shared__ __align__(8) unsigned long long full[STAGES_B];
     __shared__ __align__(8) unsigned long long xfull[2];
     __shared__ __align__(16) VR Ts[NTP];
     __shared__ REAL gyS[NWB][NYP];
@@ -871,7 +872,7 @@ __device__ __forceinline__ void bwd_staged(const BwdArgs& A) {
     cta_items(CONV ? A.s_rowptr : nullptr, A.n_items, S.i0, S.i1);
     if (S.i0 >= S.i1) return;
     S.stages = smem;
-    S.xring = smem + (size_t)STAGES * BWD_STAGE;
+    S.xring = smem + (size_t)STAGES_B * BWD_STAGE;
     S.buf = reinterpret_cast<REAL*>(S.xring + 2 * (size_t)XB);
     S.full = full;
     S.xfull = xfull;
@@ -880,7 +881,7 @@ __device__ __forceinline__ void bwd_staged(const BwdArgs& A) {
     S.j_begin = CONV ? (long long)__ldg(A.s_rowptr + S.i0) : S.i0;
     S.j_end = CONV ? (long long)__ldg(A.s_rowptr + S.i1) : S.i1;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) mbar_init(&full[s], 1);
+        for (int s = 0; s < STAGES_B; ++s) mbar_init(&full[s], 1);
         mbar_init(&xfull[0], 1);
         mbar_init(&xfull[1], 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -892,7 +893,7 @@ __device__ __forceinline__ void bwd_staged(const BwdArgs& A) {
             we.init(A.s_perm, S.j_begin, S.j_end);
             wn.init(A.s_recv, S.j_begin, S.j_end);
         }
-        for (long long j = S.j_begin; j < S.j_begin + STAGES && j < S.j_end; ++j)
+        for (long long j = S.j_begin; j < S.j_begin + STAGES_B && j < S.j_end; ++j)
             bwd_issue<CONV>(A, S, we, wn, j);
     }
     bwd_issue_x(A, S, S.i0, 0);
