@@ -1,9 +1,9 @@
-"""Benchmark of the fused CG tensor-product graph convolution on GB300.
+"""Benchmark of the CG tensor-product hot path on GB300.
 
-Workload: the MACE-like fused convolution -- N = 10,000 atoms in a periodic
-box (density 0.1 / A^3, cutoff 5 A, ~525k directed edges), node features
-64x(0e,1o,2e), edge spherical harmonics l <= 3, 24 'uvu' paths to
-64x(0e,1o,1e,2o,2e,3o,3e), per-edge weights from a random radial MLP, fp32
+Default workload (the headline): the MACE-like fused convolution -- N = 10,000
+atoms in a periodic box (density 0.1 / A^3, cutoff 5 A, ~525k directed edges),
+node features 64x(0e,1o,2e), edge spherical harmonics l <= 3, 24 'uvu' paths
+to 64x(0e,1o,1e,2o,2e,3o,3e), per-edge weights from a random radial MLP, fp32
 (seeded synthetic inputs from ``workloads.config2``).
 
 One step = the whole hot path on one batch: spherical harmonics of the edge
@@ -12,6 +12,11 @@ output cotangent) -> spherical-harmonic backward (dL/dr).  ``value`` is edges
 per second of that forward+backward step; the forward alone is reported under
 ``fwd``.  All inputs are resident in HBM before the timed region; the weight
 stream (3.2 GB) is far larger than L2, so no flush is needed between steps.
+
+Other workloads (``--workload``): ``tp`` standalone product, B = 200,000
+samples, 128 channels (fwd+bwd, samples/s); ``conv64`` the fp64 fused conv,
+N = 5,000, 128 channels (forward, edges/s); ``tfn`` the TFN layer on 1000
+molecules (forward, backward, forces and the double backward, edges/s).
 
 ``--impl reference`` times the CPU oracle (the reference arm of this build) on
 a bounded subgraph of the same workload.
@@ -32,10 +37,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "CG-TP conv edges/sec (fwd, fwd+bwd) at 1 GB300 and % of HBM/FP-pipe roofline"
-WORKLOAD = ("fused CG-TP conv: N=10000 atoms, density 0.1/A^3, cutoff 5 A, "
-            "64x(0e,1o,2e) (x) Y(l<=3) -> 64x(0e,1o,1e,2o,2e,3o,3e), 24 uvu paths, fp32")
 SM_COUNT = 152
-FP32_LANES_PER_SM = 128  # FMA lanes per SM per clock
+FP32_LANES_PER_SM = 128  # FP32 FMA lanes per SM per clock
 
 
 def _peaks():
@@ -49,32 +52,28 @@ def _peaks():
 
 # ------------------------------------------------------------ work counts
 
-def algorithmic_counts(prob, N, E, esize=4):
-    """Algorithmic bytes and FLOPs per launch of each kernel of the step.
-
-    FLOPs per edge of the tensor product: mul * sum_p 2 (nnz_p + d_l3) (the
-    sparse CG multiply-adds plus the weight multiply per output component).
-    Bytes count every tensor read or written once (gathered node rows assumed
-    to hit L2)."""
-    import oracle as O  # only for the CG nonzero counts
-
+def tp_flops_per_row(prob):
+    """FLOPs of one tensor product (one edge or sample): mul * sum_p 2 (nnz_p +
+    d_l3) -- the sparse CG multiply-adds plus the weight multiply per output
+    component."""
+    import oracle as O  # CG nonzero counts only
     mul = prob.paths[0][6]
     nnz = sum(int((np.abs(O.cg_real(l1, l2, l3)) > 0).sum())
               for (_, _, _, l1, l2, l3, *_r) in prob.paths)
     d3 = sum(2 * p[5] + 1 for p in prob.paths)
-    flop_edge = mul * 2 * (nnz + d3)
+    return mul * 2 * (nnz + d3)
+
+
+def conv_counts(prob, N, E, es):
+    """Algorithmic bytes and FLOPs per launch: every tensor read or written
+    once, gathered node rows assumed to hit L2."""
     dx, dy, do, dw = prob.dim1, prob.dim2, prob.dimo, prob.wdim
-    fwd_bytes = E * (dw + dy) * esize + 4 * E + 4 * (N + 1) + N * (dx + do) * esize
-    bwd_bytes = (E * (dw + dy) * esize  # read w, y
-                 + N * (dx + do + dx) * esize  # read x, g; write gx
-                 + E * (dw + dy) * esize  # write gw, gy
-                 + 12 * E + 4 * (N + 1))  # s_perm, s_recv, s_rowptr
-    return dict(
-        sh_fwd=dict(bytes=E * (3 + dy) * esize, flops=None),
-        conv_fwd=dict(bytes=fwd_bytes, flops=E * flop_edge),
-        conv_bwd=dict(bytes=bwd_bytes, flops=3 * E * flop_edge),
-        sh_bwd=dict(bytes=E * (3 + dy + 3) * esize, flops=None),
-        flop_edge=flop_edge, nnz=nnz)
+    f = tp_flops_per_row(prob)
+    fwd = E * (dw + dy) * es + 4 * E + 4 * (N + 1) + N * (dx + do) * es
+    bwd = (E * (dw + dy) * es + N * (dx + do + dx) * es + E * (dw + dy) * es
+           + 12 * E + 4 * (N + 1))
+    return dict(conv_fwd=(fwd, E * f), conv_bwd=(bwd, 3 * E * f),
+                sh_fwd=(E * (3 + dy) * es, None), sh_bwd=(E * (6 + dy) * es, None))
 
 
 # --------------------------------------------------------------- clocks
@@ -92,7 +91,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={q}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -133,9 +132,11 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-# ------------------------------------------------------------ GPU arm
+# ------------------------------------------------------ multi-process
 
-def _dist():
+def dist_setup():
+    """(dist, rank, world): one process per GPU under torchrun; the ranks run
+    independent replicas of the workload (no collective on the data path)."""
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     if ws > 1:
         import torch.distributed as dist
@@ -145,23 +146,36 @@ def _dist():
     return None, 0, 1
 
 
-def run_gpu(args):
+def max_over_ranks(dist, value: float) -> float:
+    """Slowest rank's time (the whole job waits for it)."""
+    if dist is None:
+        return float(value)
     import torch
+    t = torch.tensor([float(value)], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
 
-    import clebsch_gordan_tensor_gb300 as cg
-    import workloads as W
 
-    dist, rank, world = _dist()
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    torch.cuda.set_device(local)
+# ------------------------------------------------------------ workloads
+
+class Workload:
+    """A named sequence of launches forming one step, with work counts."""
+
+    def __init__(self, name, desc, units, unit, dtype, kernels, counts, fwd_names, cfg,
+                 e2e=None, oracle_step=None):
+        self.name, self.desc, self.units, self.unit, self.dtype = name, desc, units, unit, dtype
+        self.kernels, self.counts, self.fwd_names, self.cfg = kernels, counts, fwd_names, cfg
+        self.e2e, self.oracle_step = e2e, oracle_step
+
+
+def make_conv(args, cg, W, torch):
+    import oracle as O
     cfg = W.config2(N=args.atoms)
     gr = cfg["graph"]
     N, E = gr.N, gr.E
     plan = cg.Plan(*cfg["irreps"])
     G = cg.Graph.from_numpy(gr)
-    x = torch.from_numpy(cfg["x"]).cuda()
-    vec = torch.from_numpy(cfg["vec"]).cuda()
-    w = torch.from_numpy(cfg["w"]).cuda()
+    x, vec, w = (torch.from_numpy(cfg[k]).cuda() for k in ("x", "vec", "w"))
     g = torch.from_numpy(np.random.default_rng(7).standard_normal(
         (N, plan.dim_out)).astype(np.float32)).cuda()
     scale = cfg["scale"]
@@ -169,29 +183,165 @@ def run_gpu(args):
     out = torch.empty(N, plan.dim_out, device="cuda")
     gx, gy, gw = torch.empty_like(x), torch.empty_like(y), torch.empty_like(w)
     gvec = torch.empty_like(vec)
-    names = ["sh_fwd", "conv_fwd", "conv_bwd", "sh_bwd"]
+    plan.compile()
+    kernels = [
+        ("sh_fwd", lambda: cg.sh_forward(vec, 3, out=y)),
+        ("conv_fwd", lambda: plan.conv_forward(G, x, y, w, scale, out=out)),
+        ("conv_bwd", lambda: plan.conv_backward(G, x, y, w, scale, g, out=(gx, gy, gw))),
+        ("sh_bwd", lambda: cg.sh_backward(vec, gy, 3, out=gvec)),
+    ]
+    prob = O.make_problem(*cfg["irreps"])
+    desc = (f"fused CG-TP conv: N={N} atoms, density 0.1/A^3, cutoff 5 A, 64x(0e,1o,2e) (x) "
+            "Y(l<=3) -> 64x(0e,1o,1e,2o,2e,3o,3e), 24 uvu paths, fp32")
+
+    def e2e_step_factory():
+        hx, hv, hw = (torch.from_numpy(cfg[k]).pin_memory() for k in ("x", "vec", "w"))
+        ho = torch.empty(N, plan.dim_out).pin_memory()
+        hgx = torch.empty(N, plan.dim_in1).pin_memory()
+
+        def step():
+            x.copy_(hx, non_blocking=True)
+            vec.copy_(hv, non_blocking=True)
+            w.copy_(hw, non_blocking=True)
+            for _, k in kernels:
+                k()
+            ho.copy_(out, non_blocking=True)
+            hgx.copy_(gx, non_blocking=True)
+        nb = lambda ts: sum(t.numel() * t.element_size() for t in ts)
+        return step, nb((hx, hv, hw)), nb((ho, hgx))
+
+    return Workload("conv", desc, E, "edges/s", "f32", kernels, conv_counts(prob, N, E, 4),
+                    ["sh_fwd", "conv_fwd"], dict(N=N, E=E, mul=64, paths=plan.n_paths),
+                    e2e_step_factory, lambda R: _oracle_conv_step(prob, cfg, R))
+
+
+def make_conv64(args, cg, W, torch):
+    import oracle as O
+    cfg = W.config3()
+    gr = cfg["graph"]
+    N, E = gr.N, gr.E
+    plan = cg.Plan(*cfg["irreps"], dtype=torch.float64)
+    G = cg.Graph.from_numpy(gr)
+    x, vec, w = (torch.from_numpy(cfg[k]).cuda() for k in ("x", "vec", "w"))
+    y = torch.empty(E, plan.dim_in2, device="cuda", dtype=torch.float64)
+    out = torch.empty(N, plan.dim_out, device="cuda", dtype=torch.float64)
+    plan.compile()
+    kernels = [("sh_fwd", lambda: cg.sh_forward(vec, 3, out=y)),
+               ("conv_fwd", lambda: plan.conv_forward(G, x, y, w, cfg["scale"], out=out))]
+    prob = O.make_problem(*cfg["irreps"])
+    c = conv_counts(prob, N, E, 8)
+    counts = {k: c[k] for k in ("sh_fwd", "conv_fwd")}
+    desc = (f"fused CG-TP conv fp64: N={N} atoms, 128x(0e,1o,2e) (x) Y(l<=3) -> "
+            "128x(0e,1o,1e,2o,2e,3o,3e), 24 uvu paths, forward only")
+    return Workload("conv64", desc, E, "edges/s", "f64", kernels, counts, ["sh_fwd", "conv_fwd"],
+                    dict(N=N, E=E, mul=128, paths=plan.n_paths), None,
+                    lambda R: _oracle_conv_step(prob, cfg, R, bwd=False))
+
+
+def make_tp(args, cg, W, torch):
+    import oracle as O
+    cfg = W.config1()
+    B = cfg["B"]
+    plan = cg.Plan(*cfg["irreps"])
+    x, vec, w = (torch.from_numpy(cfg[k]).cuda() for k in ("x", "vec", "w"))
+    g = torch.randn(B, plan.dim_out, device="cuda",
+                    generator=torch.Generator("cuda").manual_seed(7))
+    y = torch.empty(B, plan.dim_in2, device="cuda")
+    gvec = torch.empty_like(vec)
+    out = torch.empty(B, plan.dim_out, device="cuda")
+    res = {}
+    plan.compile()
+
+    def bwd():
+        res["g"] = plan.backward(x, y, w, g)
+
+    kernels = [("sh_fwd", lambda: cg.sh_forward(vec, 3, out=y)),
+               ("tp_fwd", lambda: plan.forward(x, y, w, out=out)),
+               ("tp_bwd", bwd),
+               ("sh_bwd", lambda: cg.sh_backward(vec, res["g"][1], 3, out=gvec))]
+    prob = O.make_problem(*cfg["irreps"])
+    f = tp_flops_per_row(prob)
+    rowb = (prob.dim1 + prob.dim2 + prob.wdim) * 4
+    counts = {"sh_fwd": (B * (3 + prob.dim2) * 4, None),
+              "tp_fwd": (B * (rowb + prob.dimo * 4), B * f),
+              "tp_bwd": (B * (rowb + prob.dimo * 4 + rowb), 3 * B * f),
+              "sh_bwd": (B * (6 + prob.dim2) * 4, None)}
+    desc = ("standalone CG-TP: B=200000, 128x(0e,1o,2e) (x) Y(l<=3) -> "
+            "128x(0e,1o,1e,2o,2e,3o,3e), 24 uvu paths, fp32")
+    return Workload("tp", desc, B, "samples/s", "f32", kernels, counts, ["sh_fwd", "tp_fwd"],
+                    dict(B=B, mul=128, paths=plan.n_paths), None,
+                    lambda R: _oracle_tp_step(prob, cfg, R))
+
+
+def make_tfn(args, cg, W, torch):
+    import oracle as O
+    cfg = W.config4()
+    gr = cfg["graph"]
+    N, E = gr.N, gr.E
+    plan = cg.Plan(*cfg["irreps"])
+    G = cg.Graph.from_numpy(gr)
+    x, vec, w, c, gF = (torch.from_numpy(cfg[k]).cuda() for k in ("x", "vec", "w", "c", "gF"))
+    y = torch.empty(E, plan.dim_in2, device="cuda")
+    out = torch.empty(N, plan.dim_out, device="cuda")
+    gx, gy, gw = torch.empty_like(x), torch.empty_like(y), torch.empty_like(w)
+    dEdr, q = torch.empty_like(vec), torch.empty_like(vec)
+    F = torch.empty(N, 3, device="cuda")
+    ggy = torch.empty_like(y)
+    plan.compile()
+    kernels = [
+        ("sh_fwd", lambda: cg.sh_forward(vec, 3, out=y)),
+        ("conv_fwd", lambda: plan.conv_forward(G, x, y, w, 1.0, out=out)),
+        ("conv_bwd", lambda: plan.conv_backward(G, x, y, w, 1.0, c, out=(gx, gy, gw))),
+        ("sh_bwd", lambda: cg.sh_backward(vec, gy, 3, out=dEdr)),
+        ("forces", lambda: cg.edge_forces(G, dEdr, out=F)),
+        ("forces_adj", lambda: cg.edge_forces_adjoint(G, gF, out=q)),
+        ("sh_jvp", lambda: cg.sh_jvp(vec, q, 3, out=ggy)),
+        ("conv_dbl", lambda: plan.conv_double_backward(G, x, y, w, 1.0, c, None, ggy, None,
+                                                       need=(True, False, True, False))),
+    ]
+    prob = O.make_problem(*cfg["irreps"])
+    cc = conv_counts(prob, N, E, 4)
+    counts = {"sh_fwd": cc["sh_fwd"], "conv_fwd": cc["conv_fwd"], "conv_bwd": cc["conv_bwd"],
+              "sh_bwd": cc["sh_bwd"], "forces": (E * 12 + N * 12, None),
+              "forces_adj": (E * 12 + N * 12, None), "sh_jvp": (E * (6 + 16) * 4, None),
+              "conv_dbl": (cc["conv_bwd"][0] - E * prob.dim2 * 4, cc["conv_bwd"][1] * 2 // 3)}
+    desc = ("TFN layer: 1000 molecules of 9-29 atoms, fully connected, 32x(0e,1o,2e,3o) (x) "
+            "Y(l<=3) -> 32x(0e,1o,2e,3o), 23 paths, fp32: fwd, bwd, forces, double backward")
+    return Workload("tfn", desc, E, "edges/s", "f32", kernels, counts, ["sh_fwd", "conv_fwd"],
+                    dict(N=N, E=E, mul=32, paths=plan.n_paths), None, None)
+
+
+WORKLOADS = {"conv": make_conv, "conv64": make_conv64, "tp": make_tp, "tfn": make_tfn}
+
+
+# ------------------------------------------------------------ GPU arm
+
+def run_gpu(args):
+    import torch
+
+    import clebsch_gordan_tensor_gb300 as cg
+    import workloads as W
+
+    dist, rank, world = dist_setup()
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    wl = WORKLOADS[args.workload](args, cg, W, torch)
+    names = [n for n, _ in wl.kernels]
 
     def step(ev=None):
+        for i, (_, k) in enumerate(wl.kernels):
+            if ev is not None:
+                ev[i].record()
+            k()
         if ev is not None:
-            ev[0].record()
-        cg.sh_forward(vec, 3, out=y)
-        if ev is not None:
-            ev[1].record()
-        plan.conv_forward(G, x, y, w, scale, out=out)
-        if ev is not None:
-            ev[2].record()
-        plan.conv_backward(G, x, y, w, scale, g, out=(gx, gy, gw))
-        if ev is not None:
-            ev[3].record()
-        cg.sh_backward(vec, gy, 3, out=gvec)
-        if ev is not None:
-            ev[4].record()
+            ev[-1].record()
 
-    plan.compile()
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    nk = len(wl.kernels)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)]
+           for _ in range(args.steps)]
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if dist:
         dist.barrier()
@@ -207,36 +357,27 @@ def run_gpu(args):
     launches = cg.launch_count() - launches0
     if dist:
         dist.barrier()
-    ms_total = start.elapsed_time(stop)
+    ms_step = max_over_ranks(dist, start.elapsed_time(stop)) / args.steps
     per = {n: float(np.mean([evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(args.steps)]))
            for i, n in enumerate(names)}
-    if dist:
-        t = torch.tensor([ms_total], dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
-    ms_step = ms_total / args.steps
-
-    # ---- e2e: host buffers, copies inside the timed region
-    e2e = None if args.no_e2e else run_e2e(args, plan, G, cfg, g, scale, N, E)
-
+    e2e = None
+    if wl.e2e is not None and not args.no_e2e:
+        e2e = run_e2e(args, wl)
     if rank != 0:
         return None
-    import oracle as O
-    prob = O.make_problem(*cfg["irreps"])
-    counts = algorithmic_counts(prob, N, E)
+
     peaks = _peaks()
     fp32_peak = SM_COUNT * FP32_LANES_PER_SM * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12  # TFLOP/s
     kernels = {}
     for n in names:
-        c = counts[n]
+        nbytes, flops = wl.counts[n]
         t = per[n] * 1e-3
-        gbs = c["bytes"] / t / 1e9
+        gbs = nbytes / t / 1e9
         ent = {"ms": per[n], "hbm_gbs": gbs, "hbm_frac": gbs / peaks["hbm"]}
-        if c["flops"]:
-            tf = c["flops"] / t / 1e12
-            ent.update(tflops=tf, alu_frac=tf / fp32_peak)
-            t_hbm = c["bytes"] / (peaks["hbm"] * 1e9)
-            t_alu = c["flops"] / (fp32_peak * 1e12)
+        if flops:
+            tf = flops / t / 1e12
+            ent.update(tflops=tf, fp32_frac=tf / fp32_peak)
+            t_hbm, t_alu = nbytes / (peaks["hbm"] * 1e9), flops / (fp32_peak * 1e12)
             ent["bound"] = "hbm" if t_hbm >= t_alu else "alu"
             ent["roofline_frac"] = max(t_hbm, t_alu) / t
         else:
@@ -251,75 +392,50 @@ def run_gpu(args):
     else:
         roof = {"bound": "hbm", "achieved": kd["hbm_gbs"], "peak": peaks["hbm"], "unit": "GB/s",
                 "frac": kd["hbm_gbs"] / peaks["hbm"]}
-    roof.update(kernel=dom, traffic=_traffic(dom, plan),
-                peak_source=f"{peaks['src']} (HBM copy; FP32 = 152 SM x 128 FMA x 2 x "
-                            f"{peaks['sm_max_mhz']:.0f} MHz)")
+    roof.update(kernel=dom, traffic=_traffic(args.workload, dom),
+                peak_source=f"{peaks['src']} (HBM: copy bandwidth; FP32 ALU: 152 SM x 128 FMA "
+                            f"x 2 x {peaks['sm_max_mhz']:.0f} MHz)")
+    config = {"workload": wl.desc, **wl.cfg,
+              "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+              "l2": "inputs larger than L2 (weight stream per step >> 129 MB)"}
+    fwd_ms = sum(per[n] for n in wl.fwd_names)
     line = {
-        "metric": METRIC, "value": E * world / (ms_step * 1e-3), "unit": "edges/s",
+        "metric": METRIC, "value": wl.units * world / (ms_step * 1e-3), "unit": wl.unit,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-        "data": "synthetic (seeded periodic atom cloud, random radial-MLP weights)",
-        "config": {"workload": WORKLOAD if N == 10_000 else WORKLOAD.replace("N=10000", f"N={N}"),
-                   "N": N, "E": E, "mul": 64, "paths": plan.n_paths,
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "l2": "inputs larger than L2 (3.2 GB weight stream per step)"},
-        "fwd": {"value": E * world / (per["conv_fwd"] * 1e-3 + per["sh_fwd"] * 1e-3),
-                "unit": "edges/s", "conv_fwd_ms": per["conv_fwd"]},
-        "roofline": roof,
-        "kernels": kernels,
-        "gpu_launches": launches,
-        "clocks": clk.summary(),
-        "e2e": e2e,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
+        "data": "synthetic (seeded; see workloads/)", "config": config,
+        "fwd": {"value": wl.units * world / (fwd_ms * 1e-3), "unit": wl.unit, "ms": fwd_ms},
+        "roofline": roof, "kernels": kernels, "gpu_launches": launches,
+        "clocks": clk.summary(), "e2e": e2e,
     }
-    if not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(cfg, budget_s=args.cpu_seconds)
+    if not args.no_cpu_baseline and wl.oracle_step is not None:
+        line["cpu_baseline"] = cpu_baseline(wl, budget_s=args.cpu_seconds)
     return line
 
 
-def _traffic(kernel, plan):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current kernel source (else null)."""
-    import hashlib
+def _traffic(workload, kernel):
+    """DRAM bytes per launch from the committed ncu summary for this workload
+    and kernel, if recorded on the current kernel source (else null)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
-    d = json.load(open(p)).get(kernel)
+    d = json.load(open(p)).get(f"{workload}/{kernel}")
     if not d:
         return None
-    h = hashlib.sha256(plan.source().encode()).hexdigest()[:16]
-    return d.get("bytes") if d.get("source_sha") == h else None
+    import hashlib
+    src = os.path.join(ROOT, "clebsch_gordan_tensor_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in ("tp_kernels.cuh", "plan.cpp"):
+        h.update(open(os.path.join(src, f), "rb").read())
+    return d.get("bytes") if d.get("kernel_sha") == h.hexdigest()[:16] else None
 
 
-def run_e2e(args, plan, G, cfg, g, scale, N, E):
-    """Same step through the public API with host buffers: every step copies
-    its inputs (x, edge vectors, weights) from pinned host memory and reads the
-    results (output features and dL/dx) back."""
+def run_e2e(args, wl):
+    """The same step through the public API with host buffers: every step
+    copies its inputs from pinned host memory and reads its results back."""
     import torch
-
-    import clebsch_gordan_tensor_gb300 as cg
-    hx = torch.from_numpy(cfg["x"]).pin_memory()
-    hv = torch.from_numpy(cfg["vec"]).pin_memory()
-    hw = torch.from_numpy(cfg["w"]).pin_memory()
-    ho = torch.empty(N, plan.dim_out).pin_memory()
-    hgx = torch.empty(N, plan.dim_in1).pin_memory()
-    x, vec, w = (torch.empty_like(t, device="cuda") for t in (hx, hv, hw))
-    y = torch.empty(E, plan.dim_in2, device="cuda")
-    out = torch.empty(N, plan.dim_out, device="cuda")
-    gx, gy, gw = torch.empty_like(x), torch.empty_like(y), torch.empty_like(w)
-    gvec = torch.empty_like(vec)
-
-    def step():
-        x.copy_(hx, non_blocking=True)
-        vec.copy_(hv, non_blocking=True)
-        w.copy_(hw, non_blocking=True)
-        cg.sh_forward(vec, 3, out=y)
-        plan.conv_forward(G, x, y, w, scale, out=out)
-        plan.conv_backward(G, x, y, w, scale, g, out=(gx, gy, gw))
-        cg.sh_backward(vec, gy, 3, out=gvec)
-        ho.copy_(out, non_blocking=True)
-        hgx.copy_(gx, non_blocking=True)
-
-    for _ in range(max(1, args.warmup)):
+    step, h2d, d2h = wl.e2e()
+    for _ in range(max(1, min(args.warmup, 3))):
         step()
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -330,16 +446,14 @@ def run_e2e(args, plan, G, cfg, g, scale, N, E):
     b.record()
     torch.cuda.synchronize()
     ms = a.elapsed_time(b) / steps
-    h2d = sum(t.numel() * t.element_size() for t in (hx, hv, hw))
-    d2h = sum(t.numel() * t.element_size() for t in (ho, hgx))
-    return {"value": E / (ms * 1e-3), "unit": "edges/s", "ms_per_step": ms,
+    return {"value": wl.units / (ms * 1e-3), "unit": wl.unit, "ms_per_step": ms,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
 
 # ------------------------------------------------------------ CPU oracle
 
-def _oracle_subgraph_step(prob, cfg, R):
-    """Oracle forward + backward of the receivers [0, R) and their edges."""
+def _oracle_conv_step(prob, cfg, R, bwd=True):
+    """Oracle forward (+ backward) of the receivers [0, R) and their edges."""
     import oracle as O
     gr = cfg["graph"]
     e1 = int(gr.rowptr[R])
@@ -349,31 +463,41 @@ def _oracle_subgraph_step(prob, cfg, R):
     vec, w = cfg["vec"][:e1], cfg["w"][:e1]
     y = O.sh(3, vec)
     out = O.conv_forward(prob, rowptr, sender, cfg["x"], y, w, cfg["scale"])
-    g = np.ones_like(out)
-    _, gy, _ = O.conv_backward(prob, rowptr, sender, cfg["x"], y, w, cfg["scale"], g)
-    O.sh_vjp(3, vec, gy)
+    if bwd:
+        _, gy, _ = O.conv_backward(prob, rowptr, sender, cfg["x"], y, w, cfg["scale"],
+                                   np.ones_like(out))
+        O.sh_vjp(3, vec, gy)
     return e1
 
 
-def cpu_baseline(cfg, budget_s: float = 15.0, R0: int = 4):
-    """Time the oracle as it stands (single thread) on a bounded subgraph sized
-    to about ``budget_s`` seconds, reported in edges/s."""
+def _oracle_tp_step(prob, cfg, R):
     import oracle as O
-    prob = O.make_problem(*cfg["irreps"])
+    x, vec, w = cfg["x"][:R], cfg["vec"][:R], cfg["w"][:R]
+    y = O.sh(3, vec)
+    out = O.tp_forward(prob, x, y, w)
+    _, gy, _ = O.tp_backward(prob, x, y, w, np.ones_like(out))
+    O.sh_vjp(3, vec, gy)
+    return R
+
+
+def cpu_baseline(wl, budget_s: float = 15.0, R0: int = 4):
+    """The oracle as it stands (one host thread) on a bounded sample of the
+    same workload sized to about ``budget_s`` seconds."""
     t = time.perf_counter()
-    e = _oracle_subgraph_step(prob, cfg, R0)
+    wl.oracle_step(R0)
     dt = time.perf_counter() - t
-    R = int(max(R0, min(cfg["graph"].N, R0 * budget_s / max(dt, 1e-3))))
+    R = int(max(R0, R0 * budget_s / max(dt, 1e-3)))
+    R = min(R, wl.cfg.get("N", wl.cfg.get("B", R)))
     t = time.perf_counter()
-    e = _oracle_subgraph_step(prob, cfg, R)
+    units = wl.oracle_step(R)
     dt = time.perf_counter() - t
-    return {"value": e / dt, "unit": "edges/s", "cores": 1, "kind": "oracle",
-            "sample": f"fwd+bwd (SH, conv fwd, conv bwd, SH bwd) of receivers 0..{R - 1} "
-                      f"({e} edges) of the same workload, {dt:.1f} s on 1 host thread"}
+    return {"value": units / dt, "unit": wl.unit, "cores": 1, "kind": "oracle",
+            "sample": f"the same step on items 0..{R - 1} ({units} {wl.unit.split('/')[0]}) of "
+                      f"the workload, {dt:.1f} s on 1 host thread"}
 
 
 def run_reference(args):
-    dist, rank, world = _dist()
+    dist, rank, world = dist_setup()
     if rank != 0:
         return None
     import oracle as O
@@ -382,20 +506,23 @@ def run_reference(args):
     prob = O.make_problem(*cfg["irreps"])
     R = 24
     for _ in range(args.warmup):
-        _oracle_subgraph_step(prob, cfg, 4)
+        _oracle_conv_step(prob, cfg, 4)
     t = time.perf_counter()
     edges = 0
     for _ in range(args.steps):
-        edges += _oracle_subgraph_step(prob, cfg, R)
+        edges += _oracle_conv_step(prob, cfg, R)
     dt = time.perf_counter() - t
     v = edges / dt
+    desc = ("fused CG-TP conv: N=10000 atoms, density 0.1/A^3, cutoff 5 A, 64x(0e,1o,2e) (x) "
+            "Y(l<=3) -> 64x(0e,1o,1e,2o,2e,3o,3e), 24 uvu paths, fp32")
     return {"impl": "reference", "metric": METRIC, "value": v, "unit": "edges/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "N": cfg["graph"].N, "E": cfg["graph"].E},
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded; see workloads/)",
+            "config": {"workload": desc, "N": cfg["graph"].N, "E": cfg["graph"].E},
             "cpu_baseline": {"value": v, "unit": "edges/s", "cores": 1, "kind": "oracle",
-                             "sample": f"per step: receivers 0..{R - 1} and their edges"},
+                             "sample": f"per step: receivers 0..{R - 1} and their edges "
+                                       f"(fwd + bwd), 1 host thread"},
             "e2e": {"value": v, "unit": "edges/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
 
@@ -403,13 +530,15 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="conv", choices=sorted(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--atoms", type=int, default=10_000,
-                    help="atom count (10000 is the benchmark workload; smaller for profiling)")
+                    help="atom count of the conv workload (10000 is the benchmark; smaller "
+                         "for profiling)")
     ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args()
     line = run_reference(args) if args.impl == "reference" else run_gpu(args)

@@ -313,7 +313,7 @@ cgtp_status build_plan(Plan& p, const char* s1, const char* s2, const char* so,
     const int nt = (int)p.T.size();
     const size_t vr = p.cpt == 2 ? 8 : (p.dtype == CGTP_F64 ? 8 : 4);
     auto smem = [&](int slots) {
-        const size_t ntp = std::max(2, nt + (nt & 1));
+        const size_t ntp = std::max(4, (nt + 3) / 4 * 4);
         const size_t nyp = next_pow2(std::max(1, p.ny));
         const size_t real = p.dtype == CGTP_F64 ? 8 : 4;
         return slots * (ntp * vr + nyp * real + (p.lanes > 32 ? (p.lanes / 32) * nyp * real : 0));
@@ -343,8 +343,11 @@ cgtp_status build_plan(Plan& p, const char* s1, const char* s2, const char* so,
             cf[q] = nTp[q] + std::min(d1, d3);
             cb[q] = 2.0 * (nTp[q] + 3 * d1) + 2.0 * nTp[q] + nnzp[q];
         }
-        const int G = std::max(1, std::min(4, 128 / p.lanes));
-        auto lpt = [&](const std::vector<double>& c) {
+        // flags (0 = automatic): bits 0-3 forward warp groups, 4-7 backward
+        // warp groups, 8-11 forward ring depth, 12-15 backward ring depth
+        const int ovr_gf = (int)(p.flags & 15u), ovr_gb = (int)((p.flags >> 4) & 15u);
+        const int ovr_sf = (int)((p.flags >> 8) & 15u), ovr_sb = (int)((p.flags >> 12) & 15u);
+        auto lpt = [&](const std::vector<double>& c, int G) {
             std::vector<int> order(c.size());
             for (size_t i = 0; i < order.size(); ++i) order[i] = (int)i;
             std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return c[a] > c[b]; });
@@ -358,33 +361,29 @@ cgtp_status build_plan(Plan& p, const char* s1, const char* s2, const char* so,
             for (auto& v : grp) std::sort(v.begin(), v.end());
             return grp;
         };
-        p.fwd_groups = lpt(cf);
-        p.bwd_groups = lpt(cb);
-        // Ring depth: keep the CTAs that fit one SM (4 forward, 2 backward CTAs
-        // of 128 threads, the register-limited counts) streaming ~130-170 KB,
-        // i.e. several microseconds of HBM latency ahead of the FMA stream.
-        const size_t stat = (size_t)std::max(2, nt + (nt & 1)) * vr + 2048;
+        p.fwd_groups = lpt(cf, std::min(4, ovr_gf ? ovr_gf : 1));
+        p.bwd_groups = lpt(cb, std::min(4, ovr_gb ? ovr_gb : 1));
+        // Ring depth and groups: on the 10k-atom convolution the fastest shape
+        // was one warp group per CTA with a 2-deep ring (more resident CTAs beat
+        // deeper prefetch); flags override both.
+        const size_t stat = (size_t)std::max(4, (nt + 3) / 4 * 4) * es + 2048;
         const size_t fst = WB + XB + YB, bst = WB + GB + YB + 16;
         const size_t budget = 216 * 1024;
+        const size_t fbuf = p.fwd_groups.size() > 1 ? GB : 0;
+        const size_t bbuf = 2 * XB + (p.bwd_groups.size() > 1 ? XB : 0);
         auto depth = [&](size_t stage, size_t extra, int ctas) {
             const long long room = (long long)(budget / ctas) - (long long)(extra + stat);
-            return (int)std::max<long long>(0, std::min<long long>(12, room / (long long)stage));
+            return (int)std::max<long long>(0, std::min<long long>(15, room / (long long)stage));
         };
-        auto pick = [&](size_t stage, size_t extra, std::initializer_list<int> ks) {
-            int best = 0;
-            for (int k : ks) {  // most CTAs per SM that still keep a ring of >= 4 edges
-                best = depth(stage, extra, k);
-                if (best >= 4) break;
-            }
-            return best;
-        };
-        const int sf = pick(fst, GB, {4, 3, 2, 1}), sb = pick(bst, 3 * XB, {2, 1});
+        int sf = std::min(2, depth(fst, fbuf, 1)), sb = std::min(2, depth(bst, bbuf, 1));
+        if (ovr_sf) sf = std::max(2, std::min(ovr_sf, depth(fst, fbuf, 1)));
+        if (ovr_sb) sb = std::max(2, std::min(ovr_sb, depth(bst, bbuf, 1)));
         if (sf >= 2 && sb >= 2) {
             p.staged = true;
             p.stages_f = sf;
             p.stages_b = sb;
-            p.fwd_smem = sf * fst + GB;
-            p.bwd_smem = sb * bst + 3 * XB;
+            p.fwd_smem = sf * fst + fbuf;
+            p.bwd_smem = sb * bst + bbuf;
         }
     }
     return CGTP_OK;
@@ -414,24 +413,27 @@ struct TLoader {
     int cpt;
     std::vector<bool> loaded;
     std::ostringstream* os;
+    bool f64 = false;
+    // T entries are stored as scalars; with two fp32 channels per lane four of
+    // them come in one 128-bit shared load and each is splatted into a pair.
     std::string get(int k) {
         if (cpt != 2) return "Ts[" + std::to_string(k) + "]";
-        const int q = k / 2;
+        const int q = k / 4;
         if (!loaded[q]) {
-            *os << "    const ulonglong2 tq" << q << " = Tq[" << q << "];\n";
+            *os << "    const float4 tq" << q << " = Tq[" << q << "];\n";
             loaded[q] = true;
         }
-        return "tq" + std::to_string(q) + (k % 2 ? ".y" : ".x");
+        static const char* comp[4] = {".x", ".y", ".z", ".w"};
+        return "vsplat(tq" + std::to_string(q) + comp[k % 4] + ")";
     }
 };
-
 
 // Per-group streams of the staged kernels.  Group g of the forward owns the
 // paths fwd_groups[g]; its accumulators cover only the output rows those paths
 // touch and its x registers only the rows they read.  The backward groups keep
 // x rows and partial grad_x for their paths' input rows.
 void Plan::gen_groups(std::ostringstream& g, const std::vector<int>& k0, bool f64) const {
-    const int ntp = std::max(2, (int)T.size() + ((int)T.size() & 1));
+    const int ntp = std::max(4, ((int)T.size() + 3) / 4 * 4);
     auto emit_tloader = [&](TLoader& L) { std::fill(L.loaded.begin(), L.loaded.end(), false); };
     // ---------------------------------------------------------------- forward
     g << "template <int GRP> struct FwdG;\n";
@@ -458,9 +460,9 @@ void Plan::gen_groups(std::ostringstream& g, const std::vector<int>& k0, bool f6
             g << "    xr[" << i << "] = lds_v(xs + " << xrows[i] << " * MUL, ch);\n";
         g << "  }\n";
         g << "  template <class FW>\n  __device__ static __forceinline__ void edge(VR (&acc)[NR], "
-             "const VR* __restrict__ Ts, const VR (&xr)[NXR], FW&& W) {\n";
-        if (cpt == 2) g << "    const ulonglong2* __restrict__ Tq = reinterpret_cast<const ulonglong2*>(Ts);\n";
-        TLoader L{cpt, std::vector<bool>(ntp / 2 + 1, false), &g};
+             "const REAL* __restrict__ Ts, const VR (&xr)[NXR], FW&& W) {\n";
+        if (cpt == 2) g << "    const float4* __restrict__ Tq = reinterpret_cast<const float4*>(Ts);\n";
+        TLoader L{cpt, std::vector<bool>(ntp / 4 + 1, false), &g};
         for (int q : P_) {
             const Path& P = paths[q];
             const int d1 = 2 * P.l1 + 1, d3 = 2 * P.l3 + 1;
@@ -504,6 +506,13 @@ void Plan::gen_groups(std::ostringstream& g, const std::vector<int>& k0, bool f6
             else
                 g << "    stv(buf + " << r << " * MUL, ch, vzero());\n";
         }
+        g << "  }\n  __device__ static __forceinline__ void store(REAL* orow, const VR (&acc)[NR], int ch, "
+             "VR sc, int accumulate) {\n";
+        for (int r = 0; r < no; ++r) {
+            const std::string v = ri.count(r) ? "vmul(acc[" + std::to_string(ri[r]) + "], sc)" : "vzero()";
+            g << "    { VR v = " << v << "; if (accumulate) v = vadd(v, ldv_plain(orow + " << r
+              << " * MUL, ch)); stv(orow + " << r << " * MUL, ch, v); }\n";
+        }
         g << "  }\n  __device__ static __forceinline__ void add(REAL* buf, const VR (&acc)[NR], int ch) {\n";
         for (size_t i = 0; i < rows.size(); ++i)
             g << "    stv(buf + " << rows[i] << " * MUL, ch, vadd(lds_v(buf + " << rows[i]
@@ -528,10 +537,10 @@ void Plan::gen_groups(std::ostringstream& g, const std::vector<int>& k0, bool f6
             g << "    xr[" << i << "] = lds_v(xs + " << xrows[i] << " * MUL, ch);\n";
         g << "  }\n";
         g << "  template <bool GY, class FG, class FW>\n  __device__ static __forceinline__ void edge("
-             "VR (&gxa)[NXR], REAL (&gyl)[NYP], const VR* __restrict__ Ts, const VR (&xr)[NXR],\n"
+             "VR (&gxa)[NXR], REAL (&gyl)[NYP], const REAL* __restrict__ Ts, const VR (&xr)[NXR],\n"
              "      FG&& G, FW&& W, REAL* __restrict__ gwrow, int ch, VR sc, bool dogx, int mgw) {\n";
-        if (cpt == 2) g << "    const ulonglong2* __restrict__ Tq = reinterpret_cast<const ulonglong2*>(Ts);\n";
-        TLoader L{cpt, std::vector<bool>(ntp / 2 + 1, false), &g};
+        if (cpt == 2) g << "    const float4* __restrict__ Tq = reinterpret_cast<const float4*>(Ts);\n";
+        TLoader L{cpt, std::vector<bool>(ntp / 4 + 1, false), &g};
         for (int q : P_) {
             const Path& P = paths[q];
             const int d1 = 2 * P.l1 + 1, d3 = 2 * P.l3 + 1;
@@ -597,6 +606,13 @@ void Plan::gen_groups(std::ostringstream& g, const std::vector<int>& k0, bool f6
             else
                 g << "    stv(buf + " << r << " * MUL, ch, vzero());\n";
         }
+        g << "  }\n  __device__ static __forceinline__ void store(REAL* orow, const VR (&gxa)[NXR], int ch, "
+             "VR sc, int mode) {\n";
+        for (int r = 0; r < nx; ++r) {
+            const std::string v = xi.count(r) ? "vmul(gxa[" + std::to_string(xi[r]) + "], sc)" : "vzero()";
+            g << "    { VR v = " << v << "; if (mode == 2) v = vadd(v, ldv_plain(orow + " << r
+              << " * MUL, ch)); stv(orow + " << r << " * MUL, ch, v); }\n";
+        }
         g << "  }\n  __device__ static __forceinline__ void add(REAL* buf, const VR (&gxa)[NXR], int ch) {\n";
         for (size_t i = 0; i < xrows.size(); ++i)
             g << "    stv(buf + " << xrows[i] << " * MUL, ch, vadd(lds_v(buf + " << xrows[i]
@@ -608,7 +624,7 @@ void Plan::gen_groups(std::ostringstream& g, const std::vector<int>& k0, bool f6
 std::string Plan::kernel_source() const {
     const bool f64 = dtype == CGTP_F64;
     const int nt = (int)T.size();
-    const int ntp = std::max(2, nt + (nt & 1));
+    const int ntp = std::max(4, (nt + 3) / 4 * 4);
     const int nyp = next_pow2(std::max(1, ny));
     std::ostringstream os;
     os << "// generated for " << s1 << " (x) " << s2 << " -> " << so << ", " << paths.size()
@@ -658,10 +674,10 @@ std::string Plan::kernel_source() const {
     std::ostringstream g;
     // ---- forward stream
     g << "template <class FX, class FW>\n__device__ __forceinline__ void gen_fwd(VR (&acc)[NO],\n"
-         "    const VR* __restrict__ Ts, FX&& X, FW&& W) {\n";
-    if (cpt == 2) g << "    const ulonglong2* __restrict__ Tq = reinterpret_cast<const ulonglong2*>(Ts);\n";
+         "    const REAL* __restrict__ Ts, FX&& X, FW&& W) {\n";
+    if (cpt == 2) g << "    const float4* __restrict__ Tq = reinterpret_cast<const float4*>(Ts);\n";
     {
-        TLoader L{cpt, std::vector<bool>(ntp / 2 + 1, false), &g};
+        TLoader L{cpt, std::vector<bool>(ntp / 4 + 1, false), &g};
         for (int q = 0; q < (int)paths.size(); ++q) {
             const Path& P = paths[q];
             const int d1 = 2 * P.l1 + 1, d3 = 2 * P.l3 + 1;
@@ -701,11 +717,11 @@ std::string Plan::kernel_source() const {
 
     // ---- backward stream
     g << "template <bool GY, class FX, class FG, class FW>\n__device__ __forceinline__ void gen_bwd(\n"
-         "    VR (&gxa)[NX], REAL (&gyl)[NYP], const VR* __restrict__ Ts, FX&& X, FG&& G, FW&& W,\n"
+         "    VR (&gxa)[NX], REAL (&gyl)[NYP], const REAL* __restrict__ Ts, FX&& X, FG&& G, FW&& W,\n"
          "    REAL* __restrict__ gwrow, int ch, VR sc, bool dogx, int mgw) {\n";
-    if (cpt == 2) g << "    const ulonglong2* __restrict__ Tq = reinterpret_cast<const ulonglong2*>(Ts);\n";
+    if (cpt == 2) g << "    const float4* __restrict__ Tq = reinterpret_cast<const float4*>(Ts);\n";
     {
-        TLoader L{cpt, std::vector<bool>(ntp / 2 + 1, false), &g};
+        TLoader L{cpt, std::vector<bool>(ntp / 4 + 1, false), &g};
         for (int q = 0; q < (int)paths.size(); ++q) {
             const Path& P = paths[q];
             const int d1 = 2 * P.l1 + 1, d3 = 2 * P.l3 + 1;

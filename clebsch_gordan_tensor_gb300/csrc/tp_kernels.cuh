@@ -109,13 +109,13 @@ __device__ __forceinline__ void slot_sync(int slot) {
 #endif
 
 // Per-edge T entries, lane-strided over the slot.  Ys holds the edge's y row.
-__device__ __forceinline__ void build_T(VR* __restrict__ Ts, const REAL* __restrict__ Ys, int lane) {
+__device__ __forceinline__ void build_T(REAL* __restrict__ Ts, const REAL* __restrict__ Ys, int lane) {
     for (int k = lane; k < NT; k += LANES) {
         REAL t = (REAL)0;
 #pragma unroll
         for (int q = 0; q < MAXTERMS; ++q)
             t = fma(T_CO[k * MAXTERMS + q], Ys[T_IDX[k * MAXTERMS + q]], t);
-        Ts[k] = vsplat(t);
+        Ts[k] = t;
     }
 }
 
@@ -162,10 +162,10 @@ __device__ __forceinline__ void fwd_body(long long n_items, const int* __restric
                                          const REAL* __restrict__ x, const REAL* __restrict__ y,
                                          const REAL* __restrict__ w, long long w_stride,
                                          REAL* __restrict__ out, REAL scale, int accumulate) {
-    __shared__ __align__(16) VR Ts_all[SLOTS][NTP];
+    __shared__ __align__(16) REAL Ts_all[SLOTS][NTP];
     __shared__ __align__(16) REAL Ys_all[SLOTS][NYP];
     const int slot = threadIdx.x / LANES, lane = threadIdx.x % LANES;
-    VR* Ts = Ts_all[slot];
+    REAL* Ts = Ts_all[slot];
     REAL* Ys = Ys_all[slot];
     const int ch = lane;
     for (long long item = (long long)blockIdx.x * SLOTS + slot; item < n_items;
@@ -264,13 +264,13 @@ __device__ __forceinline__ void bwd_body(long long n_items, const int* __restric
                                          const REAL* __restrict__ g, REAL scale,
                                          REAL* __restrict__ gx, REAL* __restrict__ gy,
                                          REAL* __restrict__ gw, int mgx, int mgy, int mgw) {
-    __shared__ __align__(16) VR Ts_all[SLOTS][NTP];
+    __shared__ __align__(16) REAL Ts_all[SLOTS][NTP];
     __shared__ __align__(16) REAL Ys_all[SLOTS][NYP];
 #if LANES > 32
     __shared__ REAL Gy_all[SLOTS][LANES / 32][NYP];
 #endif
     const int slot = threadIdx.x / LANES, lane = threadIdx.x % LANES;
-    VR* Ts = Ts_all[slot];
+    REAL* Ts = Ts_all[slot];
     REAL* Ys = Ys_all[slot];
     const int ch = lane;
     const VR sc = vsplat(scale);
@@ -518,7 +518,7 @@ __device__ __noinline__ void fail_and_drain(int code, unsigned long long* bars, 
 
 // T entries of one edge, computed by all NTHR threads of the CTA.
 template <int NTHR>
-__device__ __forceinline__ void build_T_cta(VR* __restrict__ Ts, const REAL* __restrict__ Ys) {
+__device__ __forceinline__ void build_T_cta(REAL* __restrict__ Ts, const REAL* __restrict__ Ys) {
     constexpr int ROUNDS = (NT + NTHR - 1) / NTHR;
     REAL t[ROUNDS];
 #pragma unroll
@@ -534,7 +534,7 @@ __device__ __forceinline__ void build_T_cta(VR* __restrict__ Ts, const REAL* __r
 #pragma unroll
     for (int r = 0; r < ROUNDS; ++r) {
         const int k = threadIdx.x + r * NTHR;
-        if (k < NT) Ts[k] = vsplat(t[r]);
+        if (k < NT) Ts[k] = t[r];
     }
 }
 
@@ -594,7 +594,7 @@ struct FwdShared {
     unsigned char* stages;
     REAL* buf;
     unsigned long long* full;
-    VR* Ts;
+    REAL* Ts;
     long long i0, i1, e_begin, e_end;
 };
 
@@ -643,22 +643,26 @@ __device__ __forceinline__ void fwd_group(const FwdArgs& A, const FwdShared& S, 
             if constexpr (GRP == 0)
                 if (tid < 32 && j + STAGES_F < S.e_end) fwd_issue<CONV>(A, S, win, j + STAGES_F);
         }
-        // partial sums of the groups, added in group order
-        if constexpr (GRP == 0) FG::first(S.buf, acc, ch);
-        cta_sync();
+        REAL* orow = A.out + item * DIMO;
+        if constexpr (GF == 1) {
+            FG::store(orow, acc, ch, sc, A.accumulate);
+        } else {
+            // partial sums of the groups, added in group order
+            if constexpr (GRP == 0) FG::first(S.buf, acc, ch);
+            cta_sync();
 #pragma unroll
-        for (int g = 1; g < GF; ++g) {
-            if (g == GRP) FG::add(S.buf, acc, ch);
+            for (int g = 1; g < GF; ++g) {
+                if (g == GRP) FG::add(S.buf, acc, ch);
+                cta_sync();
+            }
+            for (int i = tid; i < NO * NCH; i += NTF) {
+                const int r = i / NCH, c = i % NCH;
+                VR v = vmul(lds_v(S.buf + r * MUL, c), sc);
+                if (A.accumulate) v = vadd(v, ldv_plain(orow + r * MUL, c));
+                stv(orow + r * MUL, c, v);
+            }
             cta_sync();
         }
-        REAL* orow = A.out + item * DIMO;
-        for (int i = tid; i < NO * NCH; i += NTF) {
-            const int r = i / NCH, c = i % NCH;
-            VR v = vmul(lds_v(S.buf + r * MUL, c), sc);
-            if (A.accumulate) v = vadd(v, ldv_plain(orow + r * MUL, c));
-            stv(orow + r * MUL, c, v);
-        }
-        cta_sync();
     }
 }
 
@@ -666,7 +670,7 @@ template <bool CONV>
 __device__ __forceinline__ void fwd_staged(const FwdArgs& A) {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ __align__(8) unsigned long long full[STAGES_F];
-    __shared__ __align__(16) VR Ts[NTP];
+    __shared__ __align__(16) REAL Ts[NTP];
     FwdShared S;
     cta_items(CONV ? A.rowptr : nullptr, A.n_items, S.i0, S.i1);
     if (S.i0 >= S.i1) return;
@@ -748,7 +752,7 @@ struct BwdShared {
     REAL* buf;
     unsigned long long* full;
     unsigned long long* xfull;
-    VR* Ts;
+    REAL* Ts;
     REAL (*gyS)[NYP];
     long long i0, i1, j_begin, j_end;
 };
@@ -842,21 +846,25 @@ __device__ __forceinline__ void bwd_group(const BwdArgs& A, const BwdShared& S, 
                 if (tid < 32 && j + STAGES_B < S.j_end) bwd_issue<CONV>(A, S, we, wn, j + STAGES_B);
         }
         if (A.mgx) {
-            if constexpr (GRP == 0) BG::first(S.buf, gxa, ch);
-            cta_sync();
+            REAL* orow = A.gx + item * DIMX;
+            if constexpr (GB == 1) {
+                BG::store(orow, gxa, ch, sc, A.mgx);
+            } else {
+                if constexpr (GRP == 0) BG::first(S.buf, gxa, ch);
+                cta_sync();
 #pragma unroll
-            for (int g = 1; g < GB; ++g) {
-                if (g == GRP) BG::add(S.buf, gxa, ch);
+                for (int g = 1; g < GB; ++g) {
+                    if (g == GRP) BG::add(S.buf, gxa, ch);
+                    cta_sync();
+                }
+                for (int i = tid; i < NX * NCH; i += NTB) {
+                    const int r = i / NCH, c = i % NCH;
+                    VR v = vmul(lds_v(S.buf + r * MUL, c), sc);
+                    if (A.mgx == 2) v = vadd(v, ldv_plain(orow + r * MUL, c));
+                    stv(orow + r * MUL, c, v);
+                }
                 cta_sync();
             }
-            REAL* orow = A.gx + item * DIMX;
-            for (int i = tid; i < NX * NCH; i += NTB) {
-                const int r = i / NCH, c = i % NCH;
-                VR v = vmul(lds_v(S.buf + r * MUL, c), sc);
-                if (A.mgx == 2) v = vadd(v, ldv_plain(orow + r * MUL, c));
-                stv(orow + r * MUL, c, v);
-            }
-            cta_sync();
         }
     }
 }
@@ -866,7 +874,7 @@ __device__ __forceinline__ void bwd_staged(const BwdArgs& A) {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ __align__(8) unsigned long long full[STAGES_B];
     __shared__ __align__(8) unsigned long long xfull[2];
-    __shared__ __align__(16) VR Ts[NTP];
+    __shared__ __align__(16) REAL Ts[NTP];
     __shared__ REAL gyS[NWB][NYP];
     BwdShared S;
     cta_items(CONV ? A.s_rowptr : nullptr, A.n_items, S.i0, S.i1);

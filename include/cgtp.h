@@ -85,7 +85,10 @@ typedef struct {
  * coefficients (complex CG by the angular-momentum lowering recursion, taken to
  * the real basis) and lay out the per-path work.  Host only; no GPU needed.
  * irreps_in2 must have mul 1 per irrep (spherical harmonics); in1 and out must
- * share one mul.  l <= 6.  flags: reserved, pass 0. */
+ * share one mul.  l <= 6.
+ * flags: 0 for automatic tuning, else overrides of the staged kernels' launch
+ * shape: bits 0-3 forward warp groups (1-4), bits 4-7 backward warp groups,
+ * bits 8-11 forward TMA ring depth (2-15), bits 12-15 backward ring depth. */
 cgtp_status cgtp_plan_create(cgtp_plan* out, const char* irreps_in1, const char* irreps_in2,
                              const char* irreps_out, const cgtp_instr* instr, int n_instr,
                              cgtp_dtype dtype, cgtp_wmode wmode, unsigned flags);
