@@ -367,7 +367,15 @@ cgtp_status build_plan(Plan& p, const char* s1, const char* s2, const char* so,
         // was one warp group per CTA with a 2-deep ring (more resident CTAs beat
         // deeper prefetch); flags override both.
         const size_t stat = (size_t)std::max(4, (nt + 3) / 4 * 4) * es + 2048;
-        const size_t fst = WB + XB + YB, bst = WB + GB + YB + 16;
+        // Weights loaded by the lanes (prefetched one edge ahead in registers)
+        // instead of through the ring: default for the backward (its ring then
+        // carries only the gathered gradient row), not for the forward (its
+        // registers limit residency first).  Flag bit 16 turns it on for the
+        // forward, bit 17 off for the backward; it needs a single warp group.
+        p.w_direct_f = ((p.flags >> 16) & 1u) && p.fwd_groups.size() == 1;
+        p.w_direct_b = !((p.flags >> 17) & 1u) && p.bwd_groups.size() == 1;
+        const size_t fst = (p.w_direct_f ? 0 : WB) + XB + YB;
+        const size_t bst = (p.w_direct_b ? 0 : WB) + GB + YB + 16;
         const size_t budget = 216 * 1024;
         const size_t fbuf = p.fwd_groups.size() > 1 ? GB : 0;
         const size_t bbuf = 2 * XB + (p.bwd_groups.size() > 1 ? XB : 0);
@@ -413,11 +421,19 @@ struct TLoader {
     int cpt;
     std::vector<bool> loaded;
     std::ostringstream* os;
-    bool f64 = false;
+    bool dup = false;  // entries stored as splatted pairs (two per 128-bit load)
     // T entries are stored as scalars; with two fp32 channels per lane four of
     // them come in one 128-bit shared load and each is splatted into a pair.
     std::string get(int k) {
         if (cpt != 2) return "Ts[" + std::to_string(k) + "]";
+        if (dup) {
+            const int q = k / 2;
+            if (!loaded[q]) {
+                *os << "    const ulonglong2 tp" << q << " = Tp[" << q << "];\n";
+                loaded[q] = true;
+            }
+            return "tp" + std::to_string(q) + (k % 2 ? ".y" : ".x");
+        }
         const int q = k / 4;
         if (!loaded[q]) {
             *os << "    const float4 tq" << q << " = Tq[" << q << "];\n";
@@ -539,8 +555,10 @@ void Plan::gen_groups(std::ostringstream& g, const std::vector<int>& k0, bool f6
         g << "  template <bool GY, class FG, class FW>\n  __device__ static __forceinline__ void edge("
              "VR (&gxa)[NXR], REAL (&gyl)[NYP], const REAL* __restrict__ Ts, const VR (&xr)[NXR],\n"
              "      FG&& G, FW&& W, REAL* __restrict__ gwrow, int ch, VR sc, bool dogx, int mgw) {\n";
+        // T_DUP_B selects splatted pairs for the backward's T entries; scalar
+        // entries measured faster (fewer registers), so the default is 0.
         if (cpt == 2) g << "    const float4* __restrict__ Tq = reinterpret_cast<const float4*>(Ts);\n";
-        TLoader L{cpt, std::vector<bool>(ntp / 4 + 1, false), &g};
+        TLoader L{cpt, std::vector<bool>(ntp / 4 + 1, false), &g, false};
         for (int q : P_) {
             const Path& P = paths[q];
             const int d1 = 2 * P.l1 + 1, d3 = 2 * P.l3 + 1;
@@ -638,7 +656,8 @@ std::string Plan::kernel_source() const {
        << "\n#define NTP " << ntp << "\n#define MAXTERMS " << maxterms << "\n#define YPF "
        << (ny + lanes - 1) / lanes << "\n";
     os << "#define STAGED " << (staged ? 1 : 0) << "\n#define STAGES_F " << stages_f
-       << "\n#define STAGES_B " << stages_b
+       << "\n#define STAGES_B " << stages_b << "\n#define W_DIRECT_F " << (w_direct_f ? 1 : 0)
+       << "\n#define W_DIRECT_B " << (w_direct_b ? 1 : 0) << "\n#define T_DUP_B 0"
        << "\n#define GF " << std::max<size_t>(1, fwd_groups.size()) << "\n#define GB "
        << std::max<size_t>(1, bwd_groups.size()) << "\n";
     // T tables

@@ -64,6 +64,7 @@ struct Plan {
     // staged (TMA) kernels: one slot of `lanes` threads per CTA
     bool staged = false;
     int stages_f = 3, stages_b = 3;  // TMA ring depths (forward, backward)
+    bool w_direct_f = false, w_direct_b = false;  // weights bypass the ring
     size_t fwd_smem = 0, bwd_smem = 0;  // dynamic shared memory per CTA
     // warp groups of the staged kernels: each group of `lanes` threads runs the
     // generated stream of a subset of paths (longest-processing-time split)

@@ -516,8 +516,9 @@ __device__ __noinline__ void fail_and_drain(int code, unsigned long long* bars, 
         }
 }
 
-// T entries of one edge, computed by all NTHR threads of the CTA.
-template <int NTHR>
+// T entries of one edge, computed by all NTHR threads of the CTA; with DUP the
+// entries are stored as splatted register pairs (no unpacking in the stream).
+template <int NTHR, bool DUP = false>
 __device__ __forceinline__ void build_T_cta(REAL* __restrict__ Ts, const REAL* __restrict__ Ys) {
     constexpr int ROUNDS = (NT + NTHR - 1) / NTHR;
     REAL t[ROUNDS];
@@ -534,7 +535,12 @@ __device__ __forceinline__ void build_T_cta(REAL* __restrict__ Ts, const REAL* _
 #pragma unroll
     for (int r = 0; r < ROUNDS; ++r) {
         const int k = threadIdx.x + r * NTHR;
-        if (k < NT) Ts[k] = t[r];
+        if (k < NT) {
+            if constexpr (DUP)
+                reinterpret_cast<VR*>(Ts)[k] = vsplat(t[r]);
+            else
+                Ts[k] = t[r];
+        }
     }
 }
 
@@ -544,8 +550,13 @@ constexpr unsigned WB = (unsigned)(NP * MUL) * SZ;
 constexpr unsigned XB = (unsigned)(NX * MUL) * SZ;
 constexpr unsigned GB_ = (unsigned)(NO * MUL) * SZ;
 constexpr unsigned YB = (unsigned)NY * SZ;
-constexpr unsigned FWD_STAGE = WB + XB + YB;
-constexpr unsigned BWD_STAGE = WB + GB_ + YB + 16;
+// With W_DIRECT_* the lanes load their weight pairs straight from global
+// memory (prefetched one edge ahead in registers) and the ring carries only the
+// gathered row and y.
+constexpr unsigned WSF = W_DIRECT_F ? 0u : WB;  // weight bytes in a forward stage
+constexpr unsigned WSB = W_DIRECT_B ? 0u : WB;  // weight bytes in a backward stage
+constexpr unsigned FWD_STAGE = WSF + XB + YB;
+constexpr unsigned BWD_STAGE = WSB + GB_ + YB + 16;
 constexpr int NTF = GF * LANES;  // threads of a forward CTA
 constexpr int NTB = GB * LANES;  // threads of a backward CTA
 
@@ -607,9 +618,9 @@ __device__ __forceinline__ void fwd_issue(const FwdArgs& A, const FwdShared& S, 
         unsigned char* st = S.stages + (size_t)((j - S.e_begin) % STAGES_F) * FWD_STAGE;
         unsigned long long* b = &S.full[(j - S.e_begin) % STAGES_F];
         mbar_expect_tx(b, FWD_STAGE);
-        bulk_g2s(st, A.w + j * A.w_stride, WB, b);
-        bulk_g2s(st + WB, A.x + src * DIMX, XB, b);
-        bulk_g2s(st + WB + XB, A.y + j * NY, YB, b);
+        if (!W_DIRECT_F) bulk_g2s(st, A.w + j * A.w_stride, WB, b);
+        bulk_g2s(st + WSF, A.x + src * DIMX, XB, b);
+        bulk_g2s(st + WSF + XB, A.y + j * NY, YB, b);
     }
 }
 
@@ -619,6 +630,12 @@ __device__ __forceinline__ void fwd_group(const FwdArgs& A, const FwdShared& S, 
     const int tid = threadIdx.x, ch = tid % LANES;
     const VR sc = vsplat(A.scale);
     VR acc[FG::NR];
+#if W_DIRECT_F
+    VR wcur[NP], wnext[NP];
+    if (S.e_begin < S.e_end)
+#pragma unroll
+        for (int p = 0; p < NP; ++p) wnext[p] = ldv(A.w + S.e_begin * A.w_stride + p * MUL, ch);
+#endif
     long long j = S.e_begin;
     long long nend = CONV ? (long long)__ldg(A.rowptr + S.i0 + 1) : S.i0 + 1;
     for (long long item = S.i0; item < S.i1; ++item) {
@@ -630,15 +647,24 @@ __device__ __forceinline__ void fwd_group(const FwdArgs& A, const FwdShared& S, 
             const long long k = j - S.e_begin;
             const unsigned char* st = S.stages + (size_t)(k % STAGES_F) * FWD_STAGE;
             const bool ok = mbar_wait(&S.full[k % STAGES_F], (unsigned)((k / STAGES_F) & 1));
-            build_T_cta<NTF>(S.Ts, reinterpret_cast<const REAL*>(st + WB + XB));
+            build_T_cta<NTF>(S.Ts, reinterpret_cast<const REAL*>(st + WSF + XB));
             if (!cta_all(ok)) {
                 fail_and_drain(1, S.full, STAGES_F);
                 return;
             }
             VR xr[FG::NXR];
-            FG::loadx(xr, reinterpret_cast<const REAL*>(st + WB), ch);
+            FG::loadx(xr, reinterpret_cast<const REAL*>(st + WSF), ch);
+#if W_DIRECT_F
+#pragma unroll
+            for (int p = 0; p < NP; ++p) wcur[p] = wnext[p];
+            if (j + 1 < S.e_end)
+#pragma unroll
+                for (int p = 0; p < NP; ++p) wnext[p] = ldv(A.w + (j + 1) * A.w_stride + p * MUL, ch);
+            FG::edge(acc, S.Ts, xr, [&](int p) { return wcur[p]; });
+#else
             const REAL* ws = reinterpret_cast<const REAL*>(st);
             FG::edge(acc, S.Ts, xr, [&](int p) { return lds_v(ws + p * MUL, ch); });
+#endif
             cta_sync();
             if constexpr (GRP == 0)
                 if (tid < 32 && j + STAGES_F < S.e_end) fwd_issue<CONV>(A, S, win, j + STAGES_F);
@@ -765,11 +791,11 @@ __device__ __forceinline__ void bwd_issue(const BwdArgs& A, const BwdShared& S, 
     if (threadIdx.x == 0) {
         unsigned char* st = S.stages + (size_t)((j - S.j_begin) % STAGES_B) * BWD_STAGE;
         unsigned long long* b = &S.full[(j - S.j_begin) % STAGES_B];
-        *reinterpret_cast<int*>(st + WB + GB_ + YB) = (int)e;
-        mbar_expect_tx(b, WB + GB_ + YB);
-        bulk_g2s(st, A.w + e * A.w_stride, WB, b);
-        bulk_g2s(st + WB, A.g + n * DIMO, GB_, b);
-        bulk_g2s(st + WB + GB_, A.y + e * NY, YB, b);
+        *reinterpret_cast<int*>(st + WSB + GB_ + YB) = (int)e;
+        mbar_expect_tx(b, WSB + GB_ + YB);
+        if (!W_DIRECT_B) bulk_g2s(st, A.w + e * A.w_stride, WB, b);
+        bulk_g2s(st + WSB, A.g + n * DIMO, GB_, b);
+        bulk_g2s(st + WSB + GB_, A.y + e * NY, YB, b);
     }
 }
 
@@ -789,6 +815,16 @@ __device__ __forceinline__ void bwd_group(const BwdArgs& A, const BwdShared& S, 
     const VR sc = vsplat(A.scale);
     long long j = S.j_begin;
     long long nend = CONV ? (long long)__ldg(A.s_rowptr + S.i0 + 1) : S.i0 + 1;
+#if W_DIRECT_B
+    // edge ids come from the stage headers (written before the barrier that
+    // follows their issue); the first stage was issued before this loop
+    VR wcur[NP], wnext[NP];
+    if (S.j_begin < S.j_end) {
+        const long long e0 = *reinterpret_cast<const int*>(S.stages + WSB + GB_ + YB);
+#pragma unroll
+        for (int p = 0; p < NP; ++p) wnext[p] = ldv(A.w + e0 * A.w_stride + p * MUL, ch);
+    }
+#endif
     for (long long item = S.i0; item < S.i1; ++item) {
         const long long kk = item - S.i0;
         const long long e1 = nend;
@@ -808,23 +844,38 @@ __device__ __forceinline__ void bwd_group(const BwdArgs& A, const BwdShared& S, 
             const long long k = j - S.j_begin;
             const unsigned char* st = S.stages + (size_t)(k % STAGES_B) * BWD_STAGE;
             const bool ok = mbar_wait(&S.full[k % STAGES_B], (unsigned)((k / STAGES_B) & 1));
-            const long long e = *reinterpret_cast<const int*>(st + WB + GB_ + YB);
-            build_T_cta<NTB>(S.Ts, reinterpret_cast<const REAL*>(st + WB + GB_));
+            const long long e = *reinterpret_cast<const int*>(st + WSB + GB_ + YB);
+            build_T_cta<NTB, T_DUP_B && CPT == 2>(S.Ts, reinterpret_cast<const REAL*>(st + WSB + GB_));
             if (!cta_all(ok)) {
                 fail_and_drain(3, S.full, STAGES_B);
                 fail_and_drain(3, S.xfull, 2);
                 return;
             }
-            const REAL* gs = reinterpret_cast<const REAL*>(st + WB);
-            const REAL* ws = reinterpret_cast<const REAL*>(st);
+            const REAL* gs = reinterpret_cast<const REAL*>(st + WSB);
             REAL gyl[NYP];
 #pragma unroll
             for (int i = 0; i < NYP; ++i) gyl[i] = (REAL)0;
             REAL* gwrow = A.gw ? A.gw + e * WDIM : nullptr;
+#if W_DIRECT_B
+#pragma unroll
+            for (int p = 0; p < NP; ++p) wcur[p] = wnext[p];
+            if (j + 1 < S.j_end) {
+                const unsigned char* st1 = S.stages + (size_t)((k + 1) % STAGES_B) * BWD_STAGE;
+                const long long e1 = *reinterpret_cast<const int*>(st1 + WSB + GB_ + YB);
+#pragma unroll
+                for (int p = 0; p < NP; ++p) wnext[p] = ldv(A.w + e1 * A.w_stride + p * MUL, ch);
+            }
+            BG::template edge<GY>(gxa, gyl, S.Ts, xr,
+                                  [&](int r) { return lds_v(gs + r * MUL, ch); },
+                                  [&](int p) { return wcur[p]; }, gwrow, ch, sc, A.mgx != 0,
+                                  A.mgw);
+#else
+            const REAL* ws = reinterpret_cast<const REAL*>(st);
             BG::template edge<GY>(gxa, gyl, S.Ts, xr,
                                   [&](int r) { return lds_v(gs + r * MUL, ch); },
                                   [&](int p) { return lds_v(ws + p * MUL, ch); }, gwrow, ch, sc,
                                   A.mgx != 0, A.mgw);
+#endif
             if (GY && A.mgy) {
                 int base = 0;
                 bool owner = true;
@@ -874,7 +925,7 @@ __device__ __forceinline__ void bwd_staged(const BwdArgs& A) {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ __align__(8) unsigned long long full[STAGES_B];
     __shared__ __align__(8) unsigned long long xfull[2];
-    __shared__ __align__(16) REAL Ts[NTP];
+    __shared__ __align__(16) REAL Ts[NTP * (T_DUP_B ? CPT : 1)];
     __shared__ REAL gyS[NWB][NYP];
     BwdShared S;
     cta_items(CONV ? A.s_rowptr : nullptr, A.n_items, S.i0, S.i1);
@@ -905,6 +956,7 @@ __device__ __forceinline__ void bwd_staged(const BwdArgs& A) {
             bwd_issue<CONV>(A, S, we, wn, j);
     }
     bwd_issue_x(A, S, S.i0, 0);
+    __syncthreads();  // stage headers of the first edges are visible to all threads
     const int grp = threadIdx.x / LANES;
     if (grp == 0) bwd_group<0, CONV, GY>(A, S, we, wn);
 #if GB > 1
