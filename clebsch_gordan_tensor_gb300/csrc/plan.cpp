@@ -293,6 +293,11 @@ cgtp_status build_plan(Plan& p, const char* s1, const char* s2, const char* so,
             }
     }
 
+    if (p.maxterms > 4 || p.ny > 255) {
+        err = "CG term table exceeds the packed per-thread layout (more than 4 terms or y wider than 255)";
+        return CGTP_E_UNSUPPORTED;
+    }
+
     // launch geometry
     // fp32: two channels per lane (packed f32x2) when that still fills whole
     // warps; otherwise one.  fp64: one channel per lane.
@@ -373,7 +378,8 @@ cgtp_status build_plan(Plan& p, const char* s1, const char* s2, const char* so,
         // registers limit residency first).  Flag bit 16 turns it on for the
         // forward, bit 17 off for the backward; it needs a single warp group.
         p.w_direct_f = ((p.flags >> 16) & 1u) && p.fwd_groups.size() == 1;
-        p.w_direct_b = !((p.flags >> 17) & 1u) && p.bwd_groups.size() == 1;
+        p.w_direct_b = !((p.flags >> 17) & 1u) && p.bwd_groups.size() == 1 &&
+                       p.dtype == CGTP_F32;  // fp64 pairs would double the prefetch registers
         const size_t fst = (p.w_direct_f ? 0 : WB) + XB + YB;
         const size_t bst = (p.w_direct_b ? 0 : WB) + GB + YB + 16;
         const size_t budget = 216 * 1024;
@@ -538,7 +544,12 @@ void Plan::gen_groups(std::ostringstream& g, const std::vector<int>& k0, bool f6
     // --------------------------------------------------------------- backward
     g << "template <int GRP> struct BwdG;\n";
     for (size_t gi = 0; gi < bwd_groups.size(); ++gi) {
-        const auto& P_ = bwd_groups[gi];
+        // paths ordered by output block so one block's grad-output pairs are
+        // live at a time (they are read from shared memory per path)
+        std::vector<int> P_ = bwd_groups[gi];
+        std::stable_sort(P_.begin(), P_.end(), [&](int a, int b) {
+            return std::make_pair(paths[a].i3, paths[a].i1) < std::make_pair(paths[b].i3, paths[b].i1);
+        });
         std::vector<int> xrows;
         for (int q : P_)
             for (int a = 0; a < 2 * paths[q].l1 + 1; ++a) xrows.push_back(paths[q].r1 + a);
@@ -657,7 +668,7 @@ std::string Plan::kernel_source() const {
        << (ny + lanes - 1) / lanes << "\n";
     os << "#define STAGED " << (staged ? 1 : 0) << "\n#define STAGES_F " << stages_f
        << "\n#define STAGES_B " << stages_b << "\n#define W_DIRECT_F " << (w_direct_f ? 1 : 0)
-       << "\n#define W_DIRECT_B " << (w_direct_b ? 1 : 0) << "\n#define T_DUP_B 0"
+       << "\n#define W_DIRECT_B " << (w_direct_b ? 1 : 0) << "\n#define T_DUP_B 0\n#define W_BUF2 " << (((flags >> 18) & 1u) ? 0 : 1)
        << "\n#define GF " << std::max<size_t>(1, fwd_groups.size()) << "\n#define GB "
        << std::max<size_t>(1, bwd_groups.size()) << "\n";
     // T tables

@@ -516,8 +516,32 @@ __device__ __noinline__ void fail_and_drain(int code, unsigned long long* bars, 
         }
 }
 
-// T entries of one edge, computed by all NTHR threads of the CTA; with DUP the
-// entries are stored as splatted register pairs (no unpacking in the stream).
+// The CG terms of the T entries a thread computes (entries tid, tid + NTHR,
+// ...): coefficients and packed y indices, loaded once per CTA into registers
+// so the per-edge T build reads only y from shared memory.
+template <int NTHR>
+struct TTerms {
+    static constexpr int R = (NT + NTHR - 1) / NTHR;
+    REAL c[R][MAXTERMS];
+    unsigned idx[R];  // MAXTERMS indices of 8 bits each
+    __device__ __forceinline__ void load() {
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const int k = threadIdx.x + r * NTHR;
+            idx[r] = 0u;
+#pragma unroll
+            for (int q = 0; q < MAXTERMS; ++q) {
+                c[r][q] = k < NT ? __ldg(&T_CO[k * MAXTERMS + q]) : (REAL)0;
+                const unsigned i = k < NT ? (unsigned)__ldg(&T_IDX[k * MAXTERMS + q]) : 0u;
+                idx[r] |= i << (8 * q);
+            }
+        }
+    }
+};
+
+// T entries of one edge, computed by all NTHR threads of the CTA with the CG
+// terms read from the (L1-resident) global tables.  With DUP the entries are
+// stored as splatted register pairs (no unpacking in the stream).
 template <int NTHR, bool DUP = false>
 __device__ __forceinline__ void build_T_cta(REAL* __restrict__ Ts, const REAL* __restrict__ Ys) {
     constexpr int ROUNDS = (NT + NTHR - 1) / NTHR;
@@ -540,6 +564,25 @@ __device__ __forceinline__ void build_T_cta(REAL* __restrict__ Ts, const REAL* _
                 reinterpret_cast<VR*>(Ts)[k] = vsplat(t[r]);
             else
                 Ts[k] = t[r];
+        }
+    }
+}
+
+// The same with the CG terms held in registers (TTerms).
+template <int NTHR, bool DUP = false>
+__device__ __forceinline__ void build_T_cta(REAL* __restrict__ Ts, const REAL* __restrict__ Ys,
+                                            const TTerms<NTHR>& tt) {
+#pragma unroll
+    for (int r = 0; r < TTerms<NTHR>::R; ++r) {
+        const int k = threadIdx.x + r * NTHR;
+        REAL t = (REAL)0;
+#pragma unroll
+        for (int q = 0; q < MAXTERMS; ++q) t = fma(tt.c[r][q], Ys[(tt.idx[r] >> (8 * q)) & 255u], t);
+        if (k < NT) {
+            if constexpr (DUP)
+                reinterpret_cast<VR*>(Ts)[k] = vsplat(t);
+            else
+                Ts[k] = t;
         }
     }
 }
@@ -629,12 +672,16 @@ __device__ __forceinline__ void fwd_group(const FwdArgs& A, const FwdShared& S, 
     using FG = FwdG<GRP>;
     const int tid = threadIdx.x, ch = tid % LANES;
     const VR sc = vsplat(A.scale);
+    TTerms<NTF> tt;
+    tt.load();
     VR acc[FG::NR];
 #if W_DIRECT_F
-    VR wcur[NP], wnext[NP];
+    // wbuf[p] holds this edge's weight pair of path p; the stream reads it and
+    // at once reloads the slot with the next edge's value (one edge of latency)
+    VR wbuf[NP];
     if (S.e_begin < S.e_end)
 #pragma unroll
-        for (int p = 0; p < NP; ++p) wnext[p] = ldv(A.w + S.e_begin * A.w_stride + p * MUL, ch);
+        for (int p = 0; p < NP; ++p) wbuf[p] = ldv(A.w + S.e_begin * A.w_stride + p * MUL, ch);
 #endif
     long long j = S.e_begin;
     long long nend = CONV ? (long long)__ldg(A.rowptr + S.i0 + 1) : S.i0 + 1;
@@ -647,7 +694,7 @@ __device__ __forceinline__ void fwd_group(const FwdArgs& A, const FwdShared& S, 
             const long long k = j - S.e_begin;
             const unsigned char* st = S.stages + (size_t)(k % STAGES_F) * FWD_STAGE;
             const bool ok = mbar_wait(&S.full[k % STAGES_F], (unsigned)((k / STAGES_F) & 1));
-            build_T_cta<NTF>(S.Ts, reinterpret_cast<const REAL*>(st + WSF + XB));
+            build_T_cta<NTF>(S.Ts, reinterpret_cast<const REAL*>(st + WSF + XB), tt);
             if (!cta_all(ok)) {
                 fail_and_drain(1, S.full, STAGES_F);
                 return;
@@ -655,12 +702,12 @@ __device__ __forceinline__ void fwd_group(const FwdArgs& A, const FwdShared& S, 
             VR xr[FG::NXR];
             FG::loadx(xr, reinterpret_cast<const REAL*>(st + WSF), ch);
 #if W_DIRECT_F
-#pragma unroll
-            for (int p = 0; p < NP; ++p) wcur[p] = wnext[p];
-            if (j + 1 < S.e_end)
-#pragma unroll
-                for (int p = 0; p < NP; ++p) wnext[p] = ldv(A.w + (j + 1) * A.w_stride + p * MUL, ch);
-            FG::edge(acc, S.Ts, xr, [&](int p) { return wcur[p]; });
+            const REAL* wnext = A.w + (j + 1 < S.e_end ? j + 1 : j) * A.w_stride;
+            FG::edge(acc, S.Ts, xr, [&](int p) {
+                const VR v = wbuf[p];
+                wbuf[p] = ldv(wnext + p * MUL, ch);
+                return v;
+            });
 #else
             const REAL* ws = reinterpret_cast<const REAL*>(st);
             FG::edge(acc, S.Ts, xr, [&](int p) { return lds_v(ws + p * MUL, ch); });
@@ -818,11 +865,17 @@ __device__ __forceinline__ void bwd_group(const BwdArgs& A, const BwdShared& S, 
 #if W_DIRECT_B
     // edge ids come from the stage headers (written before the barrier that
     // follows their issue); the first stage was issued before this loop
-    VR wcur[NP], wnext[NP];
+    // W_BUF2: the next edge's weights land in a second register array loaded
+    // ahead of the stream; otherwise the stream reads a path's weight and
+    // reloads that slot with the next edge's value.
+    VR wbuf[NP];
+#if W_BUF2
+    VR wnext[NP];
+#endif
     if (S.j_begin < S.j_end) {
         const long long e0 = *reinterpret_cast<const int*>(S.stages + WSB + GB_ + YB);
 #pragma unroll
-        for (int p = 0; p < NP; ++p) wnext[p] = ldv(A.w + e0 * A.w_stride + p * MUL, ch);
+        for (int p = 0; p < NP; ++p) wbuf[p] = ldv(A.w + e0 * A.w_stride + p * MUL, ch);
     }
 #endif
     for (long long item = S.i0; item < S.i1; ++item) {
@@ -857,18 +910,31 @@ __device__ __forceinline__ void bwd_group(const BwdArgs& A, const BwdShared& S, 
             for (int i = 0; i < NYP; ++i) gyl[i] = (REAL)0;
             REAL* gwrow = A.gw ? A.gw + e * WDIM : nullptr;
 #if W_DIRECT_B
-#pragma unroll
-            for (int p = 0; p < NP; ++p) wcur[p] = wnext[p];
+            long long e1 = e;
             if (j + 1 < S.j_end) {
                 const unsigned char* st1 = S.stages + (size_t)((k + 1) % STAGES_B) * BWD_STAGE;
-                const long long e1 = *reinterpret_cast<const int*>(st1 + WSB + GB_ + YB);
-#pragma unroll
-                for (int p = 0; p < NP; ++p) wnext[p] = ldv(A.w + e1 * A.w_stride + p * MUL, ch);
+                e1 = *reinterpret_cast<const int*>(st1 + WSB + GB_ + YB);
             }
+            const REAL* wrow1 = A.w + e1 * A.w_stride;
+#if W_BUF2
+#pragma unroll
+            for (int p = 0; p < NP; ++p) wnext[p] = ldv(wrow1 + p * MUL, ch);
             BG::template edge<GY>(gxa, gyl, S.Ts, xr,
                                   [&](int r) { return lds_v(gs + r * MUL, ch); },
-                                  [&](int p) { return wcur[p]; }, gwrow, ch, sc, A.mgx != 0,
+                                  [&](int p) { return wbuf[p]; }, gwrow, ch, sc, A.mgx != 0,
                                   A.mgw);
+#pragma unroll
+            for (int p = 0; p < NP; ++p) wbuf[p] = wnext[p];
+#else
+            BG::template edge<GY>(gxa, gyl, S.Ts, xr,
+                                  [&](int r) { return lds_v(gs + r * MUL, ch); },
+                                  [&](int p) {
+                                      const VR v = wbuf[p];
+                                      wbuf[p] = ldv(wrow1 + p * MUL, ch);
+                                      return v;
+                                  },
+                                  gwrow, ch, sc, A.mgx != 0, A.mgw);
+#endif
 #else
             const REAL* ws = reinterpret_cast<const REAL*>(st);
             BG::template edge<GY>(gxa, gyl, S.Ts, xr,

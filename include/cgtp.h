@@ -89,8 +89,11 @@ typedef struct {
  * flags: 0 for automatic tuning, else overrides of the staged kernels' launch
  * shape: bits 0-3 forward warp groups (1-4), bits 4-7 backward warp groups,
  * bits 8-11 forward TMA ring depth (2-15), bits 12-15 backward ring depth,
- * bit 16 / 17: forward / backward lanes load their weights directly (prefetched
- * one edge ahead in registers) instead of through the ring. */
+ * bit 16: forward lanes load their weights directly (prefetched one edge ahead
+ * in registers) instead of through the ring; bit 17: backward lanes take their
+ * weights through the ring instead of loading them directly (the default for
+ * fp32 plans); bit 18: directly loaded backward weights use one register
+ * buffer (reloaded path by path) instead of two. */
 cgtp_status cgtp_plan_create(cgtp_plan* out, const char* irreps_in1, const char* irreps_in2,
                              const char* irreps_out, const cgtp_instr* instr, int n_instr,
                              cgtp_dtype dtype, cgtp_wmode wmode, unsigned flags);
