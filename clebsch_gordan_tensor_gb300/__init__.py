@@ -76,6 +76,11 @@ def lib() -> ctypes.CDLL:
                 "cgtp_edge_forces_adjoint": [i32, i64, i64, vp, vp, vp, vp, vp],
                 "cgtp_last_cuda_error": [P(i32)],
                 "cgtp_plan_device_status": [vp, P(i32)],
+                "cgtp_weight_grad_workspace": [vp, P(ctypes.c_size_t)],
+                "cgtp_backward_ws": [vp, i64, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp],
+                "cgtp_conv_backward_ws": [vp, i64, i64, vp, vp, vp, vp, vp, vp, vp, vp,
+                                          ctypes.c_double, vp, vp, vp, vp, vp, ctypes.c_size_t,
+                                          vp],
             }
             for name, args in sig.items():
                 f = getattr(L, name)
@@ -221,6 +226,14 @@ class Plan:
         _check(lib().cgtp_plan_source(self._h, buf, need.value, None))
         return buf.value.decode()
 
+    def _workspace(self, device, gw):
+        """Scratch for the shared-weight gradient (torch-allocated), or None."""
+        if not self.shared_weights or gw is None:
+            return None, 0
+        n = ctypes.c_size_t()
+        _check(lib().cgtp_weight_grad_workspace(self._h, ctypes.byref(n)))
+        return torch.empty(n.value, dtype=torch.uint8, device=device), n.value
+
     def _wshape(self, rows):
         return (self.weight_numel,) if self.shared_weights else (rows, self.weight_numel)
 
@@ -245,8 +258,9 @@ class Plan:
         gx = torch.empty_like(x) if need[0] else None
         gy = torch.empty_like(y) if need[1] else None
         gw = torch.empty_like(w) if need[2] else None
-        _check(lib().cgtp_backward(self._h, B, _ptr(x), _ptr(y), _ptr(w), _ptr(grad_out),
-                                   _ptr(gx), _ptr(gy), _ptr(gw), _stream()))
+        ws, nws = self._workspace(x.device, gw)
+        _check(lib().cgtp_backward_ws(self._h, B, _ptr(x), _ptr(y), _ptr(w), _ptr(grad_out),
+                                      _ptr(gx), _ptr(gy), _ptr(gw), _ptr(ws), nws, _stream()))
         return gx, gy, gw
 
     def double_backward(self, x, y, w, grad_out, gg_x=None, gg_y=None, gg_w=None,
@@ -292,10 +306,12 @@ class Plan:
             gx = torch.empty_like(x) if need[0] else None
             gy = torch.empty_like(y) if need[1] else None
             gw = torch.empty_like(w) if need[2] else None
-        _check(lib().cgtp_conv_backward(self._h, g.N, g.E, _ptr(g.rowptr), _ptr(g.sender),
-                                        _ptr(g.s_rowptr), _ptr(g.s_perm), _ptr(g.s_recv),
-                                        _ptr(x), _ptr(y), _ptr(w), float(scale), _ptr(grad_out),
-                                        _ptr(gx), _ptr(gy), _ptr(gw), _stream()))
+        ws, nws = self._workspace(x.device, gw)
+        _check(lib().cgtp_conv_backward_ws(self._h, g.N, g.E, _ptr(g.rowptr), _ptr(g.sender),
+                                           _ptr(g.s_rowptr), _ptr(g.s_perm), _ptr(g.s_recv),
+                                           _ptr(x), _ptr(y), _ptr(w), float(scale),
+                                           _ptr(grad_out), _ptr(gx), _ptr(gy), _ptr(gw), _ptr(ws),
+                                           nws, _stream()))
         return gx, gy, gw
 
     def conv_double_backward(self, g: Graph, x, y, w, scale, grad_out, gg_x=None, gg_y=None,

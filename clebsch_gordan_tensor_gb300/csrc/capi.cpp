@@ -57,7 +57,7 @@ static cgtp_status check_rows(const Plan& p, std::initializer_list<const void*> 
 
 static cgtp_status launch_tp(Plan& p, const char* name, int64_t n_items, void** args,
                              cudaStream_t s, bool staged = false, size_t smem = 0,
-                             int threads = 0) {
+                             int threads = 0, int64_t max_rows = 0, int64_t* rows_used = nullptr) {
     if (n_items <= 0) return CGTP_OK;
     std::shared_ptr<Module> m;
     std::string err;
@@ -69,6 +69,8 @@ static cgtp_status launch_tp(Plan& p, const char* name, int64_t n_items, void** 
     if (!staged) {
         int64_t blocks = (n_items + p.slots - 1) / p.slots;
         if (blocks > INT_MAX) blocks = INT_MAX;
+        if (max_rows > 0) blocks = std::max<int64_t>(1, std::min<int64_t>(blocks, max_rows / p.slots));
+        if (rows_used) *rows_used = blocks * p.slots;
         e = cudaLaunchKernel((const void*)k, dim3((unsigned)blocks), dim3(p.block), args, 0, s);
     } else {
         int dev = 0;
@@ -108,7 +110,9 @@ static cgtp_status launch_tp(Plan& p, const char* name, int64_t n_items, void** 
         }
         if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
             return cuda_fail(e, "cudaDeviceGetAttribute");
-        const int64_t grid = std::min<int64_t>(n_items, (int64_t)sms * per_sm);
+        int64_t grid = std::min<int64_t>(n_items, (int64_t)sms * per_sm);
+        if (max_rows > 0) grid = std::max<int64_t>(1, std::min<int64_t>(grid, max_rows));
+        if (rows_used) *rows_used = grid;
         e = cudaLaunchKernel((const void*)k, dim3((unsigned)grid), dim3(threads), args, smem, s);
     }
     if (e != cudaSuccess) return cuda_fail(e, name);
@@ -146,21 +150,31 @@ static cgtp_status fwd_launch(Plan& p, bool conv, int64_t n_items, const int32_t
 static cgtp_status bwd_launch(Plan& p, bool conv, int64_t n_items, const int32_t* s_rowptr,
                               const int32_t* s_perm, const int32_t* s_recv, const void* x,
                               const void* y, const void* w, const void* g, double scale, void* gx,
-                              void* gy, void* gw, int mgx, int mgy, int mgw, cudaStream_t s) {
+                              void* gy, void* gw, int mgx, int mgy, int mgw, cudaStream_t s,
+                              void* wsp = nullptr, int64_t ws_rows = 0) {
     if (!mgx && !mgy && !mgw) return CGTP_OK;
     long long n = n_items;
     long long ws = p.wmode == CGTP_W_SHARED ? 0 : p.wdim;
     float sf = (float)scale;
     double sd = scale;
     void* sp = p.dtype == CGTP_F64 ? (void*)&sd : (void*)&sf;
+    const bool shared = p.wmode == CGTP_W_SHARED && mgw;
+    void* part = shared ? wsp : nullptr;
     void* args[] = {&n, &s_rowptr, &s_perm, &s_recv, &x, &y, &w, &ws, &g, sp,
-                    &gx, &gy, &gw, &mgx, &mgy, &mgw};
+                    &gx, &gy, &gw, &mgx, &mgy, &mgw, &part};
     const bool staged = p.staged && a16({x, y, w, g});
     std::string name = conv ? (mgy ? "cgtp_bwd_conv" : "cgtp_bwd_conv_nogy")
                             : (mgy ? "cgtp_bwd_single" : "cgtp_bwd_single_nogy");
     if (staged) name += "_tma";
-    return launch_tp(p, name.c_str(), n_items, args, s, staged, p.bwd_smem,
-                     (int)p.bwd_groups.size() * p.lanes);
+    int64_t rows = 0;
+    cgtp_status st = launch_tp(p, name.c_str(), n_items, args, s, staged, p.bwd_smem,
+                               (int)p.bwd_groups.size() * p.lanes, shared ? ws_rows : 0, &rows);
+    if (st != CGTP_OK || !shared) return st;
+    // ordered sum of the per-CTA partial rows into grad_w
+    cudaError_t e = launch_reduce_rows(p.dtype == CGTP_F64, wsp, rows, p.wdim, gw, s);
+    if (e != cudaSuccess) return cuda_fail(e, "weight-gradient reduction");
+    count_launch();
+    return CGTP_OK;
 }
 
 static size_t esize(const Plan& p) { return p.dtype == CGTP_F64 ? 8 : 4; }
@@ -363,6 +377,25 @@ cgtp_status cgtp_plan_device_status(cgtp_plan plan, int* code) {
     GUARD_END
 }
 
+cgtp_status cgtp_weight_grad_workspace(cgtp_plan plan, size_t* bytes) {
+    if (!plan || !bytes) return fail(CGTP_E_ARG, "NULL argument");
+    const Plan& p = plan->p;
+    *bytes = p.wmode == CGTP_W_SHARED
+                 ? (size_t)kSharedWRows * (size_t)p.wdim * (p.dtype == CGTP_F64 ? 8 : 4)
+                 : 0;
+    return CGTP_OK;
+}
+
+static cgtp_status check_ws(const Plan& p, const void* grad_w, const void* ws, size_t bytes) {
+    if (p.wmode != CGTP_W_SHARED || !grad_w) return CGTP_OK;
+    const size_t need = (size_t)kSharedWRows * (size_t)p.wdim * (p.dtype == CGTP_F64 ? 8 : 4);
+    if (!ws || bytes < need)
+        return fail(CGTP_E_ARG, "shared-weight gradient needs a workspace of " +
+                                    std::to_string(need) + " bytes (cgtp_weight_grad_workspace)");
+    if (!aligned(ws, 16)) return fail(CGTP_E_ARG, "workspace not 16-byte aligned");
+    return CGTP_OK;
+}
+
 cgtp_status cgtp_forward(cgtp_plan plan, int64_t B, const void* x, const void* y, const void* w,
                          void* out, cgtp_stream stream) {
     GUARD_BEGIN
@@ -387,11 +420,33 @@ cgtp_status cgtp_backward(cgtp_plan plan, int64_t B, const void* x, const void* 
     if (!x || !y || !w || !grad_out) return fail(CGTP_E_ARG, "NULL input tensor");
     Plan& p = plan->p;
     if (p.wmode == CGTP_W_SHARED && grad_w)
-        return fail(CGTP_E_UNSUPPORTED, "weight gradient of shared weights is not implemented");
+        return fail(CGTP_E_ARG, "shared-weight gradient needs a workspace: use cgtp_backward_ws");
     cgtp_status st = check_rows(p, {x, w, grad_out, grad_x, grad_w});
     if (st != CGTP_OK) return st;
     return bwd_launch(p, false, B, nullptr, nullptr, nullptr, x, y, w, grad_out, 1.0, grad_x,
                       grad_y, grad_w, grad_x ? 1 : 0, grad_y ? 1 : 0, grad_w ? 1 : 0, S(stream));
+    GUARD_END
+}
+
+cgtp_status cgtp_backward_ws(cgtp_plan plan, int64_t B, const void* x, const void* y,
+                             const void* w, const void* grad_out, void* grad_x, void* grad_y,
+                             void* grad_w, void* workspace, size_t workspace_bytes,
+                             cgtp_stream stream) {
+    GUARD_BEGIN
+    if (!plan) return fail(CGTP_E_ARG, "plan is NULL");
+    if (B < 0) return fail(CGTP_E_ARG, "B < 0");
+    Plan& p = plan->p;
+    cgtp_status st = check_ws(p, grad_w, workspace, workspace_bytes);
+    if (st != CGTP_OK) return st;
+    if (B == 0) {
+        if (p.wmode == CGTP_W_SHARED && grad_w) return zero(grad_w, p.wdim * (int64_t)esize(p), S(stream));
+        return CGTP_OK;
+    }
+    if (!x || !y || !w || !grad_out) return fail(CGTP_E_ARG, "NULL input tensor");
+    if ((st = check_rows(p, {x, w, grad_out, grad_x, grad_w})) != CGTP_OK) return st;
+    return bwd_launch(p, false, B, nullptr, nullptr, nullptr, x, y, w, grad_out, 1.0, grad_x,
+                      grad_y, grad_w, grad_x ? 1 : 0, grad_y ? 1 : 0, grad_w ? 1 : 0, S(stream),
+                      workspace, kSharedWRows);
     GUARD_END
 }
 
@@ -451,11 +506,38 @@ cgtp_status cgtp_conv_backward(cgtp_plan plan, int64_t N, int64_t E, const int32
     if (N == 0) return CGTP_OK;
     Plan& p = plan->p;
     if (p.wmode == CGTP_W_SHARED && grad_w)
-        return fail(CGTP_E_UNSUPPORTED, "weight gradient of shared weights is not implemented");
+        return fail(CGTP_E_ARG, "shared-weight gradient needs a workspace: use cgtp_conv_backward_ws");
     if (!x || !grad_out || (E > 0 && (!y || !w))) return fail(CGTP_E_ARG, "NULL input tensor");
     if ((st = check_rows(p, {x, w, grad_out, grad_x, grad_w})) != CGTP_OK) return st;
     return bwd_launch(p, true, N, s_rowptr, s_perm, s_recv, x, y, w, grad_out, scale, grad_x,
                       grad_y, grad_w, grad_x ? 1 : 0, grad_y ? 1 : 0, grad_w ? 1 : 0, S(stream));
+    GUARD_END
+}
+
+cgtp_status cgtp_conv_backward_ws(cgtp_plan plan, int64_t N, int64_t E, const int32_t* rowptr,
+                                  const int32_t* sender, const int32_t* s_rowptr,
+                                  const int32_t* s_perm, const int32_t* s_recv, const void* x,
+                                  const void* y, const void* w, double scale,
+                                  const void* grad_out, void* grad_x, void* grad_y, void* grad_w,
+                                  void* workspace, size_t workspace_bytes, cgtp_stream stream) {
+    GUARD_BEGIN
+    if (!plan) return fail(CGTP_E_ARG, "plan is NULL");
+    cgtp_status st = check_graph(N, E, s_rowptr, s_perm);
+    if (st != CGTP_OK) return st;
+    if (E > 0 && !s_recv) return fail(CGTP_E_GRAPH, "NULL s_recv");
+    (void)rowptr;
+    (void)sender;
+    Plan& p = plan->p;
+    if ((st = check_ws(p, grad_w, workspace, workspace_bytes)) != CGTP_OK) return st;
+    if (N == 0) {
+        if (p.wmode == CGTP_W_SHARED && grad_w) return zero(grad_w, p.wdim * (int64_t)esize(p), S(stream));
+        return CGTP_OK;
+    }
+    if (!x || !grad_out || (E > 0 && (!y || !w))) return fail(CGTP_E_ARG, "NULL input tensor");
+    if ((st = check_rows(p, {x, w, grad_out, grad_x, grad_w})) != CGTP_OK) return st;
+    return bwd_launch(p, true, N, s_rowptr, s_perm, s_recv, x, y, w, grad_out, scale, grad_x,
+                      grad_y, grad_w, grad_x ? 1 : 0, grad_y ? 1 : 0, grad_w ? 1 : 0, S(stream),
+                      workspace, kSharedWRows);
     GUARD_END
 }
 

@@ -9,6 +9,7 @@
 // deterministic, no atomics.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdint>
 
 #include "internal.hpp"
@@ -58,6 +59,18 @@ edge_forces_adjoint_kernel(int64_t N, const int32_t* __restrict__ rowptr,
     }
 }
 
+// out[c] = sum over r of partial[r][c], rows added in order (deterministic).
+template <typename T>
+__global__ void __launch_bounds__(256)
+reduce_rows_kernel(const T* __restrict__ partial, int64_t rows, int64_t cols, T* __restrict__ out) {
+    for (int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; c < cols;
+         c += (int64_t)gridDim.x * blockDim.x) {
+        T s = 0;
+        for (int64_t r = 0; r < rows; ++r) s += partial[r * cols + c];
+        out[c] = s;
+    }
+}
+
 __global__ void fill_zero_kernel(uint32_t* __restrict__ p, int64_t words) {
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < words;
          i += (int64_t)gridDim.x * blockDim.x)
@@ -92,6 +105,18 @@ cudaError_t launch_edge_forces_adjoint(bool f64, int64_t N, const int32_t* rowpt
     else
         edge_forces_adjoint_kernel<float><<<grid_for(N), 128, 0, s>>>(
             N, rowptr, sender, (const float*)gF, (float*)q);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_reduce_rows(bool f64, const void* partial, int64_t rows, int64_t cols,
+                               void* out, cudaStream_t s) {
+    const unsigned blocks = (unsigned)std::max<int64_t>(1, std::min<int64_t>((cols + 255) / 256, 4096));
+    if (f64)
+        reduce_rows_kernel<double><<<blocks, 256, 0, s>>>((const double*)partial, rows, cols,
+                                                          (double*)out);
+    else
+        reduce_rows_kernel<float><<<blocks, 256, 0, s>>>((const float*)partial, rows, cols,
+                                                         (float*)out);
     return cudaGetLastError();
 }
 

@@ -44,5 +44,10 @@ cudaError_t launch_edge_forces_adjoint(bool f64, int64_t N, const int32_t* rowpt
                                        const int32_t* sender, const void* gF, void* q,
                                        cudaStream_t s);
 cudaError_t launch_fill_zero(void* p, int64_t bytes, cudaStream_t s);
+cudaError_t launch_reduce_rows(bool f64, const void* partial, int64_t rows, int64_t cols,
+                               void* out, cudaStream_t s);
+
+// Partial weight-gradient rows a shared-weight backward may write (grid cap).
+constexpr int64_t kSharedWRows = 2048;
 
 }  // namespace cgtp

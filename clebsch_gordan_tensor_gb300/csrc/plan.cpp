@@ -367,7 +367,7 @@ cgtp_status build_plan(Plan& p, const char* s1, const char* s2, const char* so,
             return grp;
         };
         p.fwd_groups = lpt(cf, std::min(4, ovr_gf ? ovr_gf : 1));
-        p.bwd_groups = lpt(cb, std::min(4, ovr_gb ? ovr_gb : 1));
+        p.bwd_groups = lpt(cb, p.wmode == CGTP_W_SHARED ? 1 : std::min(4, ovr_gb ? ovr_gb : 1));
         // Ring depth and groups: on the 10k-atom convolution the fastest shape
         // was one warp group per CTA with a 2-deep ring (more resident CTAs beat
         // deeper prefetch); flags override both.
@@ -565,7 +565,8 @@ void Plan::gen_groups(std::ostringstream& g, const std::vector<int>& k0, bool f6
         g << "  }\n";
         g << "  template <bool GY, class FG, class FW>\n  __device__ static __forceinline__ void edge("
              "VR (&gxa)[NXR], REAL (&gyl)[NYP], const REAL* __restrict__ Ts, const VR (&xr)[NXR],\n"
-             "      FG&& G, FW&& W, REAL* __restrict__ gwrow, int ch, VR sc, bool dogx, int mgw) {\n";
+             "      FG&& G, FW&& W, REAL* __restrict__ gwrow, VR (&gwa)[NP], int ch, VR sc, bool dogx,\n"
+             "      int mgw) {\n";
         // T_DUP_B selects splatted pairs for the backward's T entries; scalar
         // entries measured faster (fewer registers), so the default is 0.
         if (cpt == 2) g << "    const float4* __restrict__ Tq = reinterpret_cast<const float4*>(Ts);\n";
@@ -601,9 +602,7 @@ void Plan::gen_groups(std::ostringstream& g, const std::vector<int>& k0, bool f6
             g << "    }\n    if (mgw) {\n      VR s = vzero();\n";
             for (int a = 0; a < d1; ++a)
                 if (hs[a]) g << "      s = vfma(xr[" << xi[P.r1 + a] << "], h" << a << ", s);\n";
-            g << "      s = vmul(s, sc);\n      REAL* gp = gwrow + " << (long long)q * mul << ";\n"
-              << "      if (mgw == 2) s = vadd(s, ldv_plain(gp, ch));\n"
-              << "      stv(gp, ch, s);\n    }\n";
+            g << "      GWOUT(" << q << ", s);\n    }\n";
             g << "    if (GY) {\n";
             const bool zx = d1 <= d3;
             if (zx) {
@@ -669,6 +668,7 @@ std::string Plan::kernel_source() const {
     os << "#define STAGED " << (staged ? 1 : 0) << "\n#define STAGES_F " << stages_f
        << "\n#define STAGES_B " << stages_b << "\n#define W_DIRECT_F " << (w_direct_f ? 1 : 0)
        << "\n#define W_DIRECT_B " << (w_direct_b ? 1 : 0) << "\n#define T_DUP_B 0\n#define W_BUF2 " << (((flags >> 18) & 1u) ? 0 : 1)
+       << "\n#define SHARED_W " << (wmode == CGTP_W_SHARED ? 1 : 0)
        << "\n#define GF " << std::max<size_t>(1, fwd_groups.size()) << "\n#define GB "
        << std::max<size_t>(1, bwd_groups.size()) << "\n";
     // T tables
@@ -748,7 +748,7 @@ std::string Plan::kernel_source() const {
     // ---- backward stream
     g << "template <bool GY, class FX, class FG, class FW>\n__device__ __forceinline__ void gen_bwd(\n"
          "    VR (&gxa)[NX], REAL (&gyl)[NYP], const REAL* __restrict__ Ts, FX&& X, FG&& G, FW&& W,\n"
-         "    REAL* __restrict__ gwrow, int ch, VR sc, bool dogx, int mgw) {\n";
+         "    REAL* __restrict__ gwrow, VR (&gwa)[NP], int ch, VR sc, bool dogx, int mgw) {\n";
     if (cpt == 2) g << "    const float4* __restrict__ Tq = reinterpret_cast<const float4*>(Ts);\n";
     {
         TLoader L{cpt, std::vector<bool>(ntp / 4 + 1, false), &g};
@@ -779,9 +779,7 @@ std::string Plan::kernel_source() const {
             g << "    }\n    if (mgw) {\n      VR s = vzero();\n";
             for (int a = 0; a < d1; ++a)
                 if (hs[a]) g << "      s = vfma(X(" << P.r1 + a << "), h" << a << ", s);\n";
-            g << "      s = vmul(s, sc);\n      REAL* gp = gwrow + " << (long long)q * mul << ";\n"
-              << "      if (mgw == 2) s = vadd(s, ldv_plain(gp, ch));\n"
-              << "      if (CH_ACTIVE(ch)) stv(gp, ch, s);\n    }\n";
+            g << "      GWOUT(" << q << ", s);\n    }\n";
             // gy partials
             g << "    if (GY) {\n";
             const bool zx = d1 <= d3;

@@ -152,6 +152,26 @@ __device__ __forceinline__ void seg_reduce(REAL* v, int lane, unsigned mask, int
 constexpr int WSEG = LANES < 32 ? LANES : 32;  // lanes of one slot inside one warp
 constexpr int NRED = NYP / WSEG > 0 ? NYP / WSEG : 1;
 
+// grad_w of one path: stored per edge, or (shared weights) added to the
+// thread's running partial, which the kernel writes once per CTA / slot.
+__device__ __forceinline__ void gw_store(REAL* gp, int ch, VR s, VR sc, int mgw) {
+    s = vmul(s, sc);
+    if (mgw == 2) s = vadd(s, ldv_plain(gp, ch));
+    if (CH_ACTIVE(ch)) stv(gp, ch, s);
+}
+#if SHARED_W
+#define GWOUT(q, s) (gwa[q] = vadd(gwa[q], (s)))
+#else
+#define GWOUT(q, s) gw_store(gwrow + (long long)(q) * MUL, ch, (s), sc, mgw)
+#endif
+// Partial weight-gradient row of a CTA or slot (shared weights).
+__device__ __forceinline__ void gw_partial(REAL* __restrict__ row, const VR (&gwa)[NP], int ch,
+                                           VR sc) {
+    if (!CH_ACTIVE(ch)) return;
+#pragma unroll
+    for (int q = 0; q < NP; ++q) stv(row + (long long)q * MUL, ch, vmul(gwa[q], sc));
+}
+
 // @@GENERATED@@ (per-plan contraction streams are inserted here)
 
 // ------------------------------------------------------------------ forward
@@ -263,7 +283,8 @@ __device__ __forceinline__ void bwd_body(long long n_items, const int* __restric
                                          const REAL* __restrict__ w, long long w_stride,
                                          const REAL* __restrict__ g, REAL scale,
                                          REAL* __restrict__ gx, REAL* __restrict__ gy,
-                                         REAL* __restrict__ gw, int mgx, int mgy, int mgw) {
+                                         REAL* __restrict__ gw, int mgx, int mgy, int mgw,
+                                         REAL* __restrict__ wsp) {
     __shared__ __align__(16) REAL Ts_all[SLOTS][NTP];
     __shared__ __align__(16) REAL Ys_all[SLOTS][NYP];
 #if LANES > 32
@@ -274,6 +295,9 @@ __device__ __forceinline__ void bwd_body(long long n_items, const int* __restric
     REAL* Ys = Ys_all[slot];
     const int ch = lane;
     const VR sc = vsplat(scale);
+    VR gwa[NP];
+#pragma unroll
+    for (int q = 0; q < NP; ++q) gwa[q] = vzero();
     for (long long item = (long long)blockIdx.x * SLOTS + slot; item < n_items;
          item += (long long)gridDim.x * SLOTS) {
         long long j0, j1;
@@ -338,8 +362,8 @@ __device__ __forceinline__ void bwd_body(long long n_items, const int* __restric
 #pragma unroll
             for (int i = 0; i < NYP; ++i) gyl[i] = (REAL)0;
             gen_bwd<GY>(gxa, gyl, Ts, [&](int r) { return xr[r]; }, [&](int r) { return gr[r]; },
-                        [&](int p) { return ldv_m(wrow + (long long)p * MUL, ch); }, gwrow, ch,
-                        sc, mgx != 0, mgw);
+                        [&](int p) { return ldv_m(wrow + (long long)p * MUL, ch); }, gwrow, gwa,
+                        ch, sc, mgx != 0, mgw);
             if (GY && mgy) {
                 int base = 0;
                 bool owner = true;
@@ -381,6 +405,7 @@ __device__ __forceinline__ void bwd_body(long long n_items, const int* __restric
             }
         }
     }
+    if (SHARED_W && mgw) gw_partial(wsp + ((long long)blockIdx.x * SLOTS + slot) * WDIM, gwa, ch, sc);
 }
 
 #define CGTP_BWD_ENTRY(NAME, CONV, GY)                                                          \
@@ -389,9 +414,9 @@ __device__ __forceinline__ void bwd_body(long long n_items, const int* __restric
         const int* __restrict__ s_recv, const REAL* __restrict__ x,                           \
         const REAL* __restrict__ y, const REAL* __restrict__ w, long long w_stride,           \
         const REAL* __restrict__ g, REAL scale, REAL* __restrict__ gx, REAL* __restrict__ gy, \
-        REAL* __restrict__ gw, int mgx, int mgy, int mgw) {                                   \
+        REAL* __restrict__ gw, int mgx, int mgy, int mgw, REAL* __restrict__ wsp) {           \
         bwd_body<CONV, GY>(n_items, s_rowptr, s_perm, s_recv, x, y, w, w_stride, g, scale,    \
-                           gx, gy, gw, mgx, mgy, mgw);                                        \
+                           gx, gy, gw, mgx, mgy, mgw, wsp);                                   \
     }
 
 CGTP_BWD_ENTRY(cgtp_bwd_conv, true, true)
@@ -815,6 +840,7 @@ struct BwdArgs {
     REAL* __restrict__ gy;
     REAL* __restrict__ gw;
     int mgx, mgy, mgw;
+    REAL* __restrict__ wsp;  // partial weight-gradient rows (shared weights)
 };
 
 constexpr int NWB = NTB / 32;  // warps of a backward CTA
@@ -860,6 +886,9 @@ __device__ __forceinline__ void bwd_group(const BwdArgs& A, const BwdShared& S, 
     using BG = BwdG<GRP>;
     const int tid = threadIdx.x, ch = tid % LANES, lane = tid & 31;
     const VR sc = vsplat(A.scale);
+    VR gwa[NP];
+#pragma unroll
+    for (int q = 0; q < NP; ++q) gwa[q] = vzero();
     long long j = S.j_begin;
     long long nend = CONV ? (long long)__ldg(A.s_rowptr + S.i0 + 1) : S.i0 + 1;
 #if W_DIRECT_B
@@ -921,8 +950,8 @@ __device__ __forceinline__ void bwd_group(const BwdArgs& A, const BwdShared& S, 
             for (int p = 0; p < NP; ++p) wnext[p] = ldv(wrow1 + p * MUL, ch);
             BG::template edge<GY>(gxa, gyl, S.Ts, xr,
                                   [&](int r) { return lds_v(gs + r * MUL, ch); },
-                                  [&](int p) { return wbuf[p]; }, gwrow, ch, sc, A.mgx != 0,
-                                  A.mgw);
+                                  [&](int p) { return wbuf[p]; }, gwrow, gwa, ch, sc,
+                                  A.mgx != 0, A.mgw);
 #pragma unroll
             for (int p = 0; p < NP; ++p) wbuf[p] = wnext[p];
 #else
@@ -933,14 +962,14 @@ __device__ __forceinline__ void bwd_group(const BwdArgs& A, const BwdShared& S, 
                                       wbuf[p] = ldv(wrow1 + p * MUL, ch);
                                       return v;
                                   },
-                                  gwrow, ch, sc, A.mgx != 0, A.mgw);
+                                  gwrow, gwa, ch, sc, A.mgx != 0, A.mgw);
 #endif
 #else
             const REAL* ws = reinterpret_cast<const REAL*>(st);
             BG::template edge<GY>(gxa, gyl, S.Ts, xr,
                                   [&](int r) { return lds_v(gs + r * MUL, ch); },
-                                  [&](int p) { return lds_v(ws + p * MUL, ch); }, gwrow, ch, sc,
-                                  A.mgx != 0, A.mgw);
+                                  [&](int p) { return lds_v(ws + p * MUL, ch); }, gwrow, gwa,
+                                  ch, sc, A.mgx != 0, A.mgw);
 #endif
             if (GY && A.mgy) {
                 int base = 0;
@@ -984,6 +1013,7 @@ __device__ __forceinline__ void bwd_group(const BwdArgs& A, const BwdShared& S, 
             }
         }
     }
+    if (SHARED_W && A.mgw) gw_partial(A.wsp + (long long)blockIdx.x * WDIM, gwa, ch, sc);
 }
 
 template <bool CONV, bool GY>
@@ -995,7 +1025,15 @@ __device__ __forceinline__ void bwd_staged(const BwdArgs& A) {
     __shared__ REAL gyS[NWB][NYP];
     BwdShared S;
     cta_items(CONV ? A.s_rowptr : nullptr, A.n_items, S.i0, S.i1);
-    if (S.i0 >= S.i1) return;
+    if (S.i0 >= S.i1) {
+        if (SHARED_W && A.mgw) {  // every CTA owns one partial row, even an empty one
+            VR z[NP];
+#pragma unroll
+            for (int q = 0; q < NP; ++q) z[q] = vzero();
+            if (threadIdx.x < LANES) gw_partial(A.wsp + (long long)blockIdx.x * WDIM, z, threadIdx.x, z[0]);
+        }
+        return;
+    }
     S.stages = smem;
     S.xring = smem + (size_t)STAGES_B * BWD_STAGE;
     S.buf = reinterpret_cast<REAL*>(S.xring + 2 * (size_t)XB);
@@ -1042,9 +1080,9 @@ __device__ __forceinline__ void bwd_staged(const BwdArgs& A) {
         const int* __restrict__ s_recv, const REAL* __restrict__ x,                           \
         const REAL* __restrict__ y, const REAL* __restrict__ w, long long w_stride,           \
         const REAL* __restrict__ g, REAL scale, REAL* __restrict__ gx, REAL* __restrict__ gy, \
-        REAL* __restrict__ gw, int mgx, int mgy, int mgw) {                                   \
+        REAL* __restrict__ gw, int mgx, int mgy, int mgw, REAL* __restrict__ wsp) {           \
         bwd_staged<CONV, GY>(BwdArgs{n_items, s_rowptr, s_perm, s_recv, x, y, w, w_stride, g, \
-                                     scale, gx, gy, gw, mgx, mgy, mgw});                      \
+                                     scale, gx, gy, gw, mgx, mgy, mgw, wsp});                 \
     }
 
 CGTP_BWD_TMA_ENTRY(cgtp_bwd_conv_tma, true, true)

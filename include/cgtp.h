@@ -137,11 +137,26 @@ cgtp_status cgtp_forward(cgtp_plan plan, int64_t B, const void* x, const void* y
  *   grad_x[b,l1,m1,u] = sum C y[m2] w[p,u] g[l3,m3,u]
  *   grad_y[b,l2,m2]   = sum C x[m1,u] w[p,u] g[m3,u]   (summed over channels)
  *   grad_w[b,p,u]     = sum C x[m1,u] y[m2] g[m3,u]
- * Any output may be NULL.  CGTP_W_SHARED plans: grad_w is not supported here
- * (CGTP_E_UNSUPPORTED if non-NULL). */
+ * Any output may be NULL.  For a CGTP_W_SHARED plan grad_w sums over the
+ * samples and needs scratch memory: use cgtp_backward_ws (CGTP_E_ARG here). */
 cgtp_status cgtp_backward(cgtp_plan plan, int64_t B, const void* x, const void* y, const void* w,
                           const void* grad_out, void* grad_x, void* grad_y, void* grad_w,
                           cgtp_stream stream);
+
+/* Bytes of device scratch the weight gradient of a CGTP_W_SHARED plan needs
+ * (0 for per-edge plans): one partial row of weight_numel per CTA, at most
+ * 2048 rows.  The partial rows are summed in order, so results do not depend
+ * on scheduling. */
+cgtp_status cgtp_weight_grad_workspace(cgtp_plan plan, size_t* bytes);
+
+/* cgtp_backward with caller-owned device scratch `workspace` (16-byte aligned,
+ * at least cgtp_weight_grad_workspace bytes; contents need no initialisation
+ * and are overwritten).  Required when grad_w != NULL on a CGTP_W_SHARED plan;
+ * grad_w [weight_numel] = sum over samples. */
+cgtp_status cgtp_backward_ws(cgtp_plan plan, int64_t B, const void* x, const void* y,
+                             const void* w, const void* grad_out, void* grad_x, void* grad_y,
+                             void* grad_w, void* workspace, size_t workspace_bytes,
+                             cgtp_stream stream);
 
 /* Higher partial derivatives ("a novel identity for the higher partial
  * derivatives", abstract of arXiv 2501.13986; the identity is not printed).
@@ -171,14 +186,25 @@ cgtp_status cgtp_conv_forward(cgtp_plan plan, int64_t N, int64_t E, const int32_
  *   grad_x[s] = scale * sum_{edges e with sender s} f_x(g[recv e]; y[e], w[e])
  *   grad_y[e] = scale * f_y(g[recv e]; x[sender e], w[e])
  *   grad_w[e] = scale * f_w(g[recv e]; x[sender e], y[e])
- * Uses the sender-grouped view (s_rowptr, s_perm, s_recv); no atomics. */
+ * Uses the sender-grouped view (s_rowptr, s_perm, s_recv); no atomics.
+ * For a CGTP_W_SHARED plan grad_w needs scratch: use cgtp_conv_backward_ws. */
 cgtp_status cgtp_conv_backward(cgtp_plan plan, int64_t N, int64_t E, const int32_t* rowptr,
                                const int32_t* sender, const int32_t* s_rowptr,
                                const int32_t* s_perm, const int32_t* s_recv, const void* x,
                                const void* y, const void* w, double scale, const void* grad_out,
                                void* grad_x, void* grad_y, void* grad_w, cgtp_stream stream);
 
-/* The identity of cgtp_double_backward applied to the fused convolution. */
+/* cgtp_conv_backward with caller-owned scratch (see cgtp_backward_ws); for a
+ * CGTP_W_SHARED plan grad_w [weight_numel] sums over all edges. */
+cgtp_status cgtp_conv_backward_ws(cgtp_plan plan, int64_t N, int64_t E, const int32_t* rowptr,
+                                  const int32_t* sender, const int32_t* s_rowptr,
+                                  const int32_t* s_perm, const int32_t* s_recv, const void* x,
+                                  const void* y, const void* w, double scale,
+                                  const void* grad_out, void* grad_x, void* grad_y, void* grad_w,
+                                  void* workspace, size_t workspace_bytes, cgtp_stream stream);
+
+/* The identity of cgtp_double_backward applied to the fused convolution.
+ * CGTP_W_SHARED plans: d_w is not supported (CGTP_E_UNSUPPORTED if non-NULL). */
 cgtp_status cgtp_conv_double_backward(cgtp_plan plan, int64_t N, int64_t E, const int32_t* rowptr,
                                       const int32_t* sender, const int32_t* s_rowptr,
                                       const int32_t* s_perm, const int32_t* s_recv, const void* x,

@@ -236,3 +236,29 @@ def test_staged_and_direct_paths_agree(case):
     code = __import__("ctypes").c_int(-1)
     assert cg.lib().cgtp_plan_device_status(plan._h, __import__("ctypes").byref(code)) == 0
     assert code.value == 0
+
+
+@pytest.mark.parametrize("case", [CASES[1], CASES[5]], ids=lambda c: f"{c[0][:12]}-{np.dtype(c[3]).name}")
+def test_conv_shared_weight_gradient(case):
+    """Fused convolution with one weight row shared by every edge: grad_w sums
+    over all edges (per-CTA partial rows, ordered reduction)."""
+    need_gpu()
+    cg = _cg()
+    a, b, c, dt = case
+    prob = O.make_problem(a, b, c)
+    plan = cg.Plan(a, b, c, dtype=torch.float64 if dt == np.float64 else torch.float32,
+                   shared_weights=True)
+    rng = np.random.default_rng(21)
+    gr = _graph(rng, 300, max_deg=12)
+    G = cg.Graph.from_numpy(gr)
+    x = rng.standard_normal((gr.N, prob.dim1)).astype(dt)
+    y = rng.standard_normal((gr.E, prob.dim2)).astype(dt)
+    w = rng.standard_normal(prob.wdim).astype(dt)
+    g = rng.standard_normal((gr.N, prob.dimo)).astype(dt)
+    out = plan.conv_forward(G, dev(x), dev(y), dev(w), 0.25)
+    assert_close(host(out), O.conv_forward(prob, gr.rowptr, gr.sender, x, y, w, 0.25), dt, "fwd")
+    gx, gy, gw = plan.conv_backward(G, dev(x), dev(y), dev(w), 0.25, dev(g))
+    rx, ry, rw = O.conv_backward(prob, gr.rowptr, gr.sender, x, y, w, 0.25, g)
+    assert_close(host(gx), rx, dt, "grad_x")
+    assert_close(host(gy), ry, dt, "grad_y")
+    assert_close(host(gw), rw, dt, "grad_w")

@@ -94,11 +94,39 @@ def test_shared_weights_forward():
     w = rng.standard_normal(prob.wdim).astype(np.float32)
     out = plan.forward(dev(x), dev(y), dev(w))
     assert_close(host(out), O.tp_forward(prob, x, y, w), np.float32, "shared forward")
-    gx, gy, _ = plan.backward(dev(x), dev(y), dev(w), dev(np.ones((50, prob.dimo), np.float32)),
-                              need=(True, True, False))
-    rx, ry, _ = O.tp_backward(prob, x, y, w, np.ones((50, prob.dimo)))
+    g = rng.standard_normal((50, prob.dimo)).astype(np.float32)
+    gx, gy, gw = plan.backward(dev(x), dev(y), dev(w), dev(g))
+    rx, ry, rw = O.tp_backward(prob, x, y, w, g)
     assert_close(host(gx), rx, np.float32, "shared grad_x")
     assert_close(host(gy), ry, np.float32, "shared grad_y")
+    assert gw.shape == (prob.wdim,)
+    assert_close(host(gw), rw, np.float32, "shared grad_w (sum over samples)")
+
+
+@pytest.mark.parametrize("B", [1, 3, 5000])
+@pytest.mark.parametrize("irreps,dt", [(("64x0e+64x1o+64x2e", "0e+1o+2e+3o",
+                                         "64x0e+64x1o+64x1e+64x2o+64x2e+64x3o+64x3e"), np.float32),
+                                       (("3x0e+3x1o", "0e+1o", "3x0e+3x1o"), np.float32),
+                                       (("8x0e+8x1o", "0e+1o+2e", "8x0e+8x1o+8x2e"), np.float64)])
+def test_shared_weight_gradient(B, irreps, dt):
+    """grad_w of a shared weight row: per-CTA partial rows reduced in order."""
+    need_gpu()
+    import clebsch_gordan_tensor_gb300 as cg
+    prob = O.make_problem(*irreps)
+    plan = cg.Plan(*irreps, dtype=torch.float64 if dt == np.float64 else torch.float32,
+                   shared_weights=True)
+    rng = np.random.default_rng(B)
+    x = rng.standard_normal((B, prob.dim1)).astype(dt)
+    y = rng.standard_normal((B, prob.dim2)).astype(dt)
+    w = rng.standard_normal(prob.wdim).astype(dt)
+    g = rng.standard_normal((B, prob.dimo)).astype(dt)
+    _, _, gw = plan.backward(dev(x), dev(y), dev(w), dev(g), need=(False, False, True))
+    _, _, rw = O.tp_backward(prob, x, y, w, g)
+    assert_close(host(gw), rw, dt, "shared grad_w")
+    with pytest.raises(cg.CgtpError, match="workspace"):
+        cg._check(cg.lib().cgtp_backward(plan._h, B, cg._ptr(dev(x)), cg._ptr(dev(y)),
+                                         cg._ptr(dev(w)), cg._ptr(dev(g)), None, None,
+                                         cg._ptr(torch.empty_like(dev(w))), cg._stream()))
 
 
 def test_empty_batch_is_noop():

@@ -111,7 +111,14 @@ def test_c_abi_argument_errors():
     assert L.cgtp_plan_destroy(h) == 0
     s = cg.Plan("2x0e", "0e", "2x0e", shared_weights=True)
     gx = ctypes.c_void_p(0x1000)
-    assert L.cgtp_backward(s._h, 1, gx, gx, gx, gx, null, null, gx, null) == 4
+    # shared-weight gradient: needs the workspace variant, and enough scratch
+    assert L.cgtp_backward(s._h, 1, gx, gx, gx, gx, null, null, gx, null) == 1
+    n = ctypes.c_size_t()
+    assert L.cgtp_weight_grad_workspace(s._h, ctypes.byref(n)) == 0 and n.value == 2048 * 2 * 4
+    assert L.cgtp_backward_ws(s._h, 1, gx, gx, gx, gx, null, null, gx, gx, ctypes.c_size_t(8),
+                              null) == 1
+    pe = cg.Plan("2x0e", "0e", "2x0e")
+    assert L.cgtp_weight_grad_workspace(pe._h, ctypes.byref(n)) == 0 and n.value == 0
 
 
 @pytest.mark.parametrize("irreps,dtype", [(W.CFG0, "f32"), (W.CFG2, "f32"), (W.CFG4, "f32"),
