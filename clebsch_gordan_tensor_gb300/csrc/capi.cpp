@@ -674,3 +674,44 @@ const char* cgtp_last_error_message(void) { return t_msg.c_str(); }
 int64_t cgtp_launch_count(void) { return g_launches.load(); }
 
 }  // extern "C"
+
+namespace cgtp {
+
+// Gradient of the fused convolution with the shared-weight partial rows
+// written to `scratch` (at most scratch_bytes / row bytes of them); used by the
+// entry point whose scratch is a fixed device array.
+cgtp_status conv_backward_into_scratch(cgtp_plan plan, int64_t N, int64_t E,
+                                       const int32_t* s_rowptr, const int32_t* s_perm,
+                                       const int32_t* s_recv, const void* x, const void* y,
+                                       const void* w, double scale, const void* grad_out,
+                                       void* grad_x, void* grad_y, void* grad_w, void* scratch,
+                                       size_t scratch_bytes, cudaStream_t s) {
+    if (!plan) return fail(CGTP_E_ARG, "plan is NULL");
+    cgtp_status st = check_graph(N, E, s_rowptr, s_perm);
+    if (st != CGTP_OK) return st;
+    if (E > 0 && !s_recv) return fail(CGTP_E_GRAPH, "NULL s_recv");
+    Plan& p = plan->p;
+    const int64_t row = p.wdim * (int64_t)esize(p);
+    const bool shared = p.wmode == CGTP_W_SHARED && grad_w;
+    const int64_t rows = shared ? (int64_t)(scratch_bytes / (size_t)row) : 0;
+    if (shared && rows < 1)
+        return fail(CGTP_E_ARG, "weight row of " + std::to_string(row) +
+                                    " bytes exceeds the fixed scratch of " +
+                                    std::to_string(scratch_bytes) + " bytes");
+    if (N == 0) return shared ? zero(grad_w, row, s) : CGTP_OK;
+    if (!x || !grad_out || (E > 0 && (!y || !w))) return fail(CGTP_E_ARG, "NULL input tensor");
+    if ((st = check_rows(p, {x, w, grad_out, grad_x, grad_w})) != CGTP_OK) return st;
+    return bwd_launch(p, true, N, s_rowptr, s_perm, s_recv, x, y, w, grad_out, scale, grad_x,
+                      grad_y, grad_w, grad_x ? 1 : 0, grad_y ? 1 : 0, grad_w ? 1 : 0, s, scratch,
+                      std::min<int64_t>(rows, kSharedWRows));
+}
+
+// True once the plan's kernels are loaded (loading them allocates device memory).
+bool plan_module_loaded(cgtp_plan plan) {
+    if (!plan) return false;
+    std::lock_guard<std::mutex> g(plan->p.mu);
+    auto it = plan->p.modules.find("tp");
+    return it != plan->p.modules.end() && it->second->lib != nullptr;
+}
+
+}  // namespace cgtp

@@ -50,4 +50,12 @@ cudaError_t launch_reduce_rows(bool f64, const void* partial, int64_t rows, int6
 // Partial weight-gradient rows a shared-weight backward may write (grid cap).
 constexpr int64_t kSharedWRows = 2048;
 
+cgtp_status conv_backward_into_scratch(cgtp_plan plan, int64_t N, int64_t E,
+                                       const int32_t* s_rowptr, const int32_t* s_perm,
+                                       const int32_t* s_recv, const void* x, const void* y,
+                                       const void* w, double scale, const void* grad_out,
+                                       void* grad_x, void* grad_y, void* grad_w, void* scratch,
+                                       size_t scratch_bytes, cudaStream_t s);
+bool plan_module_loaded(cgtp_plan plan);
+
 }  // namespace cgtp

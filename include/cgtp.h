@@ -203,6 +203,29 @@ cgtp_status cgtp_conv_backward_ws(cgtp_plan plan, int64_t N, int64_t E, const in
                                   const void* grad_out, void* grad_x, void* grad_y, void* grad_w,
                                   void* workspace, size_t workspace_bytes, cgtp_stream stream);
 
+/* cgtp_conv_backward_ws without a workspace argument, for callers that cannot
+ * allocate device memory when they need the gradient (a framework whose own
+ * pool owns all device memory, a plugin under a fixed memory budget, a loop
+ * that cannot take the implicit synchronisation of cudaMalloc / cudaFree).
+ * The pages have no counterpart: this entry point only changes where the
+ * scratch lives.  The scratch is a fixed 8 MiB device array inside the library
+ * (every GPU that loads the library holds it until exit); weight rows larger
+ * than 8 MiB are rejected with CGTP_E_ARG, and at most min(2048, 8 MiB /
+ * weight row bytes) partial rows are used.  The first call on a device looks up the
+ * array's device address (set-up; make that first call before any stream
+ * capture).  The plan's kernels must already be loaded on the device by a call
+ * through another entry point (loading allocates), else CGTP_E_ARG.  Every call
+ * shares the one array and overwrites all of the rows it reads, so nothing in
+ * it needs clearing; calls whose kernels overlap on the GPU race on it.  No
+ * call allocates or frees device memory. */
+cgtp_status cgtp_conv_backward_noalloc(cgtp_plan plan, int64_t N, int64_t E,
+                                       const int32_t* rowptr, const int32_t* sender,
+                                       const int32_t* s_rowptr, const int32_t* s_perm,
+                                       const int32_t* s_recv, const void* x, const void* y,
+                                       const void* w, double scale, const void* grad_out,
+                                       void* grad_x, void* grad_y, void* grad_w,
+                                       cgtp_stream stream);
+
 /* The identity of cgtp_double_backward applied to the fused convolution.
  * CGTP_W_SHARED plans: d_w is not supported (CGTP_E_UNSUPPORTED if non-NULL). */
 cgtp_status cgtp_conv_double_backward(cgtp_plan plan, int64_t N, int64_t E, const int32_t* rowptr,
