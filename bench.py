@@ -46,29 +46,39 @@ def _peaks():
     if os.path.exists(p):
         d = json.load(open(p))
         return dict(hbm=float(d["hbm_gbs"]), sm_max_mhz=float(d.get("sm_max_mhz", 2070.0)),
+                    bf16=float(d["bf16_tflops"]) if "bf16_tflops" in d else None,
                     src="measured")
-    return dict(hbm=6800.0, sm_max_mhz=2070.0, src="fallback")
+    return dict(hbm=6800.0, sm_max_mhz=2070.0, bf16=1900.0, src="fallback")
 
+
+# nominal dense tensor rates per GPU: tf32 1.1 PFLOP/s against bf16 2.25 PFLOP/s
+TF32_PER_BF16 = 1.1 / 2.25
 
 # ------------------------------------------------------------ work counts
 
-def tp_flops_per_row(prob):
-    """FLOPs of one tensor product (one edge or sample): mul * sum_p 2 (nnz_p +
-    d_l3) -- the sparse CG multiply-adds plus the weight multiply per output
-    component."""
-    import oracle as O  # CG nonzero counts only
-    mul = prob.paths[0][6]
-    nnz = sum(int((np.abs(O.cg_real(l1, l2, l3)) > 0).sum())
-              for (_, _, _, l1, l2, l3, *_r) in prob.paths)
-    d3 = sum(2 * p[5] + 1 for p in prob.paths)
-    return mul * 2 * (nnz + d3)
+class Dims:
+    """Row widths and FLOPs per row of a plan, read from the library's own plan
+    (path list and CG tables); the oracle is not involved."""
+
+    def __init__(self, plan):
+        self.dim1, self.dim2, self.dimo, self.wdim = (plan.dim_in1, plan.dim_in2, plan.dim_out,
+                                                      plan.weight_numel)
+        mul = plan.weight_numel // plan.n_paths
+        nnz = d3 = 0
+        for p in range(plan.n_paths):
+            nnz += int((np.abs(plan.coefficients(p)) > 0).sum())
+            d3 += 2 * plan.path(p)[2] + 1
+        # FLOPs of one tensor product (one edge or sample): mul * sum_p 2 (nnz_p
+        # + d_l3) -- the sparse CG multiply-adds plus the weight multiply per
+        # output component
+        self.flops = mul * 2 * (nnz + d3)
 
 
-def conv_counts(prob, N, E, es):
+def conv_counts(d: Dims, N, E, es):
     """Algorithmic bytes and FLOPs per launch: every tensor read or written
     once, gathered node rows assumed to hit L2."""
-    dx, dy, do, dw = prob.dim1, prob.dim2, prob.dimo, prob.wdim
-    f = tp_flops_per_row(prob)
+    dx, dy, do, dw = d.dim1, d.dim2, d.dimo, d.wdim
+    f = d.flops
     fwd = E * (dw + dy) * es + 4 * E + 4 * (N + 1) + N * (dx + do) * es
     bwd = (E * (dw + dy) * es + N * (dx + do + dx) * es + E * (dw + dy) * es
            + 12 * E + 4 * (N + 1))
@@ -162,20 +172,24 @@ class Workload:
     """A named sequence of launches forming one step, with work counts."""
 
     def __init__(self, name, desc, units, unit, dtype, kernels, counts, fwd_names, cfg,
-                 e2e=None, oracle_step=None):
+                 e2e=None, oracle_step=None, oracle_prep=None, side=None):
         self.name, self.desc, self.units, self.unit, self.dtype = name, desc, units, unit, dtype
         self.kernels, self.counts, self.fwd_names, self.cfg = kernels, counts, fwd_names, cfg
-        self.e2e, self.oracle_step = e2e, oracle_step
+        self.e2e, self.oracle_step, self.oracle_prep = e2e, oracle_step, oracle_prep
+        # kernels outside the step, timed on their own: name -> (call, bytes, flops)
+        self.side = side or {}
+        self.e2e_note = None
 
 
 def make_conv(args, cg, W, torch):
-    import oracle as O
     cfg = W.config2(N=args.atoms)
     gr = cfg["graph"]
     N, E = gr.N, gr.E
     plan = cg.Plan(*cfg["irreps"])
     G = cg.Graph.from_numpy(gr)
-    x, vec, w = (torch.from_numpy(cfg[k]).cuda() for k in ("x", "vec", "w"))
+    x, vec, W1, W2 = (torch.from_numpy(cfg[k]).cuda() for k in ("x", "vec", "W1", "W2"))
+    # per-edge weights from the radial network, on the device
+    w = cg.radial_forward(vec, W1, W2, cfg["cutoff"])
     g = torch.from_numpy(np.random.default_rng(7).standard_normal(
         (N, plan.dim_out)).astype(np.float32)).cuda()
     scale = cfg["scale"]
@@ -190,56 +204,69 @@ def make_conv(args, cg, W, torch):
         ("conv_bwd", lambda: plan.conv_backward(G, x, y, w, scale, g, out=(gx, gy, gw))),
         ("sh_bwd", lambda: cg.sh_backward(vec, gy, 3, out=gvec)),
     ]
-    prob = O.make_problem(*cfg["irreps"])
     desc = (f"fused CG-TP conv: N={N} atoms, density 0.1/A^3, cutoff 5 A, 64x(0e,1o,2e) (x) "
             "Y(l<=3) -> 64x(0e,1o,1e,2o,2e,3o,3e), 24 uvu paths, fp32")
 
     def e2e_step_factory():
-        hx, hv, hw = (torch.from_numpy(cfg[k]).pin_memory() for k in ("x", "vec", "w"))
+        # the step's inputs are what a model layer holds: node features, edge
+        # vectors and the radial network's parameters; the per-edge weights
+        # are computed on the device every step
+        hx, hv, h1, h2 = (torch.from_numpy(cfg[k]).pin_memory() for k in ("x", "vec", "W1", "W2"))
         ho = torch.empty(N, plan.dim_out).pin_memory()
         hgx = torch.empty(N, plan.dim_in1).pin_memory()
 
         def step():
             x.copy_(hx, non_blocking=True)
             vec.copy_(hv, non_blocking=True)
-            w.copy_(hw, non_blocking=True)
+            W1.copy_(h1, non_blocking=True)
+            W2.copy_(h2, non_blocking=True)
+            cg.radial_forward(vec, W1, W2, cfg["cutoff"], out=w)
             for _, k in kernels:
                 k()
             ho.copy_(out, non_blocking=True)
             hgx.copy_(gx, non_blocking=True)
         nb = lambda ts: sum(t.numel() * t.element_size() for t in ts)
-        return step, nb((hx, hv, hw)), nb((ho, hgx))
+        return step, nb((hx, hv, h1, h2)), nb((ho, hgx))
 
-    return Workload("conv", desc, E, "edges/s", "f32", kernels, conv_counts(prob, N, E, 4),
-                    ["sh_fwd", "conv_fwd"], dict(N=N, E=E, mul=64, paths=plan.n_paths),
-                    e2e_step_factory, lambda R: _oracle_conv_step(prob, cfg, R))
+    hidden, n_out = W2.shape
+    side = {"radial_fwd": (lambda: cg.radial_forward(vec, W1, W2, cfg["cutoff"], out=w),
+                           E * (3 + n_out) * 4 + (8 + n_out) * hidden * 4,
+                           2 * E * (8 * hidden + hidden * n_out))}
+    wl = Workload("conv", desc, E, "edges/s", "f32", kernels,
+                  conv_counts(Dims(plan), N, E, 4), ["sh_fwd", "conv_fwd"],
+                  dict(N=N, E=E, mul=64, paths=plan.n_paths),
+                  e2e_step_factory, lambda R: _oracle_conv_step(cfg, R),
+                  oracle_prep=lambda: _oracle_weights(cfg), side=side)
+    wl.e2e_note = ("every step: H2D of x, edge vectors and the radial network's parameters "
+                   "(pinned), radial network on the device (per-edge weights), SH, conv fwd, "
+                   "conv bwd, SH bwd, D2H of out and grad_x")
+    return wl
 
 
 def make_conv64(args, cg, W, torch):
-    import oracle as O
     cfg = W.config3()
     gr = cfg["graph"]
     N, E = gr.N, gr.E
     plan = cg.Plan(*cfg["irreps"], dtype=torch.float64)
     G = cg.Graph.from_numpy(gr)
-    x, vec, w = (torch.from_numpy(cfg[k]).cuda() for k in ("x", "vec", "w"))
+    x, vec, W1, W2 = (torch.from_numpy(cfg[k]).cuda() for k in ("x", "vec", "W1", "W2"))
+    w = cg.radial_forward(vec, W1, W2, cfg["cutoff"])
     y = torch.empty(E, plan.dim_in2, device="cuda", dtype=torch.float64)
     out = torch.empty(N, plan.dim_out, device="cuda", dtype=torch.float64)
     plan.compile()
     kernels = [("sh_fwd", lambda: cg.sh_forward(vec, 3, out=y)),
                ("conv_fwd", lambda: plan.conv_forward(G, x, y, w, cfg["scale"], out=out))]
-    prob = O.make_problem(*cfg["irreps"])
-    c = conv_counts(prob, N, E, 8)
+    c = conv_counts(Dims(plan), N, E, 8)
     counts = {k: c[k] for k in ("sh_fwd", "conv_fwd")}
     desc = (f"fused CG-TP conv fp64: N={N} atoms, 128x(0e,1o,2e) (x) Y(l<=3) -> "
             "128x(0e,1o,1e,2o,2e,3o,3e), 24 uvu paths, forward only")
     return Workload("conv64", desc, E, "edges/s", "f64", kernels, counts, ["sh_fwd", "conv_fwd"],
                     dict(N=N, E=E, mul=128, paths=plan.n_paths), None,
-                    lambda R: _oracle_conv_step(prob, cfg, R, bwd=False))
+                    lambda R: _oracle_conv_step(cfg, R, bwd=False),
+                    oracle_prep=lambda: _oracle_weights(cfg))
 
 
 def make_tp(args, cg, W, torch):
-    import oracle as O
     cfg = W.config1()
     B = cfg["B"]
     plan = cg.Plan(*cfg["irreps"])
@@ -259,8 +286,8 @@ def make_tp(args, cg, W, torch):
                ("tp_fwd", lambda: plan.forward(x, y, w, out=out)),
                ("tp_bwd", bwd),
                ("sh_bwd", lambda: cg.sh_backward(vec, res["g"][1], 3, out=gvec))]
-    prob = O.make_problem(*cfg["irreps"])
-    f = tp_flops_per_row(prob)
+    prob = Dims(plan)
+    f = prob.flops
     rowb = (prob.dim1 + prob.dim2 + prob.wdim) * 4
     counts = {"sh_fwd": (B * (3 + prob.dim2) * 4, None),
               "tp_fwd": (B * (rowb + prob.dimo * 4), B * f),
@@ -270,11 +297,10 @@ def make_tp(args, cg, W, torch):
             "128x(0e,1o,1e,2o,2e,3o,3e), 24 uvu paths, fp32")
     return Workload("tp", desc, B, "samples/s", "f32", kernels, counts, ["sh_fwd", "tp_fwd"],
                     dict(B=B, mul=128, paths=plan.n_paths), None,
-                    lambda R: _oracle_tp_step(prob, cfg, R))
+                    lambda R: _oracle_tp_step(cfg, R))
 
 
 def make_tfn(args, cg, W, torch):
-    import oracle as O
     cfg = W.config4()
     gr = cfg["graph"]
     N, E = gr.N, gr.E
@@ -299,7 +325,7 @@ def make_tfn(args, cg, W, torch):
         ("conv_dbl", lambda: plan.conv_double_backward(G, x, y, w, 1.0, c, None, ggy, None,
                                                        need=(True, False, True, False))),
     ]
-    prob = O.make_problem(*cfg["irreps"])
+    prob = Dims(plan)
     cc = conv_counts(prob, N, E, 4)
     counts = {"sh_fwd": cc["sh_fwd"], "conv_fwd": cc["conv_fwd"], "conv_bwd": cc["conv_bwd"],
               "sh_bwd": cc["sh_bwd"], "forces": (E * 12 + N * 12, None),
@@ -363,6 +389,7 @@ def run_gpu(args):
     e2e = None
     if wl.e2e is not None and not args.no_e2e:
         e2e = run_e2e(args, wl)
+    side = {n: time_side(torch, fn) for n, (fn, _, _) in wl.side.items()}
     if rank != 0:
         return None
 
@@ -384,6 +411,20 @@ def run_gpu(args):
             ent["bound"] = "hbm"
             ent["roofline_frac"] = gbs / peaks["hbm"]
         kernels[n] = ent
+    side_out = {}
+    for n, ms in side.items():
+        _, nbytes, flops = wl.side[n]
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        tf = flops / (ms * 1e-3) / 1e12
+        # tensor-core rate of the split TF32 products (three per multiply-add)
+        # against the measured bf16 GEMM peak scaled by the nominal tf32/bf16 ratio
+        tf32_peak = peaks["bf16"] * TF32_PER_BF16 if peaks.get("bf16") else None
+        side_out[n] = {"ms": ms, "hbm_gbs": gbs, "hbm_frac": gbs / peaks["hbm"], "tflops": tf,
+                       "tf32_issued_tflops": 3 * tf,
+                       "tf32_frac": 3 * tf / tf32_peak if tf32_peak else None,
+                       "bound": "hbm", "roofline_frac": gbs / peaks["hbm"],
+                       "note": "outside the step: per-edge weights from the radial network, "
+                               "recomputed every step of the e2e leg"}
     dom = max(names, key=lambda n: per[n])
     kd = kernels[dom]
     if kd["bound"] == "alu":
@@ -405,7 +446,8 @@ def run_gpu(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
         "data": "synthetic (seeded; see workloads/)", "config": config,
         "fwd": {"value": wl.units * world / (fwd_ms * 1e-3), "unit": wl.unit, "ms": fwd_ms},
-        "roofline": roof, "kernels": kernels, "gpu_launches": launches,
+        "roofline": roof, "kernels": kernels, "side_kernels": side_out or None,
+        "gpu_launches": launches,
         "clocks": clk.summary(), "e2e": e2e,
     }
     if not args.no_cpu_baseline and wl.oracle_step is not None:
@@ -430,6 +472,20 @@ def _traffic(workload, kernel):
     return d.get("bytes") if d.get("kernel_sha") == h.hexdigest()[:16] else None
 
 
+def time_side(torch, fn, reps: int = 10) -> float:
+    """Mean CUDA-event time (ms) of a kernel run on its own, after warm-up."""
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        fn()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / reps
+
+
 def run_e2e(args, wl):
     """The same step through the public API with host buffers: every step
     copies its inputs from pinned host memory and reads its results back."""
@@ -446,15 +502,35 @@ def run_e2e(args, wl):
     b.record()
     torch.cuda.synchronize()
     ms = a.elapsed_time(b) / steps
-    return {"value": wl.units / (ms * 1e-3), "unit": wl.unit, "ms_per_step": ms,
+    line = {"value": wl.units / (ms * 1e-3), "unit": wl.unit, "ms_per_step": ms,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+    if wl.e2e_note:
+        line["note"] = wl.e2e_note
+    return line
 
 
 # ------------------------------------------------------------ CPU oracle
 
-def _oracle_conv_step(prob, cfg, R, bwd=True):
+def _oracle_weights(cfg):
+    """The oracle's per-edge weights of a conv workload (computed once, before
+    any timing: they are an input of the timed oracle step)."""
+    import oracle as O
+    if "w" not in cfg:
+        cfg["w"] = O.radial_forward(cfg["vec"], cfg["W1"], cfg["W2"], cfg["cutoff"],
+                                    out_dtype=cfg["dtype"])[0]
+
+
+def _oracle_problem(cfg):
+    import oracle as O
+    if "prob" not in cfg:
+        cfg["prob"] = O.make_problem(*cfg["irreps"])
+    return cfg["prob"]
+
+
+def _oracle_conv_step(cfg, R, bwd=True):
     """Oracle forward (+ backward) of the receivers [0, R) and their edges."""
     import oracle as O
+    prob = _oracle_problem(cfg)
     gr = cfg["graph"]
     e1 = int(gr.rowptr[R])
     # receivers R.. keep no edges; senders still index all N nodes
@@ -470,8 +546,9 @@ def _oracle_conv_step(prob, cfg, R, bwd=True):
     return e1
 
 
-def _oracle_tp_step(prob, cfg, R):
+def _oracle_tp_step(cfg, R):
     import oracle as O
+    prob = _oracle_problem(cfg)
     x, vec, w = cfg["x"][:R], cfg["vec"][:R], cfg["w"][:R]
     y = O.sh(3, vec)
     out = O.tp_forward(prob, x, y, w)
@@ -483,6 +560,8 @@ def _oracle_tp_step(prob, cfg, R):
 def cpu_baseline(wl, budget_s: float = 15.0, R0: int = 4):
     """The oracle as it stands (one host thread) on a bounded sample of the
     same workload sized to about ``budget_s`` seconds."""
+    if wl.oracle_prep is not None:
+        wl.oracle_prep()
     t = time.perf_counter()
     wl.oracle_step(R0)
     dt = time.perf_counter() - t
@@ -503,14 +582,15 @@ def run_reference(args):
     import oracle as O
     import workloads as W
     cfg = W.config2()
-    prob = O.make_problem(*cfg["irreps"])
+    _oracle_problem(cfg)
+    _oracle_weights(cfg)
     R = 24
     for _ in range(args.warmup):
-        _oracle_conv_step(prob, cfg, 4)
+        _oracle_conv_step(cfg, 4)
     t = time.perf_counter()
     edges = 0
     for _ in range(args.steps):
-        edges += _oracle_conv_step(prob, cfg, R)
+        edges += _oracle_conv_step(cfg, R)
     dt = time.perf_counter() - t
     v = edges / dt
     desc = ("fused CG-TP conv: N=10000 atoms, density 0.1/A^3, cutoff 5 A, 64x(0e,1o,2e) (x) "

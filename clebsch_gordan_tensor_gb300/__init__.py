@@ -81,6 +81,12 @@ def lib() -> ctypes.CDLL:
                 "cgtp_conv_backward_ws": [vp, i64, i64, vp, vp, vp, vp, vp, vp, vp, vp,
                                           ctypes.c_double, vp, vp, vp, vp, vp, ctypes.c_size_t,
                                           vp],
+                "cgtp_conv_backward_noalloc": [vp, i64, i64, vp, vp, vp, vp, vp, vp, vp, vp,
+                                               ctypes.c_double, vp, vp, vp, vp, vp],
+                "cgtp_radial_forward": [i32, i64, i32, ctypes.c_double, i32, i64, vp, vp, vp,
+                                        vp, vp, ctypes.c_uint, vp],
+                "cgtp_radial_path": [i32, i32, i32, i64, P(i32)],
+                "cgtp_radial_device_status": [P(i32)],
             }
             for name, args in sig.items():
                 f = getattr(L, name)
@@ -364,6 +370,42 @@ def sh_jvp(vec, tangent_vec, lmax: int, out=None):
     _check(lib().cgtp_sh_jvp(lmax, _dt(vec.dtype), E, _ptr(vec), _ptr(tangent_vec), _ptr(out),
                              _stream()))
     return out
+
+
+def radial_forward(vec, W1, W2, cutoff: float = 5.0, out=None, hidden_out=None,
+                   cuda_cores: bool = False):
+    """Per-edge weights of the radial network: w[e] = silu(b(|vec[e]|) W1) W2
+    with the Bessel basis b_n(r) = sqrt(2/rc) sin(n pi r / rc) / r.  Returns w
+    [E, n_out]; ``hidden_out`` [E, hidden], if given, receives silu(b W1)."""
+    E = vec.shape[0]
+    _need(vec, "vec", vec.dtype, (E, 3))
+    nb, hidden = W1.shape
+    _need(W1, "W1", vec.dtype, (nb, hidden))
+    n_out = W2.shape[1]
+    _need(W2, "W2", vec.dtype, (hidden, n_out))
+    if out is None:
+        out = torch.empty(E, n_out, dtype=vec.dtype, device=vec.device)
+    _need(out, "out", vec.dtype, (E, n_out))
+    _need(hidden_out, "hidden_out", vec.dtype, (E, hidden))
+    _check(lib().cgtp_radial_forward(_dt(vec.dtype), E, nb, float(cutoff), hidden, n_out,
+                                     _ptr(vec), _ptr(W1), _ptr(W2), _ptr(out), _ptr(hidden_out),
+                                     1 if cuda_cores else 0, _stream()))
+    return out
+
+
+def radial_uses_tensor_cores(dtype, n_basis: int, hidden: int, n_out: int) -> bool:
+    """Whether radial_forward takes the tensor-core path for these sizes (with
+    16-byte aligned tensors)."""
+    v = ctypes.c_int(0)
+    _check(lib().cgtp_radial_path(_dt(dtype), n_basis, hidden, n_out, ctypes.byref(v)))
+    return bool(v.value)
+
+
+def radial_device_status() -> int:
+    """Reads and clears the radial kernels' device error flag (synchronous)."""
+    v = ctypes.c_int(0)
+    _check(lib().cgtp_radial_device_status(ctypes.byref(v)))
+    return int(v.value)
 
 
 def edge_forces(g: Graph, dEdr, out=None):

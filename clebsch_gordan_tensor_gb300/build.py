@@ -55,7 +55,7 @@ def build(verbose: bool = False) -> str:
         jobs.append((obj, [src, *headers], cmd))
     jobs.append((embed + ".o", [embed],
                  ["g++", "-std=c++17", "-O2", "-fPIC", "-c", embed, "-o", embed + ".o"]))
-    for name in ("sh.cu", "graph.cu", "noalloc.cu"):
+    for name in ("sh.cu", "graph.cu", "radial.cu", "noalloc.cu"):
         src = os.path.join(CSRC, name)
         obj = os.path.join(OUT, name + ".o")
         cmd = [os.path.join(CUDA, "bin", "nvcc"), *ARCH, "-std=c++17", "-O3", "-lineinfo",

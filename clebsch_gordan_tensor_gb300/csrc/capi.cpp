@@ -6,6 +6,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <cmath>
 #include <mutex>
 #include <climits>
 #include <cstring>
@@ -607,6 +608,60 @@ cgtp_status cgtp_sh_jvp(int lmax, cgtp_dtype dtype, int64_t E, const void* vec,
     cudaError_t e = launch_sh_jvp(lmax, dtype == CGTP_F64, E, vec, tangent_vec, tangent_y, S(stream));
     if (e != cudaSuccess) return cuda_fail(e, "sh_jvp");
     count_launch();
+    return CGTP_OK;
+    GUARD_END
+}
+
+static cgtp_status radial_check(cgtp_dtype dt, int64_t E, int nb, double cutoff, int hidden,
+                                int64_t n_out) {
+    if (dt != CGTP_F32 && dt != CGTP_F64) return fail(CGTP_E_ARG, "bad dtype");
+    if (E < 0) return fail(CGTP_E_ARG, "E < 0");
+    if (nb < 1 || nb > 32) return fail(CGTP_E_ARG, "n_basis must be in 1..32");
+    if (hidden < 1 || hidden > 256) return fail(CGTP_E_ARG, "hidden must be in 1..256");
+    if (n_out < 1) return fail(CGTP_E_ARG, "n_out must be >= 1");
+    if (!(cutoff > 0.0) || !std::isfinite(cutoff)) return fail(CGTP_E_ARG, "cutoff must be > 0");
+    return CGTP_OK;
+}
+
+cgtp_status cgtp_radial_forward(cgtp_dtype dtype, int64_t E, int n_basis, double cutoff,
+                                int hidden, int64_t n_out, const void* vec, const void* W1,
+                                const void* W2, void* w, void* h, unsigned flags,
+                                cgtp_stream stream) {
+    GUARD_BEGIN
+    cgtp_status st = radial_check(dtype, E, n_basis, cutoff, hidden, n_out);
+    if (st != CGTP_OK || E == 0) return st;
+    if (!vec || !W1 || !W2 || !w) return fail(CGTP_E_ARG, "NULL tensor");
+    const size_t es = dtype == CGTP_F64 ? 8 : 4;
+    for (const void* q : {vec, W1, W2, (const void*)w, (const void*)h})
+        if (!aligned(q, es)) return fail(CGTP_E_ARG, "tensor pointer not aligned to its element");
+    const bool f64 = dtype == CGTP_F64;
+    const bool tc = !(flags & CGTP_RADIAL_CUDA_CORES) &&
+                    radial_tc_eligible(f64, n_basis, hidden, n_out, vec, W2, w, h);
+    cudaError_t e = launch_radial_forward(f64, tc, E, n_basis, cutoff, hidden, n_out, vec, W1,
+                                          W2, w, h, S(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "radial_forward");
+    count_launch();
+    return CGTP_OK;
+    GUARD_END
+}
+
+cgtp_status cgtp_radial_path(cgtp_dtype dtype, int n_basis, int hidden, int64_t n_out,
+                             int* tensor_cores) {
+    GUARD_BEGIN
+    cgtp_status st = radial_check(dtype, 0, n_basis, 1.0, hidden, n_out);
+    if (st != CGTP_OK) return st;
+    if (!tensor_cores) return fail(CGTP_E_ARG, "NULL output");
+    *tensor_cores = radial_tc_eligible(dtype == CGTP_F64, n_basis, hidden, n_out, nullptr,
+                                       nullptr, nullptr, nullptr) ? 1 : 0;
+    return CGTP_OK;
+    GUARD_END
+}
+
+cgtp_status cgtp_radial_device_status(int* code) {
+    GUARD_BEGIN
+    if (!code) return fail(CGTP_E_ARG, "NULL output");
+    cudaError_t e = radial_device_status(code);
+    if (e != cudaSuccess) return cuda_fail(e, "radial_device_status");
     return CGTP_OK;
     GUARD_END
 }

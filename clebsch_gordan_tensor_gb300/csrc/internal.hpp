@@ -47,6 +47,14 @@ cudaError_t launch_fill_zero(void* p, int64_t bytes, cudaStream_t s);
 cudaError_t launch_reduce_rows(bool f64, const void* partial, int64_t rows, int64_t cols,
                                void* out, cudaStream_t s);
 
+// Radial network (radial.cu).
+bool radial_tc_eligible(bool f64, int nb, int hidden, int64_t n_out, const void* vec,
+                        const void* W2, const void* w, const void* h);
+cudaError_t launch_radial_forward(bool f64, bool tensor_cores, int64_t E, int nb, double rc,
+                                  int hidden, int64_t n_out, const void* vec, const void* W1,
+                                  const void* W2, void* w, void* h, cudaStream_t s);
+cudaError_t radial_device_status(int* code);
+
 // Partial weight-gradient rows a shared-weight backward may write (grid cap).
 constexpr int64_t kSharedWRows = 2048;
 

@@ -264,6 +264,38 @@ cgtp_status cgtp_edge_forces_adjoint(cgtp_dtype dtype, int64_t N, int64_t E,
                                      const int32_t* rowptr, const int32_t* sender,
                                      const void* grad_forces, void* grad_dEdr, cgtp_stream stream);
 
+/* --------------------------------------------------- radial network ---- */
+/* Per-edge tensor-product weights from the radial network: the radial profile
+ * of a TFN layer is a fully connected network of the edge length (NVIDIA
+ * SE(3)-Transformer blog, "Fused key and value computation").  For edge e with
+ * r = |vec[e]|:
+ *   b_n  = sqrt(2/cutoff) sin(n pi r / cutoff) / r,  n = 1..n_basis
+ *          (at r = 0 its limit sqrt(2/cutoff) n pi / cutoff)
+ *   h[e] = silu(b W1),  silu(a) = a / (1 + exp(-a))
+ *   w[e] = h[e] W2
+ * vec [E,3], W1 [n_basis, hidden], W2 [hidden, n_out], w [E, n_out] and the
+ * optional h [E, hidden] (NULL: not stored) are row-major device arrays of
+ * `dtype`, owned by the caller; w and h are overwritten.  Limits:
+ * 1 <= n_basis <= 32, 1 <= hidden <= 256, n_out >= 1, cutoff > 0; else
+ * CGTP_E_ARG.  fp32 with hidden % 8 == 0, hidden <= 64, n_out % 128 == 0 and
+ * 16-byte aligned vec / W2 / w / h runs the last layer on the tensor cores
+ * (TF32 in three split products, fp32 accuracy); other shapes, fp64, or
+ * flags & CGTP_RADIAL_CUDA_CORES run it on the CUDA cores.  Asynchronous on
+ * `stream`; allocates nothing. */
+#define CGTP_RADIAL_CUDA_CORES 1u
+cgtp_status cgtp_radial_forward(cgtp_dtype dtype, int64_t E, int n_basis, double cutoff,
+                                int hidden, int64_t n_out, const void* vec, const void* W1,
+                                const void* W2, void* w, void* h, unsigned flags,
+                                cgtp_stream stream);
+/* Host query: *tensor_cores = 1 if cgtp_radial_forward with these sizes (and
+ * 16-byte aligned pointers, flags 0) takes the tensor-core path, else 0. */
+cgtp_status cgtp_radial_path(cgtp_dtype dtype, int n_basis, int hidden, int64_t n_out,
+                             int* tensor_cores);
+/* Reads and clears the radial kernels' device error flag (synchronous): 0, or
+ * 1 when a bounded wait of the tensor-core kernel timed out (its output is then
+ * incomplete). */
+cgtp_status cgtp_radial_device_status(int* code);
+
 /* ------------------------------------------------------------ misc ------ */
 const char* cgtp_status_str(cgtp_status s);
 /* CUDA error code behind the calling thread's last CGTP_E_CUDA / CGTP_E_COMPILE. */

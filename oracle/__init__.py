@@ -369,3 +369,80 @@ def edge_forces(rowptr, sender, dEdr) -> np.ndarray:
     _load().oracle_edge_forces(N, sender.shape[0], _p(rowptr, ctypes.c_int32),
                                _p(sender, ctypes.c_int32), _p(d), _p(F))
     return F
+
+
+# ------------------------------------------------------ radial network ---
+#
+# NVIDIA's SE(3)-Transformer blog, section "Fused key and value computation":
+# the radial profile inside a TFN layer is a fully connected network of the
+# edge length, and it supplies the per-edge weights of the tensor product.
+# The benchmark workload fixes its shape: 8 Bessel functions of the edge
+# length -> Linear(8, hidden) -> SiLU -> Linear(hidden, paths * mul), no
+# biases, no envelope.  Written here in fp64 with numpy matmuls as the only
+# library steps.
+
+def radial_basis(r, n_basis: int, cutoff: float) -> np.ndarray:
+    """b_n(r) = sqrt(2/rc) sin(n pi r / rc) / r for n = 1..n_basis, with its
+    limit sqrt(2/rc) n pi / rc at r = 0.  Returns [E, n_basis]."""
+    r = _f64(r).reshape(-1, 1)
+    n = np.arange(1, n_basis + 1, dtype=np.float64).reshape(1, -1)
+    k = n * np.pi / cutoff
+    safe = np.where(r > 0.0, r, 1.0)
+    b = np.sin(k * r) / safe
+    b = np.where(r > 0.0, b, k)
+    return np.sqrt(2.0 / cutoff) * b
+
+
+def silu(a):
+    """a * sigmoid(a)."""
+    return a / (1.0 + np.exp(-a))
+
+
+def radial_forward(vec, W1, W2, cutoff: float = 5.0, out_dtype=np.float64,
+                   chunk: int = 1 << 15):
+    """Per-edge weights of the radial network.  vec [E, 3] (edge vectors; only
+    their length is used), W1 [n_basis, hidden], W2 [hidden, n_out].
+    Returns (w [E, n_out] in out_dtype, h [E, hidden] fp64): h is the hidden
+    activation silu(basis @ W1), w = h @ W2.  Rows are done in chunks of
+    ``chunk`` edges so large workloads fit in host memory."""
+    v = np.asarray(vec).reshape(-1, 3)
+    W1, W2 = _f64(W1), _f64(W2)
+    if W1.ndim != 2 or W2.ndim != 2 or W1.shape[1] != W2.shape[0]:
+        raise ValueError("W1 [n_basis, hidden] and W2 [hidden, n_out] do not match")
+    E = v.shape[0]
+    w = np.empty((E, W2.shape[1]), dtype=out_dtype)
+    h = np.empty((E, W1.shape[1]))
+    for a in range(0, E, chunk):
+        r = np.linalg.norm(_f64(v[a:a + chunk]), axis=1)
+        h[a:a + chunk] = silu(radial_basis(r, W1.shape[0], cutoff) @ W1)
+        w[a:a + chunk] = h[a:a + chunk] @ W2
+    return w, h
+
+
+def radial_backward(vec, W1, W2, grad_w, cutoff: float = 5.0):
+    """Vector-Jacobian product of ``radial_forward``'s w: returns
+    (grad_vec [E, 3], grad_W1, grad_W2) for the cotangent grad_w [E, n_out].
+    Chain: gh = grad_w W2^T; gpre = gh * silu'(pre) with
+    silu'(a) = s (1 + a (1 - s)), s = sigmoid(a); gW2 = h^T grad_w;
+    gW1 = b^T gpre; gb = gpre W1^T; dr = sum_n gb_n db_n/dr with
+    db_n/dr = sqrt(2/rc) (k_n cos(k_n r) / r - sin(k_n r) / r^2); grad_vec =
+    dr vec / r (zero at r = 0, where the basis is flat)."""
+    v = _f64(vec).reshape(-1, 3)
+    W1, W2, g = _f64(W1), _f64(W2), _f64(grad_w)
+    r = np.linalg.norm(v, axis=1)
+    b = radial_basis(r, W1.shape[0], cutoff)
+    pre = b @ W1
+    s = 1.0 / (1.0 + np.exp(-pre))
+    h = pre * s
+    gh = g @ W2.T
+    gpre = gh * s * (1.0 + pre * (1.0 - s))
+    gW2 = h.T @ g
+    gW1 = b.T @ gpre
+    gb = gpre @ W1.T
+    n = np.arange(1, W1.shape[0] + 1, dtype=np.float64).reshape(1, -1)
+    k = n * np.pi / cutoff
+    rr = np.where(r > 0.0, r, 1.0).reshape(-1, 1)
+    db = np.sqrt(2.0 / cutoff) * (k * np.cos(k * rr) / rr - np.sin(k * rr) / rr ** 2)
+    dr = np.where(r > 0.0, (gb * db).sum(axis=1), 0.0)
+    gvec = v * (dr / np.where(r > 0.0, r, 1.0)).reshape(-1, 1)
+    return gvec, gW1, gW2

@@ -41,3 +41,14 @@ def assert_close(got, ref, dtype, what=""):
     e = relerr(got, ref)
     assert e <= TOL[np.dtype(dtype)], f"{what}: normwise relative error {e:.3e}"
     return e
+
+
+def conv_weights(cfg):
+    """The per-edge weights of a conv workload: the oracle's radial network on
+    the workload's edge vectors and parameters, rounded to the workload dtype
+    (an input shared by both sides of a parity test)."""
+    import oracle as O
+    if "w" not in cfg:
+        cfg["w"] = O.radial_forward(cfg["vec"], cfg["W1"], cfg["W2"], cfg["cutoff"],
+                                    out_dtype=cfg["dtype"])[0]
+    return cfg["w"]

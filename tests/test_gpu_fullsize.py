@@ -14,7 +14,7 @@ import pytest
 
 import oracle as O
 import workloads as W
-from tests.gpu_util import assert_close, dev, host, need_gpu, torch
+from tests.gpu_util import assert_close, conv_weights, dev, host, need_gpu, torch
 
 pytestmark = pytest.mark.gpu
 
@@ -78,6 +78,7 @@ def _conv_sampled(cfg, dt, do_bwd: bool):
     prob = O.make_problem(*cfg["irreps"])
     plan = cg.Plan(*cfg["irreps"], dtype=torch.float64 if dt == np.float64 else torch.float32)
     G = cg.Graph.from_numpy(gr)
+    conv_weights(cfg)
     x, v, w = dev(cfg["x"]), dev(cfg["vec"]), dev(cfg["w"])
     y = cg.sh_forward(v, 3)
     out = plan.conv_forward(G, x, y, w, cfg["scale"])

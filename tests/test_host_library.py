@@ -15,6 +15,7 @@ import pytest
 import oracle as O
 import workloads as W
 import clebsch_gordan_tensor_gb300 as cg
+import torch
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 ALL_CFGS = [W.CFG0, W.CFG1, W.CFG2, W.CFG3, W.CFG4]
@@ -119,6 +120,31 @@ def test_c_abi_argument_errors():
                               null) == 1
     pe = cg.Plan("2x0e", "0e", "2x0e")
     assert L.cgtp_weight_grad_workspace(pe._h, ctypes.byref(n)) == 0 and n.value == 0
+
+
+def test_radial_argument_errors_and_path():
+    L = cg.lib()
+    null = ctypes.c_void_p()
+    # sizes and pointers are checked before any CUDA call
+    args = lambda E, nb, rc, hid, no, p=null: (0, E, nb, rc, hid, no, p, p, p, p, null, 0, null)
+    assert L.cgtp_radial_forward(*args(0, 8, 5.0, 64, 1536)) == 0
+    assert L.cgtp_radial_forward(*args(-1, 8, 5.0, 64, 1536)) == 1
+    assert L.cgtp_radial_forward(*args(4, 0, 5.0, 64, 1536)) == 1
+    assert L.cgtp_radial_forward(*args(4, 33, 5.0, 64, 1536)) == 1
+    assert L.cgtp_radial_forward(*args(4, 8, 0.0, 64, 1536)) == 1
+    assert L.cgtp_radial_forward(*args(4, 8, 5.0, 257, 1536)) == 1
+    assert L.cgtp_radial_forward(*args(4, 8, 5.0, 64, 0)) == 1
+    assert L.cgtp_radial_forward(*args(4, 8, 5.0, 64, 1536)) == 1  # NULL tensors
+    assert L.cgtp_radial_forward(*args(4, 8, 5.0, 64, 1536, ctypes.c_void_p(0x1002))) == 1
+    assert cg.radial_uses_tensor_cores(torch.float32, 8, 64, 1536)
+    assert cg.radial_uses_tensor_cores(torch.float32, 8, 32, 256)
+    assert not cg.radial_uses_tensor_cores(torch.float32, 8, 12, 1536)   # hidden % 8
+    assert not cg.radial_uses_tensor_cores(torch.float32, 8, 128, 1536)  # hidden > 64
+    assert not cg.radial_uses_tensor_cores(torch.float32, 8, 64, 100)    # n_out % 128
+    assert not cg.radial_uses_tensor_cores(torch.float64, 8, 64, 1536)
+    v = ctypes.c_int()
+    assert L.cgtp_radial_path(0, 8, 64, 1536, None) == 1
+    assert L.cgtp_radial_path(0, 40, 64, 1536, ctypes.byref(v)) == 1
 
 
 @pytest.mark.parametrize("irreps,dtype", [(W.CFG0, "f32"), (W.CFG2, "f32"), (W.CFG4, "f32"),

@@ -1,9 +1,11 @@
 """Seeded synthetic inputs for the Clebsch-Gordan tensor-product workloads.
 
 This module is shared by the tests, the benchmark and the oracle checks.  It
-holds no tensor-product, spherical-harmonic or CG arithmetic: it draws random
-numbers, builds neighbour graphs and evaluates the per-edge radial weight
-generator (a fixed random two-layer MLP on a Bessel basis), all in numpy.
+holds none of the library's arithmetic (tensor product, spherical harmonics,
+CG coefficients, the radial network): it draws random numbers and builds
+neighbour graphs, all in numpy.  Conv workloads carry the radial network's
+parameters; the per-edge weights are computed from them by the library on the
+GPU and by the oracle on the host.
 
 The pages measure on QM9, MACE foundation-model inference and water MD (see
 "An Efficient Sparse Kernel Generator for O(3)-Equivariant Deep Networks",
@@ -134,26 +136,15 @@ def molecules(rng, n_mol: int, n_min: int = 9, n_max: int = 29, step=(1.0, 1.6))
     return pos, make_graph(base, recv, send, pos[recv] - pos[send])
 
 
-def radial_weights(rng, r: np.ndarray, n_out: int, cutoff: float = 5.0, n_basis: int = 8,
-                   hidden: int = 64, dtype=np.float32) -> np.ndarray:
-    """Per-edge weights from a fixed random radial MLP:
-    Bessel basis sqrt(2/rc) sin(n pi r / rc) / r, n = 1..8 -> Linear(8, 64) ->
-    SiLU -> Linear(64, n_out); no biases, weights N(0,1)/sqrt(fan_in); the
-    last layer runs in the workload dtype.
-    Draws: W1 [8, 64], W2 [64, n_out] (float64)."""
+def radial_params(rng, n_out: int, n_basis: int = 8, hidden: int = 64, dtype=np.float32):
+    """Parameters of the fixed random radial network that produces the per-edge
+    weights (Bessel(n_basis) -> Linear(n_basis, hidden) -> SiLU ->
+    Linear(hidden, n_out), no biases): W1 [n_basis, hidden] ~ N(0,1)/sqrt(n_basis)
+    and W2 [hidden, n_out] ~ N(0,1)/sqrt(hidden), both rounded to the workload
+    dtype.  Draws: W1, then W2 (float64 normals)."""
     W1 = rng.standard_normal((n_basis, hidden)) / np.sqrt(n_basis)
     W2 = rng.standard_normal((hidden, n_out)) / np.sqrt(hidden)
-    W2c = W2.astype(dtype)
-    n = np.arange(1, n_basis + 1)
-    out = np.empty((r.shape[0], n_out), dtype=dtype)
-    chunk = 1 << 15
-    for a in range(0, r.shape[0], chunk):
-        rr = r[a:a + chunk, None]
-        basis = np.sqrt(2.0 / cutoff) * np.sin(n * np.pi * rr / cutoff) / rr
-        h = basis @ W1
-        h = (h / (1.0 + np.exp(-h))).astype(dtype)
-        out[a:a + chunk] = h @ W2c
-    return out
+    return W1.astype(dtype), W2.astype(dtype)
 
 
 # ---------------------------------------------------------------- configs --
@@ -192,16 +183,18 @@ def config1(B: int = 200_000) -> dict:
 def conv_cloud(seed: int, irreps, N: int, n_paths: int, dtype) -> dict:
     """Fused graph convolution on a periodic atom cloud (density 0.1 / A^3,
     cutoff 5 A).  Draws, in order: positions (``periodic_cloud``); x [N, dim1]
-    ~ N(0,1); radial MLP weights (``radial_weights``, n_out = n_paths * mul).
+    ~ N(0,1); radial network parameters (``radial_params``, n_out = n_paths *
+    mul).  The per-edge weights are that network applied to the edge lengths;
+    this module does not evaluate it (the library and the oracle each do).
     scale = 1 / average degree = N / E."""
     rng = np.random.default_rng(seed)
     pos, L, g = periodic_cloud(rng, N)
     mul = int(irreps[0].split("x")[0])
     x = normal(rng, (N, irreps_dim(irreps[0])), dtype)
-    r = np.linalg.norm(g.vec, axis=1)
-    w = radial_weights(rng, r, n_paths * mul, dtype=dtype)
-    return dict(irreps=irreps, graph=g, pos=pos, box=L, x=x, vec=g.vec.astype(dtype), w=w,
-                lmax=3, scale=float(N) / float(max(g.E, 1)), dtype=np.dtype(dtype))
+    W1, W2 = radial_params(rng, n_paths * mul, dtype=dtype)
+    return dict(irreps=irreps, graph=g, pos=pos, box=L, x=x, vec=g.vec.astype(dtype), W1=W1,
+                W2=W2, cutoff=5.0, lmax=3, scale=float(N) / float(max(g.E, 1)),
+                dtype=np.dtype(dtype))
 
 
 def config2(N: int = 10_000) -> dict:
