@@ -84,7 +84,8 @@ def lib() -> ctypes.CDLL:
                 "cgtp_conv_backward_noalloc": [vp, i64, i64, vp, vp, vp, vp, vp, vp, vp, vp,
                                                ctypes.c_double, vp, vp, vp, vp, vp],
                 "cgtp_radial_forward": [i32, i64, i32, ctypes.c_double, i32, i64, vp, vp, vp,
-                                        vp, vp, ctypes.c_uint, vp],
+                                        vp, vp, vp, ctypes.c_size_t, ctypes.c_uint, vp],
+                "cgtp_radial_workspace": [i32, i32, i32, i64, P(ctypes.c_size_t)],
                 "cgtp_radial_path": [i32, i32, i32, i64, P(i32)],
                 "cgtp_radial_device_status": [P(i32)],
             }
@@ -387,9 +388,12 @@ def radial_forward(vec, W1, W2, cutoff: float = 5.0, out=None, hidden_out=None,
         out = torch.empty(E, n_out, dtype=vec.dtype, device=vec.device)
     _need(out, "out", vec.dtype, (E, n_out))
     _need(hidden_out, "hidden_out", vec.dtype, (E, hidden))
+    n = ctypes.c_size_t(0)
+    _check(lib().cgtp_radial_workspace(_dt(vec.dtype), nb, hidden, n_out, ctypes.byref(n)))
+    ws = torch.empty(n.value, dtype=torch.uint8, device=vec.device) if n.value else None
     _check(lib().cgtp_radial_forward(_dt(vec.dtype), E, nb, float(cutoff), hidden, n_out,
                                      _ptr(vec), _ptr(W1), _ptr(W2), _ptr(out), _ptr(hidden_out),
-                                     1 if cuda_cores else 0, _stream()))
+                                     _ptr(ws), n.value, 1 if cuda_cores else 0, _stream()))
     return out
 
 

@@ -623,10 +623,21 @@ static cgtp_status radial_check(cgtp_dtype dt, int64_t E, int nb, double cutoff,
     return CGTP_OK;
 }
 
+cgtp_status cgtp_radial_workspace(cgtp_dtype dtype, int n_basis, int hidden, int64_t n_out,
+                                  size_t* bytes) {
+    GUARD_BEGIN
+    cgtp_status st = radial_check(dtype, 0, n_basis, 1.0, hidden, n_out);
+    if (st != CGTP_OK) return st;
+    if (!bytes) return fail(CGTP_E_ARG, "NULL output");
+    *bytes = radial_workspace_bytes(dtype == CGTP_F64, n_basis, hidden, n_out);
+    return CGTP_OK;
+    GUARD_END
+}
+
 cgtp_status cgtp_radial_forward(cgtp_dtype dtype, int64_t E, int n_basis, double cutoff,
                                 int hidden, int64_t n_out, const void* vec, const void* W1,
-                                const void* W2, void* w, void* h, unsigned flags,
-                                cgtp_stream stream) {
+                                const void* W2, void* w, void* h, void* workspace,
+                                size_t workspace_bytes, unsigned flags, cgtp_stream stream) {
     GUARD_BEGIN
     cgtp_status st = radial_check(dtype, E, n_basis, cutoff, hidden, n_out);
     if (st != CGTP_OK || E == 0) return st;
@@ -635,10 +646,12 @@ cgtp_status cgtp_radial_forward(cgtp_dtype dtype, int64_t E, int n_basis, double
     for (const void* q : {vec, W1, W2, (const void*)w, (const void*)h})
         if (!aligned(q, es)) return fail(CGTP_E_ARG, "tensor pointer not aligned to its element");
     const bool f64 = dtype == CGTP_F64;
-    const bool tc = !(flags & CGTP_RADIAL_CUDA_CORES) &&
+    const size_t need = radial_workspace_bytes(f64, n_basis, hidden, n_out);
+    const bool tc = !(flags & CGTP_RADIAL_CUDA_CORES) && need > 0 && workspace &&
+                    workspace_bytes >= need && aligned(workspace, 16) &&
                     radial_tc_eligible(f64, n_basis, hidden, n_out, vec, W2, w, h);
     cudaError_t e = launch_radial_forward(f64, tc, E, n_basis, cutoff, hidden, n_out, vec, W1,
-                                          W2, w, h, S(stream));
+                                          W2, w, h, workspace, workspace_bytes, S(stream));
     if (e != cudaSuccess) return cuda_fail(e, "radial_forward");
     count_launch();
     return CGTP_OK;

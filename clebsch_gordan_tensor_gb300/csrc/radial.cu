@@ -10,16 +10,19 @@
 //   w[e]  = h W2                  W2 [hidden, n_out]
 //
 // Two kernels:
-//   * radial_tc_kernel (fp32, hidden % 8 == 0 and <= 64, n_out % 128 == 0):
+//   * radial_tc_kernel (fp32, n_basis <= 16, hidden % 8 == 0 and <= 64,
+//     n_out % 128 == 0):
 //     the last layer -- the only dense contraction, 2 hidden * n_out FLOP per
 //     edge -- runs on the tensor cores.  A tile of 128 edges' hidden
 //     activations (A, 128 x hidden) and a 128-column slice of W2 (B) sit in
 //     shared memory as TF32 "hi" and "lo" parts (x = hi + lo, both TF32);
 //     tcgen05.mma accumulates hi*hi + hi*lo + lo*hi into a 128 x 128 fp32
 //     accumulator in tensor memory, which keeps fp32 accuracy (the dropped
-//     lo*lo term is 2^-22 relative).  One thread issues the MMAs; completion
-//     arrives on an mbarrier; four warps read the accumulator back with
-//     tcgen05.ld and store the rows.
+//     lo*lo term is 2^-22 relative).  Four producer warps build A and B
+//     (double-buffered) and one of their threads issues the MMAs; completion
+//     arrives on an mbarrier; four epilogue warps read the accumulators
+//     (double-buffered in tensor memory) back with tcgen05.ld and store whole
+//     row segments.
 //   * radial_simt_kernel (fp32 / fp64, any shape): shared-memory tiles and
 //     FMA micro-tiles on the CUDA cores.
 // Both compute b and h the same way on the CUDA cores.
@@ -123,16 +126,21 @@ radial_simt_kernel(int64_t E, int nb, T rc, int hidden, int64_t n_out, const T* 
 
 // ------------------------------------------------------------ tensor cores
 
-constexpr int kTcM = 128;         // edges per tile (MMA M, TMEM lanes)
-constexpr int kTcN = 128;         // output columns per chunk (MMA N)
-constexpr int kTcKMax = 64;       // hidden width held in one tile
-constexpr int kTcThreads = 128;   // four warps: one TMEM lane quarter each
-constexpr unsigned kTcTmemCols = 128;
-// Operand bytes: A hi/lo [128 x K] and B hi/lo [128 x K], tf32.
-constexpr unsigned kTcOperand = kTcM * kTcKMax * 4;  // 32 KB each
-// The operand region is followed by padding so that a descriptor stride read
-// the other way round would still stay inside this CTA's shared memory.
-constexpr unsigned kTcSmem = 4 * kTcOperand + 64 * 1024;
+constexpr int kTcM = 128;          // edges per tile (MMA M, TMEM lanes)
+constexpr int kTcN = 128;          // output columns per chunk (MMA N)
+constexpr int kTcKMax = 64;        // hidden width held in one tile
+constexpr int kTcNbMax = 16;       // basis functions held in registers
+constexpr int kTcEpiWarps = 8;     // two per TMEM lane quarter, 64 columns each
+constexpr int kTcProdWarps = 4;    // one edge row per thread
+constexpr int kTcThreads = 32 * (kTcEpiWarps + kTcProdWarps + 1);  // + the MMA issuer warp
+constexpr int kTcBSlots = 2;       // B ring depth
+constexpr unsigned kTcTmemCols = 2 * kTcN;  // two fp32 accumulators
+constexpr unsigned kTcA = kTcM * kTcKMax * 4;   // one tf32 part of A (32 KB)
+constexpr unsigned kTcB = kTcN * kTcKMax * 4;   // one tf32 part of B (32 KB)
+constexpr unsigned kTcStagePitch = 36;                // floats per staged row (conflict-free)
+constexpr unsigned kTcStage = 16 * kTcStagePitch * 4; // one epilogue warp's 16 x 32 half block
+// A hi/lo, the B ring (hi/lo per slot), the epilogue staging blocks
+constexpr unsigned kTcSmem = 2 * kTcA + 2 * kTcBSlots * kTcB + kTcEpiWarps * kTcStage;
 
 __device__ __forceinline__ unsigned smem_addr(const void* p) {
     return (unsigned)__cvta_generic_to_shared(p);
@@ -140,14 +148,15 @@ __device__ __forceinline__ unsigned smem_addr(const void* p) {
 
 // Canonical K-major layout without swizzle: 8-row x 16-byte core matrices;
 // the 8-row groups of one 4-wide K slice are contiguous (128 B apart) and the
-// K slices follow each other (LBO = rows / 8 * 128 B apart).
+// K slices follow each other (rows / 8 * 128 B apart).
 __device__ __forceinline__ unsigned kmajor_offset(int row, int k, int rows) {
     return (unsigned)((k >> 2) * (rows / 8) * 128 + (row >> 3) * 128 + (row & 7) * 16 + (k & 3) * 4);
 }
 
 // Shared-memory matrix descriptor (tcgen05): start >> 4 in bits 0-13, leading
-// byte offset >> 4 in 16-29, stride byte offset >> 4 in 32-45, the fixed
-// version value 1 in bits 46-47, no swizzle (bits 61-63 = 0).
+// byte offset (between K-adjacent core matrices) >> 4 in 16-29, stride byte
+// offset (between 8-row groups) >> 4 in 32-45, the fixed version value 1 in
+// bits 46-47, no swizzle (bits 61-63 = 0).
 __device__ __forceinline__ uint64_t smem_desc(unsigned addr, unsigned lbo, unsigned sbo) {
     return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
            ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46);
@@ -173,8 +182,33 @@ __device__ __forceinline__ void mma_tf32(unsigned tmem_d, uint64_t a, uint64_t b
         : "memory");
 }
 
-__device__ __forceinline__ void tc_mbar_init(unsigned long long* b) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(b)) : "memory");
+__device__ __forceinline__ void tc_commit(unsigned long long* b) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     smem_addr(b))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_mbar_init(unsigned long long* b, unsigned count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(b)), "r"(count)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_mbar_arrive(unsigned long long* b) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(b)) : "memory");
+}
+
+__device__ __forceinline__ void tc_expect_tx(unsigned long long* b, unsigned bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(b)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_bulk_g2s(void* dst, const void* src, unsigned bytes,
+                                            unsigned long long* b) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(b))
+        : "memory");
 }
 
 // Bounded wait for phase `parity` (about a second at most).
@@ -209,19 +243,63 @@ __device__ __forceinline__ void tmem_ld32(unsigned taddr, float (&v)[32]) {
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// W2 packed once per call as the shared-memory image of B: per 128-column
+// chunk c, the TF32 "hi" part then the "lo" part, each 128 rows (output
+// columns) x hidden in the K-major core-matrix layout (128 * hidden * 4 bytes).
+__global__ void radial_pack_kernel(int hidden, int64_t n_out, const float* __restrict__ W2,
+                                   unsigned char* __restrict__ img) {
+    const int64_t total = (int64_t)hidden * n_out;
+    const size_t part = (size_t)kTcN * hidden * 4;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int k = (int)(i / n_out);
+        const int64_t col = i % n_out;
+        const int64_t c = col / kTcN;
+        const int n = (int)(col % kTcN);
+        const float x = W2[i];
+        const float hi = to_tf32(x), lo = to_tf32(x - hi);
+        unsigned char* base = img + (size_t)c * 2 * part + kmajor_offset(n, k, kTcN);
+        *reinterpret_cast<float*>(base) = hi;
+        *reinterpret_cast<float*>(base + part) = lo;
+    }
+}
+
+// Warp roles, all persistent over this CTA's tiles of 128 edges:
+//   producers (warps 8-11): thread = edge row; the hidden activations of the
+//     next tile are computed into registers while the current tile is being
+//     multiplied, then written to A (TF32 hi/lo) once a_free says the last MMA
+//     reading A has completed; arrival on a_full publishes A.
+//   issuer (warp 12, one thread): streams the packed W2 chunks into a 2-slot
+//     ring with bulk copies (b_full), issues each chunk's MMAs into
+//     accumulator chunk % 2 and commits them to mma_done (and, after a tile's
+//     last chunk, to a_free).  Each CTA walks the column chunks in an order
+//     rotated by its index, so the SMs do not all read the same image at once.
+//   epilogue (warps 0-7): per chunk, wait for mma_done, read a 32-row x
+//     64-column block of the accumulator (warp % 4 picks the TMEM lane
+//     quarter, warp / 4 the column half), arrive on acc_free, then transpose
+//     16 x 32 pieces through shared memory and store whole 128-byte row
+//     segments.
+// Chunk k of this CTA uses phase k / 2 of barriers k % 2 (accumulators and
+// ring); tile t uses phase t of a_full and a_free.  Each waiter is never more
+// than one phase behind the barrier it waits on.  Every wait is bounded; a
+// timeout sets `fail`, each role leaves its loop, and the CTA releases its
+// tensor memory after a grace period.
 __global__ void __launch_bounds__(kTcThreads, 1)
 radial_tc_kernel(int64_t E, int nb, float rc, int hidden, int64_t n_out,
                  const float* __restrict__ vec, const float* __restrict__ W1,
-                 const float* __restrict__ W2, float* __restrict__ w, float* __restrict__ h) {
+                 const unsigned char* __restrict__ img, float* __restrict__ w,
+                 float* __restrict__ h) {
     extern __shared__ __align__(1024) unsigned char smem[];
-    __shared__ __align__(8) unsigned long long mma_done;
+    __shared__ __align__(8) unsigned long long mma_done[2], acc_free[2], b_full[kTcBSlots];
+    __shared__ __align__(8) unsigned long long a_full, a_free;
+    __shared__ __align__(16) float W1s[kTcNbMax * kTcKMax];
     __shared__ unsigned tmem_base;
-    __shared__ float bS[kTcM][33];
+    __shared__ int fail;
     unsigned char* Ahi = smem;
-    unsigned char* Alo = smem + kTcOperand;
-    unsigned char* Bhi = smem + 2 * kTcOperand;
-    unsigned char* Blo = smem + 3 * kTcOperand;
-    const int tid = threadIdx.x, warp = tid >> 5;
+    unsigned char* Alo = smem + kTcA;
+    unsigned char* ring = smem + 2 * kTcA;  // slot s: hi at 2 s kTcB, lo at (2 s + 1) kTcB
+    float* stage_all = reinterpret_cast<float*>(smem + 2 * kTcA + 2 * kTcBSlots * kTcB);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -231,110 +309,218 @@ radial_tc_kernel(int64_t E, int nb, float rc, int hidden, int64_t n_out,
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
     if (tid == 0) {
-        tc_mbar_init(&mma_done);
+        for (int i = 0; i < 2; ++i) {
+            tc_mbar_init(&mma_done[i], 1);
+            tc_mbar_init(&acc_free[i], 32 * kTcEpiWarps);
+        }
+        for (int i = 0; i < kTcBSlots; ++i) tc_mbar_init(&b_full[i], 1);
+        tc_mbar_init(&a_full, 32 * kTcProdWarps);
+        tc_mbar_init(&a_free, 1);
+        fail = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    for (int i = tid; i < nb * hidden; i += kTcThreads) W1s[i] = W1[i];
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const unsigned tmem = tmem_base;
-    const float pref = sqrtf(2.0f / rc);
-    const unsigned lbo = (kTcM / 8) * 128;  // next 4-wide K slice (A and B both have 128 rows)
-    unsigned phase = 0;
-    bool ok = true;
+    const int64_t nchunk = n_out / kTcN;
+    const int64_t tiles = (E + kTcM - 1) / kTcM;
+    const int64_t my_tiles =
+        tiles > (int64_t)blockIdx.x ? (tiles - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+    const int64_t nk = my_tiles * nchunk;  // chunks this CTA multiplies
+    const unsigned part = (unsigned)(kTcN * hidden * 4);
 
-    for (int64_t e0 = (int64_t)blockIdx.x * kTcM; e0 < E && ok; e0 += (int64_t)gridDim.x * kTcM) {
-        // hidden activations of the tile: thread tid owns edge row tid
-        const int64_t e = e0 + tid;
-        const bool live = e < E;
-        {
+    if (warp >= kTcEpiWarps && warp < kTcEpiWarps + kTcProdWarps) {
+        // ---------------------------------------------------------- producers
+        const int p = tid - 32 * kTcEpiWarps;
+        const float pref = sqrtf(2.0f / rc);
+        float hv[kTcKMax];
+        auto hidden_row = [&](int64_t t) {  // activations of row p of this CTA's tile t
+            const int64_t e = ((int64_t)blockIdx.x + t * gridDim.x) * kTcM + p;
+            const bool live = e < E;
+            float b[kTcNbMax];
             float r = 0.0f;
             if (live) {
                 const float* v = vec + 3 * e;
                 r = sqrtf(v[0] * v[0] + v[1] * v[1] + v[2] * v[2]);
             }
-            for (int n = 0; n < nb; ++n) bS[tid][n] = live ? bessel_f<float>(n + 1, r, rc, pref) : 0.0f;
-        }
-        for (int k4 = 0; k4 < hidden; k4 += 4) {
-            float hv[4], hi[4], lo[4];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                float a = 0.0f;
-                for (int n = 0; n < nb; ++n) a = fmaf(bS[tid][n], __ldg(W1 + n * hidden + k4 + q), a);
-                hv[q] = live ? silu_f<float>(a) : 0.0f;
-                hi[q] = to_tf32(hv[q]);
-                lo[q] = to_tf32(hv[q] - hi[q]);
+            for (int n = 0; n < kTcNbMax; ++n)
+                b[n] = (live && n < nb) ? bessel_f<float>(n + 1, r, rc, pref) : 0.0f;
+#pragma unroll
+            for (int k4 = 0; k4 < kTcKMax; k4 += 4) {
+                if (k4 >= hidden) break;
+                float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
+#pragma unroll
+                for (int n = 0; n < kTcNbMax; ++n)
+                    if (n < nb) {
+                        const float4 wv = *reinterpret_cast<const float4*>(W1s + n * hidden + k4);
+                        a0 = fmaf(b[n], wv.x, a0);
+                        a1 = fmaf(b[n], wv.y, a1);
+                        a2 = fmaf(b[n], wv.z, a2);
+                        a3 = fmaf(b[n], wv.w, a3);
+                    }
+                hv[k4] = live ? silu_f<float>(a0) : 0.0f;
+                hv[k4 + 1] = live ? silu_f<float>(a1) : 0.0f;
+                hv[k4 + 2] = live ? silu_f<float>(a2) : 0.0f;
+                hv[k4 + 3] = live ? silu_f<float>(a3) : 0.0f;
+                if (h && live)
+                    *reinterpret_cast<float4*>(h + e * hidden + k4) =
+                        make_float4(hv[k4], hv[k4 + 1], hv[k4 + 2], hv[k4 + 3]);
             }
-            if (h && live)
-                *reinterpret_cast<float4*>(h + e * hidden + k4) = make_float4(hv[0], hv[1], hv[2], hv[3]);
-            const unsigned off = kmajor_offset(tid, k4, kTcM);
-            *reinterpret_cast<float4*>(Ahi + off) = make_float4(hi[0], hi[1], hi[2], hi[3]);
-            *reinterpret_cast<float4*>(Alo + off) = make_float4(lo[0], lo[1], lo[2], lo[3]);
-        }
-        for (int64_t c0 = 0; c0 < n_out; c0 += kTcN) {
-            // B = W2[:, c0 : c0 + 128] as 128 K-major rows (row = output column)
-            for (int i = tid; i < kTcN * (hidden / 4); i += kTcThreads) {
-                const int n = i % kTcN, k4 = (i / kTcN) * 4;
+        };
+        if (my_tiles > 0) hidden_row(0);
+        for (int64_t t = 0; t < my_tiles; ++t) {
+            // A is free once the previous tile's last MMA has completed
+            if (t > 0 && !tc_mbar_wait(&a_free, (unsigned)((t - 1) & 1))) {
+                atomicExch(&fail, 1);
+                break;
+            }
+#pragma unroll
+            for (int k4 = 0; k4 < kTcKMax; k4 += 4) {
+                if (k4 >= hidden) break;
                 float hi[4], lo[4];
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
-                    const float x = __ldg(W2 + (int64_t)(k4 + q) * n_out + c0 + n);
-                    hi[q] = to_tf32(x);
-                    lo[q] = to_tf32(x - hi[q]);
+                    hi[q] = to_tf32(hv[k4 + q]);
+                    lo[q] = to_tf32(hv[k4 + q] - hi[q]);
                 }
-                const unsigned off = kmajor_offset(n, k4, kTcN);
-                *reinterpret_cast<float4*>(Bhi + off) = make_float4(hi[0], hi[1], hi[2], hi[3]);
-                *reinterpret_cast<float4*>(Blo + off) = make_float4(lo[0], lo[1], lo[2], lo[3]);
+                const unsigned off = kmajor_offset(p, k4, kTcM);
+                *reinterpret_cast<float4*>(Ahi + off) = make_float4(hi[0], hi[1], hi[2], hi[3]);
+                *reinterpret_cast<float4*>(Alo + off) = make_float4(lo[0], lo[1], lo[2], lo[3]);
             }
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            __syncthreads();
-            if (tid == 0) {
-                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                for (int k8 = 0; k8 < hidden; k8 += 8) {
-                    const unsigned koff = (unsigned)(k8 >> 2) * lbo;
-                    const uint64_t ah = smem_desc(smem_addr(Ahi) + koff, lbo, 128);
-                    const uint64_t al = smem_desc(smem_addr(Alo) + koff, lbo, 128);
-                    const uint64_t bh = smem_desc(smem_addr(Bhi) + koff, lbo, 128);
-                    const uint64_t bl = smem_desc(smem_addr(Blo) + koff, lbo, 128);
-                    mma_tf32(tmem, ah, bh, k8 > 0 ? 1u : 0u);
-                    mma_tf32(tmem, ah, bl, 1u);
-                    mma_tf32(tmem, al, bh, 1u);
-                }
-                asm volatile(
-                    "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                        smem_addr(&mma_done))
-                    : "memory");
-            }
-            // every thread waits; all agree on the outcome before any
-            // warp-collective tcgen05.ld
-            const bool got = tc_mbar_wait(&mma_done, phase);
-            if (!__syncthreads_and(got)) {
-                if (tid == 0) atomicExch(&cgtp_radial_error, 1);
-                ok = false;
-                break;
-            }
-            phase ^= 1u;
-            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-            // accumulator rows 32 warp .. +31 -> this thread's edge row
-#pragma unroll 1
-            for (int cc = 0; cc < kTcN; cc += 32) {
-                float v[32];
-                tmem_ld32(tmem + ((unsigned)(warp * 32) << 16) + (unsigned)cc, v);
-                if (live) {
-                    float4* dst = reinterpret_cast<float4*>(w + e * n_out + c0 + cc);
-#pragma unroll
-                    for (int q = 0; q < 8; ++q)
-                        dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-                }
-            }
-            asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-            __syncthreads();
+            tc_mbar_arrive(&a_full);
+            if (t + 1 < my_tiles) hidden_row(t + 1);
+            if (*(volatile int*)&fail) break;
         }
+    } else if (warp == kTcEpiWarps + kTcProdWarps) {
+        // ------------------------------------------------------------- issuer
+        if (lane == 0 && nk > 0) {
+            const unsigned la = (kTcM / 8) * 128, lb = (kTcN / 8) * 128;  // K-slice strides
+            auto issue_b = [&](int64_t k) {
+                const int s = (int)(k % kTcBSlots);
+                const int64_t col = (k % nchunk + blockIdx.x) % nchunk;
+                const unsigned char* src = img + (size_t)col * 2 * part;
+                unsigned char* dst = ring + (size_t)s * 2 * kTcB;
+                tc_expect_tx(&b_full[s], 2 * part);
+                tc_bulk_g2s(dst, src, part, &b_full[s]);
+                tc_bulk_g2s(dst + kTcB, src + part, part, &b_full[s]);
+            };
+            for (int64_t k = 0; k < nk && k < kTcBSlots - 1; ++k) issue_b(k);
+            int64_t k = 0;
+            bool ok = true;
+            for (int64_t t = 0; t < my_tiles && ok; ++t) {
+                if (!tc_mbar_wait(&a_full, (unsigned)(t & 1))) {
+                    ok = false;
+                    break;
+                }
+                for (int64_t c = 0; c < nchunk; ++c, ++k) {
+                    const int s = (int)(k & 1), rs = (int)(k % kTcBSlots);
+                    // B landed and the accumulator is free (the epilogue has
+                    // read chunk k - 2)
+                    if (!tc_mbar_wait(&b_full[rs], (unsigned)((k / kTcBSlots) & 1)) ||
+                        (k >= 2 && !tc_mbar_wait(&acc_free[s], (unsigned)(((k - 2) >> 1) & 1)))) {
+                        ok = false;
+                        break;
+                    }
+                    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                    const unsigned d = tmem + (unsigned)(s * kTcN);
+                    const unsigned bhi = smem_addr(ring + (size_t)rs * 2 * kTcB);
+                    for (int k8 = 0; k8 < hidden; k8 += 8) {
+                        const unsigned ka = (unsigned)(k8 >> 2) * la, kb = (unsigned)(k8 >> 2) * lb;
+                        const uint64_t ah = smem_desc(smem_addr(Ahi) + ka, la, 128);
+                        const uint64_t al = smem_desc(smem_addr(Alo) + ka, la, 128);
+                        const uint64_t bh = smem_desc(bhi + kb, lb, 128);
+                        const uint64_t bl = smem_desc(bhi + kTcB + kb, lb, 128);
+                        mma_tf32(d, ah, bh, k8 > 0 ? 1u : 0u);
+                        mma_tf32(d, ah, bl, 1u);
+                        mma_tf32(d, al, bh, 1u);
+                    }
+                    tc_commit(&mma_done[s]);
+                    if (c == nchunk - 1) tc_commit(&a_free);
+                    // refill the ring slot of chunk k - 1 with chunk k + 1 once
+                    // chunk k - 1 has been multiplied
+                    if (k + kTcBSlots - 1 < nk) {
+                        if (k >= 1 &&
+                            !tc_mbar_wait(&mma_done[(k - 1) & 1], (unsigned)(((k - 1) >> 1) & 1))) {
+                            ok = false;
+                            break;
+                        }
+                        issue_b(k + kTcBSlots - 1);
+                    }
+                    if (*(volatile int*)&fail) {
+                        ok = false;
+                        break;
+                    }
+                }
+            }
+            if (!ok) atomicExch(&fail, 1);
+        }
+    } else {
+        // ----------------------------------------------------------- epilogue
+        float* stage = stage_all + warp * (16 * kTcStagePitch);
+        const int quarter = warp & 3, half = warp >> 2;
+        int64_t k = 0;
+        bool ok = true;
+        for (int64_t t = 0; t < my_tiles && ok; ++t) {
+            const int64_t e0 = ((int64_t)blockIdx.x + t * gridDim.x) * kTcM + quarter * 32;
+            for (int64_t c = 0; c < nchunk; ++c, ++k) {
+                const int s = (int)(k & 1);
+                const int64_t col0 = ((c + blockIdx.x) % nchunk) * kTcN + half * 64;
+                // warp-uniform outcome before the warp-collective tcgen05.ld
+                bool got = tc_mbar_wait(&mma_done[s], (unsigned)((k >> 1) & 1));
+                got = __all_sync(0xffffffffu, got && !*(volatile int*)&fail);
+                if (!got) {
+                    ok = false;
+                    break;
+                }
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                const unsigned ta = tmem + ((unsigned)(quarter * 32) << 16) + (unsigned)(s * kTcN + half * 64);
+                float v0[32], v1[32];
+                tmem_ld32(ta, v0);
+                tmem_ld32(ta + 32, v1);
+                asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+                tc_mbar_arrive(&acc_free[s]);
+#pragma unroll
+                for (int blk = 0; blk < 2; ++blk) {
+                    const float* v = blk ? v1 : v0;
+#pragma unroll
+                    for (int hp = 0; hp < 2; ++hp) {
+                        // rows 16 hp .. 16 hp + 15 of the 32 x 32 block into shared
+                        // memory, then out as four 128-byte row segments per instruction
+                        if ((lane >> 4) == hp) {
+#pragma unroll
+                            for (int q = 0; q < 8; ++q)
+                                *reinterpret_cast<float4*>(stage + (lane & 15) * kTcStagePitch + 4 * q) =
+                                    make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                        }
+                        __syncwarp();
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const int r = 4 * i + (lane >> 3);
+                            const int64_t e = e0 + 16 * hp + r;
+                            const float4 val = *reinterpret_cast<const float4*>(
+                                stage + r * kTcStagePitch + (lane & 7) * 4);
+                            if (e < E)
+                                *reinterpret_cast<float4*>(w + e * n_out + col0 + blk * 32 +
+                                                           (lane & 7) * 4) = val;
+                        }
+                        __syncwarp();
+                    }
+                }
+            }
+        }
+        if (!ok) atomicExch(&fail, 1);
     }
-    // after a timed-out wait give the MMAs in flight a second bounded wait,
-    // then release the accumulator (every thread agrees on the exit first)
-    if (!ok) tc_mbar_wait(&mma_done, phase);
     __syncthreads();
+    if (fail) {
+        if (tid == 0) atomicExch(&cgtp_radial_error, 1);
+        // let copies and MMAs that may still be in flight finish before the
+        // CTA's shared and tensor memory are released
+        for (int i = 0; i < 1000; ++i) __nanosleep(1000);
+    }
     if (warp == 0)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                      "r"(kTcTmemCols)
@@ -346,13 +532,19 @@ radial_tc_kernel(int64_t E, int nb, float rc, int hidden, int64_t n_out,
 bool radial_tc_eligible(bool f64, int nb, int hidden, int64_t n_out, const void* vec,
                         const void* W2, const void* w, const void* h) {
     auto a16 = [](const void* p) { return p == nullptr || ((uintptr_t)p % 16) == 0; };
-    return !f64 && nb <= 32 && hidden % 8 == 0 && hidden <= kTcKMax && n_out % kTcN == 0 &&
+    return !f64 && nb <= kTcNbMax && hidden % 8 == 0 && hidden <= kTcKMax && n_out % kTcN == 0 &&
            a16(w) && a16(h) && a16(W2) && a16(vec);
+}
+
+size_t radial_workspace_bytes(bool f64, int nb, int hidden, int64_t n_out) {
+    if (!radial_tc_eligible(f64, nb, hidden, n_out, nullptr, nullptr, nullptr, nullptr)) return 0;
+    return (size_t)n_out * hidden * 8;  // TF32 hi and lo parts of W2, packed
 }
 
 cudaError_t launch_radial_forward(bool f64, bool tensor_cores, int64_t E, int nb, double rc,
                                   int hidden, int64_t n_out, const void* vec, const void* W1,
-                                  const void* W2, void* w, void* h, cudaStream_t s) {
+                                  const void* W2, void* w, void* h, void* ws, size_t ws_bytes,
+                                  cudaStream_t s) {
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -361,11 +553,18 @@ cudaError_t launch_radial_forward(bool f64, bool tensor_cores, int64_t E, int nb
         e = cudaFuncSetAttribute(radial_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)kTcSmem);
         if (e != cudaSuccess) return e;
+        const int64_t total = (int64_t)hidden * n_out;
+        const unsigned pg =
+            (unsigned)std::max<int64_t>(1, std::min<int64_t>((total + 255) / 256, (int64_t)sms * 8));
+        radial_pack_kernel<<<pg, 256, 0, s>>>(hidden, n_out, (const float*)W2, (unsigned char*)ws);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
         const int64_t tiles = (E + kTcM - 1) / kTcM;
         const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(tiles, sms));
-        radial_tc_kernel<<<grid, kTcThreads, kTcSmem, s>>>(
-            E, nb, (float)rc, hidden, n_out, (const float*)vec, (const float*)W1,
-            (const float*)W2, (float*)w, (float*)h);
+        radial_tc_kernel<<<grid, kTcThreads, kTcSmem, s>>>(E, nb, (float)rc, hidden, n_out,
+                                                           (const float*)vec, (const float*)W1,
+                                                           (const unsigned char*)ws, (float*)w,
+                                                           (float*)h);
         return cudaGetLastError();
     }
     const size_t es = f64 ? 8 : 4;

@@ -277,18 +277,25 @@ cgtp_status cgtp_edge_forces_adjoint(cgtp_dtype dtype, int64_t N, int64_t E,
  * optional h [E, hidden] (NULL: not stored) are row-major device arrays of
  * `dtype`, owned by the caller; w and h are overwritten.  Limits:
  * 1 <= n_basis <= 32, 1 <= hidden <= 256, n_out >= 1, cutoff > 0; else
- * CGTP_E_ARG.  fp32 with hidden % 8 == 0, hidden <= 64, n_out % 128 == 0 and
- * 16-byte aligned vec / W2 / w / h runs the last layer on the tensor cores
- * (TF32 in three split products, fp32 accuracy); other shapes, fp64, or
- * flags & CGTP_RADIAL_CUDA_CORES run it on the CUDA cores.  Asynchronous on
- * `stream`; allocates nothing. */
+ * CGTP_E_ARG.  The last layer runs on the tensor cores (TF32 in three split
+ * products, fp32 accuracy) for fp32 with n_basis <= 16, hidden % 8 == 0,
+ * hidden <= 64, n_out % 128 == 0, 16-byte aligned vec / W2 / w / h and a
+ * workspace of at least cgtp_radial_workspace() bytes (device, caller-owned,
+ * 16-byte aligned, contents need not be set; the call packs W2's TF32 parts
+ * into it, so calls sharing a workspace must not overlap in time).  Other
+ * shapes, fp64, no workspace, or flags & CGTP_RADIAL_CUDA_CORES run it on the
+ * CUDA cores.  Asynchronous on `stream`; allocates nothing. */
 #define CGTP_RADIAL_CUDA_CORES 1u
 cgtp_status cgtp_radial_forward(cgtp_dtype dtype, int64_t E, int n_basis, double cutoff,
                                 int hidden, int64_t n_out, const void* vec, const void* W1,
-                                const void* W2, void* w, void* h, unsigned flags,
-                                cgtp_stream stream);
+                                const void* W2, void* w, void* h, void* workspace,
+                                size_t workspace_bytes, unsigned flags, cgtp_stream stream);
+/* Workspace bytes cgtp_radial_forward uses for these sizes (0: it uses none). */
+cgtp_status cgtp_radial_workspace(cgtp_dtype dtype, int n_basis, int hidden, int64_t n_out,
+                                  size_t* bytes);
 /* Host query: *tensor_cores = 1 if cgtp_radial_forward with these sizes (and
- * 16-byte aligned pointers, flags 0) takes the tensor-core path, else 0. */
+ * 16-byte aligned pointers, a large enough workspace, flags 0) takes the
+ * tensor-core path, else 0. */
 cgtp_status cgtp_radial_path(cgtp_dtype dtype, int n_basis, int hidden, int64_t n_out,
                              int* tensor_cores);
 /* Reads and clears the radial kernels' device error flag (synchronous): 0, or

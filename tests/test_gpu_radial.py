@@ -30,6 +30,8 @@ CASES = [  # E, n_basis, hidden, n_out, dtype
     (5000, 8, 64, 384, np.float32),
     (333, 5, 40, 256, np.float32),
     (300, 8, 12, 100, np.float32),
+    (200, 8, 64, 192, np.float32),
+    (257, 16, 8, 64, np.float32),
     (300, 32, 256, 96, np.float32),
     (777, 8, 64, 1536, np.float64),
     (50, 3, 7, 5, np.float64),
@@ -53,7 +55,7 @@ def test_radial_forward_matches_oracle(case, cuda_cores):
     assert_close(host(hid), rh, dt, "hidden")
     assert cg.radial_device_status() == 0
     if not cuda_cores and dt == np.float32:
-        expect_tc = hidden % 8 == 0 and hidden <= 64 and n_out % 128 == 0
+        expect_tc = nb <= 16 and hidden % 8 == 0 and hidden <= 64 and n_out % 128 == 0
         assert cg.radial_uses_tensor_cores(tdt, nb, hidden, n_out) == expect_tc
 
 

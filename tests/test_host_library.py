@@ -126,7 +126,8 @@ def test_radial_argument_errors_and_path():
     L = cg.lib()
     null = ctypes.c_void_p()
     # sizes and pointers are checked before any CUDA call
-    args = lambda E, nb, rc, hid, no, p=null: (0, E, nb, rc, hid, no, p, p, p, p, null, 0, null)
+    args = lambda E, nb, rc, hid, no, p=null: (0, E, nb, rc, hid, no, p, p, p, p, null, null,
+                                                0, 0, null)
     assert L.cgtp_radial_forward(*args(0, 8, 5.0, 64, 1536)) == 0
     assert L.cgtp_radial_forward(*args(-1, 8, 5.0, 64, 1536)) == 1
     assert L.cgtp_radial_forward(*args(4, 0, 5.0, 64, 1536)) == 1
@@ -141,7 +142,13 @@ def test_radial_argument_errors_and_path():
     assert not cg.radial_uses_tensor_cores(torch.float32, 8, 12, 1536)   # hidden % 8
     assert not cg.radial_uses_tensor_cores(torch.float32, 8, 128, 1536)  # hidden > 64
     assert not cg.radial_uses_tensor_cores(torch.float32, 8, 64, 100)    # n_out % 128
+    assert not cg.radial_uses_tensor_cores(torch.float32, 8, 64, 192)
     assert not cg.radial_uses_tensor_cores(torch.float64, 8, 64, 1536)
+    assert not cg.radial_uses_tensor_cores(torch.float32, 17, 64, 1536)  # n_basis > 16
+    n = ctypes.c_size_t()
+    assert L.cgtp_radial_workspace(0, 8, 64, 1536, ctypes.byref(n)) == 0 and n.value == 1536 * 64 * 8
+    assert L.cgtp_radial_workspace(1, 8, 64, 1536, ctypes.byref(n)) == 0 and n.value == 0
+    assert L.cgtp_radial_workspace(0, 8, 12, 1536, ctypes.byref(n)) == 0 and n.value == 0
     v = ctypes.c_int()
     assert L.cgtp_radial_path(0, 8, 64, 1536, None) == 1
     assert L.cgtp_radial_path(0, 40, 64, 1536, ctypes.byref(v)) == 1
