@@ -39,6 +39,7 @@ sys.path.insert(0, ROOT)
 METRIC = "CG-TP conv edges/sec (fwd, fwd+bwd) at 1 GB300 and % of HBM/FP-pipe roofline"
 SM_COUNT = 152
 FP32_LANES_PER_SM = 128  # FP32 FMA lanes per SM per clock
+FP64_NOMINAL_TFLOPS = 1.25
 
 
 def _peaks():
@@ -429,7 +430,12 @@ def run_gpu(args):
         return None
 
     peaks = _peaks()
-    fp32_peak = SM_COUNT * FP32_LANES_PER_SM * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12  # TFLOP/s
+    if wl.dtype == "f64":
+        # the FP64 pipe: GB300's nominal 1.25 TFLOP/s (no measured figure exists)
+        fp32_peak, alu_src = FP64_NOMINAL_TFLOPS, "FP64 pipe: nominal 1.25 TFLOP/s"
+    else:
+        fp32_peak = SM_COUNT * FP32_LANES_PER_SM * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12  # TFLOP/s
+        alu_src = f"FP32 ALU: 152 SM x 128 FMA x 2 x {peaks['sm_max_mhz']:.0f} MHz"
     kernels = {}
     for n in names:
         nbytes, flops = wl.counts[n]
@@ -469,8 +475,7 @@ def run_gpu(args):
         roof = {"bound": "hbm", "achieved": kd["hbm_gbs"], "peak": peaks["hbm"], "unit": "GB/s",
                 "frac": kd["hbm_gbs"] / peaks["hbm"]}
     roof.update(kernel=dom, traffic=_traffic(args.workload, dom),
-                peak_source=f"{peaks['src']} (HBM: copy bandwidth; FP32 ALU: 152 SM x 128 FMA "
-                            f"x 2 x {peaks['sm_max_mhz']:.0f} MHz)")
+                peak_source=f"{peaks['src']} (HBM: copy bandwidth; {alu_src})")
     config = {"workload": wl.desc, **wl.cfg,
               "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
               "l2": "inputs larger than L2 (weight stream per step >> 129 MB)"}
