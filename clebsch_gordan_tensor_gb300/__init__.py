@@ -29,6 +29,7 @@ _lib = None
 
 F32, F64 = 0, 1
 W_PER_EDGE, W_SHARED = 0, 1
+WEIGHTS_BF16 = 1 << 24  # plan flag: weights stored as bfloat16
 
 
 class CgtpError(RuntimeError):
@@ -171,9 +172,16 @@ class Plan:
     its kernels compiled for sm_103a on first use."""
 
     def __init__(self, irreps_in1: str, irreps_in2: str, irreps_out: str,
-                 dtype=torch.float32, shared_weights: bool = False, instructions=None):
+                 dtype=torch.float32, shared_weights: bool = False, instructions=None,
+                 weight_dtype=None):
+        """weight_dtype=torch.bfloat16 stores the weights as bfloat16 (fp32 plans;
+        arithmetic, features and grad_w stay fp32)."""
         L = lib()
         self.dtype = dtype
+        self.wdtype = dtype if weight_dtype is None else weight_dtype
+        if self.wdtype not in (dtype, torch.bfloat16):
+            raise CgtpError(f"weight_dtype {weight_dtype} is not supported")
+        flags = WEIGHTS_BF16 if self.wdtype == torch.bfloat16 else 0
         self.irreps = (irreps_in1, irreps_in2, irreps_out)
         h = ctypes.c_void_p()
         arr, n = None, 0
@@ -184,7 +192,7 @@ class Plan:
                 arr[k] = _Instr(a, b, c, b"uvu")
         _check(L.cgtp_plan_create(ctypes.byref(h), irreps_in1.encode(), irreps_in2.encode(),
                                   irreps_out.encode(), arr, n, _dt(dtype),
-                                  W_SHARED if shared_weights else W_PER_EDGE, 0))
+                                  W_SHARED if shared_weights else W_PER_EDGE, flags))
         self._h = h
         d1, d2, do, wn = (ctypes.c_int64() for _ in range(4))
         npth = ctypes.c_int()
@@ -249,7 +257,7 @@ class Plan:
         B = x.shape[0]
         _need(x, "x", self.dtype, (B, self.dim_in1))
         _need(y, "y", self.dtype, (B, self.dim_in2))
-        _need(w, "w", self.dtype, self._wshape(B))
+        _need(w, "w", self.wdtype, self._wshape(B))
         if out is None:
             out = torch.empty(B, self.dim_out, dtype=self.dtype, device=x.device)
         _need(out, "out", self.dtype, (B, self.dim_out))
@@ -260,11 +268,11 @@ class Plan:
         B = x.shape[0]
         _need(x, "x", self.dtype, (B, self.dim_in1))
         _need(y, "y", self.dtype, (B, self.dim_in2))
-        _need(w, "w", self.dtype, self._wshape(B))
+        _need(w, "w", self.wdtype, self._wshape(B))
         _need(grad_out, "grad_out", self.dtype, (B, self.dim_out))
         gx = torch.empty_like(x) if need[0] else None
         gy = torch.empty_like(y) if need[1] else None
-        gw = torch.empty_like(w) if need[2] else None
+        gw = torch.empty(w.shape, dtype=self.dtype, device=w.device) if need[2] else None
         ws, nws = self._workspace(x.device, gw)
         _check(lib().cgtp_backward_ws(self._h, B, _ptr(x), _ptr(y), _ptr(w), _ptr(grad_out),
                                       _ptr(gx), _ptr(gy), _ptr(gw), _ptr(ws), nws, _stream()))
@@ -277,7 +285,7 @@ class Plan:
                         ("w", w, self._wshape(B)), ("grad_out", grad_out, (B, self.dim_out)),
                         ("gg_x", gg_x, (B, self.dim_in1)), ("gg_y", gg_y, (B, self.dim_in2)),
                         ("gg_w", gg_w, self._wshape(B))):
-            _need(t, n, self.dtype, s)
+            _need(t, n, self.wdtype if n in ("w", "gg_w") else self.dtype, s)
         dx = torch.empty_like(x) if need[0] else None
         dy = torch.empty_like(y) if need[1] else None
         dw = torch.empty_like(w) if need[2] else None
@@ -291,7 +299,7 @@ class Plan:
     def _conv_check(self, g: Graph, x, y, w):
         _need(x, "x", self.dtype, (g.N, self.dim_in1))
         _need(y, "y", self.dtype, (g.E, self.dim_in2))
-        _need(w, "w", self.dtype, self._wshape(g.E))
+        _need(w, "w", self.wdtype, self._wshape(g.E))
 
     def conv_forward(self, g: Graph, x, y, w, scale: float = 1.0, out=None):
         self._conv_check(g, x, y, w)
@@ -312,7 +320,7 @@ class Plan:
         else:
             gx = torch.empty_like(x) if need[0] else None
             gy = torch.empty_like(y) if need[1] else None
-            gw = torch.empty_like(w) if need[2] else None
+            gw = torch.empty(w.shape, dtype=self.dtype, device=w.device) if need[2] else None
         ws, nws = self._workspace(x.device, gw)
         _check(lib().cgtp_conv_backward_ws(self._h, g.N, g.E, _ptr(g.rowptr), _ptr(g.sender),
                                            _ptr(g.s_rowptr), _ptr(g.s_perm), _ptr(g.s_recv),
@@ -327,7 +335,7 @@ class Plan:
         _need(grad_out, "grad_out", self.dtype, (g.N, self.dim_out))
         _need(gg_x, "gg_x", self.dtype, (g.N, self.dim_in1))
         _need(gg_y, "gg_y", self.dtype, (g.E, self.dim_in2))
-        _need(gg_w, "gg_w", self.dtype, self._wshape(g.E))
+        _need(gg_w, "gg_w", self.wdtype, self._wshape(g.E))
         dx = torch.empty_like(x) if need[0] else None
         dy = torch.empty_like(y) if need[1] else None
         dw = torch.empty_like(w) if need[2] else None
@@ -374,7 +382,7 @@ def sh_jvp(vec, tangent_vec, lmax: int, out=None):
 
 
 def radial_forward(vec, W1, W2, cutoff: float = 5.0, out=None, hidden_out=None,
-                   cuda_cores: bool = False):
+                   cuda_cores: bool = False, out_dtype=None):
     """Per-edge weights of the radial network: w[e] = silu(b(|vec[e]|) W1) W2
     with the Bessel basis b_n(r) = sqrt(2/rc) sin(n pi r / rc) / r.  Returns w
     [E, n_out]; ``hidden_out`` [E, hidden], if given, receives silu(b W1)."""
@@ -384,16 +392,19 @@ def radial_forward(vec, W1, W2, cutoff: float = 5.0, out=None, hidden_out=None,
     _need(W1, "W1", vec.dtype, (nb, hidden))
     n_out = W2.shape[1]
     _need(W2, "W2", vec.dtype, (hidden, n_out))
+    odt = vec.dtype if out_dtype is None else out_dtype
     if out is None:
-        out = torch.empty(E, n_out, dtype=vec.dtype, device=vec.device)
-    _need(out, "out", vec.dtype, (E, n_out))
+        out = torch.empty(E, n_out, dtype=odt, device=vec.device)
+    _need(out, "out", odt, (E, n_out))
     _need(hidden_out, "hidden_out", vec.dtype, (E, hidden))
     n = ctypes.c_size_t(0)
     _check(lib().cgtp_radial_workspace(_dt(vec.dtype), nb, hidden, n_out, ctypes.byref(n)))
     ws = torch.empty(n.value, dtype=torch.uint8, device=vec.device) if n.value else None
     _check(lib().cgtp_radial_forward(_dt(vec.dtype), E, nb, float(cutoff), hidden, n_out,
                                      _ptr(vec), _ptr(W1), _ptr(W2), _ptr(out), _ptr(hidden_out),
-                                     _ptr(ws), n.value, 1 if cuda_cores else 0, _stream()))
+                                     _ptr(ws), n.value,
+                                     (1 if cuda_cores else 0) | (2 if odt == torch.bfloat16 else 0),
+                                     _stream()))
     return out
 
 

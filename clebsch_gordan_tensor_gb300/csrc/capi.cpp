@@ -48,6 +48,17 @@ static size_t row_align(const Plan& p) {
     return p.dtype == CGTP_F64 ? 8 : (p.cpt == 2 ? 8 : 4);
 }
 
+// Weight rows: bfloat16 pairs are read as one 32-bit word per lane.
+static size_t w_align(const Plan& p) {
+    return p.w_bf16 ? (p.cpt == 2 ? 4 : 2) : row_align(p);
+}
+
+static cgtp_status check_w(const Plan& p, const void* w) {
+    if (!aligned(w, w_align(p)))
+        return fail(CGTP_E_ARG, "weight pointer not aligned to " + std::to_string(w_align(p)) + " bytes");
+    return CGTP_OK;
+}
+
 static cgtp_status check_rows(const Plan& p, std::initializer_list<const void*> ptrs) {
     const size_t a = row_align(p);
     for (const void* q : ptrs)
@@ -270,10 +281,14 @@ cgtp_status cgtp_plan_create(cgtp_plan* out, const char* irreps_in1, const char*
     *out = nullptr;
     if (dtype != CGTP_F32 && dtype != CGTP_F64) return fail(CGTP_E_ARG, "bad dtype");
     if (wmode != CGTP_W_PER_EDGE && wmode != CGTP_W_SHARED) return fail(CGTP_E_ARG, "bad wmode");
+    const bool w_bf16 = (flags & CGTP_PLAN_WEIGHTS_BF16) != 0;
+    if (w_bf16 && dtype != CGTP_F32)
+        return fail(CGTP_E_UNSUPPORTED, "bfloat16 weights need an fp32 plan");
     auto* h = new cgtp_plan_s();
     h->p.dtype = dtype;
     h->p.wmode = wmode;
     h->p.flags = flags;
+    h->p.w_bf16 = w_bf16;
     std::string err;
     cgtp_status st = build_plan(h->p, irreps_in1, irreps_in2, irreps_out, instr, n_instr, err);
     if (st != CGTP_OK) {
@@ -405,8 +420,9 @@ cgtp_status cgtp_forward(cgtp_plan plan, int64_t B, const void* x, const void* y
     if (B == 0) return CGTP_OK;
     if (!x || !y || !w || !out) return fail(CGTP_E_ARG, "NULL tensor");
     Plan& p = plan->p;
-    cgtp_status st = check_rows(p, {x, w, out});
+    cgtp_status st = check_rows(p, {x, out});
     if (st != CGTP_OK) return st;
+    if ((st = check_w(p, w)) != CGTP_OK) return st;
     return fwd_launch(p, false, B, nullptr, nullptr, x, y, w, 1.0, out, 0, S(stream));
     GUARD_END
 }
@@ -422,8 +438,9 @@ cgtp_status cgtp_backward(cgtp_plan plan, int64_t B, const void* x, const void* 
     Plan& p = plan->p;
     if (p.wmode == CGTP_W_SHARED && grad_w)
         return fail(CGTP_E_ARG, "shared-weight gradient needs a workspace: use cgtp_backward_ws");
-    cgtp_status st = check_rows(p, {x, w, grad_out, grad_x, grad_w});
+    cgtp_status st = check_rows(p, {x, grad_out, grad_x, grad_w});
     if (st != CGTP_OK) return st;
+    if ((st = check_w(p, w)) != CGTP_OK) return st;
     return bwd_launch(p, false, B, nullptr, nullptr, nullptr, x, y, w, grad_out, 1.0, grad_x,
                       grad_y, grad_w, grad_x ? 1 : 0, grad_y ? 1 : 0, grad_w ? 1 : 0, S(stream));
     GUARD_END
@@ -444,7 +461,8 @@ cgtp_status cgtp_backward_ws(cgtp_plan plan, int64_t B, const void* x, const voi
         return CGTP_OK;
     }
     if (!x || !y || !w || !grad_out) return fail(CGTP_E_ARG, "NULL input tensor");
-    if ((st = check_rows(p, {x, w, grad_out, grad_x, grad_w})) != CGTP_OK) return st;
+    if ((st = check_rows(p, {x, grad_out, grad_x, grad_w})) != CGTP_OK) return st;
+    if ((st = check_w(p, w)) != CGTP_OK) return st;
     return bwd_launch(p, false, B, nullptr, nullptr, nullptr, x, y, w, grad_out, 1.0, grad_x,
                       grad_y, grad_w, grad_x ? 1 : 0, grad_y ? 1 : 0, grad_w ? 1 : 0, S(stream),
                       workspace, kSharedWRows);
@@ -461,8 +479,10 @@ cgtp_status cgtp_double_backward(cgtp_plan plan, int64_t B, const void* x, const
     if (B == 0) return CGTP_OK;
     if (!x || !y || !w || !grad_out) return fail(CGTP_E_ARG, "NULL input tensor");
     Plan& p = plan->p;
-    cgtp_status st = check_rows(p, {x, w, grad_out, gg_x, gg_w, d_x, d_w, d_grad_out});
+    if (p.w_bf16) return fail(CGTP_E_UNSUPPORTED, "double backward of a bfloat16-weight plan");
+    cgtp_status st = check_rows(p, {x, grad_out, gg_x, gg_w, d_x, d_w, d_grad_out});
     if (st != CGTP_OK) return st;
+    if ((st = check_w(p, w)) != CGTP_OK) return st;
     return double_backward(p, false, B, B, B, nullptr, nullptr, nullptr, nullptr, nullptr, x, y,
                            w, 1.0, grad_out, gg_x, gg_y, gg_w, d_x, d_y, d_w, d_grad_out,
                            S(stream));
@@ -487,7 +507,8 @@ cgtp_status cgtp_conv_forward(cgtp_plan plan, int64_t N, int64_t E, const int32_
     if (N == 0) return CGTP_OK;
     if (!out || (E > 0 && (!x || !y || !w))) return fail(CGTP_E_ARG, "NULL tensor");
     Plan& p = plan->p;
-    if ((st = check_rows(p, {x, w, out})) != CGTP_OK) return st;
+    if ((st = check_rows(p, {x, out})) != CGTP_OK) return st;
+    if ((st = check_w(p, w)) != CGTP_OK) return st;
     return fwd_launch(p, true, N, rowptr, sender, x, y, w, scale, out, 0, S(stream));
     GUARD_END
 }
@@ -509,7 +530,8 @@ cgtp_status cgtp_conv_backward(cgtp_plan plan, int64_t N, int64_t E, const int32
     if (p.wmode == CGTP_W_SHARED && grad_w)
         return fail(CGTP_E_ARG, "shared-weight gradient needs a workspace: use cgtp_conv_backward_ws");
     if (!x || !grad_out || (E > 0 && (!y || !w))) return fail(CGTP_E_ARG, "NULL input tensor");
-    if ((st = check_rows(p, {x, w, grad_out, grad_x, grad_w})) != CGTP_OK) return st;
+    if ((st = check_rows(p, {x, grad_out, grad_x, grad_w})) != CGTP_OK) return st;
+    if ((st = check_w(p, w)) != CGTP_OK) return st;
     return bwd_launch(p, true, N, s_rowptr, s_perm, s_recv, x, y, w, grad_out, scale, grad_x,
                       grad_y, grad_w, grad_x ? 1 : 0, grad_y ? 1 : 0, grad_w ? 1 : 0, S(stream));
     GUARD_END
@@ -535,7 +557,8 @@ cgtp_status cgtp_conv_backward_ws(cgtp_plan plan, int64_t N, int64_t E, const in
         return CGTP_OK;
     }
     if (!x || !grad_out || (E > 0 && (!y || !w))) return fail(CGTP_E_ARG, "NULL input tensor");
-    if ((st = check_rows(p, {x, w, grad_out, grad_x, grad_w})) != CGTP_OK) return st;
+    if ((st = check_rows(p, {x, grad_out, grad_x, grad_w})) != CGTP_OK) return st;
+    if ((st = check_w(p, w)) != CGTP_OK) return st;
     return bwd_launch(p, true, N, s_rowptr, s_perm, s_recv, x, y, w, grad_out, scale, grad_x,
                       grad_y, grad_w, grad_x ? 1 : 0, grad_y ? 1 : 0, grad_w ? 1 : 0, S(stream),
                       workspace, kSharedWRows);
@@ -558,8 +581,10 @@ cgtp_status cgtp_conv_double_backward(cgtp_plan plan, int64_t N, int64_t E, cons
     if (N == 0) return CGTP_OK;
     if (!x || !grad_out || (E > 0 && (!y || !w))) return fail(CGTP_E_ARG, "NULL input tensor");
     Plan& p = plan->p;
-    if ((st = check_rows(p, {x, w, grad_out, gg_x, gg_w, d_x, d_w, d_grad_out})) != CGTP_OK)
+    if (p.w_bf16) return fail(CGTP_E_UNSUPPORTED, "double backward of a bfloat16-weight plan");
+    if ((st = check_rows(p, {x, grad_out, gg_x, gg_w, d_x, d_w, d_grad_out})) != CGTP_OK)
         return st;
+    if ((st = check_w(p, w)) != CGTP_OK) return st;
     return double_backward(p, true, N, E, N, rowptr, sender, s_rowptr, s_perm, s_recv, x, y, w,
                            scale, grad_out, gg_x, gg_y, gg_w, d_x, d_y, d_w, d_grad_out,
                            S(stream));
@@ -643,15 +668,20 @@ cgtp_status cgtp_radial_forward(cgtp_dtype dtype, int64_t E, int n_basis, double
     if (st != CGTP_OK || E == 0) return st;
     if (!vec || !W1 || !W2 || !w) return fail(CGTP_E_ARG, "NULL tensor");
     const size_t es = dtype == CGTP_F64 ? 8 : 4;
-    for (const void* q : {vec, W1, W2, (const void*)w, (const void*)h})
+    const bool out_bf16 = (flags & CGTP_RADIAL_OUT_BF16) != 0;
+    if (out_bf16 && dtype != CGTP_F32)
+        return fail(CGTP_E_UNSUPPORTED, "bfloat16 output needs fp32 inputs");
+    for (const void* q : {vec, W1, W2, (const void*)h})
         if (!aligned(q, es)) return fail(CGTP_E_ARG, "tensor pointer not aligned to its element");
+    if (!aligned(w, out_bf16 ? 2 : es)) return fail(CGTP_E_ARG, "w not aligned to its element");
     const bool f64 = dtype == CGTP_F64;
     const size_t need = radial_workspace_bytes(f64, n_basis, hidden, n_out);
     const bool tc = !(flags & CGTP_RADIAL_CUDA_CORES) && need > 0 && workspace &&
                     workspace_bytes >= need && aligned(workspace, 16) &&
                     radial_tc_eligible(f64, n_basis, hidden, n_out, vec, W2, w, h);
-    cudaError_t e = launch_radial_forward(f64, tc, E, n_basis, cutoff, hidden, n_out, vec, W1,
-                                          W2, w, h, workspace, workspace_bytes, S(stream));
+    cudaError_t e = launch_radial_forward(f64, tc, out_bf16, E, n_basis, cutoff, hidden, n_out,
+                                          vec, W1, W2, w, h, workspace, workspace_bytes,
+                                          S(stream));
     if (e != cudaSuccess) return cuda_fail(e, "radial_forward");
     count_launch();
     return CGTP_OK;
@@ -768,7 +798,8 @@ cgtp_status conv_backward_into_scratch(cgtp_plan plan, int64_t N, int64_t E,
                                     std::to_string(scratch_bytes) + " bytes");
     if (N == 0) return shared ? zero(grad_w, row, s) : CGTP_OK;
     if (!x || !grad_out || (E > 0 && (!y || !w))) return fail(CGTP_E_ARG, "NULL input tensor");
-    if ((st = check_rows(p, {x, w, grad_out, grad_x, grad_w})) != CGTP_OK) return st;
+    if ((st = check_rows(p, {x, grad_out, grad_x, grad_w})) != CGTP_OK) return st;
+    if ((st = check_w(p, w)) != CGTP_OK) return st;
     return bwd_launch(p, true, N, s_rowptr, s_perm, s_recv, x, y, w, grad_out, scale, grad_x,
                       grad_y, grad_w, grad_x ? 1 : 0, grad_y ? 1 : 0, grad_w ? 1 : 0, s, scratch,
                       std::min<int64_t>(rows, kSharedWRows));

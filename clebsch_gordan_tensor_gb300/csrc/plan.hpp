@@ -53,6 +53,7 @@ struct Plan {
     int maxterms = 1;
     cgtp_dtype dtype = CGTP_F32;
     cgtp_wmode wmode = CGTP_W_PER_EDGE;
+    bool w_bf16 = false;  // weights stored as bfloat16 (fp32 arithmetic)
     unsigned flags = 0;
 
     // launch geometry (fixed at plan creation)

@@ -26,6 +26,7 @@
 //   * radial_simt_kernel (fp32 / fp64, any shape): shared-memory tiles and
 //     FMA micro-tiles on the CUDA cores.
 // Both compute b and h the same way on the CUDA cores.
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -37,6 +38,13 @@
 namespace cgtp {
 
 __device__ int cgtp_radial_error;  // nonzero: a bounded wait timed out
+
+// Output element: the compute type, or bfloat16 (rounded to nearest even).
+template <typename TW, typename T>
+__device__ __forceinline__ TW out_cast(T v) {
+    if constexpr (sizeof(TW) == 2) return __float2bfloat16_rn((float)v);
+    else return (TW)v;
+}
 
 template <typename T>
 __device__ __forceinline__ T silu_f(T a) {
@@ -56,10 +64,10 @@ constexpr int kSimtEdges = 32;   // edges per tile
 constexpr int kSimtCols = 128;   // output columns per pass
 constexpr int kSimtThreads = 256;
 
-template <typename T>
+template <typename T, typename TW>
 __global__ void __launch_bounds__(kSimtThreads)
 radial_simt_kernel(int64_t E, int nb, T rc, int hidden, int64_t n_out, const T* __restrict__ vec,
-                   const T* __restrict__ W1, const T* __restrict__ W2, T* __restrict__ w,
+                   const T* __restrict__ W1, const T* __restrict__ W2, TW* __restrict__ w,
                    T* __restrict__ h) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     T* bS = reinterpret_cast<T*>(smem_raw);  // [kSimtEdges][nb]
@@ -116,7 +124,7 @@ radial_simt_kernel(int64_t E, int nb, T rc, int hidden, int64_t n_out, const T* 
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     const int64_t c = c0 + cgp * 4 + q;
-                    if (c < n_out) w[(e0 + le) * n_out + c] = acc[i][q];
+                    if (c < n_out) w[(e0 + le) * n_out + c] = out_cast<TW>(acc[i][q]);
                 }
             }
         }
@@ -284,10 +292,11 @@ __global__ void radial_pack_kernel(int hidden, int64_t n_out, const float* __res
 // than one phase behind the barrier it waits on.  Every wait is bounded; a
 // timeout sets `fail`, each role leaves its loop, and the CTA releases its
 // tensor memory after a grace period.
+template <typename TW>
 __global__ void __launch_bounds__(kTcThreads, 1)
 radial_tc_kernel(int64_t E, int nb, float rc, int hidden, int64_t n_out,
                  const float* __restrict__ vec, const float* __restrict__ W1,
-                 const unsigned char* __restrict__ img, float* __restrict__ w,
+                 const unsigned char* __restrict__ img, TW* __restrict__ w,
                  float* __restrict__ h) {
     extern __shared__ __align__(1024) unsigned char smem[];
     __shared__ __align__(8) unsigned long long mma_done[2], acc_free[2], b_full[kTcBSlots];
@@ -503,9 +512,19 @@ radial_tc_kernel(int64_t E, int nb, float rc, int hidden, int64_t n_out,
                             const int64_t e = e0 + 16 * hp + r;
                             const float4 val = *reinterpret_cast<const float4*>(
                                 stage + r * kTcStagePitch + (lane & 7) * 4);
-                            if (e < E)
-                                *reinterpret_cast<float4*>(w + e * n_out + col0 + blk * 32 +
-                                                           (lane & 7) * 4) = val;
+                            if (e < E) {
+                                TW* dst = w + e * n_out + col0 + blk * 32 + (lane & 7) * 4;
+                                if constexpr (sizeof(TW) == 2) {
+                                    const __nv_bfloat162 a = __floats2bfloat162_rn(val.x, val.y);
+                                    const __nv_bfloat162 b2 = __floats2bfloat162_rn(val.z, val.w);
+                                    uint2 u;
+                                    u.x = *reinterpret_cast<const unsigned*>(&a);
+                                    u.y = *reinterpret_cast<const unsigned*>(&b2);
+                                    *reinterpret_cast<uint2*>(dst) = u;
+                                } else {
+                                    *reinterpret_cast<float4*>(dst) = val;
+                                }
+                            }
                         }
                         __syncwarp();
                     }
@@ -541,17 +560,18 @@ size_t radial_workspace_bytes(bool f64, int nb, int hidden, int64_t n_out) {
     return (size_t)n_out * hidden * 8;  // TF32 hi and lo parts of W2, packed
 }
 
-cudaError_t launch_radial_forward(bool f64, bool tensor_cores, int64_t E, int nb, double rc,
-                                  int hidden, int64_t n_out, const void* vec, const void* W1,
-                                  const void* W2, void* w, void* h, void* ws, size_t ws_bytes,
-                                  cudaStream_t s) {
+cudaError_t launch_radial_forward(bool f64, bool tensor_cores, bool out_bf16, int64_t E, int nb,
+                                  double rc, int hidden, int64_t n_out, const void* vec,
+                                  const void* W1, const void* W2, void* w, void* h, void* ws,
+                                  size_t ws_bytes, cudaStream_t s) {
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
+    (void)ws_bytes;
     if (tensor_cores) {
-        e = cudaFuncSetAttribute(radial_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)kTcSmem);
+        auto* kern = out_bf16 ? (void*)radial_tc_kernel<__nv_bfloat16> : (void*)radial_tc_kernel<float>;
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTcSmem);
         if (e != cudaSuccess) return e;
         const int64_t total = (int64_t)hidden * n_out;
         const unsigned pg =
@@ -561,29 +581,42 @@ cudaError_t launch_radial_forward(bool f64, bool tensor_cores, int64_t E, int nb
         if (e != cudaSuccess) return e;
         const int64_t tiles = (E + kTcM - 1) / kTcM;
         const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(tiles, sms));
-        radial_tc_kernel<<<grid, kTcThreads, kTcSmem, s>>>(E, nb, (float)rc, hidden, n_out,
-                                                           (const float*)vec, (const float*)W1,
-                                                           (const unsigned char*)ws, (float*)w,
-                                                           (float*)h);
+        if (out_bf16)
+            radial_tc_kernel<__nv_bfloat16><<<grid, kTcThreads, kTcSmem, s>>>(
+                E, nb, (float)rc, hidden, n_out, (const float*)vec, (const float*)W1,
+                (const unsigned char*)ws, (__nv_bfloat16*)w, (float*)h);
+        else
+            radial_tc_kernel<float><<<grid, kTcThreads, kTcSmem, s>>>(
+                E, nb, (float)rc, hidden, n_out, (const float*)vec, (const float*)W1,
+                (const unsigned char*)ws, (float*)w, (float*)h);
         return cudaGetLastError();
     }
     const size_t es = f64 ? 8 : 4;
     const size_t smem = (size_t)kSimtEdges * (nb + hidden) * es;
-    auto* k64 = radial_simt_kernel<double>;
-    auto* k32 = radial_simt_kernel<float>;
-    e = f64 ? cudaFuncSetAttribute(k64, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)
-            : cudaFuncSetAttribute(k32, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
     const int64_t tiles = (E + kSimtEdges - 1) / kSimtEdges;
     const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(tiles, (int64_t)sms * 8));
-    if (f64)
-        k64<<<grid, kSimtThreads, smem, s>>>(E, nb, rc, hidden, n_out, (const double*)vec,
-                                             (const double*)W1, (const double*)W2, (double*)w,
-                                             (double*)h);
-    else
-        k32<<<grid, kSimtThreads, smem, s>>>(E, nb, (float)rc, hidden, n_out, (const float*)vec,
-                                             (const float*)W1, (const float*)W2, (float*)w,
-                                             (float*)h);
+    if (f64) {
+        auto* k = radial_simt_kernel<double, double>;
+        e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        k<<<grid, kSimtThreads, smem, s>>>(E, nb, rc, hidden, n_out, (const double*)vec,
+                                           (const double*)W1, (const double*)W2, (double*)w,
+                                           (double*)h);
+    } else if (out_bf16) {
+        auto* k = radial_simt_kernel<float, __nv_bfloat16>;
+        e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        k<<<grid, kSimtThreads, smem, s>>>(E, nb, (float)rc, hidden, n_out, (const float*)vec,
+                                           (const float*)W1, (const float*)W2, (__nv_bfloat16*)w,
+                                           (float*)h);
+    } else {
+        auto* k = radial_simt_kernel<float, float>;
+        e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        k<<<grid, kSimtThreads, smem, s>>>(E, nb, (float)rc, hidden, n_out, (const float*)vec,
+                                           (const float*)W1, (const float*)W2, (float*)w,
+                                           (float*)h);
+    }
     return cudaGetLastError();
 }
 

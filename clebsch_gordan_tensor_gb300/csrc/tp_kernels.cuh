@@ -87,6 +87,38 @@ __device__ __forceinline__ VR ldv_m(const REAL* p, int ch) {
     return CH_ACTIVE(ch) ? ldv(p, ch) : vzero();
 }
 
+// Weight storage: REAL, or bfloat16 (W_BF16) widened exactly to fp32 on load;
+// the arithmetic is the same either way.  WRAW is what one lane loads for its
+// channels (two bf16 in one 32-bit word when CPT == 2: channel 2ch in the low
+// half).
+#if W_BF16
+typedef unsigned short WT;
+#if CPT == 2
+typedef unsigned WRAW;
+__device__ __forceinline__ VR wcvt(WRAW u) {
+    return ((u64)(u & 0xffff0000u) << 32) | (u64)(u << 16);
+}
+#else
+typedef unsigned short WRAW;
+__device__ __forceinline__ VR wcvt(WRAW u) { return __uint_as_float((unsigned)u << 16); }
+#endif
+#else
+typedef REAL WT;
+typedef VR WRAW;
+__device__ __forceinline__ VR wcvt(WRAW u) { return u; }
+#endif
+__device__ __forceinline__ WRAW ldw_raw(const WT* p, int ch) {
+    return __ldg(reinterpret_cast<const WRAW*>(p) + ch);
+}
+__device__ __forceinline__ VR ldw(const WT* p, int ch) { return wcvt(ldw_raw(p, ch)); }
+__device__ __forceinline__ VR ldw_m(const WT* p, int ch) {
+    return CH_ACTIVE(ch) ? ldw(p, ch) : vzero();
+}
+// from a shared-memory stage
+__device__ __forceinline__ VR lds_w(const WT* p, int ch) {
+    return wcvt(reinterpret_cast<const WRAW*>(p)[ch]);
+}
+
 // Weight of path p for this lane's channels, from global memory (direct
 // kernels) or from the shared-memory stage (staged kernels).
 __device__ __forceinline__ VR lds_v(const REAL* p, int ch) {
@@ -180,7 +212,7 @@ template <bool CONV>
 __device__ __forceinline__ void fwd_body(long long n_items, const int* __restrict__ rowptr,
                                          const int* __restrict__ sender,
                                          const REAL* __restrict__ x, const REAL* __restrict__ y,
-                                         const REAL* __restrict__ w, long long w_stride,
+                                         const WT* __restrict__ w, long long w_stride,
                                          REAL* __restrict__ out, REAL scale, int accumulate) {
     __shared__ __align__(16) REAL Ts_all[SLOTS][NTP];
     __shared__ __align__(16) REAL Ys_all[SLOTS][NYP];
@@ -233,9 +265,9 @@ __device__ __forceinline__ void fwd_body(long long n_items, const int* __restric
             const REAL* xrow = x + src * DIMX;
 #pragma unroll
             for (int r = 0; r < NX; ++r) xr[r] = ldv_m(xrow + r * MUL, ch);
-            const REAL* wrow = w + e * w_stride;
+            const WT* wrow = w + e * w_stride;
             gen_fwd(acc, Ts, [&](int r) { return xr[r]; },
-                    [&](int p) { return ldv_m(wrow + (long long)p * MUL, ch); });
+                    [&](int p) { return ldw_m(wrow + (long long)p * MUL, ch); });
             slot_sync(slot);
         }
         if (CH_ACTIVE(ch)) {
@@ -253,14 +285,14 @@ __device__ __forceinline__ void fwd_body(long long n_items, const int* __restric
 
 extern "C" __global__ void __launch_bounds__(BLOCK)
 cgtp_fwd_conv(long long n_items, const int* __restrict__ rowptr, const int* __restrict__ sender,
-              const REAL* __restrict__ x, const REAL* __restrict__ y, const REAL* __restrict__ w,
+              const REAL* __restrict__ x, const REAL* __restrict__ y, const WT* __restrict__ w,
               long long w_stride, REAL* __restrict__ out, REAL scale, int accumulate) {
     fwd_body<true>(n_items, rowptr, sender, x, y, w, w_stride, out, scale, accumulate);
 }
 
 extern "C" __global__ void __launch_bounds__(BLOCK)
 cgtp_fwd_single(long long n_items, const REAL* __restrict__ x, const REAL* __restrict__ y,
-                const REAL* __restrict__ w, long long w_stride, REAL* __restrict__ out, REAL scale,
+                const WT* __restrict__ w, long long w_stride, REAL* __restrict__ out, REAL scale,
                 int accumulate) {
     fwd_body<false>(n_items, nullptr, nullptr, x, y, w, w_stride, out, scale, accumulate);
 }
@@ -280,7 +312,7 @@ __device__ __forceinline__ void bwd_body(long long n_items, const int* __restric
                                          const int* __restrict__ s_perm,
                                          const int* __restrict__ s_recv,
                                          const REAL* __restrict__ x, const REAL* __restrict__ y,
-                                         const REAL* __restrict__ w, long long w_stride,
+                                         const WT* __restrict__ w, long long w_stride,
                                          const REAL* __restrict__ g, REAL scale,
                                          REAL* __restrict__ gx, REAL* __restrict__ gy,
                                          REAL* __restrict__ gw, int mgx, int mgy, int mgw,
@@ -356,13 +388,13 @@ __device__ __forceinline__ void bwd_body(long long n_items, const int* __restric
             const REAL* grow = g + n * DIMO;
 #pragma unroll
             for (int r = 0; r < NO; ++r) gr[r] = ldv_m(grow + r * MUL, ch);
-            const REAL* wrow = w + e * w_stride;
+            const WT* wrow = w + e * w_stride;
             REAL* gwrow = gw ? gw + e * WDIM : nullptr;
             REAL gyl[NYP];
 #pragma unroll
             for (int i = 0; i < NYP; ++i) gyl[i] = (REAL)0;
             gen_bwd<GY>(gxa, gyl, Ts, [&](int r) { return xr[r]; }, [&](int r) { return gr[r]; },
-                        [&](int p) { return ldv_m(wrow + (long long)p * MUL, ch); }, gwrow, gwa,
+                        [&](int p) { return ldw_m(wrow + (long long)p * MUL, ch); }, gwrow, gwa,
                         ch, sc, mgx != 0, mgw);
             if (GY && mgy) {
                 int base = 0;
@@ -412,7 +444,7 @@ __device__ __forceinline__ void bwd_body(long long n_items, const int* __restric
     extern "C" __global__ void __launch_bounds__(BLOCK) NAME(                                 \
         long long n_items, const int* __restrict__ s_rowptr, const int* __restrict__ s_perm,  \
         const int* __restrict__ s_recv, const REAL* __restrict__ x,                           \
-        const REAL* __restrict__ y, const REAL* __restrict__ w, long long w_stride,           \
+        const REAL* __restrict__ y, const WT* __restrict__ w, long long w_stride,             \
         const REAL* __restrict__ g, REAL scale, REAL* __restrict__ gx, REAL* __restrict__ gy, \
         REAL* __restrict__ gw, int mgx, int mgy, int mgw, REAL* __restrict__ wsp) {           \
         bwd_body<CONV, GY>(n_items, s_rowptr, s_perm, s_recv, x, y, w, w_stride, g, scale,    \
@@ -614,7 +646,7 @@ __device__ __forceinline__ void build_T_cta(REAL* __restrict__ Ts, const REAL* _
 
 // Stage layout: [W row][x or g row][y row][int header]; all offsets 16-aligned.
 constexpr unsigned SZ = sizeof(REAL);
-constexpr unsigned WB = (unsigned)(NP * MUL) * SZ;
+constexpr unsigned WB = (unsigned)(NP * MUL) * (unsigned)sizeof(WT);
 constexpr unsigned XB = (unsigned)(NX * MUL) * SZ;
 constexpr unsigned GB_ = (unsigned)(NO * MUL) * SZ;
 constexpr unsigned YB = (unsigned)NY * SZ;
@@ -662,7 +694,7 @@ struct FwdArgs {
     const int* __restrict__ sender;
     const REAL* __restrict__ x;
     const REAL* __restrict__ y;
-    const REAL* __restrict__ w;
+    const WT* __restrict__ w;
     long long w_stride;
     REAL* __restrict__ out;
     REAL scale;
@@ -706,7 +738,7 @@ __device__ __forceinline__ void fwd_group(const FwdArgs& A, const FwdShared& S, 
     VR wbuf[NP];
     if (S.e_begin < S.e_end)
 #pragma unroll
-        for (int p = 0; p < NP; ++p) wbuf[p] = ldv(A.w + S.e_begin * A.w_stride + p * MUL, ch);
+        for (int p = 0; p < NP; ++p) wbuf[p] = ldw(A.w + S.e_begin * A.w_stride + p * MUL, ch);
 #endif
     long long j = S.e_begin;
     long long nend = CONV ? (long long)__ldg(A.rowptr + S.i0 + 1) : S.i0 + 1;
@@ -727,15 +759,15 @@ __device__ __forceinline__ void fwd_group(const FwdArgs& A, const FwdShared& S, 
             VR xr[FG::NXR];
             FG::loadx(xr, reinterpret_cast<const REAL*>(st + WSF), ch);
 #if W_DIRECT_F
-            const REAL* wnext = A.w + (j + 1 < S.e_end ? j + 1 : j) * A.w_stride;
+            const WT* wnext = A.w + (j + 1 < S.e_end ? j + 1 : j) * A.w_stride;
             FG::edge(acc, S.Ts, xr, [&](int p) {
                 const VR v = wbuf[p];
-                wbuf[p] = ldv(wnext + p * MUL, ch);
+                wbuf[p] = ldw(wnext + p * MUL, ch);
                 return v;
             });
 #else
-            const REAL* ws = reinterpret_cast<const REAL*>(st);
-            FG::edge(acc, S.Ts, xr, [&](int p) { return lds_v(ws + p * MUL, ch); });
+            const WT* ws = reinterpret_cast<const WT*>(st);
+            FG::edge(acc, S.Ts, xr, [&](int p) { return lds_w(ws + p * MUL, ch); });
 #endif
             cta_sync();
             if constexpr (GRP == 0)
@@ -805,14 +837,14 @@ __device__ __forceinline__ void fwd_staged(const FwdArgs& A) {
 extern "C" __global__ void __launch_bounds__(NTF)
 cgtp_fwd_conv_tma(long long n_items, const int* __restrict__ rowptr,
                   const int* __restrict__ sender, const REAL* __restrict__ x,
-                  const REAL* __restrict__ y, const REAL* __restrict__ w, long long w_stride,
+                  const REAL* __restrict__ y, const WT* __restrict__ w, long long w_stride,
                   REAL* __restrict__ out, REAL scale, int accumulate) {
     fwd_staged<true>(FwdArgs{n_items, rowptr, sender, x, y, w, w_stride, out, scale, accumulate});
 }
 
 extern "C" __global__ void __launch_bounds__(NTF)
 cgtp_fwd_single_tma(long long n_items, const REAL* __restrict__ x, const REAL* __restrict__ y,
-                    const REAL* __restrict__ w, long long w_stride, REAL* __restrict__ out,
+                    const WT* __restrict__ w, long long w_stride, REAL* __restrict__ out,
                     REAL scale, int accumulate) {
     fwd_staged<false>(FwdArgs{n_items, nullptr, nullptr, x, y, w, w_stride, out, scale, accumulate});
 }
@@ -832,7 +864,7 @@ struct BwdArgs {
     const int* __restrict__ s_recv;
     const REAL* __restrict__ x;
     const REAL* __restrict__ y;
-    const REAL* __restrict__ w;
+    const WT* __restrict__ w;
     long long w_stride;
     const REAL* __restrict__ g;
     REAL scale;
@@ -897,14 +929,14 @@ __device__ __forceinline__ void bwd_group(const BwdArgs& A, const BwdShared& S, 
     // W_BUF2: the next edge's weights land in a second register array loaded
     // ahead of the stream; otherwise the stream reads a path's weight and
     // reloads that slot with the next edge's value.
-    VR wbuf[NP];
+    WRAW wbuf[NP];
 #if W_BUF2
-    VR wnext[NP];
+    WRAW wnext[NP];
 #endif
     if (S.j_begin < S.j_end) {
         const long long e0 = *reinterpret_cast<const int*>(S.stages + WSB + GB_ + YB);
 #pragma unroll
-        for (int p = 0; p < NP; ++p) wbuf[p] = ldv(A.w + e0 * A.w_stride + p * MUL, ch);
+        for (int p = 0; p < NP; ++p) wbuf[p] = ldw_raw(A.w + e0 * A.w_stride + p * MUL, ch);
     }
 #endif
     for (long long item = S.i0; item < S.i1; ++item) {
@@ -944,13 +976,13 @@ __device__ __forceinline__ void bwd_group(const BwdArgs& A, const BwdShared& S, 
                 const unsigned char* st1 = S.stages + (size_t)((k + 1) % STAGES_B) * BWD_STAGE;
                 e1 = *reinterpret_cast<const int*>(st1 + WSB + GB_ + YB);
             }
-            const REAL* wrow1 = A.w + e1 * A.w_stride;
+            const WT* wrow1 = A.w + e1 * A.w_stride;
 #if W_BUF2
 #pragma unroll
-            for (int p = 0; p < NP; ++p) wnext[p] = ldv(wrow1 + p * MUL, ch);
+            for (int p = 0; p < NP; ++p) wnext[p] = ldw_raw(wrow1 + p * MUL, ch);
             BG::template edge<GY>(gxa, gyl, S.Ts, xr,
                                   [&](int r) { return lds_v(gs + r * MUL, ch); },
-                                  [&](int p) { return wbuf[p]; }, gwrow, gwa, ch, sc,
+                                  [&](int p) { return wcvt(wbuf[p]); }, gwrow, gwa, ch, sc,
                                   A.mgx != 0, A.mgw);
 #pragma unroll
             for (int p = 0; p < NP; ++p) wbuf[p] = wnext[p];
@@ -958,17 +990,17 @@ __device__ __forceinline__ void bwd_group(const BwdArgs& A, const BwdShared& S, 
             BG::template edge<GY>(gxa, gyl, S.Ts, xr,
                                   [&](int r) { return lds_v(gs + r * MUL, ch); },
                                   [&](int p) {
-                                      const VR v = wbuf[p];
-                                      wbuf[p] = ldv(wrow1 + p * MUL, ch);
+                                      const VR v = wcvt(wbuf[p]);
+                                      wbuf[p] = ldw_raw(wrow1 + p * MUL, ch);
                                       return v;
                                   },
                                   gwrow, gwa, ch, sc, A.mgx != 0, A.mgw);
 #endif
 #else
-            const REAL* ws = reinterpret_cast<const REAL*>(st);
+            const WT* ws = reinterpret_cast<const WT*>(st);
             BG::template edge<GY>(gxa, gyl, S.Ts, xr,
                                   [&](int r) { return lds_v(gs + r * MUL, ch); },
-                                  [&](int p) { return lds_v(ws + p * MUL, ch); }, gwrow, gwa,
+                                  [&](int p) { return lds_w(ws + p * MUL, ch); }, gwrow, gwa,
                                   ch, sc, A.mgx != 0, A.mgw);
 #endif
             if (GY && A.mgy) {
@@ -1078,7 +1110,7 @@ __device__ __forceinline__ void bwd_staged(const BwdArgs& A) {
     extern "C" __global__ void __launch_bounds__(NTB) NAME(                                   \
         long long n_items, const int* __restrict__ s_rowptr, const int* __restrict__ s_perm,  \
         const int* __restrict__ s_recv, const REAL* __restrict__ x,                           \
-        const REAL* __restrict__ y, const REAL* __restrict__ w, long long w_stride,           \
+        const REAL* __restrict__ y, const WT* __restrict__ w, long long w_stride,             \
         const REAL* __restrict__ g, REAL scale, REAL* __restrict__ gx, REAL* __restrict__ gy, \
         REAL* __restrict__ gw, int mgx, int mgy, int mgw, REAL* __restrict__ wsp) {           \
         bwd_staged<CONV, GY>(BwdArgs{n_items, s_rowptr, s_perm, s_recv, x, y, w, w_stride, g, \

@@ -93,7 +93,14 @@ typedef struct {
  * in registers) instead of through the ring; bit 17: backward lanes take their
  * weights through the ring instead of loading them directly (the default for
  * fp32 plans); bit 18: directly loaded backward weights use one register
- * buffer (reloaded path by path) instead of two. */
+ * buffer (reloaded path by path) instead of two.
+ * CGTP_PLAN_WEIGHTS_BF16 (bit 24): the weights (w, per edge or shared) are
+ * stored as bfloat16 and widened exactly to fp32 on load; all arithmetic,
+ * every other tensor and grad_w stay fp32.  This halves the dominant weight
+ * stream ("BF16/FP16 ... with FP32 accumulation", "Speeding Up MACE",
+ * abstract).  fp32 plans only (else CGTP_E_UNSUPPORTED); the double backward
+ * of such a plan returns CGTP_E_UNSUPPORTED. */
+#define CGTP_PLAN_WEIGHTS_BF16 (1u << 24)
 cgtp_status cgtp_plan_create(cgtp_plan* out, const char* irreps_in1, const char* irreps_in2,
                              const char* irreps_out, const cgtp_instr* instr, int n_instr,
                              cgtp_dtype dtype, cgtp_wmode wmode, unsigned flags);
@@ -286,6 +293,10 @@ cgtp_status cgtp_edge_forces_adjoint(cgtp_dtype dtype, int64_t N, int64_t E,
  * shapes, fp64, no workspace, or flags & CGTP_RADIAL_CUDA_CORES run it on the
  * CUDA cores.  Asynchronous on `stream`; allocates nothing. */
 #define CGTP_RADIAL_CUDA_CORES 1u
+/* flags & CGTP_RADIAL_OUT_BF16: w is written as bfloat16 (rounded to nearest
+ * even; fp32 inputs only, else CGTP_E_UNSUPPORTED) for plans created with
+ * CGTP_PLAN_WEIGHTS_BF16; h stays fp32. */
+#define CGTP_RADIAL_OUT_BF16 2u
 cgtp_status cgtp_radial_forward(cgtp_dtype dtype, int64_t E, int n_basis, double cutoff,
                                 int hidden, int64_t n_out, const void* vec, const void* W1,
                                 const void* W2, void* w, void* h, void* workspace,

@@ -1,0 +1,136 @@
+"""GPU parity of plans whose weights are stored as bfloat16 (fp32 arithmetic,
+features and gradients): standalone and fused-conv forward and backward, the
+staged and the direct kernels, per-edge and shared weights, and the radial
+network writing bfloat16 weights.  The oracle receives the same bfloat16
+values widened to fp64, so the comparison keeps the fp32 tolerance."""
+import numpy as np
+import pytest
+
+import oracle as O
+import workloads as W
+from tests.gpu_util import assert_close, dev, host, need_gpu, torch
+
+pytestmark = pytest.mark.gpu
+
+
+def _bf16(a):
+    """bfloat16 device tensor and the exact fp64 values it holds."""
+    t = torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(torch.bfloat16).cuda()
+    return t, t.float().cpu().numpy().astype(np.float64)
+
+
+CASES = [
+    W.CFG2,                                                   # mul 64: two channels per lane, staged
+    ("3x0e+3x1o", "0e+1o+2e", "3x0e+3x1o+3x2e"),              # masked lanes, direct
+    ("5x0e+5x1o", "0e+1o+2e", "5x0e+5x1o+5x2e"),              # odd mul: one channel per lane
+    (W.CFG1[0], W.CFG1[1], W.CFG1[2]),                        # mul 128: two warps per item
+]
+
+
+@pytest.mark.parametrize("irreps", CASES, ids=lambda c: c[0][:10])
+@pytest.mark.parametrize("B", [1, 333])
+def test_standalone_bf16_weights(irreps, B):
+    need_gpu()
+    import clebsch_gordan_tensor_gb300 as cg
+    prob = O.make_problem(*irreps)
+    plan = cg.Plan(*irreps, weight_dtype=torch.bfloat16)
+    rng = np.random.default_rng(B)
+    x = rng.standard_normal((B, prob.dim1)).astype(np.float32)
+    y = rng.standard_normal((B, prob.dim2)).astype(np.float32)
+    wd, wr = _bf16(rng.standard_normal((B, prob.wdim)))
+    g = rng.standard_normal((B, prob.dimo)).astype(np.float32)
+    out = plan.forward(dev(x), dev(y), wd)
+    assert_close(host(out), O.tp_forward(prob, x, y, wr), np.float32, "forward")
+    gx, gy, gw = plan.backward(dev(x), dev(y), wd, dev(g))
+    assert gw.dtype == torch.float32
+    rx, ry, rw = O.tp_backward(prob, x, y, wr, g)
+    assert_close(host(gx), rx, np.float32, "grad_x")
+    assert_close(host(gy), ry, np.float32, "grad_y")
+    assert_close(host(gw), rw, np.float32, "grad_w")
+    with pytest.raises(cg.CgtpError, match="unsupported"):
+        plan.double_backward(dev(x), dev(y), wd, dev(g), gg_x=dev(x))
+
+
+def _cloud(n):
+    rng = np.random.default_rng(n)
+    _, _, gr = W.periodic_cloud(rng, n)
+    return gr, rng
+
+
+@pytest.mark.parametrize("misaligned", [False, True], ids=["staged", "direct"])
+def test_conv_bf16_weights(misaligned):
+    need_gpu()
+    import clebsch_gordan_tensor_gb300 as cg
+    gr, rng = _cloud(600)
+    irreps = W.CFG2
+    prob = O.make_problem(*irreps)
+    plan = cg.Plan(*irreps, weight_dtype=torch.bfloat16)
+    G = cg.Graph.from_numpy(gr)
+    x = rng.standard_normal((gr.N, prob.dim1)).astype(np.float32)
+    y = rng.standard_normal((gr.E, prob.dim2)).astype(np.float32)
+    wd, wr = _bf16(rng.standard_normal((gr.E, prob.wdim)))
+    if misaligned:  # a 4-byte offset view: not 16-byte aligned, so the direct kernels run
+        buf = torch.empty(gr.E * prob.wdim + 2, dtype=torch.bfloat16, device="cuda")
+        view = buf[2:].view(gr.E, prob.wdim)
+        view.copy_(wd)
+        wd = view
+    g = rng.standard_normal((gr.N, prob.dimo)).astype(np.float32)
+    out = plan.conv_forward(G, dev(x), dev(y), wd, 0.02)
+    ref = O.conv_forward(prob, gr.rowptr, gr.sender, x, y, wr, 0.02)
+    assert_close(host(out), ref, np.float32, "conv out")
+    gx, gy, gw = plan.conv_backward(G, dev(x), dev(y), wd, 0.02, dev(g))
+    rx, ry, rw = O.conv_backward(prob, gr.rowptr, gr.sender, x, y, wr, 0.02, g)
+    assert_close(host(gx), rx, np.float32, "conv grad_x")
+    assert_close(host(gy), ry, np.float32, "conv grad_y")
+    assert_close(host(gw), rw, np.float32, "conv grad_w")
+    assert plan.device_status() == 0
+
+
+def test_shared_bf16_weights():
+    need_gpu()
+    import clebsch_gordan_tensor_gb300 as cg
+    irreps = ("8x0e+8x1o", "0e+1o+2e", "8x0e+8x1o+8x2e")
+    prob = O.make_problem(*irreps)
+    plan = cg.Plan(*irreps, shared_weights=True, weight_dtype=torch.bfloat16)
+    rng = np.random.default_rng(4)
+    B = 700
+    x = rng.standard_normal((B, prob.dim1)).astype(np.float32)
+    y = rng.standard_normal((B, prob.dim2)).astype(np.float32)
+    wd, wr = _bf16(rng.standard_normal(prob.wdim))
+    g = rng.standard_normal((B, prob.dimo)).astype(np.float32)
+    out = plan.forward(dev(x), dev(y), wd)
+    assert_close(host(out), O.tp_forward(prob, x, y, wr), np.float32, "shared forward")
+    _, _, gw = plan.backward(dev(x), dev(y), wd, dev(g), need=(False, False, True))
+    assert_close(host(gw), O.tp_backward(prob, x, y, wr, g)[2], np.float32, "shared grad_w")
+
+
+@pytest.mark.parametrize("cuda_cores", [False, True])
+def test_radial_writes_bf16(cuda_cores):
+    """bfloat16 output: each element is the fp32 result rounded to nearest (8
+    significant bits), so it lies within half a bfloat16 unit (at most 2^-8
+    relative) of the fp32 result, which is itself within the fp32 normwise
+    tolerance (1e-5 of the largest value) of the oracle; and it is exactly
+    torch's rounding of the fp32 path's output."""
+    need_gpu()
+    import clebsch_gordan_tensor_gb300 as cg
+    rng = np.random.default_rng(8)
+    E, nb, hidden, n_out = 1111, 8, 64, 1536
+    d = rng.standard_normal((E, 3))
+    vec = (d / np.linalg.norm(d, axis=1, keepdims=True) * rng.uniform(0.5, 5, (E, 1))).astype(np.float32)
+    W1 = (rng.standard_normal((nb, hidden)) / np.sqrt(nb)).astype(np.float32)
+    W2 = (rng.standard_normal((hidden, n_out)) / 8).astype(np.float32)
+    w = cg.radial_forward(dev(vec), dev(W1), dev(W2), out_dtype=torch.bfloat16,
+                          cuda_cores=cuda_cores)
+    assert w.dtype == torch.bfloat16
+    rw, _ = O.radial_forward(vec, W1, W2)
+    got = w.float().cpu().numpy().astype(np.float64)
+    err = np.abs(got - rw)
+    assert np.all(err <= 2.0 ** -8 * np.abs(rw) * (1 + 1e-3) + 1e-5 * np.abs(rw).max())
+    # rounding is to nearest: the typical error is a quarter of a unit or less
+    assert np.median(err / np.maximum(np.abs(rw), 1e-30)) < 2.0 ** -9
+    wf = cg.radial_forward(dev(vec), dev(W1), dev(W2), cuda_cores=cuda_cores)
+    assert torch.equal(w, wf.to(torch.bfloat16))
+    assert cg.radial_device_status() == 0
+    # and it feeds a bfloat16-weight plan directly
+    plan = cg.Plan(*W.CFG2, weight_dtype=torch.bfloat16)
+    assert w.shape[1] == plan.weight_numel

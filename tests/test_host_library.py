@@ -110,6 +110,15 @@ def test_c_abi_argument_errors():
     err = ctypes.c_int(-1)
     assert L.cgtp_last_cuda_error(ctypes.byref(err)) == 0
     assert L.cgtp_plan_destroy(h) == 0
+    # bfloat16 weights: fp32 plans only; their weight rows need 4-byte alignment
+    assert L.cgtp_plan_create(ctypes.byref(h), b"64x0e", b"0e", b"64x0e", None, 0, 1, 0,
+                              1 << 24) == 4
+    assert L.cgtp_plan_create(ctypes.byref(h), b"64x0e", b"0e", b"64x0e", None, 0, 0, 0,
+                              1 << 24) == 0
+    a8, a2 = ctypes.c_void_p(0x1000), ctypes.c_void_p(0x1002)
+    assert L.cgtp_forward(h, 5, a8, a8, a2, a8, null) == 1
+    assert b"weight pointer" in L.cgtp_last_error_message()
+    assert L.cgtp_plan_destroy(h) == 0
     s = cg.Plan("2x0e", "0e", "2x0e", shared_weights=True)
     gx = ctypes.c_void_p(0x1000)
     # shared-weight gradient: needs the workspace variant, and enough scratch
