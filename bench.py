@@ -266,7 +266,12 @@ def make_conv(args, cg, W, torch):
     hidden, n_out = W2.shape
     side = {"radial_fwd": (lambda: cg.radial_forward(vec, W1, W2, cfg["cutoff"], out=w),
                            E * (3 + n_out) * 4 + (8 + n_out) * hidden * 4,
-                           2 * E * (8 * hidden + hidden * n_out))}
+                           2 * E * (8 * hidden + hidden * n_out)),
+            # gradient of the radial network for the conv gradient's grad_w:
+            # grad_w is read twice (gh = grad_w W2^T; grad_W2 = h^T grad_w)
+            "radial_bwd": (lambda: cg.radial_backward(vec, W1, W2, gw, cfg["cutoff"]),
+                           2 * E * n_out * 4 + E * 3 * 8 + (8 + n_out) * hidden * 4,
+                           4 * E * hidden * n_out + 4 * E * 8 * hidden)}
     wl = Workload("conv", desc, E, "edges/s", "f32", kernels,
                   conv_counts(Dims(plan), N, E, 4), ["sh_fwd", "conv_fwd"],
                   dict(N=N, E=E, mul=64, paths=plan.n_paths),
@@ -457,15 +462,22 @@ def run_gpu(args):
         _, nbytes, flops = wl.side[n]
         gbs = nbytes / (ms * 1e-3) / 1e9
         tf = flops / (ms * 1e-3) / 1e12
-        # tensor-core rate of the split TF32 products (three per multiply-add)
-        # against the measured bf16 GEMM peak scaled by the nominal tf32/bf16 ratio
-        tf32_peak = peaks["bf16"] * TF32_PER_BF16 if peaks.get("bf16") else None
-        side_out[n] = {"ms": ms, "hbm_gbs": gbs, "hbm_frac": gbs / peaks["hbm"], "tflops": tf,
-                       "tf32_issued_tflops": 3 * tf,
-                       "tf32_frac": 3 * tf / tf32_peak if tf32_peak else None,
-                       "bound": "hbm", "roofline_frac": gbs / peaks["hbm"],
-                       "note": "outside the step: per-edge weights from the radial network, "
-                               "recomputed every step of the e2e leg"}
+        if n == "radial_fwd":
+            # tensor-core rate of the split TF32 products (three per multiply-add)
+            # against the measured bf16 GEMM peak scaled by the nominal tf32/bf16 ratio
+            tf32_peak = peaks["bf16"] * TF32_PER_BF16 if peaks.get("bf16") else None
+            side_out[n] = {"ms": ms, "hbm_gbs": gbs, "hbm_frac": gbs / peaks["hbm"],
+                           "tflops": tf, "tf32_issued_tflops": 3 * tf,
+                           "tf32_frac": 3 * tf / tf32_peak if tf32_peak else None,
+                           "bound": "hbm", "roofline_frac": gbs / peaks["hbm"],
+                           "note": "outside the step: per-edge weights from the radial network, "
+                                   "recomputed every step of the e2e leg"}
+        else:
+            side_out[n] = {"ms": ms, "hbm_gbs": gbs, "hbm_frac": gbs / peaks["hbm"],
+                           "tflops": tf, "fp32_frac": tf / fp32_peak, "bound": "alu",
+                           "roofline_frac": tf / fp32_peak,
+                           "note": "outside the step: radial-network gradient (CUDA cores) "
+                                   "for the conv gradient's grad_w"}
     dom = max(names, key=lambda n: per[n])
     kd = kernels[dom]
     if kd["bound"] == "alu":

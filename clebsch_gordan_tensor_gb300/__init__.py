@@ -87,6 +87,9 @@ def lib() -> ctypes.CDLL:
                 "cgtp_radial_forward": [i32, i64, i32, ctypes.c_double, i32, i64, vp, vp, vp,
                                         vp, vp, vp, ctypes.c_size_t, ctypes.c_uint, vp],
                 "cgtp_radial_workspace": [i32, i32, i32, i64, P(ctypes.c_size_t)],
+                "cgtp_radial_backward": [i32, i64, i32, ctypes.c_double, i32, i64, vp, vp, vp, vp,
+                                         vp, vp, vp, vp, ctypes.c_size_t, vp],
+                "cgtp_radial_backward_workspace": [i32, i64, i32, i32, i64, P(ctypes.c_size_t)],
                 "cgtp_radial_path": [i32, i32, i32, i64, P(i32)],
                 "cgtp_radial_device_status": [P(i32)],
             }
@@ -406,6 +409,29 @@ def radial_forward(vec, W1, W2, cutoff: float = 5.0, out=None, hidden_out=None,
                                      (1 if cuda_cores else 0) | (2 if odt == torch.bfloat16 else 0),
                                      _stream()))
     return out
+
+
+def radial_backward(vec, W1, W2, grad_w, cutoff: float = 5.0, need=(True, True, True)):
+    """Gradients of radial_forward's output for the cotangent grad_w: returns
+    (grad_vec, grad_W1, grad_W2); entries not in `need` are None."""
+    E = vec.shape[0]
+    _need(vec, "vec", vec.dtype, (E, 3))
+    nb, hidden = W1.shape
+    n_out = W2.shape[1]
+    _need(W1, "W1", vec.dtype, (nb, hidden))
+    _need(W2, "W2", vec.dtype, (hidden, n_out))
+    _need(grad_w, "grad_w", vec.dtype, (E, n_out))
+    gv = torch.empty_like(vec) if need[0] else None
+    g1 = torch.empty_like(W1) if need[1] else None
+    g2 = torch.empty_like(W2) if need[2] else None
+    n = ctypes.c_size_t(0)
+    _check(lib().cgtp_radial_backward_workspace(_dt(vec.dtype), E, nb, hidden, n_out,
+                                                ctypes.byref(n)))
+    ws = torch.empty(n.value, dtype=torch.uint8, device=vec.device) if n.value else None
+    _check(lib().cgtp_radial_backward(_dt(vec.dtype), E, nb, float(cutoff), hidden, n_out,
+                                      _ptr(vec), _ptr(W1), _ptr(W2), _ptr(grad_w), _ptr(gv),
+                                      _ptr(g1), _ptr(g2), _ptr(ws), n.value, _stream()))
+    return gv, g1, g2
 
 
 def radial_uses_tensor_cores(dtype, n_basis: int, hidden: int, n_out: int) -> bool:

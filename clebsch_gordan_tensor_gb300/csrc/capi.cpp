@@ -688,6 +688,53 @@ cgtp_status cgtp_radial_forward(cgtp_dtype dtype, int64_t E, int n_basis, double
     GUARD_END
 }
 
+cgtp_status cgtp_radial_backward_workspace(cgtp_dtype dtype, int64_t E, int n_basis, int hidden,
+                                           int64_t n_out, size_t* bytes) {
+    GUARD_BEGIN
+    cgtp_status st = radial_check(dtype, E, n_basis, 1.0, hidden, n_out);
+    if (st != CGTP_OK) return st;
+    if (!bytes) return fail(CGTP_E_ARG, "NULL output");
+    *bytes = radial_backward_workspace_bytes(dtype == CGTP_F64, E, n_basis, hidden, n_out);
+    return CGTP_OK;
+    GUARD_END
+}
+
+cgtp_status cgtp_radial_backward(cgtp_dtype dtype, int64_t E, int n_basis, double cutoff,
+                                 int hidden, int64_t n_out, const void* vec, const void* W1,
+                                 const void* W2, const void* grad_w, void* grad_vec,
+                                 void* grad_W1, void* grad_W2, void* workspace,
+                                 size_t workspace_bytes, cgtp_stream stream) {
+    GUARD_BEGIN
+    cgtp_status st = radial_check(dtype, E, n_basis, cutoff, hidden, n_out);
+    if (st != CGTP_OK) return st;
+    const bool f64 = dtype == CGTP_F64;
+    const size_t es = f64 ? 8 : 4;
+    if (!grad_vec && !grad_W1 && !grad_W2) return CGTP_OK;
+    for (const void* q : {vec, W1, W2, grad_w, (const void*)grad_vec, (const void*)grad_W1,
+                          (const void*)grad_W2, (const void*)workspace})
+        if (!aligned(q, es)) return fail(CGTP_E_ARG, "tensor pointer not aligned to its element");
+    if (E == 0) {  // empty sums
+        if (grad_W1 && (st = zero(grad_W1, (int64_t)n_basis * hidden * es, S(stream))) != CGTP_OK)
+            return st;
+        if (grad_W2 && (st = zero(grad_W2, (int64_t)hidden * n_out * es, S(stream))) != CGTP_OK)
+            return st;
+        return CGTP_OK;
+    }
+    if (!vec || !W1 || !W2 || !grad_w) return fail(CGTP_E_ARG, "NULL input tensor");
+    const size_t need = radial_backward_workspace_bytes(f64, E, n_basis, hidden, n_out);
+    if ((grad_W1 || grad_W2) && (!workspace || workspace_bytes < need))
+        return fail(CGTP_E_ARG, "workspace of " + std::to_string(workspace_bytes) +
+                                    " bytes is smaller than the " + std::to_string(need) +
+                                    " bytes cgtp_radial_backward_workspace reports");
+    cudaError_t e = launch_radial_backward(f64, E, n_basis, cutoff, hidden, n_out, vec, W1, W2,
+                                           grad_w, grad_vec, grad_W1, grad_W2, workspace,
+                                           S(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "radial_backward");
+    count_launch();
+    return CGTP_OK;
+    GUARD_END
+}
+
 cgtp_status cgtp_radial_path(cgtp_dtype dtype, int n_basis, int hidden, int64_t n_out,
                              int* tensor_cores) {
     GUARD_BEGIN

@@ -546,6 +546,297 @@ radial_tc_kernel(int64_t E, int nb, float rc, int hidden, int64_t n_out,
                      : "memory");
 }
 
+// ---------------------------------------------------------------- gradient
+//
+// Vector-Jacobian product of w = silu(b(r) W1) W2 for a cotangent gw:
+//   gh   = gw W2^T,   gpre = gh * silu'(pre),   silu'(a) = s (1 + a (1 - s))
+//   gW2  = h^T gw,    gW1 = b^T gpre,           gb = gpre W1^T
+//   dr   = sum_n gb_n db_n/dr,  db_n/dr = sqrt(2/rc) (k cos(k r) / r - sin(k r) / r^2)
+//   gvec = dr vec / r   (0 at r = 0, where the basis is flat)
+// Sums over edges (gW1, gW2) are per-CTA partial rows in the caller's
+// workspace, added in fixed order afterwards: deterministic, no atomics.
+
+constexpr int kBwEdges = 32;   // edges per tile
+constexpr int kBwCols = 32;    // grad_w / W2 columns staged per step (edge kernel)
+constexpr int kBwThreads = 256;
+constexpr int kBwGrid1 = 512;  // CTAs of the edge kernel (at most)
+constexpr int kBwW2Cols = 128; // output columns per CTA of the W2 kernel
+constexpr int kBwW2Rows = 64;  // hidden units per pass of the W2 kernel
+
+static inline int64_t bw_tiles(int64_t E) { return (E + kBwEdges - 1) / kBwEdges; }
+static inline int64_t bw_grid1(int64_t E) {
+    return std::max<int64_t>(1, std::min<int64_t>(bw_tiles(E), kBwGrid1));
+}
+static inline int64_t bw_splits(int64_t E, int64_t n_out) {
+    const int64_t nc = (n_out + kBwW2Cols - 1) / kBwW2Cols;
+    return std::max<int64_t>(1, std::min<int64_t>(bw_tiles(E), std::max<int64_t>(1, kBwGrid1 / nc)));
+}
+
+// Basis values of a tile's edges into bS [kBwEdges][nb] and, per edge, r.
+template <typename T>
+__device__ __forceinline__ void bw_basis(int64_t e0, int ne, int nb, T rc, const T* __restrict__ vec,
+                                         T* bS, T* rS) {
+    const T pref = sqrt((T)2 / rc);
+    for (int i = threadIdx.x; i < kBwEdges * nb; i += blockDim.x) {
+        const int le = i / nb, n = i % nb;
+        T b = (T)0;
+        if (le < ne) {
+            const T* v = vec + 3 * (e0 + le);
+            const T r = sqrt(v[0] * v[0] + v[1] * v[1] + v[2] * v[2]);
+            b = bessel_f<T>(n + 1, r, rc, pref);
+            if (n == 0) rS[le] = r;
+        }
+        bS[i] = b;
+    }
+}
+
+// Per edge tile: gh (K = n_out), gpre, gb, dr and gvec; gW1 partial row of
+// this CTA accumulated in place (the CTA owns the row).
+template <typename T>
+__global__ void __launch_bounds__(kBwThreads)
+radial_bwd_edge_kernel(int64_t E, int nb, T rc, int hidden, int64_t n_out, const T* __restrict__ vec,
+                       const T* __restrict__ W1, const T* __restrict__ W2,
+                       const T* __restrict__ gw, T* __restrict__ gvec, T* __restrict__ gW1part) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    T* bS = reinterpret_cast<T*>(smem_raw);         // [kBwEdges][nb]
+    T* rS = bS + kBwEdges * nb;                      // [kBwEdges]
+    T* preS = rS + kBwEdges;                         // [kBwEdges][hidden]: pre, then gpre
+    T* gS = preS + kBwEdges * hidden;                // [kBwEdges][kBwCols + 1]
+    T* w2S = gS + kBwEdges * (kBwCols + 1);          // [hidden][kBwCols + 1]
+    T* gbS = w2S + hidden * (kBwCols + 1);           // [kBwEdges][nb]
+    const int tid = threadIdx.x;
+    T* part = gW1part ? gW1part + (int64_t)blockIdx.x * nb * hidden : nullptr;
+    if (part)
+        for (int i = tid; i < nb * hidden; i += kBwThreads) part[i] = (T)0;
+    const T pref = sqrt((T)2 / rc);
+    const int eg = tid / 32, hq = tid % 32;  // 4 edges x hidden units hq, hq + 32, ...
+    const int nt = (hidden + 31) / 32;       // at most 8
+    for (int64_t e0 = (int64_t)blockIdx.x * kBwEdges; e0 < E; e0 += (int64_t)gridDim.x * kBwEdges) {
+        const int ne = E - e0 < kBwEdges ? (int)(E - e0) : kBwEdges;
+        bw_basis<T>(e0, ne, nb, rc, vec, bS, rS);
+        __syncthreads();
+        for (int i = tid; i < kBwEdges * hidden; i += kBwThreads) {
+            const int le = i / hidden, j = i % hidden;
+            T a = (T)0;
+            for (int n = 0; n < nb; ++n) a = fma(bS[le * nb + n], __ldg(W1 + n * hidden + j), a);
+            preS[i] = a;
+        }
+        // gh = gw W2^T, columns staged kBwCols at a time
+        T acc[4][8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int t = 0; t < 8; ++t) acc[i][t] = (T)0;
+        for (int64_t k0 = 0; k0 < n_out; k0 += kBwCols) {
+            const int kc = n_out - k0 < kBwCols ? (int)(n_out - k0) : kBwCols;
+            __syncthreads();
+            for (int i = tid; i < kBwEdges * kBwCols; i += kBwThreads) {
+                const int le = i / kBwCols, k = i % kBwCols;
+                gS[le * (kBwCols + 1) + k] = (le < ne && k < kc) ? gw[(e0 + le) * n_out + k0 + k] : (T)0;
+            }
+            for (int i = tid; i < hidden * kBwCols; i += kBwThreads) {
+                const int j = i / kBwCols, k = i % kBwCols;
+                w2S[j * (kBwCols + 1) + k] = k < kc ? __ldg(W2 + (int64_t)j * n_out + k0 + k) : (T)0;
+            }
+            __syncthreads();
+            for (int k = 0; k < kBwCols; ++k) {
+                T a[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) a[i] = gS[(eg * 4 + i) * (kBwCols + 1) + k];
+#pragma unroll
+                for (int t = 0; t < 8; ++t) {
+                    if (t >= nt) break;
+                    const int j = hq + 32 * t;
+                    const T bv = j < hidden ? w2S[j * (kBwCols + 1) + k] : (T)0;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) acc[i][t] = fma(a[i], bv, acc[i][t]);
+                }
+            }
+        }
+        __syncthreads();
+        // gpre = gh * silu'(pre), in place of pre
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+                const int j = hq + 32 * t;
+                if (t < nt && j < hidden) {
+                    const int idx = (eg * 4 + i) * hidden + j;
+                    const T pre = preS[idx];
+                    const T sg = (T)1 / ((T)1 + exp(-pre));
+                    preS[idx] = acc[i][t] * sg * ((T)1 + pre * ((T)1 - sg));
+                }
+            }
+        __syncthreads();
+        // gb = gpre W1^T, then dr and gvec per edge
+        for (int i = tid; i < kBwEdges * nb; i += kBwThreads) {
+            const int le = i / nb, n = i % nb;
+            T v = (T)0;
+            for (int j = 0; j < hidden; ++j) v = fma(preS[le * hidden + j], __ldg(W1 + n * hidden + j), v);
+            gbS[i] = v;
+        }
+        __syncthreads();
+        if (gvec && tid < ne) {
+            const T r = rS[tid];
+            T dr = (T)0;
+            if (r > (T)0) {
+                for (int n = 0; n < nb; ++n) {
+                    const T k = (T)(n + 1) * (T)3.14159265358979323846 / rc;
+                    dr = fma(gbS[tid * nb + n], pref * (k * cos(k * r) / r - sin(k * r) / (r * r)), dr);
+                }
+                dr /= r;
+            }
+            const T* v = vec + 3 * (e0 + tid);
+            T* o = gvec + 3 * (e0 + tid);
+            o[0] = dr * v[0];
+            o[1] = dr * v[1];
+            o[2] = dr * v[2];
+        }
+        // gW1 partial += b^T gpre (this CTA's row, entries owned by threads)
+        if (part)
+            for (int i = tid; i < nb * hidden; i += kBwThreads) {
+                const int n = i / hidden, j = i % hidden;
+                T v = part[i];
+                for (int le = 0; le < ne; ++le) v = fma(bS[le * nb + n], preS[le * hidden + j], v);
+                part[i] = v;
+            }
+        __syncthreads();
+    }
+}
+
+// gW2 partial rows: CTA (chunk c, split s) sums h^T gw over its edge range for
+// output columns [128 c, 128 c + 128), hidden units in passes of 64.
+template <typename T>
+__global__ void __launch_bounds__(kBwThreads)
+radial_bwd_w2_kernel(int64_t E, int nb, T rc, int hidden, int64_t n_out, int64_t splits,
+                     const T* __restrict__ vec, const T* __restrict__ W1,
+                     const T* __restrict__ gw, T* __restrict__ part) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    T* bS = reinterpret_cast<T*>(smem_raw);  // [kBwEdges][nb]
+    T* rS = bS + kBwEdges * nb;               // [kBwEdges]
+    T* hS = rS + kBwEdges;                    // [kBwEdges][kBwW2Rows]
+    T* gS = hS + kBwEdges * kBwW2Rows;        // [kBwEdges][kBwW2Cols]
+    const int tid = threadIdx.x;
+    const int64_t c = blockIdx.x / splits, sp = blockIdx.x % splits;
+    const int64_t col0 = c * kBwW2Cols;
+    const int ncol = n_out - col0 < kBwW2Cols ? (int)(n_out - col0) : kBwW2Cols;
+    const int64_t ea = E * sp / splits, eb = E * (sp + 1) / splits;
+    const int jg = tid / 32, cq = tid % 32;  // hidden rows jg, jg + 8, ...; columns 4 cq .. 4 cq + 3
+    T* out = part + sp * (int64_t)hidden * n_out;
+    for (int j0 = 0; j0 < hidden; j0 += kBwW2Rows) {
+        const int nj = hidden - j0 < kBwW2Rows ? hidden - j0 : kBwW2Rows;
+        T acc[8][4];
+#pragma unroll
+        for (int t = 0; t < 8; ++t)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) acc[t][q] = (T)0;
+        for (int64_t e0 = ea; e0 < eb; e0 += kBwEdges) {
+            const int ne = eb - e0 < kBwEdges ? (int)(eb - e0) : kBwEdges;
+            __syncthreads();
+            bw_basis<T>(e0, ne, nb, rc, vec, bS, rS);
+            for (int i = tid; i < kBwEdges * kBwW2Cols; i += kBwThreads) {
+                const int le = i / kBwW2Cols, k = i % kBwW2Cols;
+                gS[i] = (le < ne && k < ncol) ? gw[(e0 + le) * n_out + col0 + k] : (T)0;
+            }
+            __syncthreads();
+            for (int i = tid; i < kBwEdges * kBwW2Rows; i += kBwThreads) {
+                const int le = i / kBwW2Rows, j = i % kBwW2Rows;
+                T a = (T)0;
+                if (le < ne && j < nj) {
+                    for (int n = 0; n < nb; ++n) a = fma(bS[le * nb + n], __ldg(W1 + n * hidden + j0 + j), a);
+                    a = silu_f<T>(a);
+                }
+                hS[i] = a;
+            }
+            __syncthreads();
+            for (int le = 0; le < ne; ++le) {
+                T g4[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) g4[q] = gS[le * kBwW2Cols + 4 * cq + q];
+#pragma unroll
+                for (int t = 0; t < 8; ++t) {
+                    const T hv = hS[le * kBwW2Rows + jg + 8 * t];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) acc[t][q] = fma(hv, g4[q], acc[t][q]);
+                }
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+            const int j = jg + 8 * t;
+            if (j >= nj) continue;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int k = 4 * cq + q;
+                if (k < ncol) out[(int64_t)(j0 + j) * n_out + col0 + k] = acc[t][q];
+            }
+        }
+    }
+}
+
+size_t radial_backward_workspace_bytes(bool f64, int64_t E, int nb, int hidden, int64_t n_out) {
+    const size_t es = f64 ? 8 : 4;
+    return es * ((size_t)bw_grid1(E) * nb * hidden + (size_t)bw_splits(E, n_out) * hidden * n_out);
+}
+
+cudaError_t launch_radial_backward(bool f64, int64_t E, int nb, double rc, int hidden,
+                                   int64_t n_out, const void* vec, const void* W1, const void* W2,
+                                   const void* gw, void* gvec, void* gW1, void* gW2, void* ws,
+                                   cudaStream_t s) {
+    const size_t es = f64 ? 8 : 4;
+    const int64_t g1 = bw_grid1(E), sp = bw_splits(E, n_out);
+    const int64_t nc = (n_out + kBwW2Cols - 1) / kBwW2Cols;
+    unsigned char* p1 = (unsigned char*)ws;
+    unsigned char* p2 = p1 + (size_t)g1 * nb * hidden * es;
+    const size_t sm1 = es * ((size_t)kBwEdges * nb + kBwEdges + (size_t)kBwEdges * hidden +
+                             (size_t)kBwEdges * (kBwCols + 1) + (size_t)hidden * (kBwCols + 1) +
+                             (size_t)kBwEdges * nb);
+    const size_t sm2 = es * ((size_t)kBwEdges * nb + kBwEdges + (size_t)kBwEdges * kBwW2Rows +
+                             (size_t)kBwEdges * kBwW2Cols);
+    cudaError_t e;
+    if (gvec || gW1) {
+        if (f64) {
+            auto* k = radial_bwd_edge_kernel<double>;
+            if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm1)))
+                return e;
+            k<<<(unsigned)g1, kBwThreads, sm1, s>>>(E, nb, rc, hidden, n_out, (const double*)vec,
+                                                   (const double*)W1, (const double*)W2,
+                                                   (const double*)gw, (double*)gvec,
+                                                   gW1 ? (double*)p1 : nullptr);
+        } else {
+            auto* k = radial_bwd_edge_kernel<float>;
+            if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm1)))
+                return e;
+            k<<<(unsigned)g1, kBwThreads, sm1, s>>>(E, nb, (float)rc, hidden, n_out,
+                                                   (const float*)vec, (const float*)W1,
+                                                   (const float*)W2, (const float*)gw,
+                                                   (float*)gvec, gW1 ? (float*)p1 : nullptr);
+        }
+        if ((e = cudaGetLastError())) return e;
+        if (gW1 && (e = launch_reduce_rows(f64, p1, g1, (int64_t)nb * hidden, gW1, s))) return e;
+    }
+    if (gW2) {
+        if (f64) {
+            auto* k = radial_bwd_w2_kernel<double>;
+            if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm2)))
+                return e;
+            k<<<(unsigned)(nc * sp), kBwThreads, sm2, s>>>(E, nb, rc, hidden, n_out, sp,
+                                                          (const double*)vec, (const double*)W1,
+                                                          (const double*)gw, (double*)p2);
+        } else {
+            auto* k = radial_bwd_w2_kernel<float>;
+            if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm2)))
+                return e;
+            k<<<(unsigned)(nc * sp), kBwThreads, sm2, s>>>(E, nb, (float)rc, hidden, n_out, sp,
+                                                          (const float*)vec, (const float*)W1,
+                                                          (const float*)gw, (float*)p2);
+        }
+        if ((e = cudaGetLastError())) return e;
+        if ((e = launch_reduce_rows(f64, p2, sp, (int64_t)hidden * n_out, gW2, s))) return e;
+    }
+    return cudaSuccess;
+}
+
 // ------------------------------------------------------------------ host
 
 bool radial_tc_eligible(bool f64, int nb, int hidden, int64_t n_out, const void* vec,

@@ -95,3 +95,65 @@ def test_radial_benchmark_workload_sampled():
     rw, _ = O.radial_forward(cfg["vec"][idx], cfg["W1"], cfg["W2"], cfg["cutoff"])
     assert_close(host(w[torch.from_numpy(idx).cuda()]), rw, np.float32, "w rows")
     assert cg.radial_device_status() == 0
+
+
+BWD_CASES = [  # E, n_basis, hidden, n_out, dtype
+    (1000, 8, 64, 1536, np.float32),
+    (1, 8, 64, 256, np.float32),
+    (333, 5, 40, 200, np.float32),
+    (129, 32, 256, 96, np.float32),
+    (700, 8, 64, 384, np.float64),
+    (50, 3, 7, 5, np.float64),
+]
+
+
+@pytest.mark.parametrize("case", BWD_CASES, ids=lambda c: f"E{c[0]}-nb{c[1]}-h{c[2]}-o{c[3]}-{np.dtype(c[4]).name}")
+def test_radial_backward_matches_oracle(case):
+    need_gpu()
+    import clebsch_gordan_tensor_gb300 as cg
+    E, nb, hidden, n_out, dt = case
+    rng = np.random.default_rng(E + 7 * hidden)
+    vec, W1, W2 = _inputs(rng, E, nb, hidden, n_out, dt)
+    vec[0] = 0.0  # zero-length edge: no gradient
+    g = rng.standard_normal((E, n_out)).astype(dt)
+    gv, g1, g2 = cg.radial_backward(dev(vec), dev(W1), dev(W2), dev(g), 5.0)
+    rv, r1, r2 = O.radial_backward(vec, W1, W2, g, 5.0)
+    assert_close(host(gv), rv, dt, "grad_vec")
+    assert_close(host(g1), r1, dt, "grad_W1")
+    assert_close(host(g2), r2, dt, "grad_W2")
+    assert np.all(host(gv)[0] == 0.0)
+    # subsets, and a second call gives the same bits (ordered reductions)
+    _, g1b, g2b = cg.radial_backward(dev(vec), dev(W1), dev(W2), dev(g), 5.0,
+                                     need=(False, True, True))
+    assert torch.equal(g1b, g1) and torch.equal(g2b, g2)
+    gvb, n1, n2 = cg.radial_backward(dev(vec), dev(W1), dev(W2), dev(g), 5.0,
+                                     need=(True, False, False))
+    assert n1 is None and n2 is None and torch.equal(gvb, gv)
+
+
+def test_radial_backward_empty():
+    need_gpu()
+    import clebsch_gordan_tensor_gb300 as cg
+    W1 = torch.ones(8, 16, device="cuda")
+    W2 = torch.ones(16, 32, device="cuda")
+    gv, g1, g2 = cg.radial_backward(torch.zeros(0, 3, device="cuda"), W1, W2,
+                                    torch.zeros(0, 32, device="cuda"))
+    assert gv.shape == (0, 3)
+    assert float(g1.abs().max()) == 0.0 and float(g2.abs().max()) == 0.0
+
+
+def test_radial_backward_benchmark_workload():
+    """Full size (525k edges, 8 -> 64 -> 1536): the oracle's grad_W1 / grad_W2
+    over all edges (fp64 matmuls) and grad_vec on sampled edges."""
+    need_gpu()
+    import clebsch_gordan_tensor_gb300 as cg
+    cfg = W.config2()
+    E = cfg["graph"].E
+    g = np.random.default_rng(5).standard_normal((E, 1536)).astype(np.float32)
+    gv, g1, g2 = cg.radial_backward(dev(cfg["vec"]), dev(cfg["W1"]), dev(cfg["W2"]), dev(g),
+                                    cfg["cutoff"])
+    rv, r1, r2 = O.radial_backward(cfg["vec"], cfg["W1"], cfg["W2"], g, cfg["cutoff"])
+    assert_close(host(g1), r1, np.float32, "grad_W1")
+    assert_close(host(g2), r2, np.float32, "grad_W2")
+    idx = np.unique(np.concatenate([np.random.default_rng(6).choice(E, 3000, replace=False), [0, E - 1]]))
+    assert_close(host(gv)[idx], rv[idx], np.float32, "grad_vec rows")
