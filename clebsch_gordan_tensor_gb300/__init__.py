@@ -88,7 +88,7 @@ def lib() -> ctypes.CDLL:
                                         vp, vp, vp, ctypes.c_size_t, ctypes.c_uint, vp],
                 "cgtp_radial_workspace": [i32, i32, i32, i64, P(ctypes.c_size_t)],
                 "cgtp_radial_backward": [i32, i64, i32, ctypes.c_double, i32, i64, vp, vp, vp, vp,
-                                         vp, vp, vp, vp, ctypes.c_size_t, vp],
+                                         vp, vp, vp, vp, ctypes.c_size_t, ctypes.c_uint, vp],
                 "cgtp_radial_backward_workspace": [i32, i64, i32, i32, i64, P(ctypes.c_size_t)],
                 "cgtp_radial_path": [i32, i32, i32, i64, P(i32)],
                 "cgtp_radial_device_status": [P(i32)],
@@ -411,7 +411,8 @@ def radial_forward(vec, W1, W2, cutoff: float = 5.0, out=None, hidden_out=None,
     return out
 
 
-def radial_backward(vec, W1, W2, grad_w, cutoff: float = 5.0, need=(True, True, True)):
+def radial_backward(vec, W1, W2, grad_w, cutoff: float = 5.0, need=(True, True, True),
+                    cuda_cores: bool = False):
     """Gradients of radial_forward's output for the cotangent grad_w: returns
     (grad_vec, grad_W1, grad_W2); entries not in `need` are None."""
     E = vec.shape[0]
@@ -430,7 +431,8 @@ def radial_backward(vec, W1, W2, grad_w, cutoff: float = 5.0, need=(True, True, 
     ws = torch.empty(n.value, dtype=torch.uint8, device=vec.device) if n.value else None
     _check(lib().cgtp_radial_backward(_dt(vec.dtype), E, nb, float(cutoff), hidden, n_out,
                                       _ptr(vec), _ptr(W1), _ptr(W2), _ptr(grad_w), _ptr(gv),
-                                      _ptr(g1), _ptr(g2), _ptr(ws), n.value, _stream()))
+                                      _ptr(g1), _ptr(g2), _ptr(ws), n.value,
+                                      1 if cuda_cores else 0, _stream()))
     return gv, g1, g2
 
 

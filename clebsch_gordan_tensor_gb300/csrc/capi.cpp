@@ -703,7 +703,7 @@ cgtp_status cgtp_radial_backward(cgtp_dtype dtype, int64_t E, int n_basis, doubl
                                  int hidden, int64_t n_out, const void* vec, const void* W1,
                                  const void* W2, const void* grad_w, void* grad_vec,
                                  void* grad_W1, void* grad_W2, void* workspace,
-                                 size_t workspace_bytes, cgtp_stream stream) {
+                                 size_t workspace_bytes, unsigned flags, cgtp_stream stream) {
     GUARD_BEGIN
     cgtp_status st = radial_check(dtype, E, n_basis, cutoff, hidden, n_out);
     if (st != CGTP_OK) return st;
@@ -722,12 +722,14 @@ cgtp_status cgtp_radial_backward(cgtp_dtype dtype, int64_t E, int n_basis, doubl
     }
     if (!vec || !W1 || !W2 || !grad_w) return fail(CGTP_E_ARG, "NULL input tensor");
     const size_t need = radial_backward_workspace_bytes(f64, E, n_basis, hidden, n_out);
-    if ((grad_W1 || grad_W2) && (!workspace || workspace_bytes < need))
+    if (!workspace || workspace_bytes < need || !aligned(workspace, 16))
         return fail(CGTP_E_ARG, "workspace of " + std::to_string(workspace_bytes) +
                                     " bytes is smaller than the " + std::to_string(need) +
                                     " bytes cgtp_radial_backward_workspace reports");
-    cudaError_t e = launch_radial_backward(f64, E, n_basis, cutoff, hidden, n_out, vec, W1, W2,
-                                           grad_w, grad_vec, grad_W1, grad_W2, workspace,
+    const bool tc = !(flags & CGTP_RADIAL_CUDA_CORES) &&
+                    radial_tc_eligible(f64, n_basis, hidden, n_out, vec, W2, grad_w, nullptr);
+    cudaError_t e = launch_radial_backward(f64, tc, E, n_basis, cutoff, hidden, n_out, vec, W1,
+                                           W2, grad_w, grad_vec, grad_W1, grad_W2, workspace,
                                            S(stream));
     if (e != cudaSuccess) return cuda_fail(e, "radial_backward");
     count_launch();

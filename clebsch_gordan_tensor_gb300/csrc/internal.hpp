@@ -57,10 +57,10 @@ cudaError_t launch_radial_forward(bool f64, bool tensor_cores, bool out_bf16, in
                                   size_t ws_bytes, cudaStream_t s);
 cudaError_t radial_device_status(int* code);
 size_t radial_backward_workspace_bytes(bool f64, int64_t E, int nb, int hidden, int64_t n_out);
-cudaError_t launch_radial_backward(bool f64, int64_t E, int nb, double rc, int hidden,
-                                   int64_t n_out, const void* vec, const void* W1, const void* W2,
-                                   const void* gw, void* gvec, void* gW1, void* gW2, void* ws,
-                                   cudaStream_t s);
+cudaError_t launch_radial_backward(bool f64, bool tensor_cores, int64_t E, int nb, double rc,
+                                   int hidden, int64_t n_out, const void* vec, const void* W1,
+                                   const void* W2, const void* gw, void* gvec, void* gW1,
+                                   void* gW2, void* ws, cudaStream_t s);
 
 // Partial weight-gradient rows a shared-weight backward may write (grid cap).
 constexpr int64_t kSharedWRows = 2048;

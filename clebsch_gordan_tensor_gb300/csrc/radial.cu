@@ -251,6 +251,17 @@ __device__ __forceinline__ void tmem_ld32(unsigned taddr, float (&v)[32]) {
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+__device__ __forceinline__ void tmem_ld8(unsigned taddr, float (&v)[8]) {
+    uint32_t r[8];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                   "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 // W2 packed once per call as the shared-memory image of B: per 128-column
 // chunk c, the TF32 "hi" part then the "lo" part, each 128 rows (output
 // columns) x hidden in the K-major core-matrix layout (128 * hidden * 4 bytes).
@@ -774,27 +785,361 @@ radial_bwd_w2_kernel(int64_t E, int nb, T rc, int hidden, int64_t n_out, int64_t
     }
 }
 
-size_t radial_backward_workspace_bytes(bool f64, int64_t E, int nb, int hidden, int64_t n_out) {
-    const size_t es = f64 ? 8 : 4;
-    return es * ((size_t)bw_grid1(E) * nb * hidden + (size_t)bw_splits(E, n_out) * hidden * n_out);
+// ------------------------------------------------- gradient on tensor cores
+//
+// gh = gw W2^T as an MMA with M = 128 edges, K = n_out (streamed 32 columns
+// at a time), and N = 2 hidden: B holds W2^T's TF32 hi part in rows
+// [0, hidden) and its lo part in rows [hidden, 2 hidden), so the two MMAs
+// A_hi B and A_lo B give hi.hi + lo.hi in columns [0, hidden) and hi.lo +
+// lo.lo in [hidden, 2 hidden); gh is their sum (fp32 accuracy, full-rate
+// N = 128 instructions for hidden = 64).  The epilogue finishes the chain per
+// edge (pre, silu', gpre, gb, dr, gvec) and adds b^T gpre of the tile to the
+// CTA's grad_W1 partial row in fixed edge order.
+
+constexpr int kGhK = 32;                 // grad_w columns per chunk
+constexpr int kGhThreads = 32 * 9;       // 4 producer, 4 epilogue, 1 issuer warps
+constexpr unsigned kGhA = kTcM * kGhK * 4;          // one tf32 part of an A chunk (16 KB)
+constexpr unsigned kGhB = 2 * kTcKMax * kGhK * 4;   // a B chunk at hidden = 64 (16 KB)
+constexpr int kGhBSlots = 4;                        // B ring depth
+constexpr int kGhGp = kTcKMax + 1;   // padded row pitch of the gpre / basis staging
+constexpr int kGhBp = kTcNbMax + 1;
+constexpr unsigned kGhSmem =
+    2 * 2 * kGhA + kGhBSlots * kGhB + kTcM * kGhGp * 4 + kTcM * kGhBp * 4;
+
+__host__ __device__ constexpr uint32_t gh_idesc(int n) {
+    return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(kTcM >> 4) << 24);
 }
 
-cudaError_t launch_radial_backward(bool f64, int64_t E, int nb, double rc, int hidden,
-                                   int64_t n_out, const void* vec, const void* W1, const void* W2,
-                                   const void* gw, void* gvec, void* gW1, void* gW2, void* ws,
-                                   cudaStream_t s) {
+__device__ __forceinline__ void mma_tf32_n(unsigned tmem_d, uint64_t a, uint64_t b, uint32_t idesc,
+                                           unsigned acc) {
+    asm volatile(
+        "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
+// W2^T packed per 32-column chunk c: rows r < hidden hold hi(W2[r][32 c + k]),
+// rows hidden + r hold lo(...), K-major core matrices, 2 hidden x 32 x 4 bytes.
+__global__ void radial_pack_t_kernel(int hidden, int64_t n_out, const float* __restrict__ W2,
+                                     unsigned char* __restrict__ img) {
+    const int64_t total = (int64_t)hidden * n_out;
+    const size_t chunk = (size_t)2 * hidden * kGhK * 4;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int j = (int)(i / n_out);
+        const int64_t col = i % n_out;
+        const int64_t c = col / kGhK;
+        const int k = (int)(col % kGhK);
+        const float x = W2[i];
+        const float hi = to_tf32(x), lo = to_tf32(x - hi);
+        unsigned char* base = img + (size_t)c * chunk;
+        *reinterpret_cast<float*>(base + kmajor_offset(j, k, 2 * hidden)) = hi;
+        *reinterpret_cast<float*>(base + kmajor_offset(hidden + j, k, 2 * hidden)) = lo;
+    }
+}
+
+__global__ void __launch_bounds__(kGhThreads, 1)
+radial_bwd_tc_kernel(int64_t E, int nb, float rc, int hidden, int64_t n_out,
+                     const float* __restrict__ vec, const float* __restrict__ W1,
+                     const unsigned char* __restrict__ img, const float* __restrict__ gw,
+                     float* __restrict__ gvec, float* __restrict__ gW1part) {
+    extern __shared__ __align__(1024) unsigned char smem[];
+    __shared__ __align__(8) unsigned long long a_full[2], mma_done[2], b_full[kGhBSlots];
+    __shared__ __align__(8) unsigned long long acc_full[2], acc_free[2];
+    __shared__ __align__(16) float W1s[kTcNbMax * kTcKMax];
+    __shared__ unsigned tmem_base;
+    __shared__ int fail;
+    unsigned char* Aring = smem;                   // slot s: hi at 2 s kGhA, lo at (2 s + 1) kGhA
+    unsigned char* Bring = smem + 4 * kGhA;        // slot s at s kGhB
+    // [128][kGhGp] and [128][kGhBp]: odd pitches keep a warp's row-per-thread
+    // stores in distinct banks
+    float* gpS = reinterpret_cast<float*>(smem + 4 * kGhA + kGhBSlots * kGhB);
+    float* bS = gpS + kTcM * kGhGp;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int NB = 2 * hidden;
+    const uint32_t idesc = gh_idesc(NB);
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_addr(&tmem_base)),
+                     "r"(256u)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    if (tid == 0) {
+        for (int i = 0; i < 2; ++i) {
+            tc_mbar_init(&a_full[i], 4);  // one arrival per producer warp
+            tc_mbar_init(&mma_done[i], 1);
+            tc_mbar_init(&acc_full[i], 1);
+            tc_mbar_init(&acc_free[i], 128);
+        }
+        for (int i = 0; i < kGhBSlots; ++i) tc_mbar_init(&b_full[i], 1);
+        fail = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    for (int i = tid; i < nb * hidden; i += kGhThreads) W1s[i] = W1[i];
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    const unsigned tmem = tmem_base;
+    const int64_t nchunk = n_out / kGhK;
+    const int64_t tiles = (E + kTcM - 1) / kTcM;
+    const int64_t my_tiles =
+        tiles > (int64_t)blockIdx.x ? (tiles - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+    const int64_t nk = my_tiles * nchunk;
+    const unsigned bchunk = (unsigned)(NB * kGhK * 4);
+    const unsigned lslice = (kTcM / 8) * 128, bslice = (unsigned)(NB / 8) * 128;  // K-slice strides
+    const float pref = sqrtf(2.0f / rc);
+    float* part = gW1part + (int64_t)blockIdx.x * nb * hidden;
+
+    if (warp < 4) {
+        // ---------------------------------------------------------- producers
+        const int p = tid;
+        // this thread's row chunks, loaded two chunks ahead of their use (the
+        // loads of chunks k + 1 and k + 2 are in flight while chunk k waits);
+        // the chunk loop is unrolled by three so the buffers stay in registers
+        auto load_chunk = [&](int64_t kk, float4 (&dst)[kGhK / 4]) {
+            const int64_t t = kk / nchunk, c = (kk % nchunk + blockIdx.x) % nchunk;
+            const int64_t e = ((int64_t)blockIdx.x + t * gridDim.x) * kTcM + p;
+#pragma unroll
+            for (int q4 = 0; q4 < kGhK / 4; ++q4)
+                dst[q4] = (kk < nk && e < E)
+                              ? __ldg(reinterpret_cast<const float4*>(gw + e * n_out + c * kGhK) + q4)
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+        };
+        // chunk kk from `cur` into A slot kk % 2, chunk kk + 2 loaded into `nxt`
+        auto step = [&](int64_t kk, const float4 (&cur)[kGhK / 4], float4 (&nxt)[kGhK / 4]) {
+            load_chunk(kk + 2, nxt);
+            const int s = (int)(kk & 1);
+            if (kk >= 2 && !tc_mbar_wait(&mma_done[s], (unsigned)(((kk - 2) >> 1) & 1))) return false;
+            unsigned char* hi = Aring + (size_t)(2 * s) * kGhA;
+            unsigned char* lo = hi + kGhA;
+#pragma unroll
+            for (int k4 = 0; k4 < kGhK; k4 += 4) {
+                const float4 v = cur[k4 / 4];
+                float4 h4, l4;
+                h4.x = to_tf32(v.x); l4.x = to_tf32(v.x - h4.x);
+                h4.y = to_tf32(v.y); l4.y = to_tf32(v.y - h4.y);
+                h4.z = to_tf32(v.z); l4.z = to_tf32(v.z - h4.z);
+                h4.w = to_tf32(v.w); l4.w = to_tf32(v.w - h4.w);
+                const unsigned off = kmajor_offset(p, k4, kTcM);
+                *reinterpret_cast<float4*>(hi + off) = h4;
+                *reinterpret_cast<float4*>(lo + off) = l4;
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();  // the warp's stores are ordered before its one arrival
+            if ((p & 31) == 0) tc_mbar_arrive(&a_full[s]);
+            return !*(volatile int*)&fail;
+        };
+        float4 b0[kGhK / 4], b1[kGhK / 4], b2[kGhK / 4];
+        load_chunk(0, b0);
+        load_chunk(1, b1);
+        bool ok = true;
+        for (int64_t kk = 0; kk < nk && ok; kk += 3) {
+            ok = step(kk, b0, b2);
+            if (ok && kk + 1 < nk) ok = step(kk + 1, b1, b0);
+            if (ok && kk + 2 < nk) ok = step(kk + 2, b2, b1);
+        }
+        if (!ok) atomicExch(&fail, 1);
+    } else if (warp == 8) {
+        // ------------------------------------------------------------- issuer
+        if (lane == 0 && nk > 0) {
+            // chunk k's B into ring slot k % kGhBSlots; CTAs walk the K chunks
+            // in an order rotated by their index (the producers do the same)
+            auto issue_b = [&](int64_t k) {
+                const int s = (int)(k % kGhBSlots);
+                const int64_t col = (k % nchunk + blockIdx.x) % nchunk;
+                tc_expect_tx(&b_full[s], bchunk);
+                tc_bulk_g2s(Bring + (size_t)s * kGhB, img + (size_t)col * bchunk, bchunk, &b_full[s]);
+            };
+            for (int64_t k = 0; k < nk && k < kGhBSlots - 1; ++k) issue_b(k);
+            int64_t k = 0;
+            bool ok = true;
+            for (int64_t t = 0; t < my_tiles && ok; ++t) {
+                const int as = (int)(t & 1);
+                if (t >= 2 && !tc_mbar_wait(&acc_free[as], (unsigned)(((t - 2) >> 1) & 1))) {
+                    ok = false;
+                    break;
+                }
+                const unsigned d = tmem + (unsigned)(as * 128);
+                for (int64_t c = 0; c < nchunk; ++c, ++k) {
+                    const int s = (int)(k & 1);
+                    const int bs = (int)(k % kGhBSlots);
+                    if (!tc_mbar_wait(&a_full[s], (unsigned)((k >> 1) & 1)) ||
+                        !tc_mbar_wait(&b_full[bs], (unsigned)((k / kGhBSlots) & 1))) {
+                        ok = false;
+                        break;
+                    }
+                    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                    const unsigned ahi = smem_addr(Aring + (size_t)(2 * s) * kGhA);
+                    const unsigned bb = smem_addr(Bring + (size_t)bs * kGhB);
+                    for (int k8 = 0; k8 < kGhK; k8 += 8) {
+                        const unsigned ka = (unsigned)(k8 >> 2) * lslice, kb = (unsigned)(k8 >> 2) * bslice;
+                        const uint64_t bd = smem_desc(bb + kb, bslice, 128);
+                        mma_tf32_n(d, smem_desc(ahi + ka, lslice, 128), bd, idesc,
+                                   (c > 0 || k8 > 0) ? 1u : 0u);
+                        mma_tf32_n(d, smem_desc(ahi + kGhA + ka, lslice, 128), bd, idesc, 1u);
+                    }
+                    tc_commit(&mma_done[s]);
+                    if (c == nchunk - 1) tc_commit(&acc_full[as]);
+                    // chunk k + 3's B into the slot of chunk k - 1 once that is done
+                    if (k + kGhBSlots - 1 < nk) {
+                        if (k >= 1 && !tc_mbar_wait(&mma_done[s ^ 1], (unsigned)(((k - 1) >> 1) & 1))) {
+                            ok = false;
+                            break;
+                        }
+                        issue_b(k + kGhBSlots - 1);
+                    }
+                    if (*(volatile int*)&fail) {
+                        ok = false;
+                        break;
+                    }
+                }
+            }
+            if (!ok) atomicExch(&fail, 1);
+        }
+    } else {
+        // ----------------------------------------------------------- epilogue
+        const int q = tid - 128;  // edge row of the tile; TMEM lane quarter = warp % 4
+        for (int64_t t = 0; t < my_tiles; ++t) {
+            const int64_t e = ((int64_t)blockIdx.x + t * gridDim.x) * kTcM + q;
+            const bool live = e < E;
+            float r = 0.0f, vx = 0.0f, vy = 0.0f, vz = 0.0f;
+            if (live) {
+                vx = vec[3 * e]; vy = vec[3 * e + 1]; vz = vec[3 * e + 2];
+                r = sqrtf(vx * vx + vy * vy + vz * vz);
+            }
+            float b[kTcNbMax];
+#pragma unroll
+            for (int n = 0; n < kTcNbMax; ++n) b[n] = (live && n < nb) ? bessel_f<float>(n + 1, r, rc, pref) : 0.0f;
+            const int as = (int)(t & 1);
+            // every epilogue thread waits (bounded) and the four warps agree on
+            // the outcome at their named barrier before any of them leaves
+            if (!tc_mbar_wait(&acc_full[as], (unsigned)((t >> 1) & 1))) atomicExch(&fail, 1);
+            asm volatile("bar.sync 2, 128;" ::: "memory");
+            if (*(volatile int*)&fail) break;
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            const unsigned ta = tmem + ((unsigned)((warp & 3) * 32) << 16) + (unsigned)(as * 128);
+            float gb[kTcNbMax];
+#pragma unroll
+            for (int n = 0; n < kTcNbMax; ++n) gb[n] = 0.0f;
+#pragma unroll 1
+            for (int j0 = 0; j0 < hidden; j0 += 8) {  // hidden % 8 == 0
+                float d0[8], d1[8];
+                tmem_ld8(ta + (unsigned)j0, d0);
+                tmem_ld8(ta + (unsigned)(hidden + j0), d1);
+#pragma unroll
+                for (int jj = 0; jj < 8; ++jj) {
+                    const int j = j0 + jj;
+                    float pre = 0.0f;
+#pragma unroll
+                    for (int n = 0; n < kTcNbMax; ++n)
+                        if (n < nb) pre = fmaf(b[n], W1s[n * hidden + j], pre);
+                    const float sg = 1.0f / (1.0f + expf(-pre));
+                    const float gp = live ? (d0[jj] + d1[jj]) * sg * (1.0f + pre * (1.0f - sg)) : 0.0f;
+                    gpS[q * kGhGp + j] = gp;
+#pragma unroll
+                    for (int n = 0; n < kTcNbMax; ++n)
+                        if (n < nb) gb[n] = fmaf(gp, W1s[n * hidden + j], gb[n]);
+                }
+            }
+            asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+            tc_mbar_arrive(&acc_free[as]);
+#pragma unroll
+            for (int n = 0; n < kTcNbMax; ++n)
+                if (n < nb) bS[q * kGhBp + n] = b[n];
+            if (gvec && live) {
+                float dr = 0.0f;
+                if (r > 0.0f) {
+#pragma unroll
+                    for (int n = 0; n < kTcNbMax; ++n)
+                        if (n < nb) {
+                            const float kk = (float)(n + 1) * 3.14159265358979323846f / rc;
+                            dr = fmaf(gb[n], pref * (kk * cosf(kk * r) / r - sinf(kk * r) / (r * r)), dr);
+                        }
+                    dr /= r;
+                }
+                gvec[3 * e] = dr * vx;
+                gvec[3 * e + 1] = dr * vy;
+                gvec[3 * e + 2] = dr * vz;
+            }
+            // grad_W1 partial += b^T gpre over the tile's edges, fixed order
+            asm volatile("bar.sync 2, 128;" ::: "memory");
+            for (int i = q; i < nb * hidden; i += 128) {
+                const int n = i / hidden, j = i % hidden;
+                float v = t == 0 ? 0.0f : part[i];
+                for (int le = 0; le < kTcM; ++le) v = fmaf(bS[le * kGhBp + n], gpS[le * kGhGp + j], v);
+                part[i] = v;
+            }
+            asm volatile("bar.sync 2, 128;" ::: "memory");
+        }
+        if (my_tiles == 0)
+            for (int i = q; i < nb * hidden; i += 128) part[i] = 0.0f;
+    }
+    __syncthreads();
+    if (fail) {
+        if (tid == 0) atomicExch(&cgtp_radial_error, 1);
+        for (int i = 0; i < 1000; ++i) __nanosleep(1000);
+    }
+    if (warp == 0)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(256u)
+                     : "memory");
+}
+
+static bool radial_bwd_tc_eligible(bool f64, int nb, int hidden, int64_t n_out) {
+    return !f64 && nb <= kTcNbMax && hidden % 8 == 0 && hidden <= kTcKMax && n_out % kGhK == 0;
+}
+
+// Workspace: [packed W2^T image, tensor-core path only][grad_W1 partial rows]
+// [grad_W2 partial rows]; every region starts 16-byte aligned.
+static size_t bw_image_bytes(bool f64, int nb, int hidden, int64_t n_out) {
+    return radial_bwd_tc_eligible(f64, nb, hidden, n_out) ? (size_t)n_out * 2 * hidden * 4 : 0;
+}
+
+size_t radial_backward_workspace_bytes(bool f64, int64_t E, int nb, int hidden, int64_t n_out) {
+    const size_t es = f64 ? 8 : 4;
+    const size_t p1 = ((size_t)bw_grid1(E) * nb * hidden * es + 15) / 16 * 16;
+    return bw_image_bytes(f64, nb, hidden, n_out) + p1 +
+           (size_t)bw_splits(E, n_out) * hidden * n_out * es;
+}
+
+cudaError_t launch_radial_backward(bool f64, bool tensor_cores, int64_t E, int nb, double rc,
+                                   int hidden, int64_t n_out, const void* vec, const void* W1,
+                                   const void* W2, const void* gw, void* gvec, void* gW1,
+                                   void* gW2, void* ws, cudaStream_t s) {
     const size_t es = f64 ? 8 : 4;
     const int64_t g1 = bw_grid1(E), sp = bw_splits(E, n_out);
     const int64_t nc = (n_out + kBwW2Cols - 1) / kBwW2Cols;
-    unsigned char* p1 = (unsigned char*)ws;
-    unsigned char* p2 = p1 + (size_t)g1 * nb * hidden * es;
+    unsigned char* img = (unsigned char*)ws;
+    unsigned char* p1 = img + bw_image_bytes(f64, nb, hidden, n_out);
+    unsigned char* p2 = p1 + ((size_t)g1 * nb * hidden * es + 15) / 16 * 16;
+    const bool tc = tensor_cores && radial_bwd_tc_eligible(f64, nb, hidden, n_out);
     const size_t sm1 = es * ((size_t)kBwEdges * nb + kBwEdges + (size_t)kBwEdges * hidden +
                              (size_t)kBwEdges * (kBwCols + 1) + (size_t)hidden * (kBwCols + 1) +
                              (size_t)kBwEdges * nb);
     const size_t sm2 = es * ((size_t)kBwEdges * nb + kBwEdges + (size_t)kBwEdges * kBwW2Rows +
                              (size_t)kBwEdges * kBwW2Cols);
     cudaError_t e;
-    if (gvec || gW1) {
+    if ((gvec || gW1) && tc) {
+        int dev = 0, sms = 0;
+        if ((e = cudaGetDevice(&dev))) return e;
+        if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev))) return e;
+        const int64_t total = (int64_t)hidden * n_out;
+        const unsigned pg =
+            (unsigned)std::max<int64_t>(1, std::min<int64_t>((total + 255) / 256, (int64_t)sms * 8));
+        radial_pack_t_kernel<<<pg, 256, 0, s>>>(hidden, n_out, (const float*)W2, img);
+        if ((e = cudaGetLastError())) return e;
+        if ((e = cudaFuncSetAttribute(radial_bwd_tc_kernel,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGhSmem)))
+            return e;
+        const int64_t tiles = (E + kTcM - 1) / kTcM;
+        const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(tiles, sms));
+        radial_bwd_tc_kernel<<<(unsigned)grid, kGhThreads, kGhSmem, s>>>(
+            E, nb, (float)rc, hidden, n_out, (const float*)vec, (const float*)W1, img,
+            (const float*)gw, (float*)gvec, (float*)p1);
+        if ((e = cudaGetLastError())) return e;
+        if (gW1 && (e = launch_reduce_rows(false, p1, grid, (int64_t)nb * hidden, gW1, s))) return e;
+    } else if (gvec || gW1) {
         if (f64) {
             auto* k = radial_bwd_edge_kernel<double>;
             if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm1)))

@@ -310,15 +310,18 @@ cgtp_status cgtp_radial_workspace(cgtp_dtype dtype, int n_basis, int hidden, int
  * (NULL: not computed), all `dtype`, device, caller-owned, overwritten.  Chain
  * rule: gh = grad_w W2^T, gpre = gh silu'(b W1), grad_W2 = h^T grad_w,
  * grad_W1 = b^T gpre, grad_vec = (gpre W1^T . db/dr) vec / r.  The sums over
- * edges are per-CTA partial rows in `workspace` (device, caller-owned, at
- * least cgtp_radial_backward_workspace() bytes; contents need not be set) added
- * in fixed order, so results are deterministic.  Same size limits as the
- * forward; CUDA cores.  Asynchronous on `stream`; allocates nothing. */
+ * edges are per-CTA partial rows in `workspace` (device, caller-owned, 16-byte
+ * aligned, at least cgtp_radial_backward_workspace() bytes; contents need not
+ * be set) added in fixed order, so results are deterministic.  Same size
+ * limits as the forward.  gh = grad_w W2^T runs on the tensor cores (TF32
+ * split products, fp32 accuracy) when the forward's tensor-core conditions
+ * hold and flags lacks CGTP_RADIAL_CUDA_CORES; grad_W2 on the CUDA cores.
+ * Asynchronous on `stream`; allocates nothing. */
 cgtp_status cgtp_radial_backward(cgtp_dtype dtype, int64_t E, int n_basis, double cutoff,
                                  int hidden, int64_t n_out, const void* vec, const void* W1,
                                  const void* W2, const void* grad_w, void* grad_vec,
                                  void* grad_W1, void* grad_W2, void* workspace,
-                                 size_t workspace_bytes, cgtp_stream stream);
+                                 size_t workspace_bytes, unsigned flags, cgtp_stream stream);
 /* Workspace bytes cgtp_radial_backward needs for these sizes. */
 cgtp_status cgtp_radial_backward_workspace(cgtp_dtype dtype, int64_t E, int n_basis, int hidden,
                                            int64_t n_out, size_t* bytes);

@@ -100,6 +100,8 @@ def test_radial_benchmark_workload_sampled():
 BWD_CASES = [  # E, n_basis, hidden, n_out, dtype
     (1000, 8, 64, 1536, np.float32),
     (1, 8, 64, 256, np.float32),
+    (300, 16, 32, 128, np.float32),
+    (4000, 8, 64, 384, np.float32),
     (333, 5, 40, 200, np.float32),
     (129, 32, 256, 96, np.float32),
     (700, 8, 64, 384, np.float64),
@@ -108,7 +110,8 @@ BWD_CASES = [  # E, n_basis, hidden, n_out, dtype
 
 
 @pytest.mark.parametrize("case", BWD_CASES, ids=lambda c: f"E{c[0]}-nb{c[1]}-h{c[2]}-o{c[3]}-{np.dtype(c[4]).name}")
-def test_radial_backward_matches_oracle(case):
+@pytest.mark.parametrize("cuda_cores", [False, True])
+def test_radial_backward_matches_oracle(case, cuda_cores):
     need_gpu()
     import clebsch_gordan_tensor_gb300 as cg
     E, nb, hidden, n_out, dt = case
@@ -116,7 +119,7 @@ def test_radial_backward_matches_oracle(case):
     vec, W1, W2 = _inputs(rng, E, nb, hidden, n_out, dt)
     vec[0] = 0.0  # zero-length edge: no gradient
     g = rng.standard_normal((E, n_out)).astype(dt)
-    gv, g1, g2 = cg.radial_backward(dev(vec), dev(W1), dev(W2), dev(g), 5.0)
+    gv, g1, g2 = cg.radial_backward(dev(vec), dev(W1), dev(W2), dev(g), 5.0, cuda_cores=cuda_cores)
     rv, r1, r2 = O.radial_backward(vec, W1, W2, g, 5.0)
     assert_close(host(gv), rv, dt, "grad_vec")
     assert_close(host(g1), r1, dt, "grad_W1")
@@ -124,10 +127,10 @@ def test_radial_backward_matches_oracle(case):
     assert np.all(host(gv)[0] == 0.0)
     # subsets, and a second call gives the same bits (ordered reductions)
     _, g1b, g2b = cg.radial_backward(dev(vec), dev(W1), dev(W2), dev(g), 5.0,
-                                     need=(False, True, True))
+                                     need=(False, True, True), cuda_cores=cuda_cores)
     assert torch.equal(g1b, g1) and torch.equal(g2b, g2)
     gvb, n1, n2 = cg.radial_backward(dev(vec), dev(W1), dev(W2), dev(g), 5.0,
-                                     need=(True, False, False))
+                                     need=(True, False, False), cuda_cores=cuda_cores)
     assert n1 is None and n2 is None and torch.equal(gvb, gv)
 
 
