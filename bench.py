@@ -16,7 +16,9 @@ stream (3.2 GB) is far larger than L2, so no flush is needed between steps.
 Other workloads (``--workload``): ``tp`` standalone product, B = 200,000
 samples, 128 channels (fwd+bwd, samples/s); ``conv64`` the fp64 fused conv,
 N = 5,000, 128 channels (forward, edges/s); ``tfn`` the TFN layer on 1000
-molecules (forward, backward, forces and the double backward, edges/s).
+molecules (forward, backward, forces and the double backward, edges/s); ``kv``
+the same molecules at 64 channels, keys and values of an SE(3)-Transformer layer
+from one TFN (fwd+bwd, edges/s).
 
 ``--impl reference`` times the CPU oracle (the reference arm of this build) on
 a bounded subgraph of the same workload.
@@ -378,7 +380,35 @@ def make_tfn(args, cg, W, torch):
                     dict(N=N, E=E, mul=32, paths=plan.n_paths), None, None)
 
 
-WORKLOADS = {"conv": make_conv, "conv64": make_conv64, "tp": make_tp, "tfn": make_tfn}
+def make_kv(args, cg, W, torch):
+    """SE(3)-Transformer keys and values from one TFN with doubled channels:
+    the molecule graph of the TFN workload at 64 channels per irrep."""
+    cfg = W.config4_kv()
+    gr = cfg["graph"]
+    N, E = gr.N, gr.E
+    plan = cg.Plan(*cfg["irreps"])
+    G = cg.Graph.from_numpy(gr)
+    x, vec, w, g = (torch.from_numpy(cfg[k]).cuda() for k in ("x", "vec", "w", "g"))
+    y = torch.empty(E, plan.dim_in2, device="cuda")
+    out = torch.empty(N, plan.dim_out, device="cuda")
+    gx, gy, gw = torch.empty_like(x), torch.empty_like(y), torch.empty_like(w)
+    gvec = torch.empty_like(vec)
+    plan.compile()
+    kernels = [
+        ("sh_fwd", lambda: cg.sh_forward(vec, 3, out=y)),
+        ("conv_fwd", lambda: plan.conv_forward(G, x, y, w, 1.0, out=out)),
+        ("conv_bwd", lambda: plan.conv_backward(G, x, y, w, 1.0, g, out=(gx, gy, gw))),
+        ("sh_bwd", lambda: cg.sh_backward(vec, gy, 3, out=gvec)),
+    ]
+    desc = ("fused keys/values (one TFN, doubled channels): 1000 molecules of 9-29 atoms, "
+            "fully connected, 64x(0e,1o,2e,3o) (x) Y(l<=3) -> 64x(0e,1o,2e,3o), 23 paths, fp32")
+    return Workload("kv", desc, E, "edges/s", "f32", kernels,
+                    conv_counts(Dims(plan), N, E, 4), ["sh_fwd", "conv_fwd"],
+                    dict(N=N, E=E, mul=64, paths=plan.n_paths), None, None)
+
+
+WORKLOADS = {"conv": make_conv, "conv64": make_conv64, "tp": make_tp, "tfn": make_tfn,
+             "kv": make_kv}
 
 
 # ------------------------------------------------------------ GPU arm

@@ -153,3 +153,12 @@ def test_config4_chain_sampled():
                                 edges=edges)
     assert_close(res["d_x"][nodes], dx[nodes], np.float32, "dL/dx rows")
     assert_close(res["d_w"][edges], dw[edges], np.float32, "dL/dw rows")
+
+
+def test_config4_fused_kv_sampled():
+    """Keys and values from one TFN (the config-4 graph at 64 channels): forward
+    and gradient at full size, sampled receivers / senders / edges."""
+    need_gpu()
+    cfg = W.config4_kv()
+    conv_weights(cfg)  # the workload carries its own w
+    _conv_sampled(cfg, np.float32, True)

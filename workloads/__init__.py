@@ -33,6 +33,8 @@ CFG2 = ("64x0e+64x1o+64x2e", "0e+1o+2e+3o", "64x0e+64x1o+64x1e+64x2o+64x2e+64x3o
 CFG3 = ("128x0e+128x1o+128x2e", "0e+1o+2e+3o",
         "128x0e+128x1o+128x1e+128x2o+128x2e+128x3o+128x3e")
 CFG4 = ("32x0e+32x1o+32x2e+32x3o", "0e+1o+2e+3o", "32x0e+32x1o+32x2e+32x3o")
+# the config-4 layer with keys and values computed by one TFN: channels doubled
+CFG4_KV = ("64x0e+64x1o+64x2e+64x3o", "0e+1o+2e+3o", "64x0e+64x1o+64x2e+64x3o")
 
 
 def irreps_dim(s: str) -> int:
@@ -195,6 +197,21 @@ def conv_cloud(seed: int, irreps, N: int, n_paths: int, dtype) -> dict:
     return dict(irreps=irreps, graph=g, pos=pos, box=L, x=x, vec=g.vec.astype(dtype), W1=W1,
                 W2=W2, cutoff=5.0, lmax=3, scale=float(N) / float(max(g.E, 1)),
                 dtype=np.dtype(dtype))
+
+
+def config4_kv(n_mol: int = 1000) -> dict:
+    """The config-4 molecules (same seed, same graph) with 64 channels per
+    irrep: the keys and values of an SE(3)-Transformer attention layer from one
+    TFN with doubled channels instead of two.  Draws, in order: molecules; x
+    [N, 1024] ~ N(0,1); w [E, 23 * 64] ~ N(0,1)/sqrt(23); g [N, 1024] ~ N(0,1)
+    (output cotangent)."""
+    rng = np.random.default_rng(4)
+    pos, g = molecules(rng, n_mol)
+    x = normal(rng, (g.N, 1024), np.float32)
+    w = normal(rng, (g.E, 23 * 64), np.float32) * np.float32(1.0 / np.sqrt(23.0))
+    go = normal(rng, (g.N, 1024), np.float32)
+    return dict(irreps=CFG4_KV, graph=g, pos=pos, x=x, vec=g.vec.astype(np.float32), w=w, g=go,
+                lmax=3, scale=1.0, dtype=np.dtype(np.float32))
 
 
 def config2(N: int = 10_000) -> dict:
