@@ -74,6 +74,7 @@ def _load():
             lib.oracle_sh.argtypes = [i32, i64, pd, pd]
             lib.oracle_sh_vjp.argtypes = [i32, i64, pd, pd, pd]
             lib.oracle_sh_jvp.argtypes = [i32, i64, pd, pd, pd]
+            lib.oracle_sh_hvp.argtypes = [i32, i64, pd, pd, pd, pd]
             lib.oracle_tp_forward.argtypes = [i32, P(_Path), i64, i64, i64, i64, i64, i64,
                                               pd, pd, pd, pd]
             lib.oracle_tp_backward.argtypes = [i32, P(_Path), i64, i64, i64, i64, i64, i64,
@@ -85,7 +86,7 @@ def _load():
                                                  i64, i64, i64, pd, pd, pd, d, pd, pd, pd, pd,
                                                  P(ctypes.c_uint8), P(ctypes.c_uint8)]
             lib.oracle_edge_forces.argtypes = [i64, i64, pi32, pi32, pd, pd]
-            for f in ("oracle_cg_real", "oracle_sh", "oracle_sh_vjp", "oracle_sh_jvp",
+            for f in ("oracle_cg_real", "oracle_sh", "oracle_sh_vjp", "oracle_sh_jvp", "oracle_sh_hvp",
                       "oracle_tp_forward", "oracle_tp_backward", "oracle_conv_forward",
                       "oracle_conv_backward", "oracle_edge_forces"):
                 getattr(lib, f).restype = ctypes.c_int
@@ -209,6 +210,16 @@ def sh_jvp(lmax: int, vec, tangent_vec) -> np.ndarray:
     v, t = _f64(vec).reshape(-1, 3), _f64(tangent_vec).reshape(-1, 3)
     out = np.empty((v.shape[0], (lmax + 1) ** 2))
     _load().oracle_sh_jvp(lmax, v.shape[0], _p(v), _p(t), _p(out))
+    return out
+
+
+def sh_hvp(lmax: int, vec, grad_y, tangent_vec) -> np.ndarray:
+    """Second derivative of grad_y . Y(vec) in vec, applied to tangent_vec:
+    the derivative of ``sh_vjp`` along tangent_vec with grad_y held fixed."""
+    v, g = _f64(vec).reshape(-1, 3), _f64(grad_y)
+    t = _f64(tangent_vec).reshape(-1, 3)
+    out = np.empty_like(v)
+    _load().oracle_sh_hvp(lmax, v.shape[0], _p(v), _p(g), _p(t), _p(out))
     return out
 
 

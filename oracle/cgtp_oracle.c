@@ -297,6 +297,86 @@ int oracle_sh_jvp(int lmax, int64_t n, const double *vec, const double *tangent_
     return 0;
 }
 
+/* Second derivatives of the same polynomials in u: d2/dz2 Q_lm = Q_l,m+2,
+ * d2/dx2 (x+iy)^m = m(m-1)(x+iy)^(m-2), d2/dxdy = i m(m-1)(x+iy)^(m-2),
+ * d2/dy2 = -m(m-1)(x+iy)^(m-2), d2/dxdz = dQ m (x+iy)^(m-1), d2/dydz =
+ * dQ i m (x+iy)^(m-1).  h[i][k] for k = xx, xy, xz, yy, yz, zz; the real
+ * part for m >= 0, the imaginary part for m < 0.
+ */
+static void sh_unit_hess(int lmax, double x, double y, double z, double (*h)[6]) {
+    for (int l = 0; l <= lmax; ++l) {
+        for (int m = -l; m <= l; ++m) {
+            int am = abs(m), i = l * l + (m + l);
+            double N = sh_norm(l, am);
+            double Q = legendre_deriv(l, am, z);
+            double dQ = (am + 1 <= l) ? legendre_deriv(l, am + 1, z) : 0.0;
+            double d2Q = (am + 2 <= l) ? legendre_deriv(l, am + 2, z) : 0.0;
+            double re, im, re1 = 0, im1 = 0, re2 = 0, im2 = 0;
+            xy_power(am, x, y, &re, &im);
+            if (am >= 1) xy_power(am - 1, x, y, &re1, &im1);
+            if (am >= 2) xy_power(am - 2, x, y, &re2, &im2);
+            double complex w0 = re + I * im;
+            double complex w1 = (double)am * (re1 + I * im1);
+            double complex w2 = (double)am * (double)(am - 1) * (re2 + I * im2);
+            double complex d[6] = {Q * w2, Q * I * w2, dQ * w1, -Q * w2, dQ * I * w1, d2Q * w0};
+            for (int k = 0; k < 6; ++k) h[i][k] = N * ((m >= 0) ? creal(d[k]) : cimag(d[k]));
+        }
+    }
+}
+
+/* Hessian-vector product of s(r) = grad_y . Y(r/|r|):
+ *   out[e] = (d^2 s / dr^2) tangent_vec[e].
+ * With f = grad_u (grad_y . P)(u), F its second derivatives in u, rho = |r|,
+ * u = r/rho and Pi = I - u u^T (chain rule through u = r/|r|, differentiated
+ * twice):
+ *   d^2 s/dr_j dr_k = [ (Pi F Pi)_jk - f_j u_k - f_k u_j - (f.u) delta_jk
+ *                       + 3 (f.u) u_j u_k ] / rho^2.
+ * It is the derivative of oracle_sh_vjp along tangent_vec (grad_y held fixed).
+ */
+int oracle_sh_hvp(int lmax, int64_t n, const double *vec, const double *grad_y,
+                  const double *tangent_vec, double *out) {
+    if (lmax < 0 || lmax > ORACLE_LMAX) return -1;
+    int dim = (lmax + 1) * (lmax + 1);
+    double gx[64], gy[64], gz[64], h[64][6];
+    static const int sym[3][3] = {{0, 1, 2}, {1, 3, 4}, {2, 4, 5}};
+    for (int64_t e = 0; e < n; ++e) {
+        const double *v = vec + 3 * e, *g = grad_y + e * dim, *t = tangent_vec + 3 * e;
+        double rho = sqrt(v[0] * v[0] + v[1] * v[1] + v[2] * v[2]);
+        double u[3] = {v[0] / rho, v[1] / rho, v[2] / rho};
+        sh_unit_grad(lmax, u[0], u[1], u[2], gx, gy, gz);
+        sh_unit_hess(lmax, u[0], u[1], u[2], h);
+        double f[3] = {0, 0, 0}, F[3][3] = {{0}};
+        for (int i = 0; i < dim; ++i) {
+            f[0] += g[i] * gx[i];
+            f[1] += g[i] * gy[i];
+            f[2] += g[i] * gz[i];
+            for (int a = 0; a < 3; ++a)
+                for (int b = 0; b < 3; ++b) F[a][b] += g[i] * h[i][sym[a][b]];
+        }
+        double Pi[3][3], PFP[3][3];
+        for (int a = 0; a < 3; ++a)
+            for (int b = 0; b < 3; ++b) Pi[a][b] = (a == b ? 1.0 : 0.0) - u[a] * u[b];
+        for (int a = 0; a < 3; ++a)
+            for (int b = 0; b < 3; ++b) {
+                double s = 0;
+                for (int c = 0; c < 3; ++c)
+                    for (int d = 0; d < 3; ++d) s += Pi[a][c] * F[c][d] * Pi[d][b];
+                PFP[a][b] = s;
+            }
+        double fu = f[0] * u[0] + f[1] * u[1] + f[2] * u[2];
+        for (int j = 0; j < 3; ++j) {
+            double s = 0;
+            for (int k = 0; k < 3; ++k) {
+                double H = PFP[j][k] - f[j] * u[k] - f[k] * u[j] - (j == k ? fu : 0.0) +
+                           3.0 * fu * u[j] * u[k];
+                s += H * t[k];
+            }
+            out[3 * e + j] = s / (rho * rho);
+        }
+    }
+    return 0;
+}
+
 /* ------------------------------------------------------ tensor product -- */
 
 /* One 'uvu' path: out block (l3) channel u gets

@@ -92,3 +92,43 @@ def test_vjp_jvp_finite_differences(lmax):
     assert np.abs((vjp * t).sum(1) - (gy * jvp).sum(1)).max() < 1e-12
     # gradient is orthogonal to the radial direction (Y depends on r/|r| only)
     assert np.abs((vjp * v).sum(1)).max() < 1e-11
+
+
+@pytest.mark.parametrize("lmax", [0, 1, 2, 3, 6])
+def test_hvp_finite_differences_symmetry_homogeneity(lmax):
+    """Second derivatives of s(r) = gy . Y(r): central differences of the
+    (separately pinned) vector-Jacobian product, symmetry of the Hessian, and
+    Euler's identity for a function of degree 0 in r, H r = -grad s."""
+    rng = np.random.default_rng(11 + lmax)
+    v = rng.standard_normal((10, 3)) * rng.uniform(0.5, 3.0, (10, 1))
+    gy = rng.standard_normal((10, (lmax + 1) ** 2))
+    a, b = rng.standard_normal((10, 3)), rng.standard_normal((10, 3))
+    h = 1e-5
+    fd = (O.sh_vjp(lmax, v + h * a, gy) - O.sh_vjp(lmax, v - h * a, gy)) / (2 * h)
+    Ha = O.sh_hvp(lmax, v, gy, a)
+    scale = max(1.0, np.abs(fd).max())
+    assert np.abs(Ha - fd).max() < 1e-7 * scale
+    Hb = O.sh_hvp(lmax, v, gy, b)
+    assert np.abs((Ha * b).sum(1) - (Hb * a).sum(1)).max() < 1e-11 * scale
+    Hv = O.sh_hvp(lmax, v, gy, v)
+    assert np.abs(Hv + O.sh_vjp(lmax, v, gy)).max() < 1e-11 * scale
+    # degree -2 in |r|: H(2 r) = H(r) / 4
+    assert np.abs(O.sh_hvp(lmax, 2 * v, gy, a) - Ha / 4).max() < 1e-12 * scale
+
+
+def test_hvp_closed_form_l1():
+    """l = 1: gy . Y(r) = sqrt(3) (c . r) / |r| with c = (gy_x, gy_y, gy_z) =
+    (gy[3], gy[1], gy[2]); its Hessian is
+    [-(c r^T + r c^T) - (c.r) I + 3 (c.r) r r^T / |r|^2] / |r|^3."""
+    rng = np.random.default_rng(5)
+    v = rng.standard_normal((8, 3))
+    gy = rng.standard_normal((8, 4))
+    t = rng.standard_normal((8, 3))
+    got = O.sh_hvp(1, v, gy, t)
+    for e in range(8):
+        r, c = v[e], math.sqrt(3) * np.array([gy[e, 3], gy[e, 1], gy[e, 2]])
+        rho = np.linalg.norm(r)
+        cr = c @ r
+        H = (-(np.outer(c, r) + np.outer(r, c)) - cr * np.eye(3)
+             + 3 * cr * np.outer(r, r) / rho ** 2) / rho ** 3
+        assert np.abs(got[e] - H @ t[e]).max() < 1e-13

@@ -225,6 +225,37 @@ def test_forces_chain_finite_differences():
         assert abs(fd + (F * t).sum()) < 1e-6 * max(1.0, abs(fd))
 
 
+def test_force_loss_position_gradient_finite_differences():
+    """L(pos) = sum gF * F(pos) for the forces of the chain above.  Its gradient
+    in the positions goes through the second derivatives of the SH only (the
+    gradient of the energy in Y does not depend on Y): with q_e = gF[send] -
+    gF[recv], dL/dr_e = H_e q_e where H_e is the Hessian in r_e of
+    gY_e . Y(r_e), and dL/dpos = -edge_forces(dL/dr)."""
+    rng = np.random.default_rng(8)
+    prob = O.make_problem("2x0e+2x1o+1x2e", "0e+1o+2e+3o", "2x0e+2x1o+1x2e")
+    pos, gr = W.molecules(rng, 3, 4, 6)
+    x = rng.standard_normal((gr.N, prob.dim1))
+    w = rng.standard_normal((gr.E, prob.wdim))
+    c = rng.standard_normal((gr.N, prob.dimo))
+    gF = rng.standard_normal((gr.N, 3))
+
+    def forces(p):
+        vec = p[gr.receiver] - p[gr.sender]
+        gy = O.conv_backward(prob, gr.rowptr, gr.sender, x, O.sh(3, vec), w, 1.0, c)[1]
+        return O.edge_forces(gr.rowptr, gr.sender, O.sh_vjp(3, vec, gy)), gy
+
+    F, gy = forces(pos)
+    vec = pos[gr.receiver] - pos[gr.sender]
+    q = gF[gr.sender] - gF[gr.receiver]
+    dLdpos = -O.edge_forces(gr.rowptr, gr.sender, O.sh_hvp(3, vec, gy, q))
+    assert np.abs(dLdpos.sum(0)).max() < 1e-10  # translation invariance
+    h = 1e-5
+    for _ in range(3):
+        t = rng.standard_normal(pos.shape)
+        fd = ((gF * forces(pos + h * t)[0]).sum() - (gF * forces(pos - h * t)[0]).sum()) / (2 * h)
+        assert abs(fd - (dLdpos * t).sum()) < 1e-6 * max(1.0, abs(fd))
+
+
 def test_empty_inputs():
     prob = O.make_problem(*ODD)
     out = O.tp_forward(prob, np.zeros((0, prob.dim1)), np.zeros((0, 16)), np.zeros((0, prob.wdim)))
