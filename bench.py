@@ -356,6 +356,7 @@ def make_tfn(args, cg, W, torch):
     dEdr, q = torch.empty_like(vec), torch.empty_like(vec)
     F = torch.empty(N, 3, device="cuda")
     ggy = torch.empty_like(y)
+    dLdr, FL = torch.empty_like(vec), torch.empty(N, 3, device="cuda")
     plan.compile()
     kernels = [
         ("sh_fwd", lambda: cg.sh_forward(vec, 3, out=y)),
@@ -367,15 +368,19 @@ def make_tfn(args, cg, W, torch):
         ("sh_jvp", lambda: cg.sh_jvp(vec, q, 3, out=ggy)),
         ("conv_dbl", lambda: plan.conv_double_backward(G, x, y, w, 1.0, c, None, ggy, None,
                                                        need=(True, False, True, False))),
+        ("sh_hvp", lambda: cg.sh_hvp(vec, gy, q, 3, out=dLdr)),
+        ("forces_pos", lambda: cg.edge_forces(G, dLdr, out=FL)),
     ]
     prob = Dims(plan)
     cc = conv_counts(prob, N, E, 4)
     counts = {"sh_fwd": cc["sh_fwd"], "conv_fwd": cc["conv_fwd"], "conv_bwd": cc["conv_bwd"],
               "sh_bwd": cc["sh_bwd"], "forces": (E * 12 + N * 12, None),
               "forces_adj": (E * 12 + N * 12, None), "sh_jvp": (E * (6 + 16) * 4, None),
-              "conv_dbl": (cc["conv_bwd"][0] - E * prob.dim2 * 4, cc["conv_bwd"][1] * 2 // 3)}
+              "conv_dbl": (cc["conv_bwd"][0] - E * prob.dim2 * 4, cc["conv_bwd"][1] * 2 // 3),
+              "sh_hvp": (E * (3 + 16 + 3 + 3) * 4, None), "forces_pos": (E * 12 + N * 12, None)}
     desc = ("TFN layer: 1000 molecules of 9-29 atoms, fully connected, 32x(0e,1o,2e,3o) (x) "
-            "Y(l<=3) -> 32x(0e,1o,2e,3o), 23 paths, fp32: fwd, bwd, forces, double backward")
+            "Y(l<=3) -> 32x(0e,1o,2e,3o), 23 paths, fp32: fwd, bwd, forces, double backward, "
+            "force-loss gradient in the positions")
     return Workload("tfn", desc, E, "edges/s", "f32", kernels, counts, ["sh_fwd", "conv_fwd"],
                     dict(N=N, E=E, mul=32, paths=plan.n_paths), None, None)
 

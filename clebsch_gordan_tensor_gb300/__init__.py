@@ -73,6 +73,7 @@ def lib() -> ctypes.CDLL:
                 "cgtp_sh_forward": [i32, i32, i64, vp, vp, vp],
                 "cgtp_sh_backward": [i32, i32, i64, vp, vp, vp, vp],
                 "cgtp_sh_jvp": [i32, i32, i64, vp, vp, vp, vp],
+                "cgtp_sh_hvp": [i32, i32, i64, vp, vp, vp, vp, vp],
                 "cgtp_edge_forces": [i32, i64, i64, vp, vp, vp, vp, vp, vp],
                 "cgtp_edge_forces_adjoint": [i32, i64, i64, vp, vp, vp, vp, vp],
                 "cgtp_last_cuda_error": [P(i32)],
@@ -381,6 +382,20 @@ def sh_jvp(vec, tangent_vec, lmax: int, out=None):
         out = torch.empty(E, (lmax + 1) ** 2, dtype=vec.dtype, device=vec.device)
     _check(lib().cgtp_sh_jvp(lmax, _dt(vec.dtype), E, _ptr(vec), _ptr(tangent_vec), _ptr(out),
                              _stream()))
+    return out
+
+
+def sh_hvp(vec, grad_y, tangent_vec, lmax: int, out=None):
+    """Hessian of grad_y . Y(vec) in vec applied to tangent_vec, per edge."""
+    E = vec.shape[0]
+    _need(vec, "vec", vec.dtype, (E, 3))
+    _need(grad_y, "grad_y", vec.dtype, (E, (lmax + 1) ** 2))
+    _need(tangent_vec, "tangent_vec", vec.dtype, (E, 3))
+    if out is None:
+        out = torch.empty_like(vec)
+    _need(out, "out", vec.dtype, (E, 3))
+    _check(lib().cgtp_sh_hvp(lmax, _dt(vec.dtype), E, _ptr(vec), _ptr(grad_y), _ptr(tangent_vec),
+                             _ptr(out), _stream()))
     return out
 
 

@@ -637,6 +637,21 @@ cgtp_status cgtp_sh_jvp(int lmax, cgtp_dtype dtype, int64_t E, const void* vec,
     GUARD_END
 }
 
+cgtp_status cgtp_sh_hvp(int lmax, cgtp_dtype dtype, int64_t E, const void* vec,
+                        const void* grad_y, const void* tangent_vec, void* out,
+                        cgtp_stream stream) {
+    GUARD_BEGIN
+    cgtp_status st = sh_check(lmax, dtype, E);
+    if (st != CGTP_OK || E == 0) return st;
+    if (!vec || !grad_y || !tangent_vec || !out) return fail(CGTP_E_ARG, "NULL tensor");
+    cudaError_t e =
+        launch_sh_hvp(lmax, dtype == CGTP_F64, E, vec, grad_y, tangent_vec, out, S(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "sh_hvp");
+    count_launch();
+    return CGTP_OK;
+    GUARD_END
+}
+
 static cgtp_status radial_check(cgtp_dtype dt, int64_t E, int nb, double cutoff, int hidden,
                                 int64_t n_out) {
     if (dt != CGTP_F32 && dt != CGTP_F64) return fail(CGTP_E_ARG, "bad dtype");

@@ -37,6 +37,8 @@ cudaError_t launch_sh_backward(int lmax, bool f64, int64_t E, const void* vec, c
                                void* gvec, cudaStream_t s);
 cudaError_t launch_sh_jvp(int lmax, bool f64, int64_t E, const void* vec, const void* tvec,
                           void* ty, cudaStream_t s);
+cudaError_t launch_sh_hvp(int lmax, bool f64, int64_t E, const void* vec, const void* gy,
+                          const void* tvec, void* out, cudaStream_t s);
 cudaError_t launch_edge_forces(bool f64, int64_t N, const int32_t* rowptr,
                                const int32_t* s_rowptr, const int32_t* s_perm, const void* dEdr,
                                void* F, cudaStream_t s);

@@ -14,6 +14,11 @@
 // and the gradient on the sphere uses dQ_l^m/dz = Q_l^(m+1), dC_m/dx = m C_{m-1},
 // dC_m/dy = -m S_{m-1}, dS_m/dx = m S_{m-1}, dS_m/dy = m C_{m-1}, projected by
 // (I - u u^T) / |r|.  One thread per edge.
+//
+// Second derivatives (the gradient of a force loss in the positions) are taken
+// in forward mode over the backward: the backward's arithmetic evaluated on
+// dual numbers a + b eps (eps^2 = 0) at r + eps t gives, in its eps part, the
+// derivative of J(r)^T g along t, i.e. the Hessian of g . Y(r) applied to t.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -21,6 +26,47 @@
 #include "internal.hpp"
 
 namespace cgtp {
+
+// Dual number a + b eps with eps^2 = 0: b carries the directional derivative.
+template <typename T>
+struct Dual {
+    T v, d;
+    __device__ __forceinline__ Dual() {}
+    __device__ __forceinline__ Dual(T a) : v(a), d((T)0) {}
+    __device__ __forceinline__ Dual(T a, T b) : v(a), d(b) {}
+    __device__ __forceinline__ Dual& operator+=(const Dual& o) {
+        v += o.v;
+        d += o.d;
+        return *this;
+    }
+    __device__ __forceinline__ Dual& operator*=(const Dual& o) {
+        d = d * o.v + v * o.d;
+        v *= o.v;
+        return *this;
+    }
+};
+template <typename T>
+__device__ __forceinline__ Dual<T> operator+(Dual<T> a, Dual<T> b) { return {a.v + b.v, a.d + b.d}; }
+template <typename T>
+__device__ __forceinline__ Dual<T> operator-(Dual<T> a, Dual<T> b) { return {a.v - b.v, a.d - b.d}; }
+template <typename T>
+__device__ __forceinline__ Dual<T> operator-(Dual<T> a) { return {-a.v, -a.d}; }
+template <typename T>
+__device__ __forceinline__ Dual<T> operator*(Dual<T> a, Dual<T> b) {
+    return {a.v * b.v, a.d * b.v + a.v * b.d};
+}
+template <typename T>
+__device__ __forceinline__ Dual<T> operator*(T a, Dual<T> b) { return {a * b.v, a * b.d}; }
+template <typename T>
+__device__ __forceinline__ Dual<T> operator/(Dual<T> a, Dual<T> b) {
+    const T inv = (T)1 / b.v, q = a.v * inv;
+    return {q, (a.d - q * b.d) * inv};
+}
+template <typename T>
+__device__ __forceinline__ Dual<T> dual_sqrt(Dual<T> a) {
+    const T s = sqrt(a.v);
+    return {s, a.d / (s + s)};
+}
 
 template <typename T>
 __device__ __forceinline__ T sh_norm(int l, int m) {
@@ -138,6 +184,38 @@ __global__ void __launch_bounds__(128) sh_deriv_kernel(int64_t E, const T* __res
     }
 }
 
+// HVP: out[e] = d/deps [J(vec[e] + eps t[e])^T g[e]] = H_e t[e], H_e the
+// Hessian of g[e] . Y(r) at r = vec[e].
+template <int L, typename T>
+__global__ void __launch_bounds__(128) sh_hvp_kernel(int64_t E, const T* __restrict__ vec,
+                                                      const T* __restrict__ gin,
+                                                      const T* __restrict__ tvec,
+                                                      T* __restrict__ out) {
+    using D = Dual<T>;
+    constexpr int D2 = (L + 1) * (L + 1);
+    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < E;
+         e += (int64_t)gridDim.x * blockDim.x) {
+        const D x(vec[3 * e], tvec[3 * e]), y(vec[3 * e + 1], tvec[3 * e + 1]),
+            z(vec[3 * e + 2], tvec[3 * e + 2]);
+        const D inv = D((T)1) / dual_sqrt(x * x + y * y + z * z);
+        const D ux = x * inv, uy = y * inv, uz = z * inv;
+        D Y[D2], gx[D2], gy[D2], gz[D2];
+        sh_unit<L, D, true>(ux, uy, uz, Y, gx, gy, gz);
+        D ax((T)0), ay((T)0), az((T)0);
+#pragma unroll
+        for (int i = 0; i < D2; ++i) {
+            const T g = gin[e * D2 + i];
+            ax += g * gx[i];
+            ay += g * gy[i];
+            az += g * gz[i];
+        }
+        const D r = ax * ux + ay * uy + az * uz;
+        out[3 * e] = ((ax - r * ux) * inv).d;
+        out[3 * e + 1] = ((ay - r * uy) * inv).d;
+        out[3 * e + 2] = ((az - r * uz) * inv).d;
+    }
+}
+
 static dim3 grid_for(int64_t E) {
     int64_t b = (E + 127) / 128;
     if (b > (1 << 20)) b = 1 << 20;
@@ -176,6 +254,23 @@ static cudaError_t sh_der_t(int lmax, int64_t E, const T* v, const T* in, T* out
     return cudaGetLastError();
 }
 
+template <typename T>
+static cudaError_t sh_hvp_t(int lmax, int64_t E, const T* v, const T* g, const T* t, T* out,
+                            cudaStream_t s) {
+    const dim3 gr = grid_for(E);
+    switch (lmax) {
+        case 0: sh_hvp_kernel<0, T><<<gr, 128, 0, s>>>(E, v, g, t, out); break;
+        case 1: sh_hvp_kernel<1, T><<<gr, 128, 0, s>>>(E, v, g, t, out); break;
+        case 2: sh_hvp_kernel<2, T><<<gr, 128, 0, s>>>(E, v, g, t, out); break;
+        case 3: sh_hvp_kernel<3, T><<<gr, 128, 0, s>>>(E, v, g, t, out); break;
+        case 4: sh_hvp_kernel<4, T><<<gr, 128, 0, s>>>(E, v, g, t, out); break;
+        case 5: sh_hvp_kernel<5, T><<<gr, 128, 0, s>>>(E, v, g, t, out); break;
+        case 6: sh_hvp_kernel<6, T><<<gr, 128, 0, s>>>(E, v, g, t, out); break;
+        default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
 cudaError_t launch_sh_forward(int lmax, bool f64, int64_t E, const void* vec, void* y,
                               cudaStream_t s) {
     if (f64) return sh_fwd_t<double>(lmax, E, (const double*)vec, (double*)y, s);
@@ -196,6 +291,15 @@ cudaError_t launch_sh_jvp(int lmax, bool f64, int64_t E, const void* vec, const 
         return sh_der_t<double, false>(lmax, E, (const double*)vec, (const double*)tvec,
                                        (double*)ty, s);
     return sh_der_t<float, false>(lmax, E, (const float*)vec, (const float*)tvec, (float*)ty, s);
+}
+
+cudaError_t launch_sh_hvp(int lmax, bool f64, int64_t E, const void* vec, const void* gy,
+                          const void* tvec, void* out, cudaStream_t s) {
+    if (f64)
+        return sh_hvp_t<double>(lmax, E, (const double*)vec, (const double*)gy,
+                                (const double*)tvec, (double*)out, s);
+    return sh_hvp_t<float>(lmax, E, (const float*)vec, (const float*)gy, (const float*)tvec,
+                           (float*)out, s);
 }
 
 }  // namespace cgtp

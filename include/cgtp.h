@@ -257,6 +257,18 @@ cgtp_status cgtp_sh_backward(int lmax, cgtp_dtype dtype, int64_t E, const void* 
 cgtp_status cgtp_sh_jvp(int lmax, cgtp_dtype dtype, int64_t E, const void* vec,
                         const void* tangent_vec, void* tangent_y, cgtp_stream stream);
 
+/* out[e] = H_e tangent_vec[e], H_e the Hessian in r of grad_y[e] . Y(r) at
+ * r = vec[e]: the derivative of cgtp_sh_backward along tangent_vec with grad_y
+ * held fixed.  With grad_y = dE/dY and tangent_vec = cgtp_edge_forces_adjoint
+ * of a force cotangent gF, out is dL/dr for L = sum gF . forces, and
+ * cgtp_edge_forces(out) = -dL/dpos (the position part of the "higher partial
+ * derivatives required to predict interatomic forces", abstract of arXiv
+ * 2501.13986; the gradient of dE/dY in Y is zero for a product linear in Y).
+ * vec, tangent_vec, out [E, 3]; grad_y [E, (lmax+1)^2]; 0 <= lmax <= 6. */
+cgtp_status cgtp_sh_hvp(int lmax, cgtp_dtype dtype, int64_t E, const void* vec,
+                        const void* grad_y, const void* tangent_vec, void* out,
+                        cgtp_stream stream);
+
 /* ---------------------------------------------------------- forces ------ */
 /* Interatomic forces from per-edge energy gradients ("higher partial
  * derivatives required to predict interatomic forces", abstract of arXiv

@@ -126,6 +126,8 @@ def test_spherical_harmonics(lmax, dt):
     assert_close(host(cg.sh_forward(dev(v), lmax)), O.sh(lmax, v), dt, "sh")
     assert_close(host(cg.sh_backward(dev(v), dev(gy), lmax)), O.sh_vjp(lmax, v, gy), dt, "vjp")
     assert_close(host(cg.sh_jvp(dev(v), dev(t), lmax)), O.sh_jvp(lmax, v, t), dt, "jvp")
+    assert_close(host(cg.sh_hvp(dev(v), dev(gy), dev(t), lmax)), O.sh_hvp(lmax, v, gy, t), dt,
+                 "hvp")
 
 
 @pytest.mark.parametrize("dt", [np.float32, np.float64])
@@ -150,7 +152,8 @@ def test_edge_forces_and_adjoint(dt):
 
 def tfn_chain_gpu(cg, plan, G, x, vec, w, c, gF, lmax=3):
     """Config-4 step: energy E = sum c * conv(x, Y(vec), w); gradients dE/dx,
-    dE/dw, dE/dvec; forces; force loss L = sum gF * F; dL/dx, dL/dw."""
+    dE/dw, dE/dvec; forces; force loss L = sum gF * F; dL/dx, dL/dw, and
+    FL = edge_forces(dL/dr) = -dL/dpos."""
     y = cg.sh_forward(vec, lmax)
     out = plan.conv_forward(G, x, y, w, 1.0)
     gx, gy, gw = plan.conv_backward(G, x, y, w, 1.0, c)
@@ -160,7 +163,9 @@ def tfn_chain_gpu(cg, plan, G, x, vec, w, c, gF, lmax=3):
     ggy = cg.sh_jvp(vec, q, lmax)
     d_x, _, d_w, _ = plan.conv_double_backward(G, x, y, w, 1.0, c, None, ggy, None,
                                                need=(True, False, True, False))
-    return dict(y=y, out=out, gx=gx, gy=gy, gw=gw, dEdr=dEdr, F=F, ggy=ggy, d_x=d_x, d_w=d_w)
+    FL = cg.edge_forces(G, cg.sh_hvp(vec, gy, q, lmax))
+    return dict(y=y, out=out, gx=gx, gy=gy, gw=gw, dEdr=dEdr, F=F, ggy=ggy, d_x=d_x, d_w=d_w,
+                FL=FL)
 
 
 def tfn_chain_oracle(prob, gr, x, vec, w, c, gF, lmax=3, nodes=None, edges=None):
@@ -175,6 +180,7 @@ def tfn_chain_oracle(prob, gr, x, vec, w, c, gF, lmax=3, nodes=None, edges=None)
     res["ggy"] = O.sh_jvp(lmax, vec, q)
     d = O.conv_double_backward(prob, gr.rowptr, gr.sender, x, y, w, 1.0, c, None, res["ggy"], None)
     res.update(d_x=d[0], d_w=d[2])
+    res["FL"] = O.edge_forces(gr.rowptr, gr.sender, O.sh_hvp(lmax, vec, gy, q))
     return res
 
 
@@ -189,7 +195,7 @@ def test_tfn_force_chain_small():
     gpu = tfn_chain_gpu(cg, plan, G, dev(cfg["x"]), dev(cfg["vec"]), dev(cfg["w"]),
                         dev(cfg["c"]), dev(cfg["gF"]))
     ref = tfn_chain_oracle(prob, gr, cfg["x"], cfg["vec"], cfg["w"], cfg["c"], cfg["gF"])
-    for k in ("y", "out", "gx", "gy", "gw", "dEdr", "F", "ggy", "d_x", "d_w"):
+    for k in ("y", "out", "gx", "gy", "gw", "dEdr", "F", "ggy", "d_x", "d_w", "FL"):
         assert_close(host(gpu[k]), ref[k], np.float32, k)
 
 

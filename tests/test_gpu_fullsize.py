@@ -153,6 +153,10 @@ def test_config4_chain_sampled():
                                 edges=edges)
     assert_close(res["d_x"][nodes], dx[nodes], np.float32, "dL/dx rows")
     assert_close(res["d_w"][edges], dw[edges], np.float32, "dL/dw rows")
+    dLdr = np.zeros((gr.E, 3))
+    dLdr[edges] = O.sh_hvp(3, vec[edges], ry[edges], q[edges])
+    FL = O.edge_forces(gr.rowptr, gr.sender, dLdr)
+    assert_close(res["FL"][nodes], FL[nodes], np.float32, "-dL/dpos rows")
 
 
 def test_config4_fused_kv_sampled():
