@@ -457,3 +457,103 @@ def radial_backward(vec, W1, W2, grad_w, cutoff: float = 5.0):
     dr = np.where(r > 0.0, (gb * db).sum(axis=1), 0.0)
     gvec = v * (dr / np.where(r > 0.0, r, 1.0)).reshape(-1, 1)
     return gvec, gW1, gW2
+
+
+# ------------------------------------------------ channel mixing ('uvw') ---
+#
+# NVIDIA's SE(3)-Transformer blog, section "TFN fusion": the pairwise degree
+# convolutions of a layer are summed per output degree, and the fused variants
+# concatenate degrees so that the channel contractions become dense products
+# whose sizes are multiples of 16, for the tensor cores.  The dense part is a
+# per-irrep channel mixing.  For an instruction (i, o) between an input and an
+# output irrep of the same l and parity, with its own matrix W [mul_in, mul_out]:
+#     out[n, o, m, w] += sum_u x[n, i, m, u] W[u, w]          (m = -l..l)
+# Readings (the pages give no formula): no normalisation factor (the caller
+# scales W); outputs that no instruction reaches are zero; the weights of the
+# instructions are stored one after another, each row-major [mul_in][mul_out].
+# numpy's einsum (a library contraction) is the only step beyond loops.
+
+def _blocks(irreps):
+    off, res = 0, []
+    for mul, l, p in irreps:
+        res.append((off, mul, l, p))
+        off += mul * (2 * l + 1)
+    return res
+
+
+def linear_instructions(irreps_in: str, irreps_out: str):
+    """Every (i, o) pair of input and output irreps with the same l and parity,
+    input-major."""
+    a, b = parse_irreps(irreps_in), parse_irreps(irreps_out)
+    return [(i, o) for i, (_, li, pi) in enumerate(a) for o, (_, lo, po) in enumerate(b)
+            if li == lo and pi == po]
+
+
+def _linear_layout(irreps_in, irreps_out, instr):
+    a, b = _blocks(parse_irreps(irreps_in)), _blocks(parse_irreps(irreps_out))
+    res, offw = [], 0
+    for i, o in instr:
+        (oi, mi, li, pi), (oo, mo, lo, po) = a[i], b[o]
+        if li != lo or pi != po:
+            raise ValueError(f"instruction ({i}, {o}) joins different irreps")
+        res.append((oi, mi, oo, mo, 2 * li + 1, offw))
+        offw += mi * mo
+    dim_in = sum(m * (2 * l + 1) for m, l, _ in parse_irreps(irreps_in))
+    dim_out = sum(m * (2 * l + 1) for m, l, _ in parse_irreps(irreps_out))
+    return res, dim_in, dim_out, offw
+
+
+def linear_forward(irreps_in: str, irreps_out: str, instr, x, W) -> np.ndarray:
+    lay, dim_in, dim_out, nw = _linear_layout(irreps_in, irreps_out, instr)
+    x, W = _f64(x), _f64(W)
+    if x.shape[1] != dim_in or W.shape != (nw,):
+        raise ValueError("x / W do not match the irreps")
+    out = np.zeros((x.shape[0], dim_out))
+    for oi, mi, oo, mo, d, ow in lay:
+        xb = x[:, oi:oi + d * mi].reshape(-1, d, mi)
+        Wj = W[ow:ow + mi * mo].reshape(mi, mo)
+        out[:, oo:oo + d * mo] += np.einsum("nmu,uw->nmw", xb, Wj).reshape(-1, d * mo)
+    return out
+
+
+def linear_backward(irreps_in: str, irreps_out: str, instr, x, W, g):
+    """(dL/dx, dL/dW) for the cotangent g = dL/dout."""
+    lay, dim_in, dim_out, nw = _linear_layout(irreps_in, irreps_out, instr)
+    x, W, g = _f64(x), _f64(W), _f64(g)
+    gx, gW = np.zeros_like(x), np.zeros(nw)
+    for oi, mi, oo, mo, d, ow in lay:
+        xb = x[:, oi:oi + d * mi].reshape(-1, d, mi)
+        gb = g[:, oo:oo + d * mo].reshape(-1, d, mo)
+        Wj = W[ow:ow + mi * mo].reshape(mi, mo)
+        gx[:, oi:oi + d * mi] += np.einsum("nmw,uw->nmu", gb, Wj).reshape(-1, d * mi)
+        gW[ow:ow + mi * mo] += np.einsum("nmu,nmw->uw", xb, gb).ravel()
+    return gx, gW
+
+
+def tp_uvw_forward(irreps_in1: str, irreps_in2: str, irreps_out: str, x, y, W) -> np.ndarray:
+    """Tensor product with full channel mixing per path ('uvw', one weight
+    matrix per path shared by all rows):
+        out[b, k, m3, w] = sum_paths->k sum_u sum_{m1,m2}
+                           C[m1, m2, m3] x[b, i1, m1, u] y[b, i2, m2] W_p[u, w]
+    Paths: every parity-allowed (i1, i2, k) with mul(in2) = 1, in1-major, then
+    in2, then out (the output multiplicity may differ from in1's).  W holds
+    the paths' [mul1, mul_out] matrices one after another."""
+    a, b, c = (_blocks(parse_irreps(s)) for s in (irreps_in1, irreps_in2, irreps_out))
+    x, y, W = _f64(x), _f64(y), _f64(W)
+    out = np.zeros((x.shape[0], sum(m * (2 * l + 1) for _, m, l, _ in c)))
+    ow = 0
+    for o1, m1, l1, p1 in a:
+        for o2, m2, l2, p2 in b:
+            for o3, m3, l3, p3 in c:
+                if not (abs(l1 - l2) <= l3 <= l1 + l2 and p3 == p1 * p2 and m2 == 1):
+                    continue
+                C = cg_real(l1, l2, l3)
+                xb = x[:, o1:o1 + (2 * l1 + 1) * m1].reshape(-1, 2 * l1 + 1, m1)
+                yb = y[:, o2:o2 + 2 * l2 + 1]
+                Wp = W[ow:ow + m1 * m3].reshape(m1, m3)
+                ow += m1 * m3
+                out[:, o3:o3 + (2 * l3 + 1) * m3] += np.einsum(
+                    "ijk,biu,bj,uw->bkw", C, xb, yb, Wp).reshape(x.shape[0], -1)
+    if W.shape != (ow,):
+        raise ValueError("W does not match the paths")
+    return out
