@@ -18,7 +18,8 @@ samples, 128 channels (fwd+bwd, samples/s); ``conv64`` the fp64 fused conv,
 N = 5,000, 128 channels (forward, edges/s); ``tfn`` the TFN layer on 1000
 molecules (forward, backward, forces and the double backward, edges/s); ``kv``
 the same molecules at 64 channels, keys and values of an SE(3)-Transformer layer
-from one TFN (fwd+bwd, edges/s).
+from one TFN (fwd+bwd, edges/s); ``uvw`` config 1's samples under a 'uvw'
+product (one shared 128x128 matrix per path; channel mixing on tcgen05).
 
 ``--impl reference`` times the CPU oracle (the reference arm of this build) on
 a bounded subgraph of the same workload.
@@ -412,8 +413,42 @@ def make_kv(args, cg, W, torch):
                     dict(N=N, E=E, mul=64, paths=plan.n_paths), None, None)
 
 
+def make_uvw(args, cg, W, torch):
+    """'uvw' product at config 1's sizes: per-path 'uvu' blocks (unit shared
+    weights), then the channel mixing on the tensor cores."""
+    cfg = W.config1_uvw()
+    B = cfg["B"]
+    uvw = cg.UVWProduct(*W.CFG1)
+    x, vec, Wm = (torch.from_numpy(cfg[k]).cuda() for k in ("x", "vec", "W"))
+    y = torch.empty(B, uvw.dim_in2, device="cuda")
+    mid = torch.empty(B, uvw.dim_mid, device="cuda")
+    out = torch.empty(B, uvw.dim_out, device="cuda")
+    ones = torch.ones(uvw.plan.weight_numel, device="cuda")
+    ws = torch.empty(uvw.linear.workspace_bytes(B)[0], dtype=torch.uint8, device="cuda")
+    uvw.plan.compile()
+    kernels = [("sh_fwd", lambda: cg.sh_forward(vec, 3, out=y)),
+               ("tp_paths", lambda: uvw.plan.forward(x, y, ones, out=mid)),
+               ("linear", lambda: uvw.linear.forward(mid, Wm, out=out, workspace=ws))]
+    d = Dims(uvw.plan)
+    mix = 0
+    for j in range(uvw.linear.n_instr):
+        i, o, _ = uvw.linear.instruction(j)
+        mix += uvw.plan.path(j)[2] * 2 + 1
+    mix_flops = 2 * B * mix * 128 * 128
+    counts = {"sh_fwd": (B * (3 + d.dim2) * 4, None),
+              "tp_paths": (B * (d.dim1 + d.dim2 + d.dimo) * 4 + d.wdim * 4, B * d.flops),
+              "linear": (B * (uvw.dim_mid + uvw.dim_out) * 4 + uvw.weight_numel * 4, mix_flops,
+                         "tensor3")}
+    desc = ("'uvw' CG-TP: B=200000, 128x(0e,1o,2e) (x) Y(l<=3) -> 128x(0e,1o,1e,2o,2e,3o,3e), "
+            "24 paths, one shared 128x128 matrix per path, fp32 (channel mixing on tcgen05, "
+            "TF32 split in three products)")
+    return Workload("uvw", desc, B, "samples/s", "f32", kernels, counts,
+                    ["sh_fwd", "tp_paths", "linear"], dict(B=B, mul=128, paths=uvw.n_paths),
+                    None, None)
+
+
 WORKLOADS = {"conv": make_conv, "conv64": make_conv64, "tp": make_tp, "tfn": make_tfn,
-             "kv": make_kv}
+             "kv": make_kv, "uvw": make_uvw}
 
 
 # ------------------------------------------------------------ GPU arm
@@ -476,13 +511,22 @@ def run_gpu(args):
     else:
         fp32_peak = SM_COUNT * FP32_LANES_PER_SM * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12  # TFLOP/s
         alu_src = f"FP32 ALU: 152 SM x 128 FMA x 2 x {peaks['sm_max_mhz']:.0f} MHz"
+    # fp32 products as three TF32 products on the tensor cores: the effective
+    # peak is the measured bf16 GEMM rate x the nominal tf32/bf16 ratio / 3
+    tc_peak = peaks["bf16"] * TF32_PER_BF16 / 3 if peaks.get("bf16") else None
     kernels = {}
     for n in names:
-        nbytes, flops = wl.counts[n]
+        nbytes, flops, *kind = wl.counts[n]
         t = per[n] * 1e-3
         gbs = nbytes / t / 1e9
         ent = {"ms": per[n], "hbm_gbs": gbs, "hbm_frac": gbs / peaks["hbm"]}
-        if flops:
+        if flops and kind and kind[0] == "tensor3" and tc_peak:
+            tf = flops / t / 1e12
+            t_hbm, t_tc = nbytes / (peaks["hbm"] * 1e9), flops / (tc_peak * 1e12)
+            ent.update(tflops=tf, tensor_frac=tf / tc_peak,
+                       bound="tensor" if t_tc >= t_hbm else "hbm",
+                       roofline_frac=max(t_hbm, t_tc) / t)
+        elif flops:
             tf = flops / t / 1e12
             ent.update(tflops=tf, fp32_frac=tf / fp32_peak)
             t_hbm, t_alu = nbytes / (peaks["hbm"] * 1e9), flops / (fp32_peak * 1e12)
@@ -515,7 +559,12 @@ def run_gpu(args):
                                    "for the conv gradient's grad_w"}
     dom = max(names, key=lambda n: per[n])
     kd = kernels[dom]
-    if kd["bound"] == "alu":
+    if kd["bound"] == "tensor":
+        roof = {"bound": "tensor", "achieved": kd["tflops"], "peak": tc_peak, "unit": "TFLOP/s",
+                "frac": kd["tflops"] / tc_peak,
+                "note": "fp32 products as three TF32 tensor-core products: peak = measured bf16 "
+                        "x nominal tf32/bf16 / 3"}
+    elif kd["bound"] == "alu":
         roof = {"bound": "alu", "achieved": kd["tflops"], "peak": fp32_peak, "unit": "TFLOP/s",
                 "frac": kd["tflops"] / fp32_peak}
     else:

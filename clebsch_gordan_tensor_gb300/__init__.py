@@ -36,6 +36,10 @@ class CgtpError(RuntimeError):
     pass
 
 
+class _LinInstr(ctypes.Structure):
+    _fields_ = [("i_in", ctypes.c_int), ("i_out", ctypes.c_int)]
+
+
 class _Instr(ctypes.Structure):
     _fields_ = [("i_in1", ctypes.c_int), ("i_in2", ctypes.c_int), ("i_out", ctypes.c_int),
                 ("mode", ctypes.c_char * 4)]
@@ -93,6 +97,18 @@ def lib() -> ctypes.CDLL:
                 "cgtp_radial_backward_workspace": [i32, i64, i32, i32, i64, P(ctypes.c_size_t)],
                 "cgtp_radial_path": [i32, i32, i32, i64, P(i32)],
                 "cgtp_radial_device_status": [P(i32)],
+                "cgtp_linear_create": [P(vp), ctypes.c_char_p, ctypes.c_char_p, P(_LinInstr),
+                                       i32, i32],
+                "cgtp_linear_destroy": [vp],
+                "cgtp_linear_info": [vp, P(i64), P(i64), P(i64), P(i32)],
+                "cgtp_linear_instruction": [vp, i32, P(i32), P(i32), P(i64)],
+                "cgtp_linear_workspace": [vp, i64, P(ctypes.c_size_t), P(ctypes.c_size_t)],
+                "cgtp_linear_path": [vp, P(i32)],
+                "cgtp_linear_forward": [vp, i64, vp, vp, vp, vp, ctypes.c_size_t, ctypes.c_uint,
+                                        vp],
+                "cgtp_linear_backward": [vp, i64, vp, vp, vp, vp, vp, vp, ctypes.c_size_t,
+                                         ctypes.c_uint, vp],
+                "cgtp_linear_device_status": [P(i32)],
             }
             for name, args in sig.items():
                 f = getattr(L, name)
@@ -483,3 +499,137 @@ def edge_forces_adjoint(g: Graph, grad_forces, out=None):
                                           _ptr(g.sender), _ptr(grad_forces), _ptr(out),
                                           _stream()))
     return out
+
+
+class Linear:
+    """Per-irrep channel mixing: out[n, o, m, w] = sum over instructions (i, o)
+    of sum_u x[n, i, m, u] W_j[u, w] (the layer of ``cgtp_linear_forward``).
+    ``instr`` lists (i_in, i_out) pairs; None takes every pair of equal irreps."""
+
+    def __init__(self, irreps_in: str, irreps_out: str, instr=None, dtype=torch.float32):
+        self.dtype = dtype
+        h = ctypes.c_void_p()
+        if instr is None:
+            arr, n = None, 0
+        else:
+            arr = (_LinInstr * max(1, len(instr)))(*[_LinInstr(i, o) for i, o in instr])
+            n = len(instr)
+        _check(lib().cgtp_linear_create(ctypes.byref(h), irreps_in.encode(), irreps_out.encode(),
+                                        arr, n, _dt(dtype)))
+        self._h = h
+        a, b, c = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+        k = ctypes.c_int()
+        _check(lib().cgtp_linear_info(h, ctypes.byref(a), ctypes.byref(b), ctypes.byref(c),
+                                      ctypes.byref(k)))
+        self.dim_in, self.dim_out, self.weight_numel, self.n_instr = a.value, b.value, c.value, k.value
+        t = ctypes.c_int()
+        _check(lib().cgtp_linear_path(h, ctypes.byref(t)))
+        self.tensor_cores = bool(t.value)
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h is not None and _lib is not None:
+            _lib.cgtp_linear_destroy(h)
+
+    def instruction(self, j: int):
+        i, o, w = ctypes.c_int(), ctypes.c_int(), ctypes.c_int64()
+        _check(lib().cgtp_linear_instruction(self._h, j, ctypes.byref(i), ctypes.byref(o),
+                                             ctypes.byref(w)))
+        return i.value, o.value, w.value
+
+    def workspace_bytes(self, n: int):
+        f, b = ctypes.c_size_t(), ctypes.c_size_t()
+        _check(lib().cgtp_linear_workspace(self._h, n, ctypes.byref(f), ctypes.byref(b)))
+        return f.value, b.value
+
+    def _ws(self, nbytes, device):
+        return torch.empty(max(1, (nbytes + 15) // 16) * 16, dtype=torch.uint8, device=device)
+
+    def forward(self, x, W, out=None, workspace=None, cuda_cores: bool = False):
+        n = x.shape[0]
+        _need(x, "x", self.dtype, (n, self.dim_in))
+        _need(W, "W", self.dtype, (self.weight_numel,))
+        if out is None:
+            out = torch.empty(n, self.dim_out, dtype=self.dtype, device=x.device)
+        _need(out, "out", self.dtype, (n, self.dim_out))
+        fb, _ = self.workspace_bytes(n)
+        if workspace is None and fb > 0:
+            workspace = self._ws(fb, x.device)
+        nb = 0 if workspace is None else workspace.numel() * workspace.element_size()
+        _check(lib().cgtp_linear_forward(self._h, n, _ptr(x), _ptr(W), _ptr(out), _ptr(workspace),
+                                         nb, 1 if cuda_cores else 0, _stream()))
+        return out
+
+    def backward(self, x, W, grad_out, need=(True, True), workspace=None, cuda_cores: bool = False):
+        """(grad_x, grad_W); an entry is None where ``need`` is False."""
+        n = x.shape[0]
+        _need(x, "x", self.dtype, (n, self.dim_in))
+        _need(W, "W", self.dtype, (self.weight_numel,))
+        _need(grad_out, "grad_out", self.dtype, (n, self.dim_out))
+        gx = torch.empty_like(x) if need[0] else None
+        gW = torch.empty_like(W) if need[1] else None
+        _, bb = self.workspace_bytes(n)
+        if workspace is None:
+            workspace = self._ws(bb, x.device)
+        nb = workspace.numel() * workspace.element_size()
+        _check(lib().cgtp_linear_backward(self._h, n, _ptr(x), _ptr(W), _ptr(grad_out), _ptr(gx),
+                                          _ptr(gW), _ptr(workspace), nb, 1 if cuda_cores else 0,
+                                          _stream()))
+        return gx, gW
+
+
+def linear_device_status() -> int:
+    c = ctypes.c_int()
+    _check(lib().cgtp_linear_device_status(ctypes.byref(c)))
+    return c.value
+
+
+def _irreps(s: str):
+    out = []
+    for tok in s.replace(" ", "").split("+"):
+        mul, _, ir = tok.rpartition("x")
+        out.append((int(mul) if mul else 1, int(ir[:-1]), 1 if ir[-1] == "e" else -1))
+    return out
+
+
+class UVWProduct:
+    """'uvw' tensor product: one [mul_in, mul_out] matrix per path, shared by
+    all rows,
+        out[b, k, m3, w] = sum_paths->k sum_u sum_{m1,m2} C[m1,m2,m3]
+                           x[b, i1, m1, u] y[b, i2, m2] W_p[u, w],
+    for every parity-allowed path (in1-major, then in2, then out).  Two library
+    calls: the 'uvu' product into one output irrep per path with a shared
+    weight row of ones (``Plan``), then the channel-mixing layer from those
+    irreps to irreps_out, instruction p joining path p's block to its target
+    irrep (``Linear``, tensor cores).  W holds the paths' matrices in order."""
+
+    def __init__(self, irreps_in1: str, irreps_in2: str, irreps_out: str, dtype=torch.float32):
+        a, b, c = _irreps(irreps_in1), _irreps(irreps_in2), _irreps(irreps_out)
+        mul = a[0][0]
+        if any(m != mul for m, _, _ in a):
+            raise CgtpError("'uvw' needs one multiplicity for every irrep of in1")
+        blocks, tp_instr, lin_instr = [], [], []
+        for i1, (_, l1, p1) in enumerate(a):
+            for i2, (m2, l2, p2) in enumerate(b):
+                for k, (_, l3, p3) in enumerate(c):
+                    if abs(l1 - l2) <= l3 <= l1 + l2 and p3 == p1 * p2 and m2 == 1:
+                        tp_instr.append((i1, i2, len(blocks)))
+                        lin_instr.append((len(blocks), k))
+                        blocks.append(f"{mul}x{l3}{'e' if p3 == 1 else 'o'}")
+        if not blocks:
+            raise CgtpError("no parity-allowed path")
+        self.mid = "+".join(blocks)
+        self.plan = Plan(irreps_in1, irreps_in2, self.mid, dtype=dtype, shared_weights=True,
+                         instructions=tp_instr)
+        self.linear = Linear(self.mid, irreps_out, instr=lin_instr, dtype=dtype)
+        self.n_paths = len(blocks)
+        self.dim_in1, self.dim_in2 = self.plan.dim_in1, self.plan.dim_in2
+        self.dim_mid, self.dim_out = self.plan.dim_out, self.linear.dim_out
+        self.weight_numel = self.linear.weight_numel
+        self.ones = None
+
+    def forward(self, x, y, W, out=None, mid=None, workspace=None):
+        if self.ones is None or self.ones.device != x.device:
+            self.ones = torch.ones(self.plan.weight_numel, dtype=x.dtype, device=x.device)
+        mid = self.plan.forward(x, y, self.ones, out=mid)
+        return self.linear.forward(mid, W, out=out, workspace=workspace)

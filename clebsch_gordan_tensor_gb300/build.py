@@ -43,7 +43,7 @@ def build(verbose: bool = False) -> str:
     os.makedirs(OUT, exist_ok=True)
     inc = ["-I", os.path.join(ROOT, "include"), "-I", CSRC, "-I", os.path.join(CUDA, "include")]
     headers = [os.path.join(ROOT, "include", "cgtp.h"), os.path.join(CSRC, "plan.hpp"),
-               os.path.join(CSRC, "internal.hpp")]
+               os.path.join(CSRC, "internal.hpp"), os.path.join(CSRC, "tcgen05.cuh")]
     embed = os.path.join(OUT, "tp_kernels_embed.cpp")
     _embed(os.path.join(CSRC, "tp_kernels.cuh"), embed, "kTpKernelsSource")
     jobs = []
@@ -55,7 +55,7 @@ def build(verbose: bool = False) -> str:
         jobs.append((obj, [src, *headers], cmd))
     jobs.append((embed + ".o", [embed],
                  ["g++", "-std=c++17", "-O2", "-fPIC", "-c", embed, "-o", embed + ".o"]))
-    for name in ("sh.cu", "graph.cu", "radial.cu", "noalloc.cu"):
+    for name in ("sh.cu", "graph.cu", "radial.cu", "linear.cu", "noalloc.cu"):
         src = os.path.join(CSRC, name)
         obj = os.path.join(OUT, name + ".o")
         cmd = [os.path.join(CUDA, "bin", "nvcc"), *ARCH, "-std=c++17", "-O3", "-lineinfo",

@@ -20,6 +20,10 @@ struct cgtp_plan_s {
     cgtp::Plan p;
 };
 
+struct cgtp_linear_s {
+    cgtp::LinearImpl* L;
+};
+
 namespace cgtp {
 
 static thread_local int t_cuda_err = 0;
@@ -648,6 +652,138 @@ cgtp_status cgtp_sh_hvp(int lmax, cgtp_dtype dtype, int64_t E, const void* vec,
         launch_sh_hvp(lmax, dtype == CGTP_F64, E, vec, grad_y, tangent_vec, out, S(stream));
     if (e != cudaSuccess) return cuda_fail(e, "sh_hvp");
     count_launch();
+    return CGTP_OK;
+    GUARD_END
+}
+
+cgtp_status cgtp_linear_create(cgtp_linear* out, const char* irreps_in, const char* irreps_out,
+                               const cgtp_linear_instr* instr, int n_instr, cgtp_dtype dtype) {
+    GUARD_BEGIN
+    if (!out) return fail(CGTP_E_ARG, "NULL output handle");
+    *out = nullptr;
+    if (dtype != CGTP_F32 && dtype != CGTP_F64) return fail(CGTP_E_ARG, "bad dtype");
+    LinearImpl* L = nullptr;
+    std::string err;
+    cgtp_status st = linear_create(irreps_in, irreps_out, instr, n_instr, dtype, &L, err);
+    if (st != CGTP_OK) return fail(st, err);
+    *out = new cgtp_linear_s{L};
+    return CGTP_OK;
+    GUARD_END
+}
+
+cgtp_status cgtp_linear_destroy(cgtp_linear lin) {
+    GUARD_BEGIN
+    if (!lin) return CGTP_OK;
+    linear_destroy(lin->L);
+    delete lin;
+    return CGTP_OK;
+    GUARD_END
+}
+
+cgtp_status cgtp_linear_info(cgtp_linear lin, int64_t* dim_in, int64_t* dim_out,
+                             int64_t* weight_numel, int* n_instr) {
+    GUARD_BEGIN
+    if (!lin) return fail(CGTP_E_ARG, "NULL linear layer");
+    linear_info(lin->L, dim_in, dim_out, weight_numel, n_instr);
+    return CGTP_OK;
+    GUARD_END
+}
+
+cgtp_status cgtp_linear_instruction(cgtp_linear lin, int j, int* i_in, int* i_out,
+                                    int64_t* weight_offset) {
+    GUARD_BEGIN
+    if (!lin) return fail(CGTP_E_ARG, "NULL linear layer");
+    if (!linear_instruction(lin->L, j, i_in, i_out, weight_offset))
+        return fail(CGTP_E_ARG, "instruction index out of range");
+    return CGTP_OK;
+    GUARD_END
+}
+
+cgtp_status cgtp_linear_workspace(cgtp_linear lin, int64_t n, size_t* fwd_bytes,
+                                  size_t* bwd_bytes) {
+    GUARD_BEGIN
+    if (!lin) return fail(CGTP_E_ARG, "NULL linear layer");
+    if (n < 0) return fail(CGTP_E_ARG, "negative row count");
+    if (fwd_bytes) *fwd_bytes = linear_fwd_workspace(lin->L);
+    if (bwd_bytes) *bwd_bytes = linear_bwd_workspace(lin->L, n);
+    return CGTP_OK;
+    GUARD_END
+}
+
+cgtp_status cgtp_linear_path(cgtp_linear lin, int* tensor_cores) {
+    GUARD_BEGIN
+    if (!lin || !tensor_cores) return fail(CGTP_E_ARG, "NULL argument");
+    *tensor_cores = linear_tensor_cores(lin->L) ? 1 : 0;
+    return CGTP_OK;
+    GUARD_END
+}
+
+static cgtp_status linear_check(cgtp_linear lin, int64_t n,
+                                std::initializer_list<const void*> ptrs) {
+    if (!lin) return fail(CGTP_E_ARG, "NULL linear layer");
+    if (n < 0) return fail(CGTP_E_ARG, "negative row count");
+    int64_t di = 0, dout = 0;
+    linear_info(lin->L, &di, &dout, nullptr, nullptr);
+    if (n > ((int64_t)1 << 40) / std::max<int64_t>(1, std::max(di, dout)))
+        return fail(CGTP_E_ARG, "row count too large");
+    for (const void* q : ptrs)
+        if (!aligned(q, 4)) return fail(CGTP_E_ARG, "tensor pointer not aligned to its element");
+    return CGTP_OK;
+}
+
+cgtp_status cgtp_linear_forward(cgtp_linear lin, int64_t n, const void* x, const void* W,
+                                void* out, void* workspace, size_t workspace_bytes,
+                                unsigned flags, cgtp_stream stream) {
+    GUARD_BEGIN
+    cgtp_status st = linear_check(lin, n, {x, W, out});
+    if (st != CGTP_OK) return st;
+    if (n == 0) return CGTP_OK;
+    if (!x || !W || !out) return fail(CGTP_E_ARG, "NULL tensor");
+    if (workspace && !aligned(workspace, 16)) return fail(CGTP_E_ARG, "workspace not 16-byte aligned");
+    cudaError_t e = launch_linear_forward(lin->L, n, x, W, out, workspace, workspace_bytes,
+                                          !(flags & CGTP_LINEAR_CUDA_CORES), S(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "linear_forward");
+    count_launch();
+    return CGTP_OK;
+    GUARD_END
+}
+
+cgtp_status cgtp_linear_backward(cgtp_linear lin, int64_t n, const void* x, const void* W,
+                                 const void* grad_out, void* grad_x, void* grad_W,
+                                 void* workspace, size_t workspace_bytes, unsigned flags,
+                                 cgtp_stream stream) {
+    GUARD_BEGIN
+    cgtp_status st = linear_check(lin, n, {x, W, grad_out, grad_x, grad_W});
+    if (st != CGTP_OK) return st;
+    if (!grad_x && !grad_W) return CGTP_OK;
+    if (n == 0) {  // no rows: grad_W is zero
+        if (!grad_W) return CGTP_OK;
+        cudaError_t e = launch_linear_backward(lin->L, 0, nullptr, nullptr, nullptr, nullptr,
+                                               grad_W, nullptr, 0, false, S(stream));
+        if (e != cudaSuccess) return cuda_fail(e, "linear_backward");
+        count_launch();
+        return CGTP_OK;
+    }
+    if (!grad_out || (grad_x && !W) || (grad_W && !x)) return fail(CGTP_E_ARG, "NULL tensor");
+    if (grad_W && (!workspace || workspace_bytes < linear_bwd_workspace(lin->L, n) ||
+                   !aligned(workspace, 16)))
+        return fail(CGTP_E_ARG, "grad_W needs a 16-byte aligned workspace of "
+                                "cgtp_linear_workspace() bwd bytes");
+    if (workspace && !aligned(workspace, 16)) return fail(CGTP_E_ARG, "workspace not 16-byte aligned");
+    cudaError_t e = launch_linear_backward(lin->L, n, x, W, grad_out, grad_x, grad_W, workspace,
+                                           workspace_bytes, !(flags & CGTP_LINEAR_CUDA_CORES),
+                                           S(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "linear_backward");
+    count_launch();
+    return CGTP_OK;
+    GUARD_END
+}
+
+cgtp_status cgtp_linear_device_status(int* code) {
+    GUARD_BEGIN
+    if (!code) return fail(CGTP_E_ARG, "NULL output");
+    cudaError_t e = linear_device_status(code);
+    if (e != cudaSuccess) return cuda_fail(e, "linear_device_status");
     return CGTP_OK;
     GUARD_END
 }

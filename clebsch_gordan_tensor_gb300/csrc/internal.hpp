@@ -64,6 +64,27 @@ cudaError_t launch_radial_backward(bool f64, bool tensor_cores, int64_t E, int n
                                    const void* W2, const void* gw, void* gvec, void* gW1,
                                    void* gW2, void* ws, cudaStream_t s);
 
+// Per-irrep channel mixing (linear.cu).
+struct LinearImpl;
+cgtp_status linear_create(const char* irreps_in, const char* irreps_out,
+                          const cgtp_linear_instr* instr, int n_instr, cgtp_dtype dt,
+                          LinearImpl** res, std::string& err);
+void linear_destroy(LinearImpl* L);
+void linear_info(const LinearImpl* L, int64_t* dim_in, int64_t* dim_out, int64_t* nw, int* ninstr);
+bool linear_instruction(const LinearImpl* L, int j, int* i_in, int* i_out, int64_t* w_off);
+bool linear_tensor_cores(const LinearImpl* L);
+size_t linear_fwd_workspace(const LinearImpl* L);
+size_t linear_bwd_workspace(const LinearImpl* L, int64_t n);
+bool linear_uses_tc(const LinearImpl* L, int64_t n, const void* a, const void* out, const void* ws,
+                    size_t ws_bytes, bool fwd);
+cudaError_t launch_linear_forward(const LinearImpl* L, int64_t n, const void* x, const void* W,
+                                  void* out, void* ws, size_t ws_bytes, bool allow_tc,
+                                  cudaStream_t s);
+cudaError_t launch_linear_backward(const LinearImpl* L, int64_t n, const void* x, const void* W,
+                                   const void* g, void* gx, void* gW, void* ws, size_t ws_bytes,
+                                   bool allow_tc, cudaStream_t s);
+cudaError_t linear_device_status(int* code);
+
 // Partial weight-gradient rows a shared-weight backward may write (grid cap).
 constexpr int64_t kSharedWRows = 2048;
 

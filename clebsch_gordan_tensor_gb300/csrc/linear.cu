@@ -1,0 +1,756 @@
+// Per-irrep channel mixing ("linear" layer, the dense 'uvw' contraction)
+// (sm_103a).
+//
+// NVIDIA's SE(3)-Transformer blog, section "TFN fusion": the pairwise degree
+// convolutions are summed per output degree, and the fused layers concatenate
+// degrees so that the channel contractions become dense products with sizes
+// that are multiples of 16, for the tensor cores.  For an instruction j that
+// joins input irrep i and output irrep o (same l and parity) with a matrix
+// W_j [mul_in, mul_out]:
+//     out[n, o, m, w] += sum_u x[n, i, m, u] W_j[u, w]          (m = -l..l)
+// Rows (n, m) of one output block form a GEMM with M = n * (2l+1) rows,
+// K = the concatenated u ranges of every instruction into that block and
+// N = mul_out.  The gradient in x is the same GEMM with W_j transposed, one
+// block per input irrep; the gradient in W_j sums x^T g over the rows.
+//
+// Kernels:
+//   * linear_tc_kernel (fp32; every mul a multiple of 32, mul_out <= 256,
+//     16-byte aligned rows): 128-row tiles on tcgen05 with kind::tf32; A (the
+//     rows, loaded and split into TF32 hi + lo parts by all four warps) and B
+//     (the packed hi/lo image of W, one bulk copy per 32-wide K chunk) sit in
+//     a two-stage shared-memory ring; one thread issues hi*hi + hi*lo + lo*hi
+//     into a 128 x mul_out fp32 accumulator in tensor memory (the dropped
+//     lo*lo term is 2^-22 relative).  The next chunk's rows are loaded into
+//     registers while the current chunk multiplies.
+//   * linear_simt_kernel (fp32 / fp64, any shape): shared-memory tiles and 4 x 4
+//     FMA micro-tiles on the CUDA cores.
+//   * linear_wgrad_kernel: per-CTA partial sums of x^T g over a fixed row
+//     range, then the partial rows are added in a fixed order (deterministic).
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+
+#include "internal.hpp"
+#include "tcgen05.cuh"
+
+namespace cgtp {
+
+__device__ int cgtp_linear_error;  // nonzero: a bounded wait timed out
+
+// ------------------------------------------------------------ descriptors
+
+// One output block of a GEMM pass (an output irrep in the forward, an input
+// irrep in the x-gradient): rows (n, m), m < d, written at
+// out[n * out_stride + out_off + m * ncols + c] for c < ncols.
+struct LinBlock {
+    int out_off, ncols, d, chunk0, nchunk;
+};
+// One K chunk of a block: columns a_off + m * a_mul + k0 + k (k < kc) of the
+// input rows, against B[k][c] = W[w_off + (k0 + k) * w_ks + c * w_ns]; the
+// packed tensor-core image of the chunk starts at byte img_off.
+struct LinChunk {
+    int a_off, a_mul, k0, kc, w_off, w_ks, w_ns, img_off;
+};
+
+constexpr int kLinMaxBlocks = 32;
+constexpr int kLinMaxChunks = 384;
+struct LinDesc {
+    int nblocks, nchunks;
+    int64_t in_stride, out_stride;
+    LinBlock blk[kLinMaxBlocks];
+    LinChunk ch[kLinMaxChunks];
+};
+
+// --------------------------------------------------------------- CUDA cores
+
+constexpr int kLsT = 64;   // rows per tile
+constexpr int kLsC = 64;   // columns per tile
+constexpr int kLsK = 16;   // K per shared-memory step
+constexpr int kLsThreads = 256;
+
+// grid: x = row tile, y = column tile, z = block
+template <typename T>
+__global__ void __launch_bounds__(kLsThreads)
+linear_simt_kernel(const __grid_constant__ LinDesc D, int64_t n, const T* __restrict__ x,
+                   const T* __restrict__ W, T* __restrict__ out) {
+    const LinBlock& B = D.blk[blockIdx.z];
+    const int64_t rows = n * B.d;
+    const int64_t r0 = (int64_t)blockIdx.x * kLsT;
+    const int c0 = blockIdx.y * kLsC;
+    if (r0 >= rows || c0 >= B.ncols) return;
+    __shared__ T As[kLsK][kLsT + 1];
+    __shared__ T Bs[kLsK][kLsC];
+    const int tid = threadIdx.x, tr = tid / 16, tc = tid % 16;
+    T acc[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = (T)0;
+    for (int ci = 0; ci < B.nchunk; ++ci) {
+        const LinChunk& C = D.ch[B.chunk0 + ci];
+        for (int kk = 0; kk < C.kc; kk += kLsK) {
+            __syncthreads();
+            for (int i = tid; i < kLsK * kLsT; i += kLsThreads) {
+                const int k = i % kLsK, r = i / kLsK;
+                const int64_t R = r0 + r;
+                T v = (T)0;
+                if (R < rows && kk + k < C.kc) {
+                    const int64_t item = R / B.d;
+                    const int m = (int)(R % B.d);
+                    v = x[item * D.in_stride + C.a_off + (int64_t)m * C.a_mul + C.k0 + kk + k];
+                }
+                As[k][r] = v;
+            }
+            for (int i = tid; i < kLsK * kLsC; i += kLsThreads) {
+                const int c = i % kLsC, k = i / kLsC;
+                T v = (T)0;
+                if (c0 + c < B.ncols && kk + k < C.kc)
+                    v = W[C.w_off + (int64_t)(C.k0 + kk + k) * C.w_ks + (int64_t)(c0 + c) * C.w_ns];
+                Bs[k][c] = v;
+            }
+            __syncthreads();
+#pragma unroll
+            for (int k = 0; k < kLsK; ++k) {
+                T a[4], b[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) a[i] = As[k][tr * 4 + i];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) b[j] = Bs[k][tc + 16 * j];
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) acc[i][j] = fma(a[i], b[j], acc[i][j]);
+            }
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int64_t R = r0 + tr * 4 + i;
+        if (R >= rows) continue;
+        const int64_t item = R / B.d;
+        const int m = (int)(R % B.d);
+        T* o = out + item * D.out_stride + B.out_off + (int64_t)m * B.ncols;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int c = c0 + tc + 16 * j;
+            if (c < B.ncols) o[c] = acc[i][j];
+        }
+    }
+}
+
+// Zero the output columns of blocks that no instruction reaches.
+template <typename T>
+__global__ void linear_zero_kernel(int64_t n, int64_t stride, int off, int width,
+                                   T* __restrict__ out) {
+    const int64_t total = n * width;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x)
+        out[(i / width) * stride + off + i % width] = (T)0;
+}
+
+// ------------------------------------------------------------- W gradient
+
+// Instruction j of the gradient: gW_j[u, w] = sum_{n, m} x[n, xo + m mi + u]
+// g[n, go + m mo + w]; tile0 = first 32 x 32 tile of j in the flat tile list.
+struct LinGrad {
+    int xo, mi, go, mo, d, w_off, tile0;
+};
+constexpr int kLinMaxGrad = 128;
+struct LinGradDesc {
+    int ninstr, ntiles;
+    int64_t x_stride, g_stride, nw;
+    LinGrad g[kLinMaxGrad];
+};
+
+constexpr int kLgRows = 32;  // rows staged per step
+
+// grid: x = tile (instruction, u tile, w tile), y = row split.  Split s covers
+// items [s * per, (s + 1) * per) and writes its partial sums to
+// partial[s * nw + ...]; every partial element is written.
+template <typename T>
+__global__ void __launch_bounds__(256)
+linear_wgrad_kernel(const __grid_constant__ LinGradDesc D, int64_t n, int64_t per,
+                    const T* __restrict__ x, const T* __restrict__ g, T* __restrict__ partial) {
+    int j = 0;
+    while (j + 1 < D.ninstr && D.g[j + 1].tile0 <= (int)blockIdx.x) ++j;
+    const LinGrad& G = D.g[j];
+    const int t = blockIdx.x - G.tile0;
+    const int ntw = (G.mo + 31) / 32;
+    const int u0 = (t / ntw) * 32, w0 = (t % ntw) * 32;
+    const int tid = threadIdx.x, ty = tid >> 5, tx = tid & 31;
+    __shared__ T Xs[kLgRows][33];
+    __shared__ T Gs[kLgRows][33];
+    T acc[4] = {(T)0, (T)0, (T)0, (T)0};
+    const int64_t i0 = (int64_t)blockIdx.y * per;
+    const int64_t i1 = min(n, i0 + per);
+    const int64_t r0 = i0 * G.d, r1 = i1 > i0 ? i1 * G.d : r0;
+    for (int64_t rb = r0; rb < r1; rb += kLgRows) {
+        __syncthreads();
+        for (int i = tid; i < kLgRows * 32; i += 256) {
+            const int r = i >> 5, c = i & 31;
+            const int64_t R = rb + r;
+            T xv = (T)0, gv = (T)0;
+            if (R < r1) {
+                const int64_t item = R / G.d;
+                const int m = (int)(R % G.d);
+                if (u0 + c < G.mi) xv = x[item * D.x_stride + G.xo + (int64_t)m * G.mi + u0 + c];
+                if (w0 + c < G.mo) gv = g[item * D.g_stride + G.go + (int64_t)m * G.mo + w0 + c];
+            }
+            Xs[r][c] = xv;
+            Gs[r][c] = gv;
+        }
+        __syncthreads();
+#pragma unroll 8
+        for (int r = 0; r < kLgRows; ++r) {
+            const T gv = Gs[r][tx];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) acc[q] = fma(Xs[r][ty * 4 + q], gv, acc[q]);
+        }
+    }
+    T* P = partial + (int64_t)blockIdx.y * D.nw + G.w_off;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const int u = u0 + ty * 4 + q, w = w0 + tx;
+        if (u < G.mi && w < G.mo) P[(int64_t)u * G.mo + w] = acc[q];
+    }
+}
+
+// ------------------------------------------------------------ tensor cores
+
+constexpr int kLtM = 128;                    // rows per tile (MMA M, TMEM lanes)
+constexpr int kLtK = 32;                     // K per chunk
+constexpr int kLtThreads = 128;              // four warps: loaders, epilogue; thread 0 issues
+constexpr unsigned kLtA = kLtM * kLtK * 4;   // one TF32 part of an A chunk (16 KB)
+
+__host__ __device__ constexpr unsigned lt_stage_bytes(int nmax) {
+    return 2 * kLtA + 2u * (unsigned)nmax * kLtK * 4;  // A hi, A lo, B hi + lo
+}
+
+// Packed B image of every chunk: rows = output columns c < ncols, K-major
+// core matrices, the TF32 hi part then the lo part (ncols * 32 * 4 bytes each).
+// grid: x = chunk.
+__global__ void linear_pack_kernel(const __grid_constant__ LinDesc D, const float* __restrict__ W,
+                                   unsigned char* __restrict__ img) {
+    const int ci = blockIdx.x;
+    int b = 0;
+    while (b + 1 < D.nblocks && D.blk[b + 1].chunk0 <= ci) ++b;
+    const int N = D.blk[b].ncols;
+    const LinChunk& C = D.ch[ci];
+    unsigned char* base = img + C.img_off;
+    const unsigned part = (unsigned)N * kLtK * 4;
+    for (int i = threadIdx.x; i < N * kLtK; i += blockDim.x) {
+        const int c = i / kLtK, k = i % kLtK;
+        const float v =
+            k < C.kc ? W[C.w_off + (int64_t)(C.k0 + k) * C.w_ks + (int64_t)c * C.w_ns] : 0.0f;
+        const float hi = to_tf32(v), lo = to_tf32(v - hi);
+        const unsigned o = kmajor_offset(c, k, N);
+        *reinterpret_cast<float*>(base + o) = hi;
+        *reinterpret_cast<float*>(base + part + o) = lo;
+    }
+}
+
+// Work units are (block, 128-row tile) pairs, blocks in order; CTA c takes
+// units c, c + grid, ...  Chunk k of this CTA (counted over all its units)
+// uses stage k % 2 and phase (k / 2) % 2 of a_full, b_full and mma_done; unit
+// t uses phase t % 2 of acc_full.  Every wait is bounded; after a timeout the
+// remaining waits return at once, the CTA finishes its current unit without
+// issuing more copies or MMAs, drains what it issued and exits.
+__global__ void __launch_bounds__(kLtThreads, 1)
+linear_tc_kernel(const __grid_constant__ LinDesc D, int64_t n, int nmax, unsigned tmem_cols,
+                 const float* __restrict__ x, const unsigned char* __restrict__ img,
+                 float* __restrict__ out) {
+    extern __shared__ __align__(1024) unsigned char smem[];
+    __shared__ __align__(8) unsigned long long a_full[2], b_full[2], mma_done[2], acc_full;
+    __shared__ unsigned tmem_base;
+    __shared__ int fail;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const unsigned stage_bytes = lt_stage_bytes(nmax);
+
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_addr(&tmem_base)),
+                     "r"(tmem_cols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    if (tid == 0) {
+        for (int i = 0; i < 2; ++i) {
+            tc_mbar_init(&a_full[i], kLtThreads);
+            tc_mbar_init(&b_full[i], 1);
+            tc_mbar_init(&mma_done[i], 1);
+        }
+        tc_mbar_init(&acc_full, 1);
+        fail = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    const unsigned tmem = tmem_base;
+
+    auto wait = [&](unsigned long long* bar, unsigned parity) -> bool {
+        if (*(volatile int*)&fail) return false;
+        if (tc_mbar_wait(bar, parity)) return true;
+        atomicExch(&fail, 1);
+        return false;
+    };
+    // unit u -> (block b, tile t)
+    auto locate = [&](int64_t u, int& b, int64_t& t) -> bool {
+        for (b = 0; b < D.nblocks; ++b) {
+            const int64_t tb = (n * D.blk[b].d + kLtM - 1) / kLtM;
+            if (u < tb) {
+                t = u;
+                return true;
+            }
+            u -= tb;
+        }
+        return false;
+    };
+    // rows 32 warp + 4 i + lane / 8, columns 4 (lane % 8) .. + 3 of a chunk
+    auto load = [&](int b, int64_t t, int ci, float4 (&v)[8]) {
+        const LinBlock& B = D.blk[b];
+        const LinChunk& C = D.ch[B.chunk0 + ci];
+        const int64_t rows = n * B.d;
+        const int k4 = (lane & 7) * 4;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int64_t R = t * kLtM + 32 * warp + 4 * i + (lane >> 3);
+            v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (R < rows && k4 < C.kc) {
+                const int64_t item = R / B.d;
+                const int m = (int)(R % B.d);
+                v[i] = *reinterpret_cast<const float4*>(
+                    x + item * D.in_stride + C.a_off + (int64_t)m * C.a_mul + C.k0 + k4);
+            }
+        }
+    };
+
+    int64_t u = blockIdx.x, t = 0;
+    int b = 0, ci = 0;
+    bool valid = locate(u, b, t);
+    float4 nxt[8];
+    if (valid) load(b, t, 0, nxt);
+    int64_t k = 0, units = 0;
+    int b_issued[2] = {0, 0}, b_waited[2] = {0, 0};
+    int64_t last_commit = -1;
+    while (valid) {
+        const int s = (int)(k & 1);
+        unsigned char* st = smem + (size_t)s * stage_bytes;
+        const LinBlock& B = D.blk[b];
+        const LinChunk& C = D.ch[B.chunk0 + ci];
+        const int N = B.ncols;
+        const unsigned bbytes = 2u * (unsigned)N * kLtK * 4;
+        // stage s is free once the MMAs of chunk k - 2 have completed
+        if (k >= 2) wait(&mma_done[s], (unsigned)(((k - 2) >> 1) & 1));
+        if (tid == 0 && !*(volatile int*)&fail) {
+            tc_expect_tx(&b_full[s], bbytes);
+            tc_bulk_g2s(st + 2 * kLtA, img + C.img_off, bbytes, &b_full[s]);
+            ++b_issued[s];
+        }
+        {
+            const int k4 = (lane & 7) * 4;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int r = 32 * warp + 4 * i + (lane >> 3);
+                const float in[4] = {nxt[i].x, nxt[i].y, nxt[i].z, nxt[i].w};
+                float hi[4], lo[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    hi[q] = to_tf32(in[q]);
+                    lo[q] = to_tf32(in[q] - hi[q]);
+                }
+                const unsigned off = kmajor_offset(r, k4, kLtM);
+                *reinterpret_cast<float4*>(st + off) = make_float4(hi[0], hi[1], hi[2], hi[3]);
+                *reinterpret_cast<float4*>(st + kLtA + off) = make_float4(lo[0], lo[1], lo[2], lo[3]);
+            }
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        tc_mbar_arrive(&a_full[s]);
+        // advance, then fetch the next chunk's rows while this one multiplies
+        const bool first = ci == 0, last = ci + 1 == B.nchunk;
+        const int eb = b;
+        const int64_t et = t;
+        if (!last) {
+            ++ci;
+        } else {
+            u += gridDim.x;
+            valid = locate(u, b, t);
+            ci = 0;
+        }
+        if (valid) load(b, t, ci, nxt);
+        if (tid == 0) {
+            const unsigned ph = (unsigned)((k >> 1) & 1);
+            const bool okb = wait(&b_full[s], ph);
+            if (okb) ++b_waited[s];
+            if (wait(&a_full[s], ph) && okb) {
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                const uint32_t idesc = tf32_idesc(kLtM, N);
+                const unsigned la = (kLtM / 8) * 128, lb = (unsigned)(N / 8) * 128;
+                const unsigned a0 = smem_addr(st), b0 = smem_addr(st + 2 * kLtA);
+                const unsigned bpart = (unsigned)N * kLtK * 4;
+#pragma unroll
+                for (int k8 = 0; k8 < kLtK; k8 += 8) {
+                    const unsigned ka = (unsigned)(k8 >> 2) * la, kb = (unsigned)(k8 >> 2) * lb;
+                    const uint64_t ah = smem_desc(a0 + ka, la, 128);
+                    const uint64_t al = smem_desc(a0 + kLtA + ka, la, 128);
+                    const uint64_t bh = smem_desc(b0 + kb, lb, 128);
+                    const uint64_t bl = smem_desc(b0 + bpart + kb, lb, 128);
+                    mma_tf32_n(tmem, ah, bh, idesc, (first && k8 == 0) ? 0u : 1u);
+                    mma_tf32_n(tmem, ah, bl, idesc, 1u);
+                    mma_tf32_n(tmem, al, bh, idesc, 1u);
+                }
+                tc_commit(&mma_done[s]);
+                if (last) tc_commit(&acc_full);
+                last_commit = k;
+            }
+        }
+        if (last) {
+            // epilogue: warp w holds rows 32 w .. 32 w + 31 (one per lane)
+            bool got = wait(&acc_full, (unsigned)(units & 1));
+            got = __all_sync(0xffffffffu, got);
+            if (got) {
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                const LinBlock& EB = D.blk[eb];
+                const int64_t R = et * kLtM + 32 * warp + lane;
+                const bool live = R < n * EB.d;
+                float* o = out;
+                if (live) {
+                    const int64_t item = R / EB.d;
+                    const int m = (int)(R % EB.d);
+                    o = out + item * D.out_stride + EB.out_off + (int64_t)m * EB.ncols;
+                }
+                for (int c0 = 0; c0 < EB.ncols; c0 += 32) {
+                    float v[32];
+                    tmem_ld32(tmem + ((unsigned)(32 * warp) << 16) + (unsigned)c0, v);
+                    if (live) {
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            *reinterpret_cast<float4*>(o + c0 + 4 * q) =
+                                make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                    }
+                }
+            }
+            ++units;
+            asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+            __syncthreads();
+            if (*(volatile int*)&fail) break;
+        }
+        ++k;
+    }
+    // drain: copies issued but never waited for, and the last committed MMAs
+    if (tid == 0) {
+        for (int q = 0; q < 2; ++q)
+            while (b_waited[q] < b_issued[q]) {
+                tc_mbar_wait(&b_full[q], (unsigned)(b_waited[q] & 1));
+                ++b_waited[q];
+            }
+        if (last_commit >= 0)
+            tc_mbar_wait(&mma_done[last_commit & 1], (unsigned)((last_commit >> 1) & 1));
+        if (fail) atomicExch(&cgtp_linear_error, 1);
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    if (warp == 0)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(tmem_cols)
+                     : "memory");
+}
+
+// ------------------------------------------------------------------- host
+
+struct LinearImpl {
+    std::vector<Irrep> in, out;
+    std::vector<int> off_in, off_out;
+    std::vector<std::pair<int, int>> instr;  // (input irrep, output irrep)
+    std::vector<int64_t> w_off;
+    int64_t dim_in = 0, dim_out = 0, nw = 0;
+    cgtp_dtype dtype = CGTP_F32;
+    LinDesc fwd{}, bwd{};  // forward (blocks = outputs) and x gradient (blocks = inputs)
+    std::vector<std::pair<int, int>> fwd_zero, bwd_zero;  // unreached blocks: (offset, width)
+    LinGradDesc grad{};
+    bool tc = false;
+    size_t fwd_img = 0, bwd_img = 0;
+    int fwd_nmax = 0, bwd_nmax = 0;
+};
+
+static size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Blocks of one pass: for every target irrep reached by an instruction, its
+// chunks (instruction order, 32 source channels each).  fwd: target = output.
+static bool build_pass(LinearImpl& L, bool fwd, std::string& err) {
+    LinDesc& D = fwd ? L.fwd : L.bwd;
+    auto& zero = fwd ? L.fwd_zero : L.bwd_zero;
+    const auto& tgt = fwd ? L.out : L.in;
+    const auto& toff = fwd ? L.off_out : L.off_in;
+    D.in_stride = fwd ? L.dim_in : L.dim_out;
+    D.out_stride = fwd ? L.dim_out : L.dim_in;
+    D.nblocks = D.nchunks = 0;
+    size_t img = 0;
+    int nmax = 0;
+    for (int t = 0; t < (int)tgt.size(); ++t) {
+        const int ncols = tgt[t].mul, d = 2 * tgt[t].l + 1;
+        const int c0 = D.nchunks;
+        for (int j = 0; j < (int)L.instr.size(); ++j) {
+            const int src = fwd ? L.instr[j].first : L.instr[j].second;
+            if ((fwd ? L.instr[j].second : L.instr[j].first) != t) continue;
+            const int mi = L.in[L.instr[j].first].mul, mo = L.out[L.instr[j].second].mul;
+            const int ksrc = fwd ? mi : mo;
+            for (int k0 = 0; k0 < ksrc; k0 += kLtK) {
+                if (D.nchunks >= kLinMaxChunks) {
+                    err = "too many weight chunks for one linear layer";
+                    return false;
+                }
+                LinChunk& C = D.ch[D.nchunks++];
+                C.a_off = fwd ? L.off_in[src] : L.off_out[src];
+                C.a_mul = ksrc;
+                C.k0 = k0;
+                C.kc = std::min(kLtK, ksrc - k0);
+                C.w_off = (int)L.w_off[j];
+                C.w_ks = fwd ? mo : 1;
+                C.w_ns = fwd ? 1 : mo;
+                C.img_off = (int)img;
+                img += (size_t)2 * ncols * kLtK * 4;
+            }
+        }
+        if (D.nchunks == c0) {
+            zero.emplace_back(toff[t], ncols * d);
+            continue;
+        }
+        if (D.nblocks >= kLinMaxBlocks) {
+            err = "too many irreps for one linear layer";
+            return false;
+        }
+        D.blk[D.nblocks++] = LinBlock{toff[t], ncols, d, c0, D.nchunks - c0};
+        nmax = std::max(nmax, ncols);
+    }
+    (fwd ? L.fwd_img : L.bwd_img) = img;
+    (fwd ? L.fwd_nmax : L.bwd_nmax) = nmax;
+    return true;
+}
+
+cgtp_status linear_create(const char* sin, const char* sout, const cgtp_linear_instr* instr,
+                          int n_instr, cgtp_dtype dt, LinearImpl** res, std::string& err) {
+    auto L = std::make_unique<LinearImpl>();
+    if (!parse_irreps(sin, L->in, err) || !parse_irreps(sout, L->out, err)) return CGTP_E_IRREPS;
+    L->dtype = dt;
+    for (auto* v : {&L->in, &L->out}) {
+        int64_t off = 0;
+        auto& offs = v == &L->in ? L->off_in : L->off_out;
+        for (const Irrep& r : *v) {
+            offs.push_back((int)off);
+            off += (int64_t)r.mul * (2 * r.l + 1);
+        }
+        (v == &L->in ? L->dim_in : L->dim_out) = off;
+    }
+    if (L->dim_in >= (1 << 30) || L->dim_out >= (1 << 30)) {
+        err = "irreps too wide";
+        return CGTP_E_IRREPS;
+    }
+    if (instr == nullptr) {
+        for (int i = 0; i < (int)L->in.size(); ++i)
+            for (int o = 0; o < (int)L->out.size(); ++o)
+                if (L->in[i].l == L->out[o].l && L->in[i].parity == L->out[o].parity)
+                    L->instr.emplace_back(i, o);
+    } else {
+        if (n_instr < 0) {
+            err = "negative instruction count";
+            return CGTP_E_ARG;
+        }
+        for (int j = 0; j < n_instr; ++j) {
+            const int i = instr[j].i_in, o = instr[j].i_out;
+            if (i < 0 || i >= (int)L->in.size() || o < 0 || o >= (int)L->out.size()) {
+                err = "instruction " + std::to_string(j) + " indexes outside the irreps";
+                return CGTP_E_PATH;
+            }
+            if (L->in[i].l != L->out[o].l || L->in[i].parity != L->out[o].parity) {
+                err = "instruction " + std::to_string(j) + " joins irreps of different l or parity";
+                return CGTP_E_PATH;
+            }
+            L->instr.emplace_back(i, o);
+        }
+    }
+    if ((int)L->instr.size() > kLinMaxGrad) {
+        err = "too many instructions for one linear layer";
+        return CGTP_E_UNSUPPORTED;
+    }
+    for (auto& [i, o] : L->instr) {
+        L->w_off.push_back(L->nw);
+        L->nw += (int64_t)L->in[i].mul * L->out[o].mul;
+    }
+    if (L->nw >= (1ll << 31)) {
+        err = "weights too large";
+        return CGTP_E_UNSUPPORTED;
+    }
+    if (!build_pass(*L, true, err) || !build_pass(*L, false, err)) return CGTP_E_UNSUPPORTED;
+    // gradient in W
+    LinGradDesc& G = L->grad;
+    G.ninstr = (int)L->instr.size();
+    G.x_stride = L->dim_in;
+    G.g_stride = L->dim_out;
+    G.nw = L->nw;
+    int tiles = 0;
+    for (int j = 0; j < G.ninstr; ++j) {
+        const auto [i, o] = L->instr[j];
+        G.g[j] = LinGrad{L->off_in[i], L->in[i].mul, L->off_out[o], L->out[o].mul,
+                         2 * L->in[i].l + 1, (int)L->w_off[j], tiles};
+        tiles += ((L->in[i].mul + 31) / 32) * ((L->out[o].mul + 31) / 32);
+    }
+    G.ntiles = tiles;
+    bool tc = dt == CGTP_F32;
+    for (const auto* v : {&L->in, &L->out})
+        for (const Irrep& r : *v) tc = tc && r.mul % 32 == 0 && r.mul <= 256;
+    L->tc = tc;
+    *res = L.release();
+    return CGTP_OK;
+}
+
+void linear_destroy(LinearImpl* L) { delete L; }
+
+void linear_info(const LinearImpl* L, int64_t* dim_in, int64_t* dim_out, int64_t* nw, int* ni) {
+    if (dim_in) *dim_in = L->dim_in;
+    if (dim_out) *dim_out = L->dim_out;
+    if (nw) *nw = L->nw;
+    if (ni) *ni = (int)L->instr.size();
+}
+
+bool linear_instruction(const LinearImpl* L, int j, int* i_in, int* i_out, int64_t* w_off) {
+    if (j < 0 || j >= (int)L->instr.size()) return false;
+    if (i_in) *i_in = L->instr[j].first;
+    if (i_out) *i_out = L->instr[j].second;
+    if (w_off) *w_off = L->w_off[j];
+    return true;
+}
+
+bool linear_tensor_cores(const LinearImpl* L) { return L->tc; }
+
+// Row splits of the W gradient: partial sums per split, added in split order.
+static int64_t wgrad_splits(int64_t n) { return std::max<int64_t>(1, std::min<int64_t>(64, (n + 63) / 64)); }
+
+size_t linear_fwd_workspace(const LinearImpl* L) { return L->tc ? L->fwd_img : 0; }
+
+size_t linear_bwd_workspace(const LinearImpl* L, int64_t n) {
+    const size_t es = L->dtype == CGTP_F64 ? 8 : 4;
+    return round_up(L->tc ? L->bwd_img : 0, 256) + (size_t)wgrad_splits(n) * L->nw * es;
+}
+
+static int sm_count() {
+    int dev = 0, v = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+        return 148;
+    return v;
+}
+
+static bool aligned16(const void* p) { return ((uintptr_t)p & 15) == 0; }
+
+template <typename T>
+static cudaError_t zero_blocks(const std::vector<std::pair<int, int>>& z, int64_t n, int64_t stride,
+                               T* out, cudaStream_t s) {
+    for (auto [off, width] : z) {
+        const int64_t total = n * width;
+        if (total == 0) continue;
+        const unsigned g = (unsigned)std::min<int64_t>((total + 255) / 256, 4096);
+        linear_zero_kernel<T><<<g, 256, 0, s>>>(n, stride, off, width, out);
+    }
+    return cudaGetLastError();
+}
+
+// One GEMM pass (forward or x gradient) into `out`.
+static cudaError_t run_pass(const LinearImpl& L, const LinDesc& D, int nmax, size_t img_bytes,
+                            int64_t n, const void* a, const void* W, void* out, void* img,
+                            bool use_tc, cudaStream_t s) {
+    if (D.nblocks == 0 || n == 0) return cudaSuccess;
+    if (L.dtype == CGTP_F64) {
+        int dmax = 1;
+        for (int b = 0; b < D.nblocks; ++b) dmax = std::max(dmax, D.blk[b].d);
+        const dim3 g((unsigned)((n * dmax + kLsT - 1) / kLsT), (unsigned)((nmax + kLsC - 1) / kLsC),
+                     (unsigned)D.nblocks);
+        linear_simt_kernel<double><<<g, kLsThreads, 0, s>>>(D, n, (const double*)a,
+                                                            (const double*)W, (double*)out);
+        return cudaGetLastError();
+    }
+    if (!use_tc) {
+        int dmax = 1;
+        for (int b = 0; b < D.nblocks; ++b) dmax = std::max(dmax, D.blk[b].d);
+        const dim3 g((unsigned)((n * dmax + kLsT - 1) / kLsT), (unsigned)((nmax + kLsC - 1) / kLsC),
+                     (unsigned)D.nblocks);
+        linear_simt_kernel<float><<<g, kLsThreads, 0, s>>>(D, n, (const float*)a, (const float*)W,
+                                                           (float*)out);
+        return cudaGetLastError();
+    }
+    linear_pack_kernel<<<(unsigned)D.nchunks, 256, 0, s>>>(D, (const float*)W, (unsigned char*)img);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    int64_t units = 0;
+    for (int b = 0; b < D.nblocks; ++b) units += (n * D.blk[b].d + kLtM - 1) / kLtM;
+    const unsigned grid = (unsigned)std::min<int64_t>(units, sm_count());
+    unsigned cols = 32;
+    while ((int)cols < nmax) cols <<= 1;
+    const size_t smem = 2 * (size_t)lt_stage_bytes(nmax);
+    e = cudaFuncSetAttribute(linear_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    (void)img_bytes;
+    linear_tc_kernel<<<grid, kLtThreads, smem, s>>>(D, n, nmax, cols, (const float*)a,
+                                                    (const unsigned char*)img, (float*)out);
+    return cudaGetLastError();
+}
+
+bool linear_uses_tc(const LinearImpl* L, int64_t n, const void* a, const void* out, const void* ws,
+                    size_t ws_bytes, bool fwd) {
+    (void)n;
+    return L->tc && ws && ws_bytes >= (fwd ? L->fwd_img : L->bwd_img) && aligned16(a) &&
+           aligned16(out) && aligned16(ws);
+}
+
+cudaError_t launch_linear_forward(const LinearImpl* L, int64_t n, const void* x, const void* W,
+                                  void* out, void* ws, size_t ws_bytes, bool allow_tc,
+                                  cudaStream_t s) {
+    cudaError_t e = L->dtype == CGTP_F64
+                        ? zero_blocks(L->fwd_zero, n, L->dim_out, (double*)out, s)
+                        : zero_blocks(L->fwd_zero, n, L->dim_out, (float*)out, s);
+    if (e != cudaSuccess) return e;
+    const bool tc = allow_tc && linear_uses_tc(L, n, x, out, ws, ws_bytes, true);
+    return run_pass(*L, L->fwd, L->fwd_nmax, L->fwd_img, n, x, W, out, ws, tc, s);
+}
+
+cudaError_t launch_linear_backward(const LinearImpl* L, int64_t n, const void* x, const void* W,
+                                   const void* g, void* gx, void* gW, void* ws, size_t ws_bytes,
+                                   bool allow_tc, cudaStream_t s) {
+    const bool f64 = L->dtype == CGTP_F64;
+    cudaError_t e = cudaSuccess;
+    if (gx) {
+        e = f64 ? zero_blocks(L->bwd_zero, n, L->dim_in, (double*)gx, s)
+                : zero_blocks(L->bwd_zero, n, L->dim_in, (float*)gx, s);
+        if (e != cudaSuccess) return e;
+        const bool tc = allow_tc && linear_uses_tc(L, n, g, gx, ws, ws_bytes, false);
+        e = run_pass(*L, L->bwd, L->bwd_nmax, L->bwd_img, n, g, W, gx, ws, tc, s);
+        if (e != cudaSuccess) return e;
+    }
+    if (gW && L->nw > 0) {
+        if (n == 0) return launch_fill_zero(gW, L->nw * (f64 ? 8 : 4), s);
+        const int64_t S = wgrad_splits(n), per = (n + S - 1) / S;
+        unsigned char* part = (unsigned char*)ws + round_up(L->tc ? L->bwd_img : 0, 256);
+        const dim3 grid((unsigned)L->grad.ntiles, (unsigned)S);
+        if (f64)
+            linear_wgrad_kernel<double><<<grid, 256, 0, s>>>(L->grad, n, per, (const double*)x,
+                                                             (const double*)g, (double*)part);
+        else
+            linear_wgrad_kernel<float><<<grid, 256, 0, s>>>(L->grad, n, per, (const float*)x,
+                                                            (const float*)g, (float*)part);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        e = launch_reduce_rows(f64, part, S, L->nw, gW, s);
+    }
+    return e;
+}
+
+cudaError_t linear_device_status(int* code) {
+    int zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(code, cgtp_linear_error, sizeof(int));
+    if (e == cudaSuccess) e = cudaMemcpyToSymbol(cgtp_linear_error, &zero, sizeof(int));
+    return e;
+}
+
+}  // namespace cgtp

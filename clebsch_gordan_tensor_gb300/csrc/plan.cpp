@@ -24,7 +24,7 @@ static constexpr int kMaxL = 6;
 
 // ------------------------------------------------------------------ irreps
 
-static bool parse_irreps(const char* s, std::vector<Irrep>& out, std::string& err) {
+bool parse_irreps(const char* s, std::vector<Irrep>& out, std::string& err) {
     out.clear();
     if (!s) {
         err = "irreps string is NULL";

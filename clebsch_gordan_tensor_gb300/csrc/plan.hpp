@@ -81,6 +81,8 @@ struct Plan {
 // plan.cpp
 cgtp_status build_plan(Plan& p, const char* s1, const char* s2, const char* so,
                        const cgtp_instr* instr, int n_instr, std::string& err);
+// "16x0e+16x1o" -> irreps; false (with a message) on a syntax error.
+bool parse_irreps(const char* s, std::vector<Irrep>& out, std::string& err);
 // Real-basis CG tensor (dense, layout as Path::cg); false if the triangle fails.
 bool real_cg(int l1, int l2, int l3, std::vector<double>& out);
 

@@ -283,6 +283,71 @@ cgtp_status cgtp_edge_forces_adjoint(cgtp_dtype dtype, int64_t N, int64_t E,
                                      const int32_t* rowptr, const int32_t* sender,
                                      const void* grad_forces, void* grad_dEdr, cgtp_stream stream);
 
+/* ------------------------------------------- channel mixing (linear) ---- */
+/* Per-irrep channel mixing, the dense 'uvw' contraction of a TFN layer: the
+ * pairwise degree convolutions are summed per output degree and the fused
+ * layers concatenate degrees so that the channel contractions become dense
+ * products whose sizes are multiples of 16, for the tensor cores (NVIDIA
+ * SE(3)-Transformer blog, "TFN fusion").  For each instruction j joining
+ * input irrep i_in and output irrep i_out of the same l and parity, with the
+ * matrix W_j [mul_in][mul_out] (row-major; instructions stored one after
+ * another):
+ *   out[n, i_out, m, w] += sum_u x[n, i_in, m, u] W_j[u, w]     (m = -l..l)
+ * Outputs no instruction reaches are zero.  No normalisation is applied.
+ * Rows use the library's layout: irrep blocks in order, [2l+1][mul] inside.
+ * A 'uvw' tensor product with one matrix per path (shared by all rows) is the
+ * 'uvu' product into one output irrep per path with a shared weight row of
+ * ones, followed by this layer with instruction p joining path p's output to
+ * the path's target irrep. */
+typedef struct cgtp_linear_s* cgtp_linear;
+typedef struct {
+    int i_in, i_out;
+} cgtp_linear_instr;
+/* instr NULL: every (i_in, i_out) pair with equal l and parity, input-major.
+ * Host only; the handle is immutable and may be shared between threads. */
+cgtp_status cgtp_linear_create(cgtp_linear* out, const char* irreps_in, const char* irreps_out,
+                               const cgtp_linear_instr* instr, int n_instr, cgtp_dtype dtype);
+cgtp_status cgtp_linear_destroy(cgtp_linear lin);
+cgtp_status cgtp_linear_info(cgtp_linear lin, int64_t* dim_in, int64_t* dim_out,
+                             int64_t* weight_numel, int* n_instr);
+/* Instruction j: its irreps and the offset of W_j in the weight vector. */
+cgtp_status cgtp_linear_instruction(cgtp_linear lin, int j, int* i_in, int* i_out,
+                                    int64_t* weight_offset);
+/* Workspace bytes: fwd for cgtp_linear_forward (0: none is used), bwd for
+ * cgtp_linear_backward with n rows. */
+cgtp_status cgtp_linear_workspace(cgtp_linear lin, int64_t n, size_t* fwd_bytes,
+                                  size_t* bwd_bytes);
+/* Host query: *tensor_cores = 1 if fp32 and every multiplicity is a multiple
+ * of 32 and at most 256 (the tcgen05 path, given a workspace and 16-byte
+ * aligned tensors). */
+cgtp_status cgtp_linear_path(cgtp_linear lin, int* tensor_cores);
+/* flags & CGTP_LINEAR_CUDA_CORES: use the CUDA-core kernels. */
+#define CGTP_LINEAR_CUDA_CORES 1u
+/* out [n, dim_out] = the layer applied to x [n, dim_in] with weights W
+ * [weight_numel]; device, caller-owned, `dtype`, out overwritten.  On the
+ * tensor-core path (see cgtp_linear_path; needs a 16-byte aligned workspace of
+ * at least fwd_bytes, whose contents need not be set) each product runs as
+ * TF32 hi*hi + hi*lo + lo*hi on tcgen05 with fp32 accumulation; calls sharing
+ * a workspace must not overlap in time.  Otherwise, and for fp64, the CUDA
+ * cores.  Asynchronous on `stream`; allocates nothing. */
+cgtp_status cgtp_linear_forward(cgtp_linear lin, int64_t n, const void* x, const void* W,
+                                void* out, void* workspace, size_t workspace_bytes,
+                                unsigned flags, cgtp_stream stream);
+/* Gradients for the cotangent grad_out [n, dim_out]: grad_x [n, dim_in]
+ * (= grad_out through the transposed matrices, the tensor-core path as in the
+ * forward) and grad_W [weight_numel] (= sum over rows of x^T grad_out per
+ * instruction, per-CTA partial sums in the workspace added in fixed order:
+ * deterministic); either may be NULL (not computed).  The workspace (at least
+ * bwd_bytes, 16-byte aligned) is required when grad_W is requested. */
+cgtp_status cgtp_linear_backward(cgtp_linear lin, int64_t n, const void* x, const void* W,
+                                 const void* grad_out, void* grad_x, void* grad_W,
+                                 void* workspace, size_t workspace_bytes, unsigned flags,
+                                 cgtp_stream stream);
+/* Device status of the tensor-core kernel: *code = 1 if a bounded wait timed
+ * out since the last query (the results of that call are invalid), then
+ * cleared.  Synchronous. */
+cgtp_status cgtp_linear_device_status(int* code);
+
 /* --------------------------------------------------- radial network ---- */
 /* Per-edge tensor-product weights from the radial network: the radial profile
  * of a TFN layer is a fully connected network of the edge length (NVIDIA

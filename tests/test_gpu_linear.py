@@ -1,0 +1,104 @@
+"""GPU parity of the per-irrep channel mixing (tcgen05 and CUDA-core kernels)
+and of the 'uvw' tensor product built on it, against the oracle."""
+import numpy as np
+import pytest
+
+import oracle as O
+from tests.gpu_util import assert_close, dev, host, need_gpu, torch
+
+pytestmark = pytest.mark.gpu
+
+# several 128-row tiles with a ragged tail; an input irrep used twice, an
+# output irrep reached by two instructions and one reached by none
+LIN = ("32x0e+32x1o+64x1o+32x2e", "64x0e+32x1o+32x2e+32x3o")
+LIN_WIDE = ("128x0e+128x1o+256x2e", "256x0e+128x1o+128x2e")
+
+
+def _cg():
+    import clebsch_gordan_tensor_gb300 as cg
+    return cg
+
+
+def _problem(rng, irreps, n, dt):
+    instr = O.linear_instructions(*irreps)
+    a, b = O.parse_irreps(irreps[0]), O.parse_irreps(irreps[1])
+    nw = sum(a[i][0] * b[o][0] for i, o in instr)
+    x = rng.standard_normal((n, O.irreps_dim(a))).astype(dt)
+    W = (rng.standard_normal(nw) / 8).astype(dt)
+    g = rng.standard_normal((n, O.irreps_dim(b))).astype(dt)
+    return instr, x, W, g
+
+
+@pytest.mark.parametrize("irreps", [LIN, LIN_WIDE], ids=["mixed", "wide"])
+@pytest.mark.parametrize("n", [1, 333])
+@pytest.mark.parametrize("path", ["tensor", "cuda", "fp64"])
+def test_linear_forward_backward(irreps, n, path):
+    need_gpu()
+    cg = _cg()
+    dt = np.float64 if path == "fp64" else np.float32
+    tdt = torch.float64 if path == "fp64" else torch.float32
+    rng = np.random.default_rng(n)
+    instr, x, W, g = _problem(rng, irreps, n, dt)
+    lin = cg.Linear(*irreps, dtype=tdt)
+    assert lin.tensor_cores == (path != "fp64")
+    cc = path == "cuda"
+    out = lin.forward(dev(x), dev(W), cuda_cores=cc)
+    assert_close(host(out), O.linear_forward(*irreps, instr, x, W), dt, "out")
+    gx, gW = lin.backward(dev(x), dev(W), dev(g), cuda_cores=cc)
+    rx, rW = O.linear_backward(*irreps, instr, x, W, g)
+    assert_close(host(gx), rx, dt, "grad_x")
+    assert_close(host(gW), rW, dt, "grad_W")
+    assert cg.linear_device_status() == 0
+
+
+def test_linear_unaligned_input_takes_cuda_cores():
+    """An 8-byte (not 16-byte) aligned x is served by the CUDA-core kernel."""
+    need_gpu()
+    cg = _cg()
+    rng = np.random.default_rng(5)
+    instr, x, W, _ = _problem(rng, LIN, 200, np.float32)
+    buf = torch.zeros(x.size + 2, device="cuda")
+    xv = buf[2:].view(x.shape)
+    xv.copy_(dev(x))
+    assert xv.data_ptr() % 16 == 8
+    lin = cg.Linear(*LIN)
+    assert_close(host(lin.forward(xv, dev(W))), O.linear_forward(*LIN, instr, x, W), np.float32,
+                 "out")
+
+
+def test_linear_empty_and_repeat():
+    need_gpu()
+    cg = _cg()
+    lin = cg.Linear(*LIN)
+    x = torch.zeros(0, lin.dim_in, device="cuda")
+    W = torch.randn(lin.weight_numel, device="cuda")
+    assert lin.forward(x, W).shape == (0, lin.dim_out)
+    gx, gW = lin.backward(x, W, torch.zeros(0, lin.dim_out, device="cuda"))
+    assert gx.shape == x.shape and not host(gW).any()
+    # the same workspace reused by consecutive calls gives identical results
+    rng = np.random.default_rng(6)
+    instr, xn, Wn, _ = _problem(rng, LIN, 1000, np.float32)
+    ws = torch.empty(lin.workspace_bytes(1000)[0], dtype=torch.uint8, device="cuda")
+    a = lin.forward(dev(xn), dev(Wn), workspace=ws).clone()
+    b = lin.forward(dev(xn), dev(Wn), workspace=ws)
+    assert torch.equal(a, b)
+
+
+UVW_SMALL = ("32x0e+32x1o+32x2e", "0e+1o+2e+3o", "64x0e+32x1o+32x1e+32x2o+32x2e+32x3o+32x3e")
+
+
+def test_uvw_product_matches_oracle():
+    """'uvw' = per-path 'uvu' blocks (unit shared weights) + channel mixing,
+    against the oracle's direct definition."""
+    need_gpu()
+    cg = _cg()
+    rng = np.random.default_rng(7)
+    B = 300
+    uvw = cg.UVWProduct(*UVW_SMALL)
+    x = rng.standard_normal((B, uvw.dim_in1)).astype(np.float32)
+    v = rng.standard_normal((B, 3)).astype(np.float32)
+    W = (rng.standard_normal(uvw.weight_numel) / 16).astype(np.float32)
+    y = cg.sh_forward(dev(v), 3)
+    out = uvw.forward(dev(x), y, dev(W))
+    ref = O.tp_uvw_forward(*UVW_SMALL, x, O.sh(3, v), W)
+    assert_close(host(out), ref, np.float32, "uvw out")

@@ -184,3 +184,30 @@ def test_generated_kernels_compile_for_sm103a(irreps, dtype):
     assert max(spills.values()) <= 256, log
     src = plan.source()
     assert "fma.rn.f32x2" in src or dtype == "f64"
+
+
+def test_linear_layer_host_side():
+    """Instruction list, weight offsets, workspace sizes and argument errors
+    of the channel-mixing layer (host only) agree with the oracle's layout."""
+    ins, outs = "32x0e+32x1o+64x1o+32x2e", "64x0e+32x1o+32x2e+32x3o"
+    lin = cg.Linear(ins, outs)
+    ref = O.linear_instructions(ins, outs)
+    assert lin.n_instr == len(ref)
+    a, b = O.parse_irreps(ins), O.parse_irreps(outs)
+    off = 0
+    for j, (i, o) in enumerate(ref):
+        assert lin.instruction(j) == (i, o, off)
+        off += a[i][0] * b[o][0]
+    assert lin.weight_numel == off
+    assert (lin.dim_in, lin.dim_out) == (O.irreps_dim(a), O.irreps_dim(b))
+    assert lin.tensor_cores
+    fb, bb = lin.workspace_bytes(1000)
+    assert fb > 0 and bb >= 4 * off
+    assert not cg.Linear("16x0e", "16x0e").tensor_cores
+    assert not cg.Linear("32x0e", "32x0e", dtype=torch.float64).tensor_cores
+    with pytest.raises(cg.CgtpError):
+        cg.Linear("4x0e", "4x1o", instr=[(0, 0)])
+    with pytest.raises(cg.CgtpError):
+        cg.Linear("4x0e", "4x0e", instr=[(0, 1)])
+    with pytest.raises(cg.CgtpError):
+        cg.Linear("4x0q", "4x0e")

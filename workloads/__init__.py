@@ -182,6 +182,17 @@ def config1(B: int = 200_000) -> dict:
     return standalone(1, CFG1, B, wdim=24 * 128, w_scale=1.0 / np.sqrt(24.0), dtype=np.float32)
 
 
+def config1_uvw(B: int = 200_000) -> dict:
+    """Config 1's samples (x, v from seed 1, as ``config1`` draws them) under a
+    'uvw' product: one [128, 128] matrix per path shared by all samples,
+    W ~ N(0,1)/sqrt(128) from seed 101 (24 paths, path-major, row-major)."""
+    cfg = config1(B)
+    cfg.pop("w")
+    rng = np.random.default_rng(101)
+    cfg["W"] = normal(rng, (24 * 128 * 128,), np.float32) * np.float32(1.0 / np.sqrt(128.0))
+    return cfg
+
+
 def conv_cloud(seed: int, irreps, N: int, n_paths: int, dtype) -> dict:
     """Fused graph convolution on a periodic atom cloud (density 0.1 / A^3,
     cutoff 5 A).  Draws, in order: positions (``periodic_cloud``); x [N, dim1]
