@@ -220,11 +220,16 @@ linear_wgrad_kernel(const __grid_constant__ LinGradDesc D, int64_t n, int64_t pe
 
 constexpr int kLtM = 128;                    // rows per tile (MMA M, TMEM lanes)
 constexpr int kLtK = 32;                     // K per chunk
-constexpr int kLtThreads = 128;              // four warps: loaders, epilogue; thread 0 issues
+constexpr int kLtEpiWarps = 4;               // one per TMEM lane quarter
+constexpr int kLtProdWarps = 8;              // 16 rows each
+constexpr int kLtProd = 32 * kLtProdWarps;
+constexpr int kLtThreads = 32 * (kLtEpiWarps + kLtProdWarps + 1);  // + the MMA issuer warp
 constexpr unsigned kLtA = kLtM * kLtK * 4;   // one TF32 part of an A chunk (16 KB)
 
-__host__ __device__ constexpr unsigned lt_stage_bytes(int nmax) {
-    return 2 * kLtA + 2u * (unsigned)nmax * kLtK * 4;  // A hi, A lo, B hi + lo
+// Dynamic shared memory: two A stages (hi, lo), RB B slots (hi + lo of up to
+// nmax rows) and RAW raw fp32 row slots.
+__host__ __device__ constexpr unsigned lt_smem_bytes(int nmax, int RB, int RAW) {
+    return 2 * 2 * kLtA + (unsigned)RB * 2u * (unsigned)nmax * kLtK * 4 + (unsigned)RAW * kLtA;
 }
 
 // Packed B image of every chunk: rows = output columns c < ncols, K-major
@@ -250,22 +255,55 @@ __global__ void linear_pack_kernel(const __grid_constant__ LinDesc D, const floa
     }
 }
 
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, unsigned src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src),
+                 "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // Work units are (block, 128-row tile) pairs, blocks in order; CTA c takes
-// units c, c + grid, ...  Chunk k of this CTA (counted over all its units)
-// uses stage k % 2 and phase (k / 2) % 2 of a_full, b_full and mma_done; unit
-// t uses phase t % 2 of acc_full.  Every wait is bounded; after a timeout the
-// remaining waits return at once, the CTA finishes its current unit without
-// issuing more copies or MMAs, drains what it issued and exits.
+// units c, c + grid, ...; every role walks the same sequence.  Warp roles:
+//   producers (warps 4-11, 16 rows each): request the raw fp32 rows of chunk
+//     k + RAW - 1 with cp.async (16 bytes per thread and row piece, slot
+//     (k + RAW - 1) % RAW, XOR-swizzled by row so that both the requests and
+//     the read-back are free of bank conflicts), then, once the MMAs of chunk
+//     k - 2 have released A stage k % 2 (a_free), split chunk k's rows into
+//     TF32 hi / lo parts in the MMA layout and arrive on a_full.  A warp reads
+//     back only rows its own lanes requested (cp.async.wait_group + syncwarp).
+//   issuer (warp 12, one thread): B chunk k arrives in ring slot k % RB by bulk
+//     copy (b_full), issued RB - 1 chunks ahead once the MMAs that read the
+//     slot have completed (b_free); it issues chunk k's hi*hi, hi*lo, lo*hi
+//     products into accumulator t % 2 of unit t (after acc_free says the
+//     epilogue has read unit t - 2), then commits them to a_free, b_free and,
+//     after a unit's last chunk, acc_full.
+//   epilogue (warps 0-3): per unit, wait acc_full, read the 32 rows of its lane
+//     quarter from tensor memory, store them, arrive on acc_free.
+// Chunk k uses phase (k / 2) % 2 of a_full / a_free and (k / RB) % 2 of
+// b_full / b_free; unit t uses phase (t / 2) % 2 of acc_full / acc_free.
+// Every wait is bounded; after a timeout the remaining waits return at once,
+// each role leaves its loop, and the issuer drains what it issued.
+template <int RAW, int RB>
 __global__ void __launch_bounds__(kLtThreads, 1)
 linear_tc_kernel(const __grid_constant__ LinDesc D, int64_t n, int nmax, unsigned tmem_cols,
                  const float* __restrict__ x, const unsigned char* __restrict__ img,
                  float* __restrict__ out) {
     extern __shared__ __align__(1024) unsigned char smem[];
-    __shared__ __align__(8) unsigned long long a_full[2], b_full[2], mma_done[2], acc_full;
+    __shared__ __align__(8) unsigned long long a_full[2], a_free[2], b_full[RB], b_free[RB];
+    __shared__ __align__(8) unsigned long long acc_full[2], acc_free[2];
     __shared__ unsigned tmem_base;
     __shared__ int fail;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const unsigned stage_bytes = lt_stage_bytes(nmax);
+    unsigned char* Abase = smem;                                   // stage s: hi at 2 s kLtA
+    unsigned char* Bbase = smem + 4 * kLtA;                        // slot j: j * bslot
+    const unsigned bslot = 2u * (unsigned)nmax * kLtK * 4;
+    unsigned char* raw = Bbase + (size_t)RB * bslot;               // slot j: j * kLtA
 
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -276,11 +314,15 @@ linear_tc_kernel(const __grid_constant__ LinDesc D, int64_t n, int nmax, unsigne
     }
     if (tid == 0) {
         for (int i = 0; i < 2; ++i) {
-            tc_mbar_init(&a_full[i], kLtThreads);
-            tc_mbar_init(&b_full[i], 1);
-            tc_mbar_init(&mma_done[i], 1);
+            tc_mbar_init(&a_full[i], kLtProd);
+            tc_mbar_init(&a_free[i], 1);
+            tc_mbar_init(&acc_full[i], 1);
+            tc_mbar_init(&acc_free[i], 32 * kLtEpiWarps);
         }
-        tc_mbar_init(&acc_full, 1);
+        for (int i = 0; i < RB; ++i) {
+            tc_mbar_init(&b_full[i], 1);
+            tc_mbar_init(&b_free[i], 1);
+        }
         fail = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -288,6 +330,7 @@ linear_tc_kernel(const __grid_constant__ LinDesc D, int64_t n, int nmax, unsigne
     __syncthreads();
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const unsigned tmem = tmem_base;
+    const unsigned acc_cols = tmem_cols / 2;  // two accumulators side by side
 
     auto wait = [&](unsigned long long* bar, unsigned parity) -> bool {
         if (*(volatile int*)&fail) return false;
@@ -295,162 +338,215 @@ linear_tc_kernel(const __grid_constant__ LinDesc D, int64_t n, int nmax, unsigne
         atomicExch(&fail, 1);
         return false;
     };
-    // unit u -> (block b, tile t)
-    auto locate = [&](int64_t u, int& b, int64_t& t) -> bool {
-        for (b = 0; b < D.nblocks; ++b) {
-            const int64_t tb = (n * D.blk[b].d + kLtM - 1) / kLtM;
+    struct Pos {
+        int64_t u, t;
+        int b, ci;
+        bool valid;
+    };
+    auto locate = [&](Pos& p) {
+        int64_t u = p.u;
+        for (p.b = 0; p.b < D.nblocks; ++p.b) {
+            const int64_t tb = (n * D.blk[p.b].d + kLtM - 1) / kLtM;
             if (u < tb) {
-                t = u;
-                return true;
+                p.t = u;
+                p.valid = true;
+                return;
             }
             u -= tb;
         }
-        return false;
+        p.valid = false;
     };
-    // rows 32 warp + 4 i + lane / 8, columns 4 (lane % 8) .. + 3 of a chunk
-    auto load = [&](int b, int64_t t, int ci, float4 (&v)[8]) {
-        const LinBlock& B = D.blk[b];
-        const LinChunk& C = D.ch[B.chunk0 + ci];
-        const int64_t rows = n * B.d;
-        const int k4 = (lane & 7) * 4;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int64_t R = t * kLtM + 32 * warp + 4 * i + (lane >> 3);
-            v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (R < rows && k4 < C.kc) {
-                const int64_t item = R / B.d;
-                const int m = (int)(R % B.d);
-                v[i] = *reinterpret_cast<const float4*>(
-                    x + item * D.in_stride + C.a_off + (int64_t)m * C.a_mul + C.k0 + k4);
-            }
+    auto advance = [&](Pos& p) {
+        if (p.ci + 1 < D.blk[p.b].nchunk) {
+            ++p.ci;
+        } else {
+            p.u += gridDim.x;
+            p.ci = 0;
+            locate(p);
         }
     };
+    Pos start{(int64_t)blockIdx.x, 0, 0, 0, false};
+    locate(start);
 
-    int64_t u = blockIdx.x, t = 0;
-    int b = 0, ci = 0;
-    bool valid = locate(u, b, t);
-    float4 nxt[8];
-    if (valid) load(b, t, 0, nxt);
-    int64_t k = 0, units = 0;
-    int b_issued[2] = {0, 0}, b_waited[2] = {0, 0};
-    int64_t last_commit = -1;
-    while (valid) {
-        const int s = (int)(k & 1);
-        unsigned char* st = smem + (size_t)s * stage_bytes;
-        const LinBlock& B = D.blk[b];
-        const LinChunk& C = D.ch[B.chunk0 + ci];
-        const int N = B.ncols;
-        const unsigned bbytes = 2u * (unsigned)N * kLtK * 4;
-        // stage s is free once the MMAs of chunk k - 2 have completed
-        if (k >= 2) wait(&mma_done[s], (unsigned)(((k - 2) >> 1) & 1));
-        if (tid == 0 && !*(volatile int*)&fail) {
-            tc_expect_tx(&b_full[s], bbytes);
-            tc_bulk_g2s(st + 2 * kLtA, img + C.img_off, bbytes, &b_full[s]);
-            ++b_issued[s];
-        }
-        {
-            const int k4 = (lane & 7) * 4;
+    if (warp >= kLtEpiWarps && warp < kLtEpiWarps + kLtProdWarps) {
+        // ---------------------------------------------------------- producers
+        const int pw = warp - kLtEpiWarps;
+        // request: rows 16 pw + 4 i + lane / 8, 16-byte piece c = lane % 8
+        auto request = [&](const Pos& p, int slot) {
+            if (p.valid) {
+                const LinBlock& B = D.blk[p.b];
+                const LinChunk& C = D.ch[B.chunk0 + p.ci];
+                const int64_t rows = n * B.d;
+                const int c = lane & 7;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int r = 32 * warp + 4 * i + (lane >> 3);
-                const float in[4] = {nxt[i].x, nxt[i].y, nxt[i].z, nxt[i].w};
+                for (int i = 0; i < 4; ++i) {
+                    const int r = 16 * pw + 4 * i + (lane >> 3);
+                    const int64_t R = p.t * kLtM + r;
+                    const float* src = x;
+                    unsigned bytes = 0;
+                    if (R < rows && 4 * c < C.kc) {
+                        const int64_t item = R / B.d;
+                        const int m = (int)(R % B.d);
+                        src = x + item * D.in_stride + C.a_off + (int64_t)m * C.a_mul + C.k0 + 4 * c;
+                        bytes = 16;
+                    }
+                    cp_async16(raw + (size_t)slot * kLtA + r * 128 + ((c ^ (r & 7)) << 4), src, bytes);
+                }
+            }
+            cp_async_commit();  // one group per chunk position, empty past the end
+        };
+        Pos pre = start, cur = start;
+        for (int q = 0; q < RAW - 1; ++q) {
+            request(pre, q);
+            if (pre.valid) advance(pre);
+        }
+        const int r = 16 * pw + (lane & 15), c0 = 4 * (lane >> 4);
+        for (int64_t k = 0; cur.valid; ++k) {
+            request(pre, (int)((k + RAW - 1) % RAW));
+            if (pre.valid) advance(pre);
+            const int s = (int)(k & 1);
+            if (k >= 2 && !wait(&a_free[s], (unsigned)(((k - 2) >> 1) & 1))) break;
+            cp_async_wait<RAW - 1>();
+            __syncwarp();
+            const unsigned char* rs = raw + (size_t)(k % RAW) * kLtA + r * 128;
+            unsigned char* st = Abase + (size_t)s * 2 * kLtA;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int c = c0 + j;
+                const float4 v = *reinterpret_cast<const float4*>(rs + ((c ^ (r & 7)) << 4));
+                const float in[4] = {v.x, v.y, v.z, v.w};
                 float hi[4], lo[4];
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     hi[q] = to_tf32(in[q]);
                     lo[q] = to_tf32(in[q] - hi[q]);
                 }
-                const unsigned off = kmajor_offset(r, k4, kLtM);
+                const unsigned off = kmajor_offset(r, 4 * c, kLtM);
                 *reinterpret_cast<float4*>(st + off) = make_float4(hi[0], hi[1], hi[2], hi[3]);
                 *reinterpret_cast<float4*>(st + kLtA + off) = make_float4(lo[0], lo[1], lo[2], lo[3]);
             }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            tc_mbar_arrive(&a_full[s]);
+            __syncwarp();  // the slot just read is requested again next iteration
+            advance(cur);
+            if (*(volatile int*)&fail) break;
         }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        tc_mbar_arrive(&a_full[s]);
-        // advance, then fetch the next chunk's rows while this one multiplies
-        const bool first = ci == 0, last = ci + 1 == B.nchunk;
-        const int eb = b;
-        const int64_t et = t;
-        if (!last) {
-            ++ci;
-        } else {
-            u += gridDim.x;
-            valid = locate(u, b, t);
-            ci = 0;
-        }
-        if (valid) load(b, t, ci, nxt);
-        if (tid == 0) {
-            const unsigned ph = (unsigned)((k >> 1) & 1);
-            const bool okb = wait(&b_full[s], ph);
-            if (okb) ++b_waited[s];
-            if (wait(&a_full[s], ph) && okb) {
+        cp_async_wait<0>();  // no request may land after the CTA exits
+    } else if (warp == kLtEpiWarps + kLtProdWarps) {
+        // ------------------------------------------------------------- issuer
+        if (lane == 0) {
+            int b_issued[RB], b_waited[RB];
+            for (int i = 0; i < RB; ++i) b_issued[i] = b_waited[i] = 0;
+            int64_t last_commit = -1;
+            Pos bp = start, cur = start;
+            auto issue_b = [&](int64_t kb) {  // B of the chunk at bp (= chunk kb)
+                const int slot = (int)(kb % RB);
+                const LinBlock& B = D.blk[bp.b];
+                const LinChunk& C = D.ch[B.chunk0 + bp.ci];
+                const unsigned bytes = 2u * (unsigned)B.ncols * kLtK * 4;
+                tc_expect_tx(&b_full[slot], bytes);
+                tc_bulk_g2s(Bbase + (size_t)slot * bslot, img + C.img_off, bytes, &b_full[slot]);
+                ++b_issued[slot];
+                advance(bp);
+            };
+            int64_t kb = 0;
+            for (; kb < RB - 1 && bp.valid; ++kb) issue_b(kb);
+            int64_t k = 0, t = 0;
+            bool ok = true;
+            while (cur.valid && ok) {
+                const int s = (int)(k & 1), slot = (int)(k % RB);
+                const LinBlock& B = D.blk[cur.b];
+                const int N = B.ncols;
+                const bool first = cur.ci == 0, last = cur.ci + 1 == B.nchunk;
+                const int acc = (int)(t & 1);
+                ok = wait(&b_full[slot], (unsigned)((k / RB) & 1));
+                if (ok) ++b_waited[slot];
+                ok = ok && wait(&a_full[s], (unsigned)((k >> 1) & 1));
+                if (ok && first && t >= 2) ok = wait(&acc_free[acc], (unsigned)(((t - 2) >> 1) & 1));
+                if (!ok) break;
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
                 const uint32_t idesc = tf32_idesc(kLtM, N);
                 const unsigned la = (kLtM / 8) * 128, lb = (unsigned)(N / 8) * 128;
-                const unsigned a0 = smem_addr(st), b0 = smem_addr(st + 2 * kLtA);
+                const unsigned a0 = smem_addr(Abase + (size_t)s * 2 * kLtA);
+                const unsigned b0 = smem_addr(Bbase + (size_t)slot * bslot);
                 const unsigned bpart = (unsigned)N * kLtK * 4;
+                const unsigned d = tmem + (unsigned)acc * acc_cols;
 #pragma unroll
                 for (int k8 = 0; k8 < kLtK; k8 += 8) {
-                    const unsigned ka = (unsigned)(k8 >> 2) * la, kb = (unsigned)(k8 >> 2) * lb;
+                    const unsigned ka = (unsigned)(k8 >> 2) * la, kk = (unsigned)(k8 >> 2) * lb;
                     const uint64_t ah = smem_desc(a0 + ka, la, 128);
                     const uint64_t al = smem_desc(a0 + kLtA + ka, la, 128);
-                    const uint64_t bh = smem_desc(b0 + kb, lb, 128);
-                    const uint64_t bl = smem_desc(b0 + bpart + kb, lb, 128);
-                    mma_tf32_n(tmem, ah, bh, idesc, (first && k8 == 0) ? 0u : 1u);
-                    mma_tf32_n(tmem, ah, bl, idesc, 1u);
-                    mma_tf32_n(tmem, al, bh, idesc, 1u);
+                    const uint64_t bh = smem_desc(b0 + kk, lb, 128);
+                    const uint64_t bl = smem_desc(b0 + bpart + kk, lb, 128);
+                    mma_tf32_n(d, ah, bh, idesc, (first && k8 == 0) ? 0u : 1u);
+                    mma_tf32_n(d, ah, bl, idesc, 1u);
+                    mma_tf32_n(d, al, bh, idesc, 1u);
                 }
-                tc_commit(&mma_done[s]);
-                if (last) tc_commit(&acc_full);
+                tc_commit(&a_free[s]);
+                tc_commit(&b_free[slot]);
+                if (last) tc_commit(&acc_full[acc]);
                 last_commit = k;
+                // refill: chunk kb goes into the slot of chunk kb - RB, free once
+                // that chunk's MMAs have completed
+                if (bp.valid) {
+                    const int fs = (int)(kb % RB);
+                    if (kb >= RB && !wait(&b_free[fs], (unsigned)(((kb - RB) / RB) & 1))) break;
+                    issue_b(kb);
+                    ++kb;
+                }
+                if (last) ++t;
+                advance(cur);
+                ++k;
+                if (*(volatile int*)&fail) break;
             }
+            // drain: bulk copies issued but never waited for, the last MMAs
+            for (int q = 0; q < RB; ++q)
+                while (b_waited[q] < b_issued[q]) {
+                    tc_mbar_wait(&b_full[q], (unsigned)(b_waited[q] & 1));
+                    ++b_waited[q];
+                }
+            if (last_commit >= 0)
+                tc_mbar_wait(&a_free[last_commit & 1], (unsigned)((last_commit >> 1) & 1));
         }
-        if (last) {
-            // epilogue: warp w holds rows 32 w .. 32 w + 31 (one per lane)
-            bool got = wait(&acc_full, (unsigned)(units & 1));
+    } else {
+        // ----------------------------------------------------------- epilogue
+        const int q = warp;  // TMEM lane quarter
+        Pos cur = start;
+        for (int64_t t = 0; cur.valid; ++t) {
+            const int acc = (int)(t & 1);
+            bool got = wait(&acc_full[acc], (unsigned)((t >> 1) & 1));
             got = __all_sync(0xffffffffu, got);
-            if (got) {
-                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                const LinBlock& EB = D.blk[eb];
-                const int64_t R = et * kLtM + 32 * warp + lane;
-                const bool live = R < n * EB.d;
-                float* o = out;
+            if (!got) break;
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            const LinBlock& EB = D.blk[cur.b];
+            const int64_t R = cur.t * kLtM + 32 * q + lane;
+            const bool live = R < n * EB.d;
+            float* o = out;
+            if (live) {
+                const int64_t item = R / EB.d;
+                const int m = (int)(R % EB.d);
+                o = out + item * D.out_stride + EB.out_off + (int64_t)m * EB.ncols;
+            }
+            for (int c0 = 0; c0 < EB.ncols; c0 += 32) {
+                float v[32];
+                tmem_ld32(tmem + ((unsigned)(32 * q) << 16) + (unsigned)acc * acc_cols + (unsigned)c0, v);
                 if (live) {
-                    const int64_t item = R / EB.d;
-                    const int m = (int)(R % EB.d);
-                    o = out + item * D.out_stride + EB.out_off + (int64_t)m * EB.ncols;
-                }
-                for (int c0 = 0; c0 < EB.ncols; c0 += 32) {
-                    float v[32];
-                    tmem_ld32(tmem + ((unsigned)(32 * warp) << 16) + (unsigned)c0, v);
-                    if (live) {
 #pragma unroll
-                        for (int q = 0; q < 8; ++q)
-                            *reinterpret_cast<float4*>(o + c0 + 4 * q) =
-                                make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-                    }
+                    for (int i = 0; i < 8; ++i)
+                        *reinterpret_cast<float4*>(o + c0 + 4 * i) =
+                            make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
                 }
             }
-            ++units;
             asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-            __syncthreads();
-            if (*(volatile int*)&fail) break;
+            tc_mbar_arrive(&acc_free[acc]);
+            // next unit of this CTA
+            cur.u += gridDim.x;
+            cur.ci = 0;
+            locate(cur);
         }
-        ++k;
     }
-    // drain: copies issued but never waited for, and the last committed MMAs
-    if (tid == 0) {
-        for (int q = 0; q < 2; ++q)
-            while (b_waited[q] < b_issued[q]) {
-                tc_mbar_wait(&b_full[q], (unsigned)(b_waited[q] & 1));
-                ++b_waited[q];
-            }
-        if (last_commit >= 0)
-            tc_mbar_wait(&mma_done[last_commit & 1], (unsigned)((last_commit >> 1) & 1));
-        if (fail) atomicExch(&cgtp_linear_error, 1);
-    }
-    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
+    if (tid == 0 && fail) atomicExch(&cgtp_linear_error, 1);
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     if (warp == 0)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
@@ -686,14 +782,17 @@ static cudaError_t run_pass(const LinearImpl& L, const LinDesc& D, int nmax, siz
     int64_t units = 0;
     for (int b = 0; b < D.nblocks; ++b) units += (n * D.blk[b].d + kLtM - 1) / kLtM;
     const unsigned grid = (unsigned)std::min<int64_t>(units, sm_count());
+    // deeper rings while they fit: (RAW, RB) = (4, 3) up to 128 columns, else (2, 2)
+    const bool deep = nmax <= 128;
     unsigned cols = 32;
-    while ((int)cols < nmax) cols <<= 1;
-    const size_t smem = 2 * (size_t)lt_stage_bytes(nmax);
-    e = cudaFuncSetAttribute(linear_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    while ((int)cols < 2 * nmax) cols <<= 1;  // two accumulators
+    const size_t smem = deep ? lt_smem_bytes(nmax, 3, 4) : lt_smem_bytes(nmax, 2, 2);
+    auto* kern = deep ? linear_tc_kernel<4, 3> : linear_tc_kernel<2, 2>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     (void)img_bytes;
-    linear_tc_kernel<<<grid, kLtThreads, smem, s>>>(D, n, nmax, cols, (const float*)a,
-                                                    (const unsigned char*)img, (float*)out);
+    kern<<<grid, kLtThreads, smem, s>>>(D, n, nmax, cols, (const float*)a,
+                                        (const unsigned char*)img, (float*)out);
     return cudaGetLastError();
 }
 
