@@ -15,13 +15,12 @@
 //
 // Kernels:
 //   * linear_tc_kernel (fp32; every mul a multiple of 32, mul_out <= 256,
-//     16-byte aligned rows): 128-row tiles on tcgen05 with kind::tf32; A (the
-//     rows, loaded and split into TF32 hi + lo parts by all four warps) and B
-//     (the packed hi/lo image of W, one bulk copy per 32-wide K chunk) sit in
-//     a two-stage shared-memory ring; one thread issues hi*hi + hi*lo + lo*hi
-//     into a 128 x mul_out fp32 accumulator in tensor memory (the dropped
-//     lo*lo term is 2^-22 relative).  The next chunk's rows are loaded into
-//     registers while the current chunk multiplies.
+//     16-byte aligned rows): 128-row tiles on tcgen05 with kind::tf32.  A (the
+//     rows, as TF32 hi + lo parts) is written into tensor memory by producer
+//     warps; B (the packed hi/lo image of W, one bulk copy per 32-wide K
+//     chunk) streams through a shared-memory ring; one thread issues hi*hi +
+//     hi*lo + lo*hi into fp32 accumulators in tensor memory (the dropped
+//     lo*lo term is about 2^-21 relative); epilogue warps store the results.
 //   * linear_simt_kernel (fp32 / fp64, any shape): shared-memory tiles and 4 x 4
 //     FMA micro-tiles on the CUDA cores.
 //   * linear_wgrad_kernel: per-CTA partial sums of x^T g over a fixed row
@@ -45,6 +44,7 @@ __device__ int cgtp_linear_error;  // nonzero: a bounded wait timed out
 // out[n * out_stride + out_off + m * ncols + c] for c < ncols.
 struct LinBlock {
     int out_off, ncols, d, chunk0, nchunk;
+    int64_t tile0;  // first 128-row tile of the block (set per launch of the tensor-core kernel)
 };
 // One K chunk of a block: columns a_off + m * a_mul + k0 + k (k < kc) of the
 // input rows, against B[k][c] = W[w_off + (k0 + k) * w_ks + c * w_ns]; the
@@ -58,7 +58,7 @@ constexpr int kLinMaxChunks = 384;
 struct LinDesc {
     int nblocks, nchunks;
     int64_t in_stride, out_stride;
-    LinBlock blk[kLinMaxBlocks];
+    LinBlock blk[kLinMaxBlocks + 1];  // + the sentinel tile0 of the tensor-core kernel
     LinChunk ch[kLinMaxChunks];
 };
 
@@ -221,15 +221,64 @@ linear_wgrad_kernel(const __grid_constant__ LinGradDesc D, int64_t n, int64_t pe
 constexpr int kLtM = 128;                    // rows per tile (MMA M, TMEM lanes)
 constexpr int kLtK = 32;                     // K per chunk
 constexpr int kLtEpiWarps = 4;               // one per TMEM lane quarter
-constexpr int kLtProdWarps = 8;              // 16 rows each
-constexpr int kLtProd = 32 * kLtProdWarps;
+constexpr int kLtProdWarps = 8;              // two per lane quarter, 16 K columns each
 constexpr int kLtThreads = 32 * (kLtEpiWarps + kLtProdWarps + 1);  // + the MMA issuer warp
-constexpr unsigned kLtA = kLtM * kLtK * 4;   // one TF32 part of an A chunk (16 KB)
+constexpr int kLtRA = 4;                     // A stages in tensor memory
+constexpr unsigned kLtTmemCols = 512;        // accumulators in [0, 256), A stages in [256, 512)
+constexpr unsigned kLtAcol = 256;            // first column of A stage 0 (hi 32, lo 32 per stage)
 
-// Dynamic shared memory: two A stages (hi, lo), RB B slots (hi + lo of up to
-// nmax rows) and RAW raw fp32 row slots.
-__host__ __device__ constexpr unsigned lt_smem_bytes(int nmax, int RB, int RAW) {
-    return 2 * 2 * kLtA + (unsigned)RB * 2u * (unsigned)nmax * kLtK * 4 + (unsigned)RAW * kLtA;
+// Dynamic shared memory: RB B slots (hi + lo of up to nmax rows), the
+// epilogue warps' staging blocks and the block / chunk tables.
+constexpr unsigned kLtStagePitch = 36;  // floats per staged epilogue row (conflict-free)
+constexpr unsigned kLtStage = 32 * kLtStagePitch * 4;  // one epilogue warp's 32 x 32 block
+__host__ __device__ constexpr unsigned lt_smem_bytes(int nmax, int RB) {
+    return (unsigned)RB * 2u * (unsigned)nmax * kLtK * 4 + kLtEpiWarps * kLtStage +
+           (unsigned)((kLinMaxBlocks + 1) * sizeof(LinBlock) + kLinMaxChunks * sizeof(LinChunk));
+}
+
+// Bounded wait that sleeps between polls (about a second at most): for the
+// producer and epilogue warps, whose polling would otherwise compete with the
+// MMA issuer for the shared-memory pipe.
+__device__ __forceinline__ bool tc_mbar_wait_sleep(unsigned long long* b, unsigned parity) {
+    const unsigned a = smem_addr(b);
+    for (unsigned it = 0; it < (1u << 22); ++it) {
+        unsigned ok;
+        asm volatile(
+            "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+            : "=r"(ok) : "r"(a), "r"(parity) : "memory");
+        if (ok) return true;
+        __nanosleep(128);
+    }
+    return false;
+}
+
+// R / d for a row index and a block's 2l+1 (32-bit division when R fits).
+__device__ __forceinline__ int64_t row_item(int64_t R, int d) {
+    return R < 0x7fffffff ? (int64_t)((unsigned)R / (unsigned)d) : R / d;
+}
+
+// tcgen05.mma with the A operand in tensor memory (kind::tf32).
+__device__ __forceinline__ void mma_tf32_tmem_a(unsigned d, unsigned a, uint64_t b, uint32_t idesc,
+                                                unsigned acc) {
+    asm volatile(
+        "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d),
+        "r"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
+// 16 consecutive 32-bit columns of this warp's 32 lanes (one row per lane).
+__device__ __forceinline__ void tmem_st16(unsigned taddr, const float (&v)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+        "%11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+        "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+        "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+        "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+        "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+        "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+        "r"(__float_as_uint(v[15]))
+        : "memory");
 }
 
 // Packed B image of every chunk: rows = output columns c < ncols, K-major
@@ -255,67 +304,71 @@ __global__ void linear_pack_kernel(const __grid_constant__ LinDesc D, const floa
     }
 }
 
-__device__ __forceinline__ void cp_async16(void* dst, const void* src, unsigned src_bytes) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src),
-                 "r"(src_bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-    asm volatile("cp.async.commit_group;" ::: "memory");
-}
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
 // Work units are (block, 128-row tile) pairs, blocks in order; CTA c takes
-// units c, c + grid, ...; every role walks the same sequence.  Warp roles:
-//   producers (warps 4-11, 16 rows each): request the raw fp32 rows of chunk
-//     k + RAW - 1 with cp.async (16 bytes per thread and row piece, slot
-//     (k + RAW - 1) % RAW, XOR-swizzled by row so that both the requests and
-//     the read-back are free of bank conflicts), then, once the MMAs of chunk
-//     k - 2 have released A stage k % 2 (a_free), split chunk k's rows into
-//     TF32 hi / lo parts in the MMA layout and arrive on a_full.  A warp reads
-//     back only rows its own lanes requested (cp.async.wait_group + syncwarp).
+// units c, c + grid, ...; every role walks the same sequence, taking a unit's
+// chunks in an order rotated by c (the CTAs then read different B chunks at
+// the same time).  Chunk k uses A stage k % 4 in tensor memory and B slot
+// k % RB.  Warp roles:
+//   producers (warps 4-11; warp 4 + p serves TMEM lanes 32 (p % 4) .. + 31,
+//     one row per lane, K columns 16 (p / 4) .. + 15 of each chunk): the rows
+//     are loaded into registers three chunks ahead; once the MMAs of chunk
+//     k - 4 have released the stage (a_free) the warp writes chunk k's values
+//     as they are (the tensor cores read them as the TF32 "hi" part, which
+//     keeps the leading 10 fraction bits) and the "lo" parts, lo =
+//     round_tf32(x - x cut to 10 fraction bits), into the stage with
+//     tcgen05.st and arrives on a_full (one arrival per warp).
 //   issuer (warp 12, one thread): B chunk k arrives in ring slot k % RB by bulk
 //     copy (b_full), issued RB - 1 chunks ahead once the MMAs that read the
 //     slot have completed (b_free); it issues chunk k's hi*hi, hi*lo, lo*hi
-//     products into accumulator t % 2 of unit t (after acc_free says the
-//     epilogue has read unit t - 2), then commits them to a_free, b_free and,
-//     after a unit's last chunk, acc_full.
+//     products (A from tensor memory, B from shared memory) into accumulator
+//     t % NACC of unit t (after acc_free says the epilogue has read unit
+//     t - NACC), then commits them to a_free, b_free and, after a unit's last
+//     chunk, acc_full.
 //   epilogue (warps 0-3): per unit, wait acc_full, read the 32 rows of its lane
-//     quarter from tensor memory, store them, arrive on acc_free.
-// Chunk k uses phase (k / 2) % 2 of a_full / a_free and (k / RB) % 2 of
-// b_full / b_free; unit t uses phase (t / 2) % 2 of acc_full / acc_free.
+//     quarter, transpose 32 x 32 pieces through shared memory, store whole
+//     128-byte row segments and arrive on acc_free.
+// Chunk k uses phase (k / 4) % 2 of a_full / a_free and (k / RB) % 2 of
+// b_full / b_free; unit t uses phase (t / NACC) % 2 of acc_full / acc_free.
 // Every wait is bounded; after a timeout the remaining waits return at once,
 // each role leaves its loop, and the issuer drains what it issued.
-template <int RAW, int RB>
+template <int RB, int NACC>
 __global__ void __launch_bounds__(kLtThreads, 1)
-linear_tc_kernel(const __grid_constant__ LinDesc D, int64_t n, int nmax, unsigned tmem_cols,
+linear_tc_kernel(const __grid_constant__ LinDesc D, int64_t n, int nmax,
                  const float* __restrict__ x, const unsigned char* __restrict__ img,
                  float* __restrict__ out) {
+    constexpr int RA = kLtRA;
+    constexpr unsigned accw = 256 / NACC;  // columns per accumulator
     extern __shared__ __align__(1024) unsigned char smem[];
-    __shared__ __align__(8) unsigned long long a_full[2], a_free[2], b_full[RB], b_free[RB];
+    __shared__ __align__(8) unsigned long long a_full[RA], a_free[RA], b_full[RB], b_free[RB];
     __shared__ __align__(8) unsigned long long acc_full[2], acc_free[2];
     __shared__ unsigned tmem_base;
     __shared__ int fail;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    unsigned char* Abase = smem;                                   // stage s: hi at 2 s kLtA
-    unsigned char* Bbase = smem + 4 * kLtA;                        // slot j: j * bslot
+    unsigned char* Bbase = smem;  // slot j: j * bslot
     const unsigned bslot = 2u * (unsigned)nmax * kLtK * 4;
-    unsigned char* raw = Bbase + (size_t)RB * bslot;               // slot j: j * kLtA
+    float* stage_all = reinterpret_cast<float*>(Bbase + (size_t)RB * bslot);
+    // the block and chunk tables, copied to shared memory (indexed lookups in
+    // the parameter space would go through the small constant cache)
+    LinBlock* sblk = reinterpret_cast<LinBlock*>(stage_all + kLtEpiWarps * 32 * kLtStagePitch);
+    LinChunk* sch = reinterpret_cast<LinChunk*>(sblk + kLinMaxBlocks + 1);
+    for (int i = tid; i <= D.nblocks; i += kLtThreads) sblk[i] = D.blk[i];
+    for (int i = tid; i < D.nchunks; i += kLtThreads) sch[i] = D.ch[i];
+    const int nblocks = D.nblocks;
+    const int64_t in_stride = D.in_stride, out_stride = D.out_stride;
 
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          smem_addr(&tmem_base)),
-                     "r"(tmem_cols)
+                     "r"(kLtTmemCols)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
     if (tid == 0) {
-        for (int i = 0; i < 2; ++i) {
-            tc_mbar_init(&a_full[i], kLtProd);
+        for (int i = 0; i < RA; ++i) {
+            tc_mbar_init(&a_full[i], kLtProdWarps);
             tc_mbar_init(&a_free[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
             tc_mbar_init(&acc_full[i], 1);
             tc_mbar_init(&acc_free[i], 32 * kLtEpiWarps);
         }
@@ -330,11 +383,11 @@ linear_tc_kernel(const __grid_constant__ LinDesc D, int64_t n, int nmax, unsigne
     __syncthreads();
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const unsigned tmem = tmem_base;
-    const unsigned acc_cols = tmem_cols / 2;  // two accumulators side by side
 
+    const bool issuer = warp == kLtEpiWarps + kLtProdWarps;
     auto wait = [&](unsigned long long* bar, unsigned parity) -> bool {
         if (*(volatile int*)&fail) return false;
-        if (tc_mbar_wait(bar, parity)) return true;
+        if (issuer ? tc_mbar_wait(bar, parity) : tc_mbar_wait_sleep(bar, parity)) return true;
         atomicExch(&fail, 1);
         return false;
     };
@@ -343,21 +396,18 @@ linear_tc_kernel(const __grid_constant__ LinDesc D, int64_t n, int nmax, unsigne
         int b, ci;
         bool valid;
     };
+    // tiles of block b: [blk[b].tile0, blk[b + 1].tile0); blk[nblocks].tile0 = total
     auto locate = [&](Pos& p) {
-        int64_t u = p.u;
-        for (p.b = 0; p.b < D.nblocks; ++p.b) {
-            const int64_t tb = (n * D.blk[p.b].d + kLtM - 1) / kLtM;
-            if (u < tb) {
-                p.t = u;
-                p.valid = true;
-                return;
-            }
-            u -= tb;
+        p.valid = p.u < sblk[nblocks].tile0;
+        if (!p.valid) return;
+        if (p.u >= sblk[p.b + 1].tile0 || p.u < sblk[p.b].tile0) {
+            p.b = 0;
+            while (p.u >= sblk[p.b + 1].tile0) ++p.b;
         }
-        p.valid = false;
+        p.t = p.u - sblk[p.b].tile0;
     };
     auto advance = [&](Pos& p) {
-        if (p.ci + 1 < D.blk[p.b].nchunk) {
+        if (p.ci + 1 < sblk[p.b].nchunk) {
             ++p.ci;
         } else {
             p.u += gridDim.x;
@@ -365,73 +415,85 @@ linear_tc_kernel(const __grid_constant__ LinDesc D, int64_t n, int nmax, unsigne
             locate(p);
         }
     };
+    // the chunks of a unit are taken in an order rotated by the CTA index, so
+    // that the CTAs do not all read the same B chunk at once
+    auto chunk_of = [&](const Pos& p) -> const LinChunk& {
+        const LinBlock& B = sblk[p.b];
+        return sch[B.chunk0 + (int)(((unsigned)p.ci + blockIdx.x) % (unsigned)B.nchunk)];
+    };
     Pos start{(int64_t)blockIdx.x, 0, 0, 0, false};
     locate(start);
 
     if (warp >= kLtEpiWarps && warp < kLtEpiWarps + kLtProdWarps) {
         // ---------------------------------------------------------- producers
-        const int pw = warp - kLtEpiWarps;
-        // request: rows 16 pw + 4 i + lane / 8, 16-byte piece c = lane % 8
-        auto request = [&](const Pos& p, int slot) {
-            if (p.valid) {
-                const LinBlock& B = D.blk[p.b];
-                const LinChunk& C = D.ch[B.chunk0 + p.ci];
-                const int64_t rows = n * B.d;
-                const int c = lane & 7;
+        const int pw = warp - kLtEpiWarps, qa = pw & 3, h = pw >> 2;
+        const int r = 32 * qa + lane;  // this lane's row of every tile
+        int64_t rbase = 0;
+        int rm = -1;
+        int64_t row_u = -1;
+        auto load = [&](const Pos& p, float4 (&v)[4]) {
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int r = 16 * pw + 4 * i + (lane >> 3);
-                    const int64_t R = p.t * kLtM + r;
-                    const float* src = x;
-                    unsigned bytes = 0;
-                    if (R < rows && 4 * c < C.kc) {
-                        const int64_t item = R / B.d;
-                        const int m = (int)(R % B.d);
-                        src = x + item * D.in_stride + C.a_off + (int64_t)m * C.a_mul + C.k0 + 4 * c;
-                        bytes = 16;
-                    }
-                    cp_async16(raw + (size_t)slot * kLtA + r * 128 + ((c ^ (r & 7)) << 4), src, bytes);
+            for (int j = 0; j < 4; ++j) v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (!p.valid) return;
+            const LinBlock& B = sblk[p.b];
+            const LinChunk& C = chunk_of(p);
+            if (p.u != row_u) {
+                row_u = p.u;
+                const int64_t R = p.t * kLtM + r;
+                rm = -1;
+                if (R < n * B.d) {
+                    const int64_t item = row_item(R, B.d);
+                    rm = (int)(R - item * B.d);
+                    rbase = item * in_stride;
                 }
             }
-            cp_async_commit();  // one group per chunk position, empty past the end
+            if (rm < 0) return;
+            const float* src = x + rbase + C.a_off + (int64_t)rm * C.a_mul + C.k0 + 16 * h;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (16 * h + 4 * j < C.kc) v[j] = *reinterpret_cast<const float4*>(src + 4 * j);
         };
         Pos pre = start, cur = start;
-        for (int q = 0; q < RAW - 1; ++q) {
-            request(pre, q);
-            if (pre.valid) advance(pre);
-        }
-        const int r = 16 * pw + (lane & 15), c0 = 4 * (lane >> 4);
+        float4 v0[4], v1[4], v2[4];
+        load(pre, v0);
+        if (pre.valid) advance(pre);
+        load(pre, v1);
+        if (pre.valid) advance(pre);
+        load(pre, v2);
+        if (pre.valid) advance(pre);
         for (int64_t k = 0; cur.valid; ++k) {
-            request(pre, (int)((k + RAW - 1) % RAW));
+            const int s = (int)(k % RA);
+            float4 v3[4];
+            load(pre, v3);  // three chunks ahead
             if (pre.valid) advance(pre);
-            const int s = (int)(k & 1);
-            if (k >= 2 && !wait(&a_free[s], (unsigned)(((k - 2) >> 1) & 1))) break;
-            cp_async_wait<RAW - 1>();
-            __syncwarp();
-            const unsigned char* rs = raw + (size_t)(k % RAW) * kLtA + r * 128;
-            unsigned char* st = Abase + (size_t)s * 2 * kLtA;
+            if (k >= RA && !wait(&a_free[s], (unsigned)(((k - RA) / RA) & 1))) break;
+            float hi[16], lo[16];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                const int c = c0 + j;
-                const float4 v = *reinterpret_cast<const float4*>(rs + ((c ^ (r & 7)) << 4));
-                const float in[4] = {v.x, v.y, v.z, v.w};
-                float hi[4], lo[4];
+                const float in[4] = {v0[j].x, v0[j].y, v0[j].z, v0[j].w};
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
-                    hi[q] = to_tf32(in[q]);
-                    lo[q] = to_tf32(in[q] - hi[q]);
+                    hi[4 * j + q] = in[q];
+                    lo[4 * j + q] =
+                        to_tf32(in[q] - __uint_as_float(__float_as_uint(in[q]) & 0xFFFFE000u));
                 }
-                const unsigned off = kmajor_offset(r, 4 * c, kLtM);
-                *reinterpret_cast<float4*>(st + off) = make_float4(hi[0], hi[1], hi[2], hi[3]);
-                *reinterpret_cast<float4*>(st + kLtA + off) = make_float4(lo[0], lo[1], lo[2], lo[3]);
             }
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            tc_mbar_arrive(&a_full[s]);
-            __syncwarp();  // the slot just read is requested again next iteration
+            const unsigned ta = tmem + ((unsigned)(32 * qa) << 16) + kLtAcol + 64u * s + 16u * h;
+            tmem_st16(ta, hi);
+            tmem_st16(ta + 32, lo);
+            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+            asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) tc_mbar_arrive(&a_full[s]);  // one arrival per warp
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                v0[j] = v1[j];
+                v1[j] = v2[j];
+                v2[j] = v3[j];
+            }
             advance(cur);
             if (*(volatile int*)&fail) break;
         }
-        cp_async_wait<0>();  // no request may land after the CTA exits
     } else if (warp == kLtEpiWarps + kLtProdWarps) {
         // ------------------------------------------------------------- issuer
         if (lane == 0) {
@@ -441,54 +503,56 @@ linear_tc_kernel(const __grid_constant__ LinDesc D, int64_t n, int nmax, unsigne
             Pos bp = start, cur = start;
             auto issue_b = [&](int64_t kb) {  // B of the chunk at bp (= chunk kb)
                 const int slot = (int)(kb % RB);
-                const LinBlock& B = D.blk[bp.b];
-                const LinChunk& C = D.ch[B.chunk0 + bp.ci];
+                const LinBlock& B = sblk[bp.b];
+                const LinChunk& C = chunk_of(bp);
                 const unsigned bytes = 2u * (unsigned)B.ncols * kLtK * 4;
                 tc_expect_tx(&b_full[slot], bytes);
                 tc_bulk_g2s(Bbase + (size_t)slot * bslot, img + C.img_off, bytes, &b_full[slot]);
                 ++b_issued[slot];
                 advance(bp);
             };
+            // B runs RB - 2 chunks ahead: the slot a refill takes was read by the
+            // MMAs of two chunks back, long complete, so the wait costs nothing
             int64_t kb = 0;
             for (; kb < RB - 1 && bp.valid; ++kb) issue_b(kb);
             int64_t k = 0, t = 0;
             bool ok = true;
             while (cur.valid && ok) {
-                const int s = (int)(k & 1), slot = (int)(k % RB);
-                const LinBlock& B = D.blk[cur.b];
+                const int s = (int)(k % RA), slot = (int)(k % RB);
+                const LinBlock& B = sblk[cur.b];
                 const int N = B.ncols;
                 const bool first = cur.ci == 0, last = cur.ci + 1 == B.nchunk;
-                const int acc = (int)(t & 1);
+                const int acc = (int)(t % NACC);
                 ok = wait(&b_full[slot], (unsigned)((k / RB) & 1));
                 if (ok) ++b_waited[slot];
-                ok = ok && wait(&a_full[s], (unsigned)((k >> 1) & 1));
-                if (ok && first && t >= 2) ok = wait(&acc_free[acc], (unsigned)(((t - 2) >> 1) & 1));
+                ok = ok && wait(&a_full[s], (unsigned)((k / RA) & 1));
+                if (ok && first && t >= NACC)
+                    ok = wait(&acc_free[acc], (unsigned)(((t - NACC) / NACC) & 1));
                 if (!ok) break;
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
                 const uint32_t idesc = tf32_idesc(kLtM, N);
-                const unsigned la = (kLtM / 8) * 128, lb = (unsigned)(N / 8) * 128;
-                const unsigned a0 = smem_addr(Abase + (size_t)s * 2 * kLtA);
+                const unsigned lb = (unsigned)(N / 8) * 128;
                 const unsigned b0 = smem_addr(Bbase + (size_t)slot * bslot);
                 const unsigned bpart = (unsigned)N * kLtK * 4;
-                const unsigned d = tmem + (unsigned)acc * acc_cols;
+                const unsigned d = tmem + (unsigned)acc * accw;
+                const unsigned a0 = tmem + kLtAcol + 64u * s;
 #pragma unroll
                 for (int k8 = 0; k8 < kLtK; k8 += 8) {
-                    const unsigned ka = (unsigned)(k8 >> 2) * la, kk = (unsigned)(k8 >> 2) * lb;
-                    const uint64_t ah = smem_desc(a0 + ka, la, 128);
-                    const uint64_t al = smem_desc(a0 + kLtA + ka, la, 128);
+                    const unsigned kk = (unsigned)(k8 >> 2) * lb;
                     const uint64_t bh = smem_desc(b0 + kk, lb, 128);
                     const uint64_t bl = smem_desc(b0 + bpart + kk, lb, 128);
-                    mma_tf32_n(d, ah, bh, idesc, (first && k8 == 0) ? 0u : 1u);
-                    mma_tf32_n(d, ah, bl, idesc, 1u);
-                    mma_tf32_n(d, al, bh, idesc, 1u);
+                    mma_tf32_tmem_a(d, a0 + k8, bh, idesc, (first && k8 == 0) ? 0u : 1u);
+                    mma_tf32_tmem_a(d, a0 + k8, bl, idesc, 1u);
+                    mma_tf32_tmem_a(d, a0 + 32 + k8, bh, idesc, 1u);
                 }
                 tc_commit(&a_free[s]);
                 tc_commit(&b_free[slot]);
                 if (last) tc_commit(&acc_full[acc]);
                 last_commit = k;
                 // refill: chunk kb goes into the slot of chunk kb - RB, free once
-                // that chunk's MMAs have completed
-                if (bp.valid) {
+                // that chunk's MMAs have completed; kb stays at most k + RB - 1
+                // and the refill waits for chunk k - 1 only when kb = k + RB - 1
+                if (bp.valid && kb <= k + RB - 2) {
                     const int fs = (int)(kb % RB);
                     if (kb >= RB && !wait(&b_free[fs], (unsigned)(((kb - RB) / RB) & 1))) break;
                     issue_b(kb);
@@ -506,51 +570,62 @@ linear_tc_kernel(const __grid_constant__ LinDesc D, int64_t n, int nmax, unsigne
                     ++b_waited[q];
                 }
             if (last_commit >= 0)
-                tc_mbar_wait(&a_free[last_commit & 1], (unsigned)((last_commit >> 1) & 1));
+                tc_mbar_wait(&a_free[last_commit % RA], (unsigned)((last_commit / RA) & 1));
         }
     } else {
         // ----------------------------------------------------------- epilogue
         const int q = warp;  // TMEM lane quarter
         Pos cur = start;
+        float* stage = stage_all + q * (32 * kLtStagePitch);
         for (int64_t t = 0; cur.valid; ++t) {
-            const int acc = (int)(t & 1);
-            bool got = wait(&acc_full[acc], (unsigned)((t >> 1) & 1));
+            const int acc = (int)(t % NACC);
+            bool got = wait(&acc_full[acc], (unsigned)((t / NACC) & 1));
             got = __all_sync(0xffffffffu, got);
             if (!got) break;
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-            const LinBlock& EB = D.blk[cur.b];
+            const LinBlock& EB = sblk[cur.b];
             const int64_t R = cur.t * kLtM + 32 * q + lane;
             const bool live = R < n * EB.d;
-            float* o = out;
+            float* o = out;  // this lane's row
             if (live) {
                 const int64_t item = R / EB.d;
-                const int m = (int)(R % EB.d);
-                o = out + item * D.out_stride + EB.out_off + (int64_t)m * EB.ncols;
+                const int m = (int)(R - item * EB.d);
+                o = out + item * out_stride + EB.out_off + (int64_t)m * EB.ncols;
             }
             for (int c0 = 0; c0 < EB.ncols; c0 += 32) {
                 float v[32];
-                tmem_ld32(tmem + ((unsigned)(32 * q) << 16) + (unsigned)acc * acc_cols + (unsigned)c0, v);
-                if (live) {
+                tmem_ld32(tmem + ((unsigned)(32 * q) << 16) + (unsigned)acc * accw + (unsigned)c0, v);
+                // transpose through shared memory: 8 lanes store one row's 128 bytes
 #pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        *reinterpret_cast<float4*>(o + c0 + 4 * i) =
-                            make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+                for (int i = 0; i < 8; ++i)
+                    *reinterpret_cast<float4*>(stage + lane * kLtStagePitch + 4 * i) =
+                        make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+                __syncwarp();
+#pragma unroll
+                for (int it = 0; it < 8; ++it) {
+                    const int rr = 4 * it + (lane >> 3), cq = lane & 7;
+                    float* orow = reinterpret_cast<float*>(
+                        __shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(o), rr));
+                    const bool rlive = __shfl_sync(0xffffffffu, live, rr);
+                    const float4 w4 = *reinterpret_cast<const float4*>(stage + rr * kLtStagePitch + 4 * cq);
+                    if (rlive) *reinterpret_cast<float4*>(orow + c0 + 4 * cq) = w4;
                 }
+                __syncwarp();
             }
             asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
             tc_mbar_arrive(&acc_free[acc]);
-            // next unit of this CTA
             cur.u += gridDim.x;
             cur.ci = 0;
             locate(cur);
         }
     }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
     if (tid == 0 && fail) atomicExch(&cgtp_linear_error, 1);
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     if (warp == 0)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
-                     "r"(tmem_cols)
+                     "r"(kLtTmemCols)
                      : "memory");
 }
 
@@ -779,20 +854,26 @@ static cudaError_t run_pass(const LinearImpl& L, const LinDesc& D, int nmax, siz
     linear_pack_kernel<<<(unsigned)D.nchunks, 256, 0, s>>>(D, (const float*)W, (unsigned char*)img);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    // per-launch copy with the tile ranges of the blocks for this n
+    auto Dn = std::make_unique<LinDesc>(D);
     int64_t units = 0;
-    for (int b = 0; b < D.nblocks; ++b) units += (n * D.blk[b].d + kLtM - 1) / kLtM;
+    for (int b = 0; b < D.nblocks; ++b) {
+        Dn->blk[b].tile0 = units;
+        units += (n * D.blk[b].d + kLtM - 1) / kLtM;
+    }
+    Dn->blk[D.nblocks].tile0 = units;
     const unsigned grid = (unsigned)std::min<int64_t>(units, sm_count());
-    // deeper rings while they fit: (RAW, RB) = (4, 3) up to 128 columns, else (2, 2)
-    const bool deep = nmax <= 128;
-    unsigned cols = 32;
-    while ((int)cols < 2 * nmax) cols <<= 1;  // two accumulators
-    const size_t smem = deep ? lt_smem_bytes(nmax, 3, 4) : lt_smem_bytes(nmax, 2, 2);
-    auto* kern = deep ? linear_tc_kernel<4, 3> : linear_tc_kernel<2, 2>;
+    // up to 128 columns: two accumulators and a 4-slot B ring; 256: one and 3
+    const bool two = nmax <= 128;
+    // at least half of the SM's shared memory: one CTA per SM, which the
+    // 512-column tensor-memory allocation needs
+    const size_t smem = std::max<size_t>(120 * 1024, two ? lt_smem_bytes(nmax, 4) : lt_smem_bytes(nmax, 3));
+    auto* kern = two ? linear_tc_kernel<4, 2> : linear_tc_kernel<3, 1>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     (void)img_bytes;
-    kern<<<grid, kLtThreads, smem, s>>>(D, n, nmax, cols, (const float*)a,
-                                        (const unsigned char*)img, (float*)out);
+    kern<<<grid, kLtThreads, smem, s>>>(*Dn, n, nmax, (const float*)a, (const unsigned char*)img,
+                                        (float*)out);
     return cudaGetLastError();
 }
 
