@@ -317,7 +317,7 @@ __global__ void linear_pack_kernel(const __grid_constant__ LinDesc D, const floa
 //     keeps the leading 10 fraction bits) and the "lo" parts, lo =
 //     round_tf32(x - x cut to 10 fraction bits), into the stage with
 //     tcgen05.st and arrives on a_full (one arrival per warp).
-//   issuer (warp 12, one thread): B chunk k arrives in ring slot k % RB by bulk
+//   issuer (warp 12, lane 0 issuing): B chunk k arrives in ring slot k % RB by bulk
 //     copy (b_full), issued RB - 1 chunks ahead once the MMAs that read the
 //     slot have completed (b_free); it issues chunk k's hi*hi, hi*lo, lo*hi
 //     products (A from tensor memory, B from shared memory) into accumulator
@@ -496,7 +496,10 @@ linear_tc_kernel(const __grid_constant__ LinDesc D, int64_t n, int nmax,
         }
     } else if (warp == kLtEpiWarps + kLtProdWarps) {
         // ------------------------------------------------------------- issuer
-        if (lane == 0) {
+        // the whole warp walks the loop (converged); lane 0 issues the copies,
+        // MMAs and commits
+        const bool leader = lane == 0;
+        {
             int b_issued[RB], b_waited[RB];
             for (int i = 0; i < RB; ++i) b_issued[i] = b_waited[i] = 0;
             int64_t last_commit = -1;
@@ -506,8 +509,10 @@ linear_tc_kernel(const __grid_constant__ LinDesc D, int64_t n, int nmax,
                 const LinBlock& B = sblk[bp.b];
                 const LinChunk& C = chunk_of(bp);
                 const unsigned bytes = 2u * (unsigned)B.ncols * kLtK * 4;
-                tc_expect_tx(&b_full[slot], bytes);
-                tc_bulk_g2s(Bbase + (size_t)slot * bslot, img + C.img_off, bytes, &b_full[slot]);
+                if (leader) {
+                    tc_expect_tx(&b_full[slot], bytes);
+                    tc_bulk_g2s(Bbase + (size_t)slot * bslot, img + C.img_off, bytes, &b_full[slot]);
+                }
                 ++b_issued[slot];
                 advance(bp);
             };
@@ -528,6 +533,7 @@ linear_tc_kernel(const __grid_constant__ LinDesc D, int64_t n, int nmax,
                 ok = ok && wait(&a_full[s], (unsigned)((k / RA) & 1));
                 if (ok && first && t >= NACC)
                     ok = wait(&acc_free[acc], (unsigned)(((t - NACC) / NACC) & 1));
+                ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
                 const uint32_t idesc = tf32_idesc(kLtM, N);
@@ -536,25 +542,29 @@ linear_tc_kernel(const __grid_constant__ LinDesc D, int64_t n, int nmax,
                 const unsigned bpart = (unsigned)N * kLtK * 4;
                 const unsigned d = tmem + (unsigned)acc * accw;
                 const unsigned a0 = tmem + kLtAcol + 64u * s;
+                if (leader) {
 #pragma unroll
-                for (int k8 = 0; k8 < kLtK; k8 += 8) {
-                    const unsigned kk = (unsigned)(k8 >> 2) * lb;
-                    const uint64_t bh = smem_desc(b0 + kk, lb, 128);
-                    const uint64_t bl = smem_desc(b0 + bpart + kk, lb, 128);
-                    mma_tf32_tmem_a(d, a0 + k8, bh, idesc, (first && k8 == 0) ? 0u : 1u);
-                    mma_tf32_tmem_a(d, a0 + k8, bl, idesc, 1u);
-                    mma_tf32_tmem_a(d, a0 + 32 + k8, bh, idesc, 1u);
+                    for (int k8 = 0; k8 < kLtK; k8 += 8) {
+                        const unsigned kk = (unsigned)(k8 >> 2) * lb;
+                        const uint64_t bh = smem_desc(b0 + kk, lb, 128);
+                        const uint64_t bl = smem_desc(b0 + bpart + kk, lb, 128);
+                        mma_tf32_tmem_a(d, a0 + k8, bh, idesc, (first && k8 == 0) ? 0u : 1u);
+                        mma_tf32_tmem_a(d, a0 + k8, bl, idesc, 1u);
+                        mma_tf32_tmem_a(d, a0 + 32 + k8, bh, idesc, 1u);
+                    }
+                    tc_commit(&a_free[s]);
+                    tc_commit(&b_free[slot]);
+                    if (last) tc_commit(&acc_full[acc]);
                 }
-                tc_commit(&a_free[s]);
-                tc_commit(&b_free[slot]);
-                if (last) tc_commit(&acc_full[acc]);
+                __syncwarp();
                 last_commit = k;
                 // refill: chunk kb goes into the slot of chunk kb - RB, free once
                 // that chunk's MMAs have completed; kb stays at most k + RB - 1
                 // and the refill waits for chunk k - 1 only when kb = k + RB - 1
                 if (bp.valid && kb <= k + RB - 2) {
                     const int fs = (int)(kb % RB);
-                    if (kb >= RB && !wait(&b_free[fs], (unsigned)(((kb - RB) / RB) & 1))) break;
+                    const bool freed = kb < RB || wait(&b_free[fs], (unsigned)(((kb - RB) / RB) & 1));
+                    if (!__all_sync(0xffffffffu, freed)) break;
                     issue_b(kb);
                     ++kb;
                 }
@@ -564,13 +574,15 @@ linear_tc_kernel(const __grid_constant__ LinDesc D, int64_t n, int nmax,
                 if (*(volatile int*)&fail) break;
             }
             // drain: bulk copies issued but never waited for, the last MMAs
-            for (int q = 0; q < RB; ++q)
-                while (b_waited[q] < b_issued[q]) {
-                    tc_mbar_wait(&b_full[q], (unsigned)(b_waited[q] & 1));
-                    ++b_waited[q];
-                }
-            if (last_commit >= 0)
-                tc_mbar_wait(&a_free[last_commit % RA], (unsigned)((last_commit / RA) & 1));
+            if (leader) {
+                for (int q = 0; q < RB; ++q)
+                    while (b_waited[q] < b_issued[q]) {
+                        tc_mbar_wait(&b_full[q], (unsigned)(b_waited[q] & 1));
+                        ++b_waited[q];
+                    }
+                if (last_commit >= 0)
+                    tc_mbar_wait(&a_free[last_commit % RA], (unsigned)((last_commit / RA) & 1));
+            }
         }
     } else {
         // ----------------------------------------------------------- epilogue
