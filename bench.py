@@ -311,7 +311,7 @@ def make_conv64(args, cg, W, torch):
 
 
 def make_tp(args, cg, W, torch):
-    cfg = W.config1()
+    cfg = W.config1(args.samples)
     B = cfg["B"]
     plan = cg.Plan(*cfg["irreps"])
     x, vec, w = (torch.from_numpy(cfg[k]).cuda() for k in ("x", "vec", "w"))
@@ -337,7 +337,7 @@ def make_tp(args, cg, W, torch):
               "tp_fwd": (B * (rowb + prob.dimo * 4), B * f),
               "tp_bwd": (B * (rowb + prob.dimo * 4 + rowb), 3 * B * f),
               "sh_bwd": (B * (6 + prob.dim2) * 4, None)}
-    desc = ("standalone CG-TP: B=200000, 128x(0e,1o,2e) (x) Y(l<=3) -> "
+    desc = (f"standalone CG-TP: B={B}, 128x(0e,1o,2e) (x) Y(l<=3) -> "
             "128x(0e,1o,1e,2o,2e,3o,3e), 24 uvu paths, fp32")
     return Workload("tp", desc, B, "samples/s", "f32", kernels, counts, ["sh_fwd", "tp_fwd"],
                     dict(B=B, mul=128, paths=plan.n_paths), None,
@@ -416,7 +416,7 @@ def make_kv(args, cg, W, torch):
 def make_uvw(args, cg, W, torch):
     """'uvw' product at config 1's sizes: per-path 'uvu' blocks (unit shared
     weights), then the channel mixing on the tensor cores."""
-    cfg = W.config1_uvw()
+    cfg = W.config1_uvw(args.samples)
     B = cfg["B"]
     uvw = cg.UVWProduct(*W.CFG1)
     x, vec, Wm = (torch.from_numpy(cfg[k]).cuda() for k in ("x", "vec", "W"))
@@ -439,7 +439,7 @@ def make_uvw(args, cg, W, torch):
               "tp_paths": (B * (d.dim1 + d.dim2 + d.dimo) * 4 + d.wdim * 4, B * d.flops),
               "linear": (B * (uvw.dim_mid + uvw.dim_out) * 4 + uvw.weight_numel * 4, mix_flops,
                          "tensor3")}
-    desc = ("'uvw' CG-TP: B=200000, 128x(0e,1o,2e) (x) Y(l<=3) -> 128x(0e,1o,1e,2o,2e,3o,3e), "
+    desc = (f"'uvw' CG-TP: B={B}, 128x(0e,1o,2e) (x) Y(l<=3) -> 128x(0e,1o,1e,2o,2e,3o,3e), "
             "24 paths, one shared 128x128 matrix per path, fp32 (channel mixing on tcgen05, "
             "TF32 split in three products)")
     return Workload("uvw", desc, B, "samples/s", "f32", kernels, counts,
@@ -603,7 +603,7 @@ def _traffic(workload, kernel):
     import hashlib
     src = os.path.join(ROOT, "clebsch_gordan_tensor_gb300", "csrc")
     h = hashlib.sha256()
-    for f in ("tp_kernels.cuh", "plan.cpp"):
+    for f in d.get("sources", ("tp_kernels.cuh", "plan.cpp")):
         h.update(open(os.path.join(src, f), "rb").read())
     return d.get("bytes") if d.get("kernel_sha") == h.hexdigest()[:16] else None
 
@@ -758,6 +758,9 @@ def main():
     ap.add_argument("--atoms", type=int, default=10_000,
                     help="atom count of the conv workload (10000 is the benchmark; smaller "
                          "for profiling)")
+    ap.add_argument("--samples", type=int, default=200_000,
+                    help="sample count of the tp and uvw workloads (200000 is the benchmark; "
+                         "smaller for profiling)")
     ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args()
     line = run_reference(args) if args.impl == "reference" else run_gpu(args)
