@@ -189,7 +189,6 @@ static cgtp_status bwd_launch(Plan& p, bool conv, int64_t n_items, const int32_t
     // ordered sum of the per-CTA partial rows into grad_w
     cudaError_t e = launch_reduce_rows(p.dtype == CGTP_F64, wsp, rows, p.wdim, gw, s);
     if (e != cudaSuccess) return cuda_fail(e, "weight-gradient reduction");
-    count_launch();
     return CGTP_OK;
 }
 
@@ -199,7 +198,6 @@ static cgtp_status zero(void* ptr, int64_t bytes, cudaStream_t s) {
     if (!ptr || bytes <= 0) return CGTP_OK;
     cudaError_t e = launch_fill_zero(ptr, bytes, s);
     if (e != cudaSuccess) return cuda_fail(e, "fill_zero");
-    count_launch();
     return CGTP_OK;
 }
 
@@ -610,7 +608,6 @@ cgtp_status cgtp_sh_forward(int lmax, cgtp_dtype dtype, int64_t E, const void* v
     if (!vec || !y) return fail(CGTP_E_ARG, "NULL tensor");
     cudaError_t e = launch_sh_forward(lmax, dtype == CGTP_F64, E, vec, y, S(stream));
     if (e != cudaSuccess) return cuda_fail(e, "sh_forward");
-    count_launch();
     return CGTP_OK;
     GUARD_END
 }
@@ -623,7 +620,6 @@ cgtp_status cgtp_sh_backward(int lmax, cgtp_dtype dtype, int64_t E, const void* 
     if (!vec || !grad_y || !grad_vec) return fail(CGTP_E_ARG, "NULL tensor");
     cudaError_t e = launch_sh_backward(lmax, dtype == CGTP_F64, E, vec, grad_y, grad_vec, S(stream));
     if (e != cudaSuccess) return cuda_fail(e, "sh_backward");
-    count_launch();
     return CGTP_OK;
     GUARD_END
 }
@@ -636,7 +632,6 @@ cgtp_status cgtp_sh_jvp(int lmax, cgtp_dtype dtype, int64_t E, const void* vec,
     if (!vec || !tangent_vec || !tangent_y) return fail(CGTP_E_ARG, "NULL tensor");
     cudaError_t e = launch_sh_jvp(lmax, dtype == CGTP_F64, E, vec, tangent_vec, tangent_y, S(stream));
     if (e != cudaSuccess) return cuda_fail(e, "sh_jvp");
-    count_launch();
     return CGTP_OK;
     GUARD_END
 }
@@ -651,7 +646,6 @@ cgtp_status cgtp_sh_hvp(int lmax, cgtp_dtype dtype, int64_t E, const void* vec,
     cudaError_t e =
         launch_sh_hvp(lmax, dtype == CGTP_F64, E, vec, grad_y, tangent_vec, out, S(stream));
     if (e != cudaSuccess) return cuda_fail(e, "sh_hvp");
-    count_launch();
     return CGTP_OK;
     GUARD_END
 }
@@ -743,7 +737,6 @@ cgtp_status cgtp_linear_forward(cgtp_linear lin, int64_t n, const void* x, const
     cudaError_t e = launch_linear_forward(lin->L, n, x, W, out, workspace, workspace_bytes,
                                           !(flags & CGTP_LINEAR_CUDA_CORES), S(stream));
     if (e != cudaSuccess) return cuda_fail(e, "linear_forward");
-    count_launch();
     return CGTP_OK;
     GUARD_END
 }
@@ -761,7 +754,6 @@ cgtp_status cgtp_linear_backward(cgtp_linear lin, int64_t n, const void* x, cons
         cudaError_t e = launch_linear_backward(lin->L, 0, nullptr, nullptr, nullptr, nullptr,
                                                grad_W, nullptr, 0, false, S(stream));
         if (e != cudaSuccess) return cuda_fail(e, "linear_backward");
-        count_launch();
         return CGTP_OK;
     }
     if (!grad_out || (grad_x && !W) || (grad_W && !x)) return fail(CGTP_E_ARG, "NULL tensor");
@@ -774,7 +766,6 @@ cgtp_status cgtp_linear_backward(cgtp_linear lin, int64_t n, const void* x, cons
                                            workspace_bytes, !(flags & CGTP_LINEAR_CUDA_CORES),
                                            S(stream));
     if (e != cudaSuccess) return cuda_fail(e, "linear_backward");
-    count_launch();
     return CGTP_OK;
     GUARD_END
 }
@@ -834,7 +825,6 @@ cgtp_status cgtp_radial_forward(cgtp_dtype dtype, int64_t E, int n_basis, double
                                           vec, W1, W2, w, h, workspace, workspace_bytes,
                                           S(stream));
     if (e != cudaSuccess) return cuda_fail(e, "radial_forward");
-    count_launch();
     return CGTP_OK;
     GUARD_END
 }
@@ -883,7 +873,6 @@ cgtp_status cgtp_radial_backward(cgtp_dtype dtype, int64_t E, int n_basis, doubl
                                            W2, grad_w, grad_vec, grad_W1, grad_W2, workspace,
                                            S(stream));
     if (e != cudaSuccess) return cuda_fail(e, "radial_backward");
-    count_launch();
     return CGTP_OK;
     GUARD_END
 }
@@ -922,7 +911,6 @@ cgtp_status cgtp_edge_forces(cgtp_dtype dtype, int64_t N, int64_t E, const int32
     cudaError_t e = launch_edge_forces(dtype == CGTP_F64, N, rowptr, s_rowptr, s_perm, dEdr,
                                        forces, S(stream));
     if (e != cudaSuccess) return cuda_fail(e, "edge_forces");
-    count_launch();
     return CGTP_OK;
     GUARD_END
 }
@@ -940,7 +928,6 @@ cgtp_status cgtp_edge_forces_adjoint(cgtp_dtype dtype, int64_t N, int64_t E,
     cudaError_t e = launch_edge_forces_adjoint(dtype == CGTP_F64, N, rowptr, sender, grad_forces,
                                                grad_dEdr, S(stream));
     if (e != cudaSuccess) return cuda_fail(e, "edge_forces_adjoint");
-    count_launch();
     return CGTP_OK;
     GUARD_END
 }

@@ -93,6 +93,7 @@ cudaError_t launch_edge_forces(bool f64, int64_t N, const int32_t* rowptr,
     else
         edge_forces_kernel<float><<<grid_for(N), 128, 0, s>>>(N, rowptr, s_rowptr, s_perm,
                                                              (const float*)dEdr, (float*)F);
+    count_launch();
     return cudaGetLastError();
 }
 
@@ -105,6 +106,7 @@ cudaError_t launch_edge_forces_adjoint(bool f64, int64_t N, const int32_t* rowpt
     else
         edge_forces_adjoint_kernel<float><<<grid_for(N), 128, 0, s>>>(
             N, rowptr, sender, (const float*)gF, (float*)q);
+    count_launch();
     return cudaGetLastError();
 }
 
@@ -117,6 +119,7 @@ cudaError_t launch_reduce_rows(bool f64, const void* partial, int64_t rows, int6
     else
         reduce_rows_kernel<float><<<blocks, 256, 0, s>>>((const float*)partial, rows, cols,
                                                          (float*)out);
+    count_launch();
     return cudaGetLastError();
 }
 
@@ -124,6 +127,7 @@ cudaError_t launch_reduce_rows(bool f64, const void* partial, int64_t rows, int6
 cudaError_t launch_fill_zero(void* p, int64_t bytes, cudaStream_t s) {
     const int64_t words = bytes / 4;
     fill_zero_kernel<<<grid_for(words), 128, 0, s>>>((uint32_t*)p, words);
+    count_launch();
     return cudaGetLastError();
 }
 

@@ -836,6 +836,7 @@ static cudaError_t zero_blocks(const std::vector<std::pair<int, int>>& z, int64_
         if (total == 0) continue;
         const unsigned g = (unsigned)std::min<int64_t>((total + 255) / 256, 4096);
         linear_zero_kernel<T><<<g, 256, 0, s>>>(n, stride, off, width, out);
+        count_launch();
     }
     return cudaGetLastError();
 }
@@ -852,6 +853,7 @@ static cudaError_t run_pass(const LinearImpl& L, const LinDesc& D, int nmax, siz
                      (unsigned)D.nblocks);
         linear_simt_kernel<double><<<g, kLsThreads, 0, s>>>(D, n, (const double*)a,
                                                             (const double*)W, (double*)out);
+        count_launch();
         return cudaGetLastError();
     }
     if (!use_tc) {
@@ -861,9 +863,11 @@ static cudaError_t run_pass(const LinearImpl& L, const LinDesc& D, int nmax, siz
                      (unsigned)D.nblocks);
         linear_simt_kernel<float><<<g, kLsThreads, 0, s>>>(D, n, (const float*)a, (const float*)W,
                                                            (float*)out);
+        count_launch();
         return cudaGetLastError();
     }
     linear_pack_kernel<<<(unsigned)D.nchunks, 256, 0, s>>>(D, (const float*)W, (unsigned char*)img);
+    count_launch();
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     // per-launch copy with the tile ranges of the blocks for this n
@@ -886,6 +890,7 @@ static cudaError_t run_pass(const LinearImpl& L, const LinDesc& D, int nmax, siz
     (void)img_bytes;
     kern<<<grid, kLtThreads, smem, s>>>(*Dn, n, nmax, (const float*)a, (const unsigned char*)img,
                                         (float*)out);
+    count_launch();
     return cudaGetLastError();
 }
 
@@ -931,6 +936,7 @@ cudaError_t launch_linear_backward(const LinearImpl* L, int64_t n, const void* x
         else
             linear_wgrad_kernel<float><<<grid, 256, 0, s>>>(L->grad, n, per, (const float*)x,
                                                             (const float*)g, (float*)part);
+        count_launch();
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
         e = launch_reduce_rows(f64, part, S, L->nw, gW, s);

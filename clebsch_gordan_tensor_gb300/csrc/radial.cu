@@ -1018,6 +1018,7 @@ cudaError_t launch_radial_backward(bool f64, bool tensor_cores, int64_t E, int n
         const unsigned pg =
             (unsigned)std::max<int64_t>(1, std::min<int64_t>((total + 255) / 256, (int64_t)sms * 8));
         radial_pack_t_kernel<<<pg, 256, 0, s>>>(hidden, n_out, (const float*)W2, img);
+        count_launch();
         if ((e = cudaGetLastError())) return e;
         if ((e = cudaFuncSetAttribute(radial_bwd_tc_kernel,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGhSmem)))
@@ -1027,6 +1028,7 @@ cudaError_t launch_radial_backward(bool f64, bool tensor_cores, int64_t E, int n
         radial_bwd_tc_kernel<<<(unsigned)grid, kGhThreads, kGhSmem, s>>>(
             E, nb, (float)rc, hidden, n_out, (const float*)vec, (const float*)W1, img,
             (const float*)gw, (float*)gvec, (float*)p1);
+        count_launch();
         if ((e = cudaGetLastError())) return e;
         if (gW1 && (e = launch_reduce_rows(false, p1, grid, (int64_t)nb * hidden, gW1, s))) return e;
     } else if (gvec || gW1) {
@@ -1038,6 +1040,7 @@ cudaError_t launch_radial_backward(bool f64, bool tensor_cores, int64_t E, int n
                                                    (const double*)W1, (const double*)W2,
                                                    (const double*)gw, (double*)gvec,
                                                    gW1 ? (double*)p1 : nullptr);
+            count_launch();
         } else {
             auto* k = radial_bwd_edge_kernel<float>;
             if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm1)))
@@ -1046,6 +1049,7 @@ cudaError_t launch_radial_backward(bool f64, bool tensor_cores, int64_t E, int n
                                                    (const float*)vec, (const float*)W1,
                                                    (const float*)W2, (const float*)gw,
                                                    (float*)gvec, gW1 ? (float*)p1 : nullptr);
+            count_launch();
         }
         if ((e = cudaGetLastError())) return e;
         if (gW1 && (e = launch_reduce_rows(f64, p1, g1, (int64_t)nb * hidden, gW1, s))) return e;
@@ -1058,6 +1062,7 @@ cudaError_t launch_radial_backward(bool f64, bool tensor_cores, int64_t E, int n
             k<<<(unsigned)(nc * sp), kBwThreads, sm2, s>>>(E, nb, rc, hidden, n_out, sp,
                                                           (const double*)vec, (const double*)W1,
                                                           (const double*)gw, (double*)p2);
+            count_launch();
         } else {
             auto* k = radial_bwd_w2_kernel<float>;
             if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm2)))
@@ -1065,6 +1070,7 @@ cudaError_t launch_radial_backward(bool f64, bool tensor_cores, int64_t E, int n
             k<<<(unsigned)(nc * sp), kBwThreads, sm2, s>>>(E, nb, (float)rc, hidden, n_out, sp,
                                                           (const float*)vec, (const float*)W1,
                                                           (const float*)gw, (float*)p2);
+            count_launch();
         }
         if ((e = cudaGetLastError())) return e;
         if ((e = launch_reduce_rows(f64, p2, sp, (int64_t)hidden * n_out, gW2, s))) return e;
@@ -1103,18 +1109,22 @@ cudaError_t launch_radial_forward(bool f64, bool tensor_cores, bool out_bf16, in
         const unsigned pg =
             (unsigned)std::max<int64_t>(1, std::min<int64_t>((total + 255) / 256, (int64_t)sms * 8));
         radial_pack_kernel<<<pg, 256, 0, s>>>(hidden, n_out, (const float*)W2, (unsigned char*)ws);
+        count_launch();
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
         const int64_t tiles = (E + kTcM - 1) / kTcM;
         const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(tiles, sms));
-        if (out_bf16)
+        if (out_bf16) {
             radial_tc_kernel<__nv_bfloat16><<<grid, kTcThreads, kTcSmem, s>>>(
                 E, nb, (float)rc, hidden, n_out, (const float*)vec, (const float*)W1,
                 (const unsigned char*)ws, (__nv_bfloat16*)w, (float*)h);
-        else
+            count_launch();
+        } else {
             radial_tc_kernel<float><<<grid, kTcThreads, kTcSmem, s>>>(
                 E, nb, (float)rc, hidden, n_out, (const float*)vec, (const float*)W1,
                 (const unsigned char*)ws, (float*)w, (float*)h);
+            count_launch();
+        }
         return cudaGetLastError();
     }
     const size_t es = f64 ? 8 : 4;
@@ -1128,6 +1138,7 @@ cudaError_t launch_radial_forward(bool f64, bool tensor_cores, bool out_bf16, in
         k<<<grid, kSimtThreads, smem, s>>>(E, nb, rc, hidden, n_out, (const double*)vec,
                                            (const double*)W1, (const double*)W2, (double*)w,
                                            (double*)h);
+        count_launch();
     } else if (out_bf16) {
         auto* k = radial_simt_kernel<float, __nv_bfloat16>;
         e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -1135,6 +1146,7 @@ cudaError_t launch_radial_forward(bool f64, bool tensor_cores, bool out_bf16, in
         k<<<grid, kSimtThreads, smem, s>>>(E, nb, (float)rc, hidden, n_out, (const float*)vec,
                                            (const float*)W1, (const float*)W2, (__nv_bfloat16*)w,
                                            (float*)h);
+        count_launch();
     } else {
         auto* k = radial_simt_kernel<float, float>;
         e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -1142,6 +1154,7 @@ cudaError_t launch_radial_forward(bool f64, bool tensor_cores, bool out_bf16, in
         k<<<grid, kSimtThreads, smem, s>>>(E, nb, (float)rc, hidden, n_out, (const float*)vec,
                                            (const float*)W1, (const float*)W2, (float*)w,
                                            (float*)h);
+        count_launch();
     }
     return cudaGetLastError();
 }

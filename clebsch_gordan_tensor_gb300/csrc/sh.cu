@@ -235,6 +235,7 @@ static cudaError_t sh_fwd_t(int lmax, int64_t E, const T* v, T* y, cudaStream_t 
         case 6: sh_forward_kernel<6, T><<<g, 128, 0, s>>>(E, v, y); break;
         default: return cudaErrorInvalidValue;
     }
+    count_launch();
     return cudaGetLastError();
 }
 
@@ -251,6 +252,7 @@ static cudaError_t sh_der_t(int lmax, int64_t E, const T* v, const T* in, T* out
         case 6: sh_deriv_kernel<6, T, B><<<g, 128, 0, s>>>(E, v, in, out); break;
         default: return cudaErrorInvalidValue;
     }
+    count_launch();
     return cudaGetLastError();
 }
 
@@ -268,6 +270,7 @@ static cudaError_t sh_hvp_t(int lmax, int64_t E, const T* v, const T* g, const T
         case 6: sh_hvp_kernel<6, T><<<gr, 128, 0, s>>>(E, v, g, t, out); break;
         default: return cudaErrorInvalidValue;
     }
+    count_launch();
     return cudaGetLastError();
 }
 
