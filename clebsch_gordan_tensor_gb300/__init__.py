@@ -68,12 +68,17 @@ def lib() -> ctypes.CDLL:
                 "cgtp_forward": [vp, i64, vp, vp, vp, vp, vp],
                 "cgtp_backward": [vp, i64, vp, vp, vp, vp, vp, vp, vp, vp],
                 "cgtp_double_backward": [vp, i64, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp],
+                "cgtp_double_backward_ws": [vp, i64, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                            vp, ctypes.c_size_t, vp],
                 "cgtp_conv_forward": [vp, i64, i64, vp, vp, vp, vp, vp, ctypes.c_double, vp, vp],
                 "cgtp_conv_backward": [vp, i64, i64, vp, vp, vp, vp, vp, vp, vp, vp,
                                        ctypes.c_double, vp, vp, vp, vp, vp],
                 "cgtp_conv_double_backward": [vp, i64, i64, vp, vp, vp, vp, vp, vp, vp, vp,
                                               ctypes.c_double, vp, vp, vp, vp, vp, vp, vp, vp,
                                               vp],
+                "cgtp_conv_double_backward_ws": [vp, i64, i64, vp, vp, vp, vp, vp, vp, vp, vp,
+                                                 ctypes.c_double, vp, vp, vp, vp, vp, vp, vp, vp,
+                                                 vp, ctypes.c_size_t, vp],
                 "cgtp_sh_forward": [i32, i32, i64, vp, vp, vp],
                 "cgtp_sh_backward": [i32, i32, i64, vp, vp, vp, vp],
                 "cgtp_sh_jvp": [i32, i32, i64, vp, vp, vp, vp],
@@ -261,13 +266,15 @@ class Plan:
         _check(lib().cgtp_plan_source(self._h, buf, need.value, None))
         return buf.value.decode()
 
-    def _workspace(self, device, gw):
-        """Scratch for the shared-weight gradient (torch-allocated), or None."""
+    def _workspace(self, device, gw, copies: int = 1):
+        """Scratch for the shared-weight gradient (torch-allocated), or None;
+        the double backward takes two copies."""
         if not self.shared_weights or gw is None:
             return None, 0
         n = ctypes.c_size_t()
         _check(lib().cgtp_weight_grad_workspace(self._h, ctypes.byref(n)))
-        return torch.empty(n.value, dtype=torch.uint8, device=device), n.value
+        nb = copies * n.value
+        return torch.empty(nb, dtype=torch.uint8, device=device), nb
 
     def _wshape(self, rows):
         return (self.weight_numel,) if self.shared_weights else (rows, self.weight_numel)
@@ -310,9 +317,10 @@ class Plan:
         dy = torch.empty_like(y) if need[1] else None
         dw = torch.empty_like(w) if need[2] else None
         dg = torch.empty_like(grad_out) if need[3] else None
-        _check(lib().cgtp_double_backward(self._h, B, _ptr(x), _ptr(y), _ptr(w), _ptr(grad_out),
-                                          _ptr(gg_x), _ptr(gg_y), _ptr(gg_w), _ptr(dx), _ptr(dy),
-                                          _ptr(dw), _ptr(dg), _stream()))
+        ws, nws = self._workspace(x.device, dw, 2)
+        _check(lib().cgtp_double_backward_ws(self._h, B, _ptr(x), _ptr(y), _ptr(w), _ptr(grad_out),
+                                             _ptr(gg_x), _ptr(gg_y), _ptr(gg_w), _ptr(dx), _ptr(dy),
+                                             _ptr(dw), _ptr(dg), _ptr(ws), nws, _stream()))
         return dx, dy, dw, dg
 
     # ---- fused convolution
@@ -360,10 +368,12 @@ class Plan:
         dy = torch.empty_like(y) if need[1] else None
         dw = torch.empty_like(w) if need[2] else None
         dg = torch.empty_like(grad_out) if need[3] else None
-        _check(lib().cgtp_conv_double_backward(
+        ws, nws = self._workspace(x.device, dw, 2)
+        _check(lib().cgtp_conv_double_backward_ws(
             self._h, g.N, g.E, _ptr(g.rowptr), _ptr(g.sender), _ptr(g.s_rowptr), _ptr(g.s_perm),
             _ptr(g.s_recv), _ptr(x), _ptr(y), _ptr(w), float(scale), _ptr(grad_out), _ptr(gg_x),
-            _ptr(gg_y), _ptr(gg_w), _ptr(dx), _ptr(dy), _ptr(dw), _ptr(dg), _stream()))
+            _ptr(gg_y), _ptr(gg_w), _ptr(dx), _ptr(dy), _ptr(dw), _ptr(dg), _ptr(ws), nws,
+            _stream()))
         return dx, dy, dw, dg
 
 

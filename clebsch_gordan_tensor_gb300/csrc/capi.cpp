@@ -167,7 +167,8 @@ static cgtp_status bwd_launch(Plan& p, bool conv, int64_t n_items, const int32_t
                               const int32_t* s_perm, const int32_t* s_recv, const void* x,
                               const void* y, const void* w, const void* g, double scale, void* gx,
                               void* gy, void* gw, int mgx, int mgy, int mgw, cudaStream_t s,
-                              void* wsp = nullptr, int64_t ws_rows = 0) {
+                              void* wsp = nullptr, int64_t ws_rows = 0,
+                              int64_t* rows_out = nullptr) {
     if (!mgx && !mgy && !mgw) return CGTP_OK;
     long long n = n_items;
     long long ws = p.wmode == CGTP_W_SHARED ? 0 : p.wdim;
@@ -186,6 +187,10 @@ static cgtp_status bwd_launch(Plan& p, bool conv, int64_t n_items, const int32_t
     cgtp_status st = launch_tp(p, name.c_str(), n_items, args, s, staged, p.bwd_smem,
                                (int)p.bwd_groups.size() * p.lanes, shared ? ws_rows : 0, &rows);
     if (st != CGTP_OK || !shared) return st;
+    if (rows_out) {  // the caller adds these partial rows up with others
+        *rows_out = rows;
+        return CGTP_OK;
+    }
     // ordered sum of the per-CTA partial rows into grad_w
     cudaError_t e = launch_reduce_rows(p.dtype == CGTP_F64, wsp, rows, p.wdim, gw, s);
     if (e != cudaSuccess) return cuda_fail(e, "weight-gradient reduction");
@@ -208,10 +213,20 @@ static cgtp_status double_backward(Plan& p, bool conv, int64_t n_x, int64_t n_e,
                                    const int32_t* s_recv, const void* x, const void* y,
                                    const void* w, double scale, const void* g, const void* ggx,
                                    const void* ggy, const void* ggw, void* dx, void* dy, void* dw,
-                                   void* dg, cudaStream_t s) {
+                                   void* dg, cudaStream_t s, void* wsp = nullptr,
+                                   size_t wsb = 0) {
     cgtp_status st;
-    if (p.wmode == CGTP_W_SHARED && dw)
-        return fail(CGTP_E_UNSUPPORTED, "weight gradient of shared weights is not implemented");
+    // shared weight row: both d_w terms leave per-CTA partial rows side by side
+    // in the workspace, added up in one ordered reduction at the end
+    const bool shw = p.wmode == CGTP_W_SHARED && dw;
+    const int64_t es = esize(p);
+    const size_t part_bytes = (size_t)kSharedWRows * (size_t)p.wdim * (size_t)es;
+    if (shw && (!wsp || wsb < 2 * part_bytes || !aligned(wsp, 16)))
+        return fail(CGTP_E_ARG, "d_w of a shared weight row needs a 16-byte aligned workspace of " +
+                                    std::to_string(2 * part_bytes) +
+                                    " bytes (twice cgtp_weight_grad_workspace): use the _ws entry");
+    int64_t rows_total = 0;
+    auto part_at = [&]() { return (void*)((char*)wsp + rows_total * p.wdim * es); };
     if (dg) {
         int acc = 0;
         const void* terms[3][3] = {{ggx, y, w}, {x, ggy, w}, {x, y, ggw}};
@@ -234,9 +249,12 @@ static cgtp_status double_backward(Plan& p, bool conv, int64_t n_x, int64_t n_e,
     };
     if (ggy) {  // f_x(g; ggy, w) -> dx, f_w(g; x, ggy) -> dw
         const int mx = mode(dx, wx), mw = mode(dw, ww);
+        int64_t rows = 0;
         st = bwd_launch(p, conv, n_x, s_rowptr, s_perm, s_recv, x, ggy, w, g, scale, dx, nullptr,
-                        dw, mx, 0, mw, s);
+                        dw, mx, 0, mw, s, shw ? part_at() : nullptr, kSharedWRows,
+                        shw ? &rows : nullptr);
         if (st != CGTP_OK) return st;
+        rows_total += rows;
     }
     if (ggw) {  // f_x(g; y, ggw) -> dx, f_y(g; x, ggw) -> dy
         const int mx = mode(dx, wx), my = mode(dy, wy);
@@ -246,14 +264,22 @@ static cgtp_status double_backward(Plan& p, bool conv, int64_t n_x, int64_t n_e,
     }
     if (ggx) {  // f_y(g; ggx, w) -> dy, f_w(g; ggx, y) -> dw
         const int my = mode(dy, wy), mw = mode(dw, ww);
+        int64_t rows = 0;
         st = bwd_launch(p, conv, n_x, s_rowptr, s_perm, s_recv, ggx, y, w, g, scale, nullptr, dy,
-                        dw, 0, my, mw, s);
+                        dw, 0, my, mw, s, shw ? part_at() : nullptr, kSharedWRows,
+                        shw ? &rows : nullptr);
         if (st != CGTP_OK) return st;
+        rows_total += rows;
     }
-    const int64_t es = esize(p);
+    if (shw && rows_total > 0) {
+        cudaError_t e = launch_reduce_rows(p.dtype == CGTP_F64, wsp, rows_total, p.wdim, dw, s);
+        if (e != cudaSuccess) return cuda_fail(e, "weight-gradient reduction");
+    }
     if (dx && !wx && (st = zero(dx, n_x * p.dimx * es, s)) != CGTP_OK) return st;
     if (dy && !wy && (st = zero(dy, n_e * p.dimy * es, s)) != CGTP_OK) return st;
-    if (dw && !ww && (st = zero(dw, n_e * p.wdim * es, s)) != CGTP_OK) return st;
+    if (dw && (shw ? rows_total == 0 : !ww) &&
+        (st = zero(dw, (shw ? 1 : n_e) * p.wdim * es, s)) != CGTP_OK)
+        return st;
     return CGTP_OK;
 }
 
@@ -475,10 +501,23 @@ cgtp_status cgtp_double_backward(cgtp_plan plan, int64_t B, const void* x, const
                                  const void* w, const void* grad_out, const void* gg_x,
                                  const void* gg_y, const void* gg_w, void* d_x, void* d_y,
                                  void* d_w, void* d_grad_out, cgtp_stream stream) {
+    return cgtp_double_backward_ws(plan, B, x, y, w, grad_out, gg_x, gg_y, gg_w, d_x, d_y, d_w,
+                                   d_grad_out, nullptr, 0, stream);
+}
+
+cgtp_status cgtp_double_backward_ws(cgtp_plan plan, int64_t B, const void* x, const void* y,
+                                    const void* w, const void* grad_out, const void* gg_x,
+                                    const void* gg_y, const void* gg_w, void* d_x, void* d_y,
+                                    void* d_w, void* d_grad_out, void* workspace,
+                                    size_t workspace_bytes, cgtp_stream stream) {
     GUARD_BEGIN
     if (!plan) return fail(CGTP_E_ARG, "plan is NULL");
     if (B < 0) return fail(CGTP_E_ARG, "B < 0");
-    if (B == 0) return CGTP_OK;
+    if (B == 0) {  // no rows: a shared weight row's d_w is zero
+        Plan& p0 = plan->p;
+        if (p0.wmode == CGTP_W_SHARED && d_w) return zero(d_w, p0.wdim * (int64_t)esize(p0), S(stream));
+        return CGTP_OK;
+    }
     if (!x || !y || !w || !grad_out) return fail(CGTP_E_ARG, "NULL input tensor");
     Plan& p = plan->p;
     if (p.w_bf16) return fail(CGTP_E_UNSUPPORTED, "double backward of a bfloat16-weight plan");
@@ -487,7 +526,7 @@ cgtp_status cgtp_double_backward(cgtp_plan plan, int64_t B, const void* x, const
     if ((st = check_w(p, w)) != CGTP_OK) return st;
     return double_backward(p, false, B, B, B, nullptr, nullptr, nullptr, nullptr, nullptr, x, y,
                            w, 1.0, grad_out, gg_x, gg_y, gg_w, d_x, d_y, d_w, d_grad_out,
-                           S(stream));
+                           S(stream), workspace, workspace_bytes);
     GUARD_END
 }
 
@@ -574,6 +613,20 @@ cgtp_status cgtp_conv_double_backward(cgtp_plan plan, int64_t N, int64_t E, cons
                                       const void* grad_out, const void* gg_x, const void* gg_y,
                                       const void* gg_w, void* d_x, void* d_y, void* d_w,
                                       void* d_grad_out, cgtp_stream stream) {
+    return cgtp_conv_double_backward_ws(plan, N, E, rowptr, sender, s_rowptr, s_perm, s_recv, x,
+                                        y, w, scale, grad_out, gg_x, gg_y, gg_w, d_x, d_y, d_w,
+                                        d_grad_out, nullptr, 0, stream);
+}
+
+cgtp_status cgtp_conv_double_backward_ws(cgtp_plan plan, int64_t N, int64_t E,
+                                         const int32_t* rowptr, const int32_t* sender,
+                                         const int32_t* s_rowptr, const int32_t* s_perm,
+                                         const int32_t* s_recv, const void* x, const void* y,
+                                         const void* w, double scale, const void* grad_out,
+                                         const void* gg_x, const void* gg_y, const void* gg_w,
+                                         void* d_x, void* d_y, void* d_w, void* d_grad_out,
+                                         void* workspace, size_t workspace_bytes,
+                                         cgtp_stream stream) {
     GUARD_BEGIN
     if (!plan) return fail(CGTP_E_ARG, "plan is NULL");
     cgtp_status st = check_graph(N, E, rowptr, sender);
@@ -589,7 +642,7 @@ cgtp_status cgtp_conv_double_backward(cgtp_plan plan, int64_t N, int64_t E, cons
     if ((st = check_w(p, w)) != CGTP_OK) return st;
     return double_backward(p, true, N, E, N, rowptr, sender, s_rowptr, s_perm, s_recv, x, y, w,
                            scale, grad_out, gg_x, gg_y, gg_w, d_x, d_y, d_w, d_grad_out,
-                           S(stream));
+                           S(stream), workspace, workspace_bytes);
     GUARD_END
 }
 

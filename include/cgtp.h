@@ -178,6 +178,16 @@ cgtp_status cgtp_double_backward(cgtp_plan plan, int64_t B, const void* x, const
                                  const void* w, const void* grad_out, const void* gg_x,
                                  const void* gg_y, const void* gg_w, void* d_x, void* d_y,
                                  void* d_w, void* d_grad_out, cgtp_stream stream);
+/* cgtp_double_backward with caller scratch: required (16-byte aligned, at
+ * least twice cgtp_weight_grad_workspace() bytes, contents need not be set)
+ * when d_w is requested from a CGTP_W_SHARED plan, whose d_w sums both terms
+ * over all rows through per-CTA partial rows added in fixed order
+ * (deterministic).  Calls sharing a workspace must not overlap in time. */
+cgtp_status cgtp_double_backward_ws(cgtp_plan plan, int64_t B, const void* x, const void* y,
+                                    const void* w, const void* grad_out, const void* gg_x,
+                                    const void* gg_y, const void* gg_w, void* d_x, void* d_y,
+                                    void* d_w, void* d_grad_out, void* workspace,
+                                    size_t workspace_bytes, cgtp_stream stream);
 
 /* -------------------------------------------- fused graph convolution -- */
 
@@ -234,7 +244,8 @@ cgtp_status cgtp_conv_backward_noalloc(cgtp_plan plan, int64_t N, int64_t E,
                                        cgtp_stream stream);
 
 /* The identity of cgtp_double_backward applied to the fused convolution.
- * CGTP_W_SHARED plans: d_w is not supported (CGTP_E_UNSUPPORTED if non-NULL). */
+ * CGTP_W_SHARED plans: d_w needs the workspace of cgtp_conv_double_backward_ws
+ * (without one, a non-NULL d_w returns CGTP_E_ARG). */
 cgtp_status cgtp_conv_double_backward(cgtp_plan plan, int64_t N, int64_t E, const int32_t* rowptr,
                                       const int32_t* sender, const int32_t* s_rowptr,
                                       const int32_t* s_perm, const int32_t* s_recv, const void* x,
@@ -242,6 +253,16 @@ cgtp_status cgtp_conv_double_backward(cgtp_plan plan, int64_t N, int64_t E, cons
                                       const void* grad_out, const void* gg_x, const void* gg_y,
                                       const void* gg_w, void* d_x, void* d_y, void* d_w,
                                       void* d_grad_out, cgtp_stream stream);
+/* cgtp_conv_double_backward with caller scratch, as cgtp_double_backward_ws. */
+cgtp_status cgtp_conv_double_backward_ws(cgtp_plan plan, int64_t N, int64_t E,
+                                         const int32_t* rowptr, const int32_t* sender,
+                                         const int32_t* s_rowptr, const int32_t* s_perm,
+                                         const int32_t* s_recv, const void* x, const void* y,
+                                         const void* w, double scale, const void* grad_out,
+                                         const void* gg_x, const void* gg_y, const void* gg_w,
+                                         void* d_x, void* d_y, void* d_w, void* d_grad_out,
+                                         void* workspace, size_t workspace_bytes,
+                                         cgtp_stream stream);
 
 /* --------------------------------------------- spherical harmonics ------ */
 /* The per-edge basis "depends on spherical harmonics" of the relative position

@@ -268,3 +268,10 @@ def test_conv_shared_weight_gradient(case):
     assert_close(host(gx), rx, dt, "grad_x")
     assert_close(host(gy), ry, dt, "grad_y")
     assert_close(host(gw), rw, dt, "grad_w")
+    # double backward: d_w sums both terms over all edges
+    ggx, ggy, ggw = (rng.standard_normal(a.shape).astype(dt) for a in (x, y, w))
+    got = plan.conv_double_backward(G, dev(x), dev(y), dev(w), 0.25, dev(g), dev(ggx), dev(ggy),
+                                    dev(ggw))
+    ref = O.conv_double_backward(prob, gr.rowptr, gr.sender, x, y, w, 0.25, g, ggx, ggy, ggw)
+    for a, r, n in zip(got, ref, ("d_x", "d_y", "d_w", "d_g")):
+        assert_close(host(a), r, dt, "double backward " + n)

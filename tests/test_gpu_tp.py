@@ -129,6 +129,41 @@ def test_shared_weight_gradient(B, irreps, dt):
                                          cg._ptr(torch.empty_like(dev(w))), cg._stream()))
 
 
+@pytest.mark.parametrize("B", [1, 3, 5000])
+@pytest.mark.parametrize("irreps,dt", [(("64x0e+64x1o+64x2e", "0e+1o+2e+3o",
+                                         "64x0e+64x1o+64x1e+64x2o+64x2e+64x3o+64x3e"), np.float32),
+                                       (("8x0e+8x1o", "0e+1o+2e", "8x0e+8x1o+8x2e"), np.float64)])
+def test_shared_weight_double_backward(B, irreps, dt):
+    """Double backward of a shared weight row: d_w sums both terms over all
+    samples (partial rows of the two terms side by side, one ordered sum)."""
+    need_gpu()
+    import clebsch_gordan_tensor_gb300 as cg
+    prob = O.make_problem(*irreps)
+    plan = cg.Plan(*irreps, dtype=torch.float64 if dt == np.float64 else torch.float32,
+                   shared_weights=True)
+    rng = np.random.default_rng(B + 1)
+    x = rng.standard_normal((B, prob.dim1)).astype(dt)
+    y = rng.standard_normal((B, prob.dim2)).astype(dt)
+    w = rng.standard_normal(prob.wdim).astype(dt)
+    g = rng.standard_normal((B, prob.dimo)).astype(dt)
+    ggx, ggy, ggw = (rng.standard_normal(a.shape).astype(dt) for a in (x, y, w))
+    got = plan.double_backward(dev(x), dev(y), dev(w), dev(g), dev(ggx), dev(ggy), dev(ggw))
+    ref = O.tp_double_backward(prob, x, y, w, g, ggx, ggy, ggw)
+    for a, r, n in zip(got, ref, ("d_x", "d_y", "d_w", "d_g")):
+        assert_close(host(a), r, dt, n)
+    # d_w from the gg_y term alone
+    _, _, dw, _ = plan.double_backward(dev(x), dev(y), dev(w), dev(g), None, dev(ggy), None,
+                                       need=(False, False, True, False))
+    assert_close(host(dw), O.tp_double_backward(prob, x, y, w, g, None, ggy, None)[2], dt,
+                 "d_w (gg_y only)")
+    # without the workspace the entry point refuses a shared d_w
+    with pytest.raises(cg.CgtpError, match="workspace"):
+        cg._check(cg.lib().cgtp_double_backward(
+            plan._h, B, cg._ptr(dev(x)), cg._ptr(dev(y)), cg._ptr(dev(w)), cg._ptr(dev(g)),
+            cg._ptr(dev(ggx)), None, None, None, None, cg._ptr(torch.empty_like(dev(w))), None,
+            cg._stream()))
+
+
 def test_empty_batch_is_noop():
     need_gpu()
     plan = _plan(*CASES[0])

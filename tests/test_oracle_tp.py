@@ -111,10 +111,13 @@ def test_shared_weights_backward_sums_rows():
     assert np.abs(gw - gw_rows.sum(0)).max() < 1e-12
 
 
-def test_double_backward_finite_differences():
+@pytest.mark.parametrize("shared", [False, True])
+def test_double_backward_finite_differences(shared):
     rng = np.random.default_rng(4)
     prob = O.make_problem(*SMALL)
     x, y, w = _rand(rng, prob, 3)
+    if shared:  # one weight row for every sample: d_w sums the rows
+        w = w[0].copy()
     g = rng.standard_normal((3, prob.dimo))
     ggx, ggy, ggw = (rng.standard_normal(a.shape) for a in (x, y, w))
 
