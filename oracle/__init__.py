@@ -557,3 +557,28 @@ def tp_uvw_forward(irreps_in1: str, irreps_in2: str, irreps_out: str, x, y, W) -
     if W.shape != (ow,):
         raise ValueError("W does not match the paths")
     return out
+
+
+def tp_uvw_backward(irreps_in1: str, irreps_in2: str, irreps_out: str, x, y, W, g):
+    """(dL/dx, dL/dy, dL/dW) of ``tp_uvw_forward`` for dL/dout = g: the
+    contraction with one operand left out at a time (W summed over rows)."""
+    a, b, c = (_blocks(parse_irreps(s)) for s in (irreps_in1, irreps_in2, irreps_out))
+    x, y, W, g = _f64(x), _f64(y), _f64(W), _f64(g)
+    gx, gy, gW = np.zeros_like(x), np.zeros_like(y), np.zeros_like(W)
+    B, ow = x.shape[0], 0
+    for o1, m1, l1, p1 in a:
+        for o2, m2, l2, p2 in b:
+            for o3, m3, l3, p3 in c:
+                if not (abs(l1 - l2) <= l3 <= l1 + l2 and p3 == p1 * p2 and m2 == 1):
+                    continue
+                C = cg_real(l1, l2, l3)
+                xb = x[:, o1:o1 + (2 * l1 + 1) * m1].reshape(B, 2 * l1 + 1, m1)
+                yb = y[:, o2:o2 + 2 * l2 + 1]
+                gb = g[:, o3:o3 + (2 * l3 + 1) * m3].reshape(B, 2 * l3 + 1, m3)
+                Wp = W[ow:ow + m1 * m3].reshape(m1, m3)
+                gx[:, o1:o1 + (2 * l1 + 1) * m1] += np.einsum(
+                    "ijk,bj,uw,bkw->biu", C, yb, Wp, gb).reshape(B, -1)
+                gy[:, o2:o2 + 2 * l2 + 1] += np.einsum("ijk,biu,uw,bkw->bj", C, xb, Wp, gb)
+                gW[ow:ow + m1 * m3] += np.einsum("ijk,biu,bj,bkw->uw", C, xb, yb, gb).ravel()
+                ow += m1 * m3
+    return gx, gy, gW

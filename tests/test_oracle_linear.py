@@ -137,3 +137,32 @@ def test_shape_errors():
         O.linear_forward("2x0e", "2x1o", [(0, 0)], np.zeros((1, 2)), np.zeros(4))
     with pytest.raises(ValueError):
         O.linear_forward("2x0e", "2x0e", [(0, 0)], np.zeros((1, 2)), np.zeros(3))
+
+
+def test_uvw_backward_adjoints_and_finite_differences():
+    """The 'uvw' product is linear in x, in y and in W: <g, f> equals each of
+    <f_x^T g, x>, <f_y^T g, y>, <f_W^T g, W>; central differences in all three."""
+    rng = np.random.default_rng(6)
+    ins = ("3x0e+3x1o+3x2e", "0e+1o+2e", "2x0e+4x1o+2x1e+3x2e")
+    a = O.parse_irreps(ins[0])
+    # the same path list at 3 output channels; one [3, mul_out] matrix per path
+    prob = O.make_problem("3x0e+3x1o+3x2e", "0e+1o+2e", "3x0e+3x1o+3x1e+3x2e")
+    outs = {(l, p): m for m, l, p in O.parse_irreps(ins[2])}
+    nW = sum(3 * outs[(path[5], prob.out[path[2]][2])] for path in prob.paths)
+    x = rng.standard_normal((4, O.irreps_dim(a)))
+    y = O.sh(2, rng.standard_normal((4, 3)))
+    W = rng.standard_normal(nW)
+    g = rng.standard_normal((4, O.irreps_dim(O.parse_irreps(ins[2]))))
+    f = lambda x_, y_, W_: O.tp_uvw_forward(*ins, x_, y_, W_)
+    gx, gy, gW = O.tp_uvw_backward(*ins, x, y, W, g)
+    s = (g * f(x, y, W)).sum()
+    for d, v in ((gx, x), (gy, y), (gW, W)):
+        assert abs((d * v).sum() - s) < 1e-11 * abs(s)
+    h = 1e-6
+    for k, (d, v) in enumerate(((gx, x), (gy, y), (gW, W))):
+        t = rng.standard_normal(v.shape)
+        args_p, args_m = [x, y, W], [x, y, W]
+        args_p[k] = v + h * t
+        args_m[k] = v - h * t
+        fd = ((g * f(*args_p)).sum() - (g * f(*args_m)).sum()) / (2 * h)
+        assert abs(fd - (d * t).sum()) < 1e-8 * max(1.0, abs(fd))
