@@ -638,8 +638,41 @@ class UVWProduct:
         self.weight_numel = self.linear.weight_numel
         self.ones = None
 
-    def forward(self, x, y, W, out=None, mid=None, workspace=None):
+    def _ones(self, x):
         if self.ones is None or self.ones.device != x.device:
             self.ones = torch.ones(self.plan.weight_numel, dtype=x.dtype, device=x.device)
-        mid = self.plan.forward(x, y, self.ones, out=mid)
+        return self.ones
+
+    def forward(self, x, y, W, out=None, mid=None, workspace=None):
+        """out; ``mid`` (optional) receives the per-path blocks [B, dim_mid]."""
+        mid = self.plan.forward(x, y, self._ones(x), out=mid)
         return self.linear.forward(mid, W, out=out, workspace=workspace)
+
+    def backward(self, x, y, W, grad_out, mid=None, need=(True, True, True)):
+        """(grad_x, grad_y, grad_W) for dL/dout = grad_out; ``mid`` = the
+        forward's per-path blocks (recomputed when None)."""
+        if mid is None:
+            mid = self.plan.forward(x, y, self._ones(x))
+        gmid, gW = self.linear.backward(mid, W, grad_out, need=(need[0] or need[1], need[2]))
+        gx = gy = None
+        if need[0] or need[1]:
+            gx, gy, _ = self.plan.backward(x, y, self._ones(x), gmid,
+                                           need=(need[0], need[1], False))
+        return gx, gy, gW
+
+    def conv_forward(self, g: "Graph", x, y, W, scale: float = 1.0, out=None, mid=None):
+        """The fused convolution with 'uvw' paths: receiver sums of the per-path
+        blocks (``mid`` [N, dim_mid]), then the mixing per node."""
+        mid = self.plan.conv_forward(g, x, y, self._ones(x), scale, out=mid)
+        return self.linear.forward(mid, W, out=out)
+
+    def conv_backward(self, g: "Graph", x, y, W, scale, grad_out, mid=None,
+                      need=(True, True, True)):
+        if mid is None:
+            mid = self.plan.conv_forward(g, x, y, self._ones(x), scale)
+        gmid, gW = self.linear.backward(mid, W, grad_out, need=(need[0] or need[1], need[2]))
+        gx = gy = None
+        if need[0] or need[1]:
+            gx, gy, _ = self.plan.conv_backward(g, x, y, self._ones(x), scale, gmid,
+                                                need=(need[0], need[1], False))
+        return gx, gy, gW

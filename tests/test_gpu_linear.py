@@ -102,3 +102,50 @@ def test_uvw_product_matches_oracle():
     out = uvw.forward(dev(x), y, dev(W))
     ref = O.tp_uvw_forward(*UVW_SMALL, x, O.sh(3, v), W)
     assert_close(host(out), ref, np.float32, "uvw out")
+
+
+def test_uvw_backward_matches_oracle():
+    need_gpu()
+    cg = _cg()
+    rng = np.random.default_rng(8)
+    B = 257
+    uvw = cg.UVWProduct(*UVW_SMALL)
+    x = rng.standard_normal((B, uvw.dim_in1)).astype(np.float32)
+    v = rng.standard_normal((B, 3)).astype(np.float32)
+    W = (rng.standard_normal(uvw.weight_numel) / 16).astype(np.float32)
+    g = rng.standard_normal((B, uvw.dim_out)).astype(np.float32)
+    y = cg.sh_forward(dev(v), 3)
+    gx, gy, gW = uvw.backward(dev(x), y, dev(W), dev(g))
+    rx, ry, rW = O.tp_uvw_backward(*UVW_SMALL, x, host(y), W, g)
+    assert_close(host(gx), rx, np.float32, "uvw grad_x")
+    assert_close(host(gy), ry, np.float32, "uvw grad_y")
+    assert_close(host(gW), rW, np.float32, "uvw grad_W")
+
+
+def test_uvw_convolution_matches_oracle():
+    """Fused convolution with 'uvw' paths: the standalone 'uvw' product of each
+    edge, summed per receiver (and its gradient), on a random graph."""
+    need_gpu()
+    cg = _cg()
+    from tests.test_gpu_conv import _graph
+    rng = np.random.default_rng(9)
+    gr = _graph(rng, 120, max_deg=9)
+    G = cg.Graph.from_numpy(gr)
+    uvw = cg.UVWProduct(*UVW_SMALL)
+    x = rng.standard_normal((gr.N, uvw.dim_in1)).astype(np.float32)
+    y = O.sh(3, rng.standard_normal((gr.E, 3))).astype(np.float32)
+    W = (rng.standard_normal(uvw.weight_numel) / 16).astype(np.float32)
+    g = rng.standard_normal((gr.N, uvw.dim_out)).astype(np.float32)
+    scale = 0.5
+    out = uvw.conv_forward(G, dev(x), dev(y), dev(W), scale)
+    per_edge = O.tp_uvw_forward(*UVW_SMALL, x[gr.sender], y, W)
+    ref = np.zeros((gr.N, uvw.dim_out))
+    np.add.at(ref, gr.receiver, scale * per_edge)
+    assert_close(host(out), ref, np.float32, "uvw conv out")
+    gx, gy, gW = uvw.conv_backward(G, dev(x), dev(y), dev(W), scale, dev(g))
+    ex, ey, eW = O.tp_uvw_backward(*UVW_SMALL, x[gr.sender], y, W, scale * g[gr.receiver])
+    rx = np.zeros((gr.N, uvw.dim_in1))
+    np.add.at(rx, gr.sender, ex)
+    assert_close(host(gx), rx, np.float32, "uvw conv grad_x")
+    assert_close(host(gy), ey, np.float32, "uvw conv grad_y")
+    assert_close(host(gW), eW, np.float32, "uvw conv grad_W")
