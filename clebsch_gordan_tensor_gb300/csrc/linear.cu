@@ -282,10 +282,12 @@ __device__ __forceinline__ void tmem_st16(unsigned taddr, const float (&v)[16]) 
 }
 
 // Packed B image of every chunk: rows = output columns c < ncols, K-major
-// core matrices, the TF32 hi part then the lo part (ncols * 32 * 4 bytes each).
+// core matrices, the TF32 hi part then the lo part (ncols * 32 * 4 bytes each);
+// stacked: one image of 2 ncols rows, hi in rows c, lo in rows ncols + c (the
+// B operand of a single N = 2 ncols product A_hi [B_hi | B_lo]).
 // grid: x = chunk.
 __global__ void linear_pack_kernel(const __grid_constant__ LinDesc D, const float* __restrict__ W,
-                                   unsigned char* __restrict__ img) {
+                                   unsigned char* __restrict__ img, bool stacked) {
     const int ci = blockIdx.x;
     int b = 0;
     while (b + 1 < D.nblocks && D.blk[b + 1].chunk0 <= ci) ++b;
@@ -298,9 +300,14 @@ __global__ void linear_pack_kernel(const __grid_constant__ LinDesc D, const floa
         const float v =
             k < C.kc ? W[C.w_off + (int64_t)(C.k0 + k) * C.w_ks + (int64_t)c * C.w_ns] : 0.0f;
         const float hi = to_tf32(v), lo = to_tf32(v - hi);
-        const unsigned o = kmajor_offset(c, k, N);
-        *reinterpret_cast<float*>(base + o) = hi;
-        *reinterpret_cast<float*>(base + part + o) = lo;
+        if (stacked) {
+            *reinterpret_cast<float*>(base + kmajor_offset(c, k, 2 * N)) = hi;
+            *reinterpret_cast<float*>(base + kmajor_offset(N + c, k, 2 * N)) = lo;
+        } else {
+            const unsigned o = kmajor_offset(c, k, N);
+            *reinterpret_cast<float*>(base + o) = hi;
+            *reinterpret_cast<float*>(base + part + o) = lo;
+        }
     }
 }
 
@@ -331,7 +338,7 @@ __global__ void linear_pack_kernel(const __grid_constant__ LinDesc D, const floa
 // b_full / b_free; unit t uses phase (t / NACC) % 2 of acc_full / acc_free.
 // Every wait is bounded; after a timeout the remaining waits return at once,
 // each role leaves its loop, and the issuer drains what it issued.
-template <int RB, int NACC>
+template <int RB, int NACC, bool STACK>
 __global__ void __launch_bounds__(kLtThreads, 1)
 linear_tc_kernel(const __grid_constant__ LinDesc D, int64_t n, int nmax,
                  const float* __restrict__ x, const unsigned char* __restrict__ img,
@@ -385,15 +392,19 @@ linear_tc_kernel(const __grid_constant__ LinDesc D, int64_t n, int nmax,
     const unsigned tmem = tmem_base;
 
     const bool issuer = warp == kLtEpiWarps + kLtProdWarps;
+    // after a timeout elsewhere the remaining waits return at once (the issuer
+    // reads the flag once per unit instead, and its next wait runs out)
     auto wait = [&](unsigned long long* bar, unsigned parity) -> bool {
-        if (*(volatile int*)&fail) return false;
+        if (!issuer && *(volatile int*)&fail) return false;
         if (issuer ? tc_mbar_wait(bar, parity) : tc_mbar_wait_sleep(bar, parity)) return true;
         atomicExch(&fail, 1);
         return false;
     };
+    // position in this CTA's chunk sequence, with the current block's fields
+    // held in registers (the issuer reads no table per chunk)
     struct Pos {
         int64_t u, t;
-        int b, ci;
+        int b, ci, nch, ncols, chunk0, rot;
         bool valid;
     };
     // tiles of block b: [blk[b].tile0, blk[b + 1].tile0); blk[nblocks].tile0 = total
@@ -404,10 +415,17 @@ linear_tc_kernel(const __grid_constant__ LinDesc D, int64_t n, int nmax,
             p.b = 0;
             while (p.u >= sblk[p.b + 1].tile0) ++p.b;
         }
-        p.t = p.u - sblk[p.b].tile0;
+        const LinBlock& B = sblk[p.b];
+        p.t = p.u - B.tile0;
+        p.nch = B.nchunk;
+        p.ncols = B.ncols;
+        p.chunk0 = B.chunk0;
+        // the chunks of a unit are taken in an order rotated by the CTA index,
+        // so that the CTAs do not all read the same B chunk at once
+        p.rot = (int)(blockIdx.x % (unsigned)B.nchunk);
     };
     auto advance = [&](Pos& p) {
-        if (p.ci + 1 < sblk[p.b].nchunk) {
+        if (p.ci + 1 < p.nch) {
             ++p.ci;
         } else {
             p.u += gridDim.x;
@@ -415,13 +433,12 @@ linear_tc_kernel(const __grid_constant__ LinDesc D, int64_t n, int nmax,
             locate(p);
         }
     };
-    // the chunks of a unit are taken in an order rotated by the CTA index, so
-    // that the CTAs do not all read the same B chunk at once
-    auto chunk_of = [&](const Pos& p) -> const LinChunk& {
-        const LinBlock& B = sblk[p.b];
-        return sch[B.chunk0 + (int)(((unsigned)p.ci + blockIdx.x) % (unsigned)B.nchunk)];
+    auto chunk_index = [&](const Pos& p) {
+        const int c = p.ci + p.rot;
+        return p.chunk0 + (c >= p.nch ? c - p.nch : c);
     };
-    Pos start{(int64_t)blockIdx.x, 0, 0, 0, false};
+    auto chunk_of = [&](const Pos& p) -> const LinChunk& { return sch[chunk_index(p)]; };
+    Pos start{(int64_t)blockIdx.x, 0, 0, 0, 1, 0, 0, 0, false};
     locate(start);
 
     if (warp >= kLtEpiWarps && warp < kLtEpiWarps + kLtProdWarps) {
@@ -500,20 +517,23 @@ linear_tc_kernel(const __grid_constant__ LinDesc D, int64_t n, int nmax,
         // MMAs and commits
         const bool leader = lane == 0;
         {
-            int b_issued[RB], b_waited[RB];
-            for (int i = 0; i < RB; ++i) b_issued[i] = b_waited[i] = 0;
+            int64_t kw = 0;  // chunks whose B copy has been waited for
             int64_t last_commit = -1;
             Pos bp = start, cur = start;
+            int img_b = -1, img0 = 0;  // block whose first-chunk image offset is cached
             auto issue_b = [&](int64_t kb) {  // B of the chunk at bp (= chunk kb)
                 const int slot = (int)(kb % RB);
-                const LinBlock& B = sblk[bp.b];
-                const LinChunk& C = chunk_of(bp);
-                const unsigned bytes = 2u * (unsigned)B.ncols * kLtK * 4;
+                const unsigned bytes = 2u * (unsigned)bp.ncols * kLtK * 4;
+                if (bp.b != img_b) {  // a block's chunk images are consecutive, equal in size
+                    img_b = bp.b;
+                    img0 = sch[bp.chunk0].img_off;
+                }
+                const int c = chunk_index(bp) - bp.chunk0;
                 if (leader) {
                     tc_expect_tx(&b_full[slot], bytes);
-                    tc_bulk_g2s(Bbase + (size_t)slot * bslot, img + C.img_off, bytes, &b_full[slot]);
+                    tc_bulk_g2s(Bbase + (size_t)slot * bslot, img + img0 + (size_t)c * bytes, bytes,
+                                &b_full[slot]);
                 }
-                ++b_issued[slot];
                 advance(bp);
             };
             // B runs RB - 2 chunks ahead: the slot a refill takes was read by the
@@ -524,12 +544,11 @@ linear_tc_kernel(const __grid_constant__ LinDesc D, int64_t n, int nmax,
             bool ok = true;
             while (cur.valid && ok) {
                 const int s = (int)(k % RA), slot = (int)(k % RB);
-                const LinBlock& B = sblk[cur.b];
-                const int N = B.ncols;
-                const bool first = cur.ci == 0, last = cur.ci + 1 == B.nchunk;
+                const int N = cur.ncols;
+                const bool first = cur.ci == 0, last = cur.ci + 1 == cur.nch;
                 const int acc = (int)(t % NACC);
                 ok = wait(&b_full[slot], (unsigned)((k / RB) & 1));
-                if (ok) ++b_waited[slot];
+                if (ok) kw = k + 1;
                 ok = ok && wait(&a_full[s], (unsigned)((k / RA) & 1));
                 if (ok && first && t >= NACC)
                     ok = wait(&acc_free[acc], (unsigned)(((t - NACC) / NACC) & 1));
@@ -537,12 +556,23 @@ linear_tc_kernel(const __grid_constant__ LinDesc D, int64_t n, int nmax,
                 if (!ok) break;
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
                 const uint32_t idesc = tf32_idesc(kLtM, N);
-                const unsigned lb = (unsigned)(N / 8) * 128;
                 const unsigned b0 = smem_addr(Bbase + (size_t)slot * bslot);
-                const unsigned bpart = (unsigned)N * kLtK * 4;
                 const unsigned d = tmem + (unsigned)acc * accw;
                 const unsigned a0 = tmem + kLtAcol + 64u * s;
-                if (leader) {
+                if (leader && STACK) {
+                    // A_hi [B_hi | B_lo] (N = 2 ncols) into columns [0, 2 ncols),
+                    // A_lo B_hi into [0, ncols); the epilogue adds the halves
+                    const uint32_t idesc2 = tf32_idesc(kLtM, 2 * N);
+                    const unsigned lb = (unsigned)(2 * N / 8) * 128;
+#pragma unroll
+                    for (int k8 = 0; k8 < kLtK; k8 += 8) {
+                        const uint64_t bd = smem_desc(b0 + (unsigned)(k8 >> 2) * lb, lb, 128);
+                        mma_tf32_tmem_a(d, a0 + k8, bd, idesc2, (first && k8 == 0) ? 0u : 1u);
+                        mma_tf32_tmem_a(d, a0 + 32 + k8, bd, idesc, 1u);
+                    }
+                } else if (leader) {
+                    const unsigned lb = (unsigned)(N / 8) * 128;
+                    const unsigned bpart = (unsigned)N * kLtK * 4;
 #pragma unroll
                     for (int k8 = 0; k8 < kLtK; k8 += 8) {
                         const unsigned kk = (unsigned)(k8 >> 2) * lb;
@@ -552,6 +582,8 @@ linear_tc_kernel(const __grid_constant__ LinDesc D, int64_t n, int nmax,
                         mma_tf32_tmem_a(d, a0 + k8, bl, idesc, 1u);
                         mma_tf32_tmem_a(d, a0 + 32 + k8, bh, idesc, 1u);
                     }
+                }
+                if (leader) {
                     tc_commit(&a_free[s]);
                     tc_commit(&b_free[slot]);
                     if (last) tc_commit(&acc_full[acc]);
@@ -571,15 +603,12 @@ linear_tc_kernel(const __grid_constant__ LinDesc D, int64_t n, int nmax,
                 if (last) ++t;
                 advance(cur);
                 ++k;
-                if (*(volatile int*)&fail) break;
+                if (last && __any_sync(0xffffffffu, *(volatile int*)&fail)) break;
             }
             // drain: bulk copies issued but never waited for, the last MMAs
             if (leader) {
-                for (int q = 0; q < RB; ++q)
-                    while (b_waited[q] < b_issued[q]) {
-                        tc_mbar_wait(&b_full[q], (unsigned)(b_waited[q] & 1));
-                        ++b_waited[q];
-                    }
+                for (int64_t c = kw; c < kb; ++c)  // copies issued, never waited for
+                    tc_mbar_wait(&b_full[c % RB], (unsigned)((c / RB) & 1));
                 if (last_commit >= 0)
                     tc_mbar_wait(&a_free[last_commit % RA], (unsigned)((last_commit / RA) & 1));
             }
@@ -606,7 +635,14 @@ linear_tc_kernel(const __grid_constant__ LinDesc D, int64_t n, int nmax,
             }
             for (int c0 = 0; c0 < EB.ncols; c0 += 32) {
                 float v[32];
-                tmem_ld32(tmem + ((unsigned)(32 * q) << 16) + (unsigned)acc * accw + (unsigned)c0, v);
+                const unsigned ta = tmem + ((unsigned)(32 * q) << 16) + (unsigned)acc * accw + (unsigned)c0;
+                tmem_ld32(ta, v);
+                if (STACK) {  // + the A_hi B_lo half
+                    float v2[32];
+                    tmem_ld32(ta + (unsigned)EB.ncols, v2);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] += v2[i];
+                }
                 // transpose through shared memory: 8 lanes store one row's 128 bytes
 #pragma unroll
                 for (int i = 0; i < 8; ++i)
@@ -866,7 +902,11 @@ static cudaError_t run_pass(const LinearImpl& L, const LinDesc& D, int nmax, siz
         count_launch();
         return cudaGetLastError();
     }
-    linear_pack_kernel<<<(unsigned)D.nchunks, 256, 0, s>>>(D, (const float*)W, (unsigned char*)img);
+    // up to 128 columns: A_hi [B_hi | B_lo] as one N = 2 ncols product (stacked
+    // B image), one accumulator of 2 ncols columns; 256: three products
+    const bool stack = nmax <= 128;
+    linear_pack_kernel<<<(unsigned)D.nchunks, 256, 0, s>>>(D, (const float*)W, (unsigned char*)img,
+                                                          stack);
     count_launch();
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -879,12 +919,9 @@ static cudaError_t run_pass(const LinearImpl& L, const LinDesc& D, int nmax, siz
     }
     Dn->blk[D.nblocks].tile0 = units;
     const unsigned grid = (unsigned)std::min<int64_t>(units, sm_count());
-    // up to 128 columns: two accumulators and a 4-slot B ring; 256: one and 3
-    const bool two = nmax <= 128;
-    // at least half of the SM's shared memory: one CTA per SM, which the
-    // 512-column tensor-memory allocation needs
-    const size_t smem = std::max<size_t>(120 * 1024, two ? lt_smem_bytes(nmax, 4) : lt_smem_bytes(nmax, 3));
-    auto* kern = two ? linear_tc_kernel<4, 2> : linear_tc_kernel<3, 1>;
+    // B ring: 4 slots up to 128 columns, 3 at 256
+    const size_t smem = std::max<size_t>(120 * 1024, stack ? lt_smem_bytes(nmax, 4) : lt_smem_bytes(nmax, 3));
+    auto* kern = stack ? linear_tc_kernel<4, 1, true> : linear_tc_kernel<3, 1, false>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     (void)img_bytes;
