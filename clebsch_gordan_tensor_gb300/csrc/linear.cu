@@ -222,17 +222,21 @@ constexpr int kLtM = 128;                    // rows per tile (MMA M, TMEM lanes
 constexpr int kLtK = 32;                     // K per chunk
 constexpr int kLtEpiWarps = 4;               // one per TMEM lane quarter
 constexpr int kLtProdWarps = 8;              // two per lane quarter, 16 K columns each
-constexpr int kLtThreads = 32 * (kLtEpiWarps + kLtProdWarps + 1);  // + the MMA issuer warp
-constexpr int kLtRA = 4;                     // A stages in tensor memory
+constexpr int kLtThreads = 32 * (kLtEpiWarps + kLtProdWarps + 2);  // + MMA issuer, loader
 constexpr unsigned kLtTmemCols = 512;        // accumulators in [0, 256), A stages in [256, 512)
 constexpr unsigned kLtAcol = 256;            // first column of A stage 0 (hi 32, lo 32 per stage)
 
 // Dynamic shared memory: RB B slots (hi + lo of up to nmax rows), the
 // epilogue warps' staging blocks and the block / chunk tables.
 constexpr unsigned kLtStagePitch = 36;  // floats per staged epilogue row (conflict-free)
-constexpr unsigned kLtStage = 32 * kLtStagePitch * 4;  // one epilogue warp's 32 x 32 block
-__host__ __device__ constexpr unsigned lt_smem_bytes(int nmax, int RB) {
-    return (unsigned)RB * 2u * (unsigned)nmax * kLtK * 4 + kLtEpiWarps * kLtStage +
+// Epilogue staging per warp: 32 rows x (nmax + 4) floats holding a whole tile
+// row block (stacked products), else one 32 x 32 block at a time.
+__host__ __device__ constexpr unsigned lt_stage_pitch(int nmax, bool wide) {
+    return wide ? (unsigned)nmax + 4 : kLtStagePitch;
+}
+__host__ __device__ constexpr unsigned lt_smem_bytes(int nmax, int RB, bool wide) {
+    return (unsigned)RB * 2u * (unsigned)nmax * kLtK * 4 +
+           kLtEpiWarps * 32 * lt_stage_pitch(nmax, wide) * 4 +
            (unsigned)((kLinMaxBlocks + 1) * sizeof(LinBlock) + kLinMaxChunks * sizeof(LinChunk));
 }
 
@@ -314,39 +318,42 @@ __global__ void linear_pack_kernel(const __grid_constant__ LinDesc D, const floa
 // Work units are (block, 128-row tile) pairs, blocks in order; CTA c takes
 // units c, c + grid, ...; every role walks the same sequence, taking a unit's
 // chunks in an order rotated by c (the CTAs then read different B chunks at
-// the same time).  Chunk k uses A stage k % 4 in tensor memory and B slot
-// k % RB.  Warp roles:
+// the same time).  Chunk k uses stage k % S: A columns in tensor memory and a
+// B slot in shared memory.  Warp roles:
 //   producers (warps 4-11; warp 4 + p serves TMEM lanes 32 (p % 4) .. + 31,
 //     one row per lane, K columns 16 (p / 4) .. + 15 of each chunk): the rows
 //     are loaded into registers three chunks ahead; once the MMAs of chunk
-//     k - 4 have released the stage (a_free) the warp writes chunk k's values
+//     k - S have released the stage (empty) the warp writes chunk k's values
 //     as they are (the tensor cores read them as the TF32 "hi" part, which
 //     keeps the leading 10 fraction bits) and the "lo" parts, lo =
-//     round_tf32(x - x cut to 10 fraction bits), into the stage with
-//     tcgen05.st and arrives on a_full (one arrival per warp).
-//   issuer (warp 12, lane 0 issuing): B chunk k arrives in ring slot k % RB by bulk
-//     copy (b_full), issued RB - 1 chunks ahead once the MMAs that read the
-//     slot have completed (b_free); it issues chunk k's hi*hi, hi*lo, lo*hi
-//     products (A from tensor memory, B from shared memory) into accumulator
-//     t % NACC of unit t (after acc_free says the epilogue has read unit
-//     t - NACC), then commits them to a_free, b_free and, after a unit's last
-//     chunk, acc_full.
+//     round_tf32(x - x cut to 10 fraction bits), with tcgen05.st and arrives
+//     on full (one arrival per warp).
+//   loader (warp 13, one thread): once the stage is empty, starts the bulk
+//     copy of chunk k's B image into its slot, arriving on full with the
+//     expected byte count.
+//   MMA issuer (warp 12, lane 0 issuing): one wait per chunk (full: A written
+//     and B landed), then the products (A from tensor memory, B from shared
+//     memory) into accumulator t % NACC of unit t (after acc_free says the
+//     epilogue has read unit t - NACC), committed to empty and, after a unit's
+//     last chunk, to acc_full.  Each wait of this thread leaves the tensor
+//     pipe without queued work for its latency, so it waits once per chunk.
 //   epilogue (warps 0-3): per unit, wait acc_full, read the 32 rows of its lane
 //     quarter, transpose 32 x 32 pieces through shared memory, store whole
 //     128-byte row segments and arrive on acc_free.
-// Chunk k uses phase (k / 4) % 2 of a_full / a_free and (k / RB) % 2 of
-// b_full / b_free; unit t uses phase (t / NACC) % 2 of acc_full / acc_free.
-// Every wait is bounded; after a timeout the remaining waits return at once,
-// each role leaves its loop, and the issuer drains what it issued.
-template <int RB, int NACC, bool STACK>
+// Chunk k uses phase (k / S) % 2 of full / empty; unit t uses phase
+// (t / NACC) % 2 of acc_full / acc_free.  Every wait is bounded; after a
+// timeout the remaining waits return at once, each role leaves its loop, and
+// the loader drains the copies it started.
+template <int S, int NACC, bool STACK>
 __global__ void __launch_bounds__(kLtThreads, 1)
 linear_tc_kernel(const __grid_constant__ LinDesc D, int64_t n, int nmax,
                  const float* __restrict__ x, const unsigned char* __restrict__ img,
                  float* __restrict__ out) {
-    constexpr int RA = kLtRA;
+    constexpr int RA = S;
+    constexpr int RB = S;
     constexpr unsigned accw = 256 / NACC;  // columns per accumulator
     extern __shared__ __align__(1024) unsigned char smem[];
-    __shared__ __align__(8) unsigned long long a_full[RA], a_free[RA], b_full[RB], b_free[RB];
+    __shared__ __align__(8) unsigned long long full[S], empty[S];
     __shared__ __align__(8) unsigned long long acc_full[2], acc_free[2];
     __shared__ unsigned tmem_base;
     __shared__ int fail;
@@ -356,7 +363,8 @@ linear_tc_kernel(const __grid_constant__ LinDesc D, int64_t n, int nmax,
     float* stage_all = reinterpret_cast<float*>(Bbase + (size_t)RB * bslot);
     // the block and chunk tables, copied to shared memory (indexed lookups in
     // the parameter space would go through the small constant cache)
-    LinBlock* sblk = reinterpret_cast<LinBlock*>(stage_all + kLtEpiWarps * 32 * kLtStagePitch);
+    const unsigned pitch = lt_stage_pitch(nmax, STACK);
+    LinBlock* sblk = reinterpret_cast<LinBlock*>(stage_all + kLtEpiWarps * 32 * pitch);
     LinChunk* sch = reinterpret_cast<LinChunk*>(sblk + kLinMaxBlocks + 1);
     for (int i = tid; i <= D.nblocks; i += kLtThreads) sblk[i] = D.blk[i];
     for (int i = tid; i < D.nchunks; i += kLtThreads) sch[i] = D.ch[i];
@@ -371,17 +379,13 @@ linear_tc_kernel(const __grid_constant__ LinDesc D, int64_t n, int nmax,
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
     if (tid == 0) {
-        for (int i = 0; i < RA; ++i) {
-            tc_mbar_init(&a_full[i], kLtProdWarps);
-            tc_mbar_init(&a_free[i], 1);
+        for (int i = 0; i < S; ++i) {
+            tc_mbar_init(&full[i], kLtProdWarps + 1);  // producer warps + the loader
+            tc_mbar_init(&empty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
             tc_mbar_init(&acc_full[i], 1);
             tc_mbar_init(&acc_free[i], 32 * kLtEpiWarps);
-        }
-        for (int i = 0; i < RB; ++i) {
-            tc_mbar_init(&b_full[i], 1);
-            tc_mbar_init(&b_free[i], 1);
         }
         fail = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -392,11 +396,13 @@ linear_tc_kernel(const __grid_constant__ LinDesc D, int64_t n, int nmax,
     const unsigned tmem = tmem_base;
 
     const bool issuer = warp == kLtEpiWarps + kLtProdWarps;
+    const bool loader = warp == kLtEpiWarps + kLtProdWarps + 1;
     // after a timeout elsewhere the remaining waits return at once (the issuer
     // reads the flag once per unit instead, and its next wait runs out)
     auto wait = [&](unsigned long long* bar, unsigned parity) -> bool {
         if (!issuer && *(volatile int*)&fail) return false;
-        if (issuer ? tc_mbar_wait(bar, parity) : tc_mbar_wait_sleep(bar, parity)) return true;
+        if (issuer || loader ? tc_mbar_wait(bar, parity) : tc_mbar_wait_sleep(bar, parity))
+            return true;
         atomicExch(&fail, 1);
         return false;
     };
@@ -483,7 +489,7 @@ linear_tc_kernel(const __grid_constant__ LinDesc D, int64_t n, int nmax,
             float4 v3[4];
             load(pre, v3);  // three chunks ahead
             if (pre.valid) advance(pre);
-            if (k >= RA && !wait(&a_free[s], (unsigned)(((k - RA) / RA) & 1))) break;
+            if (k >= S && !wait(&empty[s], (unsigned)(((k - S) / S) & 1))) break;
             float hi[16], lo[16];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
@@ -501,7 +507,7 @@ linear_tc_kernel(const __grid_constant__ LinDesc D, int64_t n, int nmax,
             asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
             asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
             __syncwarp();
-            if (lane == 0) tc_mbar_arrive(&a_full[s]);  // one arrival per warp
+            if (lane == 0) tc_mbar_arrive(&full[s]);  // one arrival per warp
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 v0[j] = v1[j];
@@ -511,55 +517,59 @@ linear_tc_kernel(const __grid_constant__ LinDesc D, int64_t n, int nmax,
             advance(cur);
             if (*(volatile int*)&fail) break;
         }
-    } else if (warp == kLtEpiWarps + kLtProdWarps) {
-        // ------------------------------------------------------------- issuer
-        // the whole warp walks the loop (converged); lane 0 issues the copies,
-        // MMAs and commits
-        const bool leader = lane == 0;
-        {
-            int64_t kw = 0;  // chunks whose B copy has been waited for
-            int64_t last_commit = -1;
-            Pos bp = start, cur = start;
+    } else if (loader) {
+        // ------------------------------------------------------------- loader
+        if (lane == 0) {
+            Pos bp = start;
             int img_b = -1, img0 = 0;  // block whose first-chunk image offset is cached
-            auto issue_b = [&](int64_t kb) {  // B of the chunk at bp (= chunk kb)
-                const int slot = (int)(kb % RB);
+            int64_t k = 0;
+            for (; bp.valid; ++k) {
+                const int s = (int)(k % S);
+                if (k >= S && !wait(&empty[s], (unsigned)(((k - S) / S) & 1))) break;
                 const unsigned bytes = 2u * (unsigned)bp.ncols * kLtK * 4;
                 if (bp.b != img_b) {  // a block's chunk images are consecutive, equal in size
                     img_b = bp.b;
                     img0 = sch[bp.chunk0].img_off;
                 }
                 const int c = chunk_index(bp) - bp.chunk0;
-                if (leader) {
-                    tc_expect_tx(&b_full[slot], bytes);
-                    tc_bulk_g2s(Bbase + (size_t)slot * bslot, img + img0 + (size_t)c * bytes, bytes,
-                                &b_full[slot]);
-                }
+                tc_expect_tx(&full[s], bytes);
+                tc_bulk_g2s(Bbase + (size_t)s * bslot, img + img0 + (size_t)c * bytes, bytes,
+                            &full[s]);
                 advance(bp);
-            };
-            // B runs RB - 2 chunks ahead: the slot a refill takes was read by the
-            // MMAs of two chunks back, long complete, so the wait costs nothing
-            int64_t kb = 0;
-            for (; kb < RB - 1 && bp.valid; ++kb) issue_b(kb);
-            int64_t k = 0, t = 0;
-            bool ok = true;
-            while (cur.valid && ok) {
-                const int s = (int)(k % RA), slot = (int)(k % RB);
-                const int N = cur.ncols;
-                const bool first = cur.ci == 0, last = cur.ci + 1 == cur.nch;
-                const int acc = (int)(t % NACC);
-                ok = wait(&b_full[slot], (unsigned)((k / RB) & 1));
-                if (ok) kw = k + 1;
-                ok = ok && wait(&a_full[s], (unsigned)((k / RA) & 1));
-                if (ok && first && t >= NACC)
-                    ok = wait(&acc_free[acc], (unsigned)(((t - NACC) / NACC) & 1));
-                ok = __all_sync(0xffffffffu, ok);
-                if (!ok) break;
-                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                const uint32_t idesc = tf32_idesc(kLtM, N);
-                const unsigned b0 = smem_addr(Bbase + (size_t)slot * bslot);
-                const unsigned d = tmem + (unsigned)acc * accw;
-                const unsigned a0 = tmem + kLtAcol + 64u * s;
-                if (leader && STACK) {
+                if ((k & 15) == 15 && *(volatile int*)&fail) {
+                    ++k;
+                    break;
+                }
+            }
+            // drain: the copies of the last S chunks may still be in flight;
+            // each completes its stage's phase once the producers arrived too,
+            // so wait on the copies alone through a fresh phase check of the
+            // transaction count (bounded)
+            for (int64_t c = k > S ? k - S : 0; c < k; ++c)
+                tc_mbar_wait(&full[c % S], (unsigned)((c / S) & 1));
+        }
+    } else if (issuer) {
+        // ---------------------------------------------------------- MMA issuer
+        // the whole warp walks the loop (converged); lane 0 issues
+        const bool leader = lane == 0;
+        Pos cur = start;
+        int64_t k = 0, t = 0, last_commit = -1;
+        while (cur.valid) {
+            const int s = (int)(k % S);
+            const int N = cur.ncols;
+            const bool first = cur.ci == 0, last = cur.ci + 1 == cur.nch;
+            const int acc = (int)(t % NACC);
+            bool ok = wait(&full[s], (unsigned)((k / S) & 1));
+            if (ok && first && t >= NACC)
+                ok = wait(&acc_free[acc], (unsigned)(((t - NACC) / NACC) & 1));
+            if (!__all_sync(0xffffffffu, ok)) break;
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            const uint32_t idesc = tf32_idesc(kLtM, N);
+            const unsigned b0 = smem_addr(Bbase + (size_t)s * bslot);
+            const unsigned d = tmem + (unsigned)acc * accw;
+            const unsigned a0 = tmem + kLtAcol + 64u * s;
+            if (leader) {
+                if (STACK) {
                     // A_hi [B_hi | B_lo] (N = 2 ncols) into columns [0, 2 ncols),
                     // A_lo B_hi into [0, ncols); the epilogue adds the halves
                     const uint32_t idesc2 = tf32_idesc(kLtM, 2 * N);
@@ -570,7 +580,7 @@ linear_tc_kernel(const __grid_constant__ LinDesc D, int64_t n, int nmax,
                         mma_tf32_tmem_a(d, a0 + k8, bd, idesc2, (first && k8 == 0) ? 0u : 1u);
                         mma_tf32_tmem_a(d, a0 + 32 + k8, bd, idesc, 1u);
                     }
-                } else if (leader) {
+                } else {
                     const unsigned lb = (unsigned)(N / 8) * 128;
                     const unsigned bpart = (unsigned)N * kLtK * 4;
 #pragma unroll
@@ -583,41 +593,23 @@ linear_tc_kernel(const __grid_constant__ LinDesc D, int64_t n, int nmax,
                         mma_tf32_tmem_a(d, a0 + 32 + k8, bh, idesc, 1u);
                     }
                 }
-                if (leader) {
-                    tc_commit(&a_free[s]);
-                    tc_commit(&b_free[slot]);
-                    if (last) tc_commit(&acc_full[acc]);
-                }
-                __syncwarp();
-                last_commit = k;
-                // refill: chunk kb goes into the slot of chunk kb - RB, free once
-                // that chunk's MMAs have completed; kb stays at most k + RB - 1
-                // and the refill waits for chunk k - 1 only when kb = k + RB - 1
-                if (bp.valid && kb <= k + RB - 2) {
-                    const int fs = (int)(kb % RB);
-                    const bool freed = kb < RB || wait(&b_free[fs], (unsigned)(((kb - RB) / RB) & 1));
-                    if (!__all_sync(0xffffffffu, freed)) break;
-                    issue_b(kb);
-                    ++kb;
-                }
-                if (last) ++t;
-                advance(cur);
-                ++k;
-                if (last && __any_sync(0xffffffffu, *(volatile int*)&fail)) break;
+                tc_commit(&empty[s]);
+                if (last) tc_commit(&acc_full[acc]);
             }
-            // drain: bulk copies issued but never waited for, the last MMAs
-            if (leader) {
-                for (int64_t c = kw; c < kb; ++c)  // copies issued, never waited for
-                    tc_mbar_wait(&b_full[c % RB], (unsigned)((c / RB) & 1));
-                if (last_commit >= 0)
-                    tc_mbar_wait(&a_free[last_commit % RA], (unsigned)((last_commit / RA) & 1));
-            }
+            __syncwarp();
+            last_commit = k;
+            if (last) ++t;
+            advance(cur);
+            ++k;
+            if (last && __any_sync(0xffffffffu, *(volatile int*)&fail)) break;
         }
+        if (leader && last_commit >= 0)  // the MMAs must finish before tensor memory is freed
+            tc_mbar_wait(&empty[last_commit % S], (unsigned)((last_commit / S) & 1));
     } else {
         // ----------------------------------------------------------- epilogue
         const int q = warp;  // TMEM lane quarter
         Pos cur = start;
-        float* stage = stage_all + q * (32 * kLtStagePitch);
+        float* stage = stage_all + q * (32 * pitch);
         for (int64_t t = 0; cur.valid; ++t) {
             const int acc = (int)(t % NACC);
             bool got = wait(&acc_full[acc], (unsigned)((t / NACC) & 1));
@@ -625,43 +617,67 @@ linear_tc_kernel(const __grid_constant__ LinDesc D, int64_t n, int nmax,
             if (!got) break;
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
             const LinBlock& EB = sblk[cur.b];
+            const int N = EB.ncols;
             const int64_t R = cur.t * kLtM + 32 * q + lane;
             const bool live = R < n * EB.d;
             float* o = out;  // this lane's row
             if (live) {
-                const int64_t item = R / EB.d;
+                const int64_t item = row_item(R, EB.d);
                 const int m = (int)(R - item * EB.d);
-                o = out + item * out_stride + EB.out_off + (int64_t)m * EB.ncols;
+                o = out + item * out_stride + EB.out_off + (int64_t)m * N;
             }
-            for (int c0 = 0; c0 < EB.ncols; c0 += 32) {
-                float v[32];
-                const unsigned ta = tmem + ((unsigned)(32 * q) << 16) + (unsigned)acc * accw + (unsigned)c0;
-                tmem_ld32(ta, v);
-                if (STACK) {  // + the A_hi B_lo half
-                    float v2[32];
-                    tmem_ld32(ta + (unsigned)EB.ncols, v2);
+            if (STACK) {
+                // the whole row block into shared memory (+ the A_hi B_lo half),
+                // then the accumulator is free while the rows go out
+                for (int c0 = 0; c0 < N; c0 += 32) {
+                    float v[32], v2[32];
+                    const unsigned ta =
+                        tmem + ((unsigned)(32 * q) << 16) + (unsigned)acc * accw + (unsigned)c0;
+                    tmem_ld32(ta, v);
+                    tmem_ld32(ta + (unsigned)N, v2);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] += v2[i];
+                    for (int i = 0; i < 8; ++i)
+                        *reinterpret_cast<float4*>(stage + lane * pitch + c0 + 4 * i) = make_float4(
+                            v[4 * i] + v2[4 * i], v[4 * i + 1] + v2[4 * i + 1],
+                            v[4 * i + 2] + v2[4 * i + 2], v[4 * i + 3] + v2[4 * i + 3]);
                 }
-                // transpose through shared memory: 8 lanes store one row's 128 bytes
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    *reinterpret_cast<float4*>(stage + lane * kLtStagePitch + 4 * i) =
-                        make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+                asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+                tc_mbar_arrive(&acc_free[acc]);
                 __syncwarp();
-#pragma unroll
-                for (int it = 0; it < 8; ++it) {
-                    const int rr = 4 * it + (lane >> 3), cq = lane & 7;
+                for (int rr = 0; rr < 32; ++rr) {  // one row per step, 16 bytes per lane
                     float* orow = reinterpret_cast<float*>(
                         __shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(o), rr));
                     const bool rlive = __shfl_sync(0xffffffffu, live, rr);
-                    const float4 w4 = *reinterpret_cast<const float4*>(stage + rr * kLtStagePitch + 4 * cq);
-                    if (rlive) *reinterpret_cast<float4*>(orow + c0 + 4 * cq) = w4;
+                    for (int c = 4 * lane; c < N; c += 128)
+                        if (rlive)
+                            *reinterpret_cast<float4*>(orow + c) =
+                                *reinterpret_cast<const float4*>(stage + rr * pitch + c);
                 }
                 __syncwarp();
+            } else {
+                for (int c0 = 0; c0 < N; c0 += 32) {
+                    float v[32];
+                    tmem_ld32(tmem + ((unsigned)(32 * q) << 16) + (unsigned)acc * accw + (unsigned)c0, v);
+                    // transpose through shared memory: 8 lanes store one row's 128 bytes
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        *reinterpret_cast<float4*>(stage + lane * pitch + 4 * i) =
+                            make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+                    __syncwarp();
+#pragma unroll
+                    for (int it = 0; it < 8; ++it) {
+                        const int rr = 4 * it + (lane >> 3), cq = lane & 7;
+                        float* orow = reinterpret_cast<float*>(
+                            __shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(o), rr));
+                        const bool rlive = __shfl_sync(0xffffffffu, live, rr);
+                        const float4 w4 = *reinterpret_cast<const float4*>(stage + rr * pitch + 4 * cq);
+                        if (rlive) *reinterpret_cast<float4*>(orow + c0 + 4 * cq) = w4;
+                    }
+                    __syncwarp();
+                }
+                asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+                tc_mbar_arrive(&acc_free[acc]);
             }
-            asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-            tc_mbar_arrive(&acc_free[acc]);
             cur.u += gridDim.x;
             cur.ci = 0;
             locate(cur);
@@ -919,8 +935,9 @@ static cudaError_t run_pass(const LinearImpl& L, const LinDesc& D, int nmax, siz
     }
     Dn->blk[D.nblocks].tile0 = units;
     const unsigned grid = (unsigned)std::min<int64_t>(units, sm_count());
-    // B ring: 4 slots up to 128 columns, 3 at 256
-    const size_t smem = std::max<size_t>(120 * 1024, stack ? lt_smem_bytes(nmax, 4) : lt_smem_bytes(nmax, 3));
+    // stages (A in tensor memory, B in shared memory): 4 up to 128 columns, 3 at 256
+    const size_t smem = std::max<size_t>(
+        120 * 1024, stack ? lt_smem_bytes(nmax, 4, true) : lt_smem_bytes(nmax, 3, false));
     auto* kern = stack ? linear_tc_kernel<4, 1, true> : linear_tc_kernel<3, 1, false>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
