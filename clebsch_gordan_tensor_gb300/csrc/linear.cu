@@ -322,7 +322,8 @@ __global__ void linear_pack_kernel(const __grid_constant__ LinDesc D, const floa
 // B slot in shared memory.  Warp roles:
 //   producers (warps 4-11; warp 4 + p serves TMEM lanes 32 (p % 4) .. + 31,
 //     one row per lane, K columns 16 (p / 4) .. + 15 of each chunk): the rows
-//     are loaded into registers three chunks ahead; once the MMAs of chunk
+//     are loaded into registers three chunks ahead (four buffers taken in
+//     rotation by name, so no copy waits for a load); once the MMAs of chunk
 //     k - S have released the stage (empty) the warp writes chunk k's values
 //     as they are (the tensor cores read them as the TF32 "hi" part, which
 //     keeps the leading 10 fraction bits) and the "lo" parts, lo =
@@ -477,23 +478,20 @@ linear_tc_kernel(const __grid_constant__ LinDesc D, int64_t n, int nmax,
                 if (16 * h + 4 * j < C.kc) v[j] = *reinterpret_cast<const float4*>(src + 4 * j);
         };
         Pos pre = start, cur = start;
-        float4 v0[4], v1[4], v2[4];
-        load(pre, v0);
-        if (pre.valid) advance(pre);
-        load(pre, v1);
-        if (pre.valid) advance(pre);
-        load(pre, v2);
-        if (pre.valid) advance(pre);
-        for (int64_t k = 0; cur.valid; ++k) {
+        bool stop = false;
+        // chunk k: load chunk k + 3 into `nxt`, then write chunk k (in `v`)
+        auto step = [&](int64_t k, float4 (&v)[4], float4 (&nxt)[4]) {
             const int s = (int)(k % RA);
-            float4 v3[4];
-            load(pre, v3);  // three chunks ahead
+            load(pre, nxt);
             if (pre.valid) advance(pre);
-            if (k >= S && !wait(&empty[s], (unsigned)(((k - S) / S) & 1))) break;
+            if (k >= S && !wait(&empty[s], (unsigned)(((k - S) / S) & 1))) {
+                stop = true;
+                return;
+            }
             float hi[16], lo[16];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                const float in[4] = {v0[j].x, v0[j].y, v0[j].z, v0[j].w};
+                const float in[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     hi[4 * j + q] = in[q];
@@ -508,14 +506,26 @@ linear_tc_kernel(const __grid_constant__ LinDesc D, int64_t n, int nmax,
             asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
             __syncwarp();
             if (lane == 0) tc_mbar_arrive(&full[s]);  // one arrival per warp
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                v0[j] = v1[j];
-                v1[j] = v2[j];
-                v2[j] = v3[j];
-            }
             advance(cur);
-            if (*(volatile int*)&fail) break;
+            if (*(volatile int*)&fail) stop = true;
+        };
+        // four register buffers taken in rotation by name (a copy between
+        // them would wait for the load just issued)
+        float4 b0[4], b1[4], b2[4], b3[4];
+        load(pre, b0);
+        if (pre.valid) advance(pre);
+        load(pre, b1);
+        if (pre.valid) advance(pre);
+        load(pre, b2);
+        if (pre.valid) advance(pre);
+        for (int64_t k = 0; cur.valid && !stop; k += 4) {
+            step(k, b0, b3);
+            if (!cur.valid || stop) break;
+            step(k + 1, b1, b0);
+            if (!cur.valid || stop) break;
+            step(k + 2, b2, b1);
+            if (!cur.valid || stop) break;
+            step(k + 3, b3, b2);
         }
     } else if (loader) {
         // ------------------------------------------------------------- loader
