@@ -18,7 +18,7 @@ samples, 128 channels (fwd+bwd, samples/s); ``conv64`` the fp64 fused conv,
 N = 5,000, 128 channels (forward, edges/s); ``tfn`` the TFN layer on 1000
 molecules (forward, backward, forces and the double backward, edges/s); ``kv``
 the same molecules at 64 channels, keys and values of an SE(3)-Transformer layer
-from one TFN (fwd+bwd, edges/s); ``uvw`` config 1's samples under a 'uvw'
+from one TFN (fwd+bwd, edges/s); ``uvw`` the 200,000 samples of ``tp`` under a 'uvw'
 product (one shared 128x128 matrix per path; channel mixing on tcgen05).
 
 ``--impl reference`` times the CPU oracle (the reference arm of this build) on
@@ -414,8 +414,9 @@ def make_kv(args, cg, W, torch):
 
 
 def make_uvw(args, cg, W, torch):
-    """'uvw' product at config 1's sizes: per-path 'uvu' blocks (unit shared
-    weights), then the channel mixing on the tensor cores."""
+    """'uvw' product on the 200,000-sample, 128-channel inputs of ``tp``:
+    per-path 'uvu' blocks (unit shared weights), then the channel mixing on the
+    tensor cores."""
     cfg = W.config1_uvw(args.samples)
     B = cfg["B"]
     uvw = cg.UVWProduct(*W.CFG1)

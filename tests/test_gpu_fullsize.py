@@ -160,7 +160,7 @@ def test_config4_chain_sampled():
 
 
 def test_config4_fused_kv_sampled():
-    """Keys and values from one TFN (the config-4 graph at 64 channels): forward
+    """Keys and values from one TFN (the 1000-molecule graph at 64 channels): forward
     and gradient at full size, sampled receivers / senders / edges."""
     need_gpu()
     cfg = W.config4_kv()

@@ -33,7 +33,7 @@ CFG2 = ("64x0e+64x1o+64x2e", "0e+1o+2e+3o", "64x0e+64x1o+64x1e+64x2o+64x2e+64x3o
 CFG3 = ("128x0e+128x1o+128x2e", "0e+1o+2e+3o",
         "128x0e+128x1o+128x1e+128x2o+128x2e+128x3o+128x3e")
 CFG4 = ("32x0e+32x1o+32x2e+32x3o", "0e+1o+2e+3o", "32x0e+32x1o+32x2e+32x3o")
-# the config-4 layer with keys and values computed by one TFN: channels doubled
+# the small-molecule TFN layer with keys and values from one TFN: channels doubled
 CFG4_KV = ("64x0e+64x1o+64x2e+64x3o", "0e+1o+2e+3o", "64x0e+64x1o+64x2e+64x3o")
 
 
@@ -183,9 +183,10 @@ def config1(B: int = 200_000) -> dict:
 
 
 def config1_uvw(B: int = 200_000) -> dict:
-    """Config 1's samples (x, v from seed 1, as ``config1`` draws them) under a
-    'uvw' product: one [128, 128] matrix per path shared by all samples,
-    W ~ N(0,1)/sqrt(128) from seed 101 (24 paths, path-major, row-major)."""
+    """The 200,000-sample, 128-channel standalone inputs (x, v from seed 1, as
+    ``config1`` draws them) under a 'uvw' product: one [128, 128] matrix per
+    path shared by all samples, W ~ N(0,1)/sqrt(128) from seed 101 (24 paths,
+    path-major, row-major)."""
     cfg = config1(B)
     cfg.pop("w")
     rng = np.random.default_rng(101)
@@ -211,7 +212,7 @@ def conv_cloud(seed: int, irreps, N: int, n_paths: int, dtype) -> dict:
 
 
 def config4_kv(n_mol: int = 1000) -> dict:
-    """The config-4 molecules (same seed, same graph) with 64 channels per
+    """The TFN workload's 1000 molecules (same seed, same graph) with 64 channels per
     irrep: the keys and values of an SE(3)-Transformer attention layer from one
     TFN with doubled channels instead of two.  Draws, in order: molecules; x
     [N, 1024] ~ N(0,1); w [E, 23 * 64] ~ N(0,1)/sqrt(23); g [N, 1024] ~ N(0,1)
