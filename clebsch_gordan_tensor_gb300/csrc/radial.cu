@@ -470,7 +470,7 @@ constexpr int kBwEdges = 32;   // edges per tile
 constexpr int kBwCols = 32;    // grad_w / W2 columns staged per step (edge kernel)
 constexpr int kBwThreads = 256;
 constexpr int kBwGrid1 = 512;  // CTAs of the edge kernel (at most)
-constexpr int kBwW2Cols = 128; // output columns per CTA of the W2 kernel
+constexpr int kBwW2Cols = 256; // output columns per CTA of the W2 kernel
 constexpr int kBwW2Rows = 64;  // hidden units per pass of the W2 kernel
 
 static inline int64_t bw_tiles(int64_t E) { return (E + kBwEdges - 1) / kBwEdges; }
@@ -614,32 +614,50 @@ radial_bwd_edge_kernel(int64_t E, int nb, T rc, int hidden, int64_t n_out, const
     }
 }
 
+// Four consecutive values from shared memory (one 128-bit load for fp32).
+template <typename T>
+__device__ __forceinline__ void ld4(const T* p, T (&v)[4]) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) v[q] = p[q];
+}
+template <>
+__device__ __forceinline__ void ld4<float>(const float* p, float (&v)[4]) {
+    const float4 t = *reinterpret_cast<const float4*>(p);
+    v[0] = t.x;
+    v[1] = t.y;
+    v[2] = t.z;
+    v[3] = t.w;
+}
+
 // gW2 partial rows: CTA (chunk c, split s) sums h^T gw over its edge range for
-// output columns [128 c, 128 c + 128), hidden units in passes of 64.
+// output columns [256 c, 256 c + 256), hidden units in passes of 64.  Thread
+// (ty, tx) = (tid / 32, tid % 32) owns hidden rows 8 ty .. 8 ty + 7 and columns
+// 4 tx .. 4 tx + 3 and 128 + 4 tx .. 128 + 4 tx + 3: per edge two broadcast
+// loads of h and two 128-bit loads of gw feed 64 FMAs.
 template <typename T>
 __global__ void __launch_bounds__(kBwThreads)
 radial_bwd_w2_kernel(int64_t E, int nb, T rc, int hidden, int64_t n_out, int64_t splits,
                      const T* __restrict__ vec, const T* __restrict__ W1,
                      const T* __restrict__ gw, T* __restrict__ part) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    T* bS = reinterpret_cast<T*>(smem_raw);  // [kBwEdges][nb]
-    T* rS = bS + kBwEdges * nb;               // [kBwEdges]
-    T* hS = rS + kBwEdges;                    // [kBwEdges][kBwW2Rows]
+    T* hS = reinterpret_cast<T*>(smem_raw);   // [kBwEdges][kBwW2Rows]
     T* gS = hS + kBwEdges * kBwW2Rows;        // [kBwEdges][kBwW2Cols]
+    T* bS = gS + kBwEdges * kBwW2Cols;        // [kBwEdges][nb]
+    T* rS = bS + kBwEdges * nb;               // [kBwEdges]
     const int tid = threadIdx.x;
     const int64_t c = blockIdx.x / splits, sp = blockIdx.x % splits;
     const int64_t col0 = c * kBwW2Cols;
     const int ncol = n_out - col0 < kBwW2Cols ? (int)(n_out - col0) : kBwW2Cols;
     const int64_t ea = E * sp / splits, eb = E * (sp + 1) / splits;
-    const int jg = tid / 32, cq = tid % 32;  // hidden rows jg, jg + 8, ...; columns 4 cq .. 4 cq + 3
+    const int ty = tid / 32, tx = tid % 32;
     T* out = part + sp * (int64_t)hidden * n_out;
     for (int j0 = 0; j0 < hidden; j0 += kBwW2Rows) {
         const int nj = hidden - j0 < kBwW2Rows ? hidden - j0 : kBwW2Rows;
-        T acc[8][4];
+        T acc[8][8];
 #pragma unroll
         for (int t = 0; t < 8; ++t)
 #pragma unroll
-            for (int q = 0; q < 4; ++q) acc[t][q] = (T)0;
+            for (int q = 0; q < 8; ++q) acc[t][q] = (T)0;
         for (int64_t e0 = ea; e0 < eb; e0 += kBwEdges) {
             const int ne = eb - e0 < kBwEdges ? (int)(eb - e0) : kBwEdges;
             __syncthreads();
@@ -660,24 +678,27 @@ radial_bwd_w2_kernel(int64_t E, int nb, T rc, int hidden, int64_t n_out, int64_t
             }
             __syncthreads();
             for (int le = 0; le < ne; ++le) {
-                T g4[4];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) g4[q] = gS[le * kBwW2Cols + 4 * cq + q];
+                T ha[4], hb[4], ga[4], gb[4];
+                ld4(hS + le * kBwW2Rows + 8 * ty, ha);
+                ld4(hS + le * kBwW2Rows + 8 * ty + 4, hb);
+                ld4(gS + le * kBwW2Cols + 4 * tx, ga);
+                ld4(gS + le * kBwW2Cols + 128 + 4 * tx, gb);
 #pragma unroll
                 for (int t = 0; t < 8; ++t) {
-                    const T hv = hS[le * kBwW2Rows + jg + 8 * t];
+                    const T hv = t < 4 ? ha[t] : hb[t - 4];
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) acc[t][q] = fma(hv, g4[q], acc[t][q]);
+                    for (int q = 0; q < 8; ++q)
+                        acc[t][q] = fma(hv, q < 4 ? ga[q] : gb[q - 4], acc[t][q]);
                 }
             }
         }
 #pragma unroll
         for (int t = 0; t < 8; ++t) {
-            const int j = jg + 8 * t;
+            const int j = 8 * ty + t;
             if (j >= nj) continue;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int k = 4 * cq + q;
+            for (int q = 0; q < 8; ++q) {
+                const int k = (q < 4 ? 4 * tx + q : 128 + 4 * tx + q - 4);
                 if (k < ncol) out[(int64_t)(j0 + j) * n_out + col0 + k] = acc[t][q];
             }
         }
@@ -1007,8 +1028,8 @@ cudaError_t launch_radial_backward(bool f64, bool tensor_cores, int64_t E, int n
     const size_t sm1 = es * ((size_t)kBwEdges * nb + kBwEdges + (size_t)kBwEdges * hidden +
                              (size_t)kBwEdges * (kBwCols + 1) + (size_t)hidden * (kBwCols + 1) +
                              (size_t)kBwEdges * nb);
-    const size_t sm2 = es * ((size_t)kBwEdges * nb + kBwEdges + (size_t)kBwEdges * kBwW2Rows +
-                             (size_t)kBwEdges * kBwW2Cols);
+    const size_t sm2 = es * ((size_t)kBwEdges * kBwW2Rows + (size_t)kBwEdges * kBwW2Cols +
+                             (size_t)kBwEdges * nb + kBwEdges);
     cudaError_t e;
     if ((gvec || gW1) && tc) {
         int dev = 0, sms = 0;
