@@ -425,11 +425,24 @@ def make_uvw(args, cg, W, torch):
     mid = torch.empty(B, uvw.dim_mid, device="cuda")
     out = torch.empty(B, uvw.dim_out, device="cuda")
     ones = torch.ones(uvw.plan.weight_numel, device="cuda")
-    ws = torch.empty(uvw.linear.workspace_bytes(B)[0], dtype=torch.uint8, device="cuda")
+    fwb, bwb = uvw.linear.workspace_bytes(B)
+    ws = torch.empty(fwb, dtype=torch.uint8, device="cuda")
+    wsb = torch.empty(bwb, dtype=torch.uint8, device="cuda")
+    g = torch.randn(B, uvw.dim_out, device="cuda", generator=torch.Generator("cuda").manual_seed(7))
+    res = {}
     uvw.plan.compile()
+
+    def mix_bwd_x():
+        res["gmid"] = uvw.linear.backward(mid, Wm, g, need=(True, False), workspace=wsb)[0]
+
     kernels = [("sh_fwd", lambda: cg.sh_forward(vec, 3, out=y)),
                ("tp_paths", lambda: uvw.plan.forward(x, y, ones, out=mid)),
-               ("linear", lambda: uvw.linear.forward(mid, Wm, out=out, workspace=ws))]
+               ("linear", lambda: uvw.linear.forward(mid, Wm, out=out, workspace=ws)),
+               ("linear_bwd_x", mix_bwd_x),
+               ("linear_bwd_w", lambda: uvw.linear.backward(mid, Wm, g, need=(False, True),
+                                                            workspace=wsb)),
+               ("tp_paths_bwd", lambda: uvw.plan.backward(x, y, ones, res["gmid"],
+                                                          need=(True, True, False)))]
     d = Dims(uvw.plan)
     mix = 0
     for j in range(uvw.linear.n_instr):
@@ -439,10 +452,15 @@ def make_uvw(args, cg, W, torch):
     counts = {"sh_fwd": (B * (3 + d.dim2) * 4, None),
               "tp_paths": (B * (d.dim1 + d.dim2 + d.dimo) * 4 + d.wdim * 4, B * d.flops),
               "linear": (B * (uvw.dim_mid + uvw.dim_out) * 4 + uvw.weight_numel * 4, mix_flops,
-                         "tensor3")}
+                         "tensor3"),
+              "linear_bwd_x": (B * (uvw.dim_mid + uvw.dim_out) * 4 + uvw.weight_numel * 4,
+                               mix_flops, "tensor3"),
+              "linear_bwd_w": (B * (uvw.dim_mid + uvw.dim_out) * 4 + uvw.weight_numel * 4,
+                               mix_flops, "tensor3"),
+              "tp_paths_bwd": (B * (2 * d.dim1 + 2 * d.dim2 + d.dimo) * 4, 2 * B * d.flops)}
     desc = (f"'uvw' CG-TP: B={B}, 128x(0e,1o,2e) (x) Y(l<=3) -> 128x(0e,1o,1e,2o,2e,3o,3e), "
-            "24 paths, one shared 128x128 matrix per path, fp32 (channel mixing on tcgen05, "
-            "TF32 split in three products)")
+            "24 paths, one shared 128x128 matrix per path, fp32, forward and gradient (channel "
+            "mixing and its x-gradient on tcgen05, TF32 split in three products)")
     return Workload("uvw", desc, B, "samples/s", "f32", kernels, counts,
                     ["sh_fwd", "tp_paths", "linear"], dict(B=B, mul=128, paths=uvw.n_paths),
                     None, None)

@@ -155,10 +155,11 @@ __global__ void linear_zero_kernel(int64_t n, int64_t stride, int off, int width
 // g[n, go + m mo + w]; tile0 = first 32 x 32 tile of j in the flat tile list.
 struct LinGrad {
     int xo, mi, go, mo, d, w_off, tile0;
+    int mt0;  // first 128-row M tile of j in the tensor-core kernel's list
 };
 constexpr int kLinMaxGrad = 128;
 struct LinGradDesc {
-    int ninstr, ntiles;
+    int ninstr, ntiles, nmt;  // nmt: M tiles (128 input channels) over all instructions
     int64_t x_stride, g_stride, nw;
     LinGrad g[kLinMaxGrad];
 };
@@ -703,6 +704,293 @@ linear_tc_kernel(const __grid_constant__ LinDesc D, int64_t n, int nmax,
                      : "memory");
 }
 
+// --------------------------------------------- W gradient on tensor cores
+//
+// gW_j = X_j^T G_j summed over the rows (n, m) of instruction j, as
+// D[u, w] = sum_k A[u, k] B[w, k] with K = rows: A = X^T in tensor memory (lane
+// = input channel u, columns = 32 rows of a chunk), B = G^T in shared memory
+// (K-major, [hi | lo] stacked along N = 2 mul_out), the same three split
+// products as the forward in two instructions per K step.  Work units are
+// (instruction, 128-channel M tile, row split s), split s holding the rows of
+// items [s per, (s + 1) per); each unit writes its partial sums to
+// partial[s nw + ...] (zeros for an empty split), added in fixed order
+// afterwards.  Warp roles:
+//   epilogue (warps 0-3): per unit, wait acc_full, read D (lane u), add the
+//     two halves and store the partial row; arrive on acc_free.
+//   A producers (warps 4-7, lane quarter warp % 4): each thread loads its
+//     channel u of the chunk's 32 rows (one chunk ahead into registers), writes
+//     hi = the values and lo = round_tf32(x - x cut to 10 bits) with
+//     tcgen05.st once the stage is empty, and arrives on full.
+//   B producers (warps 8-15, output channel w = 32 (warp - 8) + lane): load w
+//     of the 32 rows, write four rows at a time into the K-major image (hi rows
+//     w, lo rows mul_out + w), fence to the async proxy, arrive on full.
+//   MMA issuer (warp 16): one wait per chunk, the products, commit to empty
+//     (and acc_full after a unit's last chunk).
+// Chunk k (counted over the CTA's units) uses stage k % 4 and phase (k / 4) % 2
+// of full / empty; the t-th unit with rows uses phase t % 2 of acc_full /
+// acc_free.  Waits are bounded as in the forward kernel.
+constexpr int kWgStages = 4;
+constexpr int kWgThreads = 32 * 17;
+constexpr int kWgRows = 32;  // rows (K) per chunk
+
+__global__ void __launch_bounds__(kWgThreads, 1)
+linear_wgrad_tc_kernel(const __grid_constant__ LinGradDesc D, int64_t n, int64_t per, int S,
+                       const float* __restrict__ x, const float* __restrict__ g,
+                       float* __restrict__ partial) {
+    extern __shared__ __align__(1024) unsigned char smem[];
+    __shared__ __align__(8) unsigned long long full[kWgStages], empty[kWgStages];
+    __shared__ __align__(8) unsigned long long acc_full, acc_free;
+    __shared__ unsigned tmem_base;
+    __shared__ int fail;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    constexpr unsigned bslot = 2u * 128 * kWgRows * 4;  // stacked image, mul_out <= 128
+
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_addr(&tmem_base)),
+                     "r"(kLtTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    if (tid == 0) {
+        for (int i = 0; i < kWgStages; ++i) {
+            tc_mbar_init(&full[i], 12);  // 4 A warps + 8 B warps
+            tc_mbar_init(&empty[i], 1);
+        }
+        tc_mbar_init(&acc_full, 1);
+        tc_mbar_init(&acc_free, 128);
+        fail = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    const unsigned tmem = tmem_base;
+    const bool issuer = warp == 16;
+    auto wait = [&](unsigned long long* bar, unsigned parity) -> bool {
+        if (!issuer && *(volatile int*)&fail) return false;
+        if (issuer ? tc_mbar_wait(bar, parity) : tc_mbar_wait_sleep(bar, parity)) return true;
+        atomicExch(&fail, 1);
+        return false;
+    };
+    // unit u -> instruction j, M tile mt, split s and its rows [r0, r1)
+    struct Unit {
+        int j, mt, nch;
+        int64_t r0, r1;
+    };
+    const int64_t units = (int64_t)D.nmt * S;
+    auto unit_of = [&](int64_t u, Unit& U) {
+        const int sp = (int)(u % S);
+        const int q = (int)(u / S);
+        int j = 0;
+        while (j + 1 < D.ninstr && D.g[j + 1].mt0 <= q) ++j;
+        U.j = j;
+        U.mt = q - D.g[j].mt0;
+        const int64_t i0 = (int64_t)sp * per, i1 = i0 + per < n ? i0 + per : n;
+        const int d = D.g[j].d;
+        U.r0 = i0 < n ? i0 * d : 0;
+        U.r1 = i0 < n ? i1 * d : 0;
+        U.nch = (int)((U.r1 - U.r0 + kWgRows - 1) / kWgRows);
+    };
+
+    if (warp >= 4 && warp < 16) {
+        // ---------------------------------------------------------- producers
+        const bool isA = warp < 8;
+        const int q = warp & 3;
+        // column of this thread: A -> input channel (in the M tile), B -> output channel
+        auto load = [&](const Unit& U, int ci, float (&v)[kWgRows]) {
+            const LinGrad& G = D.g[U.j];
+            const int col = isA ? U.mt * 128 + 32 * q + lane : 32 * (warp - 8) + lane;
+            const int lim = isA ? G.mi : G.mo;
+            const int64_t rb = U.r0 + (int64_t)ci * kWgRows;
+            int64_t item = row_item(rb, G.d);
+            int m = (int)(rb - item * G.d);
+            const float* base = isA ? x + G.xo + col : g + G.go + col;
+            const int64_t stride = isA ? D.x_stride : D.g_stride;
+            const int mstride = isA ? G.mi : G.mo;
+#pragma unroll
+            for (int i = 0; i < kWgRows; ++i) {
+                const bool ok = col < lim && rb + i < U.r1;
+                v[i] = ok ? base[item * stride + (int64_t)m * mstride] : 0.0f;
+                if (++m == G.d) {
+                    m = 0;
+                    ++item;
+                }
+            }
+        };
+        auto lo = [](float v) {
+            return to_tf32(v - __uint_as_float(__float_as_uint(v) & 0xFFFFE000u));
+        };
+        float va[kWgRows], vb[kWgRows];
+        int64_t k = 0;
+        bool stop = false;
+        // write chunk k (values v) into stage k % 4
+        auto put = [&](const Unit& U, float (&v)[kWgRows]) {
+            const int st = (int)(k % kWgStages);
+            if (k >= kWgStages && !wait(&empty[st], (unsigned)(((k - kWgStages) / kWgStages) & 1))) {
+                stop = true;
+                return;
+            }
+            if (isA) {
+                const unsigned ta = tmem + ((unsigned)(32 * q) << 16) + kLtAcol + 64u * st;
+                float h[16], l[16];
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        h[i] = v[16 * half + i];
+                        l[i] = lo(v[16 * half + i]);
+                    }
+                    tmem_st16(ta + 16u * half, h);
+                    tmem_st16(ta + 32 + 16u * half, l);
+                }
+                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+            } else {
+                const int w = 32 * (warp - 8) + lane;
+                const int mo = D.g[U.j].mo;
+                if (w < mo) {
+                    unsigned char* bs = smem + (size_t)st * bslot;
+#pragma unroll
+                    for (int k4 = 0; k4 < kWgRows; k4 += 4) {
+                        *reinterpret_cast<float4*>(bs + kmajor_offset(w, k4, 2 * mo)) =
+                            make_float4(v[k4], v[k4 + 1], v[k4 + 2], v[k4 + 3]);
+                        *reinterpret_cast<float4*>(bs + kmajor_offset(mo + w, k4, 2 * mo)) =
+                            make_float4(lo(v[k4]), lo(v[k4 + 1]), lo(v[k4 + 2]), lo(v[k4 + 3]));
+                    }
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            }
+            __syncwarp();
+            if (lane == 0) tc_mbar_arrive(&full[st]);
+            ++k;
+        };
+        // chunk sequence over this CTA's units, one chunk loaded ahead
+        Unit U{}, Un{};
+        int64_t u = blockIdx.x;
+        if (u < units) unit_of(u, U);
+        int ci = 0;
+        // advance to the first unit with rows
+        while (u < units && U.nch == 0) {
+            u += gridDim.x;
+            if (u < units) unit_of(u, U);
+        }
+        if (u < units) load(U, 0, va);
+        bool flip = false;
+        while (u < units && !stop) {
+            // next position
+            int64_t un = u;
+            int cn = ci + 1;
+            Un = U;
+            if (cn == U.nch) {
+                cn = 0;
+                do {
+                    un += gridDim.x;
+                    if (un < units) unit_of(un, Un);
+                } while (un < units && Un.nch == 0);
+            }
+            if (!flip) {
+                if (un < units) load(Un, cn, vb);
+                put(U, va);
+            } else {
+                if (un < units) load(Un, cn, va);
+                put(U, vb);
+            }
+            flip = !flip;
+            u = un;
+            ci = cn;
+            U = Un;
+            if (*(volatile int*)&fail) break;
+        }
+    } else if (issuer) {
+        // ---------------------------------------------------------- MMA issuer
+        const bool leader = lane == 0;
+        int64_t k = 0, t = 0, last_commit = -1;
+        for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
+            Unit U;
+            unit_of(u, U);
+            if (U.nch == 0) continue;
+            const int mo = D.g[U.j].mo;
+            const uint32_t idesc = tf32_idesc(kLtM, mo), idesc2 = tf32_idesc(kLtM, 2 * mo);
+            const unsigned lb = (unsigned)(2 * mo / 8) * 128;
+            bool ok = true;
+            for (int ci = 0; ci < U.nch && ok; ++ci, ++k) {
+                const int st = (int)(k % kWgStages);
+                ok = wait(&full[st], (unsigned)((k / kWgStages) & 1));
+                if (ok && ci == 0 && t >= 1) ok = wait(&acc_free, (unsigned)((t - 1) & 1));
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                if (leader) {
+                    const unsigned b0 = smem_addr(smem + (size_t)st * bslot);
+                    const unsigned a0 = tmem + kLtAcol + 64u * st;
+#pragma unroll
+                    for (int k8 = 0; k8 < kWgRows; k8 += 8) {
+                        const uint64_t bd = smem_desc(b0 + (unsigned)(k8 >> 2) * lb, lb, 128);
+                        mma_tf32_tmem_a(tmem, a0 + k8, bd, idesc2, (ci == 0 && k8 == 0) ? 0u : 1u);
+                        mma_tf32_tmem_a(tmem, a0 + 32 + k8, bd, idesc, 1u);
+                    }
+                    tc_commit(&empty[st]);
+                    if (ci + 1 == U.nch) tc_commit(&acc_full);
+                }
+                __syncwarp();
+                last_commit = k;
+            }
+            if (!ok) break;
+            ++t;
+            if (__any_sync(0xffffffffu, *(volatile int*)&fail)) break;
+        }
+        if (leader && last_commit >= 0)
+            tc_mbar_wait(&empty[last_commit % kWgStages], (unsigned)((last_commit / kWgStages) & 1));
+    } else if (warp < 4) {
+        // ----------------------------------------------------------- epilogue
+        int64_t t = 0;
+        for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
+            Unit U;
+            unit_of(u, U);
+            const LinGrad& G = D.g[U.j];
+            const int sp = (int)(u % S);
+            const int urow = U.mt * 128 + 32 * warp + lane;  // input channel of this lane
+            float* prow = partial + (int64_t)sp * D.nw + G.w_off + (int64_t)urow * G.mo;
+            const bool live = urow < G.mi;
+            if (U.nch == 0) {  // empty split: its partial sums are zero
+                if (live)
+                    for (int w = 0; w < G.mo; w += 4)
+                        *reinterpret_cast<float4*>(prow + w) = make_float4(0.f, 0.f, 0.f, 0.f);
+                continue;
+            }
+            bool got = wait(&acc_full, (unsigned)(t & 1));
+            got = __all_sync(0xffffffffu, got);
+            if (!got) break;
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            for (int c0 = 0; c0 < G.mo; c0 += 32) {
+                float v[32], v2[32];
+                const unsigned ta = tmem + ((unsigned)(32 * warp) << 16) + (unsigned)c0;
+                tmem_ld32(ta, v);
+                tmem_ld32(ta + (unsigned)G.mo, v2);
+                if (live) {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        *reinterpret_cast<float4*>(prow + c0 + 4 * i) =
+                            make_float4(v[4 * i] + v2[4 * i], v[4 * i + 1] + v2[4 * i + 1],
+                                        v[4 * i + 2] + v2[4 * i + 2], v[4 * i + 3] + v2[4 * i + 3]);
+                }
+            }
+            asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+            tc_mbar_arrive(&acc_free);
+            ++t;
+        }
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    if (tid == 0 && fail) atomicExch(&cgtp_linear_error, 1);
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    if (warp == 0)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(kLtTmemCols)
+                     : "memory");
+}
+
 // ------------------------------------------------------------------- host
 
 struct LinearImpl {
@@ -839,8 +1127,9 @@ cgtp_status linear_create(const char* sin, const char* sout, const cgtp_linear_i
     for (int j = 0; j < G.ninstr; ++j) {
         const auto [i, o] = L->instr[j];
         G.g[j] = LinGrad{L->off_in[i], L->in[i].mul, L->off_out[o], L->out[o].mul,
-                         2 * L->in[i].l + 1, (int)L->w_off[j], tiles};
+                         2 * L->in[i].l + 1, (int)L->w_off[j], tiles, G.nmt};
         tiles += ((L->in[i].mul + 31) / 32) * ((L->out[o].mul + 31) / 32);
+        G.nmt += (L->in[i].mul + 127) / 128;
     }
     G.ntiles = tiles;
     bool tc = dt == CGTP_F32;
@@ -976,6 +1265,15 @@ cudaError_t launch_linear_forward(const LinearImpl* L, int64_t n, const void* x,
     return run_pass(*L, L->fwd, L->fwd_nmax, L->fwd_img, n, x, W, out, ws, tc, s);
 }
 
+// The tensor-core weight gradient: fp32 tensor-core layer with every output
+// multiplicity at most 128 (the stacked [hi | lo] image), 16-byte aligned data.
+static bool linear_wgrad_tc_ok(const LinearImpl* L, const void* x, const void* g, const void* part) {
+    if (!L->tc) return false;
+    for (int j = 0; j < L->grad.ninstr; ++j)
+        if (L->grad.g[j].mo > 128) return false;
+    return aligned16(x) && aligned16(g) && aligned16(part);
+}
+
 cudaError_t launch_linear_backward(const LinearImpl* L, int64_t n, const void* x, const void* W,
                                    const void* g, void* gx, void* gW, void* ws, size_t ws_bytes,
                                    bool allow_tc, cudaStream_t s) {
@@ -994,7 +1292,17 @@ cudaError_t launch_linear_backward(const LinearImpl* L, int64_t n, const void* x
         const int64_t S = wgrad_splits(n), per = (n + S - 1) / S;
         unsigned char* part = (unsigned char*)ws + round_up(L->tc ? L->bwd_img : 0, 256);
         const dim3 grid((unsigned)L->grad.ntiles, (unsigned)S);
-        if (f64)
+        if (allow_tc && linear_wgrad_tc_ok(L, x, g, part)) {
+            const int64_t units = (int64_t)L->grad.nmt * S;
+            const unsigned gr = (unsigned)std::min<int64_t>(units, sm_count());
+            const size_t smem = kWgStages * (size_t)(2 * 128 * kWgRows * 4);
+            e = cudaFuncSetAttribute(linear_wgrad_tc_kernel,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (e != cudaSuccess) return e;
+            linear_wgrad_tc_kernel<<<gr, kWgThreads, smem, s>>>(L->grad, n, per, (int)S,
+                                                                (const float*)x, (const float*)g,
+                                                                (float*)part);
+        } else if (f64)
             linear_wgrad_kernel<double><<<grid, 256, 0, s>>>(L->grad, n, per, (const double*)x,
                                                              (const double*)g, (double*)part);
         else

@@ -149,3 +149,19 @@ def test_uvw_convolution_matches_oracle():
     assert_close(host(gx), rx, np.float32, "uvw conv grad_x")
     assert_close(host(gy), ey, np.float32, "uvw conv grad_y")
     assert_close(host(gW), eW, np.float32, "uvw conv grad_W")
+
+
+def test_linear_weight_gradient_long_sums():
+    """grad_W summed over many rows (20,000 items x (1 + 3 + 5) rows per
+    matrix): the tensor-core reduction and the CUDA-core one against the oracle."""
+    need_gpu()
+    cg = _cg()
+    irreps = ("128x0e+128x1o+128x2e", "128x0e+128x1o+64x2e")
+    rng = np.random.default_rng(11)
+    instr, x, W, g = _problem(rng, irreps, 20000, np.float32)
+    lin = cg.Linear(*irreps)
+    rx, rW = O.linear_backward(*irreps, instr, x, W, g)
+    for cc in (False, True):
+        _, gW = lin.backward(dev(x), dev(W), dev(g), need=(False, True), cuda_cores=cc)
+        assert_close(host(gW), rW, np.float32, f"grad_W (cuda cores: {cc})")
+    assert cg.linear_device_status() == 0
