@@ -23,8 +23,11 @@
 //     lo*lo term is about 2^-21 relative); epilogue warps store the results.
 //   * linear_simt_kernel (fp32 / fp64, any shape): shared-memory tiles and 4 x 4
 //     FMA micro-tiles on the CUDA cores.
-//   * linear_wgrad_kernel: per-CTA partial sums of x^T g over a fixed row
-//     range, then the partial rows are added in a fixed order (deterministic).
+//   * linear_wgrad_tc_kernel (fp32 tensor-core layers, mul_out <= 128): the
+//     gradient in W on tcgen05, K = the rows: X^T in tensor memory, G^T as a
+//     stacked K-major image, per-unit partial sums over a fixed row range;
+//     linear_wgrad_kernel does the same on the CUDA cores for other layers.
+//     The partial rows are added in a fixed order (deterministic).
 #include <cuda_runtime.h>
 
 #include <algorithm>

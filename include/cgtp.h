@@ -357,8 +357,10 @@ cgtp_status cgtp_linear_forward(cgtp_linear lin, int64_t n, const void* x, const
 /* Gradients for the cotangent grad_out [n, dim_out]: grad_x [n, dim_in]
  * (= grad_out through the transposed matrices, the tensor-core path as in the
  * forward) and grad_W [weight_numel] (= sum over rows of x^T grad_out per
- * instruction, per-CTA partial sums in the workspace added in fixed order:
- * deterministic); either may be NULL (not computed).  The workspace (at least
+ * instruction, on the tensor cores for tensor-core layers whose output
+ * multiplicities are at most 128, else on the CUDA cores; partial sums over
+ * fixed row ranges in the workspace, added in fixed order: deterministic);
+ * either may be NULL (not computed).  The workspace (at least
  * bwd_bytes, 16-byte aligned) is required when grad_W is requested. */
 cgtp_status cgtp_linear_backward(cgtp_linear lin, int64_t n, const void* x, const void* W,
                                  const void* grad_out, void* grad_x, void* grad_W,
