@@ -84,6 +84,9 @@ cudaError_t launch_linear_backward(const LinearImpl* L, int64_t n, const void* x
                                    const void* g, void* gx, void* gW, void* ws, size_t ws_bytes,
                                    bool allow_tc, cudaStream_t s);
 cudaError_t linear_device_status(int* code);
+bool radial_w2_tc_eligible(int hidden, int64_t n_out);
+cudaError_t launch_radial_w2_tc(int64_t E, int hidden, int64_t n_out, const float* h,
+                                const float* gw, float* partial, int64_t S, cudaStream_t s);
 
 // Partial weight-gradient rows a shared-weight backward may write (grid cap).
 constexpr int64_t kSharedWRows = 2048;

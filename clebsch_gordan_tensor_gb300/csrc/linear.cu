@@ -159,6 +159,8 @@ __global__ void linear_zero_kernel(int64_t n, int64_t stride, int off, int width
 struct LinGrad {
     int xo, mi, go, mo, d, w_off, tile0;
     int mt0;  // first 128-row M tile of j in the tensor-core kernel's list
+    int ldw;  // row stride of gW_j in the output (mo for the layer's own layout)
+    int tr;   // 1: gW_j is stored transposed, element (u, w) at w_off + w ldw + u
 };
 constexpr int kLinMaxGrad = 128;
 struct LinGradDesc {
@@ -216,7 +218,8 @@ linear_wgrad_kernel(const __grid_constant__ LinGradDesc D, int64_t n, int64_t pe
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
         const int u = u0 + ty * 4 + q, w = w0 + tx;
-        if (u < G.mi && w < G.mo) P[(int64_t)u * G.mo + w] = acc[q];
+        if (u < G.mi && w < G.mo)
+            P[G.tr ? (int64_t)w * G.ldw + u : (int64_t)u * G.ldw + w] = acc[q];
     }
 }
 
@@ -713,13 +716,15 @@ linear_tc_kernel(const __grid_constant__ LinDesc D, int64_t n, int nmax,
 // D[u, w] = sum_k A[u, k] B[w, k] with K = rows: A = X^T in tensor memory (lane
 // = input channel u, columns = 32 rows of a chunk), B = G^T in shared memory
 // (K-major, [hi | lo] stacked along N = 2 mul_out), the same three split
-// products as the forward in two instructions per K step.  Work units are
+// products as the forward in two instructions per K step (A_hi [B_hi | B_lo]
+// into 2 mul_out columns, A_lo B_hi added to the first mul_out).  Work units are
 // (instruction, 128-channel M tile, row split s), split s holding the rows of
 // items [s per, (s + 1) per); each unit writes its partial sums to
 // partial[s nw + ...] (zeros for an empty split), added in fixed order
 // afterwards.  Warp roles:
-//   epilogue (warps 0-3): per unit, wait acc_full, read D (lane u), add the
-//     two halves and store the partial row; arrive on acc_free.
+//   epilogue (warps 0-3): per segment, wait acc_full, read D (lane u), add it
+//     to the unit's sums; after the last one store the partial row; arrive on
+//     acc_free.
 //   A producers (warps 4-7, lane quarter warp % 4): each thread loads its
 //     channel u of the chunk's 32 rows (one chunk ahead into registers), writes
 //     hi = the values and lo = round_tf32(x - x cut to 10 bits) with
@@ -730,19 +735,31 @@ linear_tc_kernel(const __grid_constant__ LinDesc D, int64_t n, int nmax,
 //   MMA issuer (warp 16): one wait per chunk, the products, commit to empty
 //     (and acc_full after a unit's last chunk).
 // Chunk k (counted over the CTA's units) uses stage k % 4 and phase (k / 4) % 2
-// of full / empty; the t-th unit with rows uses phase t % 2 of acc_full /
-// acc_free.  Waits are bounded as in the forward kernel.
+// of full / empty.  Precision: the tensor core's fp32 accumulator loses low
+// bits on every addition, so its error grows with the number of rows it sums.
+// A unit's chunks are therefore cut into segments; each segment starts a
+// fresh accumulator and the epilogue adds it, in plain fp32 arithmetic and
+// segment order, into the unit's sums in shared memory.  With every mul_out <=
+// 64 (accumulators of at most 128 columns) two buffers, columns [0, 128) and
+// [128, 256), alternate so that the epilogue drains one while the MMA fills the
+// other, with segments of kWgSeg / 2 chunks; wider outputs use one buffer and
+// segments of kWgSeg chunks.  The t-th segment (counted over the CTA) uses
+// buffer t % nacc and phase (t / nacc) % 2 of acc_full / acc_free.
+// Waits are bounded as in the forward kernel.
 constexpr int kWgStages = 4;
 constexpr int kWgThreads = 32 * 17;
 constexpr int kWgRows = 32;  // rows (K) per chunk
+constexpr int kWgSeg = 16;   // chunks (512 rows) per segment of a single buffer
+// dynamic shared memory: the stages, then the epilogue's sums [128 w][128 u]
+constexpr size_t kWgSmem = kWgStages * (size_t)(2 * 128 * kWgRows * 4) + 128 * 128 * 4;
 
 __global__ void __launch_bounds__(kWgThreads, 1)
 linear_wgrad_tc_kernel(const __grid_constant__ LinGradDesc D, int64_t n, int64_t per, int S,
-                       const float* __restrict__ x, const float* __restrict__ g,
+                       int nacc, const float* __restrict__ x, const float* __restrict__ g,
                        float* __restrict__ partial) {
     extern __shared__ __align__(1024) unsigned char smem[];
     __shared__ __align__(8) unsigned long long full[kWgStages], empty[kWgStages];
-    __shared__ __align__(8) unsigned long long acc_full, acc_free;
+    __shared__ __align__(8) unsigned long long acc_full[2], acc_free[2];
     __shared__ unsigned tmem_base;
     __shared__ int fail;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -760,8 +777,10 @@ linear_wgrad_tc_kernel(const __grid_constant__ LinGradDesc D, int64_t n, int64_t
             tc_mbar_init(&full[i], 12);  // 4 A warps + 8 B warps
             tc_mbar_init(&empty[i], 1);
         }
-        tc_mbar_init(&acc_full, 1);
-        tc_mbar_init(&acc_free, 128);
+        for (int i = 0; i < 2; ++i) {
+            tc_mbar_init(&acc_full[i], 1);
+            tc_mbar_init(&acc_free[i], 128);
+        }
         fail = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -770,6 +789,7 @@ linear_wgrad_tc_kernel(const __grid_constant__ LinGradDesc D, int64_t n, int64_t
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const unsigned tmem = tmem_base;
     const bool issuer = warp == 16;
+    const int seg = nacc == 2 ? kWgSeg / 2 : kWgSeg;
     auto wait = [&](unsigned long long* bar, unsigned parity) -> bool {
         if (!issuer && *(volatile int*)&fail) return false;
         if (issuer ? tc_mbar_wait(bar, parity) : tc_mbar_wait_sleep(bar, parity)) return true;
@@ -919,28 +939,33 @@ linear_wgrad_tc_kernel(const __grid_constant__ LinGradDesc D, int64_t n, int64_t
             bool ok = true;
             for (int ci = 0; ci < U.nch && ok; ++ci, ++k) {
                 const int st = (int)(k % kWgStages);
+                const bool first = ci % seg == 0;
+                const bool last = ci + 1 == U.nch || (ci + 1) % seg == 0;
+                const int b = (int)(t % nacc);
                 ok = wait(&full[st], (unsigned)((k / kWgStages) & 1));
-                if (ok && ci == 0 && t >= 1) ok = wait(&acc_free, (unsigned)((t - 1) & 1));
+                if (ok && first && t >= nacc)
+                    ok = wait(&acc_free[b], (unsigned)(((t - nacc) / nacc) & 1));
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
                 if (leader) {
                     const unsigned b0 = smem_addr(smem + (size_t)st * bslot);
                     const unsigned a0 = tmem + kLtAcol + 64u * st;
+                    const unsigned acc = tmem + 128u * b;
 #pragma unroll
                     for (int k8 = 0; k8 < kWgRows; k8 += 8) {
                         const uint64_t bd = smem_desc(b0 + (unsigned)(k8 >> 2) * lb, lb, 128);
-                        mma_tf32_tmem_a(tmem, a0 + k8, bd, idesc2, (ci == 0 && k8 == 0) ? 0u : 1u);
-                        mma_tf32_tmem_a(tmem, a0 + 32 + k8, bd, idesc, 1u);
+                        mma_tf32_tmem_a(acc, a0 + k8, bd, idesc2, (first && k8 == 0) ? 0u : 1u);
+                        mma_tf32_tmem_a(acc, a0 + 32 + k8, bd, idesc, 1u);
                     }
                     tc_commit(&empty[st]);
-                    if (ci + 1 == U.nch) tc_commit(&acc_full);
+                    if (last) tc_commit(&acc_full[b]);
                 }
                 __syncwarp();
                 last_commit = k;
+                if (last) ++t;
             }
             if (!ok) break;
-            ++t;
             if (__any_sync(0xffffffffu, *(volatile int*)&fail)) break;
         }
         if (leader && last_commit >= 0)
@@ -954,34 +979,54 @@ linear_wgrad_tc_kernel(const __grid_constant__ LinGradDesc D, int64_t n, int64_t
             const LinGrad& G = D.g[U.j];
             const int sp = (int)(u % S);
             const int urow = U.mt * 128 + 32 * warp + lane;  // input channel of this lane
-            float* prow = partial + (int64_t)sp * D.nw + G.w_off + (int64_t)urow * G.mo;
+            // element (urow, w) at prow[w * ws]: rows of the layer's layout, or
+            // a column of a transposed output (lanes then store consecutive words)
+            float* prow = partial + (int64_t)sp * D.nw + G.w_off +
+                          (G.tr ? (int64_t)urow : (int64_t)urow * G.ldw);
+            const int64_t ws = G.tr ? G.ldw : 1;
             const bool live = urow < G.mi;
             if (U.nch == 0) {  // empty split: its partial sums are zero
                 if (live)
-                    for (int w = 0; w < G.mo; w += 4)
-                        *reinterpret_cast<float4*>(prow + w) = make_float4(0.f, 0.f, 0.f, 0.f);
+                    for (int w = 0; w < G.mo; ++w) prow[w * ws] = 0.0f;
                 continue;
             }
-            bool got = wait(&acc_full, (unsigned)(t & 1));
-            got = __all_sync(0xffffffffu, got);
-            if (!got) break;
-            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-            for (int c0 = 0; c0 < G.mo; c0 += 32) {
-                float v[32], v2[32];
-                const unsigned ta = tmem + ((unsigned)(32 * warp) << 16) + (unsigned)c0;
-                tmem_ld32(ta, v);
-                tmem_ld32(ta + (unsigned)G.mo, v2);
-                if (live) {
+            // this thread's running sums, column w at sums[128 w] (lanes contiguous)
+            float* sums = reinterpret_cast<float*>(smem + kWgStages * (size_t)bslot) + 32 * warp + lane;
+            const int nseg = (U.nch + seg - 1) / seg;
+            bool got = true;
+            for (int sg = 0; sg < nseg && got; ++sg, ++t) {
+                const int b = (int)(t % nacc);
+                got = wait(&acc_full[b], (unsigned)((t / nacc) & 1));
+                got = __all_sync(0xffffffffu, got);
+                if (!got) break;
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                const bool fin = sg + 1 == nseg;
+                for (int c0 = 0; c0 < G.mo; c0 += 32) {
+                    float v[32], v2[32];
+                    const unsigned ta = tmem + ((unsigned)(32 * warp) << 16) + 128u * b + (unsigned)c0;
+                    tmem_ld32(ta, v);
+                    tmem_ld32(ta + (unsigned)G.mo, v2);
 #pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        *reinterpret_cast<float4*>(prow + c0 + 4 * i) =
-                            make_float4(v[4 * i] + v2[4 * i], v[4 * i + 1] + v2[4 * i + 1],
-                                        v[4 * i + 2] + v2[4 * i + 2], v[4 * i + 3] + v2[4 * i + 3]);
+                    for (int i = 0; i < 32; ++i) {
+                        v[i] += v2[i];
+                        if (sg > 0) v[i] = sums[128 * (c0 + i)] + v[i];
+                        if (!fin) sums[128 * (c0 + i)] = v[i];
+                    }
+                    if (!fin) continue;
+                    if (live && !G.tr) {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            *reinterpret_cast<float4*>(prow + c0 + 4 * i) =
+                                make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+                    } else if (live) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) prow[(int64_t)(c0 + i) * ws] = v[i];
+                    }
                 }
+                asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+                tc_mbar_arrive(&acc_free[b]);
             }
-            asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-            tc_mbar_arrive(&acc_free);
-            ++t;
+            if (!got) break;
         }
     }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -1130,7 +1175,7 @@ cgtp_status linear_create(const char* sin, const char* sout, const cgtp_linear_i
     for (int j = 0; j < G.ninstr; ++j) {
         const auto [i, o] = L->instr[j];
         G.g[j] = LinGrad{L->off_in[i], L->in[i].mul, L->off_out[o], L->out[o].mul,
-                         2 * L->in[i].l + 1, (int)L->w_off[j], tiles, G.nmt};
+                         2 * L->in[i].l + 1, (int)L->w_off[j], tiles, G.nmt, L->out[o].mul, 0};
         tiles += ((L->in[i].mul + 31) / 32) * ((L->out[o].mul + 31) / 32);
         G.nmt += (L->in[i].mul + 127) / 128;
     }
@@ -1268,6 +1313,14 @@ cudaError_t launch_linear_forward(const LinearImpl* L, int64_t n, const void* x,
     return run_pass(*L, L->fwd, L->fwd_nmax, L->fwd_img, n, x, W, out, ws, tc, s);
 }
 
+// Accumulator buffers of the tensor-core weight gradient: two when every
+// stacked [hi | lo] accumulator (2 mul_out columns) fits in 128 columns.
+static int wgrad_accumulators(const LinGradDesc& G) {
+    for (int j = 0; j < G.ninstr; ++j)
+        if (G.g[j].mo > 64) return 1;
+    return 2;
+}
+
 // The tensor-core weight gradient: fp32 tensor-core layer with every output
 // multiplicity at most 128 (the stacked [hi | lo] image), 16-byte aligned data.
 static bool linear_wgrad_tc_ok(const LinearImpl* L, const void* x, const void* g, const void* part) {
@@ -1298,11 +1351,11 @@ cudaError_t launch_linear_backward(const LinearImpl* L, int64_t n, const void* x
         if (allow_tc && linear_wgrad_tc_ok(L, x, g, part)) {
             const int64_t units = (int64_t)L->grad.nmt * S;
             const unsigned gr = (unsigned)std::min<int64_t>(units, sm_count());
-            const size_t smem = kWgStages * (size_t)(2 * 128 * kWgRows * 4);
             e = cudaFuncSetAttribute(linear_wgrad_tc_kernel,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kWgSmem);
             if (e != cudaSuccess) return e;
-            linear_wgrad_tc_kernel<<<gr, kWgThreads, smem, s>>>(L->grad, n, per, (int)S,
+            linear_wgrad_tc_kernel<<<gr, kWgThreads, kWgSmem, s>>>(L->grad, n, per, (int)S,
+                                                                wgrad_accumulators(L->grad),
                                                                 (const float*)x, (const float*)g,
                                                                 (float*)part);
         } else if (f64)
@@ -1324,6 +1377,39 @@ cudaError_t linear_device_status(int* code) {
     cudaError_t e = cudaMemcpyFromSymbol(code, cgtp_linear_error, sizeof(int));
     if (e == cudaSuccess) e = cudaMemcpyToSymbol(cgtp_linear_error, &zero, sizeof(int));
     return e;
+}
+
+// grad_W2 = h^T grad_w of the radial network (a sum over edges) on the tensor
+// cores through the weight-gradient kernel: "x" = grad_w [E, n_out] in
+// 128-column instructions (M = the output columns), "g" = h [E, hidden]
+// (N = hidden), each instruction's [128 x hidden] block stored transposed into
+// the row-major [hidden, n_out] partial rows.  fp32, hidden % 32 == 0 and
+// <= 128, n_out % 128 == 0 and <= 128 * kLinMaxGrad, 16-byte aligned data.
+bool radial_w2_tc_eligible(int hidden, int64_t n_out) {
+    return hidden % 32 == 0 && hidden <= 128 && n_out % 128 == 0 && n_out / 128 <= kLinMaxGrad;
+}
+
+cudaError_t launch_radial_w2_tc(int64_t E, int hidden, int64_t n_out, const float* h,
+                                const float* gw, float* partial, int64_t S, cudaStream_t s) {
+    auto G = std::make_unique<LinGradDesc>();
+    G->ninstr = (int)(n_out / 128);
+    G->ntiles = 0;
+    G->nmt = G->ninstr;
+    G->x_stride = n_out;
+    G->g_stride = hidden;
+    G->nw = (int64_t)hidden * n_out;
+    for (int j = 0; j < G->ninstr; ++j)
+        G->g[j] = LinGrad{128 * j, 128, 0, hidden, 1, 128 * j, 0, j, (int)n_out, 1};
+    const int64_t per = (E + S - 1) / S;
+    const int64_t units = (int64_t)G->nmt * S;
+    const unsigned gr = (unsigned)std::min<int64_t>(units, sm_count());
+    cudaError_t e = cudaFuncSetAttribute(linear_wgrad_tc_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kWgSmem);
+    if (e != cudaSuccess) return e;
+    linear_wgrad_tc_kernel<<<gr, kWgThreads, kWgSmem, s>>>(*G, E, per, (int)S,
+                                                           wgrad_accumulators(*G), gw, h, partial);
+    count_launch();
+    return cudaGetLastError();
 }
 
 }  // namespace cgtp

@@ -1007,11 +1007,45 @@ static size_t bw_image_bytes(bool f64, int nb, int hidden, int64_t n_out) {
     return radial_bwd_tc_eligible(f64, nb, hidden, n_out) ? (size_t)n_out * 2 * hidden * 4 : 0;
 }
 
+// The hidden activations h [E, hidden] stored for the tensor-core grad_W2.
+static size_t bw_h_bytes(bool f64, int64_t E, int hidden, int64_t n_out) {
+    return !f64 && radial_w2_tc_eligible(hidden, n_out) ? ((size_t)E * hidden * 4 + 255) / 256 * 256
+                                                         : 0;
+}
+
 size_t radial_backward_workspace_bytes(bool f64, int64_t E, int nb, int hidden, int64_t n_out) {
     const size_t es = f64 ? 8 : 4;
     const size_t p1 = ((size_t)bw_grid1(E) * nb * hidden * es + 15) / 16 * 16;
-    return bw_image_bytes(f64, nb, hidden, n_out) + p1 +
-           (size_t)bw_splits(E, n_out) * hidden * n_out * es;
+    const size_t p2 = ((size_t)bw_splits(E, n_out) * hidden * n_out * es + 255) / 256 * 256;
+    return bw_image_bytes(f64, nb, hidden, n_out) + p1 + p2 + bw_h_bytes(f64, E, hidden, n_out);
+}
+
+// h[e] = silu(b(|vec[e]|) W1), one thread per edge (for the tensor-core grad_W2).
+__global__ void __launch_bounds__(128) radial_h_kernel(int64_t E, int nb, float rc, int hidden,
+                                                       const float* __restrict__ vec,
+                                                       const float* __restrict__ W1,
+                                                       float* __restrict__ h) {
+    const float pref = sqrtf(2.0f / rc);
+    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < E;
+         e += (int64_t)gridDim.x * blockDim.x) {
+        const float* v = vec + 3 * e;
+        const float r = sqrtf(v[0] * v[0] + v[1] * v[1] + v[2] * v[2]);
+        float b[kTcNbMax];
+#pragma unroll
+        for (int n = 0; n < kTcNbMax; ++n) b[n] = n < nb ? bessel_f<float>(n + 1, r, rc, pref) : 0.0f;
+        for (int k4 = 0; k4 < hidden; k4 += 4) {
+            float a[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int n = 0; n < kTcNbMax; ++n)
+                if (n < nb) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) a[q] = fmaf(b[n], __ldg(W1 + n * hidden + k4 + q), a[q]);
+                }
+            *reinterpret_cast<float4*>(h + e * hidden + k4) =
+                make_float4(silu_f<float>(a[0]), silu_f<float>(a[1]), silu_f<float>(a[2]),
+                            silu_f<float>(a[3]));
+        }
+    }
 }
 
 cudaError_t launch_radial_backward(bool f64, bool tensor_cores, int64_t E, int nb, double rc,
@@ -1075,7 +1109,20 @@ cudaError_t launch_radial_backward(bool f64, bool tensor_cores, int64_t E, int n
         if ((e = cudaGetLastError())) return e;
         if (gW1 && (e = launch_reduce_rows(f64, p1, g1, (int64_t)nb * hidden, gW1, s))) return e;
     }
-    if (gW2) {
+    if (gW2 && !f64 && tensor_cores && radial_w2_tc_eligible(hidden, n_out) && nb <= kTcNbMax &&
+        ((uintptr_t)gw & 15) == 0) {
+        // h into the workspace, then h^T grad_w on the tensor cores
+        float* hbuf = reinterpret_cast<float*>(
+            p2 + ((size_t)sp * hidden * n_out * es + 255) / 256 * 256);
+        const unsigned hg = (unsigned)std::max<int64_t>(1, std::min<int64_t>((E + 127) / 128, 65535));
+        radial_h_kernel<<<hg, 128, 0, s>>>(E, nb, (float)rc, hidden, (const float*)vec,
+                                           (const float*)W1, hbuf);
+        count_launch();
+        if ((e = cudaGetLastError())) return e;
+        if ((e = launch_radial_w2_tc(E, hidden, n_out, hbuf, (const float*)gw, (float*)p2, sp, s)))
+            return e;
+        if ((e = launch_reduce_rows(false, p2, sp, (int64_t)hidden * n_out, gW2, s))) return e;
+    } else if (gW2) {
         if (f64) {
             auto* k = radial_bwd_w2_kernel<double>;
             if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm2)))
