@@ -8,6 +8,7 @@ Workloads (seeded recipes in ``workloads``):
   2  fused conv, N = 10,000 atoms, ~525k edges, fp32     (sampled rows)
   3  fused conv, N = 5,000 atoms, 128 channels, fp64     (forward, sampled)
   4  TFN layer on 1000 molecules, fwd + bwd + double backward and forces, fp32
+  and the 'uvw' channel mixing of workload 1 (200,000 samples, fp32)
 """
 import numpy as np
 import pytest
@@ -166,3 +167,41 @@ def test_config4_fused_kv_sampled():
     cfg = W.config4_kv()
     conv_weights(cfg)  # the workload carries its own w
     _conv_sampled(cfg, np.float32, True)
+
+
+def test_uvw_mixing_full_size():
+    """The 'uvw' workload's channel mixing at full size (200,000 samples; 24
+    path blocks of 128 channels into 128x(0e,1o,1e,2o,2e,3o,3e); its 24 shared
+    [128, 128] matrices): forward, x-gradient and W-gradient through the
+    calls the benchmark times.  The input is a 1000-sample block repeated 200
+    times and copy k of the cotangent carries a sign s_k (107 plus, 93 minus,
+    shuffled), so the oracle's results on the block give every output row and
+    the W-gradient, a sum over 1.8 million rows per matrix set, is
+    (sum_k s_k) = 14 times the block's."""
+    need_gpu()
+    cg = _cg()
+    B, P = 200_000, 1000
+    uvw = cg.UVWProduct(*W.CFG1)
+    lin = uvw.linear
+    assert lin.tensor_cores
+    instr = [lin.instruction(j)[:2] for j in range(lin.n_instr)]
+    Wm = W.config1_uvw(P)["W"]
+    rng = np.random.default_rng(23)
+    X0 = rng.standard_normal((P, uvw.dim_mid)).astype(np.float32)
+    G0 = rng.standard_normal((P, uvw.dim_out)).astype(np.float32)
+    s = np.array([1.0] * 107 + [-1.0] * 93, dtype=np.float32)
+    rng.shuffle(s)
+    x = dev(X0).repeat(B // P, 1)
+    g = (dev(G0).unsqueeze(0) * dev(s)[:, None, None]).reshape(B, uvw.dim_out)
+    out = lin.forward(x, dev(Wm))
+    gx, _ = lin.backward(x, dev(Wm), g, need=(True, False))
+    _, gW = lin.backward(x, dev(Wm), g, need=(False, True))
+    rout = O.linear_forward(uvw.mid, W.CFG1[2], instr, X0, Wm)
+    rx, rW = O.linear_backward(uvw.mid, W.CFG1[2], instr, X0, Wm, G0)
+    idx = _sample(rng, B, 3000)
+    ti = torch.from_numpy(idx).cuda()
+    assert_close(host(out[ti]), rout[idx % P], np.float32, "out rows")
+    assert_close(host(gx[ti]), s[idx // P, None].astype(np.float64) * rx[idx % P], np.float32,
+                 "grad_x rows")
+    assert_close(host(gW), float(s.sum()) * rW, np.float32, "grad_W")
+    assert cg.linear_device_status() == 0
