@@ -30,6 +30,7 @@ _lib = None
 F32, F64 = 0, 1
 W_PER_EDGE, W_SHARED = 0, 1
 WEIGHTS_BF16 = 1 << 24  # plan flag: weights stored as bfloat16
+WEIGHTS_F16 = 1 << 25  # plan flag: weights stored as IEEE binary16
 
 
 class CgtpError(RuntimeError):
@@ -199,14 +200,14 @@ class Plan:
     def __init__(self, irreps_in1: str, irreps_in2: str, irreps_out: str,
                  dtype=torch.float32, shared_weights: bool = False, instructions=None,
                  weight_dtype=None):
-        """weight_dtype=torch.bfloat16 stores the weights as bfloat16 (fp32 plans;
-        arithmetic, features and grad_w stay fp32)."""
+        """weight_dtype=torch.bfloat16 or torch.float16 stores the weights in that
+        16-bit format (fp32 plans; arithmetic, features and grad_w stay fp32)."""
         L = lib()
         self.dtype = dtype
         self.wdtype = dtype if weight_dtype is None else weight_dtype
-        if self.wdtype not in (dtype, torch.bfloat16):
+        if self.wdtype not in (dtype, torch.bfloat16, torch.float16):
             raise CgtpError(f"weight_dtype {weight_dtype} is not supported")
-        flags = WEIGHTS_BF16 if self.wdtype == torch.bfloat16 else 0
+        flags = {torch.bfloat16: WEIGHTS_BF16, torch.float16: WEIGHTS_F16}.get(self.wdtype, 0)
         self.irreps = (irreps_in1, irreps_in2, irreps_out)
         h = ctypes.c_void_p()
         arr, n = None, 0
@@ -447,7 +448,8 @@ def radial_forward(vec, W1, W2, cutoff: float = 5.0, out=None, hidden_out=None,
     _check(lib().cgtp_radial_forward(_dt(vec.dtype), E, nb, float(cutoff), hidden, n_out,
                                      _ptr(vec), _ptr(W1), _ptr(W2), _ptr(out), _ptr(hidden_out),
                                      _ptr(ws), n.value,
-                                     (1 if cuda_cores else 0) | (2 if odt == torch.bfloat16 else 0),
+                                     (1 if cuda_cores else 0) | (2 if odt == torch.bfloat16 else 0)
+                                     | (4 if odt == torch.float16 else 0),
                                      _stream()))
     return out
 

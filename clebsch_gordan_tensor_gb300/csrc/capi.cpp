@@ -54,7 +54,7 @@ static size_t row_align(const Plan& p) {
 
 // Weight rows: bfloat16 pairs are read as one 32-bit word per lane.
 static size_t w_align(const Plan& p) {
-    return p.w_bf16 ? (p.cpt == 2 ? 4 : 2) : row_align(p);
+    return p.w16() ? (p.cpt == 2 ? 4 : 2) : row_align(p);
 }
 
 static cgtp_status check_w(const Plan& p, const void* w) {
@@ -310,13 +310,16 @@ cgtp_status cgtp_plan_create(cgtp_plan* out, const char* irreps_in1, const char*
     if (dtype != CGTP_F32 && dtype != CGTP_F64) return fail(CGTP_E_ARG, "bad dtype");
     if (wmode != CGTP_W_PER_EDGE && wmode != CGTP_W_SHARED) return fail(CGTP_E_ARG, "bad wmode");
     const bool w_bf16 = (flags & CGTP_PLAN_WEIGHTS_BF16) != 0;
-    if (w_bf16 && dtype != CGTP_F32)
-        return fail(CGTP_E_UNSUPPORTED, "bfloat16 weights need an fp32 plan");
+    const bool w_f16 = (flags & CGTP_PLAN_WEIGHTS_F16) != 0;
+    if (w_bf16 && w_f16) return fail(CGTP_E_ARG, "both 16-bit weight formats requested");
+    if ((w_bf16 || w_f16) && dtype != CGTP_F32)
+        return fail(CGTP_E_UNSUPPORTED, "16-bit weights need an fp32 plan");
     auto* h = new cgtp_plan_s();
     h->p.dtype = dtype;
     h->p.wmode = wmode;
     h->p.flags = flags;
     h->p.w_bf16 = w_bf16;
+    h->p.w_f16 = w_f16;
     std::string err;
     cgtp_status st = build_plan(h->p, irreps_in1, irreps_in2, irreps_out, instr, n_instr, err);
     if (st != CGTP_OK) {
@@ -520,7 +523,7 @@ cgtp_status cgtp_double_backward_ws(cgtp_plan plan, int64_t B, const void* x, co
     }
     if (!x || !y || !w || !grad_out) return fail(CGTP_E_ARG, "NULL input tensor");
     Plan& p = plan->p;
-    if (p.w_bf16) return fail(CGTP_E_UNSUPPORTED, "double backward of a bfloat16-weight plan");
+    if (p.w16()) return fail(CGTP_E_UNSUPPORTED, "double backward of a 16-bit-weight plan");
     cgtp_status st = check_rows(p, {x, grad_out, gg_x, gg_w, d_x, d_w, d_grad_out});
     if (st != CGTP_OK) return st;
     if ((st = check_w(p, w)) != CGTP_OK) return st;
@@ -636,7 +639,7 @@ cgtp_status cgtp_conv_double_backward_ws(cgtp_plan plan, int64_t N, int64_t E,
     if (N == 0) return CGTP_OK;
     if (!x || !grad_out || (E > 0 && (!y || !w))) return fail(CGTP_E_ARG, "NULL input tensor");
     Plan& p = plan->p;
-    if (p.w_bf16) return fail(CGTP_E_UNSUPPORTED, "double backward of a bfloat16-weight plan");
+    if (p.w16()) return fail(CGTP_E_UNSUPPORTED, "double backward of a 16-bit-weight plan");
     if ((st = check_rows(p, {x, grad_out, gg_x, gg_w, d_x, d_w, d_grad_out})) != CGTP_OK)
         return st;
     if ((st = check_w(p, w)) != CGTP_OK) return st;
@@ -864,17 +867,21 @@ cgtp_status cgtp_radial_forward(cgtp_dtype dtype, int64_t E, int n_basis, double
     if (!vec || !W1 || !W2 || !w) return fail(CGTP_E_ARG, "NULL tensor");
     const size_t es = dtype == CGTP_F64 ? 8 : 4;
     const bool out_bf16 = (flags & CGTP_RADIAL_OUT_BF16) != 0;
-    if (out_bf16 && dtype != CGTP_F32)
-        return fail(CGTP_E_UNSUPPORTED, "bfloat16 output needs fp32 inputs");
+    const bool out_f16 = (flags & CGTP_RADIAL_OUT_F16) != 0;
+    if (out_bf16 && out_f16) return fail(CGTP_E_ARG, "both 16-bit output formats requested");
+    if ((out_bf16 || out_f16) && dtype != CGTP_F32)
+        return fail(CGTP_E_UNSUPPORTED, "16-bit output needs fp32 inputs");
     for (const void* q : {vec, W1, W2, (const void*)h})
         if (!aligned(q, es)) return fail(CGTP_E_ARG, "tensor pointer not aligned to its element");
-    if (!aligned(w, out_bf16 ? 2 : es)) return fail(CGTP_E_ARG, "w not aligned to its element");
+    if (!aligned(w, out_bf16 || out_f16 ? 2 : es))
+        return fail(CGTP_E_ARG, "w not aligned to its element");
     const bool f64 = dtype == CGTP_F64;
     const size_t need = radial_workspace_bytes(f64, n_basis, hidden, n_out);
     const bool tc = !(flags & CGTP_RADIAL_CUDA_CORES) && need > 0 && workspace &&
                     workspace_bytes >= need && aligned(workspace, 16) &&
                     radial_tc_eligible(f64, n_basis, hidden, n_out, vec, W2, w, h);
-    cudaError_t e = launch_radial_forward(f64, tc, out_bf16, E, n_basis, cutoff, hidden, n_out,
+    cudaError_t e = launch_radial_forward(f64, tc, out_bf16 ? 1 : out_f16 ? 2 : 0, E, n_basis,
+                                          cutoff, hidden, n_out,
                                           vec, W1, W2, w, h, workspace, workspace_bytes,
                                           S(stream));
     if (e != cudaSuccess) return cuda_fail(e, "radial_forward");

@@ -53,7 +53,7 @@ cudaError_t launch_reduce_rows(bool f64, const void* partial, int64_t rows, int6
 bool radial_tc_eligible(bool f64, int nb, int hidden, int64_t n_out, const void* vec,
                         const void* W2, const void* w, const void* h);
 size_t radial_workspace_bytes(bool f64, int nb, int hidden, int64_t n_out);
-cudaError_t launch_radial_forward(bool f64, bool tensor_cores, bool out_bf16, int64_t E, int nb,
+cudaError_t launch_radial_forward(bool f64, bool tensor_cores, int out16, int64_t E, int nb,
                                   double rc, int hidden, int64_t n_out, const void* vec,
                                   const void* W1, const void* W2, void* w, void* h, void* ws,
                                   size_t ws_bytes, cudaStream_t s);

@@ -332,7 +332,7 @@ cgtp_status build_plan(Plan& p, const char* s1, const char* s2, const char* so,
 
     // staged kernels: whole warps of full channel groups, 16-byte rows
     const size_t es = p.dtype == CGTP_F64 ? 8 : 4;
-    const size_t WB = (size_t)p.wdim * (p.w_bf16 ? 2 : es), XB = (size_t)p.dimx * es,
+    const size_t WB = (size_t)p.wdim * (p.w16() ? 2 : es), XB = (size_t)p.dimx * es,
                  GB = (size_t)p.dimo * es,
                  YB = (size_t)p.ny * es;
     const bool rows16 = WB % 16 == 0 && XB % 16 == 0 && GB % 16 == 0 && YB % 16 == 0;
@@ -668,7 +668,7 @@ std::string Plan::kernel_source() const {
        << (ny + lanes - 1) / lanes << "\n";
     os << "#define STAGED " << (staged ? 1 : 0) << "\n#define STAGES_F " << stages_f
        << "\n#define STAGES_B " << stages_b << "\n#define W_DIRECT_F " << (w_direct_f ? 1 : 0)
-       << "\n#define W_DIRECT_B " << (w_direct_b ? 1 : 0) << "\n#define W_BF16 " << (w_bf16 ? 1 : 0)
+       << "\n#define W_DIRECT_B " << (w_direct_b ? 1 : 0) << "\n#define W_STORE " << (w_bf16 ? 1 : w_f16 ? 2 : 0)
        << "\n#define T_DUP_B 0\n#define W_BUF2 " << (((flags >> 18) & 1u) ? 0 : 1)
        << "\n#define SHARED_W " << (wmode == CGTP_W_SHARED ? 1 : 0)
        << "\n#define GF " << std::max<size_t>(1, fwd_groups.size()) << "\n#define GB "

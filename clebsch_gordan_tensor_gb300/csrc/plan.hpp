@@ -54,6 +54,8 @@ struct Plan {
     cgtp_dtype dtype = CGTP_F32;
     cgtp_wmode wmode = CGTP_W_PER_EDGE;
     bool w_bf16 = false;  // weights stored as bfloat16 (fp32 arithmetic)
+    bool w_f16 = false;   // weights stored as IEEE binary16 (fp32 arithmetic)
+    bool w16() const { return w_bf16 || w_f16; }
     unsigned flags = 0;
 
     // launch geometry (fixed at plan creation)

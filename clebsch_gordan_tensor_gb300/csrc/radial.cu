@@ -27,6 +27,7 @@
 //     FMA micro-tiles on the CUDA cores.
 // Both compute b and h the same way on the CUDA cores.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -40,11 +41,25 @@ namespace cgtp {
 
 __device__ int cgtp_radial_error;  // nonzero: a bounded wait timed out
 
-// Output element: the compute type, or bfloat16 (rounded to nearest even).
+// Output element: the compute type, bfloat16 or IEEE binary16 (each rounded
+// to nearest even).
 template <typename TW, typename T>
 __device__ __forceinline__ TW out_cast(T v) {
-    if constexpr (sizeof(TW) == 2) return __float2bfloat16_rn((float)v);
+    if constexpr (std::is_same_v<TW, __nv_bfloat16>) return __float2bfloat16_rn((float)v);
+    else if constexpr (std::is_same_v<TW, __half>) return __float2half_rn((float)v);
     else return (TW)v;
+}
+
+// Two 16-bit outputs in one word (a in the low half).
+template <typename TW>
+__device__ __forceinline__ unsigned out_pack2(float a, float b) {
+    if constexpr (std::is_same_v<TW, __nv_bfloat16>) {
+        const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+        return *reinterpret_cast<const unsigned*>(&v);
+    } else {
+        const __half2 v = __floats2half2_rn(a, b);
+        return *reinterpret_cast<const unsigned*>(&v);
+    }
 }
 
 template <typename T>
@@ -425,12 +440,8 @@ radial_tc_kernel(int64_t E, int nb, float rc, int hidden, int64_t n_out,
                             if (e < E) {
                                 TW* dst = w + e * n_out + col0 + blk * 32 + (lane & 7) * 4;
                                 if constexpr (sizeof(TW) == 2) {
-                                    const __nv_bfloat162 a = __floats2bfloat162_rn(val.x, val.y);
-                                    const __nv_bfloat162 b2 = __floats2bfloat162_rn(val.z, val.w);
-                                    uint2 u;
-                                    u.x = *reinterpret_cast<const unsigned*>(&a);
-                                    u.y = *reinterpret_cast<const unsigned*>(&b2);
-                                    *reinterpret_cast<uint2*>(dst) = u;
+                                    *reinterpret_cast<uint2*>(dst) =
+                                        make_uint2(out_pack2<TW>(val.x, val.y), out_pack2<TW>(val.z, val.w));
                                 } else {
                                     *reinterpret_cast<float4*>(dst) = val;
                                 }
@@ -1160,7 +1171,43 @@ size_t radial_workspace_bytes(bool f64, int nb, int hidden, int64_t n_out) {
     return (size_t)n_out * hidden * 8;  // TF32 hi and lo parts of W2, packed
 }
 
-cudaError_t launch_radial_forward(bool f64, bool tensor_cores, bool out_bf16, int64_t E, int nb,
+// The fp32 launches for output element TW (float, bfloat16 or binary16).
+template <typename TW>
+static cudaError_t radial_forward_f32(bool tensor_cores, int sms, int64_t E, int nb, float rc,
+                                      int hidden, int64_t n_out, const float* vec,
+                                      const float* W1, const float* W2, TW* w, float* h,
+                                      void* ws, cudaStream_t s) {
+    cudaError_t e;
+    if (tensor_cores) {
+        e = cudaFuncSetAttribute(radial_tc_kernel<TW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kTcSmem);
+        if (e != cudaSuccess) return e;
+        const int64_t total = (int64_t)hidden * n_out;
+        const unsigned pg =
+            (unsigned)std::max<int64_t>(1, std::min<int64_t>((total + 255) / 256, (int64_t)sms * 8));
+        radial_pack_kernel<<<pg, 256, 0, s>>>(hidden, n_out, W2, (unsigned char*)ws);
+        count_launch();
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        const int64_t tiles = (E + kTcM - 1) / kTcM;
+        const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(tiles, sms));
+        radial_tc_kernel<TW><<<grid, kTcThreads, kTcSmem, s>>>(E, nb, rc, hidden, n_out, vec, W1,
+                                                               (const unsigned char*)ws, w, h);
+        count_launch();
+        return cudaGetLastError();
+    }
+    const size_t smem = (size_t)kSimtEdges * (nb + hidden) * 4;
+    const int64_t tiles = (E + kSimtEdges - 1) / kSimtEdges;
+    const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(tiles, (int64_t)sms * 8));
+    auto* k = radial_simt_kernel<float, TW>;
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    k<<<grid, kSimtThreads, smem, s>>>(E, nb, rc, hidden, n_out, vec, W1, W2, w, h);
+    count_launch();
+    return cudaGetLastError();
+}
+
+cudaError_t launch_radial_forward(bool f64, bool tensor_cores, int out16, int64_t E, int nb,
                                   double rc, int hidden, int64_t n_out, const void* vec,
                                   const void* W1, const void* W2, void* w, void* h, void* ws,
                                   size_t ws_bytes, cudaStream_t s) {
@@ -1169,37 +1216,11 @@ cudaError_t launch_radial_forward(bool f64, bool tensor_cores, bool out_bf16, in
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
     (void)ws_bytes;
-    if (tensor_cores) {
-        auto* kern = out_bf16 ? (void*)radial_tc_kernel<__nv_bfloat16> : (void*)radial_tc_kernel<float>;
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTcSmem);
-        if (e != cudaSuccess) return e;
-        const int64_t total = (int64_t)hidden * n_out;
-        const unsigned pg =
-            (unsigned)std::max<int64_t>(1, std::min<int64_t>((total + 255) / 256, (int64_t)sms * 8));
-        radial_pack_kernel<<<pg, 256, 0, s>>>(hidden, n_out, (const float*)W2, (unsigned char*)ws);
-        count_launch();
-        e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
-        const int64_t tiles = (E + kTcM - 1) / kTcM;
-        const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(tiles, sms));
-        if (out_bf16) {
-            radial_tc_kernel<__nv_bfloat16><<<grid, kTcThreads, kTcSmem, s>>>(
-                E, nb, (float)rc, hidden, n_out, (const float*)vec, (const float*)W1,
-                (const unsigned char*)ws, (__nv_bfloat16*)w, (float*)h);
-            count_launch();
-        } else {
-            radial_tc_kernel<float><<<grid, kTcThreads, kTcSmem, s>>>(
-                E, nb, (float)rc, hidden, n_out, (const float*)vec, (const float*)W1,
-                (const unsigned char*)ws, (float*)w, (float*)h);
-            count_launch();
-        }
-        return cudaGetLastError();
-    }
-    const size_t es = f64 ? 8 : 4;
-    const size_t smem = (size_t)kSimtEdges * (nb + hidden) * es;
-    const int64_t tiles = (E + kSimtEdges - 1) / kSimtEdges;
-    const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(tiles, (int64_t)sms * 8));
     if (f64) {
+        const size_t smem = (size_t)kSimtEdges * (nb + hidden) * 8;
+        const int64_t tiles = (E + kSimtEdges - 1) / kSimtEdges;
+        const unsigned grid =
+            (unsigned)std::max<int64_t>(1, std::min<int64_t>(tiles, (int64_t)sms * 8));
         auto* k = radial_simt_kernel<double, double>;
         e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
@@ -1207,24 +1228,19 @@ cudaError_t launch_radial_forward(bool f64, bool tensor_cores, bool out_bf16, in
                                            (const double*)W1, (const double*)W2, (double*)w,
                                            (double*)h);
         count_launch();
-    } else if (out_bf16) {
-        auto* k = radial_simt_kernel<float, __nv_bfloat16>;
-        e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        k<<<grid, kSimtThreads, smem, s>>>(E, nb, (float)rc, hidden, n_out, (const float*)vec,
-                                           (const float*)W1, (const float*)W2, (__nv_bfloat16*)w,
-                                           (float*)h);
-        count_launch();
-    } else {
-        auto* k = radial_simt_kernel<float, float>;
-        e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        k<<<grid, kSimtThreads, smem, s>>>(E, nb, (float)rc, hidden, n_out, (const float*)vec,
-                                           (const float*)W1, (const float*)W2, (float*)w,
-                                           (float*)h);
-        count_launch();
+        return cudaGetLastError();
     }
-    return cudaGetLastError();
+    const float* v = (const float*)vec;
+    const float* a = (const float*)W1;
+    const float* b = (const float*)W2;
+    if (out16 == 1)
+        return radial_forward_f32(tensor_cores, sms, E, nb, (float)rc, hidden, n_out, v, a, b,
+                                  (__nv_bfloat16*)w, (float*)h, ws, s);
+    if (out16 == 2)
+        return radial_forward_f32(tensor_cores, sms, E, nb, (float)rc, hidden, n_out, v, a, b,
+                                  (__half*)w, (float*)h, ws, s);
+    return radial_forward_f32(tensor_cores, sms, E, nb, (float)rc, hidden, n_out, v, a, b,
+                              (float*)w, (float*)h, ws, s);
 }
 
 cudaError_t radial_device_status(int* code) {

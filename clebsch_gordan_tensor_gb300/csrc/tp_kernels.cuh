@@ -87,20 +87,37 @@ __device__ __forceinline__ VR ldv_m(const REAL* p, int ch) {
     return CH_ACTIVE(ch) ? ldv(p, ch) : vzero();
 }
 
-// Weight storage: REAL, or bfloat16 (W_BF16) widened exactly to fp32 on load;
-// the arithmetic is the same either way.  WRAW is what one lane loads for its
-// channels (two bf16 in one 32-bit word when CPT == 2: channel 2ch in the low
-// half).
-#if W_BF16
+// Weight storage (W_STORE): 0 = REAL; 1 = bfloat16, 2 = IEEE binary16, each
+// widened exactly to fp32 on load (every value of either format is an fp32
+// value); the arithmetic is the same in all three.  WRAW is what one lane
+// loads for its channels (two 16-bit values in one 32-bit word when CPT == 2:
+// channel 2ch in the low half).
+#if W_STORE == 2
+__device__ __forceinline__ float h2f(unsigned short h) {
+    float f;
+    asm("cvt.f32.f16 %0, %1;" : "=f"(f) : "h"(h));
+    return f;
+}
+#endif
+#if W_STORE != 0
 typedef unsigned short WT;
 #if CPT == 2
 typedef unsigned WRAW;
 __device__ __forceinline__ VR wcvt(WRAW u) {
+#if W_STORE == 1
     return ((u64)(u & 0xffff0000u) << 32) | (u64)(u << 16);
+#else
+    return ((u64)__float_as_uint(h2f((unsigned short)(u >> 16))) << 32) |
+           (u64)__float_as_uint(h2f((unsigned short)(u & 0xffffu)));
+#endif
 }
 #else
 typedef unsigned short WRAW;
+#if W_STORE == 1
 __device__ __forceinline__ VR wcvt(WRAW u) { return __uint_as_float((unsigned)u << 16); }
+#else
+__device__ __forceinline__ VR wcvt(WRAW u) { return h2f(u); }
+#endif
 #endif
 #else
 typedef REAL WT;

@@ -101,6 +101,11 @@ typedef struct {
  * abstract).  fp32 plans only (else CGTP_E_UNSUPPORTED); the double backward
  * of such a plan returns CGTP_E_UNSUPPORTED. */
 #define CGTP_PLAN_WEIGHTS_BF16 (1u << 24)
+/* CGTP_PLAN_WEIGHTS_F16 (bit 25): as CGTP_PLAN_WEIGHTS_BF16 with the weights
+ * stored as IEEE binary16 (11 significant bits, range +-65504; values below
+ * 2^-14 are subnormal), widened exactly to fp32 on load.  Not combined with
+ * CGTP_PLAN_WEIGHTS_BF16 (CGTP_E_ARG); the same restrictions otherwise. */
+#define CGTP_PLAN_WEIGHTS_F16 (1u << 25)
 cgtp_status cgtp_plan_create(cgtp_plan* out, const char* irreps_in1, const char* irreps_in2,
                              const char* irreps_out, const cgtp_instr* instr, int n_instr,
                              cgtp_dtype dtype, cgtp_wmode wmode, unsigned flags);
@@ -397,6 +402,10 @@ cgtp_status cgtp_linear_device_status(int* code);
  * even; fp32 inputs only, else CGTP_E_UNSUPPORTED) for plans created with
  * CGTP_PLAN_WEIGHTS_BF16; h stays fp32. */
 #define CGTP_RADIAL_OUT_BF16 2u
+/* flags & CGTP_RADIAL_OUT_F16: w is written as IEEE binary16 (rounded to
+ * nearest even), for plans created with CGTP_PLAN_WEIGHTS_F16; fp32 inputs
+ * only; not combined with CGTP_RADIAL_OUT_BF16 (CGTP_E_ARG). */
+#define CGTP_RADIAL_OUT_F16 4u
 cgtp_status cgtp_radial_forward(cgtp_dtype dtype, int64_t E, int n_basis, double cutoff,
                                 int hidden, int64_t n_out, const void* vec, const void* W1,
                                 const void* W2, void* w, void* h, void* workspace,

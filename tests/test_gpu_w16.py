@@ -1,8 +1,9 @@
-"""GPU parity of plans whose weights are stored as bfloat16 (fp32 arithmetic,
-features and gradients): standalone and fused-conv forward and backward, the
-staged and the direct kernels, per-edge and shared weights, and the radial
-network writing bfloat16 weights.  The oracle receives the same bfloat16
-values widened to fp64, so the comparison keeps the fp32 tolerance."""
+"""GPU parity of plans whose weights are stored in a 16-bit format, bfloat16
+or IEEE binary16 (fp32 arithmetic, features and gradients): standalone and
+fused-conv forward and backward, the staged and the direct kernels, per-edge
+and shared weights, and the radial network writing 16-bit weights.  The oracle
+receives the same 16-bit values widened to fp64, so the comparison keeps the
+fp32 tolerance."""
 import numpy as np
 import pytest
 
@@ -13,9 +14,12 @@ from tests.gpu_util import assert_close, dev, host, need_gpu, torch
 pytestmark = pytest.mark.gpu
 
 
-def _bf16(a):
-    """bfloat16 device tensor and the exact fp64 values it holds."""
-    t = torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(torch.bfloat16).cuda()
+WDT = ["bfloat16", "float16"]
+
+
+def _w16(a, wdt):
+    """16-bit device tensor and the exact fp64 values it holds."""
+    t = torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(getattr(torch, wdt)).cuda()
     return t, t.float().cpu().numpy().astype(np.float64)
 
 
@@ -29,15 +33,16 @@ CASES = [
 
 @pytest.mark.parametrize("irreps", CASES, ids=lambda c: c[0][:10])
 @pytest.mark.parametrize("B", [1, 333])
-def test_standalone_bf16_weights(irreps, B):
+@pytest.mark.parametrize("wdt", WDT)
+def test_standalone_16bit_weights(irreps, B, wdt):
     need_gpu()
     import clebsch_gordan_tensor_gb300 as cg
     prob = O.make_problem(*irreps)
-    plan = cg.Plan(*irreps, weight_dtype=torch.bfloat16)
+    plan = cg.Plan(*irreps, weight_dtype=getattr(torch, wdt))
     rng = np.random.default_rng(B)
     x = rng.standard_normal((B, prob.dim1)).astype(np.float32)
     y = rng.standard_normal((B, prob.dim2)).astype(np.float32)
-    wd, wr = _bf16(rng.standard_normal((B, prob.wdim)))
+    wd, wr = _w16(rng.standard_normal((B, prob.wdim)), wdt)
     g = rng.standard_normal((B, prob.dimo)).astype(np.float32)
     out = plan.forward(dev(x), dev(y), wd)
     assert_close(host(out), O.tp_forward(prob, x, y, wr), np.float32, "forward")
@@ -58,19 +63,20 @@ def _cloud(n):
 
 
 @pytest.mark.parametrize("misaligned", [False, True], ids=["staged", "direct"])
-def test_conv_bf16_weights(misaligned):
+@pytest.mark.parametrize("wdt", WDT)
+def test_conv_16bit_weights(misaligned, wdt):
     need_gpu()
     import clebsch_gordan_tensor_gb300 as cg
     gr, rng = _cloud(600)
     irreps = W.CFG2
     prob = O.make_problem(*irreps)
-    plan = cg.Plan(*irreps, weight_dtype=torch.bfloat16)
+    plan = cg.Plan(*irreps, weight_dtype=getattr(torch, wdt))
     G = cg.Graph.from_numpy(gr)
     x = rng.standard_normal((gr.N, prob.dim1)).astype(np.float32)
     y = rng.standard_normal((gr.E, prob.dim2)).astype(np.float32)
-    wd, wr = _bf16(rng.standard_normal((gr.E, prob.wdim)))
+    wd, wr = _w16(rng.standard_normal((gr.E, prob.wdim)), wdt)
     if misaligned:  # a 4-byte offset view: not 16-byte aligned, so the direct kernels run
-        buf = torch.empty(gr.E * prob.wdim + 2, dtype=torch.bfloat16, device="cuda")
+        buf = torch.empty(gr.E * prob.wdim + 2, dtype=getattr(torch, wdt), device="cuda")
         view = buf[2:].view(gr.E, prob.wdim)
         view.copy_(wd)
         wd = view
@@ -86,17 +92,18 @@ def test_conv_bf16_weights(misaligned):
     assert plan.device_status() == 0
 
 
-def test_shared_bf16_weights():
+@pytest.mark.parametrize("wdt", WDT)
+def test_shared_16bit_weights(wdt):
     need_gpu()
     import clebsch_gordan_tensor_gb300 as cg
     irreps = ("8x0e+8x1o", "0e+1o+2e", "8x0e+8x1o+8x2e")
     prob = O.make_problem(*irreps)
-    plan = cg.Plan(*irreps, shared_weights=True, weight_dtype=torch.bfloat16)
+    plan = cg.Plan(*irreps, shared_weights=True, weight_dtype=getattr(torch, wdt))
     rng = np.random.default_rng(4)
     B = 700
     x = rng.standard_normal((B, prob.dim1)).astype(np.float32)
     y = rng.standard_normal((B, prob.dim2)).astype(np.float32)
-    wd, wr = _bf16(rng.standard_normal(prob.wdim))
+    wd, wr = _w16(rng.standard_normal(prob.wdim), wdt)
     g = rng.standard_normal((B, prob.dimo)).astype(np.float32)
     out = plan.forward(dev(x), dev(y), wd)
     assert_close(host(out), O.tp_forward(prob, x, y, wr), np.float32, "shared forward")
@@ -105,12 +112,13 @@ def test_shared_bf16_weights():
 
 
 @pytest.mark.parametrize("cuda_cores", [False, True])
-def test_radial_writes_bf16(cuda_cores):
-    """bfloat16 output: each element is the fp32 result rounded to nearest (8
-    significant bits), so it lies within half a bfloat16 unit (at most 2^-8
-    relative) of the fp32 result, which is itself within the fp32 normwise
-    tolerance (1e-5 of the largest value) of the oracle; and it is exactly
-    torch's rounding of the fp32 path's output."""
+@pytest.mark.parametrize("wdt", WDT)
+def test_radial_writes_16bit(cuda_cores, wdt):
+    """16-bit output: each element is the fp32 result rounded to nearest (p = 8
+    significant bits for bfloat16, 11 for binary16), so it lies within half a
+    unit (at most 2^-p relative) of the fp32 result, which is itself within the
+    fp32 normwise tolerance (1e-5 of the largest value) of the oracle; and it is
+    exactly torch's rounding of the fp32 path's output."""
     need_gpu()
     import clebsch_gordan_tensor_gb300 as cg
     rng = np.random.default_rng(8)
@@ -119,18 +127,19 @@ def test_radial_writes_bf16(cuda_cores):
     vec = (d / np.linalg.norm(d, axis=1, keepdims=True) * rng.uniform(0.5, 5, (E, 1))).astype(np.float32)
     W1 = (rng.standard_normal((nb, hidden)) / np.sqrt(nb)).astype(np.float32)
     W2 = (rng.standard_normal((hidden, n_out)) / 8).astype(np.float32)
-    w = cg.radial_forward(dev(vec), dev(W1), dev(W2), out_dtype=torch.bfloat16,
-                          cuda_cores=cuda_cores)
-    assert w.dtype == torch.bfloat16
+    odt = getattr(torch, wdt)
+    p = 8 if wdt == "bfloat16" else 11
+    w = cg.radial_forward(dev(vec), dev(W1), dev(W2), out_dtype=odt, cuda_cores=cuda_cores)
+    assert w.dtype == odt
     rw, _ = O.radial_forward(vec, W1, W2)
     got = w.float().cpu().numpy().astype(np.float64)
     err = np.abs(got - rw)
-    assert np.all(err <= 2.0 ** -8 * np.abs(rw) * (1 + 1e-3) + 1e-5 * np.abs(rw).max())
+    assert np.all(err <= 2.0 ** -p * np.abs(rw) * (1 + 1e-3) + 1e-5 * np.abs(rw).max())
     # rounding is to nearest: the typical error is a quarter of a unit or less
-    assert np.median(err / np.maximum(np.abs(rw), 1e-30)) < 2.0 ** -9
+    assert np.median(err / np.maximum(np.abs(rw), 1e-30)) < 2.0 ** -(p + 1)
     wf = cg.radial_forward(dev(vec), dev(W1), dev(W2), cuda_cores=cuda_cores)
-    assert torch.equal(w, wf.to(torch.bfloat16))
+    assert torch.equal(w, wf.to(odt))
     assert cg.radial_device_status() == 0
-    # and it feeds a bfloat16-weight plan directly
-    plan = cg.Plan(*W.CFG2, weight_dtype=torch.bfloat16)
+    # and it feeds a plan with the same weight storage directly
+    plan = cg.Plan(*W.CFG2, weight_dtype=odt)
     assert w.shape[1] == plan.weight_numel

@@ -119,6 +119,15 @@ def test_c_abi_argument_errors():
     assert L.cgtp_forward(h, 5, a8, a8, a2, a8, null) == 1
     assert b"weight pointer" in L.cgtp_last_error_message()
     assert L.cgtp_plan_destroy(h) == 0
+    # binary16 weights: the same rules; one 16-bit format at a time
+    assert L.cgtp_plan_create(ctypes.byref(h), b"64x0e", b"0e", b"64x0e", None, 0, 1, 0,
+                              1 << 25) == 4
+    assert L.cgtp_plan_create(ctypes.byref(h), b"64x0e", b"0e", b"64x0e", None, 0, 0, 0,
+                              (1 << 24) | (1 << 25)) == 1
+    assert L.cgtp_plan_create(ctypes.byref(h), b"64x0e", b"0e", b"64x0e", None, 0, 0, 0,
+                              1 << 25) == 0
+    assert L.cgtp_forward(h, 5, a8, a8, a2, a8, null) == 1
+    assert L.cgtp_plan_destroy(h) == 0
     s = cg.Plan("2x0e", "0e", "2x0e", shared_weights=True)
     gx = ctypes.c_void_p(0x1000)
     # shared-weight gradient: needs the workspace variant, and enough scratch
@@ -158,9 +167,30 @@ def test_radial_argument_errors_and_path():
     assert L.cgtp_radial_workspace(0, 8, 64, 1536, ctypes.byref(n)) == 0 and n.value == 1536 * 64 * 8
     assert L.cgtp_radial_workspace(1, 8, 64, 1536, ctypes.byref(n)) == 0 and n.value == 0
     assert L.cgtp_radial_workspace(0, 8, 12, 1536, ctypes.byref(n)) == 0 and n.value == 0
+    # 16-bit outputs: fp32 inputs only, one format at a time (checked before any launch)
+    fake = ctypes.c_void_p(0x1000)
+    assert L.cgtp_radial_forward(1, 4, 8, ctypes.c_double(5.0), 64, 1536, fake, fake, fake, fake,
+                                 None, None, ctypes.c_size_t(0), 4, None) == 4
+    assert L.cgtp_radial_forward(0, 4, 8, ctypes.c_double(5.0), 64, 1536, fake, fake, fake, fake,
+                                 None, None, ctypes.c_size_t(0), 2 | 4, None) == 1
     v = ctypes.c_int()
     assert L.cgtp_radial_path(0, 8, 64, 1536, None) == 1
     assert L.cgtp_radial_path(0, 40, 64, 1536, ctypes.byref(v)) == 1
+
+
+@pytest.mark.parametrize("wdtype", ["bfloat16", "float16"])
+def test_16bit_weight_kernels_compile_for_sm103a(wdtype):
+    """The generated kernels with 16-bit weight storage (widened to fp32 on
+    load) compile for sm_103a, the forward kernels without spills."""
+    import torch
+    plan = cg.Plan(*W.CFG2, weight_dtype=getattr(torch, wdtype))
+    log = plan.compile()
+    assert "sm_103a" in log
+    assert "#define W_STORE " + ("1" if wdtype == "bfloat16" else "2") in plan.source()
+    spills = {k: int(v) for k, v in
+              re.findall(r"Function properties for (cgtp_\w+)\n.*?(\d+) bytes spill stores", log)}
+    for k in ("cgtp_fwd_conv", "cgtp_fwd_single", "cgtp_fwd_conv_tma", "cgtp_fwd_single_tma"):
+        assert spills.get(k, 0) == 0, log
 
 
 @pytest.mark.parametrize("irreps,dtype", [(W.CFG0, "f32"), (W.CFG2, "f32"), (W.CFG4, "f32"),
