@@ -4,7 +4,7 @@ Default workload (the headline): the MACE-like fused convolution -- N = 10,000
 atoms in a periodic box (density 0.1 / A^3, cutoff 5 A, ~525k directed edges),
 node features 64x(0e,1o,2e), edge spherical harmonics l <= 3, 24 'uvu' paths
 to 64x(0e,1o,1e,2o,2e,3o,3e), per-edge weights from a random radial MLP, fp32
-(seeded synthetic inputs from ``workloads.config2``).
+(seeded synthetic inputs from ``workloads.conv64_cloud10k``).
 
 One step = the whole hot path on one batch: spherical harmonics of the edge
 vectors -> fused conv forward -> conv backward (dL/dx, dL/dY, dL/dW for a fixed
@@ -186,7 +186,7 @@ class Workload:
 
 
 def make_conv(args, cg, W, torch):
-    cfg = W.config2(N=args.atoms)
+    cfg = W.conv64_cloud10k(N=args.atoms)
     gr = cfg["graph"]
     N, E = gr.N, gr.E
     plan = cg.Plan(*cfg["irreps"])
@@ -288,7 +288,7 @@ def make_conv(args, cg, W, torch):
 
 
 def make_conv64(args, cg, W, torch):
-    cfg = W.config3()
+    cfg = W.conv128_f64_cloud5k()
     gr = cfg["graph"]
     N, E = gr.N, gr.E
     plan = cg.Plan(*cfg["irreps"], dtype=torch.float64)
@@ -311,7 +311,7 @@ def make_conv64(args, cg, W, torch):
 
 
 def make_tp(args, cg, W, torch):
-    cfg = W.config1(args.samples)
+    cfg = W.mace128_b200k(args.samples)
     B = cfg["B"]
     plan = cg.Plan(*cfg["irreps"])
     x, vec, w = (torch.from_numpy(cfg[k]).cuda() for k in ("x", "vec", "w"))
@@ -345,7 +345,7 @@ def make_tp(args, cg, W, torch):
 
 
 def make_tfn(args, cg, W, torch):
-    cfg = W.config4()
+    cfg = W.tfn32_mol1000()
     gr = cfg["graph"]
     N, E = gr.N, gr.E
     plan = cg.Plan(*cfg["irreps"])
@@ -389,7 +389,7 @@ def make_tfn(args, cg, W, torch):
 def make_kv(args, cg, W, torch):
     """SE(3)-Transformer keys and values from one TFN with doubled channels:
     the molecule graph of the TFN workload at 64 channels per irrep."""
-    cfg = W.config4_kv()
+    cfg = W.tfn_kv64_mol1000()
     gr = cfg["graph"]
     N, E = gr.N, gr.E
     plan = cg.Plan(*cfg["irreps"])
@@ -417,9 +417,9 @@ def make_uvw(args, cg, W, torch):
     """'uvw' product on the 200,000-sample, 128-channel inputs of ``tp``:
     per-path 'uvu' blocks (unit shared weights), then the channel mixing on the
     tensor cores."""
-    cfg = W.config1_uvw(args.samples)
+    cfg = W.mace128_uvw_b200k(args.samples)
     B = cfg["B"]
-    uvw = cg.UVWProduct(*W.CFG1)
+    uvw = cg.UVWProduct(*W.IRREPS_MACE128)
     x, vec, Wm = (torch.from_numpy(cfg[k]).cuda() for k in ("x", "vec", "W"))
     y = torch.empty(B, uvw.dim_in2, device="cuda")
     mid = torch.empty(B, uvw.dim_mid, device="cuda")
@@ -739,7 +739,7 @@ def run_reference(args):
         return None
     import oracle as O
     import workloads as W
-    cfg = W.config2()
+    cfg = W.conv64_cloud10k()
     _oracle_problem(cfg)
     _oracle_weights(cfg)
     R = 24

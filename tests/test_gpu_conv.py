@@ -34,13 +34,13 @@ def _graph(rng, N, max_deg=9, isolated=(3,), silent=(5,)):
 
 
 CASES = [
-    (W.CFG2[0].replace("64x", "8x"), W.CFG2[1], W.CFG2[2].replace("64x", "8x"), np.float32),
-    W.CFG2 + (np.float32,),
-    W.CFG4 + (np.float32,),
-    (W.CFG1[0], W.CFG1[1], W.CFG1[2], np.float32),
+    (W.IRREPS_CONV64[0].replace("64x", "8x"), W.IRREPS_CONV64[1], W.IRREPS_CONV64[2].replace("64x", "8x"), np.float32),
+    W.IRREPS_CONV64 + (np.float32,),
+    W.IRREPS_TFN32 + (np.float32,),
+    (W.IRREPS_MACE128[0], W.IRREPS_MACE128[1], W.IRREPS_MACE128[2], np.float32),
     ("3x0e+3x1o", "0e+1o+2e", "3x0e+3x1o+3x2e", np.float32),
-    (W.CFG3[0].replace("128x", "16x"), W.CFG3[1], W.CFG3[2].replace("128x", "16x"), np.float64),
-    W.CFG3 + (np.float64,),
+    (W.IRREPS_CONV128[0].replace("128x", "16x"), W.IRREPS_CONV128[1], W.IRREPS_CONV128[2].replace("128x", "16x"), np.float64),
+    W.IRREPS_CONV128 + (np.float64,),
 ]
 
 
@@ -101,7 +101,7 @@ def test_conv_double_backward(case, which):
 def test_edgeless_graph_writes_zeros():
     need_gpu()
     cg = _cg()
-    plan = cg.Plan(*W.CFG2)
+    plan = cg.Plan(*W.IRREPS_CONV64)
     gr = W.make_graph(6, np.zeros(0, np.int64), np.zeros(0, np.int64), np.zeros((0, 3)))
     G = cg.Graph.from_numpy(gr)
     x = torch.randn(6, plan.dim_in1, device="cuda")
@@ -151,7 +151,7 @@ def test_edge_forces_and_adjoint(dt):
 
 
 def tfn_chain_gpu(cg, plan, G, x, vec, w, c, gF, lmax=3):
-    """Config-4 step: energy E = sum c * conv(x, Y(vec), w); gradients dE/dx,
+    """TFN-layer step (1000 molecules): energy E = sum c * conv(x, Y(vec), w); gradients dE/dx,
     dE/dw, dE/dvec; forces; force loss L = sum gF * F; dL/dx, dL/dw, and
     FL = edge_forces(dL/dr) = -dL/dpos."""
     y = cg.sh_forward(vec, lmax)
@@ -187,10 +187,10 @@ def tfn_chain_oracle(prob, gr, x, vec, w, c, gF, lmax=3, nodes=None, edges=None)
 def test_tfn_force_chain_small():
     need_gpu()
     cg = _cg()
-    cfg = W.config4(n_mol=40)
+    cfg = W.tfn32_mol1000(n_mol=40)
     gr = cfg["graph"]
-    prob = O.make_problem(*W.CFG4)
-    plan = cg.Plan(*W.CFG4)
+    prob = O.make_problem(*W.IRREPS_TFN32)
+    plan = cg.Plan(*W.IRREPS_TFN32)
     G = cg.Graph.from_numpy(gr)
     gpu = tfn_chain_gpu(cg, plan, G, dev(cfg["x"]), dev(cfg["vec"]), dev(cfg["w"]),
                         dev(cfg["c"]), dev(cfg["gF"]))

@@ -3,12 +3,13 @@ benchmark times.  The GPU computes every output; the oracle computes sampled
 rows (receivers, senders, edges or samples) one by one.
 
 Workloads (seeded recipes in ``workloads``):
-  0  standalone TP, B = 1000, fp32                       (compared in full)
-  1  standalone TP, B = 200,000, 128 channels, fp32      (sampled rows)
-  2  fused conv, N = 10,000 atoms, ~525k edges, fp32     (sampled rows)
-  3  fused conv, N = 5,000 atoms, 128 channels, fp64     (forward, sampled)
-  4  TFN layer on 1000 molecules, fwd + bwd + double backward and forces, fp32
-  and the 'uvw' channel mixing of workload 1 (200,000 samples, fp32)
+  tp16_b1000           standalone TP, B = 1000, fp32               (compared in full)
+  mace128_b200k        standalone TP, B = 200,000, 128 channels    (sampled rows)
+  conv64_cloud10k      fused conv, N = 10,000 atoms, ~525k edges   (sampled rows)
+  conv128_f64_cloud5k  fused conv, N = 5,000 atoms, 128 ch., fp64  (forward, sampled)
+  tfn32_mol1000        TFN layer on 1000 molecules, fwd + bwd + double backward
+                       and forces, fp32; with 64 channels for fused keys/values
+  mace128_uvw_b200k    the 'uvw' channel mixing on the 200,000 samples
 """
 import numpy as np
 import pytest
@@ -30,10 +31,10 @@ def _sample(rng, n, k):
     return np.unique(np.concatenate([idx, [0, n - 1]]))
 
 
-def test_config0_full():
+def test_tp16_full():
     need_gpu()
     cg = _cg()
-    cfg = W.config0()
+    cfg = W.tp16_b1000()
     prob = O.make_problem(*cfg["irreps"])
     plan = cg.Plan(*cfg["irreps"])
     x, v, w = cfg["x"], cfg["vec"], cfg["w"]
@@ -49,10 +50,10 @@ def test_config0_full():
         assert_close(host(a), b, np.float32, n)
 
 
-def test_config1_sampled():
+def test_mace128_b200k_sampled():
     need_gpu()
     cg = _cg()
-    cfg = W.config1()
+    cfg = W.mace128_b200k()
     prob = O.make_problem(*cfg["irreps"])
     plan = cg.Plan(*cfg["irreps"])
     B = cfg["B"]
@@ -102,25 +103,25 @@ def _conv_sampled(cfg, dt, do_bwd: bool):
     assert_close(host(gw)[edges], rw[edges], dt, "gw rows")
 
 
-def test_config2_sampled():
+def test_conv64_cloud10k_sampled():
     need_gpu()
-    _conv_sampled(W.config2(), np.float32, True)
+    _conv_sampled(W.conv64_cloud10k(), np.float32, True)
 
 
-def test_config3_sampled_fp64():
+def test_conv128_cloud5k_sampled_fp64():
     need_gpu()
-    _conv_sampled(W.config3(), np.float64, False)
+    _conv_sampled(W.conv128_f64_cloud5k(), np.float64, False)
 
 
-def test_config4_chain_sampled():
+def test_tfn32_chain_sampled():
     need_gpu()
     cg = _cg()
     from tests.test_gpu_conv import tfn_chain_gpu
 
-    cfg = W.config4()
+    cfg = W.tfn32_mol1000()
     gr = cfg["graph"]
-    prob = O.make_problem(*W.CFG4)
-    plan = cg.Plan(*W.CFG4)
+    prob = O.make_problem(*W.IRREPS_TFN32)
+    plan = cg.Plan(*W.IRREPS_TFN32)
     G = cg.Graph.from_numpy(gr)
     res = tfn_chain_gpu(cg, plan, G, dev(cfg["x"]), dev(cfg["vec"]), dev(cfg["w"]),
                         dev(cfg["c"]), dev(cfg["gF"]))
@@ -160,11 +161,11 @@ def test_config4_chain_sampled():
     assert_close(res["FL"][nodes], FL[nodes], np.float32, "-dL/dpos rows")
 
 
-def test_config4_fused_kv_sampled():
+def test_tfn_kv64_fused_sampled():
     """Keys and values from one TFN (the 1000-molecule graph at 64 channels): forward
     and gradient at full size, sampled receivers / senders / edges."""
     need_gpu()
-    cfg = W.config4_kv()
+    cfg = W.tfn_kv64_mol1000()
     conv_weights(cfg)  # the workload carries its own w
     _conv_sampled(cfg, np.float32, True)
 
@@ -181,11 +182,11 @@ def test_uvw_mixing_full_size():
     need_gpu()
     cg = _cg()
     B, P = 200_000, 1000
-    uvw = cg.UVWProduct(*W.CFG1)
+    uvw = cg.UVWProduct(*W.IRREPS_MACE128)
     lin = uvw.linear
     assert lin.tensor_cores
     instr = [lin.instruction(j)[:2] for j in range(lin.n_instr)]
-    Wm = W.config1_uvw(P)["W"]
+    Wm = W.mace128_uvw_b200k(P)["W"]
     rng = np.random.default_rng(23)
     X0 = rng.standard_normal((P, uvw.dim_mid)).astype(np.float32)
     G0 = rng.standard_normal((P, uvw.dim_out)).astype(np.float32)
@@ -196,8 +197,8 @@ def test_uvw_mixing_full_size():
     out = lin.forward(x, dev(Wm))
     gx, _ = lin.backward(x, dev(Wm), g, need=(True, False))
     _, gW = lin.backward(x, dev(Wm), g, need=(False, True))
-    rout = O.linear_forward(uvw.mid, W.CFG1[2], instr, X0, Wm)
-    rx, rW = O.linear_backward(uvw.mid, W.CFG1[2], instr, X0, Wm, G0)
+    rout = O.linear_forward(uvw.mid, W.IRREPS_MACE128[2], instr, X0, Wm)
+    rx, rW = O.linear_backward(uvw.mid, W.IRREPS_MACE128[2], instr, X0, Wm, G0)
     idx = _sample(rng, B, 3000)
     ti = torch.from_numpy(idx).cuda()
     assert_close(host(out[ti]), rout[idx % P], np.float32, "out rows")

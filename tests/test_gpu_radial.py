@@ -86,7 +86,7 @@ def test_radial_benchmark_workload_sampled():
     the GPU computes every row, the oracle sampled rows."""
     need_gpu()
     import clebsch_gordan_tensor_gb300 as cg
-    cfg = W.config2()
+    cfg = W.conv64_cloud10k()
     E = cfg["graph"].E
     w = cg.radial_forward(dev(cfg["vec"]), dev(cfg["W1"]), dev(cfg["W2"]), cfg["cutoff"])
     assert cg.radial_uses_tensor_cores(torch.float32, 8, 64, 1536)
@@ -150,7 +150,7 @@ def test_radial_backward_benchmark_workload():
     over all edges (fp64 matmuls) and grad_vec on sampled edges."""
     need_gpu()
     import clebsch_gordan_tensor_gb300 as cg
-    cfg = W.config2()
+    cfg = W.conv64_cloud10k()
     E = cfg["graph"].E
     g = np.random.default_rng(5).standard_normal((E, 1536)).astype(np.float32)
     gv, g1, g2 = cg.radial_backward(dev(cfg["vec"]), dev(cfg["W1"]), dev(cfg["W2"]), dev(g),

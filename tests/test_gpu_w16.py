@@ -24,10 +24,10 @@ def _w16(a, wdt):
 
 
 CASES = [
-    W.CFG2,                                                   # mul 64: two channels per lane, staged
+    W.IRREPS_CONV64,                                                   # mul 64: two channels per lane, staged
     ("3x0e+3x1o", "0e+1o+2e", "3x0e+3x1o+3x2e"),              # masked lanes, direct
     ("5x0e+5x1o", "0e+1o+2e", "5x0e+5x1o+5x2e"),              # odd mul: one channel per lane
-    (W.CFG1[0], W.CFG1[1], W.CFG1[2]),                        # mul 128: two warps per item
+    (W.IRREPS_MACE128[0], W.IRREPS_MACE128[1], W.IRREPS_MACE128[2]),                        # mul 128: two warps per item
 ]
 
 
@@ -68,7 +68,7 @@ def test_conv_16bit_weights(misaligned, wdt):
     need_gpu()
     import clebsch_gordan_tensor_gb300 as cg
     gr, rng = _cloud(600)
-    irreps = W.CFG2
+    irreps = W.IRREPS_CONV64
     prob = O.make_problem(*irreps)
     plan = cg.Plan(*irreps, weight_dtype=getattr(torch, wdt))
     G = cg.Graph.from_numpy(gr)
@@ -141,5 +141,5 @@ def test_radial_writes_16bit(cuda_cores, wdt):
     assert torch.equal(w, wf.to(odt))
     assert cg.radial_device_status() == 0
     # and it feeds a plan with the same weight storage directly
-    plan = cg.Plan(*W.CFG2, weight_dtype=odt)
+    plan = cg.Plan(*W.IRREPS_CONV64, weight_dtype=odt)
     assert w.shape[1] == plan.weight_numel

@@ -18,7 +18,7 @@ import clebsch_gordan_tensor_gb300 as cg
 import torch
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-ALL_CFGS = [W.CFG0, W.CFG1, W.CFG2, W.CFG3, W.CFG4]
+ALL_CFGS = [W.IRREPS_TP16, W.IRREPS_MACE128, W.IRREPS_CONV64, W.IRREPS_CONV128, W.IRREPS_TFN32]
 
 
 def _declared():
@@ -183,7 +183,7 @@ def test_16bit_weight_kernels_compile_for_sm103a(wdtype):
     """The generated kernels with 16-bit weight storage (widened to fp32 on
     load) compile for sm_103a, the forward kernels without spills."""
     import torch
-    plan = cg.Plan(*W.CFG2, weight_dtype=getattr(torch, wdtype))
+    plan = cg.Plan(*W.IRREPS_CONV64, weight_dtype=getattr(torch, wdtype))
     log = plan.compile()
     assert "sm_103a" in log
     assert "#define W_STORE " + ("1" if wdtype == "bfloat16" else "2") in plan.source()
@@ -193,8 +193,8 @@ def test_16bit_weight_kernels_compile_for_sm103a(wdtype):
         assert spills.get(k, 0) == 0, log
 
 
-@pytest.mark.parametrize("irreps,dtype", [(W.CFG0, "f32"), (W.CFG2, "f32"), (W.CFG4, "f32"),
-                                          (W.CFG1, "f32"), (W.CFG3, "f64")])
+@pytest.mark.parametrize("irreps,dtype", [(W.IRREPS_TP16, "f32"), (W.IRREPS_CONV64, "f32"), (W.IRREPS_TFN32, "f32"),
+                                          (W.IRREPS_MACE128, "f32"), (W.IRREPS_CONV128, "f64")])
 def test_generated_kernels_compile_for_sm103a(irreps, dtype):
     import torch
     plan = cg.Plan(*irreps, dtype=torch.float64 if dtype == "f64" else torch.float32)
@@ -207,7 +207,7 @@ def test_generated_kernels_compile_for_sm103a(irreps, dtype):
     assert direct <= set(spills)
     staged = set(spills) - direct
     assert staged in (set(), {k + "_tma" for k in direct}), staged
-    if irreps is not W.CFG0:
+    if irreps is not W.IRREPS_TP16:
         assert staged, "the workload plans use the staged (TMA) kernels"
     for k in ("cgtp_fwd_conv", "cgtp_fwd_single", "cgtp_fwd_conv_tma", "cgtp_fwd_single_tma"):
         assert spills.get(k, 0) == 0, log

@@ -25,13 +25,13 @@ def _rand(rng, prob, B):
 
 
 def test_path_enumeration():
-    p = O.make_problem(*W.CFG0)
+    p = O.make_problem(*W.IRREPS_TP16)
     got = [(l1, l2, l3) for (_, _, _, l1, l2, l3, *_r) in p.paths]
     assert got == [(0, 0, 0), (0, 1, 1), (0, 2, 2), (1, 0, 1), (1, 1, 0), (1, 1, 2), (1, 2, 1)]
     assert (p.dim1, p.dim2, p.dimo, p.wdim) == (64, 9, 144, 112)
-    p1 = O.make_problem(*W.CFG1)
+    p1 = O.make_problem(*W.IRREPS_MACE128)
     assert len(p1.paths) == 24 and (p1.dim1, p1.dimo, p1.wdim) == (1152, 3968, 3072)
-    assert len(O.make_problem(*W.CFG4).paths) == 23
+    assert len(O.make_problem(*W.IRREPS_TFN32).paths) == 23
     with pytest.raises(ValueError):
         O.parse_irreps("3x1q")
 

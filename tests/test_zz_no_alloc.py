@@ -43,7 +43,7 @@ def test_noalloc_conv_backward_matches_workspace_entry_point(shared):
     rng = np.random.default_rng(5)
     _, _, gr = W.periodic_cloud(rng, 800)
     G = cg.Graph.from_numpy(gr)
-    plan = cg.Plan(*W.CFG2, shared_weights=shared)
+    plan = cg.Plan(*W.IRREPS_CONV64, shared_weights=shared)
     x = dev(rng.standard_normal((gr.N, plan.dim_in1)).astype(np.float32))
     y = dev(rng.standard_normal((gr.E, plan.dim_in2)).astype(np.float32))
     wshape = (plan.weight_numel,) if shared else (gr.E, plan.weight_numel)

@@ -26,15 +26,15 @@ from dataclasses import dataclass
 import numpy as np
 
 # Irreps (in1, in2, out) of the five workloads.
-CFG0 = ("16x0e+16x1o", "0e+1o+2e", "16x0e+16x1o+16x2e")
-CFG1 = ("128x0e+128x1o+128x2e", "0e+1o+2e+3o",
+IRREPS_TP16 = ("16x0e+16x1o", "0e+1o+2e", "16x0e+16x1o+16x2e")
+IRREPS_MACE128 = ("128x0e+128x1o+128x2e", "0e+1o+2e+3o",
         "128x0e+128x1o+128x1e+128x2o+128x2e+128x3o+128x3e")
-CFG2 = ("64x0e+64x1o+64x2e", "0e+1o+2e+3o", "64x0e+64x1o+64x1e+64x2o+64x2e+64x3o+64x3e")
-CFG3 = ("128x0e+128x1o+128x2e", "0e+1o+2e+3o",
+IRREPS_CONV64 = ("64x0e+64x1o+64x2e", "0e+1o+2e+3o", "64x0e+64x1o+64x1e+64x2o+64x2e+64x3o+64x3e")
+IRREPS_CONV128 = ("128x0e+128x1o+128x2e", "0e+1o+2e+3o",
         "128x0e+128x1o+128x1e+128x2o+128x2e+128x3o+128x3e")
-CFG4 = ("32x0e+32x1o+32x2e+32x3o", "0e+1o+2e+3o", "32x0e+32x1o+32x2e+32x3o")
+IRREPS_TFN32 = ("32x0e+32x1o+32x2e+32x3o", "0e+1o+2e+3o", "32x0e+32x1o+32x2e+32x3o")
 # the small-molecule TFN layer with keys and values from one TFN: channels doubled
-CFG4_KV = ("64x0e+64x1o+64x2e+64x3o", "0e+1o+2e+3o", "64x0e+64x1o+64x2e+64x3o")
+IRREPS_TFN_KV64 = ("64x0e+64x1o+64x2e+64x3o", "0e+1o+2e+3o", "64x0e+64x1o+64x2e+64x3o")
 
 
 def irreps_dim(s: str) -> int:
@@ -149,7 +149,7 @@ def radial_params(rng, n_out: int, n_basis: int = 8, hidden: int = 64, dtype=np.
     return W1.astype(dtype), W2.astype(dtype)
 
 
-# ---------------------------------------------------------------- configs --
+# -------------------------------------------------------------- workloads --
 
 def standalone(seed: int, irreps, B: int, wdim: int, w_scale: float = 1.0,
                dtype=np.float32) -> dict:
@@ -170,24 +170,24 @@ def _lmax(irreps_in2: str) -> int:
     return max(int(t.split("x")[-1][:-1]) for t in irreps_in2.split("+"))
 
 
-def config0(B: int = 1000) -> dict:
+def tp16_b1000(B: int = 1000) -> dict:
     """Standalone TP, fp32, B = 1000, 16x0e+16x1o (x) SH(l<=2) -> 16x(0e,1o,2e),
     7 paths, per-sample weights N(0,1), seed 0."""
-    return standalone(0, CFG0, B, wdim=7 * 16, dtype=np.float32)
+    return standalone(0, IRREPS_TP16, B, wdim=7 * 16, dtype=np.float32)
 
 
-def config1(B: int = 200_000) -> dict:
+def mace128_b200k(B: int = 200_000) -> dict:
     """MACE-like standalone TP, fp32, B = 200,000, 128x(0e,1o,2e) (x) SH(l<=3)
     -> 128x(0e,1o,1e,2o,2e,3o,3e), 24 paths, weights N(0,1)/sqrt(24), seed 1."""
-    return standalone(1, CFG1, B, wdim=24 * 128, w_scale=1.0 / np.sqrt(24.0), dtype=np.float32)
+    return standalone(1, IRREPS_MACE128, B, wdim=24 * 128, w_scale=1.0 / np.sqrt(24.0), dtype=np.float32)
 
 
-def config1_uvw(B: int = 200_000) -> dict:
+def mace128_uvw_b200k(B: int = 200_000) -> dict:
     """The 200,000-sample, 128-channel standalone inputs (x, v from seed 1, as
-    ``config1`` draws them) under a 'uvw' product: one [128, 128] matrix per
+    ``mace128_b200k`` draws them) under a 'uvw' product: one [128, 128] matrix per
     path shared by all samples, W ~ N(0,1)/sqrt(128) from seed 101 (24 paths,
     path-major, row-major)."""
-    cfg = config1(B)
+    cfg = mace128_b200k(B)
     cfg.pop("w")
     rng = np.random.default_rng(101)
     cfg["W"] = normal(rng, (24 * 128 * 128,), np.float32) * np.float32(1.0 / np.sqrt(128.0))
@@ -211,7 +211,7 @@ def conv_cloud(seed: int, irreps, N: int, n_paths: int, dtype) -> dict:
                 dtype=np.dtype(dtype))
 
 
-def config4_kv(n_mol: int = 1000) -> dict:
+def tfn_kv64_mol1000(n_mol: int = 1000) -> dict:
     """The TFN workload's 1000 molecules (same seed, same graph) with 64 channels per
     irrep: the keys and values of an SE(3)-Transformer attention layer from one
     TFN with doubled channels instead of two.  Draws, in order: molecules; x
@@ -222,22 +222,22 @@ def config4_kv(n_mol: int = 1000) -> dict:
     x = normal(rng, (g.N, 1024), np.float32)
     w = normal(rng, (g.E, 23 * 64), np.float32) * np.float32(1.0 / np.sqrt(23.0))
     go = normal(rng, (g.N, 1024), np.float32)
-    return dict(irreps=CFG4_KV, graph=g, pos=pos, x=x, vec=g.vec.astype(np.float32), w=w, g=go,
+    return dict(irreps=IRREPS_TFN_KV64, graph=g, pos=pos, x=x, vec=g.vec.astype(np.float32), w=w, g=go,
                 lmax=3, scale=1.0, dtype=np.dtype(np.float32))
 
 
-def config2(N: int = 10_000) -> dict:
+def conv64_cloud10k(N: int = 10_000) -> dict:
     """Fused conv, fp32, N = 10,000 atoms, 64x(0e,1o,2e) (x) SH(l<=3) -> 64 x 7
     irreps, 24 paths, radial-MLP weights, seed 2."""
-    return conv_cloud(2, CFG2, N, 24, np.float32)
+    return conv_cloud(2, IRREPS_CONV64, N, 24, np.float32)
 
 
-def config3(N: int = 5_000) -> dict:
+def conv128_f64_cloud5k(N: int = 5_000) -> dict:
     """Fused conv, fp64, N = 5,000 atoms, 128 channels, seed 3, forward only."""
-    return conv_cloud(3, CFG3, N, 24, np.float64)
+    return conv_cloud(3, IRREPS_CONV128, N, 24, np.float64)
 
 
-def config4(n_mol: int = 1000) -> dict:
+def tfn32_mol1000(n_mol: int = 1000) -> dict:
     """TFN-style layer on small molecules, fp32, seed 4.  Draws, in order:
     molecules (``molecules``); x [N, 512] ~ N(0,1); w [E, 736] ~ N(0,1)/sqrt(23);
     c [N, 512] ~ N(0,1) (energy E = sum c * out); gF [N, 3] ~ N(0,1) (force
@@ -248,5 +248,5 @@ def config4(n_mol: int = 1000) -> dict:
     w = normal(rng, (g.E, 23 * 32), np.float32) * np.float32(1.0 / np.sqrt(23.0))
     c = normal(rng, (g.N, 512), np.float32)
     gF = normal(rng, (g.N, 3), np.float32)
-    return dict(irreps=CFG4, graph=g, pos=pos, x=x, vec=g.vec.astype(np.float32), w=w, c=c,
+    return dict(irreps=IRREPS_TFN32, graph=g, pos=pos, x=x, vec=g.vec.astype(np.float32), w=w, c=c,
                 gF=gF, lmax=3, scale=1.0, dtype=np.dtype(np.float32))
