@@ -31,6 +31,8 @@ F32, F64 = 0, 1
 W_PER_EDGE, W_SHARED = 0, 1
 WEIGHTS_BF16 = 1 << 24  # plan flag: weights stored as bfloat16
 WEIGHTS_F16 = 1 << 25  # plan flag: weights stored as IEEE binary16
+TEST_WAIT_TIMEOUT = 1 << 26  # plan flag, tests only: the first bounded wait of each CTA gives up
+GY_WARP = 1 << 19  # plan flag: grad_y on a second warp per backward CTA
 
 
 class CgtpError(RuntimeError):
@@ -115,6 +117,23 @@ def lib() -> ctypes.CDLL:
                 "cgtp_linear_backward": [vp, i64, vp, vp, vp, vp, vp, vp, ctypes.c_size_t,
                                          ctypes.c_uint, vp],
                 "cgtp_linear_device_status": [P(i32)],
+                "cgtp_fma_probe": [i32, i32, i64, i32, i64, vp, P(i64), vp],
+                "cgtp_uvw_create": [P(vp), ctypes.c_char_p, ctypes.c_char_p, ctypes.c_char_p,
+                                    i32],
+                "cgtp_uvw_destroy": [vp],
+                "cgtp_uvw_info": [vp, P(i64), P(i64), P(i64), P(i64), P(i64), P(i32)],
+                "cgtp_uvw_path": [vp, i32, P(i32), P(i32), P(i32), P(i32), P(i32), P(i32),
+                                  P(i64)],
+                "cgtp_uvw_parts": [vp, P(vp), P(vp)],
+                "cgtp_uvw_workspace": [vp, i64, P(ctypes.c_size_t), P(ctypes.c_size_t)],
+                "cgtp_uvw_forward": [vp, i64, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp],
+                "cgtp_uvw_backward": [vp, i64, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                      ctypes.c_size_t, vp],
+                "cgtp_uvw_conv_forward": [vp, i64, i64, vp, vp, vp, vp, vp, ctypes.c_double, vp,
+                                          vp, vp, ctypes.c_size_t, vp],
+                "cgtp_uvw_conv_backward": [vp, i64, i64, vp, vp, vp, vp, vp, vp, vp, vp,
+                                           ctypes.c_double, vp, vp, vp, vp, vp, vp,
+                                           ctypes.c_size_t, vp],
             }
             for name, args in sig.items():
                 f = getattr(L, name)
@@ -140,6 +159,17 @@ def _check(st: int) -> None:
 def launch_count() -> int:
     """Kernel launches issued through the library by this process."""
     return int(lib().cgtp_launch_count())
+
+
+def fma_probe(dtype, packed: bool, blocks: int, threads: int, iters: int, sink) -> int:
+    """Launch the FMA-pipe throughput probe on the current stream (see
+    cgtp_fma_probe); returns the floating-point operations it performs.  sink:
+    a device tensor of at least blocks * threads 8-byte words."""
+    assert sink.numel() * sink.element_size() >= blocks * threads * 8
+    fl = ctypes.c_int64()
+    _check(lib().cgtp_fma_probe(_dt(dtype), int(packed), blocks, threads, iters, _ptr(sink),
+                                ctypes.byref(fl), _stream()))
+    return fl.value
 
 
 def _stream():
@@ -199,15 +229,17 @@ class Plan:
 
     def __init__(self, irreps_in1: str, irreps_in2: str, irreps_out: str,
                  dtype=torch.float32, shared_weights: bool = False, instructions=None,
-                 weight_dtype=None):
+                 weight_dtype=None, flags: int = 0):
         """weight_dtype=torch.bfloat16 or torch.float16 stores the weights in that
-        16-bit format (fp32 plans; arithmetic, features and grad_w stay fp32)."""
+        16-bit format (fp32 plans; arithmetic, features and grad_w stay fp32).
+        flags: further cgtp_plan_create flags (launch-shape overrides, tests)."""
         L = lib()
         self.dtype = dtype
         self.wdtype = dtype if weight_dtype is None else weight_dtype
         if self.wdtype not in (dtype, torch.bfloat16, torch.float16):
             raise CgtpError(f"weight_dtype {weight_dtype} is not supported")
-        flags = {torch.bfloat16: WEIGHTS_BF16, torch.float16: WEIGHTS_F16}.get(self.wdtype, 0)
+        flags = int(flags) | {torch.bfloat16: WEIGHTS_BF16,
+                              torch.float16: WEIGHTS_F16}.get(self.wdtype, 0)
         self.irreps = (irreps_in1, irreps_in2, irreps_out)
         h = ctypes.c_void_p()
         arr, n = None, 0
@@ -230,7 +262,7 @@ class Plan:
 
     def __del__(self):
         h = getattr(self, "_h", None)
-        if h is not None and _lib is not None:
+        if h is not None and _lib is not None and not getattr(self, "_borrowed", False):
             _lib.cgtp_plan_destroy(h)
             self._h = None
 
@@ -540,7 +572,7 @@ class Linear:
 
     def __del__(self):
         h = getattr(self, "_h", None)
-        if h is not None and _lib is not None:
+        if h is not None and _lib is not None and not getattr(self, "_borrowed", False):
             _lib.cgtp_linear_destroy(h)
 
     def instruction(self, j: int):
@@ -596,85 +628,146 @@ def linear_device_status() -> int:
     return c.value
 
 
-def _irreps(s: str):
-    out = []
-    for tok in s.replace(" ", "").split("+"):
-        mul, _, ir = tok.rpartition("x")
-        out.append((int(mul) if mul else 1, int(ir[:-1]), 1 if ir[-1] == "e" else -1))
-    return out
-
-
 class UVWProduct:
-    """'uvw' tensor product: one [mul_in, mul_out] matrix per path, shared by
-    all rows,
+    """'uvw' tensor product (``cgtp_uvw``): one [mul_in, mul_out] matrix per
+    path, shared by all rows,
         out[b, k, m3, w] = sum_paths->k sum_u sum_{m1,m2} C[m1,m2,m3]
                            x[b, i1, m1, u] y[b, i2, m2] W_p[u, w],
-    for every parity-allowed path (in1-major, then in2, then out).  Two library
-    calls: the 'uvu' product into one output irrep per path with a shared
-    weight row of ones (``Plan``), then the channel-mixing layer from those
-    irreps to irreps_out, instruction p joining path p's block to its target
-    irrep (``Linear``, tensor cores).  W holds the paths' matrices in order."""
+    for every parity-allowed path (in1-major, then in2, then out); W holds the
+    paths' matrices in order.  The library runs it as the 'uvu' product into
+    one block per path (``mid``) followed by the channel mixing on the tensor
+    cores; ``plan`` and ``linear`` are those two parts (borrowed)."""
 
     def __init__(self, irreps_in1: str, irreps_in2: str, irreps_out: str, dtype=torch.float32):
-        a, b, c = _irreps(irreps_in1), _irreps(irreps_in2), _irreps(irreps_out)
-        mul = a[0][0]
-        if any(m != mul for m, _, _ in a):
-            raise CgtpError("'uvw' needs one multiplicity for every irrep of in1")
-        blocks, tp_instr, lin_instr = [], [], []
-        for i1, (_, l1, p1) in enumerate(a):
-            for i2, (m2, l2, p2) in enumerate(b):
-                for k, (_, l3, p3) in enumerate(c):
-                    if abs(l1 - l2) <= l3 <= l1 + l2 and p3 == p1 * p2 and m2 == 1:
-                        tp_instr.append((i1, i2, len(blocks)))
-                        lin_instr.append((len(blocks), k))
-                        blocks.append(f"{mul}x{l3}{'e' if p3 == 1 else 'o'}")
-        if not blocks:
-            raise CgtpError("no parity-allowed path")
-        self.mid = "+".join(blocks)
-        self.plan = Plan(irreps_in1, irreps_in2, self.mid, dtype=dtype, shared_weights=True,
-                         instructions=tp_instr)
-        self.linear = Linear(self.mid, irreps_out, instr=lin_instr, dtype=dtype)
-        self.n_paths = len(blocks)
-        self.dim_in1, self.dim_in2 = self.plan.dim_in1, self.plan.dim_in2
-        self.dim_mid, self.dim_out = self.plan.dim_out, self.linear.dim_out
-        self.weight_numel = self.linear.weight_numel
-        self.ones = None
+        L = lib()
+        self.dtype = dtype
+        h = ctypes.c_void_p()
+        _check(L.cgtp_uvw_create(ctypes.byref(h), irreps_in1.encode(), irreps_in2.encode(),
+                                 irreps_out.encode(), _dt(dtype)))
+        self._h = h
+        v = [ctypes.c_int64() for _ in range(5)]
+        n = ctypes.c_int()
+        _check(L.cgtp_uvw_info(h, *[ctypes.byref(t) for t in v], ctypes.byref(n)))
+        (self.dim_in1, self.dim_in2, self.dim_out, self.dim_mid,
+         self.weight_numel) = (t.value for t in v)
+        self.n_paths = n.value
+        # irreps of the per-path blocks: in1's multiplicity, each path's l3 and
+        # the parity of its target irrep
+        mul = int(irreps_in1.replace(" ", "").split("+")[0].split("x")[0])
+        par = [t.strip()[-1] for t in irreps_out.split("+")]
+        self.mid = "+".join(f"{mul}x{q[2]}{par[q[5]]}"
+                            for q in (self.path(p) for p in range(self.n_paths)))
+        ph, lh = ctypes.c_void_p(), ctypes.c_void_p()
+        _check(L.cgtp_uvw_parts(h, ctypes.byref(ph), ctypes.byref(lh)))
+        self.plan = _Borrowed(Plan, ph, self)
+        self.linear = _Borrowed(Linear, lh, self)
 
-    def _ones(self, x):
-        if self.ones is None or self.ones.device != x.device:
-            self.ones = torch.ones(self.plan.weight_numel, dtype=x.dtype, device=x.device)
-        return self.ones
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h is not None and _lib is not None:
+            _lib.cgtp_uvw_destroy(h)
+            self._h = None
+
+    def path(self, p: int):
+        """(l1, l2, l3, i_in1, i_in2, i_out, weight offset) of path p."""
+        vals = [ctypes.c_int() for _ in range(6)]
+        off = ctypes.c_int64()
+        _check(lib().cgtp_uvw_path(self._h, p, *[ctypes.byref(t) for t in vals],
+                                   ctypes.byref(off)))
+        return tuple(t.value for t in vals) + (off.value,)
+
+    def workspace_bytes(self, rows: int):
+        f, b = ctypes.c_size_t(), ctypes.c_size_t()
+        _check(lib().cgtp_uvw_workspace(self._h, rows, ctypes.byref(f), ctypes.byref(b)))
+        return f.value, b.value
+
+    def _ws(self, rows, bwd, device, workspace):
+        if workspace is not None:
+            return workspace, workspace.numel() * workspace.element_size()
+        nb = self.workspace_bytes(rows)[1 if bwd else 0]
+        t = torch.empty(max(256, nb), dtype=torch.uint8, device=device)
+        return t, t.numel()
 
     def forward(self, x, y, W, out=None, mid=None, workspace=None):
-        """out; ``mid`` (optional) receives the per-path blocks [B, dim_mid]."""
-        mid = self.plan.forward(x, y, self._ones(x), out=mid)
-        return self.linear.forward(mid, W, out=out, workspace=workspace)
+        """out [B, dim_out]; ``mid`` (optional) receives the per-path blocks."""
+        B = x.shape[0]
+        _need(x, "x", self.dtype, (B, self.dim_in1))
+        _need(y, "y", self.dtype, (B, self.dim_in2))
+        _need(W, "W", self.dtype, (self.weight_numel,))
+        if out is None:
+            out = torch.empty(B, self.dim_out, dtype=self.dtype, device=x.device)
+        _need(out, "out", self.dtype, (B, self.dim_out))
+        if mid is not None:
+            _need(mid, "mid", self.dtype, (B, self.dim_mid))
+        ws, nb = self._ws(B, False, x.device, workspace)
+        _check(lib().cgtp_uvw_forward(self._h, B, _ptr(x), _ptr(y), _ptr(W), _ptr(out),
+                                      _ptr(mid), _ptr(ws), nb, _stream()))
+        return out
 
-    def backward(self, x, y, W, grad_out, mid=None, need=(True, True, True)):
+    def backward(self, x, y, W, grad_out, mid=None, need=(True, True, True), workspace=None):
         """(grad_x, grad_y, grad_W) for dL/dout = grad_out; ``mid`` = the
         forward's per-path blocks (recomputed when None)."""
-        if mid is None:
-            mid = self.plan.forward(x, y, self._ones(x))
-        gmid, gW = self.linear.backward(mid, W, grad_out, need=(need[0] or need[1], need[2]))
-        gx = gy = None
-        if need[0] or need[1]:
-            gx, gy, _ = self.plan.backward(x, y, self._ones(x), gmid,
-                                           need=(need[0], need[1], False))
+        B = x.shape[0]
+        _need(grad_out, "grad_out", self.dtype, (B, self.dim_out))
+        gx = torch.empty_like(x) if need[0] else None
+        gy = torch.empty_like(y) if need[1] else None
+        gW = torch.empty_like(W) if need[2] else None
+        ws, nb = self._ws(B, True, x.device, workspace)
+        _check(lib().cgtp_uvw_backward(self._h, B, _ptr(x), _ptr(y), _ptr(W), _ptr(grad_out),
+                                       _ptr(mid), _ptr(gx), _ptr(gy), _ptr(gW), _ptr(ws), nb,
+                                       _stream()))
         return gx, gy, gW
 
-    def conv_forward(self, g: "Graph", x, y, W, scale: float = 1.0, out=None, mid=None):
+    def conv_forward(self, g: "Graph", x, y, W, scale: float = 1.0, out=None, mid=None,
+                     workspace=None):
         """The fused convolution with 'uvw' paths: receiver sums of the per-path
         blocks (``mid`` [N, dim_mid]), then the mixing per node."""
-        mid = self.plan.conv_forward(g, x, y, self._ones(x), scale, out=mid)
-        return self.linear.forward(mid, W, out=out)
+        if out is None:
+            out = torch.empty(g.N, self.dim_out, dtype=self.dtype, device=x.device)
+        ws, nb = self._ws(g.N, False, x.device, workspace)
+        _check(lib().cgtp_uvw_conv_forward(self._h, g.N, g.E, _ptr(g.rowptr), _ptr(g.sender),
+                                           _ptr(x), _ptr(y), _ptr(W), float(scale), _ptr(out),
+                                           _ptr(mid), _ptr(ws), nb, _stream()))
+        return out
 
     def conv_backward(self, g: "Graph", x, y, W, scale, grad_out, mid=None,
-                      need=(True, True, True)):
-        if mid is None:
-            mid = self.plan.conv_forward(g, x, y, self._ones(x), scale)
-        gmid, gW = self.linear.backward(mid, W, grad_out, need=(need[0] or need[1], need[2]))
-        gx = gy = None
-        if need[0] or need[1]:
-            gx, gy, _ = self.plan.conv_backward(g, x, y, self._ones(x), scale, gmid,
-                                                need=(need[0], need[1], False))
+                      need=(True, True, True), workspace=None):
+        gx = torch.empty_like(x) if need[0] else None
+        gy = torch.empty_like(y) if need[1] else None
+        gW = torch.empty_like(W) if need[2] else None
+        ws, nb = self._ws(g.N, True, x.device, workspace)
+        _check(lib().cgtp_uvw_conv_backward(
+            self._h, g.N, g.E, _ptr(g.rowptr), _ptr(g.sender), _ptr(g.s_rowptr), _ptr(g.s_perm),
+            _ptr(g.s_recv), _ptr(x), _ptr(y), _ptr(W), float(scale), _ptr(grad_out), _ptr(mid),
+            _ptr(gx), _ptr(gy), _ptr(gW), _ptr(ws), nb, _stream()))
         return gx, gy, gW
+
+
+def _Borrowed(cls, handle, owner):
+    """A Plan / Linear view of a handle owned by ``owner`` (never destroyed here)."""
+    obj = cls.__new__(cls)
+    obj._owner = owner
+    if cls is Plan:
+        L = lib()
+        d1, d2, do, wn = (ctypes.c_int64() for _ in range(4))
+        npth = ctypes.c_int()
+        _check(L.cgtp_plan_info(handle, ctypes.byref(d1), ctypes.byref(d2), ctypes.byref(do),
+                                ctypes.byref(wn), ctypes.byref(npth)))
+        obj.dtype = obj.wdtype = owner.dtype
+        obj.dim_in1, obj.dim_in2, obj.dim_out = d1.value, d2.value, do.value
+        obj.weight_numel, obj.n_paths = wn.value, npth.value
+        obj.shared_weights = True
+    else:
+        L = lib()
+        a, b, c = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+        k = ctypes.c_int()
+        _check(L.cgtp_linear_info(handle, ctypes.byref(a), ctypes.byref(b), ctypes.byref(c),
+                                  ctypes.byref(k)))
+        obj.dtype = owner.dtype
+        obj.dim_in, obj.dim_out, obj.weight_numel, obj.n_instr = a.value, b.value, c.value, k.value
+        t = ctypes.c_int()
+        _check(L.cgtp_linear_path(handle, ctypes.byref(t)))
+        obj.tensor_cores = bool(t.value)
+    obj._h = handle
+    obj._borrowed = True
+    return obj

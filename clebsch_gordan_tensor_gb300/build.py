@@ -47,7 +47,7 @@ def build(verbose: bool = False) -> str:
     embed = os.path.join(OUT, "tp_kernels_embed.cpp")
     _embed(os.path.join(CSRC, "tp_kernels.cuh"), embed, "kTpKernelsSource")
     jobs = []
-    for name in ("plan.cpp", "jit.cpp", "capi.cpp"):
+    for name in ("plan.cpp", "jit.cpp", "capi.cpp", "uvw.cpp"):
         src = os.path.join(CSRC, name)
         obj = os.path.join(OUT, name + ".o")
         cmd = ["g++", "-std=c++17", "-O2", "-fPIC", "-Wall", "-Wno-unused-function", *inc,
@@ -55,7 +55,7 @@ def build(verbose: bool = False) -> str:
         jobs.append((obj, [src, *headers], cmd))
     jobs.append((embed + ".o", [embed],
                  ["g++", "-std=c++17", "-O2", "-fPIC", "-c", embed, "-o", embed + ".o"]))
-    for name in ("sh.cu", "graph.cu", "radial.cu", "linear.cu", "noalloc.cu"):
+    for name in ("sh.cu", "graph.cu", "radial.cu", "linear.cu", "noalloc.cu", "probe.cu"):
         src = os.path.join(CSRC, name)
         obj = os.path.join(OUT, name + ".o")
         cmd = [os.path.join(CUDA, "bin", "nvcc"), *ARCH, "-std=c++17", "-O3", "-lineinfo",

@@ -85,7 +85,14 @@ static cgtp_status launch_tp(Plan& p, const char* name, int64_t n_items, void** 
     if (!staged) {
         int64_t blocks = (n_items + p.slots - 1) / p.slots;
         if (blocks > INT_MAX) blocks = INT_MAX;
-        if (max_rows > 0) blocks = std::max<int64_t>(1, std::min<int64_t>(blocks, max_rows / p.slots));
+        if (max_rows > 0) {
+            // each CTA writes p.slots partial rows: the scratch must hold one CTA's
+            if (max_rows < p.slots)
+                return fail(CGTP_E_ARG, "scratch holds " + std::to_string(max_rows) +
+                                            " partial weight rows, fewer than the " +
+                                            std::to_string(p.slots) + " one CTA writes");
+            blocks = std::min<int64_t>(blocks, max_rows / p.slots);
+        }
         if (rows_used) *rows_used = blocks * p.slots;
         e = cudaLaunchKernel((const void*)k, dim3((unsigned)blocks), dim3(p.block), args, 0, s);
     } else {
@@ -133,6 +140,13 @@ static cgtp_status launch_tp(Plan& p, const char* name, int64_t n_items, void** 
     }
     if (e != cudaSuccess) return cuda_fail(e, name);
     count_launch();
+    {
+        int dev = 0;
+        if (cudaGetDevice(&dev) == cudaSuccess) {
+            std::lock_guard<std::mutex> g(p.mu);
+            m->launched_on.insert(dev);
+        }
+    }
     return CGTP_OK;
 }
 
@@ -185,7 +199,7 @@ static cgtp_status bwd_launch(Plan& p, bool conv, int64_t n_items, const int32_t
     if (staged) name += "_tma";
     int64_t rows = 0;
     cgtp_status st = launch_tp(p, name.c_str(), n_items, args, s, staged, p.bwd_smem,
-                               (int)p.bwd_groups.size() * p.lanes, shared ? ws_rows : 0, &rows);
+                               p.bwd_threads(), shared ? ws_rows : 0, &rows);
     if (st != CGTP_OK || !shared) return st;
     if (rows_out) {  // the caller adds these partial rows up with others
         *rows_out = rows;
@@ -1052,12 +1066,39 @@ cgtp_status conv_backward_into_scratch(cgtp_plan plan, int64_t N, int64_t E,
                       std::min<int64_t>(rows, kSharedWRows));
 }
 
-// True once the plan's kernels are loaded (loading them allocates device memory).
-bool plan_module_loaded(cgtp_plan plan) {
+bool plan_module_loaded(cgtp_plan plan, int dev) {
     if (!plan) return false;
     std::lock_guard<std::mutex> g(plan->p.mu);
     auto it = plan->p.modules.find("tp");
-    return it != plan->p.modules.end() && it->second->lib != nullptr;
+    if (it == plan->p.modules.end() || it->second->lib == nullptr) return false;
+    const std::set<int>& on = it->second->launched_on;
+    return dev < 0 ? !on.empty() : on.count(dev) != 0;
+}
+
+int64_t plan_weight_row_bytes(cgtp_plan plan) {
+    return plan ? plan->p.wdim * (int64_t)esize(plan->p) : 0;
+}
+
+bool plan_shared_weights(cgtp_plan plan) { return plan && plan->p.wmode == CGTP_W_SHARED; }
+
+cgtp_status plan_preload_kernels(cgtp_plan plan, int dev) {
+    if (!plan) return fail(CGTP_E_ARG, "plan is NULL");
+    std::lock_guard<std::mutex> g(plan->p.mu);
+    auto it = plan->p.modules.find("tp");
+    if (it == plan->p.modules.end() || it->second->lib == nullptr)
+        return fail(CGTP_E_ARG, "the plan's kernels are not loaded");
+    Module& m = *it->second;
+    if (m.preloaded_on.count(dev)) return CGTP_OK;
+    cudaError_t e = cudaSuccess;
+    for (auto& kv : m.kernels) {
+        if (!kv.second) continue;
+        cudaFuncAttributes a;
+        if ((e = cudaFuncGetAttributes(&a, (const void*)kv.second)) != cudaSuccess)
+            return cuda_fail(e, ("load kernel " + kv.first).c_str());
+    }
+    if ((e = preload_reduce_kernels()) != cudaSuccess) return cuda_fail(e, "load reduction kernels");
+    m.preloaded_on.insert(dev);
+    return CGTP_OK;
 }
 
 }  // namespace cgtp

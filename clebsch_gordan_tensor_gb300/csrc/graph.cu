@@ -123,6 +123,34 @@ cudaError_t launch_reduce_rows(bool f64, const void* partial, int64_t rows, int6
     return cudaGetLastError();
 }
 
+template <typename T>
+__global__ void fill_ones_kernel(T* __restrict__ p, int64_t n) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * blockDim.x)
+        p[i] = (T)1;
+}
+
+cudaError_t launch_fill_ones(bool f64, void* p, int64_t n, cudaStream_t s) {
+    if (n <= 0) return cudaSuccess;
+    if (f64)
+        fill_ones_kernel<double><<<grid_for(n), 128, 0, s>>>((double*)p, n);
+    else
+        fill_ones_kernel<float><<<grid_for(n), 128, 0, s>>>((float*)p, n);
+    count_launch();
+    return cudaGetLastError();
+}
+
+// Loads the weight-gradient reduction and zero-fill kernels into the current
+// device's context now (with lazy module loading they would otherwise load,
+// and allocate, at their first launch).
+cudaError_t preload_reduce_kernels() {
+    cudaFuncAttributes a;
+    cudaError_t e = cudaFuncGetAttributes(&a, reduce_rows_kernel<float>);
+    if (e == cudaSuccess) e = cudaFuncGetAttributes(&a, reduce_rows_kernel<double>);
+    if (e == cudaSuccess) e = cudaFuncGetAttributes(&a, fill_zero_kernel);
+    return e;
+}
+
 // bytes must be a multiple of 4 (every tensor here is fp32 or fp64).
 cudaError_t launch_fill_zero(void* p, int64_t bytes, cudaStream_t s) {
     const int64_t words = bytes / 4;

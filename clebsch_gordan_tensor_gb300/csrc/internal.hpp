@@ -5,6 +5,7 @@
 
 #include <map>
 #include <memory>
+#include <set>
 #include <string>
 #include <vector>
 
@@ -20,6 +21,8 @@ struct Module {
     void* err_flag = nullptr;           // device address of cgtp_device_error (staged)
     std::map<int, int> smem_set;        // device -> dynamic smem attribute already set
     std::map<std::pair<int, std::string>, int> ctas_per_sm;
+    std::set<int> launched_on;          // devices a kernel of the module has run on
+    std::set<int> preloaded_on;         // devices all its kernels were loaded on
     ~Module();
 };
 
@@ -48,6 +51,9 @@ cudaError_t launch_edge_forces_adjoint(bool f64, int64_t N, const int32_t* rowpt
 cudaError_t launch_fill_zero(void* p, int64_t bytes, cudaStream_t s);
 cudaError_t launch_reduce_rows(bool f64, const void* partial, int64_t rows, int64_t cols,
                                void* out, cudaStream_t s);
+cudaError_t preload_reduce_kernels();
+// p[0..n) = 1 (fp32 or fp64).
+cudaError_t launch_fill_ones(bool f64, void* p, int64_t n, cudaStream_t s);
 
 // Radial network (radial.cu).
 bool radial_tc_eligible(bool f64, int nb, int hidden, int64_t n_out, const void* vec,
@@ -97,6 +103,14 @@ cgtp_status conv_backward_into_scratch(cgtp_plan plan, int64_t N, int64_t E,
                                        const void* w, double scale, const void* grad_out,
                                        void* grad_x, void* grad_y, void* grad_w, void* scratch,
                                        size_t scratch_bytes, cudaStream_t s);
-bool plan_module_loaded(cgtp_plan plan);
+// True once a kernel of the plan's module has run on device dev (dev < 0: on
+// any device); loading the module into a device's context allocates.
+bool plan_module_loaded(cgtp_plan plan, int dev);
+// Bytes of one weight row of the plan (0 for a NULL plan).
+int64_t plan_weight_row_bytes(cgtp_plan plan);
+bool plan_shared_weights(cgtp_plan plan);
+// Loads every kernel of the plan's module, and the fixed reduction kernels, into
+// the current device's context (a no-op once done for that device).
+cgtp_status plan_preload_kernels(cgtp_plan plan, int dev);
 
 }  // namespace cgtp

@@ -16,7 +16,9 @@
 // until the process exits.  Host code must not use its name as an address (on
 // the host the name is only a stand-in); the device address is looked up with
 // cudaGetSymbolAddress once per device, with that device current, on the first
-// call of the entry point on that device.
+// call of the entry point on that device.  That first call also loads the
+// plan's remaining kernels and the reduction kernels into the device's context
+// (set-up that may allocate code memory); later calls allocate nothing.
 #include <cuda_runtime.h>
 
 #include <map>
@@ -29,21 +31,20 @@
 namespace cgtp {
 
 constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;
+// Partial weight-gradient rows the array must hold at least: the most that one
+// CTA of any kernel writes (the non-staged kernels write one per work slot, at
+// most 128), so a weight row may take up to 8 MiB / 128 = 64 KiB.
+constexpr int64_t kNoAllocMinRows = 128;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 static std::mutex g_noalloc_mu;
 static std::map<int, void*> g_noalloc_addr;  // device -> address of the array
 
-// Device address of the array on the current device (set-up on first use).
-static cgtp_status noalloc_scratch(void** out) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) {
-        set_cuda_error(e);
-        set_error_message(std::string("cudaGetDevice: ") + cudaGetErrorString(e));
-        return CGTP_E_CUDA;
-    }
+// Device address of the array on device dev, the current device (looked up on
+// the first call there).
+static cgtp_status noalloc_scratch(int dev, void** out) {
+    cudaError_t e;
     std::lock_guard<std::mutex> g(g_noalloc_mu);
     auto it = g_noalloc_addr.find(dev);
     if (it != g_noalloc_addr.end()) {
@@ -77,15 +78,42 @@ extern "C" cgtp_status cgtp_conv_backward_noalloc(
             cgtp::set_error_message("plan is NULL");
             return CGTP_E_ARG;
         }
-        if (!cgtp::plan_module_loaded(plan)) {
+        // A shared weight row's gradient is summed from partial rows: at least
+        // kNoAllocMinRows of them (the most one CTA of any kernel writes) must fit.
+        const int64_t row = cgtp::plan_weight_row_bytes(plan);
+        if (cgtp::plan_shared_weights(plan) && grad_w &&
+            row > (int64_t)(cgtp::kNoAllocScratchBytes / cgtp::kNoAllocMinRows)) {
+            cgtp::set_error_message("weight row of " + std::to_string(row) +
+                                    " bytes is larger than the no-allocation limit of " +
+                                    std::to_string(cgtp::kNoAllocScratchBytes /
+                                                   cgtp::kNoAllocMinRows) +
+                                    " bytes");
+            return CGTP_E_ARG;
+        }
+        if (!cgtp::plan_module_loaded(plan, -1)) {
             cgtp::set_error_message(
-                "the plan's kernels are not loaded on this device yet (loading them allocates "
+                "the plan's kernels have not run on any device yet (loading them allocates "
                 "device memory): make one call through another entry point first");
             return CGTP_E_ARG;
         }
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) {
+            cgtp::set_cuda_error(e);
+            cgtp::set_error_message(std::string("cudaGetDevice: ") + cudaGetErrorString(e));
+            return CGTP_E_CUDA;
+        }
+        if (!cgtp::plan_module_loaded(plan, dev)) {
+            cgtp::set_error_message(
+                "the plan's kernels have not run on device " + std::to_string(dev) +
+                " yet (loading them there allocates device memory): make one call through "
+                "another entry point on this device first");
+            return CGTP_E_ARG;
+        }
         void* scratch = nullptr;
-        cgtp_status st = cgtp::noalloc_scratch(&scratch);
+        cgtp_status st = cgtp::noalloc_scratch(dev, &scratch);
         if (st != CGTP_OK) return st;
+        if ((st = cgtp::plan_preload_kernels(plan, dev)) != CGTP_OK) return st;
         return cgtp::conv_backward_into_scratch(plan, N, E, s_rowptr, s_perm, s_recv, x, y, w,
                                                 scale, grad_out, grad_x, grad_y, grad_w, scratch,
                                                 cgtp::kNoAllocScratchBytes,

@@ -377,10 +377,16 @@ cgtp_status build_plan(Plan& p, const char* s1, const char* s2, const char* so,
         // instead of through the ring: default for the backward (its ring then
         // carries only the gathered gradient row), not for the forward (its
         // registers limit residency first).  Flag bit 16 turns it on for the
-        // forward, bit 17 off for the backward; it needs a single warp group.
+        // forward (single warp group only), bit 17 off for the backward.
         p.w_direct_f = ((p.flags >> 16) & 1u) && p.fwd_groups.size() == 1;
-        p.w_direct_b = !((p.flags >> 17) & 1u) && p.bwd_groups.size() == 1 &&
+        p.w_direct_b = !((p.flags >> 17) & 1u) &&
                        p.dtype == CGTP_F32;  // fp64 pairs would double the prefetch registers
+        // bits 20-23: resident backward CTAs per SM that the register budget
+        // must allow (__launch_bounds__ minimum; 0 = no bound)
+        p.minb_b = std::max(1, (int)((p.flags >> 20) & 15u));
+        // bit 19: grad_y on a warp of its own (one-warp path group, direct weights)
+        p.gy_warp = ((p.flags >> 19) & 1u) && p.bwd_groups.size() == 1 && p.lanes == 32;
+        p.test_wait0 = (p.flags & CGTP_PLAN_TEST_WAIT_TIMEOUT) != 0;
         const size_t fst = (p.w_direct_f ? 0 : WB) + XB + YB;
         const size_t bst = (p.w_direct_b ? 0 : WB) + GB + YB + 16;
         const size_t budget = 216 * 1024;
@@ -558,53 +564,15 @@ void Plan::gen_groups(std::ostringstream& g, const std::vector<int>& k0, bool f6
         xrows.erase(std::unique(xrows.begin(), xrows.end()), xrows.end());
         std::map<int, int> xi;
         for (size_t i = 0; i < xrows.size(); ++i) xi[xrows[i]] = (int)i;
-        g << "template <> struct BwdG<" << gi << "> {\n  static constexpr int NXR = "
-          << std::max<size_t>(1, xrows.size()) << ";\n";
-        g << "  __device__ static __forceinline__ void loadx(VR (&xr)[NXR], const REAL* xs, int ch) {\n";
-        for (size_t i = 0; i < xrows.size(); ++i)
-            g << "    xr[" << i << "] = lds_v(xs + " << xrows[i] << " * MUL, ch);\n";
-        g << "  }\n";
-        g << "  template <bool GY, class FG, class FW>\n  __device__ static __forceinline__ void edge("
-             "VR (&gxa)[NXR], REAL (&gyl)[NYP], const REAL* __restrict__ Ts, const VR (&xr)[NXR],\n"
-             "      FG&& G, FW&& W, REAL* __restrict__ gwrow, VR (&gwa)[NP], int ch, VR sc, bool dogx,\n"
-             "      int mgw) {\n";
-        // T_DUP_B selects splatted pairs for the backward's T entries; scalar
-        // entries measured faster (fewer registers), so the default is 0.
-        if (cpt == 2) g << "    const float4* __restrict__ Tq = reinterpret_cast<const float4*>(Ts);\n";
-        TLoader L{cpt, std::vector<bool>(ntp / 4 + 1, false), &g, false};
-        for (int q : P_) {
+        // wi[q]: slot of path q in the group's weight registers (direct loads)
+        std::map<int, int> wi;
+        for (size_t i = 0; i < P_.size(); ++i) wi[P_[i]] = (int)i;
+        // grad_y partials of path q: per T entry the two-channel dot of (w x) and
+        // g (or x and (w g), whichever needs fewer products), spread over its CG
+        // terms into the lane's per-y-element sums
+        auto emit_gy = [&](int q) {
             const Path& P = paths[q];
             const int d1 = 2 * P.l1 + 1, d3 = 2 * P.l3 + 1;
-            g << "    { // path " << q << ": " << P.l1 << " x " << P.l2 << " -> " << P.l3 << "\n";
-            g << "    const VR w = W(" << q << ");\n";
-            emit_tloader(L);
-            // h[m1] = sum_m3 T[m1,m3] g[m3]; entries ordered m3-major to interleave chains
-            std::vector<int> ks;
-            for (int k = k0[q]; k < k0[q + 1]; ++k) ks.push_back(k);
-            std::stable_sort(ks.begin(), ks.end(), [&](int a, int b) { return T[a].m3 < T[b].m3; });
-            for (int k = k0[q]; k < k0[q + 1]; ++k) L.get(k);  // load all T of the path first
-            std::vector<bool> hs(d1, false);
-            for (int k : ks) {
-                const std::string t = L.get(k);
-                const int a = T[k].m1;
-                const std::string gv = "G(" + std::to_string(P.r3 + T[k].m3) + ")";
-                if (!hs[a]) {
-                    g << "    VR h" << a << " = vmul(" << t << ", " << gv << ");\n";
-                    hs[a] = true;
-                } else {
-                    g << "    h" << a << " = vfma(" << t << ", " << gv << ", h" << a << ");\n";
-                }
-            }
-            g << "    if (dogx) {\n";
-            for (int a = 0; a < d1; ++a)
-                if (hs[a])
-                    g << "      gxa[" << xi[P.r1 + a] << "] = vfma(w, h" << a << ", gxa["
-                      << xi[P.r1 + a] << "]);\n";
-            g << "    }\n    if (mgw) {\n      VR s = vzero();\n";
-            for (int a = 0; a < d1; ++a)
-                if (hs[a]) g << "      s = vfma(xr[" << xi[P.r1 + a] << "], h" << a << ", s);\n";
-            g << "      GWOUT(" << q << ", s);\n    }\n";
-            g << "    if (GY) {\n";
             const bool zx = d1 <= d3;
             if (zx) {
                 for (int a = 0; a < d1; ++a)
@@ -625,7 +593,78 @@ void Plan::gen_groups(std::ostringstream& g, const std::vector<int>& k0, bool f6
                       << ", d, gyl[" << term.first << "]);\n";
                 g << "      }\n";
             }
+        };
+        g << "template <> struct BwdG<" << gi << "> {\n  static constexpr int NXR = "
+          << std::max<size_t>(1, xrows.size()) << ", NPW = " << std::max<size_t>(1, P_.size())
+          << ";\n";
+        // calls f(slot, path) for every path of the group
+        g << "  template <class F> __device__ static __forceinline__ void each_w(F&& f) {\n";
+        for (size_t i = 0; i < P_.size(); ++i) g << "    f(" << i << ", " << P_[i] << ");\n";
+        g << "  }\n";
+        g << "  __device__ static __forceinline__ void loadx(VR (&xr)[NXR], const REAL* xs, int ch) {\n";
+        for (size_t i = 0; i < xrows.size(); ++i)
+            g << "    xr[" << i << "] = lds_v(xs + " << xrows[i] << " * MUL, ch);\n";
+        g << "  }\n";
+        // FIX: grad_x and grad_w are both written (mode 1), so the stream has no
+        // run-time branch and the whole edge is one block for the scheduler
+        g << "  template <bool GY, bool FIX, class FG, class FW>\n  __device__ static __forceinline__ void edge("
+             "VR (&gxa)[NXR], REAL (&gyl)[NYP], const REAL* __restrict__ Ts, const VR (&xr)[NXR],\n"
+             "      FG&& G, FW&& W, REAL* __restrict__ gwrow, VR (&gwa)[NP], int ch, VR sc, bool dogx,\n"
+             "      int mgw) {\n";
+        // flag bit 27 (T_DUP_B) stores the backward's T entries as splatted pairs
+        // (two per 128-bit load, no splat in the stream); scalar entries (four
+        // per load) are the default.
+        const bool tdup = cpt == 2 && ((flags >> 27) & 1u);
+        if (cpt == 2) g << "    const float4* __restrict__ Tq = reinterpret_cast<const float4*>(Ts);\n";
+        if (tdup) g << "    const ulonglong2* __restrict__ Tp = reinterpret_cast<const ulonglong2*>(Ts);\n";
+        TLoader L{cpt, std::vector<bool>(ntp / 2 + 1, false), &g, tdup};
+        for (int q : P_) {
+            const Path& P = paths[q];
+            const int d1 = 2 * P.l1 + 1, d3 = 2 * P.l3 + 1;
+            g << "    { // path " << q << ": " << P.l1 << " x " << P.l2 << " -> " << P.l3 << "\n";
+            g << "    const VR w = W(" << wi[q] << ", " << q << ");\n";
+            emit_tloader(L);
+            // h[m1] = sum_m3 T[m1,m3] g[m3]; entries ordered m3-major to interleave chains
+            std::vector<int> ks;
+            for (int k = k0[q]; k < k0[q + 1]; ++k) ks.push_back(k);
+            std::stable_sort(ks.begin(), ks.end(), [&](int a, int b) { return T[a].m3 < T[b].m3; });
+            for (int k = k0[q]; k < k0[q + 1]; ++k) L.get(k);  // load all T of the path first
+            std::vector<bool> hs(d1, false);
+            for (int k : ks) {
+                const std::string t = L.get(k);
+                const int a = T[k].m1;
+                const std::string gv = "G(" + std::to_string(P.r3 + T[k].m3) + ")";
+                if (!hs[a]) {
+                    g << "    VR h" << a << " = vmul(" << t << ", " << gv << ");\n";
+                    hs[a] = true;
+                } else {
+                    g << "    h" << a << " = vfma(" << t << ", " << gv << ", h" << a << ");\n";
+                }
+            }
+            g << "    if (FIX || dogx) {\n";
+            for (int a = 0; a < d1; ++a)
+                if (hs[a])
+                    g << "      gxa[" << xi[P.r1 + a] << "] = vfma(w, h" << a << ", gxa["
+                      << xi[P.r1 + a] << "]);\n";
+            g << "    }\n    if (FIX || mgw) {\n      VR s = vzero();\n";
+            for (int a = 0; a < d1; ++a)
+                if (hs[a]) g << "      s = vfma(xr[" << xi[P.r1 + a] << "], h" << a << ", s);\n";
+            g << "      GWOUT_M(" << q << ", s, FIX ? 1 : mgw);\n    }\n";
+            g << "    if (GY) {\n";
+            emit_gy(q);
             g << "    }\n    }\n";
+        }
+        g << "  }\n";
+        // grad_y alone (the CG coefficients are immediates: no T, no y), for
+        // the CTA's grad-y warp
+        g << "  template <class FG, class FW>\n  __device__ static __forceinline__ void edge_gy("
+             "REAL (&gyl)[NYP], const VR (&xr)[NXR], FG&& G, FW&& W) {\n";
+        for (int q : P_) {
+            const Path& P = paths[q];
+            g << "    { // path " << q << ": " << P.l1 << " x " << P.l2 << " -> " << P.l3 << "\n";
+            g << "    const VR w = W(" << wi[q] << ", " << q << ");\n";
+            emit_gy(q);
+            g << "    }\n";
         }
         g << "  }\n";
         g << "  __device__ static __forceinline__ void first(REAL* buf, const VR (&gxa)[NXR], int ch) {\n";
@@ -669,8 +708,11 @@ std::string Plan::kernel_source() const {
     os << "#define STAGED " << (staged ? 1 : 0) << "\n#define STAGES_F " << stages_f
        << "\n#define STAGES_B " << stages_b << "\n#define W_DIRECT_F " << (w_direct_f ? 1 : 0)
        << "\n#define W_DIRECT_B " << (w_direct_b ? 1 : 0) << "\n#define W_STORE " << (w_bf16 ? 1 : w_f16 ? 2 : 0)
-       << "\n#define T_DUP_B 0\n#define W_BUF2 " << (((flags >> 18) & 1u) ? 0 : 1)
+       << "\n#define T_DUP_B " << ((cpt == 2 && ((flags >> 27) & 1u)) ? 1 : 0) << "\n#define W_BUF2 " << (((flags >> 18) & 1u) ? 0 : 1)
        << "\n#define SHARED_W " << (wmode == CGTP_W_SHARED ? 1 : 0)
+       << "\n#define MINB_B " << minb_b << "\n#define GYW " << (gy_warp ? 1 : 0)
+       << "\n#define TEST_WAIT0 " << (test_wait0 ? 1 : 0)
+       << "\n#define W_ALT " << (((flags >> 28) & 1u) ? 1 : 0)
        << "\n#define GF " << std::max<size_t>(1, fwd_groups.size()) << "\n#define GB "
        << std::max<size_t>(1, bwd_groups.size()) << "\n";
     // T tables

@@ -69,6 +69,12 @@ struct Plan {
     int stages_f = 3, stages_b = 3;  // TMA ring depths (forward, backward)
     bool w_direct_f = false, w_direct_b = false;  // weights bypass the ring
     size_t fwd_smem = 0, bwd_smem = 0;  // dynamic shared memory per CTA
+    int minb_b = 1;  // backward: resident CTAs per SM the register budget must allow
+    // backward: a second warp per CTA computes grad_y while the first computes
+    // grad_x and grad_w (one path group of one warp)
+    bool gy_warp = false;
+    bool test_wait0 = false;  // test only: the first wait of each CTA gives up at once
+    int bwd_threads() const { return ((int)bwd_groups.size() + (gy_warp ? 1 : 0)) * lanes; }
     // warp groups of the staged kernels: each group of `lanes` threads runs the
     // generated stream of a subset of paths (longest-processing-time split)
     std::vector<std::vector<int>> fwd_groups, bwd_groups;

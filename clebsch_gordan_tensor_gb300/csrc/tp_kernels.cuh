@@ -210,8 +210,10 @@ __device__ __forceinline__ void gw_store(REAL* gp, int ch, VR s, VR sc, int mgw)
 }
 #if SHARED_W
 #define GWOUT(q, s) (gwa[q] = vadd(gwa[q], (s)))
+#define GWOUT_M(q, s, mode) (gwa[q] = vadd(gwa[q], (s)))
 #else
 #define GWOUT(q, s) gw_store(gwrow + (long long)(q) * MUL, ch, (s), sc, mgw)
+#define GWOUT_M(q, s, mode) gw_store(gwrow + (long long)(q) * MUL, ch, (s), sc, (mode))
 #endif
 // Partial weight-gradient row of a CTA or slot (shared weights).
 __device__ __forceinline__ void gw_partial(REAL* __restrict__ row, const VR (&gwa)[NP], int ch,
@@ -504,11 +506,14 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned by
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
         ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(b)) : "memory");
 }
-// Bounded wait for phase `parity` of barrier b.  Returns false on timeout.
-__device__ __forceinline__ bool mbar_wait(unsigned long long* b, unsigned parity) {
+// Bounded wait for phase `parity` of barrier b: at most `polls` polls (the
+// default, 2^24 polls sleeping 64 ns between late ones, is about a second).
+// Returns false on timeout.
+constexpr unsigned kWaitPolls = 1u << 24;
+__device__ __forceinline__ bool mbar_wait(unsigned long long* b, unsigned parity,
+                                          unsigned polls = kWaitPolls) {
     const unsigned a = smem_u32(b);
-    // about a second at most: 2^24 polls, sleeping 64 ns between late polls
-    for (unsigned it = 0; it < (1u << 24); ++it) {
+    for (unsigned it = 0; it < polls; ++it) {
         unsigned ok;
         asm volatile(
             "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
@@ -518,6 +523,10 @@ __device__ __forceinline__ bool mbar_wait(unsigned long long* b, unsigned parity
     }
     return false;
 }
+
+// TEST_WAIT0 (a test-only plan flag): the first wait of every CTA gives up at
+// once, so the timeout path (error flag, drain of the copies in flight, early
+// return) runs without any real stall.
 
 // First index n in [0, N] with ptr[n] >= target (ptr non-decreasing), computed
 // by one warp with 32-way probes.
@@ -675,7 +684,7 @@ constexpr unsigned WSB = W_DIRECT_B ? 0u : WB;  // weight bytes in a backward st
 constexpr unsigned FWD_STAGE = WSF + XB + YB;
 constexpr unsigned BWD_STAGE = WSB + GB_ + YB + 16;
 constexpr int NTF = GF * LANES;  // threads of a forward CTA
-constexpr int NTB = GB * LANES;  // threads of a backward CTA
+constexpr int NTB = (GB + GYW) * LANES;  // threads of a backward CTA (GYW: + a grad-y warp)
 
 // A 32-entry window of an int array, held one entry per lane of warp 0, with
 // the next window prefetched.  get(j) must be called by all lanes of warp 0
@@ -767,7 +776,8 @@ __device__ __forceinline__ void fwd_group(const FwdArgs& A, const FwdShared& S, 
         for (; j < e1; ++j) {
             const long long k = j - S.e_begin;
             const unsigned char* st = S.stages + (size_t)(k % STAGES_F) * FWD_STAGE;
-            const bool ok = mbar_wait(&S.full[k % STAGES_F], (unsigned)((k / STAGES_F) & 1));
+            const bool ok = mbar_wait(&S.full[k % STAGES_F], (unsigned)((k / STAGES_F) & 1),
+                                      TEST_WAIT0 && k == 0 ? 0u : kWaitPolls);
             build_T_cta<NTF>(S.Ts, reinterpret_cast<const REAL*>(st + WSF + XB), tt);
             if (!cta_all(ok)) {
                 fail_and_drain(1, S.full, STAGES_F);
@@ -929,7 +939,7 @@ __device__ __forceinline__ void bwd_issue_x(const BwdArgs& A, const BwdShared& S
     }
 }
 
-template <int GRP, bool CONV, bool GY>
+template <int GRP, bool CONV, bool GY, bool FIX>
 __device__ __forceinline__ void bwd_group(const BwdArgs& A, const BwdShared& S, IdxWindow& we,
                                           IdxWindow& wn) {
     using BG = BwdG<GRP>;
@@ -944,23 +954,25 @@ __device__ __forceinline__ void bwd_group(const BwdArgs& A, const BwdShared& S, 
     // edge ids come from the stage headers (written before the barrier that
     // follows their issue); the first stage was issued before this loop
     // W_BUF2: the next edge's weights land in a second register array loaded
-    // ahead of the stream; otherwise the stream reads a path's weight and
-    // reloads that slot with the next edge's value.
-    WRAW wbuf[NP];
+    // ahead of the stream (the arrays alternate from edge to edge); otherwise
+    // the stream reads a path's weight and reloads that slot with the next
+    // edge's value.
+    // (slot i of a group's registers holds the weight pair of its path q)
+    WRAW wbuf[BG::NPW];
 #if W_BUF2
-    WRAW wnext[NP];
+    WRAW wnext[BG::NPW];
 #endif
     if (S.j_begin < S.j_end) {
         const long long e0 = *reinterpret_cast<const int*>(S.stages + WSB + GB_ + YB);
-#pragma unroll
-        for (int p = 0; p < NP; ++p) wbuf[p] = ldw_raw(A.w + e0 * A.w_stride + p * MUL, ch);
+        BG::each_w([&](int i, int q) { wbuf[i] = ldw_raw(A.w + e0 * A.w_stride + q * MUL, ch); });
     }
 #endif
     for (long long item = S.i0; item < S.i1; ++item) {
         const long long kk = item - S.i0;
         const long long e1 = nend;
         if (item + 1 < S.i1) nend = CONV ? (long long)__ldg(A.s_rowptr + item + 2) : item + 2;
-        if (!cta_all(mbar_wait(&S.xfull[kk & 1], (unsigned)((kk >> 1) & 1)))) {
+        if (!cta_all(mbar_wait(&S.xfull[kk & 1], (unsigned)((kk >> 1) & 1),
+                               TEST_WAIT0 && kk == 0 ? 0u : kWaitPolls))) {
             fail_and_drain(2, S.full, STAGES_B);
             fail_and_drain(2, S.xfull, 2);
             return;
@@ -995,29 +1007,41 @@ __device__ __forceinline__ void bwd_group(const BwdArgs& A, const BwdShared& S, 
             }
             const WT* wrow1 = A.w + e1 * A.w_stride;
 #if W_BUF2
+            // W_ALT: the two register buffers take turns (this edge reads one
+            // while the next edge's weights land in the other, no copy between
+            // them); else the next edge's weights are copied over after use
+            if (!W_ALT || (k & 1) == 0) {
+                BG::each_w([&](int i, int q) { wnext[i] = ldw_raw(wrow1 + q * MUL, ch); });
+                BG::template edge<GY, FIX>(gxa, gyl, S.Ts, xr,
+                                           [&](int r) { return lds_v(gs + r * MUL, ch); },
+                                           [&](int i, int) { return wcvt(wbuf[i]); }, gwrow, gwa,
+                                           ch, sc, A.mgx != 0, A.mgw);
+                if (!W_ALT) {
 #pragma unroll
-            for (int p = 0; p < NP; ++p) wnext[p] = ldw_raw(wrow1 + p * MUL, ch);
-            BG::template edge<GY>(gxa, gyl, S.Ts, xr,
-                                  [&](int r) { return lds_v(gs + r * MUL, ch); },
-                                  [&](int p) { return wcvt(wbuf[p]); }, gwrow, gwa, ch, sc,
-                                  A.mgx != 0, A.mgw);
-#pragma unroll
-            for (int p = 0; p < NP; ++p) wbuf[p] = wnext[p];
+                    for (int i = 0; i < BG::NPW; ++i) wbuf[i] = wnext[i];
+                }
+            } else {
+                BG::each_w([&](int i, int q) { wbuf[i] = ldw_raw(wrow1 + q * MUL, ch); });
+                BG::template edge<GY, FIX>(gxa, gyl, S.Ts, xr,
+                                           [&](int r) { return lds_v(gs + r * MUL, ch); },
+                                           [&](int i, int) { return wcvt(wnext[i]); }, gwrow, gwa,
+                                           ch, sc, A.mgx != 0, A.mgw);
+            }
 #else
-            BG::template edge<GY>(gxa, gyl, S.Ts, xr,
+            BG::template edge<GY, FIX>(gxa, gyl, S.Ts, xr,
                                   [&](int r) { return lds_v(gs + r * MUL, ch); },
-                                  [&](int p) {
-                                      const VR v = wcvt(wbuf[p]);
-                                      wbuf[p] = ldw_raw(wrow1 + p * MUL, ch);
+                                  [&](int i, int q) {
+                                      const VR v = wcvt(wbuf[i]);
+                                      wbuf[i] = ldw_raw(wrow1 + q * MUL, ch);
                                       return v;
                                   },
                                   gwrow, gwa, ch, sc, A.mgx != 0, A.mgw);
 #endif
 #else
             const WT* ws = reinterpret_cast<const WT*>(st);
-            BG::template edge<GY>(gxa, gyl, S.Ts, xr,
+            BG::template edge<GY, FIX>(gxa, gyl, S.Ts, xr,
                                   [&](int r) { return lds_v(gs + r * MUL, ch); },
-                                  [&](int p) { return lds_w(ws + p * MUL, ch); }, gwrow, gwa,
+                                  [&](int, int q) { return lds_w(ws + q * MUL, ch); }, gwrow, gwa,
                                   ch, sc, A.mgx != 0, A.mgw);
 #endif
             if (GY && A.mgy) {
@@ -1065,6 +1089,112 @@ __device__ __forceinline__ void bwd_group(const BwdArgs& A, const BwdShared& S, 
     if (SHARED_W && A.mgw) gw_partial(A.wsp + (long long)blockIdx.x * WDIM, gwa, ch, sc);
 }
 
+#if GYW
+// The grad-y warp: walks the same items and ring stages as group 0, passing
+// the same CTA barriers in the same order, and computes only grad_y (the CG
+// coefficients are immediates, so it reads x, the staged g row and the
+// weights, not T).  Group 0 then runs without grad_y.
+template <bool CONV, bool GY>
+__device__ __forceinline__ void bwd_gy_role(const BwdArgs& A, const BwdShared& S) {
+    using BG = BwdG<0>;
+    const int tid = threadIdx.x, ch = tid % LANES, lane = tid & 31;
+    const bool dogy = GY && A.mgy;
+    long long j = S.j_begin;
+    long long nend = CONV ? (long long)__ldg(A.s_rowptr + S.i0 + 1) : S.i0 + 1;
+#if W_DIRECT_B
+    WRAW wbuf[BG::NPW];
+#if W_BUF2
+    WRAW wnext[BG::NPW];
+#endif
+    if (dogy && S.j_begin < S.j_end) {
+        const long long e0 = *reinterpret_cast<const int*>(S.stages + WSB + GB_ + YB);
+        BG::each_w([&](int i, int q) { wbuf[i] = ldw_raw(A.w + e0 * A.w_stride + q * MUL, ch); });
+    }
+#endif
+    for (long long item = S.i0; item < S.i1; ++item) {
+        const long long kk = item - S.i0;
+        const long long e1 = nend;
+        if (item + 1 < S.i1) nend = CONV ? (long long)__ldg(A.s_rowptr + item + 2) : item + 2;
+        if (!cta_all(mbar_wait(&S.xfull[kk & 1], (unsigned)((kk >> 1) & 1),
+                               TEST_WAIT0 && kk == 0 ? 0u : kWaitPolls))) {
+            fail_and_drain(2, S.full, STAGES_B);
+            fail_and_drain(2, S.xfull, 2);
+            return;
+        }
+        VR xr[BG::NXR];
+        BG::loadx(xr, reinterpret_cast<const REAL*>(S.xring + (size_t)(kk & 1) * XB), ch);
+        cta_sync();  // every thread holds its x before the slot is refilled
+        for (; j < e1; ++j) {
+            const long long k = j - S.j_begin;
+            const unsigned char* st = S.stages + (size_t)(k % STAGES_B) * BWD_STAGE;
+            const bool ok = mbar_wait(&S.full[k % STAGES_B], (unsigned)((k / STAGES_B) & 1));
+            const long long e = *reinterpret_cast<const int*>(st + WSB + GB_ + YB);
+            build_T_cta<NTB, T_DUP_B && CPT == 2>(S.Ts, reinterpret_cast<const REAL*>(st + WSB + GB_));
+            if (!cta_all(ok)) {
+                fail_and_drain(3, S.full, STAGES_B);
+                fail_and_drain(3, S.xfull, 2);
+                return;
+            }
+            if (dogy) {
+                const REAL* gs = reinterpret_cast<const REAL*>(st + WSB);
+                REAL gyl[NYP];
+#pragma unroll
+                for (int i = 0; i < NYP; ++i) gyl[i] = (REAL)0;
+#if W_DIRECT_B
+                long long en = e;
+                if (j + 1 < S.j_end) {
+                    const unsigned char* st1 = S.stages + (size_t)((k + 1) % STAGES_B) * BWD_STAGE;
+                    en = *reinterpret_cast<const int*>(st1 + WSB + GB_ + YB);
+                }
+                const WT* wrow1 = A.w + en * A.w_stride;
+#if W_BUF2
+                if (!W_ALT || (k & 1) == 0) {
+                    BG::each_w([&](int i, int q) { wnext[i] = ldw_raw(wrow1 + q * MUL, ch); });
+                    BG::edge_gy(gyl, xr, [&](int r) { return lds_v(gs + r * MUL, ch); },
+                                [&](int i, int) { return wcvt(wbuf[i]); });
+                    if (!W_ALT) {
+#pragma unroll
+                        for (int i = 0; i < BG::NPW; ++i) wbuf[i] = wnext[i];
+                    }
+                } else {
+                    BG::each_w([&](int i, int q) { wbuf[i] = ldw_raw(wrow1 + q * MUL, ch); });
+                    BG::edge_gy(gyl, xr, [&](int r) { return lds_v(gs + r * MUL, ch); },
+                                [&](int i, int) { return wcvt(wnext[i]); });
+                }
+#else
+                BG::edge_gy(gyl, xr, [&](int r) { return lds_v(gs + r * MUL, ch); },
+                            [&](int i, int q) {
+                                const VR v = wcvt(wbuf[i]);
+                                wbuf[i] = ldw_raw(wrow1 + q * MUL, ch);
+                                return v;
+                            });
+#endif
+#else
+                const WT* ws = reinterpret_cast<const WT*>(st);
+                BG::edge_gy(gyl, xr, [&](int r) { return lds_v(gs + r * MUL, ch); },
+                            [&](int, int q) { return lds_w(ws + q * MUL, ch); });
+#endif
+                int base = 0;
+                bool owner = true;
+                seg_reduce<16, NYP>(gyl, lane, 0xffffffffu, base, owner);
+                if (owner) {
+#pragma unroll
+                    for (int i = 0; i < NRED; ++i) {
+                        const int c = base + i;
+                        if (c < NY) {
+                            REAL t = gyl[i] * A.scale;
+                            if (A.mgy == 2) t += A.gy[e * NY + c];
+                            A.gy[e * NY + c] = t;
+                        }
+                    }
+                }
+            }
+            cta_sync();
+        }
+    }
+}
+#endif
+
 template <bool CONV, bool GY>
 __device__ __forceinline__ void bwd_staged(const BwdArgs& A) {
     extern __shared__ __align__(128) unsigned char smem[];
@@ -1111,20 +1241,33 @@ __device__ __forceinline__ void bwd_staged(const BwdArgs& A) {
     bwd_issue_x(A, S, S.i0, 0);
     __syncthreads();  // stage headers of the first edges are visible to all threads
     const int grp = threadIdx.x / LANES;
-    if (grp == 0) bwd_group<0, CONV, GY>(A, S, we, wn);
+    // grad_x and grad_w both written: the branch-free stream
+    const bool fix = A.mgx == 1 && A.mgw == 1;
+#define CGTP_BWD_GROUP(G_, GY_)                                  \
+    (fix ? bwd_group<G_, CONV, GY_, true>(A, S, we, wn)          \
+         : bwd_group<G_, CONV, GY_, false>(A, S, we, wn))
+#if GYW
+    if (grp == 0)
+        CGTP_BWD_GROUP(0, false);
+    else
+        bwd_gy_role<CONV, GY>(A, S);
+#else
+    if (grp == 0) CGTP_BWD_GROUP(0, GY);
+#endif
 #if GB > 1
-    else if (grp == 1) bwd_group<1, CONV, GY>(A, S, we, wn);
+    else if (grp == 1) CGTP_BWD_GROUP(1, GY);
 #endif
 #if GB > 2
-    else if (grp == 2) bwd_group<2, CONV, GY>(A, S, we, wn);
+    else if (grp == 2) CGTP_BWD_GROUP(2, GY);
 #endif
 #if GB > 3
-    else if (grp == 3) bwd_group<3, CONV, GY>(A, S, we, wn);
+    else if (grp == 3) CGTP_BWD_GROUP(3, GY);
 #endif
+#undef CGTP_BWD_GROUP
 }
 
 #define CGTP_BWD_TMA_ENTRY(NAME, CONV, GY)                                                      \
-    extern "C" __global__ void __launch_bounds__(NTB) NAME(                                   \
+    extern "C" __global__ void __launch_bounds__(NTB, MINB_B) NAME(                           \
         long long n_items, const int* __restrict__ s_rowptr, const int* __restrict__ s_perm,  \
         const int* __restrict__ s_recv, const REAL* __restrict__ x,                           \
         const REAL* __restrict__ y, const WT* __restrict__ w, long long w_stride,             \

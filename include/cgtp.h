@@ -93,7 +93,12 @@ typedef struct {
  * in registers) instead of through the ring; bit 17: backward lanes take their
  * weights through the ring instead of loading them directly (the default for
  * fp32 plans); bit 18: directly loaded backward weights use one register
- * buffer (reloaded path by path) instead of two.
+ * buffer (reloaded path by path) instead of two; bit 19: the backward puts
+ * the grad_y contraction on a second warp of each CTA (one-warp path groups);
+ * bits 20-23: the backward's register budget must allow that many resident
+ * CTAs per SM; bit 27: the backward's T entries are stored as splatted pairs;
+ * bit 28: the backward's two weight buffers alternate instead of the next
+ * edge's being copied over.
  * CGTP_PLAN_WEIGHTS_BF16 (bit 24): the weights (w, per edge or shared) are
  * stored as bfloat16 and widened exactly to fp32 on load; all arithmetic,
  * every other tensor and grad_w stay fp32.  This halves the dominant weight
@@ -106,6 +111,14 @@ typedef struct {
  * 2^-14 are subnormal), widened exactly to fp32 on load.  Not combined with
  * CGTP_PLAN_WEIGHTS_BF16 (CGTP_E_ARG); the same restrictions otherwise. */
 #define CGTP_PLAN_WEIGHTS_F16 (1u << 25)
+/* CGTP_PLAN_TEST_WAIT_TIMEOUT (bit 26), for tests of the failure path only: in
+ * the staged kernels the first bounded wait of every CTA gives up at once, as
+ * if its bulk copy had not arrived within the limit.  The kernel then records
+ * a code in the plan's device error flag, waits (bounded) for the copies it
+ * has in flight and returns without finishing its outputs;
+ * cgtp_plan_device_status returns CGTP_E_DEVICE with that code once and clears
+ * the flag.  Never set it outside a test. */
+#define CGTP_PLAN_TEST_WAIT_TIMEOUT (1u << 26)
 cgtp_status cgtp_plan_create(cgtp_plan* out, const char* irreps_in1, const char* irreps_in2,
                              const char* irreps_out, const cgtp_instr* instr, int n_instr,
                              cgtp_dtype dtype, cgtp_wmode wmode, unsigned flags);
@@ -231,15 +244,20 @@ cgtp_status cgtp_conv_backward_ws(cgtp_plan plan, int64_t N, int64_t E, const in
  * that cannot take the implicit synchronisation of cudaMalloc / cudaFree).
  * The pages have no counterpart: this entry point only changes where the
  * scratch lives.  The scratch is a fixed 8 MiB device array inside the library
- * (every GPU that loads the library holds it until exit); weight rows larger
- * than 8 MiB are rejected with CGTP_E_ARG, and at most min(2048, 8 MiB /
- * weight row bytes) partial rows are used.  The first call on a device looks up the
- * array's device address (set-up; make that first call before any stream
- * capture).  The plan's kernels must already be loaded on the device by a call
- * through another entry point (loading allocates), else CGTP_E_ARG.  Every call
- * shares the one array and overwrites all of the rows it reads, so nothing in
- * it needs clearing; calls whose kernels overlap on the GPU race on it.  No
- * call allocates or frees device memory. */
+ * (every GPU that loads the library holds it until exit).  A CGTP_W_SHARED plan
+ * asking for grad_w sums it from partial rows in that array: its weight row may
+ * take at most 64 KiB (8 MiB / 128, room for the partial rows of one CTA of any
+ * kernel), else CGTP_E_ARG; at most min(2048, 8 MiB / row bytes) partial rows
+ * are used.  The plan's kernels must already have run on the current device
+ * through another entry point (that first load allocates), else CGTP_E_ARG.
+ * Set-up: the first call on a device looks up the array's device address and
+ * loads the rest of the plan's kernels and the reduction kernels into the
+ * device's context, which can allocate device memory for their code; make that
+ * first call before any stream capture and where allocation is acceptable.
+ * Later calls on that device allocate and free nothing.  Every call shares the
+ * one array and overwrites all of the rows it reads, so nothing in it needs
+ * clearing; calls whose kernels overlap on the GPU (two streams, two threads)
+ * race on it. */
 cgtp_status cgtp_conv_backward_noalloc(cgtp_plan plan, int64_t N, int64_t E,
                                        const int32_t* rowptr, const int32_t* sender,
                                        const int32_t* s_rowptr, const int32_t* s_perm,
@@ -376,6 +394,66 @@ cgtp_status cgtp_linear_backward(cgtp_linear lin, int64_t n, const void* x, cons
  * cleared.  Synchronous. */
 cgtp_status cgtp_linear_device_status(int* code);
 
+/* ------------------------------------------------- 'uvw' product ------ */
+/* The 'uvw' tensor product: one matrix W_p [mul_in][mul_out] per path, shared
+ * by every row (NVIDIA SE(3)-Transformer blog, "TFN fusion": the pairwise
+ * degree convolutions feeding one output degree are summed and the channel
+ * contractions become dense products):
+ *   out[b, k, m3, w] = sum over paths p -> k of sum_u sum_{m1,m2}
+ *                      C_p[m1,m2,m3] x[b, i1(p), m1, u] y[b, i2(p), m2] W_p[u, w]
+ * Paths: every (i_in1, i_in2, i_out) with |l1 - l2| <= l3 <= l1 + l2 and
+ * p3 = p1 p2, listed in1-major, then in2, then out; W holds their matrices in
+ * that order (cgtp_uvw_path gives each offset).  in1 has one multiplicity
+ * (mul_in), in2 multiplicity 1 (spherical harmonics).  It runs as the 'uvu'
+ * product into one block per path (the "mid" row, dim_mid wide) with unit
+ * weights, then the channel mixing of cgtp_linear (tcgen05 for fp32); the
+ * convolution sums the blocks per receiver first and mixes once per node.
+ * Every call takes a caller-owned device workspace (256-byte aligned, at least
+ * cgtp_uvw_workspace() bytes for its row count: B samples or N nodes; contents
+ * need not be set; calls sharing one must not overlap in time).  Host only to
+ * create; the handle is immutable and may be shared between threads. */
+typedef struct cgtp_uvw_s* cgtp_uvw;
+cgtp_status cgtp_uvw_create(cgtp_uvw* out, const char* irreps_in1, const char* irreps_in2,
+                            const char* irreps_out, cgtp_dtype dtype);
+cgtp_status cgtp_uvw_destroy(cgtp_uvw u);
+cgtp_status cgtp_uvw_info(cgtp_uvw u, int64_t* dim_in1, int64_t* dim_in2, int64_t* dim_out,
+                          int64_t* dim_mid, int64_t* weight_numel, int* n_paths);
+/* Path p: l1, l2, l3, its irrep indices and the offset of W_p in W. */
+cgtp_status cgtp_uvw_path(cgtp_uvw u, int p, int* l1, int* l2, int* l3, int* i_in1, int* i_in2,
+                          int* i_out, int64_t* weight_offset);
+/* The product's two parts (borrowed handles, valid while u lives). */
+cgtp_status cgtp_uvw_parts(cgtp_uvw u, cgtp_plan* plan, cgtp_linear* lin);
+/* Workspace bytes for `rows` rows: forward and backward (the backward's figure
+ * covers recomputing the mid blocks when the caller does not pass them). */
+cgtp_status cgtp_uvw_workspace(cgtp_uvw u, int64_t rows, size_t* fwd_bytes, size_t* bwd_bytes);
+/* out [B, dim_out] from x [B, dim_in1], y [B, dim_in2], W [weight_numel];
+ * mid [B, dim_mid] (optional, device) receives the per-path blocks for a later
+ * backward.  Asynchronous on `stream`; allocates nothing. */
+cgtp_status cgtp_uvw_forward(cgtp_uvw u, int64_t B, const void* x, const void* y, const void* W,
+                             void* out, void* mid, void* workspace, size_t workspace_bytes,
+                             cgtp_stream stream);
+/* grad_x, grad_y, grad_W (each optional) for the cotangent grad_out; mid: the
+ * forward's blocks, or NULL to recompute them in the workspace.  grad_W sums
+ * over rows in fixed order (deterministic). */
+cgtp_status cgtp_uvw_backward(cgtp_uvw u, int64_t B, const void* x, const void* y, const void* W,
+                              const void* grad_out, const void* mid, void* grad_x, void* grad_y,
+                              void* grad_W, void* workspace, size_t workspace_bytes,
+                              cgtp_stream stream);
+/* The fused graph convolution with 'uvw' paths: out[n] = scale * mixing of the
+ * sum over n's edges of the per-path blocks (graph arguments as
+ * cgtp_conv_forward / cgtp_conv_backward; mid is [N, dim_mid]). */
+cgtp_status cgtp_uvw_conv_forward(cgtp_uvw u, int64_t N, int64_t E, const int32_t* rowptr,
+                                  const int32_t* sender, const void* x, const void* y,
+                                  const void* W, double scale, void* out, void* mid,
+                                  void* workspace, size_t workspace_bytes, cgtp_stream stream);
+cgtp_status cgtp_uvw_conv_backward(cgtp_uvw u, int64_t N, int64_t E, const int32_t* rowptr,
+                                   const int32_t* sender, const int32_t* s_rowptr,
+                                   const int32_t* s_perm, const int32_t* s_recv, const void* x,
+                                   const void* y, const void* W, double scale,
+                                   const void* grad_out, const void* mid, void* grad_x,
+                                   void* grad_y, void* grad_W, void* workspace,
+                                   size_t workspace_bytes, cgtp_stream stream);
+
 /* --------------------------------------------------- radial network ---- */
 /* Per-edge tensor-product weights from the radial network: the radial profile
  * of a TFN layer is a fully connected network of the edge length (NVIDIA
@@ -424,7 +502,11 @@ cgtp_status cgtp_radial_workspace(cgtp_dtype dtype, int n_basis, int hidden, int
  * be set) added in fixed order, so results are deterministic.  Same size
  * limits as the forward.  gh = grad_w W2^T runs on the tensor cores (TF32
  * split products, fp32 accuracy) when the forward's tensor-core conditions
- * hold and flags lacks CGTP_RADIAL_CUDA_CORES; grad_W2 on the CUDA cores.
+ * hold and flags lacks CGTP_RADIAL_CUDA_CORES.  grad_W2 = h^T grad_w runs on
+ * the tensor cores too (the same split products, partial sums over 256-row
+ * segments added in fp32) for fp32 with hidden a multiple of 32 up to 128,
+ * n_out a multiple of 128 up to 16384, at most 16 basis functions, a 16-byte
+ * aligned grad_w and no CGTP_RADIAL_CUDA_CORES; otherwise on the CUDA cores.
  * Asynchronous on `stream`; allocates nothing. */
 cgtp_status cgtp_radial_backward(cgtp_dtype dtype, int64_t E, int n_basis, double cutoff,
                                  int hidden, int64_t n_out, const void* vec, const void* W1,
@@ -452,6 +534,19 @@ cgtp_status cgtp_last_cuda_error(int* cuda_err);
 const char* cgtp_last_error_message(void);
 /* Number of kernel launches this process has issued through the library. */
 int64_t cgtp_launch_count(void);
+
+/* Measurement support (the pages have no counterpart): the roofline of the
+ * CUDA-core kernels takes the FMA-pipe throughput of the device as its peak,
+ * and this probe measures it instead of deriving it from unit counts.  Launches
+ * `blocks` CTAs of `threads` threads (a multiple of 32, at most 1024); each
+ * thread runs 8 independent chains of `iters` dependent fused multiply-adds in
+ * `dtype` (packed = 1: fp32 pairs, one fma.rn.f32x2 per step) and stores one
+ * 8-byte word to sink[blockIdx * threads + threadIdx] (device, caller-owned,
+ * 8-byte aligned, blocks * threads words).  *flops (optional, host) receives the
+ * floating-point operations the launch performs (2 per FMA).  Asynchronous on
+ * `stream`: time it with events on that stream.  CGTP_E_ARG on bad sizes. */
+cgtp_status cgtp_fma_probe(cgtp_dtype dtype, int packed, int64_t blocks, int threads,
+                           int64_t iters, void* sink, int64_t* flops, cgtp_stream stream);
 
 #ifdef __cplusplus
 }

@@ -241,3 +241,63 @@ def test_linear_layer_host_side():
         cg.Linear("4x0e", "4x0e", instr=[(0, 1)])
     with pytest.raises(cg.CgtpError):
         cg.Linear("4x0q", "4x0e")
+
+
+def test_noalloc_entry_point_host_errors():
+    """The no-allocation gradient rejects, before any CUDA call, a plan whose
+    kernels never ran (their first load allocates) and a shared weight row
+    too large for the fixed scratch (64 KiB at most)."""
+    L = cg.lib()
+    vp = ctypes.c_void_p
+    f = L.cgtp_conv_backward_noalloc
+    f.argtypes = [vp, ctypes.c_int64, ctypes.c_int64, vp, vp, vp, vp, vp, vp, vp, vp,
+                  ctypes.c_double, vp, vp, vp, vp, vp]
+    f.restype = ctypes.c_int
+    a = vp(0x1000)
+    args = lambda plan: (plan._h, 3, 4, a, a, a, a, a, a, a, a, 1.0, a, a, a, a, None)
+    fresh = cg.Plan(*W.IRREPS_CONV64)
+    assert f(*args(fresh)) == 1
+    assert b"have not run" in L.cgtp_last_error_message()
+    fresh_shared = cg.Plan(*W.IRREPS_CONV64, shared_weights=True)
+    assert f(*args(fresh_shared)) == 1
+    assert b"have not run" in L.cgtp_last_error_message()
+    # 24 paths x 1024 channels x 4 bytes = 96 KiB per weight row
+    big = cg.Plan("1024x0e+1024x1o+1024x2e", "0e+1o+2e+3o",
+                  "1024x0e+1024x1o+1024x1e+1024x2o+1024x2e+1024x3o+1024x3e", shared_weights=True)
+    assert big.weight_numel * 4 > 64 * 1024
+    assert f(*args(big)) == 1
+    assert b"no-allocation limit" in L.cgtp_last_error_message()
+    # the same row without a weight gradient needs no scratch: the size check passes
+    no_gw = (big._h, 3, 4, a, a, a, a, a, a, a, a, 1.0, a, a, a, None, None)
+    assert f(*no_gw) == 1
+    assert b"have not run" in L.cgtp_last_error_message()
+    assert f(None, 3, 4, a, a, a, a, a, a, a, a, 1.0, a, a, a, a, None) == 1
+
+
+def test_uvw_product_host_side():
+    """The 'uvw' product's path list (planner) is the oracle's parity-allowed
+    list, its matrices lie one after another, and bad arguments are refused
+    before any CUDA call."""
+    a, b, c = "16x0e+16x1o+16x2e", "0e+1o+2e+3o", "8x0e+8x1o+8x1e+8x2o+8x2e"
+    u = cg.UVWProduct(a, b, c)
+    ref = O.make_problem(a, b, c.replace("8x", "16x"))
+    assert u.n_paths == len(ref.paths)
+    for p, q in enumerate(ref.paths):
+        l1, l2, l3, i1, i2, io, off = u.path(p)
+        assert (i1, i2, io, l1, l2, l3) == q[:6]
+        assert off == p * 16 * 8
+    assert u.weight_numel == u.n_paths * 16 * 8
+    assert u.dim_in1 == 16 * 9 and u.dim_in2 == 16 and u.dim_out == 8 * (1 + 3 + 3 + 5 + 5)
+    assert u.dim_mid == 16 * sum(2 * q[5] + 1 for q in ref.paths)
+    f, bwd = u.workspace_bytes(1000)
+    assert f >= 1000 * u.dim_mid * 4 and bwd >= 2 * 1000 * u.dim_mid * 4
+    L = cg.lib()
+    h = ctypes.c_void_p()
+    assert L.cgtp_uvw_create(ctypes.byref(h), b"16x0e+8x1o", b"0e", b"16x0e", 0) == 2
+    assert L.cgtp_uvw_create(ctypes.byref(h), b"16x0e", b"2x0e", b"16x0e", 0) == 2
+    assert L.cgtp_uvw_create(ctypes.byref(h), b"16x0e", b"0e", b"16x1o", 0) == 3
+    assert L.cgtp_uvw_create(None, b"16x0e", b"0e", b"16x0e", 0) == 1
+    null = ctypes.c_void_p()
+    # a workspace that is missing or too small is refused
+    assert L.cgtp_uvw_forward(u._h, 4, null, null, null, null, null, null, 0, null) == 1
+    assert b"workspace" in L.cgtp_last_error_message()
