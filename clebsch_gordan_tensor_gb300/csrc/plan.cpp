@@ -549,6 +549,7 @@ void Plan::gen_groups(std::ostringstream& g, const std::vector<int>& k0, bool f6
         g << "  }\n};\n\n";
     }
     // --------------------------------------------------------------- backward
+    const int nyp_ = next_pow2(std::max(1, ny));
     g << "template <int GRP> struct BwdG;\n";
     for (size_t gi = 0; gi < bwd_groups.size(); ++gi) {
         // paths ordered by output block so one block's grad-output pairs are
@@ -570,10 +571,15 @@ void Plan::gen_groups(std::ostringstream& g, const std::vector<int>& k0, bool f6
         // grad_y partials of path q: per T entry the two-channel dot of (w x) and
         // g (or x and (w g), whichever needs fewer products), spread over its CG
         // terms into the lane's per-y-element sums
-        auto emit_gy = [&](int q) {
+        // flag bit 29: odd paths add into a second set of partials (gyl[NYP +
+        // i]), halving the dependent chains; bit 30: a path's dots are all
+        // formed before their CG terms are spread
+        const bool gy_split = (flags >> 29) & 1u, dots_first = (flags >> 30) & 1u;
+        auto emit_gy = [&](int q, int slot) {
             const Path& P = paths[q];
             const int d1 = 2 * P.l1 + 1, d3 = 2 * P.l3 + 1;
             const bool zx = d1 <= d3;
+            const int gofs = gy_split && (slot & 1) ? nyp_ : 0;
             if (zx) {
                 for (int a = 0; a < d1; ++a)
                     g << "      const VR z" << a << " = vmul(w, xr[" << xi[P.r1 + a] << "]);\n";
@@ -581,17 +587,29 @@ void Plan::gen_groups(std::ostringstream& g, const std::vector<int>& k0, bool f6
                 for (int c = 0; c < d3; ++c)
                     g << "      const VR z" << c << " = vmul(w, G(" << P.r3 + c << "));\n";
             }
-            for (int k = k0[q]; k < k0[q + 1]; ++k) {
-                const TEntry& t = T[k];
+            auto dot = [&](const TEntry& t) {
                 const std::string lhs =
                     zx ? "z" + std::to_string(t.m1) : "xr[" + std::to_string(xi[P.r1 + t.m1]) + "]";
                 const std::string rhs =
                     zx ? "G(" + std::to_string(P.r3 + t.m3) + ")" : "z" + std::to_string(t.m3);
-                g << "      { const REAL d = vdot(" << lhs << ", " << rhs << ");\n";
+                return "vdot(" + lhs + ", " + rhs + ")";
+            };
+            auto spread = [&](const TEntry& t, const std::string& d, const char* ind) {
                 for (auto& term : t.terms)
-                    g << "        gyl[" << term.first << "] = fma(" << lit(term.second, f64)
-                      << ", d, gyl[" << term.first << "]);\n";
-                g << "      }\n";
+                    g << ind << "gyl[" << term.first + gofs << "] = fma(" << lit(term.second, f64)
+                      << ", " << d << ", gyl[" << term.first + gofs << "]);\n";
+            };
+            if (dots_first) {
+                for (int k = k0[q]; k < k0[q + 1]; ++k)
+                    g << "      const REAL d" << k - k0[q] << " = " << dot(T[k]) << ";\n";
+                for (int k = k0[q]; k < k0[q + 1]; ++k)
+                    spread(T[k], "d" + std::to_string(k - k0[q]), "      ");
+            } else {
+                for (int k = k0[q]; k < k0[q + 1]; ++k) {
+                    g << "      { const REAL d = " << dot(T[k]) << ";\n";
+                    spread(T[k], "d", "        ");
+                    g << "      }\n";
+                }
             }
         };
         g << "template <> struct BwdG<" << gi << "> {\n  static constexpr int NXR = "
@@ -608,7 +626,7 @@ void Plan::gen_groups(std::ostringstream& g, const std::vector<int>& k0, bool f6
         // FIX: grad_x and grad_w are both written (mode 1), so the stream has no
         // run-time branch and the whole edge is one block for the scheduler
         g << "  template <bool GY, bool FIX, class FG, class FW>\n  __device__ static __forceinline__ void edge("
-             "VR (&gxa)[NXR], REAL (&gyl)[NYP], const REAL* __restrict__ Ts, const VR (&xr)[NXR],\n"
+             "VR (&gxa)[NXR], REAL (&gyl)[NYP * GYS], const REAL* __restrict__ Ts, const VR (&xr)[NXR],\n"
              "      FG&& G, FW&& W, REAL* __restrict__ gwrow, VR (&gwa)[NP], int ch, VR sc, bool dogx,\n"
              "      int mgw) {\n";
         // flag bit 27 (T_DUP_B) stores the backward's T entries as splatted pairs
@@ -651,19 +669,19 @@ void Plan::gen_groups(std::ostringstream& g, const std::vector<int>& k0, bool f6
                 if (hs[a]) g << "      s = vfma(xr[" << xi[P.r1 + a] << "], h" << a << ", s);\n";
             g << "      GWOUT_M(" << q << ", s, FIX ? 1 : mgw);\n    }\n";
             g << "    if (GY) {\n";
-            emit_gy(q);
+            emit_gy(q, wi[q]);
             g << "    }\n    }\n";
         }
         g << "  }\n";
         // grad_y alone (the CG coefficients are immediates: no T, no y), for
         // the CTA's grad-y warp
         g << "  template <class FG, class FW>\n  __device__ static __forceinline__ void edge_gy("
-             "REAL (&gyl)[NYP], const VR (&xr)[NXR], FG&& G, FW&& W) {\n";
+             "REAL (&gyl)[NYP * GYS], const VR (&xr)[NXR], FG&& G, FW&& W) {\n";
         for (int q : P_) {
             const Path& P = paths[q];
             g << "    { // path " << q << ": " << P.l1 << " x " << P.l2 << " -> " << P.l3 << "\n";
             g << "    const VR w = W(" << wi[q] << ", " << q << ");\n";
-            emit_gy(q);
+            emit_gy(q, wi[q]);
             g << "    }\n";
         }
         g << "  }\n";
@@ -713,6 +731,7 @@ std::string Plan::kernel_source() const {
        << "\n#define MINB_B " << minb_b << "\n#define GYW " << (gy_warp ? 1 : 0)
        << "\n#define TEST_WAIT0 " << (test_wait0 ? 1 : 0)
        << "\n#define W_ALT " << (((flags >> 28) & 1u) ? 1 : 0)
+       << "\n#define GYS " << (((flags >> 29) & 1u) ? 2 : 1)
        << "\n#define GF " << std::max<size_t>(1, fwd_groups.size()) << "\n#define GB "
        << std::max<size_t>(1, bwd_groups.size()) << "\n";
     // T tables

@@ -26,9 +26,13 @@ __global__ void __launch_bounds__(1024) fma_probe_kernel(int64_t iters, T a, T b
     T acc[kChains];
 #pragma unroll
     for (int i = 0; i < kChains; ++i) acc[i] = (T)(threadIdx.x + i) * (T)1e-3;
+    // the multiplicands in registers (the compiler cannot prove the offset is
+    // zero), as the tensor-product kernels have them
+    const T z = (T)(iters >> 62);
+    const T ar = a + z, br = b + z;
     for (int64_t it = 0; it < iters; ++it) {
 #pragma unroll
-        for (int i = 0; i < kChains; ++i) acc[i] = fma(acc[i], a, b);
+        for (int i = 0; i < kChains; ++i) acc[i] = fma(acc[i], ar, br);
     }
     T s = 0;
 #pragma unroll
@@ -45,7 +49,8 @@ __global__ void __launch_bounds__(1024) fma_probe_kernel(int64_t iters, T a, T b
 __global__ void __launch_bounds__(1024) fma_probe_f32x2_kernel(int64_t iters, float a, float b,
                                                                unsigned long long* sink) {
     typedef unsigned long long u64;
-    const u64 ua = __float_as_uint(a), ub = __float_as_uint(b);
+    const float z = (float)(iters >> 62);
+    const u64 ua = __float_as_uint(a + z), ub = __float_as_uint(b + z);
     const u64 pa = (ua << 32) | ua, pb = (ub << 32) | ub;
     u64 acc[kChains];
 #pragma unroll

@@ -995,9 +995,9 @@ __device__ __forceinline__ void bwd_group(const BwdArgs& A, const BwdShared& S, 
                 return;
             }
             const REAL* gs = reinterpret_cast<const REAL*>(st + WSB);
-            REAL gyl[NYP];
+            REAL gyl[NYP * GYS];  // GYS == 2: odd paths use the second half
 #pragma unroll
-            for (int i = 0; i < NYP; ++i) gyl[i] = (REAL)0;
+            for (int i = 0; i < NYP * GYS; ++i) gyl[i] = (REAL)0;
             REAL* gwrow = A.gw ? A.gw + e * WDIM : nullptr;
 #if W_DIRECT_B
             long long e1 = e;
@@ -1045,6 +1045,9 @@ __device__ __forceinline__ void bwd_group(const BwdArgs& A, const BwdShared& S, 
                                   ch, sc, A.mgx != 0, A.mgw);
 #endif
             if (GY && A.mgy) {
+                if (GYS == 2)
+#pragma unroll
+                    for (int i = 0; i < NYP; ++i) gyl[i] += gyl[NYP * (GYS - 1) + i];
                 int base = 0;
                 bool owner = true;
                 seg_reduce<16, NYP>(gyl, lane, 0xffffffffu, base, owner);
@@ -1137,9 +1140,9 @@ __device__ __forceinline__ void bwd_gy_role(const BwdArgs& A, const BwdShared& S
             }
             if (dogy) {
                 const REAL* gs = reinterpret_cast<const REAL*>(st + WSB);
-                REAL gyl[NYP];
+                REAL gyl[NYP * GYS];
 #pragma unroll
-                for (int i = 0; i < NYP; ++i) gyl[i] = (REAL)0;
+                for (int i = 0; i < NYP * GYS; ++i) gyl[i] = (REAL)0;
 #if W_DIRECT_B
                 long long en = e;
                 if (j + 1 < S.j_end) {
@@ -1174,6 +1177,9 @@ __device__ __forceinline__ void bwd_gy_role(const BwdArgs& A, const BwdShared& S
                 BG::edge_gy(gyl, xr, [&](int r) { return lds_v(gs + r * MUL, ch); },
                             [&](int, int q) { return lds_w(ws + q * MUL, ch); });
 #endif
+                if (GYS == 2)
+#pragma unroll
+                    for (int i = 0; i < NYP; ++i) gyl[i] += gyl[NYP * (GYS - 1) + i];
                 int base = 0;
                 bool owner = true;
                 seg_reduce<16, NYP>(gyl, lane, 0xffffffffu, base, owner);
