@@ -502,9 +502,13 @@ def make_uvw(args, cg, W, torch):
     def mix_bwd_x():
         res["gmid"] = uvw.linear.backward(mid, Wm, g, need=(True, False), workspace=wsb)[0]
 
+    wsu = torch.empty(uvw.workspace_bytes(B)[0], dtype=torch.uint8, device="cuda")
+    # forward: the fused kernel (per-path blocks computed inside the mixing);
+    # the gradient recomputes the blocks it needs (tp_paths) and runs the
+    # mixing's two gradients and the per-path gradient
     kernels = [("sh_fwd", lambda: cg.sh_forward(vec, 3, out=y)),
+               ("uvw_fwd", lambda: uvw.forward(x, y, Wm, out=out, workspace=wsu)),
                ("tp_paths", lambda: uvw.plan.forward(x, y, ones, out=mid)),
-               ("linear", lambda: uvw.linear.forward(mid, Wm, out=out, workspace=ws)),
                ("linear_bwd_x", mix_bwd_x),
                ("linear_bwd_w", lambda: uvw.linear.backward(mid, Wm, g, need=(False, True),
                                                             workspace=wsb)),
@@ -518,18 +522,19 @@ def make_uvw(args, cg, W, torch):
     mix_flops = 2 * B * mix * 128 * 128
     counts = {"sh_fwd": (B * (3 + d.dim2) * 4, None),
               "tp_paths": (B * (d.dim1 + d.dim2 + d.dimo) * 4 + d.wdim * 4, B * d.flops),
-              "linear": (B * (uvw.dim_mid + uvw.dim_out) * 4 + uvw.weight_numel * 4, mix_flops,
-                         "tensor3"),
+              "uvw_fwd": (B * (d.dim1 + d.dim2 + uvw.dim_out) * 4 + uvw.weight_numel * 4,
+                          mix_flops, "tensor3"),
               "linear_bwd_x": (B * (uvw.dim_mid + uvw.dim_out) * 4 + uvw.weight_numel * 4,
                                mix_flops, "tensor3"),
               "linear_bwd_w": (B * (uvw.dim_mid + uvw.dim_out) * 4 + uvw.weight_numel * 4,
                                mix_flops, "tensor3"),
               "tp_paths_bwd": (B * (2 * d.dim1 + 2 * d.dim2 + d.dimo) * 4, 2 * B * d.flops)}
     desc = (f"'uvw' CG-TP: B={B}, 128x(0e,1o,2e) (x) Y(l<=3) -> 128x(0e,1o,1e,2o,2e,3o,3e), "
-            "24 paths, one shared 128x128 matrix per path, fp32, forward and gradient (channel "
-            "mixing and its x-gradient on tcgen05, TF32 split in three products)")
+            "24 paths, one shared 128x128 matrix per path, fp32, forward (fused: per-path blocks "
+            "computed inside the tcgen05 channel mixing) and gradient (blocks recomputed, mixing "
+            "gradients on tcgen05, TF32 split in three products)")
     return Workload("uvw", desc, B, "samples/s", "f32", kernels, counts,
-                    ["sh_fwd", "tp_paths", "linear"], dict(B=B, mul=128, paths=uvw.n_paths),
+                    ["sh_fwd", "uvw_fwd"], dict(B=B, mul=128, paths=uvw.n_paths),
                     None, None)
 
 

@@ -1081,6 +1081,8 @@ int64_t plan_weight_row_bytes(cgtp_plan plan) {
 
 bool plan_shared_weights(cgtp_plan plan) { return plan && plan->p.wmode == CGTP_W_SHARED; }
 
+LinearImpl* cgtp_linear_impl(cgtp_linear lin) { return lin ? lin->L : nullptr; }
+
 cgtp_status plan_preload_kernels(cgtp_plan plan, int dev) {
     if (!plan) return fail(CGTP_E_ARG, "plan is NULL");
     std::lock_guard<std::mutex> g(plan->p.mu);

@@ -72,10 +72,40 @@ cudaError_t launch_radial_backward(bool f64, bool tensor_cores, int64_t E, int n
 
 // Per-irrep channel mixing (linear.cu).
 struct LinearImpl;
+
+// Tensor-product source of a mixing layer's input rows (the fused 'uvw'
+// forward): input irrep p of the layer is path p's block of the 'uvu' product
+// with unit weights,
+//   a[n, p, m3, u] = sum_m1 T[n, p, m3, m1] x1[n, x1_off + m1 mul1 + u],
+//   T[n, p, m3, m1] = sum_m2 C_p[m1, m2, m3] y[n, m2],
+// so the layer's input rows are computed where they are consumed.  T is
+// channel-independent and small (one row of tdim values per sample, path p's
+// [d3][d1] block at t_off); entry e of a T row sums the CG terms
+// [estart[e], estart[e + 1]).  Passed by value as a kernel parameter.
+constexpr int kTpMaxPaths = 64, kTpMaxT = 1024, kTpMaxTerms = 2048;
+struct LinTpPath {
+    int x1_off, mul1, t_off, d1, d3;
+};
+struct LinTpDesc {
+    int npaths = 0, nterms = 0, tdim = 0;
+    LinTpPath path[kTpMaxPaths];
+    short estart[kTpMaxT + 1];
+    unsigned char term_y[kTpMaxTerms];  // y element of the term
+    float term_c[kTpMaxTerms];
+};
+// The fused forward: T for every sample into tbuf (n * tdim floats), then out =
+// the layer applied to the rows described by tp (x1 [n, x1_stride], y [n,
+// y_stride]).  *used = false when it is not eligible (nothing is launched).
+cudaError_t launch_linear_forward_tp(const LinearImpl* L, const LinTpDesc& tp, int64_t n,
+                                     const void* x1, int64_t x1_stride, const void* y,
+                                     int64_t y_stride, const void* W, void* out, void* ws,
+                                     size_t ws_bytes, void* tbuf, size_t tbuf_bytes,
+                                     cudaStream_t s, bool* used);
 cgtp_status linear_create(const char* irreps_in, const char* irreps_out,
                           const cgtp_linear_instr* instr, int n_instr, cgtp_dtype dt,
                           LinearImpl** res, std::string& err);
 void linear_destroy(LinearImpl* L);
+LinearImpl* cgtp_linear_impl(cgtp_linear lin);
 void linear_info(const LinearImpl* L, int64_t* dim_in, int64_t* dim_out, int64_t* nw, int* ninstr);
 bool linear_instruction(const LinearImpl* L, int j, int* i_in, int* i_out, int64_t* w_off);
 bool linear_tensor_cores(const LinearImpl* L);

@@ -54,6 +54,7 @@ struct LinBlock {
 // packed tensor-core image of the chunk starts at byte img_off.
 struct LinChunk {
     int a_off, a_mul, k0, kc, w_off, w_ks, w_ns, img_off;
+    int src;  // source irrep of the chunk (its path, for a tensor-product source)
 };
 
 constexpr int kLinMaxBlocks = 32;
@@ -241,11 +242,23 @@ constexpr unsigned kLtStagePitch = 36;  // floats per staged epilogue row (confl
 __host__ __device__ constexpr unsigned lt_stage_pitch(int nmax, bool wide) {
     return wide ? (unsigned)nmax + 4 : kLtStagePitch;
 }
-__host__ __device__ constexpr unsigned lt_smem_bytes(int nmax, int RB, bool wide) {
+__host__ __device__ constexpr unsigned lt_smem_bytes(int nmax, int RB, bool wide, bool tpa = false) {
     return (unsigned)RB * 2u * (unsigned)nmax * kLtK * 4 +
            kLtEpiWarps * 32 * lt_stage_pitch(nmax, wide) * 4 +
-           (unsigned)((kLinMaxBlocks + 1) * sizeof(LinBlock) + kLinMaxChunks * sizeof(LinChunk));
+           (unsigned)((kLinMaxBlocks + 1) * sizeof(LinBlock) + kLinMaxChunks * sizeof(LinChunk)) +
+           (tpa ? (unsigned)sizeof(LinTpDesc) : 0u);
 }
+
+// Kernel argument of the tensor-product source (empty without one).
+template <bool TPA>
+struct TpArg {};
+template <>
+struct TpArg<true> {
+    LinTpDesc d;
+    const float* x1;
+    int64_t x1_stride;
+    const float* t;  // T rows, tdim floats per sample
+};
 
 // Bounded wait that sleeps between polls (about a second at most): for the
 // producer and epilogue warps, whose polling would otherwise compete with the
@@ -352,11 +365,19 @@ __global__ void linear_pack_kernel(const __grid_constant__ LinDesc D, const floa
 // (t / NACC) % 2 of acc_full / acc_free.  Every wait is bounded; after a
 // timeout the remaining waits return at once, each role leaves its loop, and
 // the loader drains the copies it started.
-template <int S, int NACC, bool STACK>
-__global__ void __launch_bounds__(kLtThreads, 1)
+//
+// TPD > 0 (the fused 'uvw' forward): the producers compute their rows from
+// the tensor-product source instead of loading them.  For row (n, m3) and a
+// chunk of path p's block: sum over m1 < d1 (at most TPD) of the T entry
+// T[n, p, m3, m1] (precomputed per sample by lin_tp_t_kernel) times the 16
+// channels of x1[n, m1].  The path table is copied to shared memory with the
+// others.
+template <int S, int NACC, bool STACK, int TPD>
+__global__ void __launch_bounds__(kLtThreads, 1)  // 128 registers: 4 of the 14 warps share a sub-partition
 linear_tc_kernel(const __grid_constant__ LinDesc D, int64_t n, int nmax,
                  const float* __restrict__ x, const unsigned char* __restrict__ img,
-                 float* __restrict__ out) {
+                 float* __restrict__ out, const __grid_constant__ TpArg<(TPD > 0)> tp) {
+    constexpr bool TPA = TPD > 0;
     constexpr int RA = S;
     constexpr int RB = S;
     constexpr unsigned accw = 256 / NACC;  // columns per accumulator
@@ -376,6 +397,12 @@ linear_tc_kernel(const __grid_constant__ LinDesc D, int64_t n, int nmax,
     LinChunk* sch = reinterpret_cast<LinChunk*>(sblk + kLinMaxBlocks + 1);
     for (int i = tid; i <= D.nblocks; i += kLtThreads) sblk[i] = D.blk[i];
     for (int i = tid; i < D.nchunks; i += kLtThreads) sch[i] = D.ch[i];
+    LinTpDesc* stp = reinterpret_cast<LinTpDesc*>(sch + kLinMaxChunks);
+    if constexpr (TPA) {
+        const int* src = reinterpret_cast<const int*>(&tp.d);
+        int* dst = reinterpret_cast<int*>(stp);
+        for (int i = tid; i < (int)(sizeof(LinTpDesc) / 4); i += kLtThreads) dst[i] = src[i];
+    }
     const int nblocks = D.nblocks;
     const int64_t in_stride = D.in_stride, out_stride = D.out_stride;
 
@@ -475,7 +502,7 @@ linear_tc_kernel(const __grid_constant__ LinDesc D, int64_t n, int nmax,
                 if (R < n * B.d) {
                     const int64_t item = row_item(R, B.d);
                     rm = (int)(R - item * B.d);
-                    rbase = item * in_stride;
+                    rbase = TPA ? item : item * in_stride;
                 }
             }
             if (rm < 0) return;
@@ -486,11 +513,9 @@ linear_tc_kernel(const __grid_constant__ LinDesc D, int64_t n, int nmax,
         };
         Pos pre = start, cur = start;
         bool stop = false;
-        // chunk k: load chunk k + 3 into `nxt`, then write chunk k (in `v`)
-        auto step = [&](int64_t k, float4 (&v)[4], float4 (&nxt)[4]) {
+        // write chunk k's values into its stage once the stage is empty
+        auto put = [&](int64_t k, const float4 (&v)[4]) {
             const int s = (int)(k % RA);
-            load(pre, nxt);
-            if (pre.valid) advance(pre);
             if (k >= S && !wait(&empty[s], (unsigned)(((k - S) / S) & 1))) {
                 stop = true;
                 return;
@@ -516,23 +541,84 @@ linear_tc_kernel(const __grid_constant__ LinDesc D, int64_t n, int nmax,
             advance(cur);
             if (*(volatile int*)&fail) stop = true;
         };
-        // four register buffers taken in rotation by name (a copy between
-        // them would wait for the load just issued)
-        float4 b0[4], b1[4], b2[4], b3[4];
-        load(pre, b0);
-        if (pre.valid) advance(pre);
-        load(pre, b1);
-        if (pre.valid) advance(pre);
-        load(pre, b2);
-        if (pre.valid) advance(pre);
-        for (int64_t k = 0; cur.valid && !stop; k += 4) {
-            step(k, b0, b3);
-            if (!cur.valid || stop) break;
-            step(k + 1, b1, b0);
-            if (!cur.valid || stop) break;
-            step(k + 2, b2, b1);
-            if (!cur.valid || stop) break;
-            step(k + 3, b3, b2);
+        // chunk k: load chunk k + 3 into `nxt`, then write chunk k (in `v`)
+        auto step = [&](int64_t k, float4 (&v)[4], float4 (&nxt)[4]) {
+            load(pre, nxt);
+            if (pre.valid) advance(pre);
+            put(k, v);
+        };
+        if constexpr (TPA) {
+            // rows computed from the tensor-product source: for the row's
+            // (n, m3) and the chunk's path p, the T entries of m1 < d1 (at most
+            // TPD) and the 16 channels of x1[n, m1], all loads independent,
+            // then the sums; each chunk when its stage comes (the eight
+            // producer warps build one chunk together)
+            constexpr int G = TPD > 0 ? TPD : 1;
+            auto load_tp = [&](const Pos& p, float4 (&v)[4]) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (!p.valid) return;
+                const LinBlock& B = sblk[p.b];
+                const LinChunk& C = chunk_of(p);
+                if (p.u != row_u) {
+                    row_u = p.u;
+                    const int64_t R = p.t * kLtM + r;
+                    rm = -1;
+                    if (R < n * B.d) {
+                        const int64_t item = row_item(R, B.d);
+                        rm = (int)(R - item * B.d);
+                        rbase = item;
+                    }
+                }
+                if (rm < 0) return;
+                const LinTpPath& P = stp->path[C.src];
+                const float* xr = tp.x1 + rbase * tp.x1_stride + P.x1_off + C.k0 + 16 * h;
+                const float* tr = tp.t + rbase * stp->tdim + P.t_off + rm * P.d1;
+                float tv[G];
+                float4 a[G][4];
+#pragma unroll
+                for (int g = 0; g < G; ++g)
+                    if (g < P.d1) {
+                        tv[g] = __ldg(tr + g);
+                        const float4* xs = reinterpret_cast<const float4*>(xr + (int64_t)g * P.mul1);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) a[g][j] = __ldg(xs + j);
+                    }
+#pragma unroll
+                for (int g = 0; g < G; ++g)
+                    if (g < P.d1)
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            v[j].x = fmaf(tv[g], a[g][j].x, v[j].x);
+                            v[j].y = fmaf(tv[g], a[g][j].y, v[j].y);
+                            v[j].z = fmaf(tv[g], a[g][j].z, v[j].z);
+                            v[j].w = fmaf(tv[g], a[g][j].w, v[j].w);
+                        }
+            };
+            for (int64_t k = 0; cur.valid && !stop; ++k) {
+                float4 v[4];
+                load_tp(cur, v);
+                put(k, v);
+            }
+        } else {
+            // four register buffers taken in rotation by name (a copy between
+            // them would wait for the load just issued)
+            float4 b0[4], b1[4], b2[4], b3[4];
+            load(pre, b0);
+            if (pre.valid) advance(pre);
+            load(pre, b1);
+            if (pre.valid) advance(pre);
+            load(pre, b2);
+            if (pre.valid) advance(pre);
+            for (int64_t k = 0; cur.valid && !stop; k += 4) {
+                step(k, b0, b3);
+                if (!cur.valid || stop) break;
+                step(k + 1, b1, b0);
+                if (!cur.valid || stop) break;
+                step(k + 2, b2, b1);
+                if (!cur.valid || stop) break;
+                step(k + 3, b3, b2);
+            }
         }
     } else if (loader) {
         // ------------------------------------------------------------- loader
@@ -1084,6 +1170,7 @@ static bool build_pass(LinearImpl& L, bool fwd, std::string& err) {
                     return false;
                 }
                 LinChunk& C = D.ch[D.nchunks++];
+                C.src = src;
                 C.a_off = fwd ? L.off_in[src] : L.off_out[src];
                 C.a_mul = ksrc;
                 C.k0 = k0;
@@ -1285,12 +1372,12 @@ static cudaError_t run_pass(const LinearImpl& L, const LinDesc& D, int nmax, siz
     // stages (A in tensor memory, B in shared memory): 4 up to 128 columns, 3 at 256
     const size_t smem = std::max<size_t>(
         120 * 1024, stack ? lt_smem_bytes(nmax, 4, true) : lt_smem_bytes(nmax, 3, false));
-    auto* kern = stack ? linear_tc_kernel<4, 1, true> : linear_tc_kernel<3, 1, false>;
+    auto* kern = stack ? linear_tc_kernel<4, 1, true, 0> : linear_tc_kernel<3, 1, false, 0>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     (void)img_bytes;
     kern<<<grid, kLtThreads, smem, s>>>(*Dn, n, nmax, (const float*)a, (const unsigned char*)img,
-                                        (float*)out);
+                                        (float*)out, TpArg<false>{});
     count_launch();
     return cudaGetLastError();
 }
@@ -1311,6 +1398,91 @@ cudaError_t launch_linear_forward(const LinearImpl* L, int64_t n, const void* x,
     if (e != cudaSuccess) return e;
     const bool tc = allow_tc && linear_uses_tc(L, n, x, out, ws, ws_bytes, true);
     return run_pass(*L, L->fwd, L->fwd_nmax, L->fwd_img, n, x, W, out, ws, tc, s);
+}
+
+// T rows of the fused 'uvw' forward: t[n, e] = sum over entry e's CG terms of
+// c * y[n, term_y] (channel-independent).  One CTA per sample at a time, the
+// term table in shared memory.
+__global__ void __launch_bounds__(256)
+lin_tp_t_kernel(const __grid_constant__ LinTpDesc D, int64_t n, const float* __restrict__ y,
+                int64_t y_stride, float* __restrict__ t) {
+    __shared__ short es[kTpMaxT + 1];
+    __shared__ unsigned char ty[kTpMaxTerms];
+    __shared__ float tc[kTpMaxTerms];
+    for (int i = threadIdx.x; i <= D.tdim; i += blockDim.x) es[i] = D.estart[i];
+    for (int i = threadIdx.x; i < D.nterms; i += blockDim.x) {
+        ty[i] = D.term_y[i];
+        tc[i] = D.term_c[i];
+    }
+    __syncthreads();
+    for (int64_t item = blockIdx.x; item < n; item += gridDim.x) {
+        const float* yr = y + item * y_stride;
+        for (int e = threadIdx.x; e < D.tdim; e += blockDim.x) {
+            float a = 0.0f;
+            for (int k = es[e]; k < es[e + 1]; ++k) a = fmaf(tc[k], __ldg(yr + ty[k]), a);
+            t[item * D.tdim + e] = a;
+        }
+    }
+}
+
+cudaError_t launch_linear_forward_tp(const LinearImpl* L, const LinTpDesc& tp, int64_t n,
+                                     const void* x1, int64_t x1_stride, const void* y,
+                                     int64_t y_stride, const void* W, void* out, void* ws,
+                                     size_t ws_bytes, void* tbuf, size_t tbuf_bytes,
+                                     cudaStream_t s, bool* used) {
+    *used = false;
+    const LinDesc& D = L->fwd;
+    const int nmax = L->fwd_nmax;
+    // the stacked tensor-core shape (every output multiplicity <= 128), one
+    // source path per input irrep, 16-byte aligned x1 rows and channel groups
+    if (!L->tc || nmax > 128 || !ws || ws_bytes < L->fwd_img || !aligned16(ws) ||
+        !aligned16(x1) || !aligned16(out) || (x1_stride % 4) != 0 || ((uintptr_t)y & 3) != 0 ||
+        tp.npaths != (int)L->in.size() || tp.tdim <= 0 || tp.tdim > kTpMaxT ||
+        tp.nterms > kTpMaxTerms || !tbuf || ((uintptr_t)tbuf & 3) != 0 ||
+        tbuf_bytes < (size_t)n * tp.tdim * 4)
+        return cudaSuccess;
+    int groups = 1;  // m1 values of one row (d1), at most 7 here
+    for (int p = 0; p < tp.npaths; ++p) {
+        if (tp.path[p].x1_off % 4 != 0 || tp.path[p].mul1 % 4 != 0 ||
+            tp.path[p].mul1 != L->in[p].mul || tp.path[p].d3 != 2 * L->in[p].l + 1)
+            return cudaSuccess;
+        groups = std::max(groups, tp.path[p].d1);
+    }
+    if (groups > 7) return cudaSuccess;
+    *used = true;
+    cudaError_t e = zero_blocks(L->fwd_zero, n, L->dim_out, (float*)out, s);
+    if (e != cudaSuccess || D.nblocks == 0 || n == 0) return e;
+    const unsigned tg = (unsigned)std::max<int64_t>(1, std::min<int64_t>(n, 8 * sm_count()));
+    lin_tp_t_kernel<<<tg, 256, 0, s>>>(tp, n, (const float*)y, y_stride, (float*)tbuf);
+    count_launch();
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    linear_pack_kernel<<<(unsigned)D.nchunks, 256, 0, s>>>(D, (const float*)W, (unsigned char*)ws,
+                                                          true);
+    count_launch();
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    auto Dn = std::make_unique<LinDesc>(D);
+    int64_t units = 0;
+    for (int b = 0; b < D.nblocks; ++b) {
+        Dn->blk[b].tile0 = units;
+        units += (n * D.blk[b].d + kLtM - 1) / kLtM;
+    }
+    Dn->blk[D.nblocks].tile0 = units;
+    const unsigned grid = (unsigned)std::min<int64_t>(units, sm_count());
+    const size_t smem = std::max<size_t>(120 * 1024, lt_smem_bytes(nmax, 4, true, true));
+    auto* kern = groups <= 3 ? linear_tc_kernel<4, 1, true, 3>
+                             : groups <= 5 ? linear_tc_kernel<4, 1, true, 5>
+                                           : linear_tc_kernel<4, 1, true, 7>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    auto arg = std::make_unique<TpArg<true>>();
+    arg->d = tp;
+    arg->x1 = (const float*)x1;
+    arg->x1_stride = x1_stride;
+    arg->t = (const float*)tbuf;
+    kern<<<grid, kLtThreads, smem, s>>>(*Dn, n, nmax, nullptr, (const unsigned char*)ws,
+                                        (float*)out, *arg);
+    count_launch();
+    return cudaGetLastError();
 }
 
 // Accumulator buffers of the tensor-core weight gradient: two when every

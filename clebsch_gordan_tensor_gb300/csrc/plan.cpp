@@ -646,7 +646,11 @@ void Plan::gen_groups(std::ostringstream& g, const std::vector<int>& k0, bool f6
             std::vector<int> ks;
             for (int k = k0[q]; k < k0[q + 1]; ++k) ks.push_back(k);
             std::stable_sort(ks.begin(), ks.end(), [&](int a, int b) { return T[a].m3 < T[b].m3; });
-            for (int k = k0[q]; k < k0[q + 1]; ++k) L.get(k);  // load all T of the path first
+            // scalar entries: load all T of the path first (four per 128-bit
+            // load); splatted pairs are loaded where first used (two per load,
+            // twice the registers otherwise)
+            if (!tdup)
+                for (int k = k0[q]; k < k0[q + 1]; ++k) L.get(k);
             std::vector<bool> hs(d1, false);
             for (int k : ks) {
                 const std::string t = L.get(k);

@@ -32,6 +32,8 @@ struct cgtp_uvw_s {
     int64_t dim1 = 0, dim2 = 0, dimo = 0, dimmid = 0, wtp = 0, wnumel = 0;
     std::vector<std::array<int, 6>> paths;  // l1, l2, l3, i_in1, i_in2, i_out
     std::vector<int64_t> woff;              // offset of W_p in the weight vector
+    cgtp::LinTpDesc tp;                     // the paths as the mixing kernel's row source
+    bool tp_ok = false;                     // tp describes every path
 };
 
 namespace cgtp {
@@ -148,6 +150,46 @@ cgtp_status cgtp_uvw_create(cgtp_uvw* out, const char* irreps_in1, const char* i
         cgtp_linear_instruction(u->lin, j, &ii, &io, &off);
         u->woff.push_back(off);
     }
+    // the per-path blocks as a row source of the mixing kernel (fused forward):
+    // path p's T entries [d3][d1] at t_off of a T row, each with its CG terms
+    {
+        LinTpDesc& T = u->tp;
+        std::vector<int> x1off(a.size()), yoff(b.size());
+        int acc = 0;
+        for (size_t i = 0; i < a.size(); ++i) x1off[i] = acc, acc += a[i].mul * (2 * a[i].l + 1);
+        acc = 0;
+        for (size_t i = 0; i < b.size(); ++i) yoff[i] = acc, acc += 2 * b[i].l + 1;
+        bool ok = (int)u->paths.size() <= kTpMaxPaths && acc <= 255;
+        for (int p = 0; ok && p < (int)u->paths.size(); ++p) {
+            const auto& q = u->paths[p];
+            const int d1 = 2 * q[0] + 1, d2 = 2 * q[1] + 1, d3 = 2 * q[2] + 1;
+            if (T.tdim + d1 * d3 > kTpMaxT) {
+                ok = false;
+                break;
+            }
+            std::vector<double> cg((size_t)d1 * d2 * d3);
+            cgtp_plan_coefficients(u->plan, p, cg.data());
+            T.path[p] = LinTpPath{x1off[q[3]], mul, T.tdim, d1, d3};
+            for (int m3 = 0; m3 < d3 && ok; ++m3)
+                for (int m1 = 0; m1 < d1 && ok; ++m1) {
+                    T.estart[T.tdim++] = (short)T.nterms;
+                    for (int m2 = 0; m2 < d2; ++m2) {
+                        const double c = cg[((size_t)m1 * d2 + m2) * d3 + m3];
+                        if (c == 0.0) continue;
+                        if (T.nterms >= kTpMaxTerms) {
+                            ok = false;
+                            break;
+                        }
+                        T.term_y[T.nterms] = (unsigned char)(yoff[q[4]] + m2);
+                        T.term_c[T.nterms] = (float)c;
+                        ++T.nterms;
+                    }
+                }
+        }
+        T.estart[T.tdim] = (short)T.nterms;
+        T.npaths = (int)u->paths.size();
+        u->tp_ok = ok && dtype == CGTP_F32;
+    }
     *out = u.release();
     return CGTP_OK;
     UGUARD_END
@@ -212,6 +254,22 @@ static cgtp_status uvw_fwd(cgtp_uvw u, bool conv, int64_t rows, int64_t E, const
     UvwLayout L;
     cgtp_status st = uvw_ws_check(*u, rows, false, mid, ws, ws_bytes, L);
     if (st != CGTP_OK) return st;
+    if (!conv && !mid && u->tp_ok) {
+        // fused: the mixing kernel computes the per-path blocks where it reads
+        // them (no intermediate in HBM)
+        if (!x || !y || !W || !out) return ufail(CGTP_E_ARG, "NULL tensor");
+        bool used = false;
+        // the T rows take the place of the blocks in the workspace (mid region)
+        cudaError_t e = launch_linear_forward_tp(
+            cgtp_linear_impl(u->lin), u->tp, rows, x, u->dim1, y, u->dim2, W, out, at(ws, L.lin),
+            ws_bytes - L.lin, at(ws, L.mid), L.gmid - L.mid,
+            reinterpret_cast<cudaStream_t>(stream), &used);
+        if (e != cudaSuccess) {
+            set_cuda_error(e);
+            return ufail(CGTP_E_CUDA, std::string("uvw fused forward: ") + cudaGetErrorString(e));
+        }
+        if (used) return CGTP_OK;
+    }
     void* ones = at(ws, L.ones);
     void* m = mid ? mid : at(ws, L.mid);
     cudaError_t e = launch_fill_ones(u->dtype == CGTP_F64, ones, u->wtp,

@@ -206,3 +206,23 @@ def test_uvw_mixing_full_size():
                  "grad_x rows")
     assert_close(host(gW), float(s.sum()) * rW, np.float32, "grad_W")
     assert cg.linear_device_status() == 0
+
+
+def test_mace128_uvw_b200k_fused_forward_sampled():
+    """The fused 'uvw' forward at full size (200,000 samples, 24 paths of 128
+    channels into 128x(0e,1o,1e,2o,2e,3o,3e), the benchmark's call): every
+    output row computed on the GPU, sampled rows by the oracle."""
+    need_gpu()
+    cg = _cg()
+    cfg = W.mace128_uvw_b200k()
+    B = cfg["B"]
+    uvw = cg.UVWProduct(*W.IRREPS_MACE128)
+    x = dev(cfg["x"])
+    y = cg.sh_forward(dev(cfg["vec"]), 3)
+    out = uvw.forward(x, y, dev(cfg["W"]))
+    rng = np.random.default_rng(29)
+    idx = _sample(rng, B, 2000)
+    ti = torch.from_numpy(idx).cuda()
+    ref = O.tp_uvw_forward(*W.IRREPS_MACE128, cfg["x"][idx], host(y[ti]), cfg["W"])
+    assert_close(host(out[ti]), ref, np.float32, "uvw out rows")
+    assert cg.linear_device_status() == 0

@@ -104,6 +104,33 @@ def test_uvw_product_matches_oracle():
     assert_close(host(out), ref, np.float32, "uvw out")
 
 
+def test_uvw_fused_forward_matches_two_step_and_oracle():
+    """The fused forward (the mixing kernel's producers compute each path's
+    block from x and y) against the two-step forward (blocks written to an
+    intermediate, then mixed) and the oracle, on a ragged row count."""
+    need_gpu()
+    cg = _cg()
+    rng = np.random.default_rng(17)
+    B = 1037
+    uvw = cg.UVWProduct(*UVW_SMALL)
+    x = rng.standard_normal((B, uvw.dim_in1)).astype(np.float32)
+    v = rng.standard_normal((B, 3)).astype(np.float32)
+    W = (rng.standard_normal(uvw.weight_numel) / 16).astype(np.float32)
+    y = cg.sh_forward(dev(v), 3)
+    n0 = cg.launch_count()
+    fused = uvw.forward(dev(x), y, dev(W))
+    n1 = cg.launch_count()
+    mid = torch.empty(B, uvw.dim_mid, device="cuda")
+    two = uvw.forward(dev(x), y, dev(W), mid=mid)
+    n2 = cg.launch_count()
+    assert n1 - n0 == 3 and n2 - n1 == 4  # fused: T rows, weight pack, mixing; else unit row, blocks, pack, mixing
+    ref = O.tp_uvw_forward(*UVW_SMALL, x, host(y), W)
+    assert_close(host(fused), ref, np.float32, "fused uvw out")
+    assert_close(host(two), ref, np.float32, "two-step uvw out")
+    assert_close(host(fused), host(two), np.float32, "fused vs two-step")
+    assert cg.linear_device_status() == 0
+
+
 def test_uvw_backward_matches_oracle():
     need_gpu()
     cg = _cg()
