@@ -244,7 +244,7 @@ class Workload:
 
 
 def make_conv(args, cg, W, torch):
-    cfg = W.conv64_cloud10k(N=args.atoms)
+    cfg = W.conv64_cloud10k(N=args.atoms or 10_000)
     gr = cfg["graph"]
     N, E = gr.N, gr.E
     plan = cg.Plan(*cfg["irreps"])
@@ -347,7 +347,7 @@ def make_conv(args, cg, W, torch):
 
 
 def make_conv64(args, cg, W, torch):
-    cfg = W.conv128_f64_cloud5k()
+    cfg = W.conv128_f64_cloud5k(N=args.atoms or 5_000)
     gr = cfg["graph"]
     N, E = gr.N, gr.E
     plan = cg.Plan(*cfg["irreps"], dtype=torch.float64)
@@ -883,9 +883,9 @@ def main():
     ap.add_argument("--workload", default="conv", choices=sorted(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
-    ap.add_argument("--atoms", type=int, default=10_000,
-                    help="atom count of the conv workload (10000 is the benchmark; smaller "
-                         "for profiling)")
+    ap.add_argument("--atoms", type=int, default=None,
+                    help="atom count of the conv (10000) and conv64 (5000) workloads; smaller "
+                         "for profiling")
     ap.add_argument("--samples", type=int, default=200_000,
                     help="sample count of the tp and uvw workloads (200000 is the benchmark; "
                          "smaller for profiling)")

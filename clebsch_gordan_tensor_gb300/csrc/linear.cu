@@ -811,17 +811,23 @@ linear_tc_kernel(const __grid_constant__ LinDesc D, int64_t n, int nmax,
 //   epilogue (warps 0-3): per segment, wait acc_full, read D (lane u), add it
 //     to the unit's sums; after the last one store the partial row; arrive on
 //     acc_free.
-//   A producers (warps 4-7, lane quarter warp % 4): each thread loads its
-//     channel u of the chunk's 32 rows (one chunk ahead into registers), writes
-//     hi = the values and lo = round_tf32(x - x cut to 10 bits) with
-//     tcgen05.st once the stage is empty, and arrives on full.
-//   B producers (warps 8-15, output channel w = 32 (warp - 8) + lane): load w
-//     of the 32 rows, write four rows at a time into the K-major image (hi rows
-//     w, lo rows mul_out + w), fence to the async proxy, arrive on full.
+//   loader (warp 12): lane i starts the bulk copies of row i of chunk k (its
+//     128 x columns of the M tile and its g row) into staging stage k % 3 once
+//     the producers have released it (raw_empty), lane 0 announcing the bytes
+//     on raw_full.
+//   A producers (warps 4-7, lane quarter warp % 4): each thread reads its
+//     channel u of the chunk's 32 staged rows, releases the staging stage,
+//     writes hi = the values and lo = round_tf32(x - x cut to 10 bits) with
+//     tcgen05.st once the MMA stage is empty, and arrives on full.
+//   B producers (warps 8-11, output channel w = 32 (warp - 8) + lane): read w
+//     of the 32 staged rows, release the staging stage, write four rows at a
+//     time into the K-major image (hi rows w, lo rows mul_out + w), fence to
+//     the async proxy, arrive on full.  (Warps 13-15 have no role.)
 //   MMA issuer (warp 16): one wait per chunk, the products, commit to empty
 //     (and acc_full after a unit's last chunk).
-// Chunk k (counted over the CTA's units) uses stage k % 4 and phase (k / 4) % 2
-// of full / empty.  Precision: the tensor core's fp32 accumulator loses low
+// Chunk k (counted over the CTA's units) uses MMA stage k % 2 and phase
+// (k / 2) % 2 of full / empty, staging stage k % 3 and phase (k / 3) % 2 of
+// raw_full / raw_empty.  Precision: the tensor core's fp32 accumulator loses low
 // bits on every addition, so its error grows with the number of rows it sums.
 // A unit's chunks are therefore cut into segments; each segment starts a
 // fresh accumulator and the epilogue adds it, in plain fp32 arithmetic and
@@ -832,12 +838,19 @@ linear_tc_kernel(const __grid_constant__ LinDesc D, int64_t n, int nmax,
 // segments of kWgSeg chunks.  The t-th segment (counted over the CTA) uses
 // buffer t % nacc and phase (t / nacc) % 2 of acc_full / acc_free.
 // Waits are bounded as in the forward kernel.
-constexpr int kWgStages = 4;
+constexpr int kWgStages = 2;    // MMA stages: A in tensor memory, B image in shared memory
+constexpr int kWgRaw = 3;       // staging stages of the rows (bulk copies)
 constexpr int kWgThreads = 32 * 17;
 constexpr int kWgRows = 32;  // rows (K) per chunk
 constexpr int kWgSeg = 16;   // chunks (512 rows) per segment of a single buffer
-// dynamic shared memory: the stages, then the epilogue's sums [128 w][128 u]
-constexpr size_t kWgSmem = kWgStages * (size_t)(2 * 128 * kWgRows * 4) + 128 * 128 * 4;
+constexpr int kWgLoaderWarp = 12;
+// one staging stage: 32 rows of x (128 columns of the M tile) and of g (up to
+// 128 output channels)
+constexpr size_t kWgRawBytes = 2 * (size_t)kWgRows * 128 * 4;
+// dynamic shared memory: the MMA stages' B images, the epilogue's sums
+// [128 w][128 u], then the staging ring
+constexpr size_t kWgSmem = kWgStages * (size_t)(2 * 128 * kWgRows * 4) + 128 * 128 * 4 +
+                           kWgRaw * kWgRawBytes;
 
 __global__ void __launch_bounds__(kWgThreads, 1)
 linear_wgrad_tc_kernel(const __grid_constant__ LinGradDesc D, int64_t n, int64_t per, int S,
@@ -845,11 +858,13 @@ linear_wgrad_tc_kernel(const __grid_constant__ LinGradDesc D, int64_t n, int64_t
                        float* __restrict__ partial) {
     extern __shared__ __align__(1024) unsigned char smem[];
     __shared__ __align__(8) unsigned long long full[kWgStages], empty[kWgStages];
+    __shared__ __align__(8) unsigned long long raw_full[kWgRaw], raw_empty[kWgRaw];
     __shared__ __align__(8) unsigned long long acc_full[2], acc_free[2];
     __shared__ unsigned tmem_base;
     __shared__ int fail;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     constexpr unsigned bslot = 2u * 128 * kWgRows * 4;  // stacked image, mul_out <= 128
+    unsigned char* const raw0 = smem + kWgStages * (size_t)bslot + 128 * 128 * 4;
 
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -860,8 +875,12 @@ linear_wgrad_tc_kernel(const __grid_constant__ LinGradDesc D, int64_t n, int64_t
     }
     if (tid == 0) {
         for (int i = 0; i < kWgStages; ++i) {
-            tc_mbar_init(&full[i], 12);  // 4 A warps + 8 B warps
+            tc_mbar_init(&full[i], 8);  // 4 A warps + 4 B warps
             tc_mbar_init(&empty[i], 1);
+        }
+        for (int i = 0; i < kWgRaw; ++i) {
+            tc_mbar_init(&raw_full[i], 1);   // the loader's arrival with the byte count
+            tc_mbar_init(&raw_empty[i], 8);  // the producer warps
         }
         for (int i = 0; i < 2; ++i) {
             tc_mbar_init(&acc_full[i], 1);
@@ -875,10 +894,11 @@ linear_wgrad_tc_kernel(const __grid_constant__ LinGradDesc D, int64_t n, int64_t
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const unsigned tmem = tmem_base;
     const bool issuer = warp == 16;
+    const bool tight = issuer || warp == kWgLoaderWarp;  // these two poll without sleeping
     const int seg = nacc == 2 ? kWgSeg / 2 : kWgSeg;
     auto wait = [&](unsigned long long* bar, unsigned parity) -> bool {
         if (!issuer && *(volatile int*)&fail) return false;
-        if (issuer ? tc_mbar_wait(bar, parity) : tc_mbar_wait_sleep(bar, parity)) return true;
+        if (tight ? tc_mbar_wait(bar, parity) : tc_mbar_wait_sleep(bar, parity)) return true;
         atomicExch(&fail, 1);
         return false;
     };
@@ -902,115 +922,129 @@ linear_wgrad_tc_kernel(const __grid_constant__ LinGradDesc D, int64_t n, int64_t
         U.nch = (int)((U.r1 - U.r0 + kWgRows - 1) / kWgRows);
     };
 
-    if (warp >= 4 && warp < 16) {
+    if (warp >= 4 && warp < 12) {
         // ---------------------------------------------------------- producers
         const bool isA = warp < 8;
         const int q = warp & 3;
-        // column of this thread: A -> input channel (in the M tile), B -> output channel
-        auto load = [&](const Unit& U, int ci, float (&v)[kWgRows]) {
-            const LinGrad& G = D.g[U.j];
-            const int col = isA ? U.mt * 128 + 32 * q + lane : 32 * (warp - 8) + lane;
-            const int lim = isA ? G.mi : G.mo;
-            const int64_t rb = U.r0 + (int64_t)ci * kWgRows;
-            int64_t item = row_item(rb, G.d);
-            int m = (int)(rb - item * G.d);
-            const float* base = isA ? x + G.xo + col : g + G.go + col;
-            const int64_t stride = isA ? D.x_stride : D.g_stride;
-            const int mstride = isA ? G.mi : G.mo;
-#pragma unroll
-            for (int i = 0; i < kWgRows; ++i) {
-                const bool ok = col < lim && rb + i < U.r1;
-                v[i] = ok ? base[item * stride + (int64_t)m * mstride] : 0.0f;
-                if (++m == G.d) {
-                    m = 0;
-                    ++item;
-                }
-            }
-        };
         auto lo = [](float v) {
             return to_tf32(v - __uint_as_float(__float_as_uint(v) & 0xFFFFE000u));
         };
-        float va[kWgRows], vb[kWgRows];
         int64_t k = 0;
         bool stop = false;
-        // write chunk k (values v) into stage k % 4
-        auto put = [&](const Unit& U, float (&v)[kWgRows]) {
-            const int st = (int)(k % kWgStages);
-            if (k >= kWgStages && !wait(&empty[st], (unsigned)(((k - kWgStages) / kWgStages) & 1))) {
-                stop = true;
-                return;
-            }
-            if (isA) {
-                const unsigned ta = tmem + ((unsigned)(32 * q) << 16) + kLtAcol + 64u * st;
-                float h[16], l[16];
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        h[i] = v[16 * half + i];
-                        l[i] = lo(v[16 * half + i]);
-                    }
-                    tmem_st16(ta + 16u * half, h);
-                    tmem_st16(ta + 32 + 16u * half, l);
+        for (int64_t u = blockIdx.x; u < units && !stop; u += gridDim.x) {
+            Unit U;
+            unit_of(u, U);
+            if (U.nch == 0) continue;
+            const LinGrad& G = D.g[U.j];
+            // this thread's column of the staged rows: A -> input channel of the
+            // M tile, B -> output channel
+            const int col = isA ? 32 * q + lane : 32 * (warp - 8) + lane;
+            const int lim = isA ? min(128, G.mi - U.mt * 128) : G.mo;
+            for (int ci = 0; ci < U.nch; ++ci, ++k) {
+                const int rs = (int)(k % kWgRaw);
+                const int64_t rb = U.r0 + (int64_t)ci * kWgRows;
+                const int valid = (int)min((int64_t)kWgRows, U.r1 - rb);
+                if (!wait(&raw_full[rs], (unsigned)((k / kWgRaw) & 1))) {
+                    stop = true;
+                    break;
                 }
-                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-                asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-            } else {
-                const int w = 32 * (warp - 8) + lane;
-                const int mo = D.g[U.j].mo;
-                if (w < mo) {
-                    unsigned char* bs = smem + (size_t)st * bslot;
+                const float* src = reinterpret_cast<const float*>(raw0 + (size_t)rs * kWgRawBytes) +
+                                   (isA ? 0 : kWgRows * 128);
+                float v[kWgRows];
 #pragma unroll
-                    for (int k4 = 0; k4 < kWgRows; k4 += 4) {
-                        *reinterpret_cast<float4*>(bs + kmajor_offset(w, k4, 2 * mo)) =
-                            make_float4(v[k4], v[k4 + 1], v[k4 + 2], v[k4 + 3]);
-                        *reinterpret_cast<float4*>(bs + kmajor_offset(mo + w, k4, 2 * mo)) =
-                            make_float4(lo(v[k4]), lo(v[k4 + 1]), lo(v[k4 + 2]), lo(v[k4 + 3]));
-                    }
+                for (int i = 0; i < kWgRows; ++i)
+                    v[i] = (i < valid && col < lim) ? src[i * 128 + col] : 0.0f;
+                __syncwarp();
+                if (lane == 0) tc_mbar_arrive(&raw_empty[rs]);
+                const int st = (int)(k % kWgStages);
+                if (k >= kWgStages &&
+                    !wait(&empty[st], (unsigned)(((k - kWgStages) / kWgStages) & 1))) {
+                    stop = true;
+                    break;
                 }
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                if (isA) {
+                    const unsigned ta = tmem + ((unsigned)(32 * q) << 16) + kLtAcol + 64u * st;
+                    float hv[16], lv[16];
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            hv[i] = v[16 * half + i];
+                            lv[i] = lo(v[16 * half + i]);
+                        }
+                        tmem_st16(ta + 16u * half, hv);
+                        tmem_st16(ta + 32 + 16u * half, lv);
+                    }
+                    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+                } else {
+                    const int w = col;
+                    const int mo = G.mo;
+                    if (w < mo) {
+                        unsigned char* bs = smem + (size_t)st * bslot;
+#pragma unroll
+                        for (int k4 = 0; k4 < kWgRows; k4 += 4) {
+                            *reinterpret_cast<float4*>(bs + kmajor_offset(w, k4, 2 * mo)) =
+                                make_float4(v[k4], v[k4 + 1], v[k4 + 2], v[k4 + 3]);
+                            *reinterpret_cast<float4*>(bs + kmajor_offset(mo + w, k4, 2 * mo)) =
+                                make_float4(lo(v[k4]), lo(v[k4 + 1]), lo(v[k4 + 2]), lo(v[k4 + 3]));
+                        }
+                    }
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                }
+                __syncwarp();
+                if (lane == 0) tc_mbar_arrive(&full[st]);
+                if (*(volatile int*)&fail) {
+                    stop = true;
+                    break;
+                }
             }
-            __syncwarp();
-            if (lane == 0) tc_mbar_arrive(&full[st]);
-            ++k;
-        };
-        // chunk sequence over this CTA's units, one chunk loaded ahead
-        Unit U{}, Un{};
-        int64_t u = blockIdx.x;
-        if (u < units) unit_of(u, U);
-        int ci = 0;
-        // advance to the first unit with rows
-        while (u < units && U.nch == 0) {
-            u += gridDim.x;
-            if (u < units) unit_of(u, U);
         }
-        if (u < units) load(U, 0, va);
-        bool flip = false;
-        while (u < units && !stop) {
-            // next position
-            int64_t un = u;
-            int cn = ci + 1;
-            Un = U;
-            if (cn == U.nch) {
-                cn = 0;
-                do {
-                    un += gridDim.x;
-                    if (un < units) unit_of(un, Un);
-                } while (un < units && Un.nch == 0);
+    } else if (warp == kWgLoaderWarp) {
+        // ------------------------------------------------------------- loader
+        int64_t k = 0;
+        bool stop = false;
+        for (int64_t u = blockIdx.x; u < units && !stop; u += gridDim.x) {
+            Unit U;
+            unit_of(u, U);
+            if (U.nch == 0) continue;
+            const LinGrad& G = D.g[U.j];
+            const int cols = min(128, G.mi - U.mt * 128);
+            const unsigned abytes = (unsigned)cols * 4, bbytes = (unsigned)G.mo * 4;
+            for (int ci = 0; ci < U.nch; ++ci, ++k) {
+                const int rs = (int)(k % kWgRaw);
+                if (k >= kWgRaw && !wait(&raw_empty[rs], (unsigned)(((k - kWgRaw) / kWgRaw) & 1))) {
+                    stop = true;
+                    break;
+                }
+                const int64_t rb = U.r0 + (int64_t)ci * kWgRows;
+                const int valid = (int)min((int64_t)kWgRows, U.r1 - rb);
+                unsigned char* dst = raw0 + (size_t)rs * kWgRawBytes;
+                if (lane == 0) tc_expect_tx(&raw_full[rs], (unsigned)valid * (abytes + bbytes));
+                __syncwarp();
+                if (lane < valid) {
+                    const int64_t R = rb + lane;
+                    const int64_t item = row_item(R, G.d);
+                    const int m = (int)(R - item * G.d);
+                    tc_bulk_g2s(dst + (size_t)lane * 512,
+                                x + G.xo + item * D.x_stride + (int64_t)m * G.mi + U.mt * 128,
+                                abytes, &raw_full[rs]);
+                    tc_bulk_g2s(dst + (size_t)(kWgRows + lane) * 512,
+                                g + G.go + item * D.g_stride + (int64_t)m * G.mo, bbytes,
+                                &raw_full[rs]);
+                }
+                if (__any_sync(0xffffffffu, *(volatile int*)&fail)) {
+                    ++k;
+                    stop = true;
+                    break;
+                }
             }
-            if (!flip) {
-                if (un < units) load(Un, cn, vb);
-                put(U, va);
-            } else {
-                if (un < units) load(Un, cn, va);
-                put(U, vb);
-            }
-            flip = !flip;
-            u = un;
-            ci = cn;
-            U = Un;
-            if (*(volatile int*)&fail) break;
         }
+        // after a timeout the copies of the last stages may still be in flight:
+        // wait for them (bounded) before the CTA's shared memory is released
+        if (stop)
+            for (int64_t c = k > kWgRaw ? k - kWgRaw : 0; c < k; ++c)
+                tc_mbar_wait(&raw_full[c % kWgRaw], (unsigned)((c / kWgRaw) & 1));
     } else if (issuer) {
         // ---------------------------------------------------------- MMA issuer
         const bool leader = lane == 0;
