@@ -28,10 +28,13 @@
 //     stacked K-major image, per-unit partial sums over a fixed row range;
 //     linear_wgrad_kernel does the same on the CUDA cores for other layers.
 //     The partial rows are added in a fixed order (deterministic).
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
 #include <cstdint>
+#include <mutex>
 
 #include "internal.hpp"
 #include "tcgen05.cuh"
@@ -852,10 +855,25 @@ constexpr size_t kWgRawBytes = 2 * (size_t)kWgRows * 128 * 4;
 constexpr size_t kWgSmem = kWgStages * (size_t)(2 * 128 * kWgRows * 4) + 128 * 128 * 4 +
                            kWgRaw * kWgRawBytes;
 
+// 2D tile copy (tensor map, box 32 rows x 128 columns) into shared memory,
+// completion on an mbarrier; coordinates: column c (innermost), row r.
+__device__ __forceinline__ void tma_tile_g2s(void* dst, const CUtensorMap* map, int c, int r,
+                                             unsigned long long* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c), "r"(r), "r"(smem_addr(bar))
+        : "memory");
+}
+
+// maps: xmap / gmap describe x and g as 2D tensors [n rows][row stride]
+// (box 32 x 128); with them, instructions of one-component irreps (d = 1,
+// rows uniformly strided) take each chunk in two tile copies.
 __global__ void __launch_bounds__(kWgThreads, 1)
 linear_wgrad_tc_kernel(const __grid_constant__ LinGradDesc D, int64_t n, int64_t per, int S,
                        int nacc, const float* __restrict__ x, const float* __restrict__ g,
-                       float* __restrict__ partial) {
+                       float* __restrict__ partial, const __grid_constant__ CUtensorMap xmap,
+                       const __grid_constant__ CUtensorMap gmap, int maps, int gbox) {
     extern __shared__ __align__(1024) unsigned char smem[];
     __shared__ __align__(8) unsigned long long full[kWgStages], empty[kWgStages];
     __shared__ __align__(8) unsigned long long raw_full[kWgRaw], raw_empty[kWgRaw];
@@ -950,10 +968,13 @@ linear_wgrad_tc_kernel(const __grid_constant__ LinGradDesc D, int64_t n, int64_t
                 }
                 const float* src = reinterpret_cast<const float*>(raw0 + (size_t)rs * kWgRawBytes) +
                                    (isA ? 0 : kWgRows * 128);
+                // staged row stride: 128 floats, except g tiles copied through the
+                // map (gbox floats per row)
+                const int pitch = (!isA && maps && G.d == 1 && rb < 0x7fffffff) ? gbox : 128;
                 float v[kWgRows];
 #pragma unroll
                 for (int i = 0; i < kWgRows; ++i)
-                    v[i] = (i < valid && col < lim) ? src[i * 128 + col] : 0.0f;
+                    v[i] = (i < valid && col < lim) ? src[i * pitch + col] : 0.0f;
                 __syncwarp();
                 if (lane == 0) tc_mbar_arrive(&raw_empty[rs]);
                 const int st = (int)(k % kWgStages);
@@ -1020,18 +1041,43 @@ linear_wgrad_tc_kernel(const __grid_constant__ LinGradDesc D, int64_t n, int64_t
                 const int64_t rb = U.r0 + (int64_t)ci * kWgRows;
                 const int valid = (int)min((int64_t)kWgRows, U.r1 - rb);
                 unsigned char* dst = raw0 + (size_t)rs * kWgRawBytes;
+                if (maps && G.d == 1 && rb < 0x7fffffff) {
+                    // two tile copies: rows rb .. rb + 31 (rows past the unit are
+                    // ignored by the producers, rows past n read as zeros)
+                    if (lane == 0) {
+                        tc_expect_tx(&raw_full[rs], (unsigned)kWgRows * (128 + gbox) * 4);
+                        tma_tile_g2s(dst, &xmap, G.xo + U.mt * 128, (int)rb, &raw_full[rs]);
+                        tma_tile_g2s(dst + (size_t)kWgRows * 512, &gmap, G.go, (int)rb,
+                                     &raw_full[rs]);
+                    }
+                    __syncwarp();
+                    if (__any_sync(0xffffffffu, *(volatile int*)&fail)) {
+                        ++k;
+                        stop = true;
+                        break;
+                    }
+                    continue;
+                }
                 if (lane == 0) tc_expect_tx(&raw_full[rs], (unsigned)valid * (abytes + bbytes));
                 __syncwarp();
                 if (lane < valid) {
+                    // rows m, m + 1, ... of one item are consecutive in memory; when a
+                    // row slice is exactly one 512-byte staging row, the lane holding
+                    // the first row of a run copies the whole run at once
                     const int64_t R = rb + lane;
                     const int64_t item = row_item(R, G.d);
                     const int m = (int)(R - item * G.d);
-                    tc_bulk_g2s(dst + (size_t)lane * 512,
-                                x + G.xo + item * D.x_stride + (int64_t)m * G.mi + U.mt * 128,
-                                abytes, &raw_full[rs]);
-                    tc_bulk_g2s(dst + (size_t)(kWgRows + lane) * 512,
-                                g + G.go + item * D.g_stride + (int64_t)m * G.mo, bbytes,
-                                &raw_full[rs]);
+                    const int run = min(G.d - m, valid - lane);
+                    const bool head = lane == 0 || m == 0;
+                    const bool arun = abytes == 512 && G.mi == 128, brun = bbytes == 512;
+                    if (!arun || head)
+                        tc_bulk_g2s(dst + (size_t)lane * 512,
+                                    x + G.xo + item * D.x_stride + (int64_t)m * G.mi + U.mt * 128,
+                                    arun ? 512u * run : abytes, &raw_full[rs]);
+                    if (!brun || head)
+                        tc_bulk_g2s(dst + (size_t)(kWgRows + lane) * 512,
+                                    g + G.go + item * D.g_stride + (int64_t)m * G.mo,
+                                    brun ? 512u * run : bbytes, &raw_full[rs]);
                 }
                 if (__any_sync(0xffffffffu, *(volatile int*)&fail)) {
                     ++k;
@@ -1519,6 +1565,43 @@ cudaError_t launch_linear_forward_tp(const LinearImpl* L, const LinTpDesc& tp, i
     return cudaGetLastError();
 }
 
+// Tensor maps of the weight gradient's x and g (2D: rows x row width, fp32,
+// box 32 rows x min(128, width) columns, zero fill outside).  Returns 0 (the
+// kernel then copies row by row) when the driver entry point is missing or a
+// shape does not qualify: both widths and strides multiples of 4 floats, x at
+// least 128 wide, 16-byte aligned bases.
+static int wgrad_maps(const void* x, int64_t rows, int64_t x_stride, const void* g,
+                      int64_t g_stride, CUtensorMap* xm, CUtensorMap* gm, int* gbox) {
+    static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        else
+            cudaGetLastError();
+    });
+    *gbox = 128;
+    if (!encode || rows < 1 || rows > 0x7fffffff || x_stride < 128 || x_stride % 4 != 0 ||
+        g_stride < 4 || g_stride % 4 != 0 || !aligned16(x) || !aligned16(g))
+        return 0;
+    *gbox = (int)std::min<int64_t>(128, g_stride);
+    auto enc = [&](CUtensorMap* m, const void* base, int64_t width, int box_cols) {
+        const cuuint64_t dims[2] = {(cuuint64_t)width, (cuuint64_t)rows};
+        const cuuint64_t strides[1] = {(cuuint64_t)width * 4};
+        const cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)kWgRows};
+        const cuuint32_t es[2] = {1, 1};
+        return encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides,
+                      box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    };
+    return enc(xm, x, x_stride, 128) && enc(gm, g, g_stride, *gbox) ? 1 : 0;
+}
+
 // Accumulator buffers of the tensor-core weight gradient: two when every
 // stacked [hi | lo] accumulator (2 mul_out columns) fits in 128 columns.
 static int wgrad_accumulators(const LinGradDesc& G) {
@@ -1560,10 +1643,13 @@ cudaError_t launch_linear_backward(const LinearImpl* L, int64_t n, const void* x
             e = cudaFuncSetAttribute(linear_wgrad_tc_kernel,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kWgSmem);
             if (e != cudaSuccess) return e;
-            linear_wgrad_tc_kernel<<<gr, kWgThreads, kWgSmem, s>>>(L->grad, n, per, (int)S,
-                                                                wgrad_accumulators(L->grad),
-                                                                (const float*)x, (const float*)g,
-                                                                (float*)part);
+            // row-by-row copies (merged per item): the layer's one-component
+            // irreps carry few of its rows, and tile copies measured no faster
+            CUtensorMap xm{}, gm{};
+            const int maps = 0, gbox = 128;
+            linear_wgrad_tc_kernel<<<gr, kWgThreads, kWgSmem, s>>>(
+                L->grad, n, per, (int)S, wgrad_accumulators(L->grad), (const float*)x,
+                (const float*)g, (float*)part, xm, gm, maps, gbox);
         } else if (f64)
             linear_wgrad_kernel<double><<<grid, 256, 0, s>>>(L->grad, n, per, (const double*)x,
                                                              (const double*)g, (double*)part);
@@ -1612,8 +1698,12 @@ cudaError_t launch_radial_w2_tc(int64_t E, int hidden, int64_t n_out, const floa
     cudaError_t e = cudaFuncSetAttribute(linear_wgrad_tc_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kWgSmem);
     if (e != cudaSuccess) return e;
+    CUtensorMap xm{}, gm{};
+    int gbox = 128;
+    const int maps = wgrad_maps(gw, E, n_out, h, hidden, &xm, &gm, &gbox);
     linear_wgrad_tc_kernel<<<gr, kWgThreads, kWgSmem, s>>>(*G, E, per, (int)S,
-                                                           wgrad_accumulators(*G), gw, h, partial);
+                                                           wgrad_accumulators(*G), gw, h, partial,
+                                                           xm, gm, maps, gbox);
     count_launch();
     return cudaGetLastError();
 }
