@@ -805,7 +805,8 @@ cgtp_status cgtp_linear_forward(cgtp_linear lin, int64_t n, const void* x, const
     if (!x || !W || !out) return fail(CGTP_E_ARG, "NULL tensor");
     if (workspace && !aligned(workspace, 16)) return fail(CGTP_E_ARG, "workspace not 16-byte aligned");
     cudaError_t e = launch_linear_forward(lin->L, n, x, W, out, workspace, workspace_bytes,
-                                          !(flags & CGTP_LINEAR_CUDA_CORES), S(stream));
+                                          !(flags & CGTP_LINEAR_CUDA_CORES), S(stream),
+                                          (flags & CGTP_LINEAR_TEST_WAIT_TIMEOUT) != 0);
     if (e != cudaSuccess) return cuda_fail(e, "linear_forward");
     return CGTP_OK;
     GUARD_END
@@ -897,7 +898,7 @@ cgtp_status cgtp_radial_forward(cgtp_dtype dtype, int64_t E, int n_basis, double
     cudaError_t e = launch_radial_forward(f64, tc, out_bf16 ? 1 : out_f16 ? 2 : 0, E, n_basis,
                                           cutoff, hidden, n_out,
                                           vec, W1, W2, w, h, workspace, workspace_bytes,
-                                          S(stream));
+                                          S(stream), (flags & CGTP_RADIAL_TEST_WAIT_TIMEOUT) != 0);
     if (e != cudaSuccess) return cuda_fail(e, "radial_forward");
     return CGTP_OK;
     GUARD_END

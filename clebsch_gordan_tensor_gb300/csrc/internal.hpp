@@ -62,7 +62,7 @@ size_t radial_workspace_bytes(bool f64, int nb, int hidden, int64_t n_out);
 cudaError_t launch_radial_forward(bool f64, bool tensor_cores, int out16, int64_t E, int nb,
                                   double rc, int hidden, int64_t n_out, const void* vec,
                                   const void* W1, const void* W2, void* w, void* h, void* ws,
-                                  size_t ws_bytes, cudaStream_t s);
+                                  size_t ws_bytes, cudaStream_t s, bool test_fail = false);
 cudaError_t radial_device_status(int* code);
 size_t radial_backward_workspace_bytes(bool f64, int64_t E, int nb, int hidden, int64_t n_out);
 cudaError_t launch_radial_backward(bool f64, bool tensor_cores, int64_t E, int nb, double rc,
@@ -115,7 +115,7 @@ bool linear_uses_tc(const LinearImpl* L, int64_t n, const void* a, const void* o
                     size_t ws_bytes, bool fwd);
 cudaError_t launch_linear_forward(const LinearImpl* L, int64_t n, const void* x, const void* W,
                                   void* out, void* ws, size_t ws_bytes, bool allow_tc,
-                                  cudaStream_t s);
+                                  cudaStream_t s, bool test_fail = false);
 cudaError_t launch_linear_backward(const LinearImpl* L, int64_t n, const void* x, const void* W,
                                    const void* g, void* gx, void* gW, void* ws, size_t ws_bytes,
                                    bool allow_tc, cudaStream_t s);

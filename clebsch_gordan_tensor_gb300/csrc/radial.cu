@@ -222,7 +222,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 radial_tc_kernel(int64_t E, int nb, float rc, int hidden, int64_t n_out,
                  const float* __restrict__ vec, const float* __restrict__ W1,
                  const unsigned char* __restrict__ img, TW* __restrict__ w,
-                 float* __restrict__ h) {
+                 float* __restrict__ h, int test_fail_first) {
     extern __shared__ __align__(1024) unsigned char smem[];
     __shared__ __align__(8) unsigned long long mma_done[2], acc_free[2], b_full[kTcBSlots];
     __shared__ __align__(8) unsigned long long a_full, a_free;
@@ -346,7 +346,9 @@ radial_tc_kernel(int64_t E, int nb, float rc, int hidden, int64_t n_out,
             int64_t k = 0;
             bool ok = true;
             for (int64_t t = 0; t < my_tiles && ok; ++t) {
-                if (!tc_mbar_wait(&a_full, (unsigned)(t & 1))) {
+                // test_fail_first (tests only): the first wait gives up at once
+                if (!tc_mbar_wait(&a_full, (unsigned)(t & 1),
+                                  test_fail_first && t == 0 ? 0u : 1u << 24)) {
                     ok = false;
                     break;
                 }
@@ -1176,7 +1178,7 @@ template <typename TW>
 static cudaError_t radial_forward_f32(bool tensor_cores, int sms, int64_t E, int nb, float rc,
                                       int hidden, int64_t n_out, const float* vec,
                                       const float* W1, const float* W2, TW* w, float* h,
-                                      void* ws, cudaStream_t s) {
+                                      void* ws, cudaStream_t s, bool test_fail) {
     cudaError_t e;
     if (tensor_cores) {
         e = cudaFuncSetAttribute(radial_tc_kernel<TW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1192,7 +1194,8 @@ static cudaError_t radial_forward_f32(bool tensor_cores, int sms, int64_t E, int
         const int64_t tiles = (E + kTcM - 1) / kTcM;
         const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(tiles, sms));
         radial_tc_kernel<TW><<<grid, kTcThreads, kTcSmem, s>>>(E, nb, rc, hidden, n_out, vec, W1,
-                                                               (const unsigned char*)ws, w, h);
+                                                               (const unsigned char*)ws, w, h,
+                                                               test_fail ? 1 : 0);
         count_launch();
         return cudaGetLastError();
     }
@@ -1210,7 +1213,7 @@ static cudaError_t radial_forward_f32(bool tensor_cores, int sms, int64_t E, int
 cudaError_t launch_radial_forward(bool f64, bool tensor_cores, int out16, int64_t E, int nb,
                                   double rc, int hidden, int64_t n_out, const void* vec,
                                   const void* W1, const void* W2, void* w, void* h, void* ws,
-                                  size_t ws_bytes, cudaStream_t s) {
+                                  size_t ws_bytes, cudaStream_t s, bool test_fail) {
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -1235,12 +1238,12 @@ cudaError_t launch_radial_forward(bool f64, bool tensor_cores, int out16, int64_
     const float* b = (const float*)W2;
     if (out16 == 1)
         return radial_forward_f32(tensor_cores, sms, E, nb, (float)rc, hidden, n_out, v, a, b,
-                                  (__nv_bfloat16*)w, (float*)h, ws, s);
+                                  (__nv_bfloat16*)w, (float*)h, ws, s, test_fail);
     if (out16 == 2)
         return radial_forward_f32(tensor_cores, sms, E, nb, (float)rc, hidden, n_out, v, a, b,
-                                  (__half*)w, (float*)h, ws, s);
+                                  (__half*)w, (float*)h, ws, s, test_fail);
     return radial_forward_f32(tensor_cores, sms, E, nb, (float)rc, hidden, n_out, v, a, b,
-                              (float*)w, (float*)h, ws, s);
+                              (float*)w, (float*)h, ws, s, test_fail);
 }
 
 cudaError_t radial_device_status(int* code) {

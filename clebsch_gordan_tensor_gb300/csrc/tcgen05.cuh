@@ -57,10 +57,12 @@ __device__ __forceinline__ void tc_bulk_g2s(void* dst, const void* src, unsigned
         : "memory");
 }
 
-// Bounded wait for phase `parity` (about a second at most).
-__device__ __forceinline__ bool tc_mbar_wait(unsigned long long* b, unsigned parity) {
+// Bounded wait for phase `parity`: at most `polls` polls (the default is about a
+// second; tests pass 0 to exercise the timeout path).
+__device__ __forceinline__ bool tc_mbar_wait(unsigned long long* b, unsigned parity,
+                                             unsigned polls = 1u << 24) {
     const unsigned a = smem_addr(b);
-    for (unsigned it = 0; it < (1u << 24); ++it) {
+    for (unsigned it = 0; it < polls; ++it) {
         unsigned ok;
         asm volatile(
             "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"

@@ -367,6 +367,12 @@ cgtp_status cgtp_linear_workspace(cgtp_linear lin, int64_t n, size_t* fwd_bytes,
 cgtp_status cgtp_linear_path(cgtp_linear lin, int* tensor_cores);
 /* flags & CGTP_LINEAR_CUDA_CORES: use the CUDA-core kernels. */
 #define CGTP_LINEAR_CUDA_CORES 1u
+/* CGTP_LINEAR_TEST_WAIT_TIMEOUT, for tests of the failure path only: in the
+ * tensor-core forward the MMA issuer's first bounded wait gives up at once;
+ * every role leaves its loop, the loader waits for the copies it started, the
+ * tensor memory is freed and cgtp_linear_device_status reports 1; out is left
+ * incomplete. */
+#define CGTP_LINEAR_TEST_WAIT_TIMEOUT 2u
 /* out [n, dim_out] = the layer applied to x [n, dim_in] with weights W
  * [weight_numel]; device, caller-owned, `dtype`, out overwritten.  On the
  * tensor-core path (see cgtp_linear_path; needs a 16-byte aligned workspace of
@@ -484,6 +490,12 @@ cgtp_status cgtp_uvw_conv_backward(cgtp_uvw u, int64_t N, int64_t E, const int32
  * nearest even), for plans created with CGTP_PLAN_WEIGHTS_F16; fp32 inputs
  * only; not combined with CGTP_RADIAL_OUT_BF16 (CGTP_E_ARG). */
 #define CGTP_RADIAL_OUT_F16 4u
+/* CGTP_RADIAL_TEST_WAIT_TIMEOUT, for tests of the failure path only: in the
+ * tensor-core forward the MMA issuer's first bounded wait gives up at once;
+ * every role then leaves its loop (their own waits are bounded), the kernel
+ * waits a grace period for copies in flight, frees its tensor memory and sets
+ * the flag cgtp_radial_device_status reports; w is left incomplete. */
+#define CGTP_RADIAL_TEST_WAIT_TIMEOUT 8u
 cgtp_status cgtp_radial_forward(cgtp_dtype dtype, int64_t E, int n_basis, double cutoff,
                                 int hidden, int64_t n_out, const void* vec, const void* W1,
                                 const void* W2, void* w, void* h, void* workspace,
