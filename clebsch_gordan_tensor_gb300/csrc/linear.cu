@@ -167,13 +167,51 @@ struct LinGrad {
     int tr;   // 1: gW_j is stored transposed, element (u, w) at w_off + w ldw + u
 };
 constexpr int kLinMaxGrad = 128;
+constexpr int kLinMaxMT = 2 * kLinMaxGrad;  // M tiles: multiplicities up to 256
+constexpr int kLinMaxCls = 16;
 struct LinGradDesc {
     int ninstr, ntiles, nmt;  // nmt: M tiles (128 input channels) over all instructions
     int64_t x_stride, g_stride, nw;
     LinGrad g[kLinMaxGrad];
+    // order of the tensor-core kernel's units (wgrad_schedule): classes of M
+    // tiles with equal rows per item, widest first; class c holds cls_n[c]
+    // consecutive entries of qord (M tile indices)
+    int ncls;
+    int cls_n[kLinMaxCls];
+    int qord[kLinMaxMT];
 };
 
 constexpr int kLgRows = 32;  // rows staged per step
+
+// The tensor-core weight gradient's unit order: M tiles grouped into classes
+// of equal rows per item (d), widest first; inside a class by g offset (the
+// output irrep), then tile index.
+static void wgrad_schedule(LinGradDesc& G) {
+    std::vector<int> q(G.nmt), dq(G.nmt), go(G.nmt);
+    for (int j = 0; j < G.ninstr; ++j) {
+        const int end = j + 1 < G.ninstr ? G.g[j + 1].mt0 : G.nmt;
+        for (int t = G.g[j].mt0; t < end; ++t) {
+            dq[t] = G.g[j].d;
+            go[t] = G.g[j].go;
+        }
+    }
+    for (int t = 0; t < G.nmt; ++t) q[t] = t;
+    std::stable_sort(q.begin(), q.end(), [&](int a, int b) {
+        if (dq[a] != dq[b]) return dq[a] > dq[b];
+        return go[a] < go[b];
+    });
+    G.ncls = 0;
+    for (int i = 0; i < G.nmt; ++i) {
+        G.qord[i] = q[i];
+        // widths beyond the class table share the last class
+        if (i == 0 || (dq[q[i]] != dq[q[i - 1]] && G.ncls < kLinMaxCls)) G.cls_n[G.ncls++] = 0;
+        ++G.cls_n[G.ncls - 1];
+    }
+    if (G.ncls == 0) {
+        G.ncls = 1;
+        G.cls_n[0] = 0;
+    }
+}
 
 // grid: x = tile (instruction, u tile, w tile), y = row split.  Split s covers
 // items [s * per, (s + 1) * per) and writes its partial sums to
@@ -924,18 +962,35 @@ linear_wgrad_tc_kernel(const __grid_constant__ LinGradDesc D, int64_t n, int64_t
         atomicExch(&fail, 1);
         return false;
     };
-    // unit u -> instruction j, M tile mt, split s and its rows [r0, r1)
+    // unit u -> instruction j, M tile mt, split s and its rows [r0, r1).
+    // Units run class by class (M tiles with the same rows per item, widest
+    // first) and split-major inside a class: the CTAs running at one time hold
+    // every M tile of a class for the same few row splits, so g rows that
+    // instructions of one output irrep share (they have the same width) are
+    // read from HBM once and served to the others from L2.  Round r of
+    // gridDim.x units goes to the CTAs in ascending order when r is even and
+    // descending when odd, which evens out the CTAs' rows.
     struct Unit {
-        int j, mt, nch;
+        int j, mt, nch, sp;
         int64_t r0, r1;
     };
     const int64_t units = (int64_t)D.nmt * S;
+    auto unit_at = [&](int64_t r) -> int64_t {
+        return r * gridDim.x + ((r & 1) ? (int64_t)(gridDim.x - 1 - blockIdx.x) : (int64_t)blockIdx.x);
+    };
     auto unit_of = [&](int64_t u, Unit& U) {
-        const int sp = (int)(u % S);
-        const int q = (int)(u / S);
+        int c = 0, q0 = 0;
+        while (c + 1 < D.ncls && u >= (int64_t)D.cls_n[c] * S) {
+            u -= (int64_t)D.cls_n[c] * S;
+            q0 += D.cls_n[c];
+            ++c;
+        }
+        const int sp = (int)(u / D.cls_n[c]);
+        const int q = D.qord[q0 + (int)(u % D.cls_n[c])];
         int j = 0;
         while (j + 1 < D.ninstr && D.g[j + 1].mt0 <= q) ++j;
         U.j = j;
+        U.sp = sp;
         U.mt = q - D.g[j].mt0;
         const int64_t i0 = (int64_t)sp * per, i1 = i0 + per < n ? i0 + per : n;
         const int d = D.g[j].d;
@@ -953,7 +1008,7 @@ linear_wgrad_tc_kernel(const __grid_constant__ LinGradDesc D, int64_t n, int64_t
         };
         int64_t k = 0;
         bool stop = false;
-        for (int64_t u = blockIdx.x; u < units && !stop; u += gridDim.x) {
+        for (int64_t r = 0, u; (u = unit_at(r)) < units && !stop; ++r) {
             Unit U;
             unit_of(u, U);
             if (U.nch == 0) continue;
@@ -1029,7 +1084,7 @@ linear_wgrad_tc_kernel(const __grid_constant__ LinGradDesc D, int64_t n, int64_t
         // ------------------------------------------------------------- loader
         int64_t k = 0;
         bool stop = false;
-        for (int64_t u = blockIdx.x; u < units && !stop; u += gridDim.x) {
+        for (int64_t r = 0, u; (u = unit_at(r)) < units && !stop; ++r) {
             Unit U;
             unit_of(u, U);
             if (U.nch == 0) continue;
@@ -1099,7 +1154,7 @@ linear_wgrad_tc_kernel(const __grid_constant__ LinGradDesc D, int64_t n, int64_t
         // ---------------------------------------------------------- MMA issuer
         const bool leader = lane == 0;
         int64_t k = 0, t = 0, last_commit = -1;
-        for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
+        for (int64_t r = 0, u; (u = unit_at(r)) < units; ++r) {
             Unit U;
             unit_of(u, U);
             if (U.nch == 0) continue;
@@ -1143,11 +1198,11 @@ linear_wgrad_tc_kernel(const __grid_constant__ LinGradDesc D, int64_t n, int64_t
     } else if (warp < 4) {
         // ----------------------------------------------------------- epilogue
         int64_t t = 0;
-        for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
+        for (int64_t r = 0, u; (u = unit_at(r)) < units; ++r) {
             Unit U;
             unit_of(u, U);
             const LinGrad& G = D.g[U.j];
-            const int sp = (int)(u % S);
+            const int sp = U.sp;
             const int urow = U.mt * 128 + 32 * warp + lane;  // input channel of this lane
             // element (urow, w) at prow[w * ws]: rows of the layer's layout, or
             // a column of a transposed output (lanes then store consecutive words)
@@ -1351,6 +1406,7 @@ cgtp_status linear_create(const char* sin, const char* sout, const cgtp_linear_i
         G.nmt += (L->in[i].mul + 127) / 128;
     }
     G.ntiles = tiles;
+    wgrad_schedule(G);
     bool tc = dt == CGTP_F32;
     for (const auto* v : {&L->in, &L->out})
         for (const Irrep& r : *v) tc = tc && r.mul % 32 == 0 && r.mul <= 256;
@@ -1699,6 +1755,7 @@ cudaError_t launch_radial_w2_tc(int64_t E, int hidden, int64_t n_out, const floa
     G->nw = (int64_t)hidden * n_out;
     for (int j = 0; j < G->ninstr; ++j)
         G->g[j] = LinGrad{128 * j, 128, 0, hidden, 1, 128 * j, 0, j, (int)n_out, 1};
+    wgrad_schedule(*G);
     const int64_t per = (E + S - 1) / S;
     const int64_t units = (int64_t)G->nmt * S;
     const unsigned gr = (unsigned)std::min<int64_t>(units, sm_count());
