@@ -121,6 +121,9 @@ cudaError_t launch_linear_backward(const LinearImpl* L, int64_t n, const void* x
                                    bool allow_tc, cudaStream_t s);
 cudaError_t linear_device_status(int* code);
 bool radial_w2_tc_eligible(int hidden, int64_t n_out);
+// The driver's cuTensorMapEncodeTiled (PFN_cuTensorMapEncodeTiled_v12000), or
+// null where the driver does not provide it.
+void* tensor_map_encoder();
 cudaError_t launch_radial_w2_tc(int64_t E, int hidden, int64_t n_out, const float* h,
                                 const float* gw, float* partial, int64_t S, cudaStream_t s);
 

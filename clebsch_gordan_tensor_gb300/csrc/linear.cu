@@ -897,25 +897,33 @@ constexpr size_t kWgRawBytes = 2 * (size_t)kWgRows * 128 * 4;
 constexpr size_t kWgSmem = kWgStages * (size_t)(2 * 128 * kWgRows * 4) + 128 * 128 * 4 +
                            kWgRaw * kWgRawBytes;
 
-// 2D tile copy (tensor map, box 32 rows x 128 columns) into shared memory,
-// completion on an mbarrier; coordinates: column c (innermost), row r.
-__device__ __forceinline__ void tma_tile_g2s(void* dst, const CUtensorMap* map, int c, int r,
-                                             unsigned long long* bar) {
+// Tensor maps of the weight gradient (wgrad_maps), for layers whose
+// instructions all take 128 input channels and the same number of output
+// channels: x viewed as [n][x_stride / 128][128] and g as
+// [n][g_stride / mo][mo]; map (d - 1) / 2 has the box [32 / d items][d][128 or
+// mo], so that one copy per operand stages a chunk of whole items (the rows
+// past 32 / d items, d of them each, are left out of the chunk).
+constexpr int kWgMaxD = 8;  // item widths d = 1, 3, ..., 15
+struct WgMaps {
+    CUtensorMap x[kWgMaxD], g[kWgMaxD];
+    int on;    // 1: the maps are set
+    int gbox;  // g channels per staged row (= mo)
+};
+
+// 3D tile copy through a tensor map, coordinates innermost first.
+__device__ __forceinline__ void tma_3d_g2s(void* dst, const CUtensorMap* map, int c0, int c1, int c2,
+                                           unsigned long long* bar) {
     asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
-        "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c), "r"(r), "r"(smem_addr(bar))
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_addr(bar))
         : "memory");
 }
 
-// maps: xmap / gmap describe x and g as 2D tensors [n rows][row stride]
-// (box 32 x 128); with them, instructions of one-component irreps (d = 1,
-// rows uniformly strided) take each chunk in two tile copies.
 __global__ void __launch_bounds__(kWgThreads, 1)
 linear_wgrad_tc_kernel(const __grid_constant__ LinGradDesc D, int64_t n, int64_t per, int S,
                        int nacc, const float* __restrict__ x, const float* __restrict__ g,
-                       float* __restrict__ partial, const __grid_constant__ CUtensorMap xmap,
-                       const __grid_constant__ CUtensorMap gmap, int maps, int gbox) {
+                       float* __restrict__ partial, const __grid_constant__ WgMaps M) {
     extern __shared__ __align__(1024) unsigned char smem[];
     __shared__ __align__(8) unsigned long long full[kWgStages], empty[kWgStages];
     __shared__ __align__(8) unsigned long long raw_full[kWgRaw], raw_empty[kWgRaw];
@@ -970,9 +978,11 @@ linear_wgrad_tc_kernel(const __grid_constant__ LinGradDesc D, int64_t n, int64_t
     // read from HBM once and served to the others from L2.  Round r of
     // gridDim.x units goes to the CTAs in ascending order when r is even and
     // descending when odd, which evens out the CTAs' rows.
+    // With the maps a chunk is ipc = 32 / d whole items (rows past ipc * d
+    // are zero); without them, 32 consecutive rows.
     struct Unit {
-        int j, mt, nch, sp;
-        int64_t r0, r1;
+        int j, mt, nch, sp, ipc;
+        int64_t r0, r1, i0, i1;
     };
     const int64_t units = (int64_t)D.nmt * S;
     auto unit_at = [&](int64_t r) -> int64_t {
@@ -994,9 +1004,25 @@ linear_wgrad_tc_kernel(const __grid_constant__ LinGradDesc D, int64_t n, int64_t
         U.mt = q - D.g[j].mt0;
         const int64_t i0 = (int64_t)sp * per, i1 = i0 + per < n ? i0 + per : n;
         const int d = D.g[j].d;
-        U.r0 = i0 < n ? i0 * d : 0;
-        U.r1 = i0 < n ? i1 * d : 0;
-        U.nch = (int)((U.r1 - U.r0 + kWgRows - 1) / kWgRows);
+        U.i0 = i0 < n ? i0 : 0;
+        U.i1 = i0 < n ? i1 : 0;
+        U.r0 = U.i0 * d;
+        U.r1 = U.i1 * d;
+        U.ipc = M.on ? kWgRows / d : 0;
+        U.nch = U.ipc ? (int)((U.i1 - U.i0 + U.ipc - 1) / U.ipc)
+                      : (int)((U.r1 - U.r0 + kWgRows - 1) / kWgRows);
+    };
+    // first row and number of live rows of chunk ci
+    auto chunk_rows = [&](const Unit& U, int ci, int64_t& rb, int& valid) {
+        if (U.ipc) {
+            const int64_t it = U.i0 + (int64_t)ci * U.ipc;
+            const int d = D.g[U.j].d;
+            rb = it * d;
+            valid = (int)min((int64_t)U.ipc, U.i1 - it) * d;
+        } else {
+            rb = U.r0 + (int64_t)ci * kWgRows;
+            valid = (int)min((int64_t)kWgRows, U.r1 - rb);
+        }
     };
 
     if (warp >= 4 && warp < 12) {
@@ -1019,17 +1045,18 @@ linear_wgrad_tc_kernel(const __grid_constant__ LinGradDesc D, int64_t n, int64_t
             const int lim = isA ? min(128, G.mi - U.mt * 128) : G.mo;
             for (int ci = 0; ci < U.nch; ++ci, ++k) {
                 const int rs = (int)(k % kWgRaw);
-                const int64_t rb = U.r0 + (int64_t)ci * kWgRows;
-                const int valid = (int)min((int64_t)kWgRows, U.r1 - rb);
+                int64_t rb;
+                int valid;
+                chunk_rows(U, ci, rb, valid);
                 if (!wait(&raw_full[rs], (unsigned)((k / kWgRaw) & 1))) {
                     stop = true;
                     break;
                 }
                 const float* src = reinterpret_cast<const float*>(raw0 + (size_t)rs * kWgRawBytes) +
                                    (isA ? 0 : kWgRows * 128);
-                // staged row stride: 128 floats, except g tiles copied through the
-                // map (gbox floats per row)
-                const int pitch = (!isA && maps && G.d == 1 && rb < 0x7fffffff) ? gbox : 128;
+                // staged row stride: 128 floats, except g rows copied through the
+                // maps (gbox floats per row)
+                const int pitch = (!isA && M.on) ? M.gbox : 128;
                 float v[kWgRows];
 #pragma unroll
                 for (int i = 0; i < kWgRows; ++i)
@@ -1097,17 +1124,21 @@ linear_wgrad_tc_kernel(const __grid_constant__ LinGradDesc D, int64_t n, int64_t
                     stop = true;
                     break;
                 }
-                const int64_t rb = U.r0 + (int64_t)ci * kWgRows;
-                const int valid = (int)min((int64_t)kWgRows, U.r1 - rb);
+                int64_t rb;
+                int valid;
+                chunk_rows(U, ci, rb, valid);
                 unsigned char* dst = raw0 + (size_t)rs * kWgRawBytes;
-                if (maps && G.d == 1 && rb < 0x7fffffff) {
-                    // two tile copies: rows rb .. rb + 31 (rows past the unit are
-                    // ignored by the producers, rows past n read as zeros)
+                if (U.ipc) {
+                    // one copy per operand: items it .. it + ipc - 1, all d rows
+                    // each (items past the unit are ignored by the producers,
+                    // items past n read as zeros); the full boxes count
                     if (lane == 0) {
-                        tc_expect_tx(&raw_full[rs], (unsigned)kWgRows * (128 + gbox) * 4);
-                        tma_tile_g2s(dst, &xmap, G.xo + U.mt * 128, (int)rb, &raw_full[rs]);
-                        tma_tile_g2s(dst + (size_t)kWgRows * 512, &gmap, G.go, (int)rb,
-                                     &raw_full[rs]);
+                        const int it = (int)(U.i0 + (int64_t)ci * U.ipc), di = (G.d - 1) / 2;
+                        const unsigned rows = (unsigned)(U.ipc * G.d);
+                        tc_expect_tx(&raw_full[rs], rows * (128u + (unsigned)M.gbox) * 4u);
+                        tma_3d_g2s(dst, &M.x[di], 0, (G.xo + U.mt * 128) / 128, it, &raw_full[rs]);
+                        tma_3d_g2s(dst + (size_t)kWgRows * 512, &M.g[di], 0, G.go / M.gbox, it,
+                                   &raw_full[rs]);
                     }
                     __syncwarp();
                     if (__any_sync(0xffffffffu, *(volatile int*)&fail)) {
@@ -1626,14 +1657,8 @@ cudaError_t launch_linear_forward_tp(const LinearImpl* L, const LinTpDesc& tp, i
     return cudaGetLastError();
 }
 
-// Tensor maps of the weight gradient's x and g (2D: rows x row width, fp32,
-// box 32 rows x min(128, width) columns, zero fill outside).  Returns 0 (the
-// kernel then copies row by row) when the driver entry point is missing or a
-// shape does not qualify: both widths and strides multiples of 4 floats, x at
-// least 128 wide, 16-byte aligned bases.
-static int wgrad_maps(const void* x, int64_t rows, int64_t x_stride, const void* g,
-                      int64_t g_stride, CUtensorMap* xm, CUtensorMap* gm, int* gbox) {
-    static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+void* tensor_map_encoder() {
+    static void* encode = nullptr;
     static std::once_flag once;
     std::call_once(once, [] {
         void* fn = nullptr;
@@ -1641,26 +1666,49 @@ static int wgrad_maps(const void* x, int64_t rows, int64_t x_stride, const void*
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
                                              cudaEnableDefault, &q) == cudaSuccess &&
             q == cudaDriverEntryPointSuccess)
-            encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+            encode = fn;
         else
             cudaGetLastError();
     });
-    *gbox = 128;
-    if (!encode || rows < 1 || rows > 0x7fffffff || x_stride < 128 || x_stride % 4 != 0 ||
-        g_stride < 4 || g_stride % 4 != 0 || !aligned16(x) || !aligned16(g))
-        return 0;
-    *gbox = (int)std::min<int64_t>(128, g_stride);
-    auto enc = [&](CUtensorMap* m, const void* base, int64_t width, int box_cols) {
-        const cuuint64_t dims[2] = {(cuuint64_t)width, (cuuint64_t)rows};
-        const cuuint64_t strides[1] = {(cuuint64_t)width * 4};
-        const cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)kWgRows};
-        const cuuint32_t es[2] = {1, 1};
-        return encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides,
+    return encode;
+}
+
+// The weight gradient's tensor maps (WgMaps) for x [n][x_stride] and g
+// [n][g_stride], fp32: set when every instruction takes 128 input channels at
+// a 128-aligned offset, all take the same mo output channels (mo % 32 == 0) at
+// mo-aligned offsets, d is odd and at most 15, and the data are 16-byte
+// aligned.  M->on stays 0 otherwise (row-by-row copies).
+static void wgrad_maps(const LinGradDesc& G, int64_t n, const void* x, const void* g, WgMaps* M) {
+    M->on = 0;
+    M->gbox = 128;
+    const auto encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tensor_map_encoder());
+    if (!encode || n < 1 || n > 0x7fffffff || G.ninstr < 1 || !aligned16(x) || !aligned16(g)) return;
+    const int mo = G.g[0].mo;
+    if (mo % 32 != 0 || mo > 128 || G.x_stride % 128 != 0 || G.g_stride % mo != 0) return;
+    bool used[kWgMaxD] = {};
+    for (int j = 0; j < G.ninstr; ++j) {
+        const LinGrad& L = G.g[j];
+        if (L.mi != 128 || L.xo % 128 != 0 || L.mo != mo || L.go % mo != 0 || L.d % 2 != 1 ||
+            L.d > 2 * kWgMaxD - 1)
+            return;
+        used[(L.d - 1) / 2] = true;
+    }
+    auto enc = [&](CUtensorMap* m, const void* base, int width, int64_t stride, int d) {
+        const cuuint64_t dims[3] = {(cuuint64_t)width, (cuuint64_t)(stride / width), (cuuint64_t)n};
+        const cuuint64_t strides[2] = {(cuuint64_t)width * 4, (cuuint64_t)stride * 4};
+        const cuuint32_t box[3] = {(cuuint32_t)width, (cuuint32_t)d, (cuuint32_t)(kWgRows / d)};
+        const cuuint32_t es[3] = {1, 1, 1};
+        return encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides,
                       box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
     };
-    return enc(xm, x, x_stride, 128) && enc(gm, g, g_stride, *gbox) ? 1 : 0;
+    for (int i = 0; i < kWgMaxD; ++i)
+        if (used[i] && !(enc(&M->x[i], x, 128, G.x_stride, 2 * i + 1) &&
+                         enc(&M->g[i], g, mo, G.g_stride, 2 * i + 1)))
+            return;
+    M->gbox = mo;
+    M->on = 1;
 }
 
 // Accumulator buffers of the tensor-core weight gradient: two when every
@@ -1706,13 +1754,13 @@ cudaError_t launch_linear_backward(const LinearImpl* L, int64_t n, const void* x
             e = cudaFuncSetAttribute(linear_wgrad_tc_kernel,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kWgSmem);
             if (e != cudaSuccess) return e;
-            // row-by-row copies (merged per item): the layer's one-component
-            // irreps carry few of its rows, and tile copies measured no faster
-            CUtensorMap xm{}, gm{};
-            const int maps = 0, gbox = 128;
+            // one copy per operand and chunk of whole items where the layer's
+            // shape allows, else row-by-row copies merged per item
+            auto M = std::make_unique<WgMaps>();
+            wgrad_maps(L->grad, n, x, g, M.get());
             linear_wgrad_tc_kernel<<<gr, kWgThreads, kWgSmem, s>>>(
                 L->grad, n, per, (int)S, wgrad_accumulators(L->grad), (const float*)x,
-                (const float*)g, (float*)part, xm, gm, maps, gbox);
+                (const float*)g, (float*)part, *M);
         } else if (f64)
             linear_wgrad_kernel<double><<<grid, 256, 0, s>>>(L->grad, n, per, (const double*)x,
                                                              (const double*)g, (double*)part);
@@ -1762,12 +1810,11 @@ cudaError_t launch_radial_w2_tc(int64_t E, int hidden, int64_t n_out, const floa
     cudaError_t e = cudaFuncSetAttribute(linear_wgrad_tc_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kWgSmem);
     if (e != cudaSuccess) return e;
-    CUtensorMap xm{}, gm{};
-    int gbox = 128;
-    const int maps = wgrad_maps(gw, E, n_out, h, hidden, &xm, &gm, &gbox);
+    auto M = std::make_unique<WgMaps>();
+    wgrad_maps(*G, E, gw, h, M.get());
     linear_wgrad_tc_kernel<<<gr, kWgThreads, kWgSmem, s>>>(*G, E, per, (int)S,
                                                            wgrad_accumulators(*G), gw, h, partial,
-                                                           xm, gm, maps, gbox);
+                                                           *M);
     count_launch();
     return cudaGetLastError();
 }

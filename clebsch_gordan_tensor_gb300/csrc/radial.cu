@@ -26,6 +26,8 @@
 //   * radial_simt_kernel (fp32 / fp64, any shape): shared-memory tiles and
 //     FMA micro-tiles on the CUDA cores.
 // Both compute b and h the same way on the CUDA cores.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -733,11 +735,15 @@ constexpr int kGhK = 32;                 // grad_w columns per chunk
 constexpr int kGhThreads = 32 * 9;       // 4 producer, 4 epilogue, 1 issuer warps
 constexpr unsigned kGhA = kTcM * kGhK * 4;          // one tf32 part of an A chunk (16 KB)
 constexpr unsigned kGhB = 2 * kTcKMax * kGhK * 4;   // a B chunk at hidden = 64 (16 KB)
-constexpr int kGhBSlots = 4;                        // B ring depth
+constexpr int kGhBSlots = 4;                        // ring depth
+// ring slot: the chunk of grad_w as copied (128 rows x 32 columns, 128-byte
+// swizzle; it is the MMA's hi part), then the chunk of the packed W2 image
+constexpr unsigned kGhSlot = kGhA + kGhB;
 constexpr int kGhGp = kTcKMax + 1;   // padded row pitch of the gpre / basis staging
 constexpr int kGhBp = kTcNbMax + 1;
+// + 1 KB to align the swizzled tiles on 1024 bytes
 constexpr unsigned kGhSmem =
-    2 * 2 * kGhA + kGhBSlots * kGhB + kTcM * kGhGp * 4 + kTcM * kGhBp * 4;
+    1024 + 2 * kGhA + kGhBSlots * kGhSlot + kTcM * kGhGp * 4 + kTcM * kGhBp * 4;
 
 __host__ __device__ constexpr uint32_t gh_idesc(int n) {
     return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(kTcM >> 4) << 24);
@@ -763,22 +769,38 @@ __global__ void radial_pack_t_kernel(int hidden, int64_t n_out, const float* __r
     }
 }
 
+// Warp roles, persistent over this CTA's tiles of 128 edges, 32 columns of
+// grad_w per chunk:
+//   issuer (warp 8, one thread): per chunk one tensor-map copy of the grad_w
+//     tile (gmap: [E][n_out], box 32 columns x 128 rows, 128-byte swizzle) and
+//     one bulk copy of the W2 image's chunk into ring slot k % 4 (b_full),
+//     refilled once chunk k - 1 has been multiplied; the MMAs of chunk k
+//     (A hi = the copied tile, A lo from the producers) into accumulator
+//     t % 2 of tile t, committed to mma_done and, after a tile's last chunk,
+//     to acc_full.
+//   producers (warps 0-3, thread = edge row): per chunk, read the row from the
+//     copied tile, write lo = round_tf32(x - x cut to 10 bits) in the same
+//     layout into lo slot k % 2 once chunk k - 2 is done, arrive on a_full.
+//     (The tensor core reads the copied fp32 values as TF32, which keeps
+//     their top 10 mantissa bits: x = hi + lo with both parts TF32.)
+//   epilogue (warps 4-7): as described above.
 __global__ void __launch_bounds__(kGhThreads, 1)
 radial_bwd_tc_kernel(int64_t E, int nb, float rc, int hidden, int64_t n_out,
                      const float* __restrict__ vec, const float* __restrict__ W1,
-                     const unsigned char* __restrict__ img, const float* __restrict__ gw,
+                     const unsigned char* __restrict__ img, const __grid_constant__ CUtensorMap gmap,
                      float* __restrict__ gvec, float* __restrict__ gW1part) {
-    extern __shared__ __align__(1024) unsigned char smem[];
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     __shared__ __align__(8) unsigned long long a_full[2], mma_done[2], b_full[kGhBSlots];
     __shared__ __align__(8) unsigned long long acc_full[2], acc_free[2];
     __shared__ __align__(16) float W1s[kTcNbMax * kTcKMax];
     __shared__ unsigned tmem_base;
     __shared__ int fail;
-    unsigned char* Aring = smem;                   // slot s: hi at 2 s kGhA, lo at (2 s + 1) kGhA
-    unsigned char* Bring = smem + 4 * kGhA;        // slot s at s kGhB
+    unsigned char* Ring = smem;                               // slot s at s kGhSlot
+    unsigned char* Lo = smem + kGhBSlots * kGhSlot;           // lo slot s at s kGhA
     // [128][kGhGp] and [128][kGhBp]: odd pitches keep a warp's row-per-thread
     // stores in distinct banks
-    float* gpS = reinterpret_cast<float*>(smem + 4 * kGhA + kGhBSlots * kGhB);
+    float* gpS = reinterpret_cast<float*>(Lo + 2 * kGhA);
     float* bS = gpS + kTcM * kGhGp;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int NB = 2 * hidden;
@@ -812,57 +834,41 @@ radial_bwd_tc_kernel(int64_t E, int nb, float rc, int hidden, int64_t n_out,
         tiles > (int64_t)blockIdx.x ? (tiles - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
     const int64_t nk = my_tiles * nchunk;
     const unsigned bchunk = (unsigned)(NB * kGhK * 4);
-    const unsigned lslice = (kTcM / 8) * 128, bslice = (unsigned)(NB / 8) * 128;  // K-slice strides
+    const unsigned bslice = (unsigned)(NB / 8) * 128;  // K-slice stride of the W2 image
     const float pref = sqrtf(2.0f / rc);
     float* part = gW1part + (int64_t)blockIdx.x * nb * hidden;
 
     if (warp < 4) {
         // ---------------------------------------------------------- producers
         const int p = tid;
-        // this thread's row chunks, loaded two chunks ahead of their use (the
-        // loads of chunks k + 1 and k + 2 are in flight while chunk k waits);
-        // the chunk loop is unrolled by three so the buffers stay in registers
-        auto load_chunk = [&](int64_t kk, float4 (&dst)[kGhK / 4]) {
-            const int64_t t = kk / nchunk, c = (kk % nchunk + blockIdx.x) % nchunk;
-            const int64_t e = ((int64_t)blockIdx.x + t * gridDim.x) * kTcM + p;
+        bool ok = true;
+        for (int64_t kk = 0; kk < nk && ok; ++kk) {
+            const int rs = (int)(kk % kGhBSlots), s = (int)(kk & 1);
+            if (!tc_mbar_wait(&b_full[rs], (unsigned)((kk / kGhBSlots) & 1))) {
+                ok = false;
+                break;
+            }
+            const unsigned char* raw = Ring + (size_t)rs * kGhSlot;
+            float4 v[kGhK / 4];
 #pragma unroll
             for (int q4 = 0; q4 < kGhK / 4; ++q4)
-                dst[q4] = (kk < nk && e < E)
-                              ? __ldg(reinterpret_cast<const float4*>(gw + e * n_out + c * kGhK) + q4)
-                              : make_float4(0.f, 0.f, 0.f, 0.f);
-        };
-        // chunk kk from `cur` into A slot kk % 2, chunk kk + 2 loaded into `nxt`
-        auto step = [&](int64_t kk, const float4 (&cur)[kGhK / 4], float4 (&nxt)[kGhK / 4]) {
-            load_chunk(kk + 2, nxt);
-            const int s = (int)(kk & 1);
-            if (kk >= 2 && !tc_mbar_wait(&mma_done[s], (unsigned)(((kk - 2) >> 1) & 1))) return false;
-            unsigned char* hi = Aring + (size_t)(2 * s) * kGhA;
-            unsigned char* lo = hi + kGhA;
-#pragma unroll
-            for (int k4 = 0; k4 < kGhK; k4 += 4) {
-                const float4 v = cur[k4 / 4];
-                float4 h4, l4;
-                h4.x = to_tf32(v.x); l4.x = to_tf32(v.x - h4.x);
-                h4.y = to_tf32(v.y); l4.y = to_tf32(v.y - h4.y);
-                h4.z = to_tf32(v.z); l4.z = to_tf32(v.z - h4.z);
-                h4.w = to_tf32(v.w); l4.w = to_tf32(v.w - h4.w);
-                const unsigned off = kmajor_offset(p, k4, kTcM);
-                *reinterpret_cast<float4*>(hi + off) = h4;
-                *reinterpret_cast<float4*>(lo + off) = l4;
+                v[q4] = *reinterpret_cast<const float4*>(raw + sw128_offset(p, 4 * q4));
+            if (kk >= 2 && !tc_mbar_wait(&mma_done[s], (unsigned)(((kk - 2) >> 1) & 1))) {
+                ok = false;
+                break;
             }
+            unsigned char* lo = Lo + (size_t)s * kGhA;
+            auto lo1 = [](float x) {
+                return to_tf32(x - __uint_as_float(__float_as_uint(x) & 0xFFFFE000u));
+            };
+#pragma unroll
+            for (int q4 = 0; q4 < kGhK / 4; ++q4)
+                *reinterpret_cast<float4*>(lo + sw128_offset(p, 4 * q4)) =
+                    make_float4(lo1(v[q4].x), lo1(v[q4].y), lo1(v[q4].z), lo1(v[q4].w));
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             __syncwarp();  // the warp's stores are ordered before its one arrival
             if ((p & 31) == 0) tc_mbar_arrive(&a_full[s]);
-            return !*(volatile int*)&fail;
-        };
-        float4 b0[kGhK / 4], b1[kGhK / 4], b2[kGhK / 4];
-        load_chunk(0, b0);
-        load_chunk(1, b1);
-        bool ok = true;
-        for (int64_t kk = 0; kk < nk && ok; kk += 3) {
-            ok = step(kk, b0, b2);
-            if (ok && kk + 1 < nk) ok = step(kk + 1, b1, b0);
-            if (ok && kk + 2 < nk) ok = step(kk + 2, b2, b1);
+            ok = !*(volatile int*)&fail;
         }
         if (!ok) atomicExch(&fail, 1);
     } else if (warp == 8) {
@@ -872,9 +878,13 @@ radial_bwd_tc_kernel(int64_t E, int nb, float rc, int hidden, int64_t n_out,
             // in an order rotated by their index (the producers do the same)
             auto issue_b = [&](int64_t k) {
                 const int s = (int)(k % kGhBSlots);
-                const int64_t col = (k % nchunk + blockIdx.x) % nchunk;
-                tc_expect_tx(&b_full[s], bchunk);
-                tc_bulk_g2s(Bring + (size_t)s * kGhB, img + (size_t)col * bchunk, bchunk, &b_full[s]);
+                const int64_t t = k / nchunk, col = (k % nchunk + blockIdx.x) % nchunk;
+                const int e0 = (int)(((int64_t)blockIdx.x + t * gridDim.x) * kTcM);
+                unsigned char* slot = Ring + (size_t)s * kGhSlot;
+                // rows past E read as zeros and still count their bytes
+                tc_expect_tx(&b_full[s], kGhA + bchunk);
+                tma_tile_g2s(slot, &gmap, (int)col * kGhK, e0, &b_full[s]);
+                tc_bulk_g2s(slot + kGhA, img + (size_t)col * bchunk, bchunk, &b_full[s]);
             };
             for (int64_t k = 0; k < nk && k < kGhBSlots - 1; ++k) issue_b(k);
             int64_t k = 0;
@@ -895,14 +905,14 @@ radial_bwd_tc_kernel(int64_t E, int nb, float rc, int hidden, int64_t n_out,
                         break;
                     }
                     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                    const unsigned ahi = smem_addr(Aring + (size_t)(2 * s) * kGhA);
-                    const unsigned bb = smem_addr(Bring + (size_t)bs * kGhB);
+                    const unsigned ahi = smem_addr(Ring + (size_t)bs * kGhSlot);
+                    const unsigned alo = smem_addr(Lo + (size_t)s * kGhA);
+                    const unsigned bb = ahi + kGhA;
                     for (int k8 = 0; k8 < kGhK; k8 += 8) {
-                        const unsigned ka = (unsigned)(k8 >> 2) * lslice, kb = (unsigned)(k8 >> 2) * bslice;
+                        const unsigned ka = (unsigned)k8 * 4, kb = (unsigned)(k8 >> 2) * bslice;
                         const uint64_t bd = smem_desc(bb + kb, bslice, 128);
-                        mma_tf32_n(d, smem_desc(ahi + ka, lslice, 128), bd, idesc,
-                                   (c > 0 || k8 > 0) ? 1u : 0u);
-                        mma_tf32_n(d, smem_desc(ahi + kGhA + ka, lslice, 128), bd, idesc, 1u);
+                        mma_tf32_n(d, smem_desc_sw128(ahi + ka), bd, idesc, (c > 0 || k8 > 0) ? 1u : 0u);
+                        mma_tf32_n(d, smem_desc_sw128(alo + ka), bd, idesc, 1u);
                     }
                     tc_commit(&mma_done[s]);
                     if (c == nchunk - 1) tc_commit(&acc_full[as]);
@@ -1061,6 +1071,21 @@ __global__ void __launch_bounds__(128) radial_h_kernel(int64_t E, int nb, float 
     }
 }
 
+// Tensor map of grad_w [E][n_out] (fp32) for the gh kernel: tiles of 32
+// columns x 128 rows with 128-byte swizzle, rows past E read as zeros.
+static bool gh_map(const float* gw, int64_t E, int64_t n_out, CUtensorMap* m) {
+    const auto encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tensor_map_encoder());
+    if (!encode || E < 1 || E > 0x7fffffff || n_out % kGhK != 0 || ((uintptr_t)gw & 15) != 0)
+        return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)n_out, (cuuint64_t)E};
+    const cuuint64_t strides[1] = {(cuuint64_t)n_out * 4};
+    const cuuint32_t box[2] = {(cuuint32_t)kGhK, (cuuint32_t)kTcM};
+    const cuuint32_t es[2] = {1, 1};
+    return encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(gw), dims, strides, box,
+                  es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 cudaError_t launch_radial_backward(bool f64, bool tensor_cores, int64_t E, int nb, double rc,
                                    int hidden, int64_t n_out, const void* vec, const void* W1,
                                    const void* W2, const void* gw, void* gvec, void* gW1,
@@ -1071,7 +1096,9 @@ cudaError_t launch_radial_backward(bool f64, bool tensor_cores, int64_t E, int n
     unsigned char* img = (unsigned char*)ws;
     unsigned char* p1 = img + bw_image_bytes(f64, nb, hidden, n_out);
     unsigned char* p2 = p1 + ((size_t)g1 * nb * hidden * es + 15) / 16 * 16;
-    const bool tc = tensor_cores && radial_bwd_tc_eligible(f64, nb, hidden, n_out);
+    CUtensorMap gmap{};
+    const bool tc = tensor_cores && radial_bwd_tc_eligible(f64, nb, hidden, n_out) &&
+                    (gvec || gW1) && gh_map((const float*)gw, E, n_out, &gmap);
     const size_t sm1 = es * ((size_t)kBwEdges * nb + kBwEdges + (size_t)kBwEdges * hidden +
                              (size_t)kBwEdges * (kBwCols + 1) + (size_t)hidden * (kBwCols + 1) +
                              (size_t)kBwEdges * nb);
@@ -1094,8 +1121,8 @@ cudaError_t launch_radial_backward(bool f64, bool tensor_cores, int64_t E, int n
         const int64_t tiles = (E + kTcM - 1) / kTcM;
         const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(tiles, sms));
         radial_bwd_tc_kernel<<<(unsigned)grid, kGhThreads, kGhSmem, s>>>(
-            E, nb, (float)rc, hidden, n_out, (const float*)vec, (const float*)W1, img,
-            (const float*)gw, (float*)gvec, (float*)p1);
+            E, nb, (float)rc, hidden, n_out, (const float*)vec, (const float*)W1, img, gmap,
+            (float*)gvec, (float*)p1);
         count_launch();
         if ((e = cudaGetLastError())) return e;
         if (gW1 && (e = launch_reduce_rows(false, p1, grid, (int64_t)nb * hidden, gW1, s))) return e;

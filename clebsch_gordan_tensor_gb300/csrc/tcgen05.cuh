@@ -2,6 +2,7 @@
 // (sm_103a, inline PTX).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -26,6 +27,34 @@ __device__ __forceinline__ unsigned kmajor_offset(int row, int k, int rows) {
 __device__ __forceinline__ uint64_t smem_desc(unsigned addr, unsigned lbo, unsigned sbo) {
     return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
            ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46);
+}
+
+// The same for the K-major layout with 128-byte swizzle, as a 2D tile copy
+// with CU_TENSOR_MAP_SWIZZLE_128B writes it: row r's 128 bytes at r * 128, its
+// 16-byte piece j at (j ^ (r % 8)) * 16; the pattern repeats every 8 rows
+// (1024 bytes, the stride byte offset); the leading byte offset is unused
+// while an MMA's K extent stays inside one 128-byte row.  Layout type 2 in
+// bits 61-63.  Advancing K inside the row adds its byte offset to `addr`;
+// the tile itself must start on a 1024-byte boundary.
+__device__ __forceinline__ uint64_t smem_desc_sw128(unsigned addr) {
+    return smem_desc(addr, 16, 1024) | (2ull << 61);
+}
+
+// Byte offset of element (row, k) of a 32-bit K-major tile with 128-byte rows
+// in the swizzled layout above (k < 32).
+__device__ __forceinline__ unsigned sw128_offset(int row, int k) {
+    return (unsigned)(row * 128 + ((((k >> 2) ^ row) & 7) << 4) + (k & 3) * 4);
+}
+
+// 2D tile copy through a tensor map into shared memory, completion on an
+// mbarrier; coordinates: column c (innermost), row r.
+__device__ __forceinline__ void tma_tile_g2s(void* dst, const CUtensorMap* map, int c, int r,
+                                             unsigned long long* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c), "r"(r), "r"(smem_addr(bar))
+        : "memory");
 }
 
 __device__ __forceinline__ void tc_commit(unsigned long long* b) {
