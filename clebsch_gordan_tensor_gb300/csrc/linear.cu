@@ -50,7 +50,6 @@ __device__ int cgtp_linear_error;  // nonzero: a bounded wait timed out
 // out[n * out_stride + out_off + m * ncols + c] for c < ncols.
 struct LinBlock {
     int out_off, ncols, d, chunk0, nchunk;
-    int64_t tile0;  // first 128-row tile of the block (set per launch of the tensor-core kernel)
 };
 // One K chunk of a block: columns a_off + m * a_mul + k0 + k (k < kc) of the
 // input rows, against B[k][c] = W[w_off + (k0 + k) * w_ks + c * w_ns]; the
@@ -65,8 +64,17 @@ constexpr int kLinMaxChunks = 384;
 struct LinDesc {
     int nblocks, nchunks;
     int64_t in_stride, out_stride;
-    LinBlock blk[kLinMaxBlocks + 1];  // + the sentinel tile0 of the tensor-core kernel
+    LinBlock blk[kLinMaxBlocks];
     LinChunk ch[kLinMaxChunks];
+    // unit order of the tensor-core kernel: groups of blocks that read the
+    // same input rows (same d, same chunk sources), tile-major inside a group,
+    // so that the blocks of a group read a row tile at the same time and all
+    // but the first read come from L2 (the x-gradient of a layer whose output
+    // irreps feed several instructions); group g holds grp_nb[g] blocks,
+    // grp_b[grp_b0[g] ..], each of grp_nt[g] tiles, from unit grp_u0[g]
+    int ngrp;
+    int grp_nb[kLinMaxBlocks], grp_b0[kLinMaxBlocks], grp_b[kLinMaxBlocks];
+    int64_t grp_nt[kLinMaxBlocks], grp_u0[kLinMaxBlocks + 1];  // per launch
 };
 
 // --------------------------------------------------------------- CUDA cores
@@ -346,6 +354,7 @@ __device__ __forceinline__ void tmem_st16(unsigned taddr, const float (&v)[16]) 
         : "memory");
 }
 
+
 // Packed B image of every chunk: rows = output columns c < ncols, K-major
 // core matrices, the TF32 hi part then the lo part (ncols * 32 * 4 bytes each);
 // stacked: one image of 2 ncols rows, hi in rows c, lo in rows ncols + c (the
@@ -437,7 +446,7 @@ linear_tc_kernel(const __grid_constant__ LinDesc D, int64_t n, int nmax,
     const unsigned pitch = lt_stage_pitch(nmax, STACK);
     LinBlock* sblk = reinterpret_cast<LinBlock*>(stage_all + kLtEpiWarps * 32 * pitch);
     LinChunk* sch = reinterpret_cast<LinChunk*>(sblk + kLinMaxBlocks + 1);
-    for (int i = tid; i <= D.nblocks; i += kLtThreads) sblk[i] = D.blk[i];
+    for (int i = tid; i < D.nblocks; i += kLtThreads) sblk[i] = D.blk[i];
     for (int i = tid; i < D.nchunks; i += kLtThreads) sch[i] = D.ch[i];
     LinTpDesc* stp = reinterpret_cast<LinTpDesc*>(sch + kLinMaxChunks);
     if constexpr (TPA) {
@@ -490,16 +499,28 @@ linear_tc_kernel(const __grid_constant__ LinDesc D, int64_t n, int nmax,
         int b, ci, nch, ncols, chunk0, rot;
         bool valid;
     };
-    // tiles of block b: [blk[b].tile0, blk[b + 1].tile0); blk[nblocks].tile0 = total
+    // unit u -> group g (units [grp_u0[g], grp_u0[g + 1])), tile-major inside
     auto locate = [&](Pos& p) {
-        p.valid = p.u < sblk[nblocks].tile0;
+        const int ng = D.ngrp;
+        p.valid = p.u < D.grp_u0[ng];
         if (!p.valid) return;
-        if (p.u >= sblk[p.b + 1].tile0 || p.u < sblk[p.b].tile0) {
-            p.b = 0;
-            while (p.u >= sblk[p.b + 1].tile0) ++p.b;
+        int g = 0;
+        while (g + 1 < ng && p.u >= D.grp_u0[g + 1]) ++g;
+        const int64_t ul = p.u - D.grp_u0[g];
+        const int nb = D.grp_nb[g];
+        int r = 0;
+        if (TPA || nb == 1) {  // the fused forward's groups are single blocks
+            p.t = ul;
+        } else if (ul < (int64_t)0xffffffff) {
+            const unsigned q = (unsigned)ul / (unsigned)nb;
+            p.t = q;
+            r = (int)((unsigned)ul - q * (unsigned)nb);
+        } else {
+            p.t = ul / nb;
+            r = (int)(ul - p.t * nb);
         }
+        p.b = D.grp_b[D.grp_b0[g] + r];
         const LinBlock& B = sblk[p.b];
-        p.t = p.u - B.tile0;
         p.nch = B.nchunk;
         p.ncols = B.ncols;
         p.chunk0 = B.chunk0;
@@ -884,7 +905,7 @@ linear_tc_kernel(const __grid_constant__ LinDesc D, int64_t n, int nmax,
 // buffer t % nacc and phase (t / nacc) % 2 of acc_full / acc_free.
 // Waits are bounded as in the forward kernel.
 constexpr int kWgStages = 2;    // MMA stages: A in tensor memory, B image in shared memory
-constexpr int kWgRaw = 3;       // staging stages of the rows (bulk copies)
+constexpr int kWgRaw = 3;       // staging stages of the rows (bulk or tensor-map copies)
 constexpr int kWgThreads = 32 * 17;
 constexpr int kWgRows = 32;  // rows (K) per chunk
 constexpr int kWgSeg = 16;   // chunks (512 rows) per segment of a single buffer
@@ -1316,6 +1337,50 @@ static size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 // Blocks of one pass: for every target irrep reached by an instruction, its
 // chunks (instruction order, 32 source channels each).  fwd: target = output.
+// Groups of blocks that read the same input rows: equal d and the same
+// chunk sequence (source offset, width, K range); the tensor-core kernel runs
+// a group's units tile-major.
+static void lin_groups(LinDesc& D) {
+    auto same = [&](int a, int b) {
+        const LinBlock &A = D.blk[a], &B = D.blk[b];
+        if (A.d != B.d || A.nchunk != B.nchunk) return false;
+        for (int i = 0; i < A.nchunk; ++i) {
+            const LinChunk &x = D.ch[A.chunk0 + i], &y = D.ch[B.chunk0 + i];
+            if (x.a_off != y.a_off || x.a_mul != y.a_mul || x.k0 != y.k0 || x.kc != y.kc) return false;
+        }
+        return true;
+    };
+    std::vector<std::vector<int>> grp;
+    for (int b = 0; b < D.nblocks; ++b) {
+        bool placed = false;
+        for (auto& g : grp)
+            if (same(g[0], b)) {
+                g.push_back(b);
+                placed = true;
+                break;
+            }
+        if (!placed) grp.push_back({b});
+    }
+    D.ngrp = (int)grp.size();
+    int k = 0;
+    for (int g = 0; g < D.ngrp; ++g) {
+        D.grp_nb[g] = (int)grp[g].size();
+        D.grp_b0[g] = k;
+        for (int b : grp[g]) D.grp_b[k++] = b;
+    }
+}
+
+// Units of the tensor-core kernel for n rows of items: per group, its blocks
+// times the 128-row tiles of one block (n d rows).
+static int64_t lin_units(LinDesc& D, int64_t n) {
+    D.grp_u0[0] = 0;
+    for (int g = 0; g < D.ngrp; ++g) {
+        D.grp_nt[g] = (n * D.blk[D.grp_b[D.grp_b0[g]]].d + kLtM - 1) / kLtM;
+        D.grp_u0[g + 1] = D.grp_u0[g] + D.grp_nb[g] * D.grp_nt[g];
+    }
+    return D.grp_u0[D.ngrp];
+}
+
 static bool build_pass(LinearImpl& L, bool fwd, std::string& err) {
     LinDesc& D = fwd ? L.fwd : L.bwd;
     auto& zero = fwd ? L.fwd_zero : L.bwd_zero;
@@ -1365,6 +1430,7 @@ static bool build_pass(LinearImpl& L, bool fwd, std::string& err) {
     }
     (fwd ? L.fwd_img : L.bwd_img) = img;
     (fwd ? L.fwd_nmax : L.bwd_nmax) = nmax;
+    lin_groups(D);
     return true;
 }
 
@@ -1534,12 +1600,7 @@ static cudaError_t run_pass(const LinearImpl& L, const LinDesc& D, int nmax, siz
     if (e != cudaSuccess) return e;
     // per-launch copy with the tile ranges of the blocks for this n
     auto Dn = std::make_unique<LinDesc>(D);
-    int64_t units = 0;
-    for (int b = 0; b < D.nblocks; ++b) {
-        Dn->blk[b].tile0 = units;
-        units += (n * D.blk[b].d + kLtM - 1) / kLtM;
-    }
-    Dn->blk[D.nblocks].tile0 = units;
+    const int64_t units = lin_units(*Dn, n);
     const unsigned grid = (unsigned)std::min<int64_t>(units, sm_count());
     // stages (A in tensor memory, B in shared memory): 4 up to 128 columns, 3 at 256
     const size_t smem = std::max<size_t>(
@@ -1621,6 +1682,8 @@ cudaError_t launch_linear_forward_tp(const LinearImpl* L, const LinTpDesc& tp, i
         groups = std::max(groups, tp.path[p].d1);
     }
     if (groups > 7) return cudaSuccess;
+    for (int g = 0; g < D.ngrp; ++g)  // the fused kernel takes single-block groups
+        if (D.grp_nb[g] != 1) return cudaSuccess;
     *used = true;
     cudaError_t e = zero_blocks(L->fwd_zero, n, L->dim_out, (float*)out, s);
     if (e != cudaSuccess || D.nblocks == 0 || n == 0) return e;
@@ -1633,12 +1696,7 @@ cudaError_t launch_linear_forward_tp(const LinearImpl* L, const LinTpDesc& tp, i
     count_launch();
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     auto Dn = std::make_unique<LinDesc>(D);
-    int64_t units = 0;
-    for (int b = 0; b < D.nblocks; ++b) {
-        Dn->blk[b].tile0 = units;
-        units += (n * D.blk[b].d + kLtM - 1) / kLtM;
-    }
-    Dn->blk[D.nblocks].tile0 = units;
+    const int64_t units = lin_units(*Dn, n);
     const unsigned grid = (unsigned)std::min<int64_t>(units, sm_count());
     const size_t smem = std::max<size_t>(120 * 1024, lt_smem_bytes(nmax, 4, true, true));
     auto* kern = groups <= 3 ? linear_tc_kernel<4, 1, true, 3>
