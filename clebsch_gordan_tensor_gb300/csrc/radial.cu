@@ -160,13 +160,16 @@ constexpr int kTcEpiWarps = 8;     // two per TMEM lane quarter, 64 columns each
 constexpr int kTcProdWarps = 4;    // one edge row per thread
 constexpr int kTcThreads = 32 * (kTcEpiWarps + kTcProdWarps + 1);  // + the MMA issuer warp
 constexpr int kTcBSlots = 2;       // B ring depth
-constexpr unsigned kTcTmemCols = 2 * kTcN;  // two fp32 accumulators
-constexpr unsigned kTcA = kTcM * kTcKMax * 4;   // one tf32 part of A (32 KB)
+// tensor memory: two fp32 accumulators (columns [0, 256)), then A: the hi part
+// of the tile's activations in [256, 256 + hidden), the lo part from 320
+constexpr unsigned kTcTmemCols = 512;
+constexpr unsigned kTcAhi = 2 * kTcN, kTcAlo = kTcAhi + kTcKMax;
 constexpr unsigned kTcB = kTcN * kTcKMax * 4;   // one tf32 part of B (32 KB)
 constexpr unsigned kTcStagePitch = 36;                // floats per staged row (conflict-free)
-constexpr unsigned kTcStage = 16 * kTcStagePitch * 4; // one epilogue warp's 16 x 32 half block
-// A hi/lo, the B ring (hi/lo per slot), the epilogue staging blocks
-constexpr unsigned kTcSmem = 2 * kTcA + 2 * kTcBSlots * kTcB + kTcEpiWarps * kTcStage;
+constexpr unsigned kTcStage = 32 * 32 * 4;  // one epilogue warp's 32 x 32 block (either layout)
+// the B ring (hi/lo per slot), the epilogue staging blocks, + 1 KB to align
+// the 128-byte-swizzled staging blocks on 1024 bytes
+constexpr unsigned kTcSmem = 1024 + 2 * kTcBSlots * kTcB + kTcEpiWarps * kTcStage;
 
 // Instruction descriptor, kind::tf32: D fp32 (bits 4-5 = 1), A and B TF32
 // (bits 7-9 and 10-12 = 2), both K-major, N >> 3 in bits 17-22, M >> 4 in
@@ -219,22 +222,27 @@ __global__ void radial_pack_kernel(int hidden, int64_t n_out, const float* __res
 // than one phase behind the barrier it waits on.  Every wait is bounded; a
 // timeout sets `fail`, each role leaves its loop, and the CTA releases its
 // tensor memory after a grace period.
+//
+// With a tensor map of w (fp32 output, wmap_on), each epilogue warp writes its
+// 32 x 32 blocks into a staging block in the 128-byte-swizzled layout and one
+// thread stores the block with a 2D tensor copy (rows past E are clipped by
+// the map); otherwise the lanes store 128-byte row segments themselves.
 template <typename TW>
 __global__ void __launch_bounds__(kTcThreads, 1)
 radial_tc_kernel(int64_t E, int nb, float rc, int hidden, int64_t n_out,
                  const float* __restrict__ vec, const float* __restrict__ W1,
                  const unsigned char* __restrict__ img, TW* __restrict__ w,
-                 float* __restrict__ h, int test_fail_first) {
-    extern __shared__ __align__(1024) unsigned char smem[];
+                 float* __restrict__ h, int test_fail_first,
+                 const __grid_constant__ CUtensorMap wmap, int wmap_on) {
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     __shared__ __align__(8) unsigned long long mma_done[2], acc_free[2], b_full[kTcBSlots];
     __shared__ __align__(8) unsigned long long a_full, a_free;
     __shared__ __align__(16) float W1s[kTcNbMax * kTcKMax];
     __shared__ unsigned tmem_base;
     __shared__ int fail;
-    unsigned char* Ahi = smem;
-    unsigned char* Alo = smem + kTcA;
-    unsigned char* ring = smem + 2 * kTcA;  // slot s: hi at 2 s kTcB, lo at (2 s + 1) kTcB
-    float* stage_all = reinterpret_cast<float*>(smem + 2 * kTcA + 2 * kTcBSlots * kTcB);
+    unsigned char* ring = smem;  // slot s: hi at 2 s kTcB, lo at (2 s + 1) kTcB
+    float* stage_all = reinterpret_cast<float*>(smem + 2 * kTcBSlots * kTcB);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     if (warp == 0) {
@@ -271,7 +279,7 @@ radial_tc_kernel(int64_t E, int nb, float rc, int hidden, int64_t n_out,
         // ---------------------------------------------------------- producers
         const int p = tid - 32 * kTcEpiWarps;
         const float pref = sqrtf(2.0f / rc);
-        float hv[kTcKMax];
+        float hv[kTcKMax] = {};
         auto hidden_row = [&](int64_t t) {  // activations of row p of this CTA's tile t
             const int64_t e = ((int64_t)blockIdx.x + t * gridDim.x) * kTcM + p;
             const bool live = e < E;
@@ -313,20 +321,22 @@ radial_tc_kernel(int64_t E, int nb, float rc, int hidden, int64_t n_out,
                 atomicExch(&fail, 1);
                 break;
             }
+            // this thread's row of A: TMEM lane p (warp % 4 is its lane quarter)
+            const unsigned ta = tmem + ((unsigned)(p & ~31) << 16);
 #pragma unroll
-            for (int k4 = 0; k4 < kTcKMax; k4 += 4) {
-                if (k4 >= hidden) break;
-                float hi[4], lo[4];
+            for (int k16 = 0; k16 < kTcKMax; k16 += 16) {
+                if (k16 >= hidden) break;
+                float hi[16], lo[16];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    hi[q] = to_tf32(hv[k4 + q]);
-                    lo[q] = to_tf32(hv[k4 + q] - hi[q]);
+                for (int q = 0; q < 16; ++q) {
+                    hi[q] = to_tf32(hv[k16 + q]);
+                    lo[q] = to_tf32(hv[k16 + q] - hi[q]);
                 }
-                const unsigned off = kmajor_offset(p, k4, kTcM);
-                *reinterpret_cast<float4*>(Ahi + off) = make_float4(hi[0], hi[1], hi[2], hi[3]);
-                *reinterpret_cast<float4*>(Alo + off) = make_float4(lo[0], lo[1], lo[2], lo[3]);
+                tmem_st16(ta + kTcAhi + (unsigned)k16, hi);
+                tmem_st16(ta + kTcAlo + (unsigned)k16, lo);
             }
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+            asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
             tc_mbar_arrive(&a_full);
             if (t + 1 < my_tiles) hidden_row(t + 1);
             if (*(volatile int*)&fail) break;
@@ -334,7 +344,7 @@ radial_tc_kernel(int64_t E, int nb, float rc, int hidden, int64_t n_out,
     } else if (warp == kTcEpiWarps + kTcProdWarps) {
         // ------------------------------------------------------------- issuer
         if (lane == 0 && nk > 0) {
-            const unsigned la = (kTcM / 8) * 128, lb = (kTcN / 8) * 128;  // K-slice strides
+            const unsigned lb = (kTcN / 8) * 128;  // K-slice stride of B
             auto issue_b = [&](int64_t k) {
                 const int s = (int)(k % kTcBSlots);
                 const int64_t col = (k % nchunk + blockIdx.x) % nchunk;
@@ -367,14 +377,13 @@ radial_tc_kernel(int64_t E, int nb, float rc, int hidden, int64_t n_out,
                     const unsigned d = tmem + (unsigned)(s * kTcN);
                     const unsigned bhi = smem_addr(ring + (size_t)rs * 2 * kTcB);
                     for (int k8 = 0; k8 < hidden; k8 += 8) {
-                        const unsigned ka = (unsigned)(k8 >> 2) * la, kb = (unsigned)(k8 >> 2) * lb;
-                        const uint64_t ah = smem_desc(smem_addr(Ahi) + ka, la, 128);
-                        const uint64_t al = smem_desc(smem_addr(Alo) + ka, la, 128);
+                        const unsigned kb = (unsigned)(k8 >> 2) * lb;
+                        const unsigned ah = tmem + kTcAhi + (unsigned)k8, al = tmem + kTcAlo + (unsigned)k8;
                         const uint64_t bh = smem_desc(bhi + kb, lb, 128);
                         const uint64_t bl = smem_desc(bhi + kTcB + kb, lb, 128);
-                        mma_tf32(d, ah, bh, k8 > 0 ? 1u : 0u);
-                        mma_tf32(d, ah, bl, 1u);
-                        mma_tf32(d, al, bh, 1u);
+                        mma_tf32_tmem_a(d, ah, bh, kTcIdesc, k8 > 0 ? 1u : 0u);
+                        mma_tf32_tmem_a(d, ah, bl, kTcIdesc, 1u);
+                        mma_tf32_tmem_a(d, al, bh, kTcIdesc, 1u);
                     }
                     tc_commit(&mma_done[s]);
                     if (c == nchunk - 1) tc_commit(&a_free);
@@ -398,7 +407,7 @@ radial_tc_kernel(int64_t E, int nb, float rc, int hidden, int64_t n_out,
         }
     } else {
         // ----------------------------------------------------------- epilogue
-        float* stage = stage_all + warp * (16 * kTcStagePitch);
+        float* stage = stage_all + warp * (kTcStage / 4);
         const int quarter = warp & 3, half = warp >> 2;
         int64_t k = 0;
         bool ok = true;
@@ -421,6 +430,33 @@ radial_tc_kernel(int64_t E, int nb, float rc, int hidden, int64_t n_out,
                 tmem_ld32(ta + 32, v1);
                 asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
                 tc_mbar_arrive(&acc_free[s]);
+                if constexpr (sizeof(TW) == 4) {
+                    if (wmap_on) {
+                        unsigned char* sb = reinterpret_cast<unsigned char*>(stage);
+#pragma unroll
+                        for (int blk = 0; blk < 2; ++blk) {
+                            const float* v = blk ? v1 : v0;
+                            // the staging block's previous store has been read
+                            if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+                            __syncwarp();
+#pragma unroll
+                            for (int q = 0; q < 8; ++q)
+                                *reinterpret_cast<float4*>(sb + sw128_offset(lane, 4 * q)) =
+                                    make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                            __syncwarp();
+                            if (lane == 0 && e0 < E) {  // blocks wholly past E store nothing
+                                asm volatile(
+                                    "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];"
+                                    ::"l"(reinterpret_cast<uint64_t>(&wmap)), "r"((int)(col0 + 32 * blk)),
+                                    "r"((int)e0), "r"(smem_addr(sb))
+                                    : "memory");
+                                asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+                            }
+                        }
+                        continue;
+                    }
+                }
 #pragma unroll
                 for (int blk = 0; blk < 2; ++blk) {
                     const float* v = blk ? v1 : v0;
@@ -456,6 +492,8 @@ radial_tc_kernel(int64_t E, int nb, float rc, int hidden, int64_t n_out,
                 }
             }
         }
+        // the tensor stores of this warp have completed
+        if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
         if (!ok) atomicExch(&fail, 1);
     }
     __syncthreads();
@@ -1220,9 +1258,25 @@ static cudaError_t radial_forward_f32(bool tensor_cores, int sms, int64_t E, int
         if (e != cudaSuccess) return e;
         const int64_t tiles = (E + kTcM - 1) / kTcM;
         const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(tiles, sms));
+        // fp32 output: stores through a tensor map of w [E][n_out] (32 x 32
+        // boxes, 128-byte swizzle, rows past E clipped)
+        CUtensorMap wmap{};
+        int wmap_on = 0;
+        const auto encode =
+            reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tensor_map_encoder());
+        if (sizeof(TW) == 4 && encode && E >= 1 && E <= 0x7fffffff && ((uintptr_t)w & 15) == 0) {
+            const cuuint64_t dims[2] = {(cuuint64_t)n_out, (cuuint64_t)E};
+            const cuuint64_t strides[1] = {(cuuint64_t)n_out * 4};
+            const cuuint32_t box[2] = {32, 32};
+            const cuuint32_t es[2] = {1, 1};
+            wmap_on = encode(&wmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, (void*)w, dims, strides, box,
+                             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                             CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+        }
         radial_tc_kernel<TW><<<grid, kTcThreads, kTcSmem, s>>>(E, nb, rc, hidden, n_out, vec, W1,
                                                                (const unsigned char*)ws, w, h,
-                                                               test_fail ? 1 : 0);
+                                                               test_fail ? 1 : 0, wmap, wmap_on);
         count_launch();
         return cudaGetLastError();
     }
