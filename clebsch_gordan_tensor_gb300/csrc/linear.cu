@@ -477,8 +477,38 @@ linear_tc_kernel(const __grid_constant__ LinDesc D, int64_t n, int nmax,
         bool valid;
     };
     // unit u -> group g (units [grp_u0[g], grp_u0[g + 1])), tile-major inside
+    // The fused forward (single-block groups) runs window by window instead: a
+    // window of 128 items holds d tiles of a block whose rows have d
+    // components, uw = sum_b d units in block order, so all blocks of a window
+    // read its x1 rows close together in time (L2 keeps them); units past a
+    // block's last tile (in the last window) are skipped by every role alike.
+    int uw = 0;
+    if constexpr (TPA)
+        for (int g = 0; g < D.ngrp; ++g) uw += sblk[D.grp_b[g]].d;
+    const int64_t nwin = (n + kLtM - 1) / kLtM;
     auto locate = [&](Pos& p) {
         const int ng = D.ngrp;
+        if constexpr (TPA) {
+            for (;;) {
+                p.valid = p.u < nwin * uw;
+                if (!p.valid) return;
+                int64_t w;
+                int r;
+                if (p.u < (int64_t)0xffffffff) {
+                    w = (unsigned)p.u / (unsigned)uw;
+                    r = (int)((unsigned)p.u - (unsigned)w * (unsigned)uw);
+                } else {
+                    w = p.u / uw;
+                    r = (int)(p.u - w * uw);
+                }
+                int g = 0, acc = 0;
+                while (g + 1 < ng && r >= acc + sblk[D.grp_b[g]].d) acc += sblk[D.grp_b[g++]].d;
+                p.b = D.grp_b[g];
+                p.t = w * sblk[p.b].d + (r - acc);
+                if (p.t < D.grp_nt[g]) break;
+                p.u += gridDim.x;
+            }
+        } else {
         p.valid = p.u < D.grp_u0[ng];
         if (!p.valid) return;
         int g = 0;
@@ -486,7 +516,7 @@ linear_tc_kernel(const __grid_constant__ LinDesc D, int64_t n, int nmax,
         const int64_t ul = p.u - D.grp_u0[g];
         const int nb = D.grp_nb[g];
         int r = 0;
-        if (TPA || nb == 1) {  // the fused forward's groups are single blocks
+        if (nb == 1) {
             p.t = ul;
         } else if (ul < (int64_t)0xffffffff) {
             const unsigned q = (unsigned)ul / (unsigned)nb;
@@ -497,6 +527,7 @@ linear_tc_kernel(const __grid_constant__ LinDesc D, int64_t n, int nmax,
             r = (int)(ul - p.t * nb);
         }
         p.b = D.grp_b[D.grp_b0[g] + r];
+        }
         const LinBlock& B = sblk[p.b];
         p.nch = B.nchunk;
         p.ncols = B.ncols;

@@ -234,8 +234,8 @@ radial_tc_kernel(int64_t E, int nb, float rc, int hidden, int64_t n_out,
                  const unsigned char* __restrict__ img, TW* __restrict__ w,
                  float* __restrict__ h, int test_fail_first,
                  const __grid_constant__ CUtensorMap wmap, int wmap_on) {
-    extern __shared__ __align__(1024) unsigned char smem_raw[];
-    unsigned char* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+    extern __shared__ __align__(1024) unsigned char smem_tc[];
+    unsigned char* smem = smem_tc + ((1024u - (smem_addr(smem_tc) & 1023u)) & 1023u);
     __shared__ __align__(8) unsigned long long mma_done[2], acc_free[2], b_full[kTcBSlots];
     __shared__ __align__(8) unsigned long long a_full, a_free;
     __shared__ __align__(16) float W1s[kTcNbMax * kTcKMax];
@@ -827,8 +827,8 @@ radial_bwd_tc_kernel(int64_t E, int nb, float rc, int hidden, int64_t n_out,
                      const float* __restrict__ vec, const float* __restrict__ W1,
                      const unsigned char* __restrict__ img, const __grid_constant__ CUtensorMap gmap,
                      float* __restrict__ gvec, float* __restrict__ gW1part) {
-    extern __shared__ __align__(1024) unsigned char smem_raw[];
-    unsigned char* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+    extern __shared__ __align__(1024) unsigned char smem_tc[];
+    unsigned char* smem = smem_tc + ((1024u - (smem_addr(smem_tc) & 1023u)) & 1023u);
     __shared__ __align__(8) unsigned long long a_full[2], mma_done[2], b_full[kGhBSlots];
     __shared__ __align__(8) unsigned long long acc_full[2], acc_free[2];
     __shared__ __align__(16) float W1s[kTcNbMax * kTcKMax];
