@@ -1599,8 +1599,15 @@ static cudaError_t run_pass(const LinearImpl& L, const LinDesc& D, int nmax, siz
         return cudaGetLastError();
     }
     // up to 128 columns: A_hi [B_hi | B_lo] as one N = 2 ncols product (stacked
-    // B image), one accumulator of 2 ncols columns; 256: three products
-    const bool stack = nmax <= 128;
+    // B image), one accumulator of 2 ncols columns; 256: three products.
+    // Blocks of at most four K chunks (the x-gradient of a layer whose
+    // instructions each take one 128-channel irrep): three products into two
+    // alternating 128-column accumulators, so that one unit's epilogue and
+    // the next unit's products overlap.
+    int kmax = 0;
+    for (int b = 0; b < D.nblocks; ++b) kmax = std::max(kmax, D.blk[b].nchunk);
+    const bool twoacc = nmax <= 128 && kmax <= 4;
+    const bool stack = nmax <= 128 && !twoacc;
     linear_pack_kernel<<<(unsigned)D.nchunks, 256, 0, s>>>(D, (const float*)W, (unsigned char*)img,
                                                           stack);
     count_launch();
@@ -1612,8 +1619,12 @@ static cudaError_t run_pass(const LinearImpl& L, const LinDesc& D, int nmax, siz
     const unsigned grid = (unsigned)std::min<int64_t>(units, sm_count());
     // stages (A in tensor memory, B in shared memory): 4 up to 128 columns, 3 at 256
     const size_t smem = std::max<size_t>(
-        120 * 1024, stack ? lt_smem_bytes(nmax, 4, true) : lt_smem_bytes(nmax, 3, false));
-    auto* kern = stack ? linear_tc_kernel<4, 1, true, 0> : linear_tc_kernel<3, 1, false, 0>;
+        120 * 1024, stack    ? lt_smem_bytes(nmax, 4, true)
+                    : twoacc ? lt_smem_bytes(nmax, 4, false)
+                             : lt_smem_bytes(nmax, 3, false));
+    auto* kern = stack    ? linear_tc_kernel<4, 1, true, 0>
+                 : twoacc ? linear_tc_kernel<4, 2, false, 0>
+                          : linear_tc_kernel<3, 1, false, 0>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     (void)img_bytes;
