@@ -544,6 +544,111 @@ WORKLOADS = {"conv": make_conv, "conv64": make_conv64, "tp": make_tp, "tfn": mak
 
 # ------------------------------------------------------------ GPU arm
 
+def analyze(wl, per, fma, peaks):
+    """Per-kernel rates and roofline fractions of a workload's step, and the
+    roofline of its dominant kernel.  per: kernel -> mean ms."""
+    names = [n for n, _ in wl.kernels]
+    # the CUDA-core kernels' ALU peak: the FMA-pipe throughput measured in this
+    # run by the library's probe (FP32: the better of scalar and packed FMA)
+    if wl.dtype == "f64":
+        fp32_peak, alu_src = fma["fp64"], "FP64 pipe: measured by cgtp_fma_probe in this run"
+    else:
+        fp32_peak, alu_src = fma["fp32"], "FP32 pipe: measured by cgtp_fma_probe in this run"
+    # fp32 products as three TF32 products on the tensor cores: the effective
+    # peak is the measured bf16 GEMM rate x the nominal tf32/bf16 ratio / 3
+    tc_peak = peaks["bf16"] * TF32_PER_BF16 / 3 if peaks.get("bf16") else None
+    kernels = {}
+    for n in names:
+        nbytes, flops, *kind = wl.counts[n]
+        t = per[n] * 1e-3
+        gbs = nbytes / t / 1e9
+        ent = {"ms": per[n], "hbm_gbs": gbs, "hbm_frac": gbs / peaks["hbm"]}
+        if flops and kind and kind[0] == "tensor3" and tc_peak:
+            tf = flops / t / 1e12
+            t_hbm, t_tc = nbytes / (peaks["hbm"] * 1e9), flops / (tc_peak * 1e12)
+            ent.update(tflops=tf, tensor_frac=tf / tc_peak,
+                       bound="tensor" if t_tc >= t_hbm else "hbm",
+                       roofline_frac=max(t_hbm, t_tc) / t)
+        elif flops:
+            tf = flops / t / 1e12
+            ent.update(tflops=tf, alu_frac=tf / fp32_peak)
+            t_hbm, t_alu = nbytes / (peaks["hbm"] * 1e9), flops / (fp32_peak * 1e12)
+            ent["bound"] = "hbm" if t_hbm >= t_alu else "alu"
+            ent["roofline_frac"] = max(t_hbm, t_alu) / t
+            ex = wl.exec_flops.get(n)
+            if ex:  # the FLOPs the kernel executes (y-first form)
+                ent.update(exec_tflops=ex / t / 1e12, exec_alu_frac=ex / t / 1e12 / fp32_peak)
+        else:
+            ent["bound"] = "hbm"
+            ent["roofline_frac"] = gbs / peaks["hbm"]
+        kernels[n] = ent
+    dom = max(names, key=lambda n: per[n])
+    kd = kernels[dom]
+    if kd["bound"] == "tensor":
+        roof = {"bound": "tensor", "achieved": kd["tflops"], "peak": tc_peak, "unit": "TFLOP/s",
+                "frac": kd["tflops"] / tc_peak,
+                "note": "fp32 products as three TF32 tensor-core products: peak = measured bf16 "
+                        "x nominal tf32/bf16 / 3"}
+    elif kd["bound"] == "alu":
+        roof = {"bound": "alu", "achieved": kd["tflops"], "peak": fp32_peak, "unit": "TFLOP/s",
+                "frac": kd["tflops"] / fp32_peak}
+        if "exec_tflops" in kd:
+            roof.update(achieved_exec=kd["exec_tflops"], frac_exec=kd["exec_alu_frac"])
+    else:
+        roof = {"bound": "hbm", "achieved": kd["hbm_gbs"], "peak": peaks["hbm"], "unit": "GB/s",
+                "frac": kd["hbm_gbs"] / peaks["hbm"]}
+    roof.update(kernel=dom, traffic=_traffic(wl.name, dom),
+                peak_source=f"HBM: {peaks['src']} copy bandwidth (MEASURED_PEAKS.json); {alu_src}")
+    return kernels, roof, fp32_peak, alu_src
+
+
+def run_workloads(args, cg, W, torch, fma, peaks):
+    """The other workloads of the benchmark set, each timed briefly in the same
+    process after the main measurement (3 warm-up steps, 20 timed steps, CUDA
+    events per kernel): their step time, rate and the roofline of their
+    dominant kernel.  A workload that fails is reported with its error."""
+    out = {}
+    for name in ("tp", "conv64", "tfn", "kv", "uvw"):
+        if name == args.workload:
+            continue
+        try:
+            wl = WORKLOADS[name](args, cg, W, torch)
+            names = [n for n, _ in wl.kernels]
+            for _ in range(3):
+                for _, k in wl.kernels:
+                    k()
+            torch.cuda.synchronize()
+            steps = 20
+            evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)]
+                   for _ in range(steps)]
+            for k in range(steps):
+                for i, (_, fn) in enumerate(wl.kernels):
+                    evs[k][i].record()
+                    fn()
+                evs[k][-1].record()
+            torch.cuda.synchronize()
+            per = {n: float(np.mean([evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(steps)]))
+                   for i, n in enumerate(names)}
+            ms_step = float(np.mean([evs[k][0].elapsed_time(evs[k][-1]) for k in range(steps)]))
+            kernels, roof, _, _ = analyze(wl, per, fma, peaks)
+            fwd_ms = sum(per[n] for n in wl.fwd_names)
+            out[name] = {
+                "workload": wl.desc, "steps": steps, "warmup": 3, "ms_per_step": ms_step,
+                "value": wl.units / (ms_step * 1e-3), "unit": wl.unit, "dtype": wl.dtype,
+                "fwd": {"value": wl.units / (fwd_ms * 1e-3), "ms": fwd_ms},
+                "roofline": roof,
+                "kernels": {n: {"ms": e["ms"], "bound": e.get("bound"),
+                                "roofline_frac": e.get("roofline_frac")}
+                            for n, e in kernels.items()},
+            }
+            del wl
+        except Exception as e:  # reported, the main line stands
+            out[name] = {"error": f"{type(e).__name__}: {e}"[:200]}
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_gpu(args):
     import torch
 
@@ -595,43 +700,14 @@ def run_gpu(args):
     side = {n: time_side(torch, fn) for n, (fn, _, _) in wl.side.items()}
     if rank != 0:
         return None
+    others = None
+    # with the benchmark sizes only (profiling runs shrink --atoms / --samples)
+    if world == 1 and not args.no_workloads and args.atoms is None and args.samples == 200_000:
+        others = run_workloads(args, cg, W, torch, wl.fma_peaks, _peaks())
 
     peaks = _peaks()
     fma = wl.fma_peaks
-    # the CUDA-core kernels' ALU peak: the FMA-pipe throughput measured in this
-    # run by the library's probe (FP32: the better of scalar and packed FMA)
-    if wl.dtype == "f64":
-        fp32_peak, alu_src = fma["fp64"], "FP64 pipe: measured by cgtp_fma_probe in this run"
-    else:
-        fp32_peak, alu_src = fma["fp32"], "FP32 pipe: measured by cgtp_fma_probe in this run"
-    # fp32 products as three TF32 products on the tensor cores: the effective
-    # peak is the measured bf16 GEMM rate x the nominal tf32/bf16 ratio / 3
-    tc_peak = peaks["bf16"] * TF32_PER_BF16 / 3 if peaks.get("bf16") else None
-    kernels = {}
-    for n in names:
-        nbytes, flops, *kind = wl.counts[n]
-        t = per[n] * 1e-3
-        gbs = nbytes / t / 1e9
-        ent = {"ms": per[n], "hbm_gbs": gbs, "hbm_frac": gbs / peaks["hbm"]}
-        if flops and kind and kind[0] == "tensor3" and tc_peak:
-            tf = flops / t / 1e12
-            t_hbm, t_tc = nbytes / (peaks["hbm"] * 1e9), flops / (tc_peak * 1e12)
-            ent.update(tflops=tf, tensor_frac=tf / tc_peak,
-                       bound="tensor" if t_tc >= t_hbm else "hbm",
-                       roofline_frac=max(t_hbm, t_tc) / t)
-        elif flops:
-            tf = flops / t / 1e12
-            ent.update(tflops=tf, alu_frac=tf / fp32_peak)
-            t_hbm, t_alu = nbytes / (peaks["hbm"] * 1e9), flops / (fp32_peak * 1e12)
-            ent["bound"] = "hbm" if t_hbm >= t_alu else "alu"
-            ent["roofline_frac"] = max(t_hbm, t_alu) / t
-            ex = wl.exec_flops.get(n)
-            if ex:  # the FLOPs the kernel executes (y-first form)
-                ent.update(exec_tflops=ex / t / 1e12, exec_alu_frac=ex / t / 1e12 / fp32_peak)
-        else:
-            ent["bound"] = "hbm"
-            ent["roofline_frac"] = gbs / peaks["hbm"]
-        kernels[n] = ent
+    kernels, roof, fp32_peak, alu_src = analyze(wl, per, fma, peaks)
     side_out = {}
     for n, ms in side.items():
         _, nbytes, flops = wl.side[n]
@@ -654,23 +730,6 @@ def run_gpu(args):
                            "note": "outside the step: radial-network gradient for the conv "
                                    "gradient's grad_w (gh = grad_w W2^T and grad_W2 on the "
                                    "tensor cores, the rest on the CUDA cores)"}
-    dom = max(names, key=lambda n: per[n])
-    kd = kernels[dom]
-    if kd["bound"] == "tensor":
-        roof = {"bound": "tensor", "achieved": kd["tflops"], "peak": tc_peak, "unit": "TFLOP/s",
-                "frac": kd["tflops"] / tc_peak,
-                "note": "fp32 products as three TF32 tensor-core products: peak = measured bf16 "
-                        "x nominal tf32/bf16 / 3"}
-    elif kd["bound"] == "alu":
-        roof = {"bound": "alu", "achieved": kd["tflops"], "peak": fp32_peak, "unit": "TFLOP/s",
-                "frac": kd["tflops"] / fp32_peak}
-        if "exec_tflops" in kd:
-            roof.update(achieved_exec=kd["exec_tflops"], frac_exec=kd["exec_alu_frac"])
-    else:
-        roof = {"bound": "hbm", "achieved": kd["hbm_gbs"], "peak": peaks["hbm"], "unit": "GB/s",
-                "frac": kd["hbm_gbs"] / peaks["hbm"]}
-    roof.update(kernel=dom, traffic=_traffic(args.workload, dom),
-                peak_source=f"HBM: {peaks['src']} copy bandwidth (MEASURED_PEAKS.json); {alu_src}")
     config = {"workload": wl.desc, **wl.cfg,
               "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
               "l2": "inputs larger than L2 (weight stream per step >> 129 MB)"}
@@ -685,6 +744,9 @@ def run_gpu(args):
         "fma_peaks": fma, "gpu_launches": launches,
         "clocks": clk.summary(), "e2e": e2e,
     }
+    if others:
+        # measured after the timed region above, outside it
+        line["workloads"] = others
     if not args.no_cpu_baseline and wl.oracle_step is not None:
         line["cpu_baseline"] = cpu_baseline(wl, budget_s=args.cpu_seconds)
     return line
@@ -890,6 +952,8 @@ def main():
                     help="sample count of the tp and uvw workloads (200000 is the benchmark; "
                          "smaller for profiling)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the brief runs of the other workloads after the main one")
     args = ap.parse_args()
     line = run_reference(args) if args.impl == "reference" else run_gpu(args)
     if line is not None:
