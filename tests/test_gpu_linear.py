@@ -192,3 +192,26 @@ def test_linear_weight_gradient_long_sums():
         _, gW = lin.backward(dev(x), dev(W), dev(g), need=(False, True), cuda_cores=cc)
         assert_close(host(gW), rW, np.float32, f"grad_W (cuda cores: {cc})")
     assert cg.linear_device_status() == 0
+
+
+@pytest.mark.parametrize("n", [5, 3001])
+def test_linear_128_channel_layer_ragged(n):
+    """A layer whose instructions all take 128 input and 128 output channels
+    (the 'uvw' mixing's shape): the W-gradient stages chunks of whole items
+    with 3D tensor-map copies (items per chunk 32 / d, a ragged last chunk and
+    split tails at these n), and the forward and x-gradient, one 128-channel
+    source per block, run the three split products into two alternating
+    accumulators; all against the oracle."""
+    need_gpu()
+    cg = _cg()
+    irreps = ("128x0e+128x1o+128x2e+128x3o", "128x0e+128x1o+128x2e+128x3o")
+    rng = np.random.default_rng(40 + n)
+    instr, x, W, g = _problem(rng, irreps, n, np.float32)
+    lin = cg.Linear(*irreps)
+    out = lin.forward(dev(x), dev(W))
+    assert_close(host(out), O.linear_forward(*irreps, instr, x, W), np.float32, "forward")
+    rx, rW = O.linear_backward(*irreps, instr, x, W, g)
+    gx, gW = lin.backward(dev(x), dev(W), dev(g))
+    assert_close(host(gx), rx, np.float32, "grad_x")
+    assert_close(host(gW), rW, np.float32, "grad_W")
+    assert cg.linear_device_status() == 0
