@@ -374,12 +374,16 @@ cgtp_status build_plan(Plan& p, const char* s1, const char* s2, const char* so,
         // deeper prefetch); flags override both.
         const size_t stat = (size_t)std::max(4, (nt + 3) / 4 * 4) * es + 2048;
         // Weights loaded by the lanes (prefetched one edge ahead in registers)
-        // instead of through the ring: default for the backward (its ring then
-        // carries only the gathered gradient row), not for the forward (its
-        // registers limit residency first).  Flag bit 16 turns it on for the
-        // forward (single warp group only), bit 17 off for the backward.
+        // instead of through the ring: default for the backward of plans with
+        // two channels per lane (a lane's weight pair is one 8-byte load per
+        // path, and the ring then carries only the gathered gradient row), not
+        // for one channel per lane (a 4-byte load per path: the ring's one
+        // bulk copy of the row measured 9% faster on the 32-channel TFN
+        // layer) nor for the forward (its registers limit residency first).
+        // Flag bit 16 turns it on for the forward (single warp group only),
+        // bit 17 off for the backward.
         p.w_direct_f = ((p.flags >> 16) & 1u) && p.fwd_groups.size() == 1;
-        p.w_direct_b = !((p.flags >> 17) & 1u) &&
+        p.w_direct_b = !((p.flags >> 17) & 1u) && p.cpt == 2 &&
                        p.dtype == CGTP_F32;  // fp64 pairs would double the prefetch registers
         // bits 20-23: resident backward CTAs per SM that the register budget
         // must allow (__launch_bounds__ minimum; 0 = no bound)

@@ -91,8 +91,9 @@ typedef struct {
  * bits 8-11 forward TMA ring depth (2-15), bits 12-15 backward ring depth,
  * bit 16: forward lanes load their weights directly (prefetched one edge ahead
  * in registers) instead of through the ring; bit 17: backward lanes take their
- * weights through the ring instead of loading them directly (the default for
- * fp32 plans); bit 18: directly loaded backward weights use one register
+ * weights through the ring instead of loading them directly (direct loads are
+ * the default for fp32 plans with two channels per lane, the ring for the
+ * others); bit 18: directly loaded backward weights use one register
  * buffer (reloaded path by path) instead of two; bit 19: the backward puts
  * the grad_y contraction on a second warp of each CTA (one-warp path groups);
  * bits 20-23: the backward's register budget must allow that many resident
