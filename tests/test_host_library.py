@@ -301,3 +301,27 @@ def test_uvw_product_host_side():
     # a workspace that is missing or too small is refused
     assert L.cgtp_uvw_forward(u._h, 4, null, null, null, null, null, null, 0, null) == 1
     assert b"workspace" in L.cgtp_last_error_message()
+
+
+def _defines(src):
+    return dict(re.findall(r"#define (W_DIRECT_B|W_DIRECT_F|GB|GF|STAGES_B|STAGES_F|CPT|LANES) (\w+)",
+                           src))
+
+
+def test_planner_automatic_launch_shapes():
+    """The automatic launch shapes the measurements chose (no GPU needed: the
+    generated source carries them): one warp group and a 2-deep ring each way;
+    backward weights loaded by the lanes with two channels per lane, through
+    the ring with one (32-channel irreps) and in fp64; forward weights through
+    the ring.  Flags override them."""
+    conv = _defines(cg.Plan(*W.IRREPS_CONV64).source())
+    assert conv == {"CPT": "2", "LANES": "32", "STAGES_F": "2", "STAGES_B": "2",
+                    "W_DIRECT_F": "0", "W_DIRECT_B": "1", "GF": "1", "GB": "1"}
+    tfn = _defines(cg.Plan(*W.tfn32_mol1000()["irreps"]).source())
+    assert (tfn["CPT"], tfn["W_DIRECT_B"], tfn["GB"], tfn["STAGES_B"]) == ("1", "0", "1", "2")
+    f64 = _defines(cg.Plan(*W.IRREPS_CONV64, dtype=torch.float64).source())
+    assert f64["W_DIRECT_B"] == "0"
+    # overrides: backward weights through the ring, 3-deep backward ring, two
+    # forward warp groups
+    ovr = _defines(cg.Plan(*W.IRREPS_CONV64, flags=(1 << 17) | (3 << 12) | 2).source())
+    assert (ovr["W_DIRECT_B"], ovr["STAGES_B"], ovr["GF"]) == ("0", "3", "2")
