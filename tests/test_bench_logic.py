@@ -72,3 +72,13 @@ def test_roofline_fraction_is_the_slower_bound_over_time(ms):
     t = ms * 1e-3
     want = max(1.0e9 / (6000.0e9), 8.0e10 / 80.0e12) / t
     assert math.isclose(kernels["k_alu"]["roofline_frac"], want)
+
+
+def test_algorithmic_flop_counts_of_the_configs():
+    """bench's per-unit FLOP count, mul * sum_p 2 (nnz_p + d_l3), from the
+    planner's CG tables: 58,496 per edge for the 64-channel conv layer (config
+    2) and 116,992 per sample for the 128-channel one (configs 1 and 3)."""
+    import clebsch_gordan_tensor_gb300 as cg
+    import workloads as W
+    assert bench.Dims(cg.Plan(*W.IRREPS_CONV64)).flops == 58_496
+    assert bench.Dims(cg.Plan(*W.IRREPS_MACE128)).flops == 116_992
